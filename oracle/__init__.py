@@ -1,0 +1,198 @@
+"""CPU oracle for the group-wise INT4 weight-only linear layer (W4A16).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never calls it and shares no code with it.
+
+The arithmetic lives in ``w4a16_oracle.c`` (plain C, binary64); this module
+compiles it with gcc into ``oracle/_build/`` and wraps it with ctypes, taking
+and returning numpy arrays.  fp16 values travel as their uint16 bit patterns.
+
+Method: forum.sourcefind.cn thread "vLLM on Hygon Z100", section 四 (W4A16):
+w = (q - z) * s per group along K, y = x @ w^T.  Every function here is pinned
+by ``tests/test_oracle_pins.py`` against exact rationals, closed forms, numpy's
+binary16 conversion or an int64 matrix product.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (portable flags: same results on x86 and Arm)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-add, every binary64 operation rounds
+    # exactly as written.
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    L = ctypes.c_long
+    lib.w4o_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.w4o_half_to_double.restype = ctypes.c_double
+    lib.w4o_double_to_half.argtypes = [ctypes.c_double]
+    lib.w4o_double_to_half.restype = ctypes.c_uint16
+    lib.w4o_pack.argtypes = [P, P, I, I, I, P, P]
+    lib.w4o_unpack.argtypes = [P, P, I, I, I, P, P]
+    lib.w4o_dequant.argtypes = [P, P, P, I, I, I, P]
+    lib.w4o_linear.argtypes = [P, P, P, P, I, I, I, I, P, I]
+    lib.w4o_linear_rows.argtypes = [P, P, P, P, I, I, I, I, P, I, P, I]
+    lib.w4o_round_to_half.argtypes = [P, L, P]
+    lib.w4o_half_array_to_double.argtypes = [P, L, P]
+    for f in (lib.w4o_pack, lib.w4o_unpack, lib.w4o_dequant, lib.w4o_linear,
+              lib.w4o_linear_rows, lib.w4o_round_to_half,
+              lib.w4o_half_array_to_double):
+        f.restype = None
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check_shape(K: int, group: int):
+    if K % group or K % 8 or group <= 0:
+        raise ValueError("K must be a multiple of group and of 8")
+
+
+def zero_words(G: int) -> int:
+    return (G + 7) // 8
+
+
+def half_to_double(bits) -> np.ndarray:
+    h = _c(np.asarray(bits, dtype=np.uint16).reshape(-1), np.uint16)
+    out = np.empty(h.size, dtype=np.float64)
+    _load().w4o_half_array_to_double(_ptr(h), h.size, _ptr(out))
+    return out.reshape(np.shape(bits))
+
+
+def double_to_half(v) -> np.ndarray:
+    d = _c(np.asarray(v, dtype=np.float64).reshape(-1), np.float64)
+    out = np.empty(d.size, dtype=np.uint16)
+    _load().w4o_round_to_half(_ptr(d), d.size, _ptr(out))
+    return out.reshape(np.shape(v))
+
+
+def pack(q: np.ndarray, z: np.ndarray, group: int = 128):
+    """q [N, K] uint8 (0..15), z [N, K/group] uint8 -> (qweight [N, K/8], zeros [N, ceil(G/8)]) uint32."""
+    q = _c(q, np.uint8)
+    z = _c(z, np.uint8)
+    N, K = q.shape
+    _check_shape(K, group)
+    G = K // group
+    assert z.shape == (N, G)
+    qw = np.empty((N, K // 8), dtype=np.uint32)
+    zw = np.empty((N, zero_words(G)), dtype=np.uint32)
+    _load().w4o_pack(_ptr(q), _ptr(z), N, K, group, _ptr(qw), _ptr(zw))
+    return qw, zw
+
+
+def unpack(qweight: np.ndarray, zeros: np.ndarray, K: int, group: int = 128):
+    qweight = _c(qweight, np.uint32)
+    zeros = _c(zeros, np.uint32)
+    N = qweight.shape[0]
+    _check_shape(K, group)
+    G = K // group
+    assert qweight.shape == (N, K // 8) and zeros.shape == (N, zero_words(G))
+    q = np.empty((N, K), dtype=np.uint8)
+    z = np.empty((N, G), dtype=np.uint8)
+    _load().w4o_unpack(_ptr(qweight), _ptr(zeros), N, K, group, _ptr(q), _ptr(z))
+    return q, z
+
+
+def dequant(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, K: int,
+            group: int = 128) -> np.ndarray:
+    """Exact w[n, k] = (q - z) * s in binary64, [N, K]."""
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint32)
+    N = qweight.shape[0]
+    _check_shape(K, group)
+    G = K // group
+    assert scales.shape == (N, G)
+    w = np.empty((N, K), dtype=np.float64)
+    _load().w4o_dequant(_ptr(qweight), _ptr(scales), _ptr(zeros), N, K, group, _ptr(w))
+    return w
+
+
+def linear(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+           group: int = 128, nthreads: int | None = None) -> np.ndarray:
+    """y[M, N] = x @ dequant(W)^T in binary64.  x is [M, K] fp16 bits (uint16)."""
+    x = _c(x, np.uint16)
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint32)
+    M, K = x.shape
+    N = qweight.shape[0]
+    _check_shape(K, group)
+    G = K // group
+    assert qweight.shape == (N, K // 8) and scales.shape == (N, G)
+    assert zeros.shape == (N, zero_words(G))
+    y = np.empty((M, N), dtype=np.float64)
+    nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
+    _load().w4o_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N, K,
+                       group, _ptr(y), nt)
+    return y
+
+
+def linear_rows(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
+                zeros: np.ndarray, rows, group: int = 128,
+                nthreads: int | None = None) -> np.ndarray:
+    """y[M, len(rows)] for the listed output rows; the weight arrays hold all N rows."""
+    x = _c(x, np.uint16)
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint32)
+    rows = _c(np.asarray(rows, dtype=np.int64), np.int64)
+    M, K = x.shape
+    N = qweight.shape[0]
+    _check_shape(K, group)
+    G = K // group
+    assert qweight.shape == (N, K // 8) and scales.shape == (N, G)
+    assert zeros.shape == (N, zero_words(G))
+    if rows.size and (rows.min() < 0 or rows.max() >= N):
+        raise IndexError("row index out of range")
+    y = np.empty((M, rows.size), dtype=np.float64)
+    nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
+    _load().w4o_linear_rows(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N,
+                            K, group, _ptr(rows), int(rows.size), _ptr(y), nt)
+    return y
+

@@ -1,0 +1,272 @@
+/*
+ * w4a16_oracle.c -- plain, slow, obviously correct CPU oracle for the
+ * group-wise INT4 weight-only linear layer (W4A16).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file; only tests/, the smoke check and the CPU-baseline leg of the
+ * benchmark do.  It shares no code, header, table or constant generator with
+ * the CUDA library: the two meet only through the seeded input generator.
+ *
+ * What it computes (the method, as the pages describe it):
+ *   forum.sourcefind.cn thread "vLLM on Hygon Z100", section 四 (W4A16):
+ *   INT4 weights carry a per-group scale and zero point; the kernel unpacks the
+ *   packed INT4 words, reads scale and zero, restores each weight and
+ *   multiply-accumulates it with the 16-bit activations.
+ *   haowenji.com V100 decode article, paragraph on "groupwise-int": integers
+ *   times a per-group scale.
+ * Written out for m < M, n < N, k < K, g = floor(k / group):
+ *     w[n,k] = (q[n,k] - z[n,g]) * s[n,g]
+ *     y[m,n] = sum_k x[m,k] * w[n,k]
+ * with q, z unsigned 4-bit, s and x IEEE binary16, y returned in binary64.
+ *
+ * Readings taken where the pages are silent (each one listed in the design doc):
+ *   - packed layout [N, K/8] 32-bit words, rows = outputs (section 四 names
+ *     "[N,K/8] int32"); element k sits in bits 4*(k%8)..4*(k%8)+3 of word k/8;
+ *   - zeros are 4-bit too, packed 8 per word along the group axis with the
+ *     same rule; a row has ceil(G/8) words, pad nibbles are written as 0;
+ *   - the sum runs in binary64 in increasing k.  Every product x*(q-z)*s is
+ *     exact in binary64 (11 + 4 + 11 significant bits), so the only rounding is
+ *     in the additions.
+ *
+ * Parity pins (tests/test_oracle_pins.py, all CPU):
+ *   half<->double conversions against numpy's IEEE binary16 conversion over
+ *   every bit pattern and a tie/overflow/subnormal battery; pack against
+ *   closed-form words; pack/unpack round trip over every nibble value in every
+ *   position; dequant against exact rationals for all 256 (q, z) pairs and a
+ *   set of scales; linear against exact-rational brute force on tiny shapes,
+ *   q == z gives 0, one nonzero group, linearity, and an integer special case
+ *   that reduces to an int64 matrix product.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------------
+ * IEEE 754 binary16 <-> binary64, written from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent field 0
+ * holds zero and subnormals (fraction * 2^-24), field 31 holds inf / NaN.
+ * ------------------------------------------------------------------------- */
+double w4o_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + f), e - 25);
+    }
+    return sign ? -v : v;
+}
+
+/* Round to nearest, ties to even.  Exact: the value is scaled by a power of
+ * two into units of the binary16 quantum at its binade, so the integer and
+ * fractional parts below are exact in binary64. */
+uint16_t w4o_double_to_half(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7e00u);
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7c00u);
+    /* 65504 is the largest finite value; 65520 is the midpoint to 2^16 and
+     * rounds (to even) upward, i.e. to infinity. */
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;               /* a in [2^E, 2^(E+1)) */
+    if (E < -14) E = -14;         /* subnormal range shares the 2^-24 quantum */
+    double r = ldexp(a, 10 - E);  /* a / 2^(E-10), exact */
+    double fl = floor(r);
+    double frac = r - fl;
+    uint64_t m = (uint64_t)fl;
+    if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;
+    if (m == 0) return sign;
+    if (m < 1024) {               /* only reachable with E == -14: subnormal */
+        return (uint16_t)(sign | (uint16_t)m);
+    }
+    if (m == 2048) {              /* rounding carried into the next binade */
+        m = 1024;
+        E++;
+    }
+    int field = E + 15;
+    if (field >= 31) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)(field << 10) | (uint16_t)(m - 1024));
+}
+
+/* ---------------------------------------------------------------------------
+ * Nibble access with the sequential little-endian rule.
+ * ------------------------------------------------------------------------- */
+static inline unsigned nibble_at(const uint32_t *row_words, long idx)
+{
+    return (row_words[idx / 8] >> (4 * (idx % 8))) & 0xfu;
+}
+
+static inline long zero_words_per_row(int G) { return (G + 7) / 8; }
+
+/* q: [N, K] bytes 0..15, z: [N, G] bytes 0..15 ->
+ * qweight: [N, K/8] words, zeros: [N, ceil(G/8)] words. */
+void w4o_pack(const uint8_t *q, const uint8_t *z, int N, int K, int group,
+              uint32_t *qweight, uint32_t *zeros)
+{
+    int G = K / group;
+    long KW = K / 8, ZW = zero_words_per_row(G);
+    for (long n = 0; n < N; n++) {
+        for (long w = 0; w < KW; w++) {
+            uint32_t word = 0;
+            for (int j = 0; j < 8; j++) {
+                uint32_t v = q[n * K + w * 8 + j] & 0xfu;
+                word |= v << (4 * j);
+            }
+            qweight[n * KW + w] = word;
+        }
+        for (long w = 0; w < ZW; w++) {
+            uint32_t word = 0;
+            for (int j = 0; j < 8; j++) {
+                long g = w * 8 + j;
+                if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);
+            }
+            zeros[n * ZW + w] = word;
+        }
+    }
+}
+
+void w4o_unpack(const uint32_t *qweight, const uint32_t *zeros, int N, int K,
+                int group, uint8_t *q, uint8_t *z)
+{
+    int G = K / group;
+    long KW = K / 8, ZW = zero_words_per_row(G);
+    for (long n = 0; n < N; n++) {
+        for (long k = 0; k < K; k++) q[n * K + k] = (uint8_t)nibble_at(qweight + n * KW, k);
+        for (long g = 0; g < G; g++) z[n * G + g] = (uint8_t)nibble_at(zeros + n * ZW, g);
+    }
+}
+
+/* w[n,k] = (q - z) * s, exact in binary64. */
+void w4o_dequant(const uint32_t *qweight, const uint16_t *scales,
+                 const uint32_t *zeros, int N, int K, int group, double *w)
+{
+    int G = K / group;
+    long KW = K / 8, ZW = zero_words_per_row(G);
+    for (long n = 0; n < N; n++) {
+        for (long k = 0; k < K; k++) {
+            long g = k / group;
+            int qv = (int)nibble_at(qweight + n * KW, k);
+            int zv = (int)nibble_at(zeros + n * ZW, g);
+            double s = w4o_half_to_double(scales[n * G + g]);
+            w[n * K + k] = (double)(qv - zv) * s;
+        }
+    }
+}
+
+/* One output element, the definition written out: dequantise each weight,
+ * multiply by the activation, add in increasing k. */
+static double linear_one(const uint16_t *x_row, const uint32_t *q_row,
+                         const uint16_t *s_row, const uint32_t *z_row, int K,
+                         int group)
+{
+    double acc = 0.0;
+    for (long k = 0; k < K; k++) {
+        long g = k / group;
+        int qv = (int)nibble_at(q_row, k);
+        int zv = (int)nibble_at(z_row, g);
+        double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);
+        acc += w4o_half_to_double(x_row[k]) * w;
+    }
+    return acc;
+}
+
+typedef struct {
+    const uint16_t *x;
+    const uint32_t *qweight;
+    const uint16_t *scales;
+    const uint32_t *zeros;
+    const int64_t *rows; /* NULL: all rows */
+    int M, N, K, group, nrows;
+    double *y; /* [M, nrows] */
+    int t, nthreads;
+} linear_job;
+
+static void *linear_worker(void *arg)
+{
+    linear_job *j = (linear_job *)arg;
+    int G = j->K / j->group;
+    long KW = j->K / 8, ZW = zero_words_per_row(G);
+    for (long i = j->t; i < j->nrows; i += j->nthreads) {
+        long n = j->rows ? (long)j->rows[i] : i;
+        for (long m = 0; m < j->M; m++) {
+            j->y[m * j->nrows + i] =
+                linear_one(j->x + m * (long)j->K, j->qweight + n * KW,
+                           j->scales + n * G, j->zeros + n * ZW, j->K, j->group);
+        }
+    }
+    return NULL;
+}
+
+static void run_linear(linear_job base, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if (nthreads == 1) {
+        base.t = 0;
+        base.nthreads = 1;
+        linear_worker(&base);
+        return;
+    }
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    linear_job *jobs = (linear_job *)malloc(sizeof(linear_job) * (size_t)nthreads);
+    int started = 0;
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = base;
+        jobs[t].t = t;
+        jobs[t].nthreads = nthreads;
+        if (pthread_create(&th[t], NULL, linear_worker, &jobs[t]) == 0) {
+            started++;
+        } else {
+            /* could not start a thread: do its share here */
+            linear_worker(&jobs[t]);
+            th[t] = 0;
+        }
+    }
+    for (int t = 0; t < nthreads; t++)
+        if (th[t]) pthread_join(th[t], NULL);
+    (void)started;
+    free(jobs);
+    free(th);
+}
+
+/* y[M, N] in binary64, rows split over nthreads host threads. */
+void w4o_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                const uint32_t *zeros, int M, int N, int K, int group, double *y,
+                int nthreads)
+{
+    linear_job j = {x, qweight, scales, zeros, NULL, M, N, K, group, N, y, 0, 1};
+    run_linear(j, nthreads);
+}
+
+/* Sampled outputs: y[M, nrows] for the listed output rows only.  The weight
+ * arrays still describe all N rows (row n starts at n * K/8 words). */
+void w4o_linear_rows(const uint16_t *x, const uint32_t *qweight,
+                     const uint16_t *scales, const uint32_t *zeros, int M, int N,
+                     int K, int group, const int64_t *rows, int nrows, double *y,
+                     int nthreads)
+{
+    linear_job j = {x, qweight, scales, zeros, rows, M, N, K, group, nrows, y, 0, 1};
+    run_linear(j, nthreads);
+}
+
+/* Elementwise binary64 -> binary16 (RNE) over an array. */
+void w4o_round_to_half(const double *v, long n, uint16_t *out)
+{
+    for (long i = 0; i < n; i++) out[i] = w4o_double_to_half(v[i]);
+}
+
+void w4o_half_array_to_double(const uint16_t *h, long n, double *out)
+{
+    for (long i = 0; i < n; i++) out[i] = w4o_half_to_double(h[i]);
+}

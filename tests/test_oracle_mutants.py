@@ -1,0 +1,84 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case copies the oracle's C source, plants one mistake (a flipped sign, a
+wrong nibble or group index, a dropped term, a transposed operand, a wrong
+rounding rule), builds the copy with gcc into a temporary directory, swaps it
+in for the real oracle and checks that at least one pin of
+``test_oracle_pins`` fails.  The mistake is planted in the oracle, on the CPU.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
+
+MUTANTS = {
+    "nibble_order_reversed": ("return (row_words[idx / 8] >> (4 * (idx % 8))) & 0xfu;",
+                              "return (row_words[idx / 8] >> (4 * (7 - idx % 8))) & 0xfu;"),
+    "sign_flipped": ("double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);",
+                     "double w = (double)(zv - qv) * w4o_half_to_double(s_row[g]);"),
+    "scale_group_ignored": ("double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);",
+                            "double w = (double)(qv - zv) * w4o_half_to_double(s_row[0]);"),
+    "zero_group_off_by_one": ("int zv = (int)nibble_at(z_row, g);",
+                              "int zv = (int)nibble_at(z_row, g ? g - 1 : 0);"),
+    "last_term_dropped": ("for (long k = 0; k < K; k++) {\n        long g = k / group;\n        int qv = (int)nibble_at(q_row, k);\n        int zv",
+                          "for (long k = 0; k < K - 1; k++) {\n        long g = k / group;\n        int qv = (int)nibble_at(q_row, k);\n        int zv"),
+    "operands_transposed": ("linear_one(j->x + m * (long)j->K, j->qweight + n * KW,",
+                            "linear_one(j->x + (n % j->M) * (long)j->K, j->qweight + (m % j->N) * KW,"),
+    "subnormal_exponent": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;",
+                            "if (frac >= 0.5) m++;"),
+    "pack_zero_pad_dirty": ("if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);",
+                            "word |= (uint32_t)(z[n * G + (g < G ? g : G - 1)] & 0xfu) << (4 * j);"),
+}
+
+
+def _pin_calls():
+    return [
+        pins.test_half_to_double_every_pattern,
+        pins.test_double_to_half_round_to_nearest_even,
+        pins.test_double_to_half_ties_closed_form,
+        pins.test_pack_closed_form_words,
+        pins.test_pack_unpack_round_trip_every_nibble_everywhere,
+        pins.test_unpack_pack_round_trip_random_words,
+        pins.test_dequant_all_q_z_pairs_exact,
+        pins.test_dequant_group_index,
+        lambda: pins.test_linear_matches_exact_rationals(2, 3, 256, 128),
+        lambda: pins.test_linear_matches_exact_rationals(2, 5, 384, 128),
+        pins.test_q_equal_z_gives_zero,
+        pins.test_single_nonzero_group_closed_form,
+        pins.test_linearity_in_x,
+        lambda: pins.test_integer_case_equals_int64_matmul(0x2C00, 1 / 16),
+        pins.test_hand_worked_example,
+    ]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-o", str(so), str(mutated), "-lm", "-lpthread"], check=True)
+    real = oracle._load()
+    oracle._lib = oracle._bind(ctypes.CDLL(str(so)))
+    failed = []
+    try:
+        for call in _pin_calls():
+            try:
+                with np.errstate(all="ignore"):
+                    call()
+            except (AssertionError, ValueError, IndexError):
+                failed.append(getattr(call, "__name__", "lambda"))
+    finally:
+        oracle._lib = real
+    assert failed, f"no pin caught the planted mistake {name}"
