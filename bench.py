@@ -1,0 +1,452 @@
+"""Benchmark: the W4A16 decode round on one GB300 (or N independent replicas).
+
+A step is one decode round: 64 layers x the four linears of a 27B-class
+decode layer (qkv 5120->8192, o 6144->5120, gate+up 5120->34816, down
+17408->5120), group 128, M = 4 tokens (1 + 3 drafted tokens of a speculative
+verify pass), back to back on one stream.  Weights are ~11.4 GB per round, far
+larger than L2, so every step streams them from HBM.
+
+Printed (one JSON line on rank 0):
+  value         algorithmic GB/s of the round (packed nibbles + fp16 scales +
+                4-bit zeros + x + y, GB = 1e9 B), whole job (sum over ranks)
+  ms_per_step   milliseconds per round
+  roofline      the dominant kernel: algorithmic bytes per launch / its mean
+                CUDA-event duration, against the measured HBM copy bandwidth
+  e2e           the same round through the C ABI with host buffers: x copied
+                in from pinned memory and every y copied back, each step
+  cpu_baseline  the oracle on the host cores, on a bounded sample of the round
+  extra         single-linear numbers for the M = 1 / 4 / 8 shapes and the
+                M sweep (L2 flushed between timed launches)
+
+--impl reference times the oracle itself (the reference arm) on a bounded
+sample of the same round, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("W4A16 linear HBM GB/s (% of GB300 peak) at M=1/4/8; 64-layer decode-round ms")
+ROUND_SHAPES = [("qkv", 5120, 8192), ("o", 6144, 5120), ("gate_up", 5120, 34816),
+                ("down", 17408, 5120)]  # (name, K, N)
+N_LAYERS = 64
+M_ROUND = 4
+GROUP = 128
+WORKLOAD = ("decode round: 64 layers x {qkv 5120x8192, o 6144x5120, gate+up 5120x34816, "
+            "down 17408x5120} (KxN), M=4, group 128, int4 weights + fp16 scales + u4 zeros, "
+            "fp16 activations")
+
+
+def linear_bytes(M: int, N: int, K: int) -> int:
+    """Algorithmic bytes of one linear: what the method must move, once."""
+    G = K // GROUP
+    return N * K // 2 + 2 * N * G + N * G // 2 + 2 * M * K + 2 * M * N
+
+
+def round_bytes(M: int = M_ROUND, layers: int = N_LAYERS) -> int:
+    return layers * sum(linear_bytes(M, N, K) for _, K, N in ROUND_SHAPES)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workload construction
+# ---------------------------------------------------------------------------
+def build_round(dev, M=M_ROUND, layers=N_LAYERS):
+    import synthetic_inputs as si
+    xs = [si.x(si.config_seed(3, 0, 8 + j), M, K) for j, (_, K, _) in enumerate(ROUND_SHAPES)]
+    xs_dev = [x.to(dev) for x in xs]
+    lin = []
+    for l in range(layers):
+        for j, (name, K, N) in enumerate(ROUND_SHAPES):
+            qw, s, zw = si.layer(si.config_seed(3, l, j), N, K, device=dev)
+            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            lin.append(dict(name=name, x=xs_dev[j], qweight=qw, scales=s, zeros=zw, y=y, N=N, K=K,
+                            j=j))
+    return lin, xs, xs_dev
+
+
+def time_round(w4, descs, steps, warmup, stream):
+    for _ in range(warmup):
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1) / 1e3
+
+
+def per_kernel_durations(w4, lin, steps, stream):
+    """Each linear launched alone with CUDA events around it, on the launching
+    stream; returns {rung: (launches, seconds, algorithmic bytes)}."""
+    stats = {}
+    evs = []
+    for _ in range(steps):
+        for L in lin:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            w4.w4a16_linear(L["x"], L["qweight"], L["scales"], L["zeros"], y=L["y"], stream=stream)
+            b.record(stream)
+            evs.append((L, a, b))
+    torch.cuda.synchronize()
+    for L, a, b in evs:
+        rung = w4.w4a16_select_rung(M_ROUND, L["N"], L["K"])
+        n, t, by = stats.get(rung, (0, 0.0, 0))
+        stats[rung] = (n + 1, t + a.elapsed_time(b) / 1e3, by + linear_bytes(M_ROUND, L["N"], L["K"]))
+    return stats
+
+
+def time_e2e(w4, lin, xs, steps, warmup, stream):
+    """x from pinned host memory in, decode round, every y back to pinned host memory."""
+    dev_x = {}
+    for L in lin:
+        dev_x[L["j"]] = L["x"]
+    pinned_x = [x.pin_memory() for x in xs]
+    pinned_y = [torch.empty(L["y"].shape, dtype=torch.float16).pin_memory() for L in lin]
+    descs = w4.make_descs(lin)
+    h2d = sum(x.numel() * 2 for x in xs)
+    d2h = sum(L["y"].numel() * 2 for L in lin)
+
+    def step():
+        for j, x in enumerate(pinned_x):
+            dev_x[j].copy_(x, non_blocking=True)
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+        for L, hy in zip(lin, pinned_y):
+            hy.copy_(L["y"], non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            step()
+        t1 = time.perf_counter()
+    return (t1 - t0), h2d, d2h
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None):
+    """Median single-launch time of one linear with L2 flushed before each launch."""
+    import synthetic_inputs as si
+    qw, s, zw = si.layer(si.config_seed(seed_cfg, 0, M), N, K, device=dev)
+    x = si.x(si.config_seed(seed_cfg, 0, M), M, K).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    for _ in range(3):
+        w4.w4a16_linear(x, qw, s, zw, y=y)
+    ts = []
+    for _ in range(reps):
+        flush_l2(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        w4.w4a16_linear(x, qw, s, zw, y=y)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+    del qw, s, zw
+    return t
+
+
+def cpu_baseline(seconds_target: float = 12.0):
+    """The oracle, as it stands, on all host cores, over a bounded sample of the
+    decode round: the first R rows of each of layer 0's four linears at M = 4,
+    R growing until the sample takes about `seconds_target` seconds."""
+    import oracle
+    import synthetic_inputs as si
+    cores = os.cpu_count() or 1
+    xs = [si.as_u16(si.x(si.config_seed(3, 0, 8 + j), M_ROUND, K))
+          for j, (_, K, _) in enumerate(ROUND_SHAPES)]
+    rows = 8
+    while True:
+        t_total, by_total = 0.0, 0
+        for j, (_, K, N) in enumerate(ROUND_SHAPES):
+            r = np.arange(min(rows, N), dtype=np.int64)
+            qw, s, zw = si.layer(si.config_seed(3, 0, j), N, K, rows=r)
+            args = (xs[j], si.as_u32(qw), si.as_u16(s), si.as_u32(zw), np.arange(r.size))
+            t0 = time.perf_counter()
+            oracle.linear_rows(*args, nthreads=cores)
+            t_total += time.perf_counter() - t0
+            G = K // GROUP
+            by_total += r.size * (K // 2 + 2 * G + G // 2) + 2 * M_ROUND * K + 2 * M_ROUND * r.size
+        if t_total >= seconds_target / 4 or rows >= 1 << 14:
+            break
+        rows *= 2
+    # scale to the target duration with one more pass at the grown size
+    factor = max(1.0, seconds_target / max(t_total, 1e-3))
+    rows = int(rows * min(factor, 4.0))
+    t_total, by_total = 0.0, 0
+    for j, (_, K, N) in enumerate(ROUND_SHAPES):
+        r = np.arange(min(rows, N), dtype=np.int64)
+        qw, s, zw = si.layer(si.config_seed(3, 0, j), N, K, rows=r)
+        args = (xs[j], si.as_u32(qw), si.as_u16(s), si.as_u32(zw), np.arange(r.size))
+        t0 = time.perf_counter()
+        oracle.linear_rows(*args, nthreads=cores)
+        t_total += time.perf_counter() - t0
+        G = K // GROUP
+        by_total += r.size * (K // 2 + 2 * G + G // 2) + 2 * M_ROUND * K + 2 * M_ROUND * r.size
+    gbs = by_total / t_total / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of each of layer 0's four linears (qkv, o, gate+up, down) "
+                      f"at M=4, {t_total:.1f} s on {cores} threads; full round would take "
+                      f"{round_bytes() / (gbs * 1e9):.0f} s",
+            "seconds": t_total}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    secs = []
+    vals = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(seconds_target=8.0 if i >= args.warmup else 2.0)
+        if i >= args.warmup:
+            vals.append(cb["value"])
+            secs.append(cb["seconds"])
+            base = cb
+    value = float(np.median(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round_bytes() / (value * 1e9) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": base["sample"]},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": base["cores"],
+                             "kind": "oracle", "sample": base["sample"]},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import weight_only_int4_w4a16_gb300 as w4
+    w4.w4a16_init(local, 512 << 20)
+
+    stream = torch.cuda.Stream(device=dev)
+    lin, xs, _ = build_round(dev, layers=args.layers)
+    descs = w4.make_descs(lin)
+    torch.cuda.synchronize()
+
+    # ---- timed region: K decode rounds --------------------------------------
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    w4.w4a16_probe_reset()
+    for _ in range(args.warmup):
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    probe0 = w4.w4a16_probe_counts()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    probe1 = w4.w4a16_probe_counts()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    launches = int(sum(probe1) - sum(probe0))
+
+    rb = round_bytes(layers=args.layers)
+    value = rb * args.steps * world / elapsed / 1e9
+    ms = elapsed / args.steps * 1e3
+    peak, peak_kind = load_peaks()
+
+    # ---- dominant kernel, timed launch by launch on the same stream ---------
+    stats = per_kernel_durations(w4, lin, max(2, min(args.steps, 4)), stream)
+    top = max(stats, key=lambda r: stats[r][1])
+    n_l, t_l, b_l = stats[top]
+    achieved = (b_l / n_l) / (t_l / n_l) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"gemv_kernel rung={w4.rung_name(top)}",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
+                "traffic": None, "launches_timed": n_l,
+                "mean_launch_us": t_l / n_l * 1e6,
+                "mean_algorithmic_bytes_per_launch": b_l / n_l}
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    e2e_s, h2d, d2h = time_e2e(w4, lin, xs, max(3, args.steps // 2), 2, stream)
+    e2e_steps = max(3, args.steps // 2)
+    e2e = {"value": rb * e2e_steps * world / e2e_s / 1e9, "unit": "GB/s",
+           "ms_per_step": e2e_s / e2e_steps * 1e3, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    # ---- graph replay of the same round --------------------------------------
+    g = w4.RoundGraph(descs, M_ROUND)
+    for _ in range(2):
+        g.launch(stream)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        g.launch(stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = a.elapsed_time(b) / args.steps
+    g.destroy()
+
+    extra = {"round_graph_ms": graph_ms, "round_graph_GBps": rb / (graph_ms / 1e3) / 1e9,
+             "round_bytes": rb, "launches_per_round": launches // max(1, args.steps),
+             "rung_per_shape": {n: w4.rung_name(w4.w4a16_select_rung(M_ROUND, N, K))
+                                for n, K, N in ROUND_SHAPES}}
+    del lin, descs
+    torch.cuda.empty_cache()
+
+    if not args.no_extra and rank == 0:
+        flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
+        singles = {}
+        for label, M, N, K, cfg in [("cfg1_M1_K5120_N34816", 1, 34816, 5120, 1),
+                                    ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
+                                    ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] + \
+                [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)]:
+            t = time_single(w4, M, N, K, cfg, dev, flush=flush)
+            by = linear_bytes(M, N, K)
+            singles[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
+                              "rung": w4.rung_name(w4.w4a16_select_rung(M, N, K))}
+        extra["single_linear_l2_flushed"] = singles
+        del flush
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cb = cpu_baseline()
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "layers": args.layers, "M": M_ROUND,
+                           "l2": "inputs larger than L2: 11.4 GB of weights per step",
+                           "percent_of_hbm_peak": 100.0 * value / world / peak,
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "cpu_baseline": cpu, "extra": extra}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) group-wise INT4 weight-only linear
+ * layer library (W4A16).
+ *
+ * The operation (forum.sourcefind.cn thread "vLLM on Hygon Z100", section 四
+ * "W4A16"; haowenji.com V100 decode article, paragraph on "groupwise-int"):
+ * weights are 4-bit integers q with one fp16 scale s and one 4-bit zero z per
+ * group of 128 consecutive inputs; the layer restores w = (q - z) * s and
+ * multiplies it with fp16 activations, accumulating in fp32:
+ *
+ *     y[m, n] = sum_k x[m, k] * (q[n, k] - z[n, k / 128]) * s[n, k / 128]
+ *
+ * for m < M (tokens: 1 for plain decode, 4..8 for a speculative verify pass of
+ * 1 + 3 .. 1 + 7 tokens that reads the weights once; section 五 of the same
+ * thread, "M = 2, 4, 8"), n < N (outputs) and k < K (inputs).
+ *
+ * Data layout (all row-major, all little-endian):
+ *   x       [M, K]            fp16 (passed as uint16_t bit patterns)
+ *   qweight [N, K/8]          uint32; element k of row n is bits
+ *                             4*(k%8) .. 4*(k%8)+3 of word k/8 (the thread's
+ *                             "[N,K/8] int32" packed INT4 layout, section 四;
+ *                             the nibble order within a word is this library's
+ *                             reading: the pages do not state one)
+ *   scales  [N, K/128]        fp16
+ *   zeros   [N, ceil(G/8)]    uint32, G = K/128; group g of row n is nibble
+ *                             g%8 of word g/8; nibbles past G are ignored
+ *   y       [M, N]            fp16, fully overwritten, round-to-nearest-even
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  The caller
+ *     owns every buffer; the library never frees or keeps caller pointers past
+ *     the call (a captured graph keeps them, see w4a16_round_graph_create).
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Work is enqueued asynchronously; nothing synchronises.
+ *   - Arguments are validated on the host before anything is enqueued.  A
+ *     nonzero status means nothing was launched.  A device fault inside a
+ *     kernel surfaces, as usual for CUDA, at the caller's next synchronisation.
+ *   - group must be 128 (W4A16_ERR_UNSUPPORTED otherwise); K must be a
+ *     positive multiple of 128, at most 2^22; 1 <= N < 2^31; 1 <= M <= 65535.
+ *   - x, qweight and y must be 16-byte aligned, scales 2-byte, zeros 4-byte
+ *     (W4A16_ERR_MISALIGNED).  x and y must not overlap (INVALID_ARG).
+ *   - w4a16_linear and w4a16_decode_round allocate nothing, free nothing and
+ *     never synchronise, so they may be captured into a CUDA graph.  They need
+ *     w4a16_init first (the split-K workspace and the kernel attributes).
+ *   - The split-K workspace is shared by every call: calls that may use it must
+ *     be ordered on one stream (or otherwise serialised).  Two such calls that
+ *     overlap on the GPU race on it.
+ *
+ * Functions return an int status (w4a16_status) unless stated otherwise.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = 1,     /* null pointer, bad size, overlap, bad rung */
+    W4A16_ERR_UNSUPPORTED = 2,     /* group != 128, or a forced rung that cannot run the shape */
+    W4A16_ERR_MISALIGNED = 3,      /* pointer alignment below the stated minimum */
+    W4A16_ERR_WORKSPACE = 4,       /* the shape needs more split-K workspace than w4a16_init reserved */
+    W4A16_ERR_NOT_INITIALIZED = 5, /* w4a16_init has not succeeded */
+    W4A16_ERR_CUDA = 6             /* a CUDA runtime call failed; see w4a16_last_cuda_error */
+} w4a16_status;
+
+/* Kernel rungs chosen by the dispatch table (w4a16_select_rung).  Every launch
+ * increments the rung's probe counter (w4a16_probe_counts). */
+typedef enum {
+    W4A16_RUNG_AUTO = -1,
+    W4A16_RUNG_GEMV = 0,        /* CUDA cores: warp per output row, whole K per CTA */
+    W4A16_RUNG_GEMV_SPLITK = 1, /* CUDA cores: K split across CTAs, fixed-order fp32 reduce */
+    W4A16_RUNG_TC = 2,          /* tcgen05 dequant-GEMM, tokens as the MMA N dimension */
+    W4A16_RUNG_TC_SPLITK = 3,   /* tcgen05 dequant-GEMM with K split across CTAs */
+    W4A16_NUM_RUNGS = 4
+} w4a16_rung;
+
+/* Select `device`, reserve `workspace_bytes` of split-K workspace (0: 64 MiB)
+ * plus the reducer's arrival counters, set kernel attributes, and read the
+ * environment once: W4A16_FORCE_RUNG=<name|id> pins a rung, W4A16_LOG=1
+ * prints each dispatch decision to stderr.  Allocates; must not run inside a
+ * stream capture.  Calling it again re-initialises (after w4a16_shutdown's
+ * implicit device synchronisation). */
+int w4a16_init(int device, size_t workspace_bytes);
+
+/* Synchronise the device, free the workspace and drop the library state. */
+int w4a16_shutdown(void);
+
+/* Bytes of split-K workspace the current dispatch needs for this shape (0 if
+ * the selected rung splits nothing).  Pure host query. */
+size_t w4a16_workspace_bytes(int M, int N, int K, int group);
+
+/* Pack 4-bit values into the layout above (load time, before any capture: the
+ * thread's section 四 notes that persistent packed tensors built lazily inside
+ * graph capture were charged to the graph's memory pool).
+ *   q [N, K] uint8 and z [N, K/group] uint8, device; only the low 4 bits of
+ *   each byte are used.  Writes qweight [N, K/8] and zeros [N, ceil(G/8)]
+ *   (pad nibbles 0).  q must be 16-byte aligned; qweight 16-byte; z, zeros
+ *   4-byte. */
+int w4a16_pack(const uint8_t *q, const uint8_t *z, int N, int K, int group,
+               uint32_t *qweight, uint32_t *zeros, void *stream);
+
+/* Inverse of w4a16_pack: q [N, K] and z [N, G] bytes 0..15. */
+int w4a16_unpack(const uint32_t *qweight, const uint32_t *zeros, int N, int K, int group,
+                 uint8_t *q, uint8_t *z, void *stream);
+
+/* Restore the weights: w_f32[n, k] = (q - z) * s exactly (the product has at
+ * most 15 significant bits, so fp32 holds it exactly), and w_f16 = that value
+ * rounded once to fp16 (nearest, ties to even).  Either output may be NULL,
+ * not both.  Outputs [N, K], 16-byte aligned. */
+int w4a16_dequant(const uint32_t *qweight, const uint16_t *scales, const uint32_t *zeros,
+                  int N, int K, int group, float *w_f32, uint16_t *w_f16, void *stream);
+
+/* y = x @ W^T for one W4A16 linear layer (the operation at the top of this
+ * file).  Enqueues one kernel for the rung w4a16_select_rung picks (the
+ * split-K rungs reduce inside the same kernel); the CUDA-core rungs enqueue one
+ * kernel per tile of up to 8 tokens. */
+int w4a16_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                 const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
+                 void *stream);
+
+/* One linear of a decode round.  x is [M, K] and y [M, N]; `group` must be 128. */
+typedef struct {
+    const uint16_t *x;
+    const uint32_t *qweight;
+    const uint16_t *scales;
+    const uint32_t *zeros;
+    uint16_t *y;
+    int N;
+    int K;
+    int group;
+} w4a16_linear_desc;
+
+/* A decode round: the linears of `descs` (a HOST array of n_descs entries,
+ * e.g. 64 layers x {qkv, o, gate+up, down}) run back to back on `stream`, all
+ * at the same M, each reading its weights once (haowenji.com V100 decode
+ * article: one round reads every weight once).  All descriptors are validated
+ * before the first launch. */
+int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream);
+
+/* Capture a decode round into an instantiated CUDA graph (an opaque handle in
+ * *graph).  Allocates and captures on an internal stream: call after
+ * w4a16_init, outside any other capture.  The graph keeps the descriptors'
+ * device pointers and the dispatch decisions made at capture time. */
+int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M,
+                             void **graph);
+/* Replay a captured round on `stream`. */
+int w4a16_round_graph_launch(void *graph, void *stream);
+/* Destroy a captured round (after its last replay has finished). */
+int w4a16_round_graph_destroy(void *graph);
+
+/* The rung the dispatch table picks for a shape (honouring a forced rung), or
+ * -1 for an invalid shape.  Pure host query. */
+int w4a16_select_rung(int M, int N, int K, int group);
+
+/* Force a rung for later calls (W4A16_RUNG_AUTO restores the table).  A forced
+ * rung that cannot run a shape makes that call return W4A16_ERR_UNSUPPORTED.
+ * Returns the previous setting, or -2 for an invalid rung.  Host state only:
+ * graphs captured earlier keep their rungs. */
+int w4a16_set_forced_rung(int rung);
+
+/* Copy min(n, W4A16_NUM_RUNGS) per-rung launch counts into counts (host);
+ * returns the number written.  Counts are host-side dispatch decisions (a
+ * graph replay does not re-count). */
+int w4a16_probe_counts(uint64_t *counts, int n);
+void w4a16_probe_reset(void);
+
+/* Static strings; "?" for unknown values. */
+const char *w4a16_rung_name(int rung);
+const char *w4a16_status_string(int status);
+
+/* The cudaError_t behind the calling thread's last W4A16_ERR_CUDA (0 if none). */
+int w4a16_last_cuda_error(void);
+
+/* Number of streaming multiprocessors of the initialised device (0 before init). */
+int w4a16_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

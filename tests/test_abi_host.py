@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed, no device work).
+
+The library must load, export every function ``include/w4a16.h`` declares,
+and reject bad arguments on the host, before any CUDA call, with the status
+codes the header documents.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def w4():
+    __graft_entry__.build()
+    import weight_only_int4_w4a16_gb300 as w4
+    return w4
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "w4a16.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a16_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(w4):
+    names = header_functions()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(w4.lib, n), f"{n} declared in include/w4a16.h but not exported"
+    assert set(names) == set(w4.binding.EXPORTED)
+
+
+def test_status_and_rung_strings(w4):
+    assert w4.lib.w4a16_status_string(0) == b"ok"
+    assert w4.lib.w4a16_status_string(99) == b"?"
+    assert [w4.rung_name(i) for i in range(4)] == ["gemv", "gemv_splitk", "tc", "tc_splitk"]
+    assert w4.rung_name(-1) == "auto" and w4.rung_name(7) == "?"
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device address": never dereferenced on these paths
+
+
+def _lin(w4, x=A, qw=2 * A, s=3 * A, z=4 * A, M=1, N=64, K=256, group=128, y=5 * A):
+    return w4.lib.w4a16_linear(x, qw, s, z, M, N, K, group, y, None)
+
+
+def test_linear_validation_codes(w4):
+    assert _lin(w4, x=None) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, y=None) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, M=0) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, M=70000) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, N=0) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, K=200) == w4.W4A16_ERR_INVALID_ARG
+    assert _lin(w4, group=64) == w4.W4A16_ERR_UNSUPPORTED
+    assert _lin(w4, x=A + 8) == w4.W4A16_ERR_MISALIGNED
+    assert _lin(w4, qw=2 * A + 4) == w4.W4A16_ERR_MISALIGNED
+    assert _lin(w4, s=3 * A + 1) == w4.W4A16_ERR_MISALIGNED
+    assert _lin(w4, z=4 * A + 2) == w4.W4A16_ERR_MISALIGNED
+    # x and y overlapping
+    assert _lin(w4, y=A + 64) == w4.W4A16_ERR_INVALID_ARG
+    # valid arguments, but no successful w4a16_init in this process
+    if w4.lib.w4a16_device_sm_count() == 0:
+        assert _lin(w4) == w4.W4A16_ERR_NOT_INITIALIZED
+
+
+def test_pack_dequant_validation_codes(w4):
+    L = w4.lib
+    assert L.w4a16_pack(None, A, 4, 256, 128, A, A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_pack(A, A, 4, 256, 32, A, A, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_pack(A + 4, A, 4, 256, 128, A, A, None) == w4.W4A16_ERR_MISALIGNED
+    assert L.w4a16_unpack(A, A, 4, 100, 128, A, A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dequant(A, A, A, 4, 256, 128, None, None, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dequant(A, A, A, 4, 256, 128, A + 4, None, None) == w4.W4A16_ERR_MISALIGNED
+
+
+def test_decode_round_validates_every_descriptor(w4):
+    descs = (w4.LinearDesc * 2)()
+    descs[0] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 64, 256, 128)
+    descs[1] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 64, 250, 128)  # bad K
+    assert w4.lib.w4a16_decode_round(descs, 2, 4, None) == w4.W4A16_ERR_INVALID_ARG
+    assert w4.lib.w4a16_decode_round(descs, 0, 4, None) == w4.W4A16_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert w4.lib.w4a16_round_graph_create(descs, 2, 4, None) == w4.W4A16_ERR_INVALID_ARG
+    assert w4.lib.w4a16_round_graph_launch(None, None) == w4.W4A16_ERR_INVALID_ARG
+    del h
+
+
+def test_dispatch_table_host_queries(w4):
+    # Pure host queries: the table picks a CUDA-core rung for M <= 8 and
+    # rejects invalid shapes.
+    assert w4.w4a16_select_rung(1, 34816, 5120) in (w4.RUNG_GEMV, w4.RUNG_GEMV_SPLITK)
+    assert w4.w4a16_select_rung(1, 1024, 500) == -1
+    assert w4.w4a16_select_rung(0, 1024, 512) == -1
+    prev = w4.w4a16_set_forced_rung(w4.RUNG_GEMV_SPLITK)
+    try:
+        assert w4.w4a16_select_rung(4, 5120, 17408) == w4.RUNG_GEMV_SPLITK
+        assert w4.w4a16_workspace_bytes(4, 5120, 17408) >= 2 * 4 * 5120 * 4
+    finally:
+        w4.w4a16_set_forced_rung(prev)
+    with pytest.raises(ValueError):
+        w4.w4a16_set_forced_rung(9)
+
+
+def test_probe_counters_reset(w4):
+    w4.w4a16_probe_reset()
+    assert w4.w4a16_probe_counts() == [0, 0, 0, 0]

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the oracle.
+
+Bit-exact for pack, unpack and dequant; within the stated tolerance for y on
+every rung; bit-exact for y in the integer special case; run-to-run
+bit-identical per rung.  Inputs come from ``synthetic_inputs`` (the only code
+the two sides share).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic_inputs as si
+from helpers import Case, assert_close, sample_rows, sampled_reference
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+CC_RUNGS = [0, 1]  # gemv, gemv_splitk
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import __graft_entry__
+    __graft_entry__.build()
+    import weight_only_int4_w4a16_gb300 as w4
+    w4.w4a16_init(0, 256 << 20)
+    yield w4
+    w4.w4a16_set_forced_rung(w4.RUNG_AUTO)
+
+
+def forced(w4, rung):
+    class _Ctx:
+        def __enter__(self):
+            self.prev = w4.w4a16_set_forced_rung(rung)
+
+        def __exit__(self, *a):
+            w4.w4a16_set_forced_rung(self.prev)
+    return _Ctx()
+
+
+def run_linear(w4, case, poison=True):
+    x, qw, s, zw = case.to(DEV)
+    y = torch.full((case.M, case.N), float("nan"), dtype=torch.float16, device=DEV) if poison else None
+    y = w4.w4a16_linear(x, qw, s, zw, y=y)
+    torch.cuda.synchronize()
+    return y
+
+
+# ---------------------------------------------------------------------------
+# generator: the same bits on the device as on the host
+# ---------------------------------------------------------------------------
+def test_synthetic_generator_device_equals_host():
+    seed = si.config_seed(3, 5, 2)
+    qh, sh, zh = si.layer(seed, 300, 1152)
+    qd, sd, zd = si.layer(seed, 300, 1152, device=DEV)
+    assert torch.equal(qd.cpu(), qh) and torch.equal(zd.cpu(), zh)
+    assert torch.equal(sd.cpu().view(torch.int16), sh.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# pack / unpack / dequant: bit-exact
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N,K", [(1, 128), (7, 384), (64, 1152), (1000, 5120), (33, 17408)])
+def test_pack_unpack_bit_exact(w4, N, K):
+    rng = np.random.default_rng(N * 7 + K)
+    q = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    z = rng.integers(0, 16, (N, K // 128), dtype=np.uint8)
+    qw_ref, zw_ref = oracle.pack(q, z)
+    qw, zw = w4.w4a16_pack(torch.from_numpy(q).to(DEV), torch.from_numpy(z).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(si.as_u32(qw), qw_ref)
+    assert np.array_equal(si.as_u32(zw), zw_ref)
+    q2, z2 = w4.w4a16_unpack(qw, zw, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(q2.cpu().numpy(), q) and np.array_equal(z2.cpu().numpy(), z)
+
+
+def test_pack_masks_high_bits(w4):
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 256, (9, 256), dtype=np.uint8)
+    z = rng.integers(0, 256, (9, 2), dtype=np.uint8)
+    qw_ref, zw_ref = oracle.pack(q & 15, z & 15)
+    qw, zw = w4.w4a16_pack(torch.from_numpy(q).to(DEV), torch.from_numpy(z).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(si.as_u32(qw), qw_ref) and np.array_equal(si.as_u32(zw), zw_ref)
+
+
+@pytest.mark.parametrize("N,K", [(256, 128), (37, 1152), (515, 5120)])
+def test_dequant_bit_exact(w4, N, K):
+    seed = si.config_seed(50, 1, N)
+    qw, s, zw = si.layer(seed, N, K)
+    # include negative, subnormal and extreme scales
+    sb = s.view(torch.int16).clone()
+    special = torch.tensor([0x0001, 0x03FF, -0x8000 + 0x0001, 0x7BFF, -0x8000 + 0x3C00, 0x0400],
+                           dtype=torch.int16)
+    sb.view(-1)[: special.numel()] = special
+    s = sb.view(torch.float16)
+    w_exact = oracle.dequant(si.as_u32(qw), si.as_u16(s), si.as_u32(zw), K)
+    w32, w16 = w4.w4a16_dequant(qw.to(DEV), s.to(DEV), zw.to(DEV), K)
+    torch.cuda.synchronize()
+    assert np.array_equal(w32.cpu().numpy(), w_exact.astype(np.float32))
+    assert np.array_equal(w32.cpu().numpy().astype(np.float64), w_exact)  # exact in fp32
+    assert np.array_equal(si.as_u16(w16), oracle.double_to_half(w_exact))
+
+
+# ---------------------------------------------------------------------------
+# linear: tolerance on every rung, seeded shapes spanning tiles and ragged tails
+# ---------------------------------------------------------------------------
+SHAPES = [(1, 1, 128), (1, 7, 256), (1, 1024, 512), (2, 1029, 1152), (3, 64, 5120),
+          (4, 1000, 2048), (5, 130, 384), (6, 257, 640), (7, 96, 1024), (8, 513, 4352),
+          (8, 2000, 17408), (12, 300, 1024), (20, 77, 768), (64, 200, 512)]
+
+
+@pytest.mark.parametrize("rung", CC_RUNGS + [-1])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_linear_matches_oracle(w4, rung, M, N, K):
+    case = Case(si.config_seed(51, M, N % 16), M, N, K)
+    if rung == w4.RUNG_GEMV_SPLITK and K // 128 < 2:
+        pytest.skip("split-K needs two groups")
+    with forced(w4, rung):
+        if rung >= 0:
+            w4.w4a16_probe_reset()
+        try:
+            y = run_linear(w4, case)
+        except w4.W4A16Error as e:
+            if rung == w4.RUNG_GEMV and e.status == w4.W4A16_ERR_UNSUPPORTED:
+                pytest.skip("shape needs split-K on the CUDA-core rung")
+            raise
+        if rung >= 0:
+            assert w4.w4a16_probe_counts()[rung] >= 1
+    assert_close(y, case.reference(), f"rung {rung} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("rung", CC_RUNGS)
+def test_integer_case_bit_exact(w4, rung):
+    # s = 1/16 and x in {-1, 0, 1}: every partial sum is an exact integer
+    # multiple of 1/16 far below 2^24, so y is exact on every rung.
+    M, N, K = 8, 700, 2048
+    rng = np.random.default_rng(11)
+    q = rng.integers(0, 16, (N, K), dtype=np.uint8)
+    z = rng.integers(0, 16, (N, K // 128), dtype=np.uint8)
+    X = rng.integers(-1, 2, (M, K)).astype(np.int64)
+    qw, zw = oracle.pack(q, z)
+    s = np.full((N, K // 128), 0x2C00, dtype=np.uint16)
+    W = q.astype(np.int64) - np.repeat(z.astype(np.int64), 128, axis=1)
+    want = (X @ W.T).astype(np.float64) / 16
+    assert np.abs(want).max() < 2048
+    x = torch.from_numpy(X.astype(np.float16)).to(DEV)
+    with forced(w4, rung):
+        y = w4.w4a16_linear(x, torch.from_numpy(qw.view(np.int32)).to(DEV),
+                            torch.from_numpy(s.view(np.float16)).to(DEV),
+                            torch.from_numpy(zw.view(np.int32)).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(y.float().cpu().numpy().astype(np.float64), want)
+
+
+@pytest.mark.parametrize("rung", CC_RUNGS)
+def test_run_to_run_bit_identical(w4, rung):
+    case = Case(si.config_seed(52), 4, 5120, 17408)
+    with forced(w4, rung):
+        try:
+            a = run_linear(w4, case)
+        except w4.W4A16Error:
+            pytest.skip("rung cannot run this shape")
+        b = run_linear(w4, case)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_varying_sizes_back_to_back(w4):
+    # Stale data between calls of different sizes shows only when sizes vary
+    # (forum thread "vLLM on Hygon Z100", section 三: the all-reduce bug found
+    # only by changing message sizes); launch them all, then check them all.
+    rng = np.random.default_rng(12)
+    cases, outs = [], []
+    for i in range(24):
+        M = int(rng.integers(1, 9))
+        N = int(rng.integers(1, 1500))
+        K = 128 * int(rng.integers(1, 40))
+        c = Case(si.config_seed(53, i), M, N, K)
+        x, qw, s, zw = c.to(DEV)
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+        w4.w4a16_linear(x, qw, s, zw, y=y)
+        cases.append(c)
+        outs.append(y)
+    torch.cuda.synchronize()
+    for c, y in zip(cases, outs):
+        assert_close(y, c.reference(), f"M={c.M} N={c.N} K={c.K}")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled rows
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K,cfg", [(1, 34816, 5120, 1), (4, 5120, 17408, 2),
+                                       (8, 5120, 17408, 2)])
+def test_full_size_sampled(w4, M, N, K, cfg):
+    seed = si.config_seed(cfg, 0, M)
+    qw, s, zw = si.layer(seed, N, K, device=DEV)
+    x = si.x(seed, M, K)
+    y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+    torch.cuda.synchronize()
+    rows = sample_rows(N, 48, seed=cfg)
+    ref = sampled_reference(seed, x, N, K, rows)
+    # max|y_ref| is taken over the sampled rows only: at most the whole
+    # output's maximum, so this bound is the stricter one
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"cfg{cfg} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
+def test_m_sweep_sampled(w4, M):
+    N, K = 27648, 5120
+    seed = si.config_seed(4)
+    qw, s, zw = si.layer(seed, N, K, device=DEV)
+    x = si.x(seed, M, K)
+    y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+    torch.cuda.synchronize()
+    rows = sample_rows(N, 16, seed=M)
+    ref = sampled_reference(seed, x, N, K, rows)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"sweep M={M}")
+
+
+ROUND_SHAPES = [(5120, 8192), (6144, 5120), (5120, 34816), (17408, 5120)]  # (K, N)
+
+
+def _round(w4, n_layers, M, seed_cfg=3):
+    layers = []
+    xs = {}
+    for j, (K, N) in enumerate(ROUND_SHAPES):
+        xs[j] = si.x(si.config_seed(seed_cfg, 0, 8 + j), M, K)
+    for l in range(n_layers):
+        for j, (K, N) in enumerate(ROUND_SHAPES):
+            seed = si.config_seed(seed_cfg, l, j)
+            qw, s, zw = si.layer(seed, N, K, device=DEV)
+            layers.append(dict(x=xs[j].to(DEV), qweight=qw, scales=s, zeros=zw,
+                               y=torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV),
+                               seed=seed, N=N, K=K, j=j))
+    return layers, xs
+
+
+def test_decode_round_eager_and_graph(w4):
+    M = 4
+    layers, xs = _round(w4, 2, M)
+    descs = w4.make_descs(layers)
+    w4.w4a16_decode_round(descs, M)
+    torch.cuda.synchronize()
+    eager = [L["y"].clone() for L in layers]
+    for L in layers:
+        L["y"].fill_(float("nan"))
+    g = w4.RoundGraph(descs, M)
+    g.launch()
+    torch.cuda.synchronize()
+    g.destroy()
+    for L, e in zip(layers, eager):
+        assert torch.equal(L["y"].view(torch.int16), e.view(torch.int16))
+        rows = sample_rows(L["N"], 8, seed=L["seed"] & 0xFFFF)
+        ref = sampled_reference(L["seed"], xs[L["j"]], L["N"], L["K"], rows)
+        assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, f"round layer j={L['j']}")
+
+
+@pytest.mark.slow
+def test_decode_round_full_64_layers_sampled(w4):
+    M = 4
+    layers, xs = _round(w4, 64, M)
+    descs = w4.make_descs(layers)
+    w4.w4a16_decode_round(descs, M)
+    torch.cuda.synchronize()
+    for L in layers:
+        rows = sample_rows(L["N"], 4, seed=L["seed"] & 0xFFFF)
+        ref = sampled_reference(L["seed"], xs[L["j"]], L["N"], L["K"], rows)
+        assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, f"layer seed {L['seed']}")
+    del layers
+    torch.cuda.empty_cache()

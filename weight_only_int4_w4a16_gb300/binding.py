@@ -1,0 +1,252 @@
+"""Thin ctypes binding over the C ABI in ``include/w4a16.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``_lib/libw4a16.so``.  Tensors are torch CUDA tensors (device memory
+and streams come from PyTorch); fp16 data crosses the ABI as uint16 bit
+patterns.  Importing this module fails loudly if the library has not been
+built: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libw4a16.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"W4A16 CUDA library not built ({LIB_PATH} missing). Build it with "
+        "`python -m weight_only_int4_w4a16_gb300.build` or __graft_entry__.build().")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+GROUP = 128
+
+W4A16_OK = 0
+W4A16_ERR_INVALID_ARG = 1
+W4A16_ERR_UNSUPPORTED = 2
+W4A16_ERR_MISALIGNED = 3
+W4A16_ERR_WORKSPACE = 4
+W4A16_ERR_NOT_INITIALIZED = 5
+W4A16_ERR_CUDA = 6
+
+RUNG_AUTO = -1
+RUNG_GEMV = 0
+RUNG_GEMV_SPLITK = 1
+RUNG_TC = 2
+RUNG_TC_SPLITK = 3
+NUM_RUNGS = 4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+class LinearDesc(ctypes.Structure):
+    """Mirror of ``w4a16_linear_desc``."""
+    _fields_ = [("x", _P), ("qweight", _P), ("scales", _P), ("zeros", _P), ("y", _P),
+                ("N", _I), ("K", _I), ("group", _I)]
+
+
+def _sig(name, args, res=_I):
+    f = getattr(lib, name)
+    f.argtypes = args
+    f.restype = res
+    return f
+
+
+_sig("w4a16_init", [_I, _SZ])
+_sig("w4a16_shutdown", [])
+_sig("w4a16_workspace_bytes", [_I, _I, _I, _I], _SZ)
+_sig("w4a16_pack", [_P, _P, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_unpack", [_P, _P, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_dequant", [_P, _P, _P, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
+_sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
+_sig("w4a16_round_graph_launch", [_P, _P])
+_sig("w4a16_round_graph_destroy", [_P])
+_sig("w4a16_select_rung", [_I, _I, _I, _I])
+_sig("w4a16_set_forced_rung", [_I])
+_sig("w4a16_probe_counts", [ctypes.POINTER(ctypes.c_uint64), _I])
+_sig("w4a16_probe_reset", [], None)
+_sig("w4a16_rung_name", [_I], ctypes.c_char_p)
+_sig("w4a16_status_string", [_I], ctypes.c_char_p)
+_sig("w4a16_last_cuda_error", [])
+_sig("w4a16_device_sm_count", [])
+
+EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
+            "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_decode_round",
+            "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
+            "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
+            "w4a16_probe_reset", "w4a16_rung_name", "w4a16_status_string",
+            "w4a16_last_cuda_error", "w4a16_device_sm_count"]
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = lib.w4a16_status_string(status).decode()
+        if status == W4A16_ERR_CUDA:
+            msg += f" (cudaError {lib.w4a16_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [status {status}]")
+
+
+def _check(status: int, what: str):
+    if status != W4A16_OK:
+        raise W4A16Error(status, what)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def rung_name(rung: int) -> str:
+    return lib.w4a16_rung_name(rung).decode()
+
+
+# ---------------------------------------------------------------------------
+# Same names as the C ABI
+# ---------------------------------------------------------------------------
+def w4a16_init(device: int = 0, workspace_bytes: int = 0) -> None:
+    _check(lib.w4a16_init(device, workspace_bytes), "w4a16_init")
+
+
+def w4a16_shutdown() -> None:
+    _check(lib.w4a16_shutdown(), "w4a16_shutdown")
+
+
+def w4a16_workspace_bytes(M: int, N: int, K: int, group: int = GROUP) -> int:
+    return int(lib.w4a16_workspace_bytes(M, N, K, group))
+
+
+def w4a16_pack(q: torch.Tensor, z: torch.Tensor, group: int = GROUP, qweight=None, zeros=None,
+               stream=None):
+    """q [N, K] uint8, z [N, K/group] uint8 -> (qweight [N, K/8], zeros [N, ceil(G/8)]) int32 (uint32 bits)."""
+    N, K = q.shape
+    G = K // group if group else 0
+    if qweight is None:
+        qweight = torch.empty((N, K // 8), dtype=torch.int32, device=q.device)
+    if zeros is None:
+        zeros = torch.empty((N, (G + 7) // 8), dtype=torch.int32, device=q.device)
+    _check(lib.w4a16_pack(_dev(q, torch.uint8, "q"), _dev(z, torch.uint8, "z"), N, K, group,
+                          _dev(qweight, torch.int32, "qweight"), _dev(zeros, torch.int32, "zeros"),
+                          _stream_ptr(stream)), "w4a16_pack")
+    return qweight, zeros
+
+
+def w4a16_unpack(qweight: torch.Tensor, zeros: torch.Tensor, K: int, group: int = GROUP,
+                 stream=None):
+    N = qweight.shape[0]
+    G = K // group if group else 0
+    q = torch.empty((N, K), dtype=torch.uint8, device=qweight.device)
+    z = torch.empty((N, G), dtype=torch.uint8, device=qweight.device)
+    _check(lib.w4a16_unpack(_dev(qweight, torch.int32, "qweight"), _dev(zeros, torch.int32, "zeros"),
+                            N, K, group, q.data_ptr(), z.data_ptr(), _stream_ptr(stream)),
+           "w4a16_unpack")
+    return q, z
+
+
+def w4a16_dequant(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, K: int,
+                  group: int = GROUP, f32: bool = True, f16: bool = True, stream=None):
+    N = qweight.shape[0]
+    w32 = torch.empty((N, K), dtype=torch.float32, device=qweight.device) if f32 else None
+    w16 = torch.empty((N, K), dtype=torch.float16, device=qweight.device) if f16 else None
+    _check(lib.w4a16_dequant(_dev(qweight, torch.int32, "qweight"),
+                             _dev(scales, torch.float16, "scales"), _dev(zeros, torch.int32, "zeros"),
+                             N, K, group, w32.data_ptr() if f32 else None,
+                             w16.data_ptr() if f16 else None, _stream_ptr(stream)), "w4a16_dequant")
+    return w32, w16
+
+
+def w4a16_linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                 zeros: torch.Tensor, group: int = GROUP, y=None, stream=None) -> torch.Tensor:
+    """y [M, N] fp16 = x [M, K] fp16 @ dequant(qweight, scales, zeros)^T."""
+    M, K = x.shape
+    N = qweight.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check(lib.w4a16_linear(_dev(x, torch.float16, "x"), _dev(qweight, torch.int32, "qweight"),
+                            _dev(scales, torch.float16, "scales"), _dev(zeros, torch.int32, "zeros"),
+                            M, N, K, group, _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+           "w4a16_linear")
+    return y
+
+
+def make_descs(layers) -> ctypes.Array:
+    """layers: iterable of dicts with x, qweight, scales, zeros, y tensors -> host desc array."""
+    layers = list(layers)
+    arr = (LinearDesc * len(layers))()
+    for i, L in enumerate(layers):
+        N, K = L["qweight"].shape[0], L["x"].shape[1]
+        arr[i] = LinearDesc(_dev(L["x"], torch.float16, "x"), _dev(L["qweight"], torch.int32, "qweight"),
+                            _dev(L["scales"], torch.float16, "scales"),
+                            _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], torch.float16, "y"),
+                            N, K, L.get("group", GROUP))
+    return arr
+
+
+def w4a16_decode_round(descs, M: int, stream=None) -> None:
+    _check(lib.w4a16_decode_round(descs, len(descs), M, _stream_ptr(stream)), "w4a16_decode_round")
+
+
+class RoundGraph:
+    """A decode round captured once into a CUDA graph and replayed."""
+
+    def __init__(self, descs, M: int):
+        self._descs = descs  # keep the host array alive for the graph's lifetime
+        h = _P()
+        _check(lib.w4a16_round_graph_create(descs, len(descs), M, ctypes.byref(h)),
+               "w4a16_round_graph_create")
+        self.handle = h.value
+
+    def launch(self, stream=None) -> None:
+        _check(lib.w4a16_round_graph_launch(self.handle, _stream_ptr(stream)),
+               "w4a16_round_graph_launch")
+
+    def destroy(self) -> None:
+        if self.handle:
+            _check(lib.w4a16_round_graph_destroy(self.handle), "w4a16_round_graph_destroy")
+            self.handle = None
+
+
+def w4a16_select_rung(M: int, N: int, K: int, group: int = GROUP) -> int:
+    return int(lib.w4a16_select_rung(M, N, K, group))
+
+
+def w4a16_set_forced_rung(rung: int) -> int:
+    prev = int(lib.w4a16_set_forced_rung(rung))
+    if prev == -2:
+        raise ValueError(f"invalid rung {rung}")
+    return prev
+
+
+def w4a16_probe_counts() -> list[int]:
+    buf = (ctypes.c_uint64 * NUM_RUNGS)()
+    n = lib.w4a16_probe_counts(buf, NUM_RUNGS)
+    return [int(buf[i]) for i in range(n)]
+
+
+def w4a16_probe_reset() -> None:
+    lib.w4a16_probe_reset()
+
+
+def w4a16_device_sm_count() -> int:
+    return int(lib.w4a16_device_sm_count())

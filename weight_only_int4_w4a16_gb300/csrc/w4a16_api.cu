@@ -1,0 +1,398 @@
+// C ABI of the W4A16 library: argument validation, the dispatch table with its
+// per-rung probe counters, the split-K workspace, decode rounds and their
+// CUDA-graph capture.  See include/w4a16.h for the contract of each call.
+//
+// Dispatch follows the ninfer-perf-tuning notes (section 二, "first ask which
+// rung ran"): rungs are chosen from the shape (M, N, K), the table is frozen
+// for the process, an environment variable read once at init can pin a rung,
+// and every launch bumps its rung's counter so a run can prove which branch it
+// took.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "w4a16_internal.h"
+
+using namespace w4a16;
+
+namespace {
+
+struct State {
+    bool initialized = false;
+    DeviceInfo dev{};
+    Workspace ws{};
+    void *ws_base = nullptr;
+    int forced_rung = W4A16_RUNG_AUTO;
+    bool log = false;
+};
+
+State g_state;
+std::mutex g_mutex;
+std::atomic<unsigned long long> g_probe[W4A16_NUM_RUNGS];
+thread_local int t_last_cuda_error = 0;
+
+constexpr size_t kDefaultWorkspace = 64ull << 20;
+constexpr int kCounters = 1 << 16;
+constexpr int kMaxM = 65535;
+
+const char *const kRungNames[W4A16_NUM_RUNGS] = {"gemv", "gemv_splitk", "tc", "tc_splitk"};
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return W4A16_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+constexpr int kMaxK = 1 << 22;
+
+int check_shape(int N, int K, int group) {
+    if (N < 1 || K < 1 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
+    if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (K % kGroup != 0) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+int check_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                 const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y) {
+    if (!x || !qweight || !scales || !zeros || !y) return W4A16_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxM) return W4A16_ERR_INVALID_ARG;
+    int st = check_shape(N, K, group);
+    if (st) return st;
+    if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
+        !aligned(zeros, 4))
+        return W4A16_ERR_MISALIGNED;
+    if (overlaps(x, (size_t)M * K * 2, y, (size_t)M * N * 2)) return W4A16_ERR_INVALID_ARG;
+    return W4A16_OK;
+}
+
+// The dispatch table.  Rungs that cannot run a shape are skipped in auto mode;
+// a forced rung that cannot run it makes the call fail with UNSUPPORTED.
+struct Decision {
+    int rung;
+    int status;
+};
+
+Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
+    const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
+    if (forced == W4A16_RUNG_GEMV) {
+        GemvPlan p = plan_gemv(Mt, N, K, 0, dev);
+        return {W4A16_RUNG_GEMV, p.ok ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
+    }
+    if (forced == W4A16_RUNG_GEMV_SPLITK) {
+        if (K / kGroup < 2) return {W4A16_RUNG_GEMV_SPLITK, W4A16_ERR_UNSUPPORTED};
+        return {W4A16_RUNG_GEMV_SPLITK, W4A16_OK};
+    }
+    if (forced == W4A16_RUNG_TC || forced == W4A16_RUNG_TC_SPLITK)
+        return {forced, W4A16_ERR_UNSUPPORTED};
+    GemvPlan p = plan_gemv(Mt, N, K, -1, dev);
+    return {p.S > 1 ? W4A16_RUNG_GEMV_SPLITK : W4A16_RUNG_GEMV, W4A16_OK};
+}
+
+// Per-launch plan for the CUDA-core rungs: one launch per tile of <= 8 tokens.
+GemvPlan gemv_plan_for(int rung, int Mt, int N, int K, const DeviceInfo &dev) {
+    return plan_gemv(Mt, N, K, rung == W4A16_RUNG_GEMV ? 0 : (rung == W4A16_RUNG_GEMV_SPLITK ? 1 : -1),
+                     dev);
+}
+
+int check_workspace(int rung, int M, int N, int K, const State &st) {
+    if (rung == W4A16_RUNG_GEMV || rung == W4A16_RUNG_GEMV_SPLITK) {
+        for (int m0 = 0; m0 < M; m0 += kGemvMaxTokens) {
+            int Mt = M - m0 < kGemvMaxTokens ? M - m0 : kGemvMaxTokens;
+            GemvPlan p = gemv_plan_for(rung, Mt, N, K, st.dev);
+            if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+            if (p.ws_bytes > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
+            if (p.S > 1 && p.n_row_blocks > st.ws.n_counters) return W4A16_ERR_WORKSPACE;
+            if (m0 + kGemvMaxTokens >= M) break;  // all full tiles share one plan
+        }
+    }
+    return W4A16_OK;
+}
+
+int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    for (int m0 = 0; m0 < a.M && e == cudaSuccess; m0 += kGemvMaxTokens) {
+        int Mt = a.M - m0 < kGemvMaxTokens ? a.M - m0 : kGemvMaxTokens;
+        GemvPlan p = gemv_plan_for(rung, Mt, a.N, a.K, st.dev);
+        LinearArgs t = a;
+        t.x = a.x + (size_t)m0 * a.K;
+        t.y = a.y + (size_t)m0 * a.N;
+        t.M = Mt;
+        e = launch_gemv(t, p, st.ws, stream);
+        g_probe[rung].fetch_add(1, std::memory_order_relaxed);
+    }
+    if (st.log)
+        fprintf(stderr, "[w4a16] linear M=%d N=%d K=%d -> %s\n", a.M, a.N, a.K, kRungNames[rung]);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int parse_rung(const char *s) {
+    if (!s || !*s) return W4A16_RUNG_AUTO;
+    for (int i = 0; i < W4A16_NUM_RUNGS; ++i)
+        if (!strcmp(s, kRungNames[i])) return i;
+    if (!strcmp(s, "auto")) return W4A16_RUNG_AUTO;
+    char *end = nullptr;
+    long v = strtol(s, &end, 10);
+    if (end && *end == 0 && v >= 0 && v < W4A16_NUM_RUNGS) return (int)v;
+    return W4A16_RUNG_AUTO;
+}
+
+int linear_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
+                void *stream, bool validated) {
+    if (!validated) {
+        int st = check_linear(x, qweight, scales, zeros, M, N, K, group, y);
+        if (st) return st;
+    }
+    const State &s = g_state;
+    if (!s.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    Decision d = decide(M, N, K, s.dev, s.forced_rung);
+    if (d.status) return d.status;
+    int st = check_workspace(d.rung, M, N, K, s);
+    if (st) return st;
+    LinearArgs a{reinterpret_cast<const __half *>(x), qweight,
+                 reinterpret_cast<const __half *>(scales), zeros,
+                 reinterpret_cast<__half *>(y), M, N, K};
+    return launch_linear(a, d.rung, s, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int w4a16_init(int device, size_t workspace_bytes) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    State &s = g_state;
+    if (s.initialized) {
+        cudaDeviceSynchronize();
+        cudaFree(s.ws_base);
+        s = State{};
+    }
+    cudaError_t e = cudaSetDevice(device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceInfo dev{};
+    dev.device = device;
+    e = cudaDeviceGetAttribute(&dev.sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&dev.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   device);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (workspace_bytes == 0) workspace_bytes = kDefaultWorkspace;
+    workspace_bytes = (workspace_bytes + 255) & ~(size_t)255;
+    const size_t counter_bytes = (size_t)kCounters * sizeof(unsigned);
+    void *base = nullptr;
+    e = cudaMalloc(&base, workspace_bytes + counter_bytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemset((char *)base + workspace_bytes, 0, counter_bytes);
+    if (e == cudaSuccess) e = gemv_init_attributes(dev);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(base);
+        return cuda_fail(e);
+    }
+    s.dev = dev;
+    s.ws_base = base;
+    s.ws.partials = (float *)base;
+    s.ws.partial_bytes = workspace_bytes;
+    s.ws.counters = (unsigned *)((char *)base + workspace_bytes);
+    s.ws.n_counters = kCounters;
+    s.forced_rung = parse_rung(getenv("W4A16_FORCE_RUNG"));
+    const char *lg = getenv("W4A16_LOG");
+    s.log = lg && *lg && strcmp(lg, "0") != 0;
+    s.initialized = true;
+    return W4A16_OK;
+}
+
+int w4a16_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    State &s = g_state;
+    if (!s.initialized) return W4A16_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t f = cudaFree(s.ws_base);
+    s = State{};
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (f != cudaSuccess) return cuda_fail(f);
+    return W4A16_OK;
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K, int group) {
+    if (M < 1 || M > kMaxM || check_shape(N, K, group)) return 0;
+    DeviceInfo dev = g_state.dev;
+    if (!g_state.initialized) dev.sm_count = 152;
+    Decision d = decide(M, N, K, dev, g_state.forced_rung);
+    if (d.status) return 0;
+    size_t need = 0;
+    for (int m0 = 0; m0 < M; m0 += kGemvMaxTokens) {
+        int Mt = M - m0 < kGemvMaxTokens ? M - m0 : kGemvMaxTokens;
+        GemvPlan p = gemv_plan_for(d.rung, Mt, N, K, dev);
+        if (p.ws_bytes > need) need = p.ws_bytes;
+        if (m0 + kGemvMaxTokens >= M) break;
+    }
+    return need;
+}
+
+int w4a16_pack(const uint8_t *q, const uint8_t *z, int N, int K, int group, uint32_t *qweight,
+               uint32_t *zeros, void *stream) {
+    if (!q || !z || !qweight || !zeros) return W4A16_ERR_INVALID_ARG;
+    int st = check_shape(N, K, group);
+    if (st) return st;
+    if (!aligned(q, 16) || !aligned(qweight, 16) || !aligned(z, 4) || !aligned(zeros, 4))
+        return W4A16_ERR_MISALIGNED;
+    cudaError_t e = launch_pack(q, z, N, K, qweight, zeros, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_unpack(const uint32_t *qweight, const uint32_t *zeros, int N, int K, int group,
+                 uint8_t *q, uint8_t *z, void *stream) {
+    if (!q || !z || !qweight || !zeros) return W4A16_ERR_INVALID_ARG;
+    int st = check_shape(N, K, group);
+    if (st) return st;
+    if (!aligned(q, 16) || !aligned(qweight, 16) || !aligned(z, 4) || !aligned(zeros, 4))
+        return W4A16_ERR_MISALIGNED;
+    cudaError_t e = launch_unpack(qweight, zeros, N, K, q, z, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_dequant(const uint32_t *qweight, const uint16_t *scales, const uint32_t *zeros, int N,
+                  int K, int group, float *w_f32, uint16_t *w_f16, void *stream) {
+    if (!qweight || !scales || !zeros || (!w_f32 && !w_f16)) return W4A16_ERR_INVALID_ARG;
+    int st = check_shape(N, K, group);
+    if (st) return st;
+    if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(zeros, 4) ||
+        (w_f32 && !aligned(w_f32, 16)) || (w_f16 && !aligned(w_f16, 16)))
+        return W4A16_ERR_MISALIGNED;
+    cudaError_t e = launch_dequant(qweight, reinterpret_cast<const __half *>(scales), zeros, N, K,
+                                   w_f32, reinterpret_cast<__half *>(w_f16), (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                 const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
+                 void *stream) {
+    return linear_impl(x, qweight, scales, zeros, M, N, K, group, y, stream, false);
+}
+
+int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {
+    if (!descs || n_descs < 1) return W4A16_ERR_INVALID_ARG;
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y);
+        if (st) return st;
+    }
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung);
+        if (dec.status) return dec.status;
+        int st = check_workspace(dec.rung, M, d.N, d.K, g_state);
+        if (st) return st;
+    }
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        int st = linear_impl(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y, stream,
+                             true);
+        if (st) return st;
+    }
+    return W4A16_OK;
+}
+
+int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M, void **graph) {
+    if (!graph) return W4A16_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    cudaStream_t s = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(s);
+        return cuda_fail(e);
+    }
+    int st = w4a16_decode_round(descs, n_descs, M, s);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(s, &g);
+    cudaStreamDestroy(s);
+    if (st) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *graph = (void *)exec;
+    return W4A16_OK;
+}
+
+int w4a16_round_graph_launch(void *graph, void *stream) {
+    if (!graph) return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = cudaGraphLaunch((cudaGraphExec_t)graph, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_round_graph_destroy(void *graph) {
+    if (!graph) return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = cudaGraphExecDestroy((cudaGraphExec_t)graph);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_select_rung(int M, int N, int K, int group) {
+    if (M < 1 || M > kMaxM || check_shape(N, K, group)) return -1;
+    DeviceInfo dev = g_state.dev;
+    if (!g_state.initialized) dev.sm_count = 152;
+    Decision d = decide(M, N, K, dev, g_state.forced_rung);
+    return d.status ? -1 : d.rung;
+}
+
+int w4a16_set_forced_rung(int rung) {
+    if (rung < W4A16_RUNG_AUTO || rung >= W4A16_NUM_RUNGS) return -2;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int prev = g_state.forced_rung;
+    g_state.forced_rung = rung;
+    return prev;
+}
+
+int w4a16_probe_counts(uint64_t *counts, int n) {
+    if (!counts || n < 0) return 0;
+    int k = n < W4A16_NUM_RUNGS ? n : W4A16_NUM_RUNGS;
+    for (int i = 0; i < k; ++i) counts[i] = g_probe[i].load(std::memory_order_relaxed);
+    return k;
+}
+
+void w4a16_probe_reset(void) {
+    for (auto &c : g_probe) c.store(0, std::memory_order_relaxed);
+}
+
+const char *w4a16_rung_name(int rung) {
+    if (rung == W4A16_RUNG_AUTO) return "auto";
+    if (rung < 0 || rung >= W4A16_NUM_RUNGS) return "?";
+    return kRungNames[rung];
+}
+
+const char *w4a16_status_string(int status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_INVALID_ARG: return "invalid argument";
+        case W4A16_ERR_UNSUPPORTED: return "unsupported shape or rung";
+        case W4A16_ERR_MISALIGNED: return "misaligned pointer";
+        case W4A16_ERR_WORKSPACE: return "split-K workspace too small";
+        case W4A16_ERR_NOT_INITIALIZED: return "w4a16_init has not succeeded";
+        case W4A16_ERR_CUDA: return "CUDA runtime error";
+    }
+    return "?";
+}
+
+int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
+
+int w4a16_device_sm_count(void) { return g_state.initialized ? g_state.dev.sm_count : 0; }
+
+}  // extern "C"

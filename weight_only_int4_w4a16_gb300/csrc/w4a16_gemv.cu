@@ -1,0 +1,363 @@
+// CUDA-core W4A16 GEMV for M = 1..8 tokens (rungs "gemv" and "gemv_splitk").
+//
+// The method: forum.sourcefind.cn thread "vLLM on Hygon Z100", sections 四 and
+// 五.  Section 四's M = 1 kernel stages the activation on chip, streams the
+// packed INT4 weights with non-temporal loads, gives each wavefront some output
+// rows, multiplies paired fp16 values and accumulates in fp32; section 五's
+// small-M kernel streams the weights once and serves every activation row from
+// them.  The same structure on sm_103a:
+//
+//   * a CTA (8 warps) stages x[:, K-slice] in shared memory once, converted to
+//     the pair order the unpack below produces (convert the input once, before
+//     the inner loop: haowenji.com V100 decode article, the fix that took two
+//     projections from 350 GB/s to full speed);
+//   * a warp owns one output row at a time; lane j streams 16-byte chunks
+//     j, j+32, ... of that row (32 k values, always inside one 128-wide group)
+//     with L1-bypassing 128-bit loads, all of a row's chunks issued before any
+//     is consumed so each lane keeps up to 8 x 16 bytes in flight;
+//   * unpack: a nibble OR-ed into the mantissa of the fp16 constant 1024 (or 64
+//     for the odd nibble positions, which sit 4 bits higher) is the fp16 value
+//     1024 + q (64 + q), two lanes of a 32-bit register at once; subtracting
+//     (1024 + z) is exact and leaves q - z as an fp16 integer.  This is the
+//     "splice the integer into the fp16 bit pattern, subtract a fixed offset"
+//     conversion of the V100 article's attention kernel, applied to nibbles;
+//   * dot product: fma.rn.f32.f16 multiplies two fp16 values exactly and adds
+//     in fp32, per token; each chunk's sum is scaled by its group's fp32 scale
+//     once (scale hoisted out of the inner loop);
+//   * the 32 lane sums of a row are combined with xor-shuffles.
+//
+// Split-K (ninfer-perf-tuning notes, rule 21 and the per-shape knob table:
+// split K only when the row grid cannot fill the GPU, keep several K steps per
+// slice; reduce in fp32): each (row block, slice) CTA writes fp32 partials,
+// bumps the row block's arrival counter, and the CTA that arrives last sums the
+// S partials in slice order 0..S-1 and writes y.  No CTA ever waits for
+// another, and the sum order does not depend on arrival order, so results are
+// bit-identical from run to run.
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxIters = 8;         // 16-byte chunks per lane per row and slice
+constexpr int kChunkK = 32;          // k values per 16-byte chunk
+constexpr int kMaxSliceChunks = 32 * kMaxIters;
+constexpr int kRowsPerCta = 64;
+constexpr int kSmemBudget = 72 * 1024;  // staged activations per CTA
+
+struct GemvParams {
+    const __half *x;
+    const uint32_t *qw;
+    const __half *scales;
+    const uint32_t *zeros;
+    __half *y;
+    float *partials;
+    unsigned *counters;
+    int N, K, G, ZW, KW;
+    int S, slice_groups;
+    int n_row_blocks;
+};
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;  // (a & b) | c
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// a0 += lo(w) * lo(x), a1 += hi(w) * hi(x): fp16 x fp16 products (exact) added in fp32.
+__device__ __forceinline__ void fma_pair(float &a0, float &a1, uint32_t w, uint32_t x) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w), "r"(x));
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 8 consecutive fp16 (h0..h7) -> pairs (h0,h4) (h1,h5) (h2,h6) (h3,h7): the
+// order in which the unpack below yields the nibbles of one word.
+__device__ __forceinline__ uint4 pair_order(uint4 v) {
+    uint4 o;
+    o.x = prmt(v.x, v.z, 0x5410);
+    o.y = prmt(v.x, v.z, 0x7632);
+    o.z = prmt(v.y, v.w, 0x5410);
+    o.w = prmt(v.y, v.w, 0x7632);
+    return o;
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(GemvParams p) {
+    extern __shared__ uint4 xs[];  // [M][nCB][4][32] uint4
+    __shared__ int s_last;
+
+    const int s = blockIdx.y;
+    const int g0 = s * p.slice_groups;
+    const int g1 = min(p.G, g0 + p.slice_groups);
+    const int k0 = g0 * kGroup;
+    const int nchunks = (g1 - g0) * (kGroup / kChunkK);
+    const int nCB = (nchunks + 31) / 32;
+
+    // Stage x[:, k0 : k0 + 32*nchunks] in pair order.  Piece (m, c, t) holds
+    // the 8 values of word t of chunk c; lane c%32 reads it with one LDS.128.
+    for (int i = threadIdx.x; i < M * nchunks * 4; i += kThreads) {
+        int m = i / (nchunks * 4);
+        int rem = i - m * nchunks * 4;
+        int c = rem >> 2, t = rem & 3;
+        uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0 + kChunkK * c +
+                                                        8 * t));
+        xs[((m * nCB + (c >> 5)) * 4 + t) * 32 + (c & 31)] = pair_order(v);
+    }
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int rb = blockIdx.x; rb < p.n_row_blocks; rb += gridDim.x) {
+        const int row0 = rb * kRowsPerCta;
+        const int row_end = min(p.N, row0 + kRowsPerCta);
+
+        for (int n = row0 + warp; n < row_end; n += kWarps) {
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(p.qw + (size_t)n * p.KW + k0 / 8);
+            uint4 wv[kMaxIters];
+            float sc[kMaxIters];
+            uint32_t zq[kMaxIters];
+#pragma unroll
+            for (int i = 0; i < kMaxIters; ++i) {
+                const int c = lane + 32 * i;
+                if (i < nCB && c < nchunks) {
+                    wv[i] = ld_stream(wrow + c);
+                    const int g = g0 + (c >> 2);
+                    sc[i] = __half2float(p.scales[(size_t)n * p.G + g]);
+                    zq[i] = (__ldg(p.zeros + (size_t)n * p.ZW + (g >> 3)) >> (4 * (g & 7))) & 0xfu;
+                }
+            }
+            float acc[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) acc[m] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMaxIters; ++i) {
+                const int c = lane + 32 * i;
+                if (i < nCB && c < nchunks) {
+                    const uint32_t z = zq[i];
+                    const uint32_t zz_hi = 0x64006400u | z | (z << 16);         // 1024 + z
+                    const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);  // 64 + z
+                    float part0[M], part1[M];
+#pragma unroll
+                    for (int m = 0; m < M; ++m) part0[m] = part1[m] = 0.f;
+                    const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t w = words[t];
+                        const uint32_t w8 = w >> 8;
+                        const uint32_t d0 = hsub2(lop3_and_or(w, 0x000f000fu, 0x64006400u), zz_hi);
+                        const uint32_t d1 = hsub2(lop3_and_or(w, 0x00f000f0u, 0x54005400u), zz_lo);
+                        const uint32_t d2 = hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi);
+                        const uint32_t d3 = hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo);
+#pragma unroll
+                        for (int m = 0; m < M; ++m) {
+                            const uint4 xv = xs[((m * nCB + i) * 4 + t) * 32 + lane];
+                            fma_pair(part0[m], part1[m], d0, xv.x);
+                            fma_pair(part0[m], part1[m], d1, xv.y);
+                            fma_pair(part0[m], part1[m], d2, xv.z);
+                            fma_pair(part0[m], part1[m], d3, xv.w);
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < M; ++m) acc[m] = fmaf(sc[i], part0[m] + part1[m], acc[m]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+            }
+            if (lane == 0) {
+                if (p.S == 1) {
+#pragma unroll
+                    for (int m = 0; m < M; ++m) p.y[(size_t)m * p.N + n] = __float2half_rn(acc[m]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < M; ++m)
+                        p.partials[((size_t)s * M + m) * p.N + n] = acc[m];
+                }
+            }
+        }
+
+        if (p.S > 1) {
+            // Publish this slice's partials, count the arrival; the last CTA of
+            // the row block sums all slices in fixed order.
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const unsigned prev = atomicAdd(p.counters + rb, 1u);
+                s_last = (prev == (unsigned)(p.S - 1));
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const int nrows = row_end - row0;
+                for (int idx = threadIdx.x; idx < M * nrows; idx += kThreads) {
+                    const int m = idx / nrows;
+                    const int n = row0 + (idx - m * nrows);
+                    float sum = 0.f;
+                    for (int s2 = 0; s2 < p.S; ++s2)
+                        sum += __ldcg(p.partials + ((size_t)s2 * M + m) * p.N + n);
+                    p.y[(size_t)m * p.N + n] = __float2half_rn(sum);
+                }
+                if (threadIdx.x == 0) p.counters[rb] = 0u;  // ready for the next launch
+            }
+            __syncthreads();
+        }
+    }
+}
+
+template <int M>
+cudaError_t launch_m(const GemvParams &p, const GemvPlan &plan, cudaStream_t stream) {
+    dim3 grid(plan.grid_x, plan.S);
+    gemv_kernel<M><<<grid, kThreads, plan.smem_bytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+int occupancy_cache[kGemvMaxTokens + 1][4];  // [M][smem bucket] resident CTAs per SM
+
+int resident_ctas(int M, int smem) {
+    // Registers bound the kernel at a few CTAs per SM; shared memory may bind
+    // it further.  Computed once per (M, 18 KB smem bucket).
+    int bucket = smem <= 18 * 1024 ? 0 : smem <= 36 * 1024 ? 1 : smem <= 54 * 1024 ? 2 : 3;
+    int &slot = occupancy_cache[M][bucket];
+    if (slot > 0) return slot;
+    int probe_smem = (bucket + 1) * 18 * 1024;
+    if (probe_smem > kSmemBudget) probe_smem = kSmemBudget;
+    int n = 0;
+    cudaError_t e = cudaSuccess;
+    switch (M) {
+#define W4A16_OCC(MM) \
+    case MM:          \
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_kernel<MM>, kThreads, probe_smem); \
+        break;
+        W4A16_OCC(1) W4A16_OCC(2) W4A16_OCC(3) W4A16_OCC(4)
+        W4A16_OCC(5) W4A16_OCC(6) W4A16_OCC(7) W4A16_OCC(8)
+#undef W4A16_OCC
+    }
+    if (e != cudaSuccess || n < 1) n = 1;
+    slot = n;
+    return n;
+}
+
+}  // namespace
+
+GemvPlan plan_gemv(int M, int N, int K, int split, const DeviceInfo &dev) {
+    GemvPlan pl{};
+    pl.M = M;
+    const int G = K / kGroup;
+    const int chunks_per_group = kGroup / kChunkK;
+    // Largest slice the kernel can hold: registers (kMaxIters chunks per lane)
+    // and the staged activations (M * slice_k * 2 bytes of shared memory).
+    // Shared memory holds M * nCB blocks of 32 chunks (2 KB each per token).
+    int max_groups = kMaxSliceChunks / chunks_per_group;
+    const int smem_groups = (kSmemBudget / (M * 32 * 4 * (int)sizeof(uint4))) * 32 / chunks_per_group;
+    if (smem_groups < max_groups) max_groups = smem_groups;
+    int S = (G + max_groups - 1) / max_groups;
+    pl.rows_per_cta = kRowsPerCta;
+    pl.n_row_blocks = (N + kRowsPerCta - 1) / kRowsPerCta;
+    if (split == 0 && S > 1) {
+        pl.ok = false;
+        return pl;
+    }
+    if (split != 0) {
+        // Fill the GPU: aim for two CTAs per SM in total when the row blocks
+        // alone cannot, keeping at least 4 groups (16 K steps per lane) per
+        // slice.
+        const int want = 2 * dev.sm_count;
+        if (pl.n_row_blocks * S < want) {
+            int s_fill = (want + pl.n_row_blocks - 1) / pl.n_row_blocks;
+            int s_cap = G / 4 > 0 ? G / 4 : 1;
+            if (s_fill > s_cap) s_fill = s_cap;
+            if (s_fill > S) S = s_fill;
+        }
+        if (split == 1 && S < 2 && G >= 2) S = 2;
+    }
+    pl.slice_groups = (G + S - 1) / S;
+    S = (G + pl.slice_groups - 1) / pl.slice_groups;
+    pl.S = S;
+    const int slice_chunks = pl.slice_groups * chunks_per_group;
+    const int nCB = (slice_chunks + 31) / 32;
+    pl.smem_bytes = M * nCB * 4 * 32 * (int)sizeof(uint4);
+    const int per_sm = resident_ctas(M, pl.smem_bytes);
+    int cap = dev.sm_count * per_sm / S;
+    if (cap < 1) cap = 1;
+    pl.grid_x = pl.n_row_blocks < cap ? pl.n_row_blocks : cap;
+    pl.ws_bytes = S > 1 ? (size_t)S * M * N * sizeof(float) : 0;
+    pl.ok = true;
+    return pl;
+}
+
+cudaError_t launch_gemv(const LinearArgs &a, const GemvPlan &plan, const Workspace &ws,
+                        cudaStream_t stream) {
+    GemvParams p;
+    p.x = a.x;
+    p.qw = a.qw;
+    p.scales = a.scales;
+    p.zeros = a.zeros;
+    p.y = a.y;
+    p.partials = ws.partials;
+    p.counters = ws.counters;
+    p.N = a.N;
+    p.K = a.K;
+    p.G = a.K / kGroup;
+    p.ZW = (p.G + 7) / 8;
+    p.KW = a.K / 8;
+    p.S = plan.S;
+    p.slice_groups = plan.slice_groups;
+    p.n_row_blocks = plan.n_row_blocks;
+    switch (plan.M) {
+        case 1: return launch_m<1>(p, plan, stream);
+        case 2: return launch_m<2>(p, plan, stream);
+        case 3: return launch_m<3>(p, plan, stream);
+        case 4: return launch_m<4>(p, plan, stream);
+        case 5: return launch_m<5>(p, plan, stream);
+        case 6: return launch_m<6>(p, plan, stream);
+        case 7: return launch_m<7>(p, plan, stream);
+        case 8: return launch_m<8>(p, plan, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t gemv_init_attributes(const DeviceInfo &dev) {
+    (void)dev;
+    cudaError_t e = cudaSuccess;
+#define W4A16_ATTR(MM)                                                                        \
+    if (e == cudaSuccess)                                                                     \
+        e = cudaFuncSetAttribute(gemv_kernel<MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 kSmemBudget);
+    W4A16_ATTR(1) W4A16_ATTR(2) W4A16_ATTR(3) W4A16_ATTR(4)
+    W4A16_ATTR(5) W4A16_ATTR(6) W4A16_ATTR(7) W4A16_ATTR(8)
+#undef W4A16_ATTR
+    for (auto &row : occupancy_cache)
+        for (int &v : row) v = 0;
+    return e;
+}
+
+}  // namespace w4a16

@@ -1,0 +1,70 @@
+// Internal interface between the C ABI (w4a16_api.cu) and the kernel files.
+// Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+constexpr int kGroup = 128;  // inputs per quantisation group
+
+// One W4A16 linear, device pointers.  x [M, K], y [M, N] fp16; qw [N, K/8];
+// scales [N, G] fp16; zeros [N, ceil(G/8)].
+struct LinearArgs {
+    const __half *x;
+    const uint32_t *qw;
+    const __half *scales;
+    const uint32_t *zeros;
+    __half *y;
+    int M, N, K;
+};
+
+// Library-owned scratch for the split-K rungs: fp32 partial outputs and one
+// arrival counter per output tile (zeroed at init, reset by the reducing CTA).
+struct Workspace {
+    float *partials;
+    size_t partial_bytes;
+    unsigned *counters;
+    int n_counters;
+};
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_smem_optin;
+};
+
+// ---- CUDA-core GEMV rungs (w4a16_gemv.cu) --------------------------------
+constexpr int kGemvMaxTokens = 8;  // tokens per launch on the CUDA-core rungs
+
+struct GemvPlan {
+    bool ok;            // false: the shape cannot run with the requested split rule
+    int M;              // tokens handled by this launch (1..8)
+    int S;              // K slices (1 = no split)
+    int slice_groups;   // groups per slice (last slice may hold fewer)
+    int rows_per_cta;   // output rows per row block
+    int n_row_blocks;   // ceil(N / rows_per_cta)
+    int grid_x;         // CTAs per slice (grid-stride over row blocks)
+    int smem_bytes;     // dynamic shared memory (staged activations)
+    size_t ws_bytes;    // split-K partial bytes (0 when S == 1)
+};
+
+// split: 0 = never split K, 1 = split K (at least 2 slices when G >= 2),
+// -1 = let the planner decide.
+GemvPlan plan_gemv(int M, int N, int K, int split, const DeviceInfo &dev);
+cudaError_t launch_gemv(const LinearArgs &a, const GemvPlan &plan, const Workspace &ws,
+                        cudaStream_t stream);
+cudaError_t gemv_init_attributes(const DeviceInfo &dev);
+
+// ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
+cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,
+                        uint32_t *zeros, cudaStream_t stream);
+cudaError_t launch_unpack(const uint32_t *qw, const uint32_t *zeros, int N, int K, uint8_t *q,
+                          uint8_t *z, cudaStream_t stream);
+cudaError_t launch_dequant(const uint32_t *qw, const __half *scales, const uint32_t *zeros,
+                           int N, int K, float *w_f32, __half *w_f16, cudaStream_t stream);
+
+}  // namespace w4a16
