@@ -207,70 +207,79 @@ def flush_l2(buf):
     buf.add_(1)
 
 
-def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None):
-    """Median single-launch time of one linear with L2 flushed before each launch."""
+def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,)):
+    """Median single-launch time of one linear with L2 flushed before each
+    launch, per rung (-1 = the dispatch table's choice); None where a rung
+    cannot run the shape."""
     import synthetic_inputs as si
     qw, s, zw = si.layer(si.config_seed(seed_cfg, 0, M), N, K, device=dev)
     x = si.x(si.config_seed(seed_cfg, 0, M), M, K).to(dev)
     y = torch.empty((M, N), dtype=torch.float16, device=dev)
-    for _ in range(3):
-        w4.w4a16_linear(x, qw, s, zw, y=y)
-    ts = []
-    for _ in range(reps):
-        flush_l2(flush)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        w4.w4a16_linear(x, qw, s, zw, y=y)
-        b.record()
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+    out = {}
+    for rung in rungs:
+        prev = w4.w4a16_set_forced_rung(rung)
+        try:
+            try:
+                for _ in range(3):
+                    w4.w4a16_linear(x, qw, s, zw, y=y)
+            except w4.W4A16Error:
+                out[rung] = None
+                continue
+            ts = []
+            for _ in range(reps):
+                flush_l2(flush)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                w4.w4a16_linear(x, qw, s, zw, y=y)
+                b.record()
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            out[rung] = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+        finally:
+            w4.w4a16_set_forced_rung(prev)
     del qw, s, zw
-    return t
+    return out
+
+
+_LAYER0 = None
+
+
+def _layer0_host():
+    """Layer 0 of the decode round on the host (oracle arrays), built once."""
+    global _LAYER0
+    if _LAYER0 is None:
+        import synthetic_inputs as si
+        out = []
+        for j, (_, K, N) in enumerate(ROUND_SHAPES):
+            qw, s, zw = si.layer(si.config_seed(3, 0, j), N, K)
+            x = si.x(si.config_seed(3, 0, 8 + j), M_ROUND, K)
+            out.append((si.as_u16(x), si.as_u32(qw), si.as_u16(s), si.as_u32(zw),
+                        linear_bytes(M_ROUND, N, K)))
+        _LAYER0 = out
+    return _LAYER0
 
 
 def cpu_baseline(seconds_target: float = 12.0):
     """The oracle, as it stands, on all host cores, over a bounded sample of the
-    decode round: the first R rows of each of layer 0's four linears at M = 4,
-    R growing until the sample takes about `seconds_target` seconds."""
+    decode round: layer 0's four linears (all rows, M = 4), passed over
+    repeatedly until about `seconds_target` seconds have elapsed."""
     import oracle
-    import synthetic_inputs as si
     cores = os.cpu_count() or 1
-    xs = [si.as_u16(si.x(si.config_seed(3, 0, 8 + j), M_ROUND, K))
-          for j, (_, K, _) in enumerate(ROUND_SHAPES)]
-    rows = 8
-    while True:
-        t_total, by_total = 0.0, 0
-        for j, (_, K, N) in enumerate(ROUND_SHAPES):
-            r = np.arange(min(rows, N), dtype=np.int64)
-            qw, s, zw = si.layer(si.config_seed(3, 0, j), N, K, rows=r)
-            args = (xs[j], si.as_u32(qw), si.as_u16(s), si.as_u32(zw), np.arange(r.size))
+    layer = _layer0_host()
+    t_total, by_total, passes = 0.0, 0, 0
+    while t_total < seconds_target or passes == 0:
+        for x, qw, s, zw, nbytes in layer:
             t0 = time.perf_counter()
-            oracle.linear_rows(*args, nthreads=cores)
+            oracle.linear(x, qw, s, zw, nthreads=cores)
             t_total += time.perf_counter() - t0
-            G = K // GROUP
-            by_total += r.size * (K // 2 + 2 * G + G // 2) + 2 * M_ROUND * K + 2 * M_ROUND * r.size
-        if t_total >= seconds_target / 4 or rows >= 1 << 14:
-            break
-        rows *= 2
-    # scale to the target duration with one more pass at the grown size
-    factor = max(1.0, seconds_target / max(t_total, 1e-3))
-    rows = int(rows * min(factor, 4.0))
-    t_total, by_total = 0.0, 0
-    for j, (_, K, N) in enumerate(ROUND_SHAPES):
-        r = np.arange(min(rows, N), dtype=np.int64)
-        qw, s, zw = si.layer(si.config_seed(3, 0, j), N, K, rows=r)
-        args = (xs[j], si.as_u32(qw), si.as_u16(s), si.as_u32(zw), np.arange(r.size))
-        t0 = time.perf_counter()
-        oracle.linear_rows(*args, nthreads=cores)
-        t_total += time.perf_counter() - t0
-        G = K // GROUP
-        by_total += r.size * (K // 2 + 2 * G + G // 2) + 2 * M_ROUND * K + 2 * M_ROUND * r.size
+            by_total += nbytes
+        passes += 1
     gbs = by_total / t_total / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of each of layer 0's four linears (qkv, o, gate+up, down) "
-                      f"at M=4, {t_total:.1f} s on {cores} threads; full round would take "
+            "sample": f"layer 0 of the decode round (qkv, o, gate+up, down; "
+                      f"{by_total / passes / 1e6:.0f} MB) at M=4, {passes} passes, "
+                      f"{t_total:.1f} s on {cores} threads; a full 64-layer round would take "
                       f"{round_bytes() / (gbs * 1e9):.0f} s",
             "seconds": t_total}
 
@@ -283,7 +292,7 @@ def run_reference(args):
     vals = []
     base = None
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(seconds_target=8.0 if i >= args.warmup else 2.0)
+        cb = cpu_baseline(seconds_target=6.0 if i >= args.warmup else 1.0)
         if i >= args.warmup:
             vals.append(cb["value"])
             secs.append(cb["seconds"])
@@ -419,10 +428,13 @@ def main():
                                     ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
                                     ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] + \
                 [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)]:
-            t = time_single(w4, M, N, K, cfg, dev, flush=flush)
+            ts = time_single(w4, M, N, K, cfg, dev, flush=flush, rungs=(-1, 0, 1, 2, 3))
             by = linear_bytes(M, N, K)
+            t = ts[-1]
             singles[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
-                              "rung": w4.rung_name(w4.w4a16_select_rung(M, N, K))}
+                              "rung": w4.rung_name(w4.w4a16_select_rung(M, N, K)),
+                              "us_per_rung": {w4.rung_name(r): (None if v is None else v * 1e6)
+                                              for r, v in ts.items() if r >= 0}}
         extra["single_linear_l2_flushed"] = singles
         del flush
 

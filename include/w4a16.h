@@ -65,7 +65,8 @@ typedef enum {
     W4A16_ERR_MISALIGNED = 3,      /* pointer alignment below the stated minimum */
     W4A16_ERR_WORKSPACE = 4,       /* the shape needs more split-K workspace than w4a16_init reserved */
     W4A16_ERR_NOT_INITIALIZED = 5, /* w4a16_init has not succeeded */
-    W4A16_ERR_CUDA = 6             /* a CUDA runtime call failed; see w4a16_last_cuda_error */
+    W4A16_ERR_CUDA = 6,            /* a CUDA runtime call failed; see w4a16_last_cuda_error */
+    W4A16_ERR_DEVICE = 7           /* a kernel gave up a bounded wait; see w4a16_device_status */
 } w4a16_status;
 
 /* Kernel rungs chosen by the dispatch table (w4a16_select_rung).  Every launch
@@ -172,6 +173,14 @@ void w4a16_probe_reset(void);
 /* Static strings; "?" for unknown values. */
 const char *w4a16_rung_name(int rung);
 const char *w4a16_status_string(int status);
+
+/* Kernels that wait on on-chip barriers (the tensor-core rungs) bound every
+ * wait by a timer; if one expires the kernel ORs a code into a device status
+ * word, drains its in-flight copies, frees its tensor memory and exits, so the
+ * CUDA context stays usable.  This call synchronises `stream`, returns
+ * W4A16_ERR_DEVICE with the accumulated code in *code (may be NULL) if any
+ * kernel reported one since the last call, and clears the word. */
+int w4a16_device_status(void *stream, int *code);
 
 /* The cudaError_t behind the calling thread's last W4A16_ERR_CUDA (0 if none). */
 int w4a16_last_cuda_error(void);

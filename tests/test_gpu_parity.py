@@ -17,6 +17,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
 CC_RUNGS = [0, 1]  # gemv, gemv_splitk
+TC_RUNGS = [2, 3]  # tc, tc_splitk
+ALL_RUNGS = CC_RUNGS + TC_RUNGS
 
 
 @pytest.fixture(scope="module")
@@ -27,6 +29,14 @@ def w4():
     w4.w4a16_init(0, 256 << 20)
     yield w4
     w4.w4a16_set_forced_rung(w4.RUNG_AUTO)
+
+
+@pytest.fixture(autouse=True)
+def no_device_errors(request):
+    yield
+    if "w4" in request.fixturenames:
+        import weight_only_int4_w4a16_gb300 as w4
+        assert w4.w4a16_device_status() == 0, "a kernel reported an expired bounded wait"
 
 
 def forced(w4, rung):
@@ -112,11 +122,11 @@ SHAPES = [(1, 1, 128), (1, 7, 256), (1, 1024, 512), (2, 1029, 1152), (3, 64, 512
           (8, 2000, 17408), (12, 300, 1024), (20, 77, 768), (64, 200, 512)]
 
 
-@pytest.mark.parametrize("rung", CC_RUNGS + [-1])
+@pytest.mark.parametrize("rung", ALL_RUNGS + [-1])
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_linear_matches_oracle(w4, rung, M, N, K):
     case = Case(si.config_seed(51, M, N % 16), M, N, K)
-    if rung == w4.RUNG_GEMV_SPLITK and K // 128 < 2:
+    if rung in (w4.RUNG_GEMV_SPLITK, w4.RUNG_TC_SPLITK) and K // 128 < 2:
         pytest.skip("split-K needs two groups")
     with forced(w4, rung):
         if rung >= 0:
@@ -132,7 +142,7 @@ def test_linear_matches_oracle(w4, rung, M, N, K):
     assert_close(y, case.reference(), f"rung {rung} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("rung", CC_RUNGS)
+@pytest.mark.parametrize("rung", ALL_RUNGS)
 def test_integer_case_bit_exact(w4, rung):
     # s = 1/16 and x in {-1, 0, 1}: every partial sum is an exact integer
     # multiple of 1/16 far below 2^24, so y is exact on every rung.
@@ -155,7 +165,7 @@ def test_integer_case_bit_exact(w4, rung):
     assert np.array_equal(y.float().cpu().numpy().astype(np.float64), want)
 
 
-@pytest.mark.parametrize("rung", CC_RUNGS)
+@pytest.mark.parametrize("rung", ALL_RUNGS)
 def test_run_to_run_bit_identical(w4, rung):
     case = Case(si.config_seed(52), 4, 5120, 17408)
     with forced(w4, rung):
@@ -191,13 +201,20 @@ def test_varying_sizes_back_to_back(w4):
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled rows
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rung", [-1] + ALL_RUNGS)
 @pytest.mark.parametrize("M,N,K,cfg", [(1, 34816, 5120, 1), (4, 5120, 17408, 2),
                                        (8, 5120, 17408, 2)])
-def test_full_size_sampled(w4, M, N, K, cfg):
+def test_full_size_sampled(w4, M, N, K, cfg, rung):
     seed = si.config_seed(cfg, 0, M)
     qw, s, zw = si.layer(seed, N, K, device=DEV)
     x = si.x(seed, M, K)
-    y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+    with forced(w4, rung):
+        try:
+            y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+        except w4.W4A16Error as e:
+            if e.status == w4.W4A16_ERR_UNSUPPORTED:
+                pytest.skip("rung cannot run this shape")
+            raise
     torch.cuda.synchronize()
     rows = sample_rows(N, 48, seed=cfg)
     ref = sampled_reference(seed, x, N, K, rows)
@@ -206,13 +223,15 @@ def test_full_size_sampled(w4, M, N, K, cfg):
     assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"cfg{cfg} M={M}")
 
 
+@pytest.mark.parametrize("rung", [-1, 2])
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
-def test_m_sweep_sampled(w4, M):
+def test_m_sweep_sampled(w4, M, rung):
     N, K = 27648, 5120
     seed = si.config_seed(4)
     qw, s, zw = si.layer(seed, N, K, device=DEV)
     x = si.x(seed, M, K)
-    y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+    with forced(w4, rung):
+        y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
     torch.cuda.synchronize()
     rows = sample_rows(N, 16, seed=M)
     ref = sampled_reference(seed, x, N, K, rows)

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libw4a16.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"W4A16 CUDA library not built ({LIB_PATH} missing). Build it with "
-        "`python -m weight_only_int4_w4a16_gb300.build` or __graft_entry__.build().")
+        "`python weight_only_int4_w4a16_gb300/build.py` or __graft_entry__.build().")
 
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -32,6 +32,7 @@ W4A16_ERR_MISALIGNED = 3
 W4A16_ERR_WORKSPACE = 4
 W4A16_ERR_NOT_INITIALIZED = 5
 W4A16_ERR_CUDA = 6
+W4A16_ERR_DEVICE = 7
 
 RUNG_AUTO = -1
 RUNG_GEMV = 0
@@ -75,6 +76,7 @@ _sig("w4a16_probe_counts", [ctypes.POINTER(ctypes.c_uint64), _I])
 _sig("w4a16_probe_reset", [], None)
 _sig("w4a16_rung_name", [_I], ctypes.c_char_p)
 _sig("w4a16_status_string", [_I], ctypes.c_char_p)
+_sig("w4a16_device_status", [_P, ctypes.POINTER(_I)])
 _sig("w4a16_last_cuda_error", [])
 _sig("w4a16_device_sm_count", [])
 
@@ -83,7 +85,7 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
             "w4a16_probe_reset", "w4a16_rung_name", "w4a16_status_string",
-            "w4a16_last_cuda_error", "w4a16_device_sm_count"]
+            "w4a16_device_status", "w4a16_last_cuda_error", "w4a16_device_sm_count"]
 
 
 class W4A16Error(RuntimeError):
@@ -246,6 +248,15 @@ def w4a16_probe_counts() -> list[int]:
 
 def w4a16_probe_reset() -> None:
     lib.w4a16_probe_reset()
+
+
+def w4a16_device_status(stream=None) -> int:
+    """Synchronise `stream`; return (and clear) the device error code (0 = none)."""
+    code = _I(0)
+    st = lib.w4a16_device_status(_stream_ptr(stream), ctypes.byref(code))
+    if st not in (W4A16_OK, W4A16_ERR_DEVICE):
+        _check(st, "w4a16_device_status")
+    return int(code.value)
 
 
 def w4a16_device_sm_count() -> int:

@@ -5,7 +5,7 @@ the objects are linked into one shared library with the CUDA runtime linked
 statically, so the library loads on a machine without a GPU driver (the
 C-ABI symbols can be inspected there; every CUDA call then fails cleanly).
 
-Usage: python -m weight_only_int4_w4a16_gb300.build [--force]
+Usage: python weight_only_int4_w4a16_gb300/build.py [--force]
 """
 from __future__ import annotations
 

@@ -76,57 +76,112 @@ int check_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *sca
 
 // The dispatch table.  Rungs that cannot run a shape are skipped in auto mode;
 // a forced rung that cannot run it makes the call fail with UNSUPPORTED.
+// Auto: up to 8 tokens on the CUDA-core GEMV (split K when the row blocks
+// alone cannot fill the GPU), more tokens on the tcgen05 dequant-GEMM.
 struct Decision {
     int rung;
     int status;
 };
 
+bool is_tc(int rung) { return rung == W4A16_RUNG_TC || rung == W4A16_RUNG_TC_SPLITK; }
+
+int tile_tokens(int rung) { return is_tc(rung) ? kTcMaxTokens : kGemvMaxTokens; }
+
 Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
-    if (forced == W4A16_RUNG_GEMV) {
-        GemvPlan p = plan_gemv(Mt, N, K, 0, dev);
-        return {W4A16_RUNG_GEMV, p.ok ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
+    const int G = K / kGroup;
+    switch (forced) {
+        case W4A16_RUNG_GEMV: {
+            GemvPlan p = plan_gemv(Mt, N, K, 0, dev);
+            return {W4A16_RUNG_GEMV, p.ok ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
+        }
+        case W4A16_RUNG_GEMV_SPLITK:
+        case W4A16_RUNG_TC_SPLITK:
+            return {forced, G >= 2 ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
+        case W4A16_RUNG_TC:
+            return {W4A16_RUNG_TC, W4A16_OK};
+        default:
+            break;
     }
-    if (forced == W4A16_RUNG_GEMV_SPLITK) {
-        if (K / kGroup < 2) return {W4A16_RUNG_GEMV_SPLITK, W4A16_ERR_UNSUPPORTED};
-        return {W4A16_RUNG_GEMV_SPLITK, W4A16_OK};
+    if (M <= kGemvMaxTokens) {
+        GemvPlan p = plan_gemv(Mt, N, K, -1, dev);
+        return {p.S > 1 ? W4A16_RUNG_GEMV_SPLITK : W4A16_RUNG_GEMV, W4A16_OK};
     }
-    if (forced == W4A16_RUNG_TC || forced == W4A16_RUNG_TC_SPLITK)
-        return {forced, W4A16_ERR_UNSUPPORTED};
-    GemvPlan p = plan_gemv(Mt, N, K, -1, dev);
-    return {p.S > 1 ? W4A16_RUNG_GEMV_SPLITK : W4A16_RUNG_GEMV, W4A16_OK};
+    const int Mtc = M < kTcMaxTokens ? M : kTcMaxTokens;
+    TcPlan t = plan_tc(Mtc, N, K, -1, dev);
+    return {t.S > 1 ? W4A16_RUNG_TC_SPLITK : W4A16_RUNG_TC, W4A16_OK};
 }
 
-// Per-launch plan for the CUDA-core rungs: one launch per tile of <= 8 tokens.
-GemvPlan gemv_plan_for(int rung, int Mt, int N, int K, const DeviceInfo &dev) {
-    return plan_gemv(Mt, N, K, rung == W4A16_RUNG_GEMV ? 0 : (rung == W4A16_RUNG_GEMV_SPLITK ? 1 : -1),
-                     dev);
+int split_rule(int rung) {
+    switch (rung) {
+        case W4A16_RUNG_GEMV:
+        case W4A16_RUNG_TC: return 0;
+        case W4A16_RUNG_GEMV_SPLITK:
+        case W4A16_RUNG_TC_SPLITK: return 1;
+    }
+    return -1;
+}
+
+// Workspace bytes and counters one launch of `rung` needs for Mt tokens;
+// false if the rung cannot run the shape.
+bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t *bytes,
+                  int *counters) {
+    if (is_tc(rung)) {
+        TcPlan p = plan_tc(Mt, N, K, split_rule(rung), dev);
+        *bytes = p.ws_bytes;
+        *counters = p.S > 1 ? p.n_tiles : 0;
+        return p.ok;
+    }
+    GemvPlan p = plan_gemv(Mt, N, K, split_rule(rung), dev);
+    *bytes = p.ws_bytes;
+    *counters = p.S > 1 ? p.n_row_blocks : 0;
+    return p.ok;
+}
+
+size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *status) {
+    const int tt = tile_tokens(rung);
+    size_t need = 0;
+    *status = W4A16_OK;
+    // every full token tile shares one plan; the last tile may be shorter
+    int sizes[2] = {M < tt ? M : tt, M > tt && M % tt ? M % tt : 0};
+    for (int Mt : sizes) {
+        if (Mt == 0) continue;
+        size_t b = 0;
+        int c = 0;
+        if (!launch_needs(rung, Mt, N, K, dev, &b, &c)) {
+            *status = W4A16_ERR_UNSUPPORTED;
+            return 0;
+        }
+        if (b > need) need = b;
+        if (c > kCounters) *status = W4A16_ERR_WORKSPACE;
+    }
+    return need;
 }
 
 int check_workspace(int rung, int M, int N, int K, const State &st) {
-    if (rung == W4A16_RUNG_GEMV || rung == W4A16_RUNG_GEMV_SPLITK) {
-        for (int m0 = 0; m0 < M; m0 += kGemvMaxTokens) {
-            int Mt = M - m0 < kGemvMaxTokens ? M - m0 : kGemvMaxTokens;
-            GemvPlan p = gemv_plan_for(rung, Mt, N, K, st.dev);
-            if (!p.ok) return W4A16_ERR_UNSUPPORTED;
-            if (p.ws_bytes > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
-            if (p.S > 1 && p.n_row_blocks > st.ws.n_counters) return W4A16_ERR_WORKSPACE;
-            if (m0 + kGemvMaxTokens >= M) break;  // all full tiles share one plan
-        }
-    }
+    int status = W4A16_OK;
+    size_t need = workspace_for(rung, M, N, K, st.dev, &status);
+    if (status) return status;
+    if (need > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
     return W4A16_OK;
 }
 
 int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
-    for (int m0 = 0; m0 < a.M && e == cudaSuccess; m0 += kGemvMaxTokens) {
-        int Mt = a.M - m0 < kGemvMaxTokens ? a.M - m0 : kGemvMaxTokens;
-        GemvPlan p = gemv_plan_for(rung, Mt, a.N, a.K, st.dev);
+    const int tt = tile_tokens(rung);
+    for (int m0 = 0; m0 < a.M && e == cudaSuccess; m0 += tt) {
+        const int Mt = a.M - m0 < tt ? a.M - m0 : tt;
         LinearArgs t = a;
         t.x = a.x + (size_t)m0 * a.K;
         t.y = a.y + (size_t)m0 * a.N;
         t.M = Mt;
-        e = launch_gemv(t, p, st.ws, stream);
+        if (is_tc(rung)) {
+            TcPlan p = plan_tc(Mt, a.N, a.K, split_rule(rung), st.dev);
+            e = launch_tc(t, p, st.ws, st.ws.status, stream);
+        } else {
+            GemvPlan p = plan_gemv(Mt, a.N, a.K, split_rule(rung), st.dev);
+            e = launch_gemv(t, p, st.ws, stream);
+        }
         g_probe[rung].fetch_add(1, std::memory_order_relaxed);
     }
     if (st.log)
@@ -187,12 +242,14 @@ int w4a16_init(int device, size_t workspace_bytes) {
     if (e != cudaSuccess) return cuda_fail(e);
     if (workspace_bytes == 0) workspace_bytes = kDefaultWorkspace;
     workspace_bytes = (workspace_bytes + 255) & ~(size_t)255;
-    const size_t counter_bytes = (size_t)kCounters * sizeof(unsigned);
+    // counters, then one status word (kept 256-byte aligned)
+    const size_t counter_bytes = (size_t)kCounters * sizeof(unsigned) + 256;
     void *base = nullptr;
     e = cudaMalloc(&base, workspace_bytes + counter_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaMemset((char *)base + workspace_bytes, 0, counter_bytes);
     if (e == cudaSuccess) e = gemv_init_attributes(dev);
+    if (e == cudaSuccess) e = tc_init(dev);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(base);
@@ -204,6 +261,7 @@ int w4a16_init(int device, size_t workspace_bytes) {
     s.ws.partial_bytes = workspace_bytes;
     s.ws.counters = (unsigned *)((char *)base + workspace_bytes);
     s.ws.n_counters = kCounters;
+    s.ws.status = (int *)((char *)base + workspace_bytes + (size_t)kCounters * sizeof(unsigned));
     s.forced_rung = parse_rung(getenv("W4A16_FORCE_RUNG"));
     const char *lg = getenv("W4A16_LOG");
     s.log = lg && *lg && strcmp(lg, "0") != 0;
@@ -229,14 +287,9 @@ size_t w4a16_workspace_bytes(int M, int N, int K, int group) {
     if (!g_state.initialized) dev.sm_count = 152;
     Decision d = decide(M, N, K, dev, g_state.forced_rung);
     if (d.status) return 0;
-    size_t need = 0;
-    for (int m0 = 0; m0 < M; m0 += kGemvMaxTokens) {
-        int Mt = M - m0 < kGemvMaxTokens ? M - m0 : kGemvMaxTokens;
-        GemvPlan p = gemv_plan_for(d.rung, Mt, N, K, dev);
-        if (p.ws_bytes > need) need = p.ws_bytes;
-        if (m0 + kGemvMaxTokens >= M) break;
-    }
-    return need;
+    int status = W4A16_OK;
+    size_t need = workspace_for(d.rung, M, N, K, dev, &status);
+    return status == W4A16_ERR_UNSUPPORTED ? 0 : need;
 }
 
 int w4a16_pack(const uint8_t *q, const uint8_t *z, int N, int K, int group, uint32_t *qweight,
@@ -387,8 +440,24 @@ const char *w4a16_status_string(int status) {
         case W4A16_ERR_WORKSPACE: return "split-K workspace too small";
         case W4A16_ERR_NOT_INITIALIZED: return "w4a16_init has not succeeded";
         case W4A16_ERR_CUDA: return "CUDA runtime error";
+        case W4A16_ERR_DEVICE: return "a kernel reported a device-side error (bounded wait expired)";
     }
     return "?";
+}
+
+int w4a16_device_status(void *stream, int *code) {
+    if (code) *code = 0;
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    int h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, g_state.ws.status, sizeof(int), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess && h != 0)
+        e = cudaMemsetAsync(g_state.ws.status, 0, sizeof(int), (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (code) *code = h;
+    return h ? W4A16_ERR_DEVICE : W4A16_OK;
 }
 
 int w4a16_last_cuda_error(void) { return t_last_cuda_error; }

@@ -29,6 +29,7 @@ struct Workspace {
     size_t partial_bytes;
     unsigned *counters;
     int n_counters;
+    int *status;  // device word: kernels OR in an error code when a bounded wait expires
 };
 
 struct DeviceInfo {
@@ -58,6 +59,26 @@ GemvPlan plan_gemv(int M, int N, int K, int split, const DeviceInfo &dev);
 cudaError_t launch_gemv(const LinearArgs &a, const GemvPlan &plan, const Workspace &ws,
                         cudaStream_t stream);
 cudaError_t gemv_init_attributes(const DeviceInfo &dev);
+
+// ---- tcgen05 dequant-GEMM rungs (w4a16_tc.cu) -----------------------------
+constexpr int kTcMaxTokens = 64;  // tokens per launch on the tensor-core rungs
+
+struct TcPlan {
+    bool ok;
+    int M;             // real tokens in this launch (1..64)
+    int T;             // MMA N: tokens padded to 16, 32 or 64
+    int S;             // K slices
+    int slice_groups;  // groups per slice
+    int n_tiles;       // 128-row weight tiles
+    size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
+};
+
+// split: 0 = never split K, 1 = split K, -1 = planner decides.
+TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev);
+// status: device word the kernel ORs an error code into when a bounded wait expires.
+cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
+                      cudaStream_t stream);
+cudaError_t tc_init(const DeviceInfo &dev);
 
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,
