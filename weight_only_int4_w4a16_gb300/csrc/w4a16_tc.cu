@@ -50,6 +50,7 @@ constexpr int kPStages = 12;                     // packed-weight stages in flig
 constexpr int kAStages = 3;                      // A (dequantised group) buffers in TMEM
 constexpr int kDStages = 4;                      // per-group accumulators in TMEM
 constexpr int kACols = kGroup / 2;               // TMEM columns per A buffer (2 fp16 / column)
+constexpr int kXAhead = 4;                       // groups of x fetched ahead with cp.async
 constexpr int kEpiWarps = 4;
 constexpr int kDeqWarps = 8;
 constexpr int kTmaWarp = kEpiWarps + kDeqWarps;  // 12
@@ -84,8 +85,10 @@ struct TcConfig {
     static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
     static constexpr int kSmemP = kPStages * kStageBytes;
     static constexpr int kSmemX = kAStages * kXBytes;
+    static constexpr int kSmemXRaw = kXAhead * kXBytes;   // x copies in flight, raw order
     static constexpr int kSmemBar = 1024;
-    static constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemP + kSmemX + kSmemBar;
+    static constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemP + kSmemX + kSmemXRaw + kSmemBar;
+    static constexpr int kPiecesPerThread = T * 16 / (kDeqWarps * 32);  // 16-byte x pieces
     // instruction descriptor: D f32, A f16, B f16, both K-major, N = T, M = 128
     static constexpr uint32_t kIdesc =
         (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
@@ -233,6 +236,20 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16-byte global -> shared copy that bypasses registers; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -260,8 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sm_p = smem;                   // packed stages
-    uint8_t *sm_x = smem + C::kSmemP;       // x buffers
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kSmemP + C::kSmemX);
+    uint8_t *sm_x = smem + C::kSmemP;       // x buffers (MMA operand layout)
+    uint8_t *sm_xraw = sm_x + C::kSmemX;    // x copies in flight (row-major pieces)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_xraw + C::kSmemXRaw);
     uint64_t *full = bars;                          // [kPStages]
     uint64_t *empty = full + kPStages;              // [kPStages]
     uint64_t *a_full = empty + kPStages;            // [kAStages]
@@ -381,10 +399,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         const int n = tile * kTileN + r;
         const uint32_t *zrow = p.zeros + (size_t)(n < p.N ? n : 0) * p.ZW;
         const int dt = dw * 32 + lane;        // 0..255 among dequant threads
+        // x pieces this thread moves: piece pc = dt + 256 i is (token pc % T,
+        // 8-block pc / T) of a group; copied kXAhead groups ahead with cp.async
+        // into a raw ring, then re-ordered into the MMA layout when its group
+        // comes up.
+        auto issue_x = [&](int c) {
+            if (c < nchunks) {
+                const int g = g0 + c;
+                uint8_t *raw = sm_xraw + (c % kXAhead) * C::kXBytes;
+#pragma unroll
+                for (int i = 0; i < C::kPiecesPerThread; ++i) {
+                    const int pc = dt + i * kDeqWarps * 32;
+                    const int t = pc % T, kb = pc / T;
+                    const __half *src =
+                        t < p.M ? p.x + (size_t)t * p.K + (size_t)g * kGroup + 8 * kb : p.x;
+                    cp_async16(smem_u32(raw + pc * 16), src, t < p.M ? 16u : 0u);
+                }
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int c = 0; c < kXAhead; ++c) issue_x(c);
+        uint32_t zw_cur = (n < p.N && nchunks > 0) ? __ldg(zrow + (g0 >> 3)) : 0u;
+        uint32_t zw_next = (n < p.N && nchunks > 1) ? __ldg(zrow + ((g0 + 1) >> 3)) : 0u;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % kPStages, a = c % kAStages;
             const int g = g0 + c;
-            const uint32_t zw = n < p.N ? __ldg(zrow + (g >> 3)) : 0u;
+            const uint32_t zw = zw_cur;
+            zw_cur = zw_next;
+            zw_next = (n < p.N && c + 2 < nchunks) ? __ldg(zrow + ((g + 2) >> 3)) : 0u;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (c / kPStages) & 1, abort))) {
                 fail(abort, p.status, kErrWaitFull);
                 break;
@@ -416,23 +459,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 v[4 * u + 3] = hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo);
             }
             tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols + 32 * half, v);
-            // stage x[:, 128g : 128g + 128] for this group: piece (token t,
-            // 8-block kb) at (t/8)*2048 + kb*128 + (t%8)*16
-            uint8_t *xb = sm_x + a * C::kXBytes;
-            for (int pc = dt; pc < T * 16; pc += kDeqWarps * 32) {
-                const int t = pc % T, kb = pc / T;
-                uint4 v4 = make_uint4(0, 0, 0, 0);
-                if (t < p.M)
-                    v4 = pair_order(__ldg(reinterpret_cast<const uint4 *>(
-                        p.x + (size_t)t * p.K + (size_t)g * kGroup + 8 * kb)));
-                *reinterpret_cast<uint4 *>(xb + (t >> 3) * 2048 + kb * 128 + (t & 7) * 16) = v4;
+            // x of this group: this thread's pieces arrived (own cp.async group);
+            // re-order to pair order at (t/8)*2048 + kb*128 + (t%8)*16
+            cp_async_wait<kXAhead - 1>();
+            {
+                const uint8_t *raw = sm_xraw + (c % kXAhead) * C::kXBytes;
+                uint8_t *xb = sm_x + a * C::kXBytes;
+#pragma unroll
+                for (int i = 0; i < C::kPiecesPerThread; ++i) {
+                    const int pc = dt + i * kDeqWarps * 32;
+                    const int t = pc % T, kb = pc / T;
+                    const uint4 v4 = pair_order(*reinterpret_cast<const uint4 *>(raw + pc * 16));
+                    *reinterpret_cast<uint4 *>(xb + (t >> 3) * 2048 + kb * 128 + (t & 7) * 16) = v4;
+                }
             }
+            issue_x(c + kXAhead);  // refills the raw slot just read
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(a_full + a));
         }
+        cp_async_wait<0>();
     } else {
         // ------------------------------------------------ epilogue (warps 0..3)
         const int quarter = warp;  // warp % 4 == warp here
@@ -442,9 +490,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         float acc[T];
 #pragma unroll
         for (int t = 0; t < T; ++t) acc[t] = 0.f;
+        // scales fetched four groups ahead (a rotating set of registers)
+        auto ld_scale = [&](int c) {
+            return (n < p.N && c < nchunks) ? __half2float(srow[g0 + c]) : 0.f;
+        };
+        float s0 = ld_scale(0), s1 = ld_scale(1), s2 = ld_scale(2), s3 = ld_scale(3);
         for (int c = 0; c < nchunks; ++c) {
             const int d = c % kDStages;
-            const float sc = n < p.N ? __half2float(srow[g0 + c]) : 0.f;
+            const float sc = s0;
+            s0 = s1;
+            s1 = s2;
+            s2 = s3;
+            s3 = ld_scale(c + 4);
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(d_full + d), (c / kDStages) & 1, abort))) {
                 fail(abort, p.status, kErrWaitDFull);
                 break;
