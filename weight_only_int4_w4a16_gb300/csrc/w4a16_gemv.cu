@@ -354,7 +354,7 @@ int resident_ctas(int M, int smem) {
     int &slot = occupancy_cache[M][bucket];
     if (slot > 0) return slot;
     int probe = (bucket + 1) * 32 * 1024;
-    if (probe > 227 * 1024) probe = 227 * 1024;
+    if (probe > 226 * 1024) probe = 226 * 1024;
     if (probe < smem) probe = smem;
     int n = 0;
     cudaError_t e = cudaSuccess;
@@ -455,12 +455,13 @@ cudaError_t launch_gemv(const LinearArgs &a, const GemvPlan &plan, const Workspa
 }
 
 cudaError_t gemv_init_attributes(const DeviceInfo &dev) {
-    (void)dev;
+    // leave room for the kernel's static shared memory (barriers, flags)
+    const int dyn = dev.max_smem_optin - 1024;
     cudaError_t e = cudaSuccess;
 #define W4A16_ATTR(MM)                                                                        \
     if (e == cudaSuccess)                                                                     \
         e = cudaFuncSetAttribute(gemv_kernel<MM>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 227 * 1024);
+                                 dyn);
     W4A16_ATTR(1) W4A16_ATTR(2) W4A16_ATTR(3) W4A16_ATTR(4)
     W4A16_ATTR(5) W4A16_ATTR(6) W4A16_ATTR(7) W4A16_ATTR(8)
 #undef W4A16_ATTR
