@@ -445,6 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 fail(abort, p.status, kErrWaitAEmpty);
                 break;
             }
+            // the MMAs that read A[a] and x[a] have completed (commit); order
+            // this warp's tensor-memory stores after that observation
+            tc_fence_after();
             const uint32_t z = (zw >> (4 * (g & 7))) & 0xfu;
             const uint32_t zz_hi = 0x64006400u | z | (z << 16);
             const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
