@@ -46,7 +46,6 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRing = 4;                 // row slices in flight per warp
 constexpr int kChunkK = 32;              // k values per 16-byte chunk
 constexpr int kMaxSliceGroups = 64;      // 4 KB of packed weights per row slice
-constexpr int kMaxLaneChunks = kMaxSliceGroups * (kGroup / kChunkK) / 32;  // 8
 constexpr int kXBudget = 64 * 1024;      // staged activations per CTA
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
 
@@ -201,21 +200,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvParams p) {
     }
     __syncthreads();
 
-    // scales and zero nibbles of a row, for this lane's chunks
-    float sc_next[kMaxLaneChunks];
-    uint32_t zq_next[kMaxLaneChunks];
+    // Per-row metadata, one row ahead: lane l holds the scales of slice groups
+    // l and l + 32, and the zeros word g0/8 + l; the chunk loop fetches the
+    // values it needs from the owning lane with shuffles.
+    const int zw0 = g0 >> 3;
+    const int nzw = ((g1 - 1) >> 3) - zw0 + 1;  // zeros words touched by the slice
+    float s_lo_next = 0.f, s_hi_next = 0.f;
+    uint32_t z_next = 0;
     auto fetch_meta = [&](int i) {
         if (i < my_rows) {
             const int n = row0 + warp + kWarps * i;
-#pragma unroll
-            for (int j = 0; j < kMaxLaneChunks; ++j) {
-                const int c = lane + 32 * j;
-                if (j < nCB && c < nchunks) {
-                    const int g = g0 + (c >> 2);
-                    sc_next[j] = __half2float(p.scales[(size_t)n * p.G + g]);
-                    zq_next[j] = (__ldg(p.zeros + (size_t)n * p.ZW + (g >> 3)) >> (4 * (g & 7))) & 0xfu;
-                }
-            }
+            const __half *srow = p.scales + (size_t)n * p.G + g0;
+            if (lane < g1 - g0) s_lo_next = __half2float(srow[lane]);
+            if (lane + 32 < g1 - g0) s_hi_next = __half2float(srow[lane + 32]);
+            if (lane < nzw) z_next = __ldg(p.zeros + (size_t)n * p.ZW + zw0 + lane);
         }
     };
     fetch_meta(0);
@@ -224,13 +222,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvParams p) {
     for (int i = 0; i < my_rows; ++i) {
         const int n = row0 + warp + kWarps * i;
         const int slot = i % kRing;
-        float sc[kMaxLaneChunks];
-        uint32_t zq[kMaxLaneChunks];
-#pragma unroll
-        for (int j = 0; j < kMaxLaneChunks; ++j) {
-            sc[j] = sc_next[j];
-            zq[j] = zq_next[j];
-        }
+        const float s_lo = s_lo_next, s_hi = s_hi_next;
+        const uint32_t zrow = z_next;
         fetch_meta(i + 1);
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars[warp][slot]), (i / kRing) & 1))) {
             if (lane == 0) atomicOr(p.status, 1);
@@ -241,12 +234,16 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvParams p) {
         float acc[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[m] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxLaneChunks; ++j) {
+        for (int j = 0; j < nCB; ++j) {
+            // chunk c = lane + 32 j lies in slice group gl = 8 j + lane / 4
             const int c = lane + 32 * j;
-            if (j < nCB && c < nchunks) {
+            const int gl = 8 * j + (lane >> 2);
+            const float sc = __shfl_sync(0xffffffffu, (j >> 2) ? s_hi : s_lo, gl & 31);
+            const int zg = g0 + gl;
+            const uint32_t zword = __shfl_sync(0xffffffffu, zrow, ((zg >> 3) - zw0) & 31);
+            if (c < nchunks) {
                 const uint4 wv = wrow[c];
-                const uint32_t z = zq[j];
+                const uint32_t z = (zword >> (4 * (zg & 7))) & 0xfu;
                 const uint32_t zz_hi = 0x64006400u | z | (z << 16);         // 1024 + z
                 const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);  // 64 + z
                 float part0[M], part1[M];
@@ -271,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvParams p) {
                     }
                 }
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc[m] = fmaf(sc[j], part0[m] + part1[m], acc[m]);
+                for (int m = 0; m < M; ++m) acc[m] = fmaf(sc, part0[m] + part1[m], acc[m]);
             }
         }
         // the slot is consumed: refill it with the row kRing ahead

@@ -48,14 +48,16 @@ constexpr int kChunkWords = kGroup / 8;          // 16 words = 64 bytes per row 
 constexpr int kStageBytes = kTileN * kChunkWords * 4;  // 8 KB per TMA stage
 constexpr int kPStages = 12;                     // packed-weight stages in flight (96 KB)
 constexpr int kAStages = 3;                      // A (dequantised group) buffers in TMEM
-constexpr int kDStages = 4;                      // per-group accumulators in TMEM
+constexpr int kDStages = 4;                      // per-group accumulator sets in TMEM
+constexpr int kDCols = 64;                       // TMEM columns per accumulator set
 constexpr int kACols = kGroup / 2;               // TMEM columns per A buffer (2 fp16 / column)
-constexpr int kXAhead = 4;                       // groups of x fetched ahead with cp.async
+constexpr int kXAhead = 2;                       // a team's groups of x fetched ahead (cp.async)
 constexpr int kEpiWarps = 4;
-constexpr int kDeqWarps = 8;
-constexpr int kTmaWarp = kEpiWarps + kDeqWarps;  // 12
-constexpr int kMmaWarp = kTmaWarp + 1;           // 13
-constexpr int kThreads = (kMmaWarp + 1) * 32;    // 448
+constexpr int kDeqTeams = 2;                     // dequant teams take alternate groups
+constexpr int kDeqWarps = 8;                     // warps per team (2 per TMEM lane quarter)
+constexpr int kTmaWarp = kEpiWarps + kDeqTeams * kDeqWarps;  // 20
+constexpr int kMmaWarp = kTmaWarp + 1;                       // 21
+constexpr int kThreads = (kMmaWarp + 1) * 32;                // 704
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 
 // error codes recorded in the device status word (bit flags)
@@ -79,13 +81,16 @@ struct TcParams {
 template <int T>
 struct TcConfig {
     static constexpr int kXBytes = T * kGroup * 2;          // one group of x, T tokens
-    static constexpr int kDCols = T;
+    // A group's 8 MMAs go round-robin into kChains independent accumulators
+    // (T columns each) so that consecutive MMAs do not wait on one another;
+    // the epilogue adds the chains.
+    static constexpr int kChains = kDCols / T;               // 4, 2, 1
     static constexpr int kDBase = kAStages * kACols;         // 192
     static constexpr int kColsUsed = kDBase + kDStages * kDCols;
     static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
     static constexpr int kSmemP = kPStages * kStageBytes;
     static constexpr int kSmemX = kAStages * kXBytes;
-    static constexpr int kSmemXRaw = kXAhead * kXBytes;   // x copies in flight, raw order
+    static constexpr int kSmemXRaw = kDeqTeams * kXAhead * kXBytes;  // x copies in flight
     static constexpr int kSmemBar = 1024;
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemP + kSmemX + kSmemXRaw + kSmemBar;
     static constexpr int kPiecesPerThread = T * 16 / (kDeqWarps * 32);  // 16-byte x pieces
@@ -93,6 +98,23 @@ struct TcConfig {
     static constexpr uint32_t kIdesc =
         (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
 };
+
+// Optional section timers (build with -DW4A16_TRACE): CTA (0, 0) records the
+// SM cycle counter at each pipeline event of its first kTraceChunks groups.
+#ifdef W4A16_TRACE
+constexpr int kTraceChunks = 32;
+constexpr int kTraceEvents = 9;
+__device__ unsigned long long g_trace[kTraceEvents * kTraceChunks];
+#define W4A16_TR(ev, c)                                                                   \
+    do {                                                                                  \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < kTraceChunks)                     \
+            g_trace[(ev) * kTraceChunks + (c)] = clock64();                               \
+    } while (0)
+#else
+#define W4A16_TR(ev, c) \
+    do {                \
+    } while (0)
+#endif
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -338,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     fail(abort, p.status, kErrWaitEmpty);
                     break;
                 }
+                W4A16_TR(0, c);
                 mbar_arrive_expect_tx(smem_u32(full + s), kStageBytes);
                 tma_load_2d(smem_u32(sm_p + s * kStageBytes), &p.tmap, (g0 + c) * kChunkWords,
                             tile * kTileN, smem_u32(full + s));
@@ -365,20 +388,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     fail(abort, p.status, kErrWaitAFull);
                     break;
                 }
+                W4A16_TR(4, c);
                 if (!mbar_wait(smem_u32(d_empty + d), ((c / kDStages) & 1) ^ 1, abort)) {
                     fail(abort, p.status, kErrWaitDEmpty);
                     break;
                 }
                 tc_fence_after();
+                W4A16_TR(5, c);
                 const uint32_t xb = smem_u32(sm_x + a * C::kXBytes);
-                const uint32_t d_tmem = tmem + C::kDBase + d * C::kDCols;
+                const uint32_t d_tmem = tmem + C::kDBase + d * kDCols;
+                const uint64_t bdesc0 = smem_desc_kmajor(xb, 128, 2048);
 #pragma unroll
                 for (int j = 0; j < kGroup / 16; ++j) {
-                    const uint64_t bdesc = smem_desc_kmajor(xb + 256 * j, 128, 2048);
-                    mma_f16_ts(d_tmem, tmem + a * kACols + 8 * j, bdesc, C::kIdesc, j > 0);
+                    // k step j: B advances 256 bytes (two 8x8 core matrices);
+                    // accumulator chain j % kChains starts fresh on its first step
+                    mma_f16_ts(d_tmem + (j % C::kChains) * T, tmem + a * kACols + 8 * j,
+                               bdesc0 + (uint64_t)(16 * j), C::kIdesc, j >= C::kChains);
                 }
                 mma_commit(smem_u32(a_empty + a));
                 mma_commit(smem_u32(d_full + d));
+                W4A16_TR(6, c);
             }
             // all MMAs of this CTA complete before the tensor memory is freed
             mma_commit(smem_u32(done));
@@ -392,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         }
     } else if (warp >= kEpiWarps) {
         // ------------------------------------------------ dequantise + stage x
-        const int dw = warp - kEpiWarps;      // 0..7
+        const int team = (warp - kEpiWarps) / kDeqWarps;  // groups team, team+2, ...
+        const int dw = (warp - kEpiWarps) % kDeqWarps;    // 0..7 within the team
         const int quarter = warp & 3;         // TMEM lanes 32*quarter ..
         const int half = dw >> 2;             // which 64 k of the group
         const int r = quarter * 32 + lane;    // row within the tile
@@ -403,10 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         // 8-block pc / T) of a group; copied kXAhead groups ahead with cp.async
         // into a raw ring, then re-ordered into the MMA layout when its group
         // comes up.
-        auto issue_x = [&](int c) {
+        uint8_t *team_raw = sm_xraw + team * kXAhead * C::kXBytes;
+        // the team's li-th group is c = team + kDeqTeams * li
+        auto issue_x = [&](int li) {
+            const int c = team + kDeqTeams * li;
             if (c < nchunks) {
                 const int g = g0 + c;
-                uint8_t *raw = sm_xraw + (c % kXAhead) * C::kXBytes;
+                uint8_t *raw = team_raw + (li % kXAhead) * C::kXBytes;
 #pragma unroll
                 for (int i = 0; i < C::kPiecesPerThread; ++i) {
                     const int pc = dt + i * kDeqWarps * 32;
@@ -419,19 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             cp_async_commit();
         };
 #pragma unroll
-        for (int c = 0; c < kXAhead; ++c) issue_x(c);
-        uint32_t zw_cur = (n < p.N && nchunks > 0) ? __ldg(zrow + (g0 >> 3)) : 0u;
-        uint32_t zw_next = (n < p.N && nchunks > 1) ? __ldg(zrow + ((g0 + 1) >> 3)) : 0u;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int li = 0; li < kXAhead; ++li) issue_x(li);
+        const int c_first = team;
+        uint32_t zw_cur = (n < p.N && c_first < nchunks) ? __ldg(zrow + ((g0 + c_first) >> 3)) : 0u;
+        uint32_t zw_next = (n < p.N && c_first + kDeqTeams < nchunks)
+                               ? __ldg(zrow + ((g0 + c_first + kDeqTeams) >> 3))
+                               : 0u;
+        int li = 0;
+        for (int c = c_first; c < nchunks; c += kDeqTeams, ++li) {
             const int s = c % kPStages, a = c % kAStages;
             const int g = g0 + c;
             const uint32_t zw = zw_cur;
             zw_cur = zw_next;
-            zw_next = (n < p.N && c + 2 < nchunks) ? __ldg(zrow + ((g + 2) >> 3)) : 0u;
+            zw_next = (n < p.N && c + 2 * kDeqTeams < nchunks)
+                          ? __ldg(zrow + ((g + 2 * kDeqTeams) >> 3))
+                          : 0u;
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (c / kPStages) & 1, abort))) {
                 fail(abort, p.status, kErrWaitFull);
                 break;
             }
+            if (dw == 0 && lane == 0) W4A16_TR(1, c);
             // this row's 32 bytes of the stage: 16-byte chunks 2*half, 2*half+1,
             // stored 64-byte swizzled (chunk ^= (row >> 1) & 3)
             const uint8_t *st = sm_p + s * kStageBytes + r * 64;
@@ -448,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             // the MMAs that read A[a] and x[a] have completed (commit); order
             // this warp's tensor-memory stores after that observation
             tc_fence_after();
+            if (dw == 0 && lane == 0) W4A16_TR(2, c);
             const uint32_t z = (zw >> (4 * (g & 7))) & 0xfu;
             const uint32_t zz_hi = 0x64006400u | z | (z << 16);
             const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
@@ -466,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             // re-order to pair order at (t/8)*2048 + kb*128 + (t%8)*16
             cp_async_wait<kXAhead - 1>();
             {
-                const uint8_t *raw = sm_xraw + (c % kXAhead) * C::kXBytes;
+                const uint8_t *raw = team_raw + (li % kXAhead) * C::kXBytes;
                 uint8_t *xb = sm_x + a * C::kXBytes;
 #pragma unroll
                 for (int i = 0; i < C::kPiecesPerThread; ++i) {
@@ -476,12 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     *reinterpret_cast<uint4 *>(xb + (t >> 3) * 2048 + kb * 128 + (t & 7) * 16) = v4;
                 }
             }
-            issue_x(c + kXAhead);  // refills the raw slot just read
+            issue_x(li + kXAhead);  // refills the raw slot just read
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(a_full + a));
+            if (dw == 0 && lane == 0) W4A16_TR(3, c);
         }
         cp_async_wait<0>();
     } else {
@@ -510,19 +552,37 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 break;
             }
             tc_fence_after();
+            if (warp == 0 && lane == 0) W4A16_TR(7, c);
             const uint32_t taddr =
-                tmem + ((uint32_t)(quarter * 32) << 16) + C::kDBase + d * C::kDCols;
+                tmem + ((uint32_t)(quarter * 32) << 16) + C::kDBase + d * kDCols;
+            if constexpr (C::kChains == 1) {
 #pragma unroll
-            for (int t0 = 0; t0 < T; t0 += 16) {
-                float v[16];
-                tmem_ld_x16(taddr + t0, v);
-                tmem_wait_ld();
+                for (int t0 = 0; t0 < T; t0 += 16) {
+                    float v[16];
+                    tmem_ld_x16(taddr + t0, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[t0 + i] = fmaf(sc, v[i], acc[t0 + i]);
+                    for (int i = 0; i < 16; ++i) acc[t0 + i] = fmaf(sc, v[i], acc[t0 + i]);
+                }
+            } else {
+                float sum[T];
+#pragma unroll
+                for (int t = 0; t < T; ++t) sum[t] = 0.f;
+#pragma unroll
+                for (int b = 0; b < kDCols / 16; ++b) {
+                    float v[16];
+                    tmem_ld_x16(taddr + 16 * b, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) sum[(16 * b + i) % T] += v[i];
+                }
+#pragma unroll
+                for (int t = 0; t < T; ++t) acc[t] = fmaf(sc, sum[t], acc[t]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(d_empty + d));
+            if (warp == 0 && lane == 0) W4A16_TR(8, c);
         }
         // one reader decides for all four epilogue warps (named barrier 1)
         asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -637,6 +697,13 @@ cudaError_t tc_init(const DeviceInfo &dev) {
                                  TcConfig<64>::kSmemBytes);
     return e;
 }
+
+#ifdef W4A16_TRACE
+extern "C" int w4a16_debug_trace(unsigned long long *out, int n) {
+    if (n > kTraceEvents * kTraceChunks) n = kTraceEvents * kTraceChunks;
+    return (int)cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long));
+}
+#endif
 
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream) {
