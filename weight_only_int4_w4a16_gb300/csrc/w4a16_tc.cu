@@ -478,8 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             const int sw = (r >> 1) & 3;
             const uint4 w0 = *reinterpret_cast<const uint4 *>(st + 16 * ((2 * half) ^ sw));
             const uint4 w1 = *reinterpret_cast<const uint4 *>(st + 16 * ((2 * half + 1) ^ sw));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(empty + s));
             if (!__all_sync(0xffffffffu,
                             mbar_wait(smem_u32(a_empty + a), ((c / kAStages) & 1) ^ 1, abort))) {
                 fail(abort, p.status, kErrWaitAEmpty);
@@ -502,6 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 v[4 * u + 2] = hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi);
                 v[4 * u + 3] = hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo);
             }
+            // every lane has consumed its words of the stage: release it
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(empty + s));
             tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols + 32 * half, v);
             // x of this group: this thread's pieces arrived (own cp.async group);
             // re-order to pair order at (t/8)*2048 + kb*128 + (t%8)*16
