@@ -428,7 +428,7 @@ def main():
                                     ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
                                     ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] + \
                 [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)]:
-            ts = time_single(w4, M, N, K, cfg, dev, flush=flush, rungs=(-1, 0, 1, 2, 3))
+            ts = time_single(w4, M, N, K, cfg, dev, flush=flush, rungs=(-1, 0, 1, 2, 3, 4, 5))
             by = linear_bytes(M, N, K)
             t = ts[-1]
             singles[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,

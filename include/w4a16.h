@@ -77,7 +77,9 @@ typedef enum {
     W4A16_RUNG_GEMV_SPLITK = 1, /* CUDA cores: K split across CTAs, fixed-order fp32 reduce */
     W4A16_RUNG_TC = 2,          /* tcgen05 dequant-GEMM, tokens as the MMA N dimension */
     W4A16_RUNG_TC_SPLITK = 3,   /* tcgen05 dequant-GEMM with K split across CTAs */
-    W4A16_NUM_RUNGS = 4
+    W4A16_RUNG_MMA = 4,         /* warp MMA (m16n8k16), A = weights dequantised in registers, M <= 8 */
+    W4A16_RUNG_MMA_SPLITK = 5,  /* the same with K split across CTAs */
+    W4A16_NUM_RUNGS = 6
 } w4a16_rung;
 
 /* Select `device`, reserve `workspace_bytes` of split-K workspace (0: 64 MiB)

@@ -39,8 +39,9 @@ def test_every_declared_symbol_is_exported(w4):
 def test_status_and_rung_strings(w4):
     assert w4.lib.w4a16_status_string(0) == b"ok"
     assert w4.lib.w4a16_status_string(99) == b"?"
-    assert [w4.rung_name(i) for i in range(4)] == ["gemv", "gemv_splitk", "tc", "tc_splitk"]
-    assert w4.rung_name(-1) == "auto" and w4.rung_name(7) == "?"
+    assert [w4.rung_name(i) for i in range(6)] == ["gemv", "gemv_splitk", "tc", "tc_splitk",
+                                                   "mma", "mma_splitk"]
+    assert w4.rung_name(-1) == "auto" and w4.rung_name(9) == "?"
 
 
 A = 1 << 20  # a fake, 16-byte aligned "device address": never dereferenced on these paths
@@ -92,9 +93,10 @@ def test_decode_round_validates_every_descriptor(w4):
 
 
 def test_dispatch_table_host_queries(w4):
-    # Pure host queries: the table picks a CUDA-core rung for M <= 8 and
-    # rejects invalid shapes.
-    assert w4.w4a16_select_rung(1, 34816, 5120) in (w4.RUNG_GEMV, w4.RUNG_GEMV_SPLITK)
+    # Pure host queries: the table picks a rung for every valid shape and
+    # rejects invalid ones.
+    assert 0 <= w4.w4a16_select_rung(1, 34816, 5120) < w4.NUM_RUNGS
+    assert w4.w4a16_select_rung(16, 27648, 5120) in (w4.RUNG_TC, w4.RUNG_TC_SPLITK)
     assert w4.w4a16_select_rung(1, 1024, 500) == -1
     assert w4.w4a16_select_rung(0, 1024, 512) == -1
     prev = w4.w4a16_set_forced_rung(w4.RUNG_GEMV_SPLITK)
@@ -109,4 +111,4 @@ def test_dispatch_table_host_queries(w4):
 
 def test_probe_counters_reset(w4):
     w4.w4a16_probe_reset()
-    assert w4.w4a16_probe_counts() == [0, 0, 0, 0]
+    assert w4.w4a16_probe_counts() == [0] * 6

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 CC_RUNGS = [0, 1]  # gemv, gemv_splitk
 TC_RUNGS = [2, 3]  # tc, tc_splitk
-ALL_RUNGS = CC_RUNGS + TC_RUNGS
+MMA_RUNGS = [4, 5]  # mma, mma_splitk
+ALL_RUNGS = CC_RUNGS + TC_RUNGS + MMA_RUNGS
 
 
 @pytest.fixture(scope="module")
@@ -126,7 +127,7 @@ SHAPES = [(1, 1, 128), (1, 7, 256), (1, 1024, 512), (2, 1029, 1152), (3, 64, 512
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_linear_matches_oracle(w4, rung, M, N, K):
     case = Case(si.config_seed(51, M, N % 16), M, N, K)
-    if rung in (w4.RUNG_GEMV_SPLITK, w4.RUNG_TC_SPLITK) and K // 128 < 2:
+    if rung in (w4.RUNG_GEMV_SPLITK, w4.RUNG_TC_SPLITK, w4.RUNG_MMA_SPLITK) and K // 128 < 2:
         pytest.skip("split-K needs two groups")
     with forced(w4, rung):
         if rung >= 0:
@@ -134,8 +135,8 @@ def test_linear_matches_oracle(w4, rung, M, N, K):
         try:
             y = run_linear(w4, case)
         except w4.W4A16Error as e:
-            if rung == w4.RUNG_GEMV and e.status == w4.W4A16_ERR_UNSUPPORTED:
-                pytest.skip("shape needs split-K on the CUDA-core rung")
+            if rung in (w4.RUNG_GEMV, w4.RUNG_MMA) and e.status == w4.W4A16_ERR_UNSUPPORTED:
+                pytest.skip("shape needs split-K on this rung")
             raise
         if rung >= 0:
             assert w4.w4a16_probe_counts()[rung] >= 1
@@ -223,7 +224,7 @@ def test_full_size_sampled(w4, M, N, K, cfg, rung):
     assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"cfg{cfg} M={M}")
 
 
-@pytest.mark.parametrize("rung", [-1, 2])
+@pytest.mark.parametrize("rung", [-1, 2, 4])
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
 def test_m_sweep_sampled(w4, M, rung):
     N, K = 27648, 5120

@@ -39,7 +39,9 @@ RUNG_GEMV = 0
 RUNG_GEMV_SPLITK = 1
 RUNG_TC = 2
 RUNG_TC_SPLITK = 3
-NUM_RUNGS = 4
+RUNG_MMA = 4
+RUNG_MMA_SPLITK = 5
+NUM_RUNGS = 6
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int

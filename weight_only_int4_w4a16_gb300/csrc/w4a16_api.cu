@@ -38,7 +38,8 @@ constexpr size_t kDefaultWorkspace = 64ull << 20;
 constexpr int kCounters = 1 << 16;
 constexpr int kMaxM = 65535;
 
-const char *const kRungNames[W4A16_NUM_RUNGS] = {"gemv", "gemv_splitk", "tc", "tc_splitk"};
+const char *const kRungNames[W4A16_NUM_RUNGS] = {"gemv", "gemv_splitk", "tc",
+                                                  "tc_splitk", "mma", "mma_splitk"};
 
 int cuda_fail(cudaError_t e) {
     t_last_cuda_error = (int)e;
@@ -84,8 +85,11 @@ struct Decision {
 };
 
 bool is_tc(int rung) { return rung == W4A16_RUNG_TC || rung == W4A16_RUNG_TC_SPLITK; }
+bool is_mma(int rung) { return rung == W4A16_RUNG_MMA || rung == W4A16_RUNG_MMA_SPLITK; }
 
-int tile_tokens(int rung) { return is_tc(rung) ? kTcMaxTokens : kGemvMaxTokens; }
+int tile_tokens(int rung) {
+    return is_tc(rung) ? kTcMaxTokens : (is_mma(rung) ? kMmaMaxTokens : kGemvMaxTokens);
+}
 
 Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
@@ -97,15 +101,20 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
         }
         case W4A16_RUNG_GEMV_SPLITK:
         case W4A16_RUNG_TC_SPLITK:
+        case W4A16_RUNG_MMA_SPLITK:
             return {forced, G >= 2 ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
         case W4A16_RUNG_TC:
             return {W4A16_RUNG_TC, W4A16_OK};
+        case W4A16_RUNG_MMA: {
+            MmaPlan p = plan_mma(Mt, N, K, 0, dev);
+            return {W4A16_RUNG_MMA, p.ok ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
+        }
         default:
             break;
     }
-    if (M <= kGemvMaxTokens) {
-        GemvPlan p = plan_gemv(Mt, N, K, -1, dev);
-        return {p.S > 1 ? W4A16_RUNG_GEMV_SPLITK : W4A16_RUNG_GEMV, W4A16_OK};
+    if (M <= kMmaMaxTokens) {
+        MmaPlan p = plan_mma(Mt, N, K, -1, dev);
+        return {p.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, W4A16_OK};
     }
     const int Mtc = M < kTcMaxTokens ? M : kTcMaxTokens;
     TcPlan t = plan_tc(Mtc, N, K, -1, dev);
@@ -115,9 +124,11 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
 int split_rule(int rung) {
     switch (rung) {
         case W4A16_RUNG_GEMV:
-        case W4A16_RUNG_TC: return 0;
+        case W4A16_RUNG_TC:
+        case W4A16_RUNG_MMA: return 0;
         case W4A16_RUNG_GEMV_SPLITK:
-        case W4A16_RUNG_TC_SPLITK: return 1;
+        case W4A16_RUNG_TC_SPLITK:
+        case W4A16_RUNG_MMA_SPLITK: return 1;
     }
     return -1;
 }
@@ -128,6 +139,12 @@ bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t 
                   int *counters) {
     if (is_tc(rung)) {
         TcPlan p = plan_tc(Mt, N, K, split_rule(rung), dev);
+        *bytes = p.ws_bytes;
+        *counters = p.S > 1 ? p.n_tiles : 0;
+        return p.ok;
+    }
+    if (is_mma(rung)) {
+        MmaPlan p = plan_mma(Mt, N, K, split_rule(rung), dev);
         *bytes = p.ws_bytes;
         *counters = p.S > 1 ? p.n_tiles : 0;
         return p.ok;
@@ -178,6 +195,9 @@ int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t s
         if (is_tc(rung)) {
             TcPlan p = plan_tc(Mt, a.N, a.K, split_rule(rung), st.dev);
             e = launch_tc(t, p, st.ws, st.ws.status, stream);
+        } else if (is_mma(rung)) {
+            MmaPlan p = plan_mma(Mt, a.N, a.K, split_rule(rung), st.dev);
+            e = launch_mma(t, p, st.ws, stream);
         } else {
             GemvPlan p = plan_gemv(Mt, a.N, a.K, split_rule(rung), st.dev);
             e = launch_gemv(t, p, st.ws, stream);
@@ -250,6 +270,7 @@ int w4a16_init(int device, size_t workspace_bytes) {
     e = cudaMemset((char *)base + workspace_bytes, 0, counter_bytes);
     if (e == cudaSuccess) e = gemv_init_attributes(dev);
     if (e == cudaSuccess) e = tc_init(dev);
+    if (e == cudaSuccess) e = mma_init(dev);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(base);

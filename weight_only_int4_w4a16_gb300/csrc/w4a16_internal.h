@@ -80,6 +80,24 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
                       cudaStream_t stream);
 cudaError_t tc_init(const DeviceInfo &dev);
 
+// ---- warp-level tensor-core MMA rungs (w4a16_mma.cu) ----------------------
+constexpr int kMmaMaxTokens = 8;  // tokens per launch (the MMA's N = 8)
+
+struct MmaPlan {
+    bool ok;
+    int M;             // tokens (1..8)
+    int S;             // K slices
+    int slice_groups;  // groups per slice
+    int n_tiles;       // 128-row tiles
+    int smem_bytes;    // staged activations
+    size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
+};
+
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev);
+cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
+                       cudaStream_t stream);
+cudaError_t mma_init(const DeviceInfo &dev);
+
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,
                         uint32_t *zeros, cudaStream_t stream);
