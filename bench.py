@@ -204,7 +204,9 @@ def time_e2e(w4, lin, xs, steps, warmup, stream):
 
 
 def flush_l2(buf):
-    buf.add_(1)
+    # read-only sweep of a buffer larger than L2: evicts the weights without
+    # leaving dirty lines whose write-back would slow the timed kernel
+    buf.sum()
 
 
 def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,)):

@@ -89,7 +89,9 @@ struct MmaPlan {
     int S;             // K slices
     int slice_groups;  // groups per slice
     int n_tiles;       // 128-row tiles
-    int smem_bytes;    // staged activations
+    int ctas_per_slice;  // persistent CTAs working on each slice
+    int grid;          // ctas_per_slice * S
+    int smem_bytes;    // copy ring + staged activations
     size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
 };
 

@@ -17,9 +17,16 @@
 //
 //   * MMA rows are weight rows n (a warp owns a 16-row tile, a CTA 128 rows),
 //     MMA columns are the M <= 8 tokens, MMA k runs along K;
-//   * lane (g = lane/4, c = lane%4) loads 16 bytes of row g and of row g + 8:
-//     the 32 k values 32c .. 32c+31 of a 128-wide group, so one warp load
-//     instruction reads 8 rows x 64 contiguous bytes, kDepth groups ahead;
+//   * lane (g = lane/4, c = lane%4) works on row g and row g + 8 of its
+//     warp's tile: the 32 k values 32c .. 32c+31 of each 128-wide group.  The
+//     lane copies its 2 x 16 bytes of weights, the two scale words and the two
+//     zero words of a group with cp.async into its own slot of a kDepth-deep
+//     ring in shared memory (a warp's copy instruction reads 8 rows x 64
+//     contiguous bytes, with a 256-byte L2 fetch), so kDepth groups are in
+//     flight per lane without holding registers, and a lane only ever reads
+//     back its own copies (cp.async.wait_group, no barrier);
+//   * CTAs are persistent: a CTA owns one K slice, stages that slice of x
+//     once, then walks its tiles with one continuous copy stream;
 //   * the unpack (exponent-bias trick, exact) turns each word into four fp16
 //     pairs (q0-z, q4-z) (q1-z, q5-z) (q2-z, q6-z) (q3-z, q7-z), which are the
 //     A fragment registers as they come: the MMA's k slots 2c, 2c+1, 2c+8,
@@ -40,9 +47,11 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTileRows = 16 * kWarps;  // 128 output rows per CTA
-constexpr int kDepth = 4;               // groups in flight per warp
-constexpr int kXBudget = 96 * 1024;     // staged activations per CTA
+constexpr int kTileRows = 16 * kWarps;  // 128 output rows per tile
+constexpr int kDepth = 6;               // groups in flight per lane
+constexpr int kSlotBytes = 48;          // per lane per group: 2x16 weights, 2x4 scales, 2x4 zeros
+constexpr int kRingBytes = kWarps * kDepth * 32 * kSlotBytes;  // 72 KB
+constexpr int kXBudget = 32 * 1024;     // staged activations per CTA
 constexpr int kMinSliceGroups = 4;
 
 struct MmaParams {
@@ -56,13 +65,14 @@ struct MmaParams {
     int N, K, G, ZW, KW;
     int M;  // tokens, 1..8
     int S, slice_groups;
+    int n_tiles, ctas_per_slice;
     int xstride;  // bytes per staged token row
 };
 
 // Staged x: 16-byte unit J of a token row (8 activations, pair order) lives
-// at unit J ^ (bit 3 of J moved to bit 1).  Together with a row stride of
-// 16 (mod 128) bytes this keeps the 16-byte reads of a quarter warp (two
-// tokens x four lanes) on distinct banks.
+// at unit J ^ (bit 3 of J moved to bit 1).  With a row stride of 16 (mod 128)
+// bytes the 16-byte reads of a quarter warp (two tokens x four lanes) fall on
+// distinct banks.
 __device__ __forceinline__ int x_unit(int J) { return J ^ (((J >> 3) & 1) << 1); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -74,46 +84,67 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// global -> shared copies that bypass registers; src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
-    extern __shared__ __align__(128) uint8_t xs[];
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
+    uint8_t *ring = smem;                // [warp][depth][lane][48 B]
+    uint8_t *xs = smem + kRingBytes;     // staged x
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int tile = blockIdx.x, slice = blockIdx.y;
+    const int slice = blockIdx.x % p.S;
+    const int q = blockIdx.x / p.S;      // index among the CTAs of this slice
     const int g0 = slice * p.slice_groups;
-    const int g1 = min(p.G, g0 + p.slice_groups);
-    const int ng = g1 - g0;
+    const int ng = min(p.G, g0 + p.slice_groups) - g0;
+    const int my_tiles = q < p.n_tiles ? (p.n_tiles - 1 - q) / p.ctas_per_slice + 1 : 0;
+    const int steps = my_tiles * ng;     // (tile, group) steps of this CTA
+    uint8_t *my_ring = ring + (size_t)warp * kDepth * 32 * kSlotBytes + lane * kSlotBytes;
 
-    const int ra = tile * kTileRows + warp * 16 + g;  // rows of this lane
-    const int rb = ra + 8;
-    const bool va = ra < p.N, vb = rb < p.N;
-    const uint32_t *wa_row = p.qw + (size_t)(va ? ra : 0) * p.KW + 4 * c;
-    const uint32_t *wb_row = p.qw + (size_t)(vb ? rb : 0) * p.KW + 4 * c;
-    const __half *sa_row = p.scales + (size_t)(va ? ra : 0) * p.G;
-    const __half *sb_row = p.scales + (size_t)(vb ? rb : 0) * p.G;
-    const uint32_t *za_row = p.zeros + (size_t)(va ? ra : 0) * p.ZW;
-    const uint32_t *zb_row = p.zeros + (size_t)(vb ? rb : 0) * p.ZW;
-
-    // ---- weights, scales, zeros of the first kDepth groups: in flight while
-    // x is staged
-    uint4 wa[kDepth], wb[kDepth];
-    float sa[kDepth], sb[kDepth];
-    uint32_t za[kDepth], zb[kDepth];
-    auto load = [&](int d, int i) {
-        const int gg = g0 + i;
-        wa[d] = va ? dev::ld_stream(wa_row + (size_t)gg * 16) : make_uint4(0, 0, 0, 0);
-        wb[d] = vb ? dev::ld_stream(wb_row + (size_t)gg * 16) : make_uint4(0, 0, 0, 0);
-        sa[d] = va ? __half2float(sa_row[gg]) : 0.f;
-        sb[d] = vb ? __half2float(sb_row[gg]) : 0.f;
-        za[d] = va ? __ldg(za_row + (gg >> 3)) : 0u;
-        zb[d] = vb ? __ldg(zb_row + (gg >> 3)) : 0u;
+    // one step's copies: weights of rows ra, rb at the lane's 16 bytes of the
+    // group, and the 32-bit words holding their scales and zeros
+    auto issue = [&](int j) {
+        if (j < steps) {
+            const int lt = j / ng, i = j - lt * ng;
+            const int tile = q + lt * p.ctas_per_slice;
+            const int gg = g0 + i;
+            const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
+            const bool va = ra < p.N, vb = rb < p.N;
+            const uint32_t dst = dev::smem_u32(my_ring + (j % kDepth) * 32 * kSlotBytes);
+            const size_t ia = (size_t)(va ? ra : 0), ib = (size_t)(vb ? rb : 0);
+            cp16(dst, p.qw + ia * p.KW + (size_t)gg * 16 + 4 * c, va ? 16u : 0u);
+            cp16(dst + 16, p.qw + ib * p.KW + (size_t)gg * 16 + 4 * c, vb ? 16u : 0u);
+            // the aligned 32-bit word holding each scale (scales are only
+            // 2-byte aligned); the half is picked when the step is consumed
+            const uintptr_t sa = (uintptr_t)(p.scales + ia * p.G + gg);
+            const uintptr_t sb = (uintptr_t)(p.scales + ib * p.G + gg);
+            cp4(dst + 32, (const void *)(sa & ~(uintptr_t)3), va ? 4u : 0u);
+            cp4(dst + 36, (const void *)(sb & ~(uintptr_t)3), vb ? 4u : 0u);
+            cp4(dst + 40, p.zeros + ia * p.ZW + (gg >> 3), va ? 4u : 0u);
+            cp4(dst + 44, p.zeros + ib * p.ZW + (gg >> 3), vb ? 4u : 0u);
+        }
+        cp_commit();
     };
 #pragma unroll
-    for (int d = 0; d < kDepth; ++d)
-        if (d < ng) load(d, d);
+    for (int j = 0; j < kDepth; ++j) issue(j);
 
-    // ---- stage x[:, slice] in pair order
+    // stage x[:, slice] in pair order (once per CTA)
     {
         const int nunits = ng * (kGroup / 8);
         const int k0 = g0 * kGroup;
@@ -131,77 +162,91 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
     const uint8_t *xrow = xs + (size_t)(has_x ? g : 0) * p.xstride;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 
-    for (int i0 = 0; i0 < ng; i0 += kDepth) {
+    for (int j = 0; j < steps; ++j) {
+        const int lt = j / ng, i = j - lt * ng;
+        const int tile = q + lt * p.ctas_per_slice;
+        const int gg = g0 + i;
+        cp_wait<kDepth - 1>();  // this lane's copies of step j have landed
+        const uint8_t *slot = my_ring + (j % kDepth) * 32 * kSlotBytes;
+        const uint4 wa = *reinterpret_cast<const uint4 *>(slot);
+        const uint4 wb = *reinterpret_cast<const uint4 *>(slot + 16);
+        const uint4 meta = *reinterpret_cast<const uint4 *>(slot + 32);
+        const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
+        const uintptr_t sa = (uintptr_t)(p.scales + (size_t)(ra < p.N ? ra : 0) * p.G + gg);
+        const uintptr_t sb = (uintptr_t)(p.scales + (size_t)(rb < p.N ? rb : 0) * p.G + gg);
+        const float sA = __half2float(
+            __ushort_as_half((unsigned short)(meta.x >> (8 * (unsigned)(sa & 2)))));
+        const float sB = __half2float(
+            __ushort_as_half((unsigned short)(meta.y >> (8 * (unsigned)(sb & 2)))));
+        const dev::ZeroPair zA = dev::zero_pair((meta.z >> (4 * (gg & 7))) & 0xfu);
+        const dev::ZeroPair zB = dev::zero_pair((meta.w >> (4 * (gg & 7))) & 0xfu);
+        const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+        const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+        float dacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-            const int i = i0 + d;
-            if (i < ng) {
-                const int gg = g0 + i;
-                const dev::ZeroPair zA = dev::zero_pair((za[d] >> (4 * (gg & 7))) & 0xfu);
-                const dev::ZeroPair zB = dev::zero_pair((zb[d] >> (4 * (gg & 7))) & 0xfu);
-                const uint32_t wA[4] = {wa[d].x, wa[d].y, wa[d].z, wa[d].w};
-                const uint32_t wB[4] = {wb[d].x, wb[d].y, wb[d].z, wb[d].w};
-                const float sA = sa[d], sB = sb[d];
-                if (i + kDepth < ng) load(d, i + kDepth);
-                float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint32_t qa[4], qb[4];
-                    dev::unpack_word(wA[u], zA, qa);
-                    dev::unpack_word(wB[u], zB, qb);
-                    uint4 xv = make_uint4(0, 0, 0, 0);
-                    if (has_x)
-                        xv = *reinterpret_cast<const uint4 *>(xrow + 16 * x_unit(16 * i + 4 * c + u));
-                    const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
-                    const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
-                    mma16816(dacc, a0, xv.x, xv.y);
-                    mma16816(dacc, a1, xv.z, xv.w);
-                }
-                acc[0] = fmaf(sA, dacc[0], acc[0]);
-                acc[1] = fmaf(sA, dacc[1], acc[1]);
-                acc[2] = fmaf(sB, dacc[2], acc[2]);
-                acc[3] = fmaf(sB, dacc[3], acc[3]);
-            }
+        for (int u = 0; u < 4; ++u) {
+            uint32_t qa[4], qb[4];
+            dev::unpack_word(wA[u], zA, qa);
+            dev::unpack_word(wB[u], zB, qb);
+            uint4 xv = make_uint4(0, 0, 0, 0);
+            if (has_x)
+                xv = *reinterpret_cast<const uint4 *>(xrow + 16 * x_unit(16 * i + 4 * c + u));
+            const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
+            const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
+            mma16816(dacc, a0, xv.x, xv.y);
+            mma16816(dacc, a1, xv.z, xv.w);
         }
-    }
+        // the slot's values are consumed (the MMAs read them): refill it
+        issue(j + kDepth);
+        acc[0] = fmaf(sA, dacc[0], acc[0]);
+        acc[1] = fmaf(sA, dacc[1], acc[1]);
+        acc[2] = fmaf(sB, dacc[2], acc[2]);
+        acc[3] = fmaf(sB, dacc[3], acc[3]);
 
-    // acc[0..1]: row ra, tokens 2c, 2c+1; acc[2..3]: row rb, tokens 2c, 2c+1
-    const int t0 = 2 * c, t1 = 2 * c + 1;
-    if (p.S == 1) {
-        if (va && t0 < p.M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
-        if (va && t1 < p.M) p.y[(size_t)t1 * p.N + ra] = __float2half_rn(acc[1]);
-        if (vb && t0 < p.M) p.y[(size_t)t0 * p.N + rb] = __float2half_rn(acc[2]);
-        if (vb && t1 < p.M) p.y[(size_t)t1 * p.N + rb] = __float2half_rn(acc[3]);
-        return;
-    }
-    float *part = p.partials + (size_t)slice * p.M * p.N;
-    if (va && t0 < p.M) part[(size_t)t0 * p.N + ra] = acc[0];
-    if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
-    if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
-    if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
-    // publish the partials, count the arrival; the last CTA of the tile sums
-    // all slices in slice order
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned prev = atomicAdd(p.counters + tile, 1u);
-        s_last = (prev == (unsigned)(p.S - 1));
-    }
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        const int row0 = tile * kTileRows;
-        const int nrows = min(kTileRows, p.N - row0);
-        for (int idx = threadIdx.x; idx < p.M * nrows; idx += kThreads) {
-            const int t = idx / nrows;
-            const int n = row0 + (idx - t * nrows);
-            float sum = 0.f;
-            for (int s2 = 0; s2 < p.S; ++s2)
-                sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
-            p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
+        if (i == ng - 1) {
+            // end of this tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
+            const int t0 = 2 * c, t1 = 2 * c + 1;
+            const bool va = ra < p.N, vb = rb < p.N;
+            if (p.S == 1) {
+                if (va && t0 < p.M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
+                if (va && t1 < p.M) p.y[(size_t)t1 * p.N + ra] = __float2half_rn(acc[1]);
+                if (vb && t0 < p.M) p.y[(size_t)t0 * p.N + rb] = __float2half_rn(acc[2]);
+                if (vb && t1 < p.M) p.y[(size_t)t1 * p.N + rb] = __float2half_rn(acc[3]);
+            } else {
+                float *part = p.partials + (size_t)slice * p.M * p.N;
+                if (va && t0 < p.M) part[(size_t)t0 * p.N + ra] = acc[0];
+                if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
+                if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
+                if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
+                // publish, count the arrival; the last CTA of the tile sums
+                // the slices in slice order
+                __threadfence();
+                __syncthreads();
+                if (threadIdx.x == 0) {
+                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
+                    s_last = (prev == (unsigned)(p.S - 1));
+                }
+                __syncthreads();
+                if (s_last) {
+                    __threadfence();
+                    const int row0 = tile * kTileRows;
+                    const int nrows = min(kTileRows, p.N - row0);
+                    for (int idx = threadIdx.x; idx < p.M * nrows; idx += kThreads) {
+                        const int t = idx / nrows;
+                        const int n = row0 + (idx - t * nrows);
+                        float sum = 0.f;
+                        for (int s2 = 0; s2 < p.S; ++s2)
+                            sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
+                        p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
+                    }
+                    if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next launch
+                }
+                __syncthreads();  // s_last is read by all before the next tile's update
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         }
-        if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next launch
     }
+    cp_wait<0>();
 }
 
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
@@ -221,12 +266,12 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
         pl.ok = false;
         return pl;
     }
+    const int slots = 2 * dev.sm_count;  // two persistent CTAs per SM
     if (split != 0) {
-        // two resident CTAs per SM; split K until the tiles cover two waves,
-        // keeping at least kMinSliceGroups groups per slice
-        const int want = 4 * dev.sm_count;
-        if (pl.n_tiles * S < want) {
-            int s_fill = (want + pl.n_tiles - 1) / pl.n_tiles;
+        // split K until every slot has a tile, keeping kMinSliceGroups groups
+        // per slice
+        if (pl.n_tiles * S < slots) {
+            int s_fill = (slots + pl.n_tiles - 1) / pl.n_tiles;
             int s_cap = G / kMinSliceGroups > 0 ? G / kMinSliceGroups : 1;
             if (s_fill > s_cap) s_fill = s_cap;
             if (s_fill > S) S = s_fill;
@@ -235,7 +280,12 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     }
     pl.slice_groups = (G + S - 1) / S;
     pl.S = (G + pl.slice_groups - 1) / pl.slice_groups;
-    pl.smem_bytes = M * xstride_for(pl.slice_groups);
+    int per_slice = slots / pl.S;
+    if (per_slice < 1) per_slice = 1;
+    if (per_slice > pl.n_tiles) per_slice = pl.n_tiles;
+    pl.ctas_per_slice = per_slice;
+    pl.grid = per_slice * pl.S;
+    pl.smem_bytes = kRingBytes + M * xstride_for(pl.slice_groups);
     pl.ws_bytes = pl.S > 1 ? (size_t)pl.S * M * N * sizeof(float) : 0;
     pl.ok = true;
     return pl;
@@ -259,14 +309,15 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     p.M = a.M;
     p.S = plan.S;
     p.slice_groups = plan.slice_groups;
+    p.n_tiles = plan.n_tiles;
+    p.ctas_per_slice = plan.ctas_per_slice;
     p.xstride = xstride_for(plan.slice_groups);
-    dim3 grid(plan.n_tiles, plan.S);
-    mma_kernel<<<grid, kThreads, plan.smem_bytes, stream>>>(p);
+    mma_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t mma_init(const DeviceInfo &dev) {
-    int dyn = kXBudget + 1024;
+    int dyn = kRingBytes + kXBudget + 1024;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     return cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
