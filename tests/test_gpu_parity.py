@@ -159,9 +159,14 @@ def test_integer_case_bit_exact(w4, rung):
     assert np.abs(want).max() < 2048
     x = torch.from_numpy(X.astype(np.float16)).to(DEV)
     with forced(w4, rung):
-        y = w4.w4a16_linear(x, torch.from_numpy(qw.view(np.int32)).to(DEV),
-                            torch.from_numpy(s.view(np.float16)).to(DEV),
-                            torch.from_numpy(zw.view(np.int32)).to(DEV))
+        try:
+            y = w4.w4a16_linear(x, torch.from_numpy(qw.view(np.int32)).to(DEV),
+                                torch.from_numpy(s.view(np.float16)).to(DEV),
+                                torch.from_numpy(zw.view(np.int32)).to(DEV))
+        except w4.W4A16Error as e:
+            if e.status == w4.W4A16_ERR_UNSUPPORTED:
+                pytest.skip("rung cannot run this shape")
+            raise
     torch.cuda.synchronize()
     assert np.array_equal(y.float().cpu().numpy().astype(np.float64), want)
 
@@ -224,7 +229,7 @@ def test_full_size_sampled(w4, M, N, K, cfg, rung):
     assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"cfg{cfg} M={M}")
 
 
-@pytest.mark.parametrize("rung", [-1, 2, 4])
+@pytest.mark.parametrize("rung", [-1, 2, 5])
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
 def test_m_sweep_sampled(w4, M, rung):
     N, K = 27648, 5120
@@ -232,7 +237,12 @@ def test_m_sweep_sampled(w4, M, rung):
     qw, s, zw = si.layer(seed, N, K, device=DEV)
     x = si.x(seed, M, K)
     with forced(w4, rung):
-        y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+        try:
+            y = w4.w4a16_linear(x.to(DEV), qw, s, zw)
+        except w4.W4A16Error as e:
+            if e.status == w4.W4A16_ERR_UNSUPPORTED:
+                pytest.skip("rung cannot run this shape")
+            raise
     torch.cuda.synchronize()
     rows = sample_rows(N, 16, seed=M)
     ref = sampled_reference(seed, x, N, K, rows)

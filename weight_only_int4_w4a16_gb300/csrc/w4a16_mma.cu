@@ -101,6 +101,32 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Row pointers of one tile for one lane (rows ra = tile*128 + warp*16 + g and
+// rb = ra + 8), set up once per tile so the per-group copies only add offsets.
+struct TileRows {
+    const uint32_t *qa, *qb;        // weights of the lane's 16 bytes at group g0
+    const uint8_t *sa, *sb;         // byte address of the scale of group g0
+    const uint32_t *za, *zb;        // zeros row
+    uint32_t bytes_a, bytes_b;      // 16 if the row exists, else 0 (copies write zeros)
+};
+
+__device__ __forceinline__ TileRows tile_rows(const MmaParams &p, int tile, int warp, int g, int c,
+                                              int g0) {
+    TileRows t;
+    const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
+    const bool va = ra < p.N, vb = rb < p.N;
+    const size_t ia = (size_t)(va ? ra : 0), ib = (size_t)(vb ? rb : 0);
+    t.qa = p.qw + ia * p.KW + (size_t)g0 * 16 + 4 * c;
+    t.qb = p.qw + ib * p.KW + (size_t)g0 * 16 + 4 * c;
+    t.sa = reinterpret_cast<const uint8_t *>(p.scales + ia * p.G + g0);
+    t.sb = reinterpret_cast<const uint8_t *>(p.scales + ib * p.G + g0);
+    t.za = p.zeros + ia * p.ZW;
+    t.zb = p.zeros + ib * p.ZW;
+    t.bytes_a = va ? 16u : 0u;
+    t.bytes_b = vb ? 16u : 0u;
+    return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
@@ -114,37 +140,40 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
     const int g0 = slice * p.slice_groups;
     const int ng = min(p.G, g0 + p.slice_groups) - g0;
     const int my_tiles = q < p.n_tiles ? (p.n_tiles - 1 - q) / p.ctas_per_slice + 1 : 0;
-    const int steps = my_tiles * ng;     // (tile, group) steps of this CTA
-    uint8_t *my_ring = ring + (size_t)warp * kDepth * 32 * kSlotBytes + lane * kSlotBytes;
+    const uint32_t ring0 =
+        dev::smem_u32(ring + (size_t)warp * kDepth * 32 * kSlotBytes + lane * kSlotBytes);
+    constexpr uint32_t kStageStride = 32 * kSlotBytes;
 
-    // one step's copies: weights of rows ra, rb at the lane's 16 bytes of the
-    // group, and the 32-bit words holding their scales and zeros
-    auto issue = [&](int j) {
-        if (j < steps) {
-            const int lt = j / ng, i = j - lt * ng;
-            const int tile = q + lt * p.ctas_per_slice;
-            const int gg = g0 + i;
-            const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
-            const bool va = ra < p.N, vb = rb < p.N;
-            const uint32_t dst = dev::smem_u32(my_ring + (j % kDepth) * 32 * kSlotBytes);
-            const size_t ia = (size_t)(va ? ra : 0), ib = (size_t)(vb ? rb : 0);
-            cp16(dst, p.qw + ia * p.KW + (size_t)gg * 16 + 4 * c, va ? 16u : 0u);
-            cp16(dst + 16, p.qw + ib * p.KW + (size_t)gg * 16 + 4 * c, vb ? 16u : 0u);
-            // the aligned 32-bit word holding each scale (scales are only
-            // 2-byte aligned); the half is picked when the step is consumed
-            const uintptr_t sa = (uintptr_t)(p.scales + ia * p.G + gg);
-            const uintptr_t sb = (uintptr_t)(p.scales + ib * p.G + gg);
-            cp4(dst + 32, (const void *)(sa & ~(uintptr_t)3), va ? 4u : 0u);
-            cp4(dst + 36, (const void *)(sb & ~(uintptr_t)3), vb ? 4u : 0u);
-            cp4(dst + 40, p.zeros + ia * p.ZW + (gg >> 3), va ? 4u : 0u);
-            cp4(dst + 44, p.zeros + ib * p.ZW + (gg >> 3), vb ? 4u : 0u);
+    // ---- copy stream: one step = one group of one tile; the issue cursor runs
+    // kDepth steps ahead of the consume cursor
+    int is_lt = 0, is_i = 0, is_slot = 0;
+    TileRows ir = tile_rows(p, q, warp, g, c, g0);
+    auto issue_next = [&]() {
+        if (is_lt < my_tiles) {
+            const uint32_t dst = ring0 + is_slot * kStageStride;
+            const int gg = g0 + is_i;
+            cp16(dst, ir.qa + is_i * 16, ir.bytes_a);
+            cp16(dst + 16, ir.qb + is_i * 16, ir.bytes_b);
+            // the aligned 32-bit words holding the scales (2-byte aligned data)
+            cp4(dst + 32, (const void *)((uintptr_t)(ir.sa + 2 * is_i) & ~(uintptr_t)3),
+                ir.bytes_a >> 2);
+            cp4(dst + 36, (const void *)((uintptr_t)(ir.sb + 2 * is_i) & ~(uintptr_t)3),
+                ir.bytes_b >> 2);
+            cp4(dst + 40, ir.za + (gg >> 3), ir.bytes_a >> 2);
+            cp4(dst + 44, ir.zb + (gg >> 3), ir.bytes_b >> 2);
+            is_slot = is_slot + 1 == kDepth ? 0 : is_slot + 1;
+            if (++is_i == ng) {
+                is_i = 0;
+                if (++is_lt < my_tiles)
+                    ir = tile_rows(p, q + is_lt * p.ctas_per_slice, warp, g, c, g0);
+            }
         }
         cp_commit();
     };
 #pragma unroll
-    for (int j = 0; j < kDepth; ++j) issue(j);
+    for (int j = 0; j < kDepth; ++j) issue_next();
 
-    // stage x[:, slice] in pair order (once per CTA)
+    // ---- stage x[:, slice] in pair order (once per CTA)
     {
         const int nunits = ng * (kGroup / 8);
         const int k0 = g0 * kGroup;
@@ -160,91 +189,97 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
 
     const bool has_x = g < p.M;
     const uint8_t *xrow = xs + (size_t)(has_x ? g : 0) * p.xstride;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // unit of word u of this lane's chunk in group i: 16 i + x_unit(4c + u)
+    const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
+    const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
+    int cs_slot = 0;
 
-    for (int j = 0; j < steps; ++j) {
-        const int lt = j / ng, i = j - lt * ng;
+    for (int lt = 0; lt < my_tiles; ++lt) {
         const int tile = q + lt * p.ctas_per_slice;
-        const int gg = g0 + i;
-        cp_wait<kDepth - 1>();  // this lane's copies of step j have landed
-        const uint8_t *slot = my_ring + (j % kDepth) * 32 * kSlotBytes;
-        const uint4 wa = *reinterpret_cast<const uint4 *>(slot);
-        const uint4 wb = *reinterpret_cast<const uint4 *>(slot + 16);
-        const uint4 meta = *reinterpret_cast<const uint4 *>(slot + 32);
         const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
-        const uintptr_t sa = (uintptr_t)(p.scales + (size_t)(ra < p.N ? ra : 0) * p.G + gg);
-        const uintptr_t sb = (uintptr_t)(p.scales + (size_t)(rb < p.N ? rb : 0) * p.G + gg);
-        const float sA = __half2float(
-            __ushort_as_half((unsigned short)(meta.x >> (8 * (unsigned)(sa & 2)))));
-        const float sB = __half2float(
-            __ushort_as_half((unsigned short)(meta.y >> (8 * (unsigned)(sb & 2)))));
-        const dev::ZeroPair zA = dev::zero_pair((meta.z >> (4 * (gg & 7))) & 0xfu);
-        const dev::ZeroPair zB = dev::zero_pair((meta.w >> (4 * (gg & 7))) & 0xfu);
-        const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-        const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-        float dacc[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool va = ra < p.N, vb = rb < p.N;
+        // byte parity of the scale of group g0 in rows ra / rb (selects the half)
+        const uint32_t spa = (uint32_t)((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0) & 2);
+        const uint32_t spb = (uint32_t)((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0) & 2);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < ng; ++i) {
+            const int gg = g0 + i;
+            cp_wait<kDepth - 1>();  // this lane's copies of the step have landed
+            const uint8_t *slot = ring + (size_t)warp * kDepth * 32 * kSlotBytes +
+                                  (size_t)cs_slot * kStageStride + lane * kSlotBytes;
+            cs_slot = cs_slot + 1 == kDepth ? 0 : cs_slot + 1;
+            const uint4 wa = *reinterpret_cast<const uint4 *>(slot);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(slot + 16);
+            const uint4 meta = *reinterpret_cast<const uint4 *>(slot + 32);
+            const uint32_t sh = 8 * ((spa + 2 * (uint32_t)i) & 2);
+            const uint32_t shb = 8 * ((spb + 2 * (uint32_t)i) & 2);
+            const float sA = __half2float(__ushort_as_half((unsigned short)(meta.x >> sh)));
+            const float sB = __half2float(__ushort_as_half((unsigned short)(meta.y >> shb)));
+            const dev::ZeroPair zA = dev::zero_pair((meta.z >> (4 * (gg & 7))) & 0xfu);
+            const dev::ZeroPair zB = dev::zero_pair((meta.w >> (4 * (gg & 7))) & 0xfu);
+            const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+            const int xo[4] = {xo0, xo1, xo2, xo3};
+            const uint8_t *xg = xrow + 256 * i;
+            float dacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            uint32_t qa[4], qb[4];
-            dev::unpack_word(wA[u], zA, qa);
-            dev::unpack_word(wB[u], zB, qb);
-            uint4 xv = make_uint4(0, 0, 0, 0);
-            if (has_x)
-                xv = *reinterpret_cast<const uint4 *>(xrow + 16 * x_unit(16 * i + 4 * c + u));
-            const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
-            const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
-            mma16816(dacc, a0, xv.x, xv.y);
-            mma16816(dacc, a1, xv.z, xv.w);
-        }
-        // the slot's values are consumed (the MMAs read them): refill it
-        issue(j + kDepth);
-        acc[0] = fmaf(sA, dacc[0], acc[0]);
-        acc[1] = fmaf(sA, dacc[1], acc[1]);
-        acc[2] = fmaf(sB, dacc[2], acc[2]);
-        acc[3] = fmaf(sB, dacc[3], acc[3]);
-
-        if (i == ng - 1) {
-            // end of this tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
-            const int t0 = 2 * c, t1 = 2 * c + 1;
-            const bool va = ra < p.N, vb = rb < p.N;
-            if (p.S == 1) {
-                if (va && t0 < p.M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
-                if (va && t1 < p.M) p.y[(size_t)t1 * p.N + ra] = __float2half_rn(acc[1]);
-                if (vb && t0 < p.M) p.y[(size_t)t0 * p.N + rb] = __float2half_rn(acc[2]);
-                if (vb && t1 < p.M) p.y[(size_t)t1 * p.N + rb] = __float2half_rn(acc[3]);
-            } else {
-                float *part = p.partials + (size_t)slice * p.M * p.N;
-                if (va && t0 < p.M) part[(size_t)t0 * p.N + ra] = acc[0];
-                if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
-                if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
-                if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
-                // publish, count the arrival; the last CTA of the tile sums
-                // the slices in slice order
-                __threadfence();
-                __syncthreads();
-                if (threadIdx.x == 0) {
-                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
-                    s_last = (prev == (unsigned)(p.S - 1));
-                }
-                __syncthreads();
-                if (s_last) {
-                    __threadfence();
-                    const int row0 = tile * kTileRows;
-                    const int nrows = min(kTileRows, p.N - row0);
-                    for (int idx = threadIdx.x; idx < p.M * nrows; idx += kThreads) {
-                        const int t = idx / nrows;
-                        const int n = row0 + (idx - t * nrows);
-                        float sum = 0.f;
-                        for (int s2 = 0; s2 < p.S; ++s2)
-                            sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
-                        p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
-                    }
-                    if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next launch
-                }
-                __syncthreads();  // s_last is read by all before the next tile's update
+            for (int u = 0; u < 4; ++u) {
+                uint32_t qa[4], qb[4];
+                dev::unpack_word(wA[u], zA, qa);
+                dev::unpack_word(wB[u], zB, qb);
+                uint4 xv = make_uint4(0, 0, 0, 0);
+                if (has_x) xv = *reinterpret_cast<const uint4 *>(xg + xo[u]);
+                const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
+                const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
+                mma16816(dacc, a0, xv.x, xv.y);
+                mma16816(dacc, a1, xv.z, xv.w);
             }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+            // the slot's values are consumed (the MMAs read them): refill it
+            issue_next();
+            acc[0] = fmaf(sA, dacc[0], acc[0]);
+            acc[1] = fmaf(sA, dacc[1], acc[1]);
+            acc[2] = fmaf(sB, dacc[2], acc[2]);
+            acc[3] = fmaf(sB, dacc[3], acc[3]);
         }
+
+        // ---- end of tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
+        const int t0 = 2 * c, t1 = 2 * c + 1;
+        if (p.S == 1) {
+            if (va && t0 < p.M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
+            if (va && t1 < p.M) p.y[(size_t)t1 * p.N + ra] = __float2half_rn(acc[1]);
+            if (vb && t0 < p.M) p.y[(size_t)t0 * p.N + rb] = __float2half_rn(acc[2]);
+            if (vb && t1 < p.M) p.y[(size_t)t1 * p.N + rb] = __float2half_rn(acc[3]);
+            continue;
+        }
+        float *part = p.partials + (size_t)slice * p.M * p.N;
+        if (va && t0 < p.M) part[(size_t)t0 * p.N + ra] = acc[0];
+        if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
+        if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
+        if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
+        // publish, count the arrival; the last CTA of the tile sums the
+        // slices in slice order
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const unsigned prev = atomicAdd(p.counters + tile, 1u);
+            s_last = (prev == (unsigned)(p.S - 1));
+        }
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            const int row0 = tile * kTileRows;
+            const int nrows = min(kTileRows, p.N - row0);
+            for (int idx = threadIdx.x; idx < p.M * nrows; idx += kThreads) {
+                const int t = idx / nrows;
+                const int n = row0 + (idx - t * nrows);
+                float sum = 0.f;
+                for (int s2 = 0; s2 < p.S; ++s2)
+                    sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
+                p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
+            }
+            if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next launch
+        }
+        __syncthreads();  // every thread has read s_last before the next update
     }
     cp_wait<0>();
 }
