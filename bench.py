@@ -86,7 +86,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -312,19 +312,47 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(M: int, N: int, K: int, rung: int, reps: int):
+    """One seeded linear launched `reps` times (the target of ncu captures)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import synthetic_inputs as si
+    import weight_only_int4_w4a16_gb300 as w4
+    dev = torch.device("cuda:0")
+    w4.w4a16_init(0, 512 << 20)
+    qw, s, zw = si.layer(si.config_seed(1), N, K, device=dev)
+    x = si.x(si.config_seed(1), M, K).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    w4.w4a16_set_forced_rung(rung)
+    for _ in range(reps):
+        w4.w4a16_linear(x, qw, s, zw, y=y)
+    torch.cuda.synchronize()
+    status = w4.w4a16_device_status()
+    print(f"case M={M} N={N} K={K} rung={w4.rung_name(w4.w4a16_select_rung(M, N, K))} "
+          f"reps={reps} device_status={status}")
+    if status:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=N_LAYERS)
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--case", type=int, nargs=5, metavar=("M", "N", "K", "RUNG", "REPS"),
+                    help="profiling helper: run one seeded linear REPS times on a forced rung "
+                         "(-1 = dispatch table) and exit; prints no benchmark line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.case:
+        run_case(*args.case)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
