@@ -19,24 +19,31 @@
 //     MMA columns are the M <= 8 tokens, MMA k runs along K;
 //   * lane (g = lane/4, c = lane%4) works on row g and row g + 8 of its
 //     warp's tile: the 32 k values 32c .. 32c+31 of each 128-wide group.  The
-//     lane copies its 2 x 16 bytes of weights, the two scale words and the two
-//     zero words of a group with cp.async into its own slot of a kDepth-deep
-//     ring in shared memory (a warp's copy instruction reads 8 rows x 64
-//     contiguous bytes, with a 256-byte L2 fetch), so kDepth groups are in
-//     flight per lane without holding registers, and a lane only ever reads
-//     back its own copies (cp.async.wait_group, no barrier);
+//     lane copies its 2 x 16 bytes of weights of a group with cp.async into
+//     its own slot of a kDepth-deep ring in shared memory (a warp's copy
+//     instruction reads 8 rows x 64 contiguous bytes, with a 256-byte L2
+//     fetch), and one of the four 32-bit words holding the scales and zeros of
+//     its row pair (the four lanes of a row pair share them), so kDepth groups
+//     are in flight per lane without holding registers;
 //   * CTAs are persistent: a CTA owns one K slice, stages that slice of x
 //     once, then walks its tiles with one continuous copy stream;
-//   * the unpack (exponent-bias trick, exact) turns each word into four fp16
-//     pairs (q0-z, q4-z) (q1-z, q5-z) (q2-z, q6-z) (q3-z, q7-z), which are the
-//     A fragment registers as they come: the MMA's k slots 2c, 2c+1, 2c+8,
-//     2c+9 stand for the actual k values k0, k4, k1, k5 (and k2, k6, k3, k7
-//     for the second MMA of the word).  The B fragment must use the same
-//     order, so x is staged once per CTA in pair order (x0,x4,x1,x5,...) and
-//     each lane reads its two MMAs' B registers with one 16-byte load;
-//   * the 8 MMAs of a group accumulate (q - z) * x exactly into a fresh fp32
-//     accumulator, which is then scaled by the group's fp32 scale into the
-//     running fp32 sums (scale hoisted out of the k loop);
+//   * the unpack is one lop3 per pair of nibbles: a nibble OR-ed into the
+//     fp16 constant 1024 (even k) or, four bits higher, 64 (odd k) gives the
+//     exact fp16 values (1024 + q) and (64 + q), in the pairs (q0,q4) (q1,q5)
+//     (q2,q6) (q3,q7).  These are the A fragment registers as they come: the
+//     MMA's k slots 2c, 2c+1, 2c+8, 2c+9 stand for the actual k values k0,
+//     k4, k1, k5 (and k2, k6, k3, k7 for the second MMA of the word).  The B
+//     fragment must use the same order, so x is staged once per CTA in pair
+//     order (x0,x4,x1,x5,...) and a lane reads its two MMAs' B registers with
+//     one 16-byte load;
+//   * the 8 MMAs of a group accumulate D = sum (bias_k + q) * x into a fresh
+//     fp32 accumulator (products exact); the zero point and the biases are
+//     removed per group with the token's sums of x over even and odd k,
+//     computed once per CTA:
+//         sum_k (q - z) x = D - (1024 + z) * S_even - (64 + z) * S_odd,
+//     and the group's fp32 scale multiplies that into the running sums.  This
+//     takes the zero subtraction out of the per-weight work (the unpack costs
+//     5 instructions per 8 weights); integer-valued cases stay exact;
 //   * split K: fp32 partials and a last-arriving-CTA reduction in slice order,
 //     as on the other rungs (deterministic, no CTA waits for another).
 #include "w4a16_device.cuh"
@@ -48,11 +55,16 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileRows = 16 * kWarps;  // 128 output rows per tile
-constexpr int kDepth = 6;               // groups in flight per lane
-constexpr int kSlotBytes = 48;          // per lane per group: 2x16 weights, 2x4 scales, 2x4 zeros
-constexpr int kRingBytes = kWarps * kDepth * 32 * kSlotBytes;  // 72 KB
+constexpr int kDepth = 4;               // groups in flight per lane
+// one ring stage of one warp: 32 lanes x 32 bytes of weights, then 8 row
+// pairs x 4 words of metadata (scale word of row g, of row g+8, zeros word of
+// row g, of row g+8)
+constexpr int kStageW = 32 * 32;
+constexpr int kStageBytes = kStageW + 8 * 16;
+constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 36 KB
 constexpr int kXBudget = 32 * 1024;     // staged activations per CTA
 constexpr int kMinSliceGroups = 4;
+constexpr int kMaxSliceGroups = 256;
 
 struct MmaParams {
     const __half *x;
@@ -101,71 +113,77 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Row pointers of one tile for one lane (rows ra = tile*128 + warp*16 + g and
-// rb = ra + 8), set up once per tile so the per-group copies only add offsets.
-struct TileRows {
-    const uint32_t *qa, *qb;        // weights of the lane's 16 bytes at group g0
-    const uint8_t *sa, *sb;         // byte address of the scale of group g0
-    const uint32_t *za, *zb;        // zeros row
-    uint32_t bytes_a, bytes_b;      // 16 if the row exists, else 0 (copies write zeros)
+// Unpack one word with the biases left in: four fp16 pairs
+// (1024+q0, 1024+q4) (64+q1, 64+q5) (1024+q2, 1024+q6) (64+q3, 64+q7).
+__device__ __forceinline__ void unpack_biased(uint32_t w, uint32_t (&d)[4]) {
+    const uint32_t w8 = w >> 8;
+    d[0] = dev::lop3_and_or(w, 0x000f000fu, 0x64006400u);
+    d[1] = dev::lop3_and_or(w, 0x00f000f0u, 0x54005400u);
+    d[2] = dev::lop3_and_or(w8, 0x000f000fu, 0x64006400u);
+    d[3] = dev::lop3_and_or(w8, 0x00f000f0u, 0x54005400u);
+}
+
+// One lane's copy sources for one tile: its two weight rows, and the one
+// metadata item it copies for its row pair (c = 0: scale of row g, 1: scale
+// of row g+8, 2: zeros word of row g, 3: zeros word of row g+8).
+struct TileSrc {
+    const uint32_t *qa, *qb;  // weights at group g0 (lane's 16 bytes)
+    const uint8_t *meta;      // scale element at group g0, or the zeros row
+    uint32_t bytes_a, bytes_b, bytes_m;
 };
 
-__device__ __forceinline__ TileRows tile_rows(const MmaParams &p, int tile, int warp, int g, int c,
-                                              int g0) {
-    TileRows t;
+__device__ __forceinline__ TileSrc tile_src(const MmaParams &p, int tile, int warp, int g, int c,
+                                            int g0) {
+    TileSrc t;
     const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
     const bool va = ra < p.N, vb = rb < p.N;
     const size_t ia = (size_t)(va ? ra : 0), ib = (size_t)(vb ? rb : 0);
     t.qa = p.qw + ia * p.KW + (size_t)g0 * 16 + 4 * c;
     t.qb = p.qw + ib * p.KW + (size_t)g0 * 16 + 4 * c;
-    t.sa = reinterpret_cast<const uint8_t *>(p.scales + ia * p.G + g0);
-    t.sb = reinterpret_cast<const uint8_t *>(p.scales + ib * p.G + g0);
-    t.za = p.zeros + ia * p.ZW;
-    t.zb = p.zeros + ib * p.ZW;
+    const size_t im = (c & 1) ? ib : ia;
+    t.meta = (c < 2) ? reinterpret_cast<const uint8_t *>(p.scales + im * p.G + g0)
+                     : reinterpret_cast<const uint8_t *>(p.zeros + im * p.ZW);
     t.bytes_a = va ? 16u : 0u;
     t.bytes_b = vb ? 16u : 0u;
+    t.bytes_m = ((c & 1) ? vb : va) ? 4u : 0u;
     return t;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
+__global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_last;
-    uint8_t *ring = smem;                // [warp][depth][lane][48 B]
-    uint8_t *xs = smem + kRingBytes;     // staged x
-
+    uint8_t *ring = smem;                   // [warp][stage][kStageBytes]
+    uint8_t *xs = smem + kRingBytes;        // staged x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int slice = blockIdx.x % p.S;
-    const int q = blockIdx.x / p.S;      // index among the CTAs of this slice
+    const int q = blockIdx.x / p.S;         // index among the CTAs of this slice
     const int g0 = slice * p.slice_groups;
     const int ng = min(p.G, g0 + p.slice_groups) - g0;
     const int my_tiles = q < p.n_tiles ? (p.n_tiles - 1 - q) / p.ctas_per_slice + 1 : 0;
-    const uint32_t ring0 =
-        dev::smem_u32(ring + (size_t)warp * kDepth * 32 * kSlotBytes + lane * kSlotBytes);
-    constexpr uint32_t kStageStride = 32 * kSlotBytes;
+    float *sums = reinterpret_cast<float *>(xs + (size_t)p.M * p.xstride);  // [ng][8][2]
+    uint8_t *wring = ring + (size_t)warp * kDepth * kStageBytes;
+    const uint32_t wring_u32 = dev::smem_u32(wring);
 
     // ---- copy stream: one step = one group of one tile; the issue cursor runs
     // kDepth steps ahead of the consume cursor
     int is_lt = 0, is_i = 0, is_slot = 0;
-    TileRows ir = tile_rows(p, q, warp, g, c, g0);
+    TileSrc src = tile_src(p, q, warp, g, c, g0);
     auto issue_next = [&]() {
         if (is_lt < my_tiles) {
-            const uint32_t dst = ring0 + is_slot * kStageStride;
-            const int gg = g0 + is_i;
-            cp16(dst, ir.qa + is_i * 16, ir.bytes_a);
-            cp16(dst + 16, ir.qb + is_i * 16, ir.bytes_b);
-            // the aligned 32-bit words holding the scales (2-byte aligned data)
-            cp4(dst + 32, (const void *)((uintptr_t)(ir.sa + 2 * is_i) & ~(uintptr_t)3),
-                ir.bytes_a >> 2);
-            cp4(dst + 36, (const void *)((uintptr_t)(ir.sb + 2 * is_i) & ~(uintptr_t)3),
-                ir.bytes_b >> 2);
-            cp4(dst + 40, ir.za + (gg >> 3), ir.bytes_a >> 2);
-            cp4(dst + 44, ir.zb + (gg >> 3), ir.bytes_b >> 2);
+            const uint32_t st = wring_u32 + is_slot * kStageBytes;
+            cp16(st + lane * 32, src.qa + is_i * 16, src.bytes_a);
+            cp16(st + lane * 32 + 16, src.qb + is_i * 16, src.bytes_b);
+            // c < 2: the aligned word holding the scale (scales are 2-byte
+            // aligned); c >= 2: the zeros word of the group
+            const uint8_t *m = c < 2 ? (const uint8_t *)((uintptr_t)(src.meta + 2 * is_i) &
+                                                         ~(uintptr_t)3)
+                                     : src.meta + 4 * ((g0 + is_i) >> 3);
+            cp4(st + kStageW + g * 16 + 4 * c, m, src.bytes_m);
             is_slot = is_slot + 1 == kDepth ? 0 : is_slot + 1;
             if (++is_i == ng) {
                 is_i = 0;
-                if (++is_lt < my_tiles)
-                    ir = tile_rows(p, q + is_lt * p.ctas_per_slice, warp, g, c, g0);
+                if (++is_lt < my_tiles) src = tile_src(p, q + is_lt * p.ctas_per_slice, warp, g, c, g0);
             }
         }
         cp_commit();
@@ -173,7 +191,8 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
 #pragma unroll
     for (int j = 0; j < kDepth; ++j) issue_next();
 
-    // ---- stage x[:, slice] in pair order (once per CTA)
+    // ---- stage x[:, slice] in pair order, then each (group, token)'s sums of
+    // x over even and over odd k (once per CTA)
     {
         const int nunits = ng * (kGroup / 8);
         const int k0 = g0 * kGroup;
@@ -184,12 +203,31 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
             *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
                 dev::pair_order(v);
         }
+        __syncthreads();
+        // pair order (x0,x4,x1,x5,x2,x6,x3,x7): even k at positions 0,1,4,5
+        for (int i = threadIdx.x; i < ng * 8; i += kThreads) {
+            const int gi = i >> 3, t = i & 7;
+            float se = 0.f, so = 0.f;
+            if (t < p.M) {
+                const uint8_t *row = xs + (size_t)t * p.xstride + 256 * gi;
+                for (int u = 0; u < 16; ++u) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * x_unit(u));
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+                    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+                    const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+                    se += (a.x + a.y) + (e.x + e.y);
+                    so += (b.x + b.y) + (f.x + f.y);
+                }
+            }
+            sums[2 * i] = se;
+            sums[2 * i + 1] = so;
+        }
     }
     __syncthreads();
 
     const bool has_x = g < p.M;
     const uint8_t *xrow = xs + (size_t)(has_x ? g : 0) * p.xstride;
-    // unit of word u of this lane's chunk in group i: 16 i + x_unit(4c + u)
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
     int cs_slot = 0;
@@ -198,35 +236,32 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
         const int tile = q + lt * p.ctas_per_slice;
         const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
         const bool va = ra < p.N, vb = rb < p.N;
-        // byte parity of the scale of group g0 in rows ra / rb (selects the half)
-        const uint32_t spa = (uint32_t)((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0) & 2);
-        const uint32_t spb = (uint32_t)((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0) & 2);
+        // byte offset (0 or 2) of group g0's scale inside its aligned word
+        const uint32_t spa =
+            (uint32_t)((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0) & 2);
+        const uint32_t spb =
+            (uint32_t)((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0) & 2);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = 0; i < ng; ++i) {
             const int gg = g0 + i;
             cp_wait<kDepth - 1>();  // this lane's copies of the step have landed
-            const uint8_t *slot = ring + (size_t)warp * kDepth * 32 * kSlotBytes +
-                                  (size_t)cs_slot * kStageStride + lane * kSlotBytes;
+            __syncwarp();           // ... and those of the other lanes of the warp
+            const uint8_t *st = wring + cs_slot * kStageBytes;
             cs_slot = cs_slot + 1 == kDepth ? 0 : cs_slot + 1;
-            const uint4 wa = *reinterpret_cast<const uint4 *>(slot);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(slot + 16);
-            const uint4 meta = *reinterpret_cast<const uint4 *>(slot + 32);
-            const uint32_t sh = 8 * ((spa + 2 * (uint32_t)i) & 2);
-            const uint32_t shb = 8 * ((spb + 2 * (uint32_t)i) & 2);
-            const float sA = __half2float(__ushort_as_half((unsigned short)(meta.x >> sh)));
-            const float sB = __half2float(__ushort_as_half((unsigned short)(meta.y >> shb)));
-            const dev::ZeroPair zA = dev::zero_pair((meta.z >> (4 * (gg & 7))) & 0xfu);
-            const dev::ZeroPair zB = dev::zero_pair((meta.w >> (4 * (gg & 7))) & 0xfu);
-            const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-            const int xo[4] = {xo0, xo1, xo2, xo3};
+            const uint4 wa = *reinterpret_cast<const uint4 *>(st + lane * 32);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
+            const uint4 meta = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
+            const float4 sx = *reinterpret_cast<const float4 *>(sums + (i * 8 + 2 * c) * 2);
+            const uint32_t xw[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t yw[4] = {wb.x, wb.y, wb.z, wb.w};
             const uint8_t *xg = xrow + 256 * i;
+            const int xo[4] = {xo0, xo1, xo2, xo3};
             float dacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 uint32_t qa[4], qb[4];
-                dev::unpack_word(wA[u], zA, qa);
-                dev::unpack_word(wB[u], zB, qb);
+                unpack_biased(xw[u], qa);
+                unpack_biased(yw[u], qb);
                 uint4 xv = make_uint4(0, 0, 0, 0);
                 if (has_x) xv = *reinterpret_cast<const uint4 *>(xg + xo[u]);
                 const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
@@ -234,12 +269,31 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
                 mma16816(dacc, a0, xv.x, xv.y);
                 mma16816(dacc, a1, xv.z, xv.w);
             }
-            // the slot's values are consumed (the MMAs read them): refill it
+            // every lane of the row pair has read the stage's metadata and its
+            // own weights: refill the slot
+            __syncwarp();
             issue_next();
-            acc[0] = fmaf(sA, dacc[0], acc[0]);
-            acc[1] = fmaf(sA, dacc[1], acc[1]);
-            acc[2] = fmaf(sB, dacc[2], acc[2]);
-            acc[3] = fmaf(sB, dacc[3], acc[3]);
+            const float sA = __half2float(__ushort_as_half(
+                (unsigned short)(meta.x >> (8 * ((spa + 2 * (uint32_t)i) & 2)))));
+            const float sB = __half2float(__ushort_as_half(
+                (unsigned short)(meta.y >> (8 * ((spb + 2 * (uint32_t)i) & 2)))));
+            const float zA = (float)((meta.z >> (4 * (gg & 7))) & 0xfu);
+            const float zB = (float)((meta.w >> (4 * (gg & 7))) & 0xfu);
+            // sum (q - z) x = D - (1024 + z) S_even - (64 + z) S_odd, per token
+            // (sx = S_even(t0), S_odd(t0), S_even(t1), S_odd(t1))
+            float v;
+            v = fmaf(-(1024.f + zA), sx.x, dacc[0]);
+            v = fmaf(-(64.f + zA), sx.y, v);
+            acc[0] = fmaf(sA, v, acc[0]);
+            v = fmaf(-(1024.f + zA), sx.z, dacc[1]);
+            v = fmaf(-(64.f + zA), sx.w, v);
+            acc[1] = fmaf(sA, v, acc[1]);
+            v = fmaf(-(1024.f + zB), sx.x, dacc[2]);
+            v = fmaf(-(64.f + zB), sx.y, v);
+            acc[2] = fmaf(sB, v, acc[2]);
+            v = fmaf(-(1024.f + zB), sx.z, dacc[3]);
+            v = fmaf(-(64.f + zB), sx.w, v);
+            acc[3] = fmaf(sB, v, acc[3]);
         }
 
         // ---- end of tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
@@ -286,6 +340,10 @@ __global__ void __launch_bounds__(kThreads, 2) mma_kernel(MmaParams p) {
 
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
 
+int smem_for(int M, int slice_groups) {
+    return kRingBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 2 * (int)sizeof(float);
+}
+
 }  // namespace
 
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
@@ -295,13 +353,14 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.n_tiles = (N + kTileRows - 1) / kTileRows;
     // largest slice whose staged x fits the budget
     int max_groups = (kXBudget / M - 16) / (kGroup * 2);
+    if (max_groups > kMaxSliceGroups) max_groups = kMaxSliceGroups;
     if (max_groups < 1) max_groups = 1;
     int S = (G + max_groups - 1) / max_groups;
     if (split == 0 && S > 1) {
         pl.ok = false;
         return pl;
     }
-    const int slots = 2 * dev.sm_count;  // two persistent CTAs per SM
+    const int slots = 3 * dev.sm_count;  // three persistent CTAs per SM
     if (split != 0) {
         // split K until every slot has a tile, keeping kMinSliceGroups groups
         // per slice
@@ -320,7 +379,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     if (per_slice > pl.n_tiles) per_slice = pl.n_tiles;
     pl.ctas_per_slice = per_slice;
     pl.grid = per_slice * pl.S;
-    pl.smem_bytes = kRingBytes + M * xstride_for(pl.slice_groups);
+    pl.smem_bytes = smem_for(M, pl.slice_groups);
     pl.ws_bytes = pl.S > 1 ? (size_t)pl.S * M * N * sizeof(float) : 0;
     pl.ok = true;
     return pl;
@@ -352,7 +411,9 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
 }
 
 cudaError_t mma_init(const DeviceInfo &dev) {
-    int dyn = kRingBytes + kXBudget + 1024;
+    int dyn = smem_for(1, kMaxSliceGroups);
+    const int dyn8 = kRingBytes + kXBudget + kMaxSliceGroups * 64;
+    if (dyn8 > dyn) dyn = dyn8;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     return cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
