@@ -81,6 +81,29 @@ struct MmaParams {
     int xstride;  // bytes per staged token row
 };
 
+// Optional section timers (build with -DW4A16_TRACE): warp 0 of CTA 0 records
+// the SM cycle counter at each step of its first kTraceSteps groups.
+#ifdef W4A16_TRACE
+constexpr int kTraceSteps = 64;
+__device__ long long g_trace_mma[4 * kTraceSteps + 4];
+#define W4A16_MMA_TR(ev, j)                                                          \
+    do {                                                                             \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (j) < kTraceSteps)                \
+            g_trace_mma[(ev) * kTraceSteps + (j)] = clock64();                       \
+    } while (0)
+#define W4A16_MMA_TR_AT(slot)                                                        \
+    do {                                                                             \
+        if (blockIdx.x == 0 && threadIdx.x == 0) g_trace_mma[slot] = clock64();      \
+    } while (0)
+#else
+#define W4A16_MMA_TR(ev, j) \
+    do {                    \
+    } while (0)
+#define W4A16_MMA_TR_AT(slot) \
+    do {                      \
+    } while (0)
+#endif
+
 // Staged x: 16-byte unit J of a token row (8 activations, pair order) lives
 // at unit J ^ (bit 3 of J moved to bit 1).  With a row stride of 16 (mod 128)
 // bytes the 16-byte reads of a quarter warp (two tokens x four lanes) fall on
@@ -156,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     uint8_t *xs = smem + kRingBytes;        // staged x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    W4A16_MMA_TR_AT(4 * kTraceSteps + 1);  // kernel start
     const int slice = blockIdx.x % p.S;
     const int q = blockIdx.x / p.S;         // index among the CTAs of this slice
     const int g0 = slice * p.slice_groups;
@@ -226,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     }
     __syncthreads();
 
+    W4A16_MMA_TR_AT(4 * kTraceSteps);  // prologue done (x staged, sums computed)
     const bool has_x = g < p.M;
     const uint8_t *xrow = xs + (size_t)(has_x ? g : 0) * p.xstride;
+    int jstep = 0;
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
     int cs_slot = 0;
@@ -244,8 +270,10 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = 0; i < ng; ++i) {
             const int gg = g0 + i;
+            W4A16_MMA_TR(0, jstep);
             cp_wait<kDepth - 1>();  // this lane's copies of the step have landed
             __syncwarp();           // ... and those of the other lanes of the warp
+            W4A16_MMA_TR(1, jstep);
             const uint8_t *st = wring + cs_slot * kStageBytes;
             cs_slot = cs_slot + 1 == kDepth ? 0 : cs_slot + 1;
             const uint4 wa = *reinterpret_cast<const uint4 *>(st + lane * 32);
@@ -269,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
                 mma16816(dacc, a0, xv.x, xv.y);
                 mma16816(dacc, a1, xv.z, xv.w);
             }
+            W4A16_MMA_TR(2, jstep);
             // every lane of the row pair has read the stage's metadata and its
             // own weights: refill the slot
             __syncwarp();
@@ -294,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
             v = fmaf(-(1024.f + zB), sx.z, dacc[3]);
             v = fmaf(-(64.f + zB), sx.w, v);
             acc[3] = fmaf(sB, v, acc[3]);
+            W4A16_MMA_TR(3, jstep);
+            ++jstep;
         }
 
         // ---- end of tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
@@ -384,6 +415,13 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.ok = true;
     return pl;
 }
+
+#ifdef W4A16_TRACE
+extern "C" int w4a16_debug_trace_mma(long long *out, int n) {
+    if (n > 4 * kTraceSteps + 4) n = 4 * kTraceSteps + 4;
+    return (int)cudaMemcpyFromSymbol(out, g_trace_mma, n * sizeof(long long));
+}
+#endif
 
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
                        cudaStream_t stream) {
