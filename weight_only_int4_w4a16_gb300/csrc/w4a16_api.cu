@@ -146,7 +146,7 @@ bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t 
     if (is_mma(rung)) {
         MmaPlan p = plan_mma(Mt, N, K, split_rule(rung), dev);
         *bytes = p.ws_bytes;
-        *counters = p.S > 1 ? p.n_tiles : 0;
+        *counters = p.S > 1 ? p.n_strips : 0;
         return p.ok;
     }
     GemvPlan p = plan_gemv(Mt, N, K, split_rule(rung), dev);

@@ -88,7 +88,7 @@ struct MmaPlan {
     int M;             // tokens (1..8)
     int S;             // K slices
     int slice_groups;  // groups per slice
-    int n_tiles;       // 128-row tiles
+    int n_strips;      // 16-row strips (one warp's unit of work)
     int ctas_per_slice;  // persistent CTAs working on each slice
     int grid;          // ctas_per_slice * S
     int smem_bytes;    // copy ring + staged activations

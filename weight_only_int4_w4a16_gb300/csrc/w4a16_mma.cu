@@ -54,7 +54,6 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kTileRows = 16 * kWarps;  // 128 output rows per tile
 constexpr int kDepth = 4;               // groups in flight per lane
 // one ring stage of one warp: 32 lanes x 32 bytes of weights, then 8 row
 // pairs x 4 words of metadata (scale word of row g, of row g+8, zeros word of
@@ -77,7 +76,7 @@ struct MmaParams {
     int N, K, G, ZW, KW;
     int M;  // tokens, 1..8
     int S, slice_groups;
-    int n_tiles, ctas_per_slice;
+    int n_strips, ctas_per_slice;  // 16-row strips; persistent CTAs per slice
     int xstride;  // bytes per staged token row
 };
 
@@ -146,19 +145,18 @@ __device__ __forceinline__ void unpack_biased(uint32_t w, uint32_t (&d)[4]) {
     d[3] = dev::lop3_and_or(w8, 0x00f000f0u, 0x54005400u);
 }
 
-// One lane's copy sources for one tile: its two weight rows, and the one
-// metadata item it copies for its row pair (c = 0: scale of row g, 1: scale
-// of row g+8, 2: zeros word of row g, 3: zeros word of row g+8).
-struct TileSrc {
+// One lane's copy sources for one 16-row strip: its two weight rows, and the
+// one metadata item it copies for its row pair (c = 0: scale of row g, 1:
+// scale of row g+8, 2: zeros word of row g, 3: zeros word of row g+8).
+struct StripSrc {
     const uint32_t *qa, *qb;  // weights at group g0 (lane's 16 bytes)
     const uint8_t *meta;      // scale element at group g0, or the zeros row
     uint32_t bytes_a, bytes_b, bytes_m;
 };
 
-__device__ __forceinline__ TileSrc tile_src(const MmaParams &p, int tile, int warp, int g, int c,
-                                            int g0) {
-    TileSrc t;
-    const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
+__device__ __forceinline__ StripSrc strip_src(const MmaParams &p, int strip, int g, int c, int g0) {
+    StripSrc t;
+    const int ra = strip * 16 + g, rb = ra + 8;
     const bool va = ra < p.N, vb = rb < p.N;
     const size_t ia = (size_t)(va ? ra : 0), ib = (size_t)(vb ? rb : 0);
     t.qa = p.qw + ia * p.KW + (size_t)g0 * 16 + 4 * c;
@@ -174,7 +172,6 @@ __device__ __forceinline__ TileSrc tile_src(const MmaParams &p, int tile, int wa
 
 __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_last;
     uint8_t *ring = smem;                   // [warp][stage][kStageBytes]
     uint8_t *xs = smem + kRingBytes;        // staged x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,17 +181,20 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     const int q = blockIdx.x / p.S;         // index among the CTAs of this slice
     const int g0 = slice * p.slice_groups;
     const int ng = min(p.G, g0 + p.slice_groups) - g0;
-    const int my_tiles = q < p.n_tiles ? (p.n_tiles - 1 - q) / p.ctas_per_slice + 1 : 0;
+    // this warp's strips: first, first + stride, ...
+    const int first = q * kWarps + warp;
+    const int stride = p.ctas_per_slice * kWarps;
+    const int my_strips = first < p.n_strips ? (p.n_strips - 1 - first) / stride + 1 : 0;
     float *sums = reinterpret_cast<float *>(xs + (size_t)p.M * p.xstride);  // [ng][8][2]
     uint8_t *wring = ring + (size_t)warp * kDepth * kStageBytes;
     const uint32_t wring_u32 = dev::smem_u32(wring);
 
-    // ---- copy stream: one step = one group of one tile; the issue cursor runs
-    // kDepth steps ahead of the consume cursor
-    int is_lt = 0, is_i = 0, is_slot = 0;
-    TileSrc src = tile_src(p, q, warp, g, c, g0);
+    // ---- copy stream: one step = one group of one strip; the issue cursor
+    // runs kDepth steps ahead of the consume cursor
+    int is_k = 0, is_i = 0, is_slot = 0;
+    StripSrc src = strip_src(p, first, g, c, g0);
     auto issue_next = [&]() {
-        if (is_lt < my_tiles) {
+        if (is_k < my_strips) {
             const uint32_t st = wring_u32 + is_slot * kStageBytes;
             cp16(st + lane * 32, src.qa + is_i * 16, src.bytes_a);
             cp16(st + lane * 32 + 16, src.qb + is_i * 16, src.bytes_b);
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
             is_slot = is_slot + 1 == kDepth ? 0 : is_slot + 1;
             if (++is_i == ng) {
                 is_i = 0;
-                if (++is_lt < my_tiles) src = tile_src(p, q + is_lt * p.ctas_per_slice, warp, g, c, g0);
+                if (++is_k < my_strips) src = strip_src(p, first + is_k * stride, g, c, g0);
             }
         }
         cp_commit();
@@ -215,37 +215,44 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
 #pragma unroll
     for (int j = 0; j < kDepth; ++j) issue_next();
 
-    // ---- stage x[:, slice] in pair order, then each (group, token)'s sums of
-    // x over even and over odd k (once per CTA)
+    // ---- stage x[:, slice] in pair order, and each (group, token)'s sums of
+    // x over even and over odd k: the 16 lanes of a half warp hold the 16
+    // units of one group of one token and add theirs with shuffles
     {
         const int nunits = ng * (kGroup / 8);
+        const int total = p.M * nunits;  // a multiple of 16
         const int k0 = g0 * kGroup;
-        for (int i = threadIdx.x; i < p.M * nunits; i += kThreads) {
+        for (int base = warp * 32; base < total; base += kThreads) {
+            const int i = base + lane;
+            const bool valid = i < total;
             const int t = i / nunits, J = i - t * nunits;
-            const uint4 v =
-                __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
-            *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
-                dev::pair_order(v);
-        }
-        __syncthreads();
-        // pair order (x0,x4,x1,x5,x2,x6,x3,x7): even k at positions 0,1,4,5
-        for (int i = threadIdx.x; i < ng * 8; i += kThreads) {
-            const int gi = i >> 3, t = i & 7;
-            float se = 0.f, so = 0.f;
-            if (t < p.M) {
-                const uint8_t *row = xs + (size_t)t * p.xstride + 256 * gi;
-                for (int u = 0; u < 16; ++u) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * x_unit(u));
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-                    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-                    const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
-                    se += (a.x + a.y) + (e.x + e.y);
-                    so += (b.x + b.y) + (f.x + f.y);
-                }
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (valid) {
+                v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
+                *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
+                    dev::pair_order(v);
             }
-            sums[2 * i] = se;
-            sums[2 * i + 1] = so;
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+            const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+            float se = (a.x + b.x) + (e.x + f.x);  // k % 8 = 0, 2, 4, 6
+            float so = (a.y + b.y) + (e.y + f.y);  // k % 8 = 1, 3, 5, 7
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) {
+                se += __shfl_xor_sync(0xffffffffu, se, off);
+                so += __shfl_xor_sync(0xffffffffu, so, off);
+            }
+            if (valid && (J & 15) == 0) {
+                sums[((J >> 4) * 8 + t) * 2] = se;
+                sums[((J >> 4) * 8 + t) * 2 + 1] = so;
+            }
+        }
+        // tokens M..7 have no x: their sums are zero
+        for (int i = threadIdx.x; i < ng * (8 - p.M); i += kThreads) {
+            const int gi = i / (8 - p.M), t = p.M + i % (8 - p.M);
+            sums[(gi * 8 + t) * 2] = 0.f;
+            sums[(gi * 8 + t) * 2 + 1] = 0.f;
         }
     }
     __syncthreads();
@@ -258,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
     int cs_slot = 0;
 
-    for (int lt = 0; lt < my_tiles; ++lt) {
-        const int tile = q + lt * p.ctas_per_slice;
-        const int ra = tile * kTileRows + warp * 16 + g, rb = ra + 8;
+    for (int k = 0; k < my_strips; ++k) {
+        const int strip = first + k * stride;
+        const int ra = strip * 16 + g, rb = ra + 8;
         const bool va = ra < p.N, vb = rb < p.N;
         // byte offset (0 or 2) of group g0's scale inside its aligned word
         const uint32_t spa =
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
             ++jstep;
         }
 
-        // ---- end of tile: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
+        // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
         const int t0 = 2 * c, t1 = 2 * c + 1;
         if (p.S == 1) {
             if (va && t0 < p.M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
@@ -341,30 +348,32 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
         if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
         if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
         if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
-        // publish, count the arrival; the last CTA of the tile sums the
-        // slices in slice order
+        // publish this slice of the strip and count the arrival; the warp that
+        // arrives last sums the slices in slice order (no warp waits)
         __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const unsigned prev = atomicAdd(p.counters + tile, 1u);
-            s_last = (prev == (unsigned)(p.S - 1));
-        }
-        __syncthreads();
-        if (s_last) {
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) prev = atomicAdd(p.counters + strip, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (unsigned)(p.S - 1)) {
             __threadfence();
-            const int row0 = tile * kTileRows;
-            const int nrows = min(kTileRows, p.N - row0);
-            for (int idx = threadIdx.x; idx < p.M * nrows; idx += kThreads) {
-                const int t = idx / nrows;
-                const int n = row0 + (idx - t * nrows);
-                float sum = 0.f;
-                for (int s2 = 0; s2 < p.S; ++s2)
-                    sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
-                p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
+            const int rows[2] = {ra, rb};
+            const bool ok[2] = {va, vb};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 2 * c + e;
+                    if (ok[h] && t < p.M) {
+                        float sum = 0.f;
+                        for (int s2 = 0; s2 < p.S; ++s2)
+                            sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + rows[h]);
+                        p.y[(size_t)t * p.N + rows[h]] = __float2half_rn(sum);
+                    }
+                }
             }
-            if (threadIdx.x == 0) p.counters[tile] = 0u;  // ready for the next launch
+            if (lane == 0) p.counters[strip] = 0u;  // ready for the next launch
         }
-        __syncthreads();  // every thread has read s_last before the next update
     }
     cp_wait<0>();
 }
@@ -381,33 +390,44 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     MmaPlan pl{};
     pl.M = M;
     const int G = K / kGroup;
-    pl.n_tiles = (N + kTileRows - 1) / kTileRows;
+    pl.n_strips = (N + 15) / 16;
     // largest slice whose staged x fits the budget
     int max_groups = (kXBudget / M - 16) / (kGroup * 2);
     if (max_groups > kMaxSliceGroups) max_groups = kMaxSliceGroups;
     if (max_groups < 1) max_groups = 1;
-    int S = (G + max_groups - 1) / max_groups;
-    if (split == 0 && S > 1) {
+    const int s_min = (G + max_groups - 1) / max_groups;
+    if (split == 0 && s_min > 1) {
         pl.ok = false;
         return pl;
     }
-    const int slots = 3 * dev.sm_count;  // three persistent CTAs per SM
-    if (split != 0) {
-        // split K until every slot has a tile, keeping kMinSliceGroups groups
-        // per slice
-        if (pl.n_tiles * S < slots) {
-            int s_fill = (slots + pl.n_tiles - 1) / pl.n_tiles;
-            int s_cap = G / kMinSliceGroups > 0 ? G / kMinSliceGroups : 1;
-            if (s_fill > s_cap) s_fill = s_cap;
-            if (s_fill > S) S = s_fill;
+    const int warps = 3 * dev.sm_count * kWarps;  // three persistent CTAs per SM
+    // Pick the number of K slices that minimises the steps of the busiest warp
+    // (strips per warp x groups per slice), plus a small charge per extra
+    // slice for the partial-sum traffic; at least kMinSliceGroups groups per
+    // slice.
+    int best_S = s_min;
+    double best_cost = 1e30;
+    int s_hi = split == 0 ? 1 : (G / kMinSliceGroups > s_min ? G / kMinSliceGroups : s_min);
+    int s_lo = s_min;
+    if (split == 1 && s_lo < 2 && G >= 2) s_lo = 2;
+    if (s_hi < s_lo) s_hi = s_lo;
+    for (int S = s_lo; S <= s_hi; ++S) {
+        const int sg = (G + S - 1) / S;
+        const int S_eff = (G + sg - 1) / sg;
+        const long long units = (long long)pl.n_strips * S_eff;
+        const long long per_warp = (units + warps - 1) / warps;
+        const double cost = (double)per_warp * sg + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best_S = S_eff;
         }
-        if (split == 1 && S < 2 && G >= 2) S = 2;
     }
-    pl.slice_groups = (G + S - 1) / S;
+    pl.slice_groups = (G + best_S - 1) / best_S;
     pl.S = (G + pl.slice_groups - 1) / pl.slice_groups;
-    int per_slice = slots / pl.S;
+    int per_slice = 3 * dev.sm_count / pl.S;
+    const int need = (pl.n_strips + kWarps - 1) / kWarps;  // CTAs to give every strip a warp
+    if (per_slice > need) per_slice = need;
     if (per_slice < 1) per_slice = 1;
-    if (per_slice > pl.n_tiles) per_slice = pl.n_tiles;
     pl.ctas_per_slice = per_slice;
     pl.grid = per_slice * pl.S;
     pl.smem_bytes = smem_for(M, pl.slice_groups);
@@ -441,7 +461,7 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     p.M = a.M;
     p.S = plan.S;
     p.slice_groups = plan.slice_groups;
-    p.n_tiles = plan.n_tiles;
+    p.n_strips = plan.n_strips;
     p.ctas_per_slice = plan.ctas_per_slice;
     p.xstride = xstride_for(plan.slice_groups);
     mma_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(p);
