@@ -111,8 +111,7 @@ __device__ __forceinline__ int x_unit(int J) { return J ^ (((J >> 3) & 1) << 1);
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -189,6 +188,20 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     uint8_t *wring = ring + (size_t)warp * kDepth * kStageBytes;
     const uint32_t wring_u32 = dev::smem_u32(wring);
 
+    // ---- the first pieces of x this thread stages are requested before the
+    // weight stream starts, so they are not queued behind it
+    const int nunits = ng * (kGroup / 8);
+    const int xtotal = p.M * nunits;  // a multiple of 16
+    const int k0 = g0 * kGroup;
+    uint4 xfirst = make_uint4(0, 0, 0, 0);
+    {
+        const int i = warp * 32 + lane;
+        if (i < xtotal) {
+            const int t = i / nunits, J = i - t * nunits;
+            xfirst = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
+        }
+    }
+
     // ---- copy stream: one step = one group of one strip; the issue cursor
     // runs kDepth steps ahead of the consume cursor
     int is_k = 0, is_i = 0, is_slot = 0;
@@ -218,42 +231,38 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     // ---- stage x[:, slice] in pair order, and each (group, token)'s sums of
     // x over even and over odd k: the 16 lanes of a half warp hold the 16
     // units of one group of one token and add theirs with shuffles
-    {
-        const int nunits = ng * (kGroup / 8);
-        const int total = p.M * nunits;  // a multiple of 16
-        const int k0 = g0 * kGroup;
-        for (int base = warp * 32; base < total; base += kThreads) {
-            const int i = base + lane;
-            const bool valid = i < total;
-            const int t = i / nunits, J = i - t * nunits;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
-                *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
-                    dev::pair_order(v);
-            }
-            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-            const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
-            float se = (a.x + b.x) + (e.x + f.x);  // k % 8 = 0, 2, 4, 6
-            float so = (a.y + b.y) + (e.y + f.y);  // k % 8 = 1, 3, 5, 7
+    for (int base = warp * 32; base < xtotal; base += kThreads) {
+        const int i = base + lane;
+        const bool valid = i < xtotal;
+        const int t = i / nunits, J = i - t * nunits;
+        uint4 v = xfirst;
+        if (base != warp * 32)
+            v = valid ? __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J))
+                      : make_uint4(0, 0, 0, 0);
+        if (valid)
+            *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
+                dev::pair_order(v);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+        const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+        float se = (a.x + b.x) + (e.x + f.x);  // k % 8 = 0, 2, 4, 6
+        float so = (a.y + b.y) + (e.y + f.y);  // k % 8 = 1, 3, 5, 7
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) {
-                se += __shfl_xor_sync(0xffffffffu, se, off);
-                so += __shfl_xor_sync(0xffffffffu, so, off);
-            }
-            if (valid && (J & 15) == 0) {
-                sums[((J >> 4) * 8 + t) * 2] = se;
-                sums[((J >> 4) * 8 + t) * 2 + 1] = so;
-            }
+        for (int off = 8; off > 0; off >>= 1) {
+            se += __shfl_xor_sync(0xffffffffu, se, off);
+            so += __shfl_xor_sync(0xffffffffu, so, off);
         }
-        // tokens M..7 have no x: their sums are zero
-        for (int i = threadIdx.x; i < ng * (8 - p.M); i += kThreads) {
-            const int gi = i / (8 - p.M), t = p.M + i % (8 - p.M);
-            sums[(gi * 8 + t) * 2] = 0.f;
-            sums[(gi * 8 + t) * 2 + 1] = 0.f;
+        if (valid && (J & 15) == 0) {
+            sums[((J >> 4) * 8 + t) * 2] = se;
+            sums[((J >> 4) * 8 + t) * 2 + 1] = so;
         }
+    }
+    // tokens M..7 have no x: their sums are zero
+    for (int i = threadIdx.x; i < ng * (8 - p.M); i += kThreads) {
+        const int gi = i / (8 - p.M), t = p.M + i % (8 - p.M);
+        sums[(gi * 8 + t) * 2] = 0.f;
+        sums[(gi * 8 + t) * 2 + 1] = 0.f;
     }
     __syncthreads();
 
@@ -286,35 +295,47 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
             const uint4 wa = *reinterpret_cast<const uint4 *>(st + lane * 32);
             const uint4 wb = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
             const uint4 meta = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
-            const float4 sx = *reinterpret_cast<const float4 *>(sums + (i * 8 + 2 * c) * 2);
-            const uint32_t xw[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t yw[4] = {wb.x, wb.y, wb.z, wb.w};
-            const uint8_t *xg = xrow + 256 * i;
-            const int xo[4] = {xo0, xo1, xo2, xo3};
-            float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint32_t qa[4], qb[4];
-                unpack_biased(xw[u], qa);
-                unpack_biased(yw[u], qb);
-                uint4 xv = make_uint4(0, 0, 0, 0);
-                if (has_x) xv = *reinterpret_cast<const uint4 *>(xg + xo[u]);
-                const uint32_t a0[4] = {qa[0], qb[0], qa[1], qb[1]};
-                const uint32_t a1[4] = {qa[2], qb[2], qa[3], qb[3]};
-                mma16816(dacc, a0, xv.x, xv.y);
-                mma16816(dacc, a1, xv.z, xv.w);
-            }
-            W4A16_MMA_TR(2, jstep);
-            // every lane of the row pair has read the stage's metadata and its
-            // own weights: refill the slot
-            __syncwarp();
-            issue_next();
+            // unpack all eight words and decode the metadata: once every lane
+            // has its values in registers the slot can be refilled
+            uint32_t qa[4][4], qb[4][4];
+            unpack_biased(wa.x, qa[0]);
+            unpack_biased(wa.y, qa[1]);
+            unpack_biased(wa.z, qa[2]);
+            unpack_biased(wa.w, qa[3]);
+            unpack_biased(wb.x, qb[0]);
+            unpack_biased(wb.y, qb[1]);
+            unpack_biased(wb.z, qb[2]);
+            unpack_biased(wb.w, qb[3]);
             const float sA = __half2float(__ushort_as_half(
                 (unsigned short)(meta.x >> (8 * ((spa + 2 * (uint32_t)i) & 2)))));
             const float sB = __half2float(__ushort_as_half(
                 (unsigned short)(meta.y >> (8 * ((spb + 2 * (uint32_t)i) & 2)))));
             const float zA = (float)((meta.z >> (4 * (gg & 7))) & 0xfu);
             const float zB = (float)((meta.w >> (4 * (gg & 7))) & 0xfu);
+            __syncwarp();
+            issue_next();
+            const float4 sx = *reinterpret_cast<const float4 *>(sums + (i * 8 + 2 * c) * 2);
+            const uint8_t *xg = xrow + 256 * i;
+            uint4 xv[4];
+            xv[0] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo0) : make_uint4(0, 0, 0, 0);
+            xv[1] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo1) : make_uint4(0, 0, 0, 0);
+            xv[2] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo2) : make_uint4(0, 0, 0, 0);
+            xv[3] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo3) : make_uint4(0, 0, 0, 0);
+            // two independent accumulator chains (words 0,1 and 2,3)
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t a0[4] = {qa[u][0], qb[u][0], qa[u][1], qb[u][1]};
+                const uint32_t a1[4] = {qa[u][2], qb[u][2], qa[u][3], qb[u][3]};
+                const uint32_t a2[4] = {qa[u + 2][0], qb[u + 2][0], qa[u + 2][1], qb[u + 2][1]};
+                const uint32_t a3[4] = {qa[u + 2][2], qb[u + 2][2], qa[u + 2][3], qb[u + 2][3]};
+                mma16816(d0, a0, xv[u].x, xv[u].y);
+                mma16816(d1, a2, xv[u + 2].x, xv[u + 2].y);
+                mma16816(d0, a1, xv[u].z, xv[u].w);
+                mma16816(d1, a3, xv[u + 2].z, xv[u + 2].w);
+            }
+            W4A16_MMA_TR(2, jstep);
+            const float dacc[4] = {d0[0] + d1[0], d0[1] + d1[1], d0[2] + d1[2], d0[3] + d1[3]};
             // sum (q - z) x = D - (1024 + z) S_even - (64 + z) S_odd, per token
             // (sx = S_even(t0), S_odd(t0), S_even(t1), S_odd(t1))
             float v;
