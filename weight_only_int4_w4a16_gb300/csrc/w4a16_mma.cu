@@ -148,8 +148,8 @@ __device__ __forceinline__ void unpack_biased(uint32_t w, uint32_t (&d)[4]) {
 // one metadata item it copies for its row pair (c = 0: scale of row g, 1:
 // scale of row g+8, 2: zeros word of row g, 3: zeros word of row g+8).
 struct StripSrc {
-    const uint32_t *qa, *qb;  // weights at group g0 (lane's 16 bytes)
-    const uint8_t *meta;      // scale element at group g0, or the zeros row
+    const uint32_t *qa, *qb;  // weights of the next group to copy (lane's 16 bytes)
+    uintptr_t meta;           // byte address: scale element, or zeros word, of that group
     uint32_t bytes_a, bytes_b, bytes_m;
 };
 
@@ -161,21 +161,31 @@ __device__ __forceinline__ StripSrc strip_src(const MmaParams &p, int strip, int
     t.qa = p.qw + ia * p.KW + (size_t)g0 * 16 + 4 * c;
     t.qb = p.qw + ib * p.KW + (size_t)g0 * 16 + 4 * c;
     const size_t im = (c & 1) ? ib : ia;
-    t.meta = (c < 2) ? reinterpret_cast<const uint8_t *>(p.scales + im * p.G + g0)
-                     : reinterpret_cast<const uint8_t *>(p.zeros + im * p.ZW);
+    t.meta = (c < 2) ? (uintptr_t)(p.scales + im * p.G + g0)
+                     : (uintptr_t)(p.zeros + im * p.ZW + (g0 >> 3));
     t.bytes_a = va ? 16u : 0u;
     t.bytes_b = vb ? 16u : 0u;
     t.bytes_m = ((c & 1) ? vb : va) ? 4u : 0u;
     return t;
 }
 
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;                   // [warp][stage][kStageBytes]
-    uint8_t *xs = smem + kRingBytes;        // staged x
+    uint8_t *xs = smem + kRingBytes;        // staged x, then 256 zero bytes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     W4A16_MMA_TR_AT(4 * kTraceSteps + 1);  // kernel start
+    // the next kernel in the stream may be scheduled as SMs free up; it waits
+    // for this grid to finish before it touches anything this grid writes
+    grid_dependents_launch();
     const int slice = blockIdx.x % p.S;
     const int q = blockIdx.x / p.S;         // index among the CTAs of this slice
     const int g0 = slice * p.slice_groups;
@@ -184,39 +194,31 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
     const int first = q * kWarps + warp;
     const int stride = p.ctas_per_slice * kWarps;
     const int my_strips = first < p.n_strips ? (p.n_strips - 1 - first) / stride + 1 : 0;
-    float *sums = reinterpret_cast<float *>(xs + (size_t)p.M * p.xstride);  // [ng][8][2]
+    uint8_t *zero_x = xs + (size_t)p.M * p.xstride;                     // 256 zero bytes
+    float *sums = reinterpret_cast<float *>(zero_x + 256);              // [ng][8][2]
     uint8_t *wring = ring + (size_t)warp * kDepth * kStageBytes;
     const uint32_t wring_u32 = dev::smem_u32(wring);
 
-    // ---- the first pieces of x this thread stages are requested before the
-    // weight stream starts, so they are not queued behind it
-    const int nunits = ng * (kGroup / 8);
-    const int xtotal = p.M * nunits;  // a multiple of 16
-    const int k0 = g0 * kGroup;
-    uint4 xfirst = make_uint4(0, 0, 0, 0);
-    {
-        const int i = warp * 32 + lane;
-        if (i < xtotal) {
-            const int t = i / nunits, J = i - t * nunits;
-            xfirst = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
-        }
-    }
-
     // ---- copy stream: one step = one group of one strip; the issue cursor
-    // runs kDepth steps ahead of the consume cursor
+    // runs kDepth steps ahead of the consume cursor.  Weights, scales and
+    // zeros are parameters (never written by a preceding kernel), so the
+    // stream starts before the grid-dependency wait.
     int is_k = 0, is_i = 0, is_slot = 0;
     StripSrc src = strip_src(p, first, g, c, g0);
+    const uint32_t dst_w = wring_u32 + lane * 32;
+    const uint32_t dst_m = wring_u32 + kStageW + g * 16 + 4 * c;
     auto issue_next = [&]() {
         if (is_k < my_strips) {
-            const uint32_t st = wring_u32 + is_slot * kStageBytes;
-            cp16(st + lane * 32, src.qa + is_i * 16, src.bytes_a);
-            cp16(st + lane * 32 + 16, src.qb + is_i * 16, src.bytes_b);
+            const uint32_t so = is_slot * kStageBytes;
+            cp16(dst_w + so, src.qa, src.bytes_a);
+            cp16(dst_w + so + 16, src.qb, src.bytes_b);
             // c < 2: the aligned word holding the scale (scales are 2-byte
             // aligned); c >= 2: the zeros word of the group
-            const uint8_t *m = c < 2 ? (const uint8_t *)((uintptr_t)(src.meta + 2 * is_i) &
-                                                         ~(uintptr_t)3)
-                                     : src.meta + 4 * ((g0 + is_i) >> 3);
-            cp4(st + kStageW + g * 16 + 4 * c, m, src.bytes_m);
+            cp4(dst_m + so, (const void *)(c < 2 ? (src.meta & ~(uintptr_t)3) : src.meta),
+                src.bytes_m);
+            src.qa += 16;
+            src.qb += 16;
+            src.meta += c < 2 ? 2 : (((g0 + is_i + 1) & 7) == 0 ? 4 : 0);
             is_slot = is_slot + 1 == kDepth ? 0 : is_slot + 1;
             if (++is_i == ng) {
                 is_i = 0;
@@ -228,128 +230,149 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
 #pragma unroll
     for (int j = 0; j < kDepth; ++j) issue_next();
 
+    // ---- from here on: x, y and the split-K workspace may belong to the
+    // preceding kernel
+    grid_dependency_wait();
+
     // ---- stage x[:, slice] in pair order, and each (group, token)'s sums of
     // x over even and over odd k: the 16 lanes of a half warp hold the 16
     // units of one group of one token and add theirs with shuffles
-    for (int base = warp * 32; base < xtotal; base += kThreads) {
-        const int i = base + lane;
-        const bool valid = i < xtotal;
-        const int t = i / nunits, J = i - t * nunits;
-        uint4 v = xfirst;
-        if (base != warp * 32)
-            v = valid ? __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J))
-                      : make_uint4(0, 0, 0, 0);
-        if (valid)
-            *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
-                dev::pair_order(v);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-        const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
-        float se = (a.x + b.x) + (e.x + f.x);  // k % 8 = 0, 2, 4, 6
-        float so = (a.y + b.y) + (e.y + f.y);  // k % 8 = 1, 3, 5, 7
+    {
+        const int nunits = ng * (kGroup / 8);
+        const int xtotal = p.M * nunits;  // a multiple of 16
+        const int k0 = g0 * kGroup;
+        for (int base = warp * 32; base < xtotal; base += kThreads) {
+            const int i = base + lane;
+            const bool valid = i < xtotal;
+            const int t = i / nunits, J = i - t * nunits;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (valid) {
+                v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
+                *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
+                    dev::pair_order(v);
+            }
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+            const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+            float se = (a.x + b.x) + (e.x + f.x);  // k % 8 = 0, 2, 4, 6
+            float so = (a.y + b.y) + (e.y + f.y);  // k % 8 = 1, 3, 5, 7
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) {
-            se += __shfl_xor_sync(0xffffffffu, se, off);
-            so += __shfl_xor_sync(0xffffffffu, so, off);
+            for (int off = 8; off > 0; off >>= 1) {
+                se += __shfl_xor_sync(0xffffffffu, se, off);
+                so += __shfl_xor_sync(0xffffffffu, so, off);
+            }
+            if (valid && (J & 15) == 0) {
+                sums[((J >> 4) * 8 + t) * 2] = se;
+                sums[((J >> 4) * 8 + t) * 2 + 1] = so;
+            }
         }
-        if (valid && (J & 15) == 0) {
-            sums[((J >> 4) * 8 + t) * 2] = se;
-            sums[((J >> 4) * 8 + t) * 2 + 1] = so;
+        // tokens M..7 have no x: their sums are zero; so is the zero block
+        for (int i = threadIdx.x; i < ng * (8 - p.M); i += kThreads) {
+            const int gi = i / (8 - p.M), t = p.M + i % (8 - p.M);
+            sums[(gi * 8 + t) * 2] = 0.f;
+            sums[(gi * 8 + t) * 2 + 1] = 0.f;
         }
-    }
-    // tokens M..7 have no x: their sums are zero
-    for (int i = threadIdx.x; i < ng * (8 - p.M); i += kThreads) {
-        const int gi = i / (8 - p.M), t = p.M + i % (8 - p.M);
-        sums[(gi * 8 + t) * 2] = 0.f;
-        sums[(gi * 8 + t) * 2 + 1] = 0.f;
+        if (threadIdx.x < 16) reinterpret_cast<uint4 *>(zero_x)[threadIdx.x] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
 
     W4A16_MMA_TR_AT(4 * kTraceSteps);  // prologue done (x staged, sums computed)
     const bool has_x = g < p.M;
     const uint8_t *xrow = xs + (size_t)(has_x ? g : 0) * p.xstride;
-    int jstep = 0;
+    // unit of word u of this lane's chunk in a group: x_unit(4c + u)
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
+    const uint8_t *cs_base = wring + lane * 32;
+    const uint8_t *cs_meta = wring + kStageW + g * 16;
     int cs_slot = 0;
+    int jstep = 0;
 
     for (int k = 0; k < my_strips; ++k) {
         const int strip = first + k * stride;
         const int ra = strip * 16 + g, rb = ra + 8;
         const bool va = ra < p.N, vb = rb < p.N;
-        // byte offset (0 or 2) of group g0's scale inside its aligned word
-        const uint32_t spa =
-            (uint32_t)((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0) & 2);
-        const uint32_t spb =
-            (uint32_t)((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0) & 2);
+        // shift that brings group g0's scale to the low half of its word; it
+        // flips by 16 bits from one group to the next
+        uint32_t sha = 8u * (uint32_t)((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0) & 2);
+        uint32_t shb = 8u * (uint32_t)((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0) & 2);
+        uint32_t zsh = 4u * (uint32_t)(g0 & 7);  // nibble of the group in its zeros word
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = 0; i < ng; ++i) {
-            const int gg = g0 + i;
             W4A16_MMA_TR(0, jstep);
             cp_wait<kDepth - 1>();  // this lane's copies of the step have landed
             __syncwarp();           // ... and those of the other lanes of the warp
             W4A16_MMA_TR(1, jstep);
-            const uint8_t *st = wring + cs_slot * kStageBytes;
+            const uint32_t so = cs_slot * kStageBytes;
             cs_slot = cs_slot + 1 == kDepth ? 0 : cs_slot + 1;
-            const uint4 wa = *reinterpret_cast<const uint4 *>(st + lane * 32);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(st + lane * 32 + 16);
-            const uint4 meta = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
-            // unpack all eight words and decode the metadata: once every lane
-            // has its values in registers the slot can be refilled
-            uint32_t qa[4][4], qb[4][4];
-            unpack_biased(wa.x, qa[0]);
-            unpack_biased(wa.y, qa[1]);
-            unpack_biased(wa.z, qa[2]);
-            unpack_biased(wa.w, qa[3]);
-            unpack_biased(wb.x, qb[0]);
-            unpack_biased(wb.y, qb[1]);
-            unpack_biased(wb.z, qb[2]);
-            unpack_biased(wb.w, qb[3]);
-            const float sA = __half2float(__ushort_as_half(
-                (unsigned short)(meta.x >> (8 * ((spa + 2 * (uint32_t)i) & 2)))));
-            const float sB = __half2float(__ushort_as_half(
-                (unsigned short)(meta.y >> (8 * ((spb + 2 * (uint32_t)i) & 2)))));
-            const float zA = (float)((meta.z >> (4 * (gg & 7))) & 0xfu);
-            const float zB = (float)((meta.w >> (4 * (gg & 7))) & 0xfu);
+            const uint4 wa = *reinterpret_cast<const uint4 *>(cs_base + so);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(cs_base + so + 16);
+            const uint4 meta = *reinterpret_cast<const uint4 *>(cs_meta + so);
+            // A fragments straight from the unpack: MMA 2u takes the pairs
+            // (q0,q4) (q1,q5) of word u, MMA 2u+1 the pairs (q2,q6) (q3,q7);
+            // rows g and g + 8 interleave as the fragment layout wants
+            uint32_t a[8][4];
+            const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t xa = wA[u], xb = wB[u], xa8 = xa >> 8, xb8 = xb >> 8;
+                a[2 * u][0] = dev::lop3_and_or(xa, 0x000f000fu, 0x64006400u);
+                a[2 * u][1] = dev::lop3_and_or(xb, 0x000f000fu, 0x64006400u);
+                a[2 * u][2] = dev::lop3_and_or(xa, 0x00f000f0u, 0x54005400u);
+                a[2 * u][3] = dev::lop3_and_or(xb, 0x00f000f0u, 0x54005400u);
+                a[2 * u + 1][0] = dev::lop3_and_or(xa8, 0x000f000fu, 0x64006400u);
+                a[2 * u + 1][1] = dev::lop3_and_or(xb8, 0x000f000fu, 0x64006400u);
+                a[2 * u + 1][2] = dev::lop3_and_or(xa8, 0x00f000f0u, 0x54005400u);
+                a[2 * u + 1][3] = dev::lop3_and_or(xb8, 0x00f000f0u, 0x54005400u);
+            }
+            // scale halves and zero nibbles of the two rows, decoded before
+            // the slot is released
+            const float sA = __half2float(__ushort_as_half((unsigned short)(meta.x >> sha)));
+            const float sB = __half2float(__ushort_as_half((unsigned short)(meta.y >> shb)));
+            const uint32_t zA = (meta.z >> zsh) & 0xfu, zB = (meta.w >> zsh) & 0xfu;
+            sha ^= 16u;
+            shb ^= 16u;
+            zsh = (zsh + 4u) & 31u;
+            // the slot's values are in registers in every lane: refill it
             __syncwarp();
             issue_next();
+            // 1024 + z and 64 + z as exact fp32 (z in the mantissa)
+            const float hA = __uint_as_float(0x44800000u | (zA << 13));
+            const float lA = __uint_as_float(0x42800000u | (zA << 17));
+            const float hB = __uint_as_float(0x44800000u | (zB << 13));
+            const float lB = __uint_as_float(0x42800000u | (zB << 17));
             const float4 sx = *reinterpret_cast<const float4 *>(sums + (i * 8 + 2 * c) * 2);
-            const uint8_t *xg = xrow + 256 * i;
-            uint4 xv[4];
-            xv[0] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo0) : make_uint4(0, 0, 0, 0);
-            xv[1] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo1) : make_uint4(0, 0, 0, 0);
-            xv[2] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo2) : make_uint4(0, 0, 0, 0);
-            xv[3] = has_x ? *reinterpret_cast<const uint4 *>(xg + xo3) : make_uint4(0, 0, 0, 0);
-            // two independent accumulator chains (words 0,1 and 2,3)
+            const uint8_t *xg = has_x ? xrow + 256 * i : zero_x;
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(xg + (has_x ? xo0 : 0));
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(xg + (has_x ? xo1 : 0));
+            const uint4 x2 = *reinterpret_cast<const uint4 *>(xg + (has_x ? xo2 : 0));
+            const uint4 x3 = *reinterpret_cast<const uint4 *>(xg + (has_x ? xo3 : 0));
+            // two independent accumulator chains (words 0,1 and words 2,3)
             float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint32_t a0[4] = {qa[u][0], qb[u][0], qa[u][1], qb[u][1]};
-                const uint32_t a1[4] = {qa[u][2], qb[u][2], qa[u][3], qb[u][3]};
-                const uint32_t a2[4] = {qa[u + 2][0], qb[u + 2][0], qa[u + 2][1], qb[u + 2][1]};
-                const uint32_t a3[4] = {qa[u + 2][2], qb[u + 2][2], qa[u + 2][3], qb[u + 2][3]};
-                mma16816(d0, a0, xv[u].x, xv[u].y);
-                mma16816(d1, a2, xv[u + 2].x, xv[u + 2].y);
-                mma16816(d0, a1, xv[u].z, xv[u].w);
-                mma16816(d1, a3, xv[u + 2].z, xv[u + 2].w);
-            }
+            mma16816(d0, a[0], x0.x, x0.y);
+            mma16816(d1, a[4], x2.x, x2.y);
+            mma16816(d0, a[1], x0.z, x0.w);
+            mma16816(d1, a[5], x2.z, x2.w);
+            mma16816(d0, a[2], x1.x, x1.y);
+            mma16816(d1, a[6], x3.x, x3.y);
+            mma16816(d0, a[3], x1.z, x1.w);
+            mma16816(d1, a[7], x3.z, x3.w);
             W4A16_MMA_TR(2, jstep);
-            const float dacc[4] = {d0[0] + d1[0], d0[1] + d1[1], d0[2] + d1[2], d0[3] + d1[3]};
             // sum (q - z) x = D - (1024 + z) S_even - (64 + z) S_odd, per token
             // (sx = S_even(t0), S_odd(t0), S_even(t1), S_odd(t1))
             float v;
-            v = fmaf(-(1024.f + zA), sx.x, dacc[0]);
-            v = fmaf(-(64.f + zA), sx.y, v);
+            v = fmaf(-hA, sx.x, d0[0] + d1[0]);
+            v = fmaf(-lA, sx.y, v);
             acc[0] = fmaf(sA, v, acc[0]);
-            v = fmaf(-(1024.f + zA), sx.z, dacc[1]);
-            v = fmaf(-(64.f + zA), sx.w, v);
+            v = fmaf(-hA, sx.z, d0[1] + d1[1]);
+            v = fmaf(-lA, sx.w, v);
             acc[1] = fmaf(sA, v, acc[1]);
-            v = fmaf(-(1024.f + zB), sx.x, dacc[2]);
-            v = fmaf(-(64.f + zB), sx.y, v);
+            v = fmaf(-hB, sx.x, d0[2] + d1[2]);
+            v = fmaf(-lB, sx.y, v);
             acc[2] = fmaf(sB, v, acc[2]);
-            v = fmaf(-(1024.f + zB), sx.z, dacc[3]);
-            v = fmaf(-(64.f + zB), sx.w, v);
+            v = fmaf(-hB, sx.z, d0[3] + d1[3]);
+            v = fmaf(-lB, sx.w, v);
             acc[3] = fmaf(sB, v, acc[3]);
             W4A16_MMA_TR(3, jstep);
             ++jstep;
@@ -369,15 +392,20 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
         if (va && t1 < p.M) part[(size_t)t1 * p.N + ra] = acc[1];
         if (vb && t0 < p.M) part[(size_t)t0 * p.N + rb] = acc[2];
         if (vb && t1 < p.M) part[(size_t)t1 * p.N + rb] = acc[3];
-        // publish this slice of the strip and count the arrival; the warp that
-        // arrives last sums the slices in slice order (no warp waits)
-        __threadfence();
+        // count this slice's arrival for the strip with one release-acquire
+        // atomic after a warp barrier (the barrier orders the other lanes'
+        // partial writes before it); the warp that arrives last sums the
+        // slices in slice order.  No warp waits for another.
         __syncwarp();
         unsigned prev = 0;
-        if (lane == 0) prev = atomicAdd(p.counters + strip, 1u);
+        if (lane == 0)
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(prev)
+                         : "l"(p.counters + strip)
+                         : "memory");
         prev = __shfl_sync(0xffffffffu, prev, 0);
+        __syncwarp();  // the other lanes' reads below come after lane 0's acquire
         if (prev == (unsigned)(p.S - 1)) {
-            __threadfence();
             const int rows[2] = {ra, rb};
             const bool ok[2] = {va, vb};
 #pragma unroll
@@ -393,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
                     }
                 }
             }
+            __syncwarp();
             if (lane == 0) p.counters[strip] = 0u;  // ready for the next launch
         }
     }
@@ -402,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 3) mma_kernel(MmaParams p) {
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
 
 int smem_for(int M, int slice_groups) {
-    return kRingBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 2 * (int)sizeof(float);
+    return kRingBytes + M * xstride_for(slice_groups) + 256 +
+           slice_groups * 8 * 2 * (int)sizeof(float);
 }
 
 }  // namespace
@@ -485,13 +515,25 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     p.n_strips = plan.n_strips;
     p.ctas_per_slice = plan.ctas_per_slice;
     p.xstride = xstride_for(plan.slice_groups);
-    mma_kernel<<<plan.grid, kThreads, plan.smem_bytes, stream>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the grid may start while the previous
+    // kernel in the stream drains; the kernel waits for it (griddepcontrol)
+    // before touching x, y or the workspace
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mma_kernel, p);
 }
 
 cudaError_t mma_init(const DeviceInfo &dev) {
     int dyn = smem_for(1, kMaxSliceGroups);
-    const int dyn8 = kRingBytes + kXBudget + kMaxSliceGroups * 64;
+    const int dyn8 = kRingBytes + kXBudget + 256 + kMaxSliceGroups * 64;
     if (dyn8 > dyn) dyn = dyn8;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     return cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
