@@ -183,6 +183,31 @@ def test_run_to_run_bit_identical(w4, rung):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,N,K", [(4, 34816, 5120), (4, 5120, 17408), (1, 8192, 5120)])
+def test_repeated_runs_bit_identical_and_sampled(w4, M, N, K):
+    # A race between the kernels' shared-memory reads and the asynchronous
+    # copies that refill the same buffers changes a few outputs in some runs
+    # only: launch the same linear ten times back to back (no host sync in
+    # between), then require every run to equal the first bit for bit, and
+    # the first to match the oracle on sampled rows.
+    seed = si.config_seed(54, 0, M)
+    qw, s, zw = si.layer(seed, N, K, device=DEV)
+    x_cpu = si.x(seed, M, K)
+    x = x_cpu.to(DEV)
+    outs = []
+    for _ in range(10):
+        y = torch.full((M, N), float("nan"), dtype=torch.float16, device=DEV)
+        w4.w4a16_linear(x, qw, s, zw, y=y)
+        outs.append(y)
+    torch.cuda.synchronize()
+    for i, y in enumerate(outs[1:], 1):
+        diff = int((y.view(torch.int16) != outs[0].view(torch.int16)).sum())
+        assert diff == 0, f"run {i} differs from run 0 in {diff} outputs"
+    rows = sample_rows(N, 24, seed=N + K)
+    ref = sampled_reference(seed, x_cpu, N, K, rows)
+    assert_close(outs[0][:, torch.from_numpy(rows).to(DEV)], ref, f"M={M} N={N} K={K}")
+
+
 def test_varying_sizes_back_to_back(w4):
     # Stale data between calls of different sizes shows only when sizes vary
     # (forum thread "vLLM on Hygon Z100", section 三: the all-reduce bug found

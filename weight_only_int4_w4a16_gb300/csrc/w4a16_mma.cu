@@ -26,20 +26,20 @@
 //     thousands of rows are in flight.  The 16 rows' scale and zero words of
 //     the stage follow the box (lanes copy them with cp.async); the copies and
 //     the box complete on one mbarrier per ring slot;
-//   * every warp runs its own two-slot ring: it waits for a slot, reads the
-//     whole stage into registers, refills the slot two stages ahead and then
-//     computes, so two stages per warp stay in flight;
+//   * every warp runs its own two-slot ring: it waits for a slot, computes
+//     the stage from it and then refills it two stages ahead, after a
+//     generic-to-async proxy fence (the lanes' shared-memory reads must be
+//     ordered before the TMA's writes into the same slot);
 //   * the unpack is one lop3 per pair of nibbles and adds no bias: a nibble at
 //     bits 0..3 of an fp16 half is the subnormal q * 2^-24, at bits 4..7 it is
 //     q * 2^-20, both exact.  The pairs (q0,q4) (q2,q6) of a word feed one
 //     MMA chain (D_lo, scale 2^-24) and (q1,q5) (q3,q7) another (D_hi, scale
 //     2^-20); the MMA k slots stand for k0,k4,k2,k6 and k1,k5,k3,k7, and x is
 //     staged once per CTA in the same order;
-//   * the zero point enters as one more MMA on the D_lo chain: sum_k (q - z) x
-//     = sum_k q x - z * S with S the group's sum of x, given to the MMA as an
-//     fp16 pair S_hi + S_lo (S_hi = fp16(S), S_lo = fp16(S - S_hi)) against
-//     the fp16 subnormal -z * 2^-24.  Then per group
-//         acc += s * (16 * D_lo + D_hi)
+//   * the zero point leaves the per-weight work: sum_k (q - z) x = sum_k q x
+//     - z * S with S the group's sum of x (per token, computed once per CTA
+//     when x is staged).  Per group
+//         acc += s * (16 * D_lo + D_hi - z * S * 2^-20)
 //     and y = 2^20 * acc, which is sum_g s_g * sum_k (q - z) x;
 //   * CTAs are persistent: a CTA owns one K slice, stages that slice of x
 //     once, then each warp walks its strips with one continuous copy stream;
@@ -68,6 +68,7 @@ constexpr int kMaxSliceGroups = 128;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr int kErrMmaWait = 128;  // device status bit: a ring wait expired
 constexpr float kTwo20 = 1048576.f;
+constexpr float kTwoM20 = 1.f / 1048576.f;
 
 struct MmaParams {
     const __half *x;
@@ -210,44 +211,65 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // that hold the stage's four (2-byte aligned) scales.
     int is_k = 0, is_j = 0, is_slot = 0;
     const int r = lane & 15, h = lane >> 4;
+    // this lane's copy sources in the issue cursor's strip, set on entering it
+    int is_row16 = 0;    // first row of the strip
+    uintptr_t is_s = 0;  // next scale word to copy (h = 0: it and the next; h = 1: word 2)
+    int is_avail = 0;    // bytes from is_s to the end of the scales array (0 past row N)
+    uintptr_t is_z = 0;  // zeros word of the next stage
+    uint32_t is_zbytes = 0;
+    auto enter_strip = [&]() {
+        is_row16 = (first + is_k * stride) * 16;
+        const int row = is_row16 + r;
+        const bool vr = row < p.N;
+        const size_t rr = (size_t)(vr ? row : 0);
+        is_s = (((uintptr_t)(p.scales + rr * p.G + g0)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
+        const uintptr_t rem = is_s < p.scales_end ? p.scales_end - is_s : 0;
+        is_avail = vr ? (int)(rem > (1u << 30) ? (1u << 30) : rem) : 0;
+        is_z = (uintptr_t)(p.zeros + rr * p.ZW + (g0 >> 3));
+        is_zbytes = vr ? 4u : 0u;
+    };
+    if (my_strips > 0) enter_strip();
     auto issue_next = [&]() {
         if (is_k >= my_strips) return;
-        const int strip = first + is_k * stride;
-        const int grp = g0 + is_j * kStageGroups;
         const uint32_t bar = bar0 + 8 * is_slot;
         const uint32_t dst = ring0 + is_slot * kStageBytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, kStageW);
-            tma_box(dst, &tmap, strip * 16, grp, bar);
+            tma_box(dst, &tmap, is_row16, g0 + is_j * kStageGroups, bar);
         }
-        const int row = strip * 16 + r;
-        const bool vr = row < p.N;
-        const size_t rr = (size_t)(vr ? row : 0);
+        // a scale word copies the part of it inside the array; a word past
+        // the end, or of a row past N, becomes zeros, reads nothing and takes
+        // the array's first word as its (valid) source address
         const uint32_t md = dst + kStageW + r * 16 + 8 * h;
-        const uintptr_t sa =
-            (((uintptr_t)(p.scales + rr * p.G + grp)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
-        // copy the part of the word at a that lies inside the scales array
-        // (a word past the end, or of a row past N, becomes zeros and reads
-        // nothing; its source address is then the array's first word)
-        auto copy_scale_word = [&](uint32_t d, uintptr_t a) {
-            const uint32_t n = !vr || a >= p.scales_end
-                                   ? 0u
-                                   : (p.scales_end - a >= 4 ? 4u : (uint32_t)(p.scales_end - a));
-            cp4(d, n ? a : p.scales_first, n);
-        };
-        copy_scale_word(md, sa);
-        if (h == 0)
-            copy_scale_word(md + 4, sa + 4);
-        else
-            cp4(md + 4, (uintptr_t)(p.zeros + rr * p.ZW + (grp >> 3)), vr ? 4u : 0u);
+        const int n0 = min(max(is_avail, 0), 4);
+        cp4(md, n0 ? is_s : p.scales_first, (uint32_t)n0);
+        if (h == 0) {
+            const int n1 = min(max(is_avail - 4, 0), 4);
+            cp4(md + 4, n1 ? is_s + 4 : p.scales_first, (uint32_t)n1);
+        } else {
+            cp4(md + 4, is_z, is_zbytes);
+        }
         cp_arrive_noinc(bar);
         is_slot ^= 1;  // kDepth == 2
+        is_s += 8;
+        is_avail -= 8;
+        // stage j covers groups g0 + 4j .. g0 + 4j + 3: a new zeros word
+        // starts with every second stage
+        if (((g0 + (is_j + 1) * kStageGroups) & 7) == 0) is_z += 4;
         if (++is_j == nst) {
             is_j = 0;
-            ++is_k;
+            if (++is_k < my_strips) enter_strip();
         }
     };
     static_assert(kDepth == 2, "the slot and phase updates assume two slots");
+    // Ask L2 for this slice of x first: the staging loads below then hit L2
+    // instead of queueing behind the weight stream.  A prefetch changes no
+    // value a later load returns, so it may run before the dependency wait.
+    if (warp == 0 && lane < p.M)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         p.x + (size_t)lane * p.K + (size_t)g0 * kGroup),
+                     "r"(ng * kGroup * 2)
+                     : "memory");
 #pragma unroll
     for (int s = 0; s < kDepth; ++s) issue_next();
 
@@ -256,38 +278,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     grid_dependency_wait();
 
     // ---- stage x[:, slice] in MMA pair order, and each (group, token)'s sum
-    // of x as an fp16 pair (S_hi, S_lo): the 16 lanes of a half warp hold the
-    // 16 units of one group of one token and add theirs with shuffles
+    // S of x (kept as S * 2^-20): the 16 lanes of a half warp hold the 16 units
+    // of one group of one token and add theirs with shuffles
     const int M = p.M;
-    uint32_t *sums = reinterpret_cast<uint32_t *>(xs + (size_t)M * p.xstride);  // [group][8]
+    float *sums = reinterpret_cast<float *>(xs + (size_t)M * p.xstride);  // [group][8] S * 2^-20
     {
+        // kXBatch loads in flight per thread: the staging costs two or three
+        // L2 round trips instead of one per unit
+        constexpr int kXBatch = 8;
         const int nunits = ng * (kGroup / 8);
         const int xtotal = M * nunits;  // a multiple of 16
         const int k0 = g0 * kGroup;
-        for (int base = warp * 32; base < xtotal; base += kThreads) {
-            const int i = base + lane;
-            const bool valid = i < xtotal;
-            const int t = i / nunits, J = i - t * nunits;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (valid) {
-                v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
-                *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
-                    mma_pair_order(v);
-            }
-            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-            const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
-            float sum = ((a.x + a.y) + (b.x + b.y)) + ((e.x + e.y) + (f.x + f.y));
+        for (int base = warp * 32; base < xtotal; base += kThreads * kXBatch) {
+            uint4 v[kXBatch];
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            if (valid && (J & 15) == 0) {
-                const __half hi = __float2half_rn(sum);
-                const __half lo = __float2half_rn(sum - __half2float(hi));
-                sums[(J >> 4) * 8 + t] = (uint32_t)__half_as_ushort(hi) |
-                                         ((uint32_t)__half_as_ushort(lo) << 16);
+            for (int b = 0; b < kXBatch; ++b) {
+                const int i = base + b * kThreads + lane;
+                v[b] = make_uint4(0, 0, 0, 0);
+                if (i < xtotal) {
+                    const int t = i / nunits, J = i - t * nunits;
+                    v[b] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kXBatch; ++b) {
+                const int i = base + b * kThreads + lane;
+                const bool valid = i < xtotal;
+                const int t = i / nunits, J = i - t * nunits;
+                if (valid)
+                    *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
+                        mma_pair_order(v[b]);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].x));
+                const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].y));
+                const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].z));
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].w));
+                float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if (valid && (J & 15) == 0) sums[(J >> 4) * 8 + t] = sum * kTwoM20;
             }
         }
+        // tokens M..7 have no x: their sums are zero
+        for (int i = threadIdx.x; i < ng * (8 - M); i += kThreads)
+            sums[(i / (8 - M)) * 8 + M + i % (8 - M)] = 0.f;
     }
     __syncthreads();
 
@@ -297,9 +330,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // unit of word u of this lane's chunk in a group: x_unit(4c + u)
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
-    // -z * 2^-24 as an fp16 pair sits in k slots 0 and 1: lanes c == 0 only
-    const uint32_t zmul = c == 0 ? 0x00010001u : 0u;
-    const uint32_t zbase = c == 0 ? 0x80008000u : 0u;
     int cs_slot = 0;
     uint32_t cs_par = 0;
 
@@ -322,21 +352,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 cp_wait_all();
                 return;
             }
-            // the whole stage into registers: this lane's 16 bytes of rows g
-            // and g + 8 of each group, and the metadata of both rows
+            // this lane's part of the stage: 16 bytes of rows g and g + 8 of
+            // each group (read just before the group), the metadata of both rows
             const uint8_t *st = wring + cs_slot * kStageBytes;
-            uint4 wa[kStageGroups], wb[kStageGroups];
-#pragma unroll
-            for (int i = 0; i < kStageGroups; ++i) {
-                wa[i] = *reinterpret_cast<const uint4 *>(st + i * 1024 + g * 64 + 16 * c);
-                wb[i] = *reinterpret_cast<const uint4 *>(st + i * 1024 + (g + 8) * 64 + 16 * c);
-            }
+            const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
             const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
             const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
-            __syncwarp();  // every lane has read the slot: refill it
-            issue_next();
-            cs_slot ^= 1;
-            if (cs_slot == 0) cs_par ^= 1;
 
             // zero nibbles of the stage's groups: the stage starts at group
             // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
@@ -345,48 +366,66 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint32_t mA[3] = {ma.x, ma.y, ma.z}, mB[3] = {mb.x, mb.y, mb.z};
             const int n_in = min(kStageGroups, ng - j * kStageGroups);
             const uint8_t *xg = xrow + (size_t)j * (kStageGroups * 256);
-            const uint32_t *sg = sums + (j * kStageGroups) * 8 + tok;
-#pragma unroll
-            for (int i = 0; i < kStageGroups; ++i) {
-                if (i < n_in) {
-                    // scales of rows ra and rb: half (off + i) of the words
-                    uint32_t hA, hB;
-                    if (i & 1) {
-                        hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
-                        hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
-                    } else {
-                        hA = mA[i >> 1] >> shA;
-                        hB = mB[i >> 1] >> shB;
-                    }
-                    const float sA = __half2float(__ushort_as_half((unsigned short)hA));
-                    const float sB = __half2float(__ushort_as_half((unsigned short)hB));
-                    const uint32_t cA = ((zwA >> (4 * i)) & 0xfu) * zmul + zbase;
-                    const uint32_t cB = ((zwB >> (4 * i)) & 0xfu) * zmul + zbase;
-                    const uint32_t sx = sg[i * 8];  // (S_hi, S_lo) of token tok
-                    const uint8_t *xi = xg + i * 256;
-                    uint4 xv[4];
-                    xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
-                    xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
-                    xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
-                    xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
-                    const uint32_t wA[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
-                    const uint32_t wB[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
-                    float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma16816(dl, cA, cB, 0u, 0u, sx, sx);  // - z * S
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t a = wA[u], b = wB[u], a8 = a >> 8, b8 = b >> 8;
-                        mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
-                                 b8 & 0x000f000fu, xv[u].x, xv[u].y);
-                        mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
-                                 b8 & 0x00f000f0u, xv[u].z, xv[u].w);
-                    }
-                    acc[0] = fmaf(sA, fmaf(16.f, dl[0], dh[0]), acc[0]);
-                    acc[1] = fmaf(sA, fmaf(16.f, dl[1], dh[1]), acc[1]);
-                    acc[2] = fmaf(sB, fmaf(16.f, dl[2], dh[2]), acc[2]);
-                    acc[3] = fmaf(sB, fmaf(16.f, dl[3], dh[3]), acc[3]);
+            const float *sg = sums + (j * kStageGroups) * 8 + 2 * c;  // tokens 2c, 2c+1
+            // one group of the stage
+            auto group = [&](const int i) {
+                // scales of rows ra and rb: half (off + i) of the words
+                uint32_t hA, hB;
+                if (i & 1) {
+                    hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
+                    hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
+                } else {
+                    hA = mA[i >> 1] >> shA;
+                    hB = mB[i >> 1] >> shB;
                 }
+                const float sA = __half2float(__ushort_as_half((unsigned short)hA));
+                const float sB = __half2float(__ushort_as_half((unsigned short)hB));
+                // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
+                const float zA = __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
+                const float zB = __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
+                const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);  // S * 2^-20
+                const uint8_t *xi = xg + i * 256;
+                uint4 xv[4];
+                xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
+                xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
+                xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
+                xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
+                const uint4 wa = *reinterpret_cast<const uint4 *>(stA + i * 1024);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(stB + i * 1024);
+                const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+                const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+                float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t a = wA[u], b = wB[u], a8 = a >> 8, b8 = b >> 8;
+                    mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
+                             b8 & 0x000f000fu, xv[u].x, xv[u].y);
+                    mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
+                             b8 & 0x00f000f0u, xv[u].z, xv[u].w);
+                }
+                // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
+                acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
+                acc[1] = fmaf(sA, fmaf(-zA, sx.y, fmaf(16.f, dl[1], dh[1])), acc[1]);
+                acc[2] = fmaf(sB, fmaf(-zB, sx.x, fmaf(16.f, dl[2], dh[2])), acc[2]);
+                acc[3] = fmaf(sB, fmaf(-zB, sx.y, fmaf(16.f, dl[3], dh[3])), acc[3]);
+            };
+            if (n_in == kStageGroups) {
+#pragma unroll
+                for (int i = 0; i < kStageGroups; ++i) group(i);
+            } else {  // the last stage of a slice that ends at K
+#pragma unroll
+                for (int i = 0; i < kStageGroups; ++i)
+                    if (i < n_in) group(i);
             }
+            // Refill the slot kDepth stages ahead once every lane is done with
+            // it.  The lanes read it through the generic proxy and the box
+            // lands through the async proxy: the proxy fence orders those
+            // reads before the new box's writes.
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_next();
+            cs_slot ^= 1;
+            if (cs_slot == 0) cs_par ^= 1;
         }
 
         // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
