@@ -388,7 +388,7 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    probe0 = w4.w4a16_probe_counts()
+    launches0 = w4.w4a16_kernel_launches()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -396,14 +396,14 @@ def main():
         w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
     ev1.record(stream)
     torch.cuda.synchronize()
-    probe1 = w4.w4a16_probe_counts()
+    launches1 = w4.w4a16_kernel_launches()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     clk = clocks.stop()
     if world > 1:
         t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed = float(t.item())
-    launches = int(sum(probe1) - sum(probe0))
+    launches = int(launches1 - launches0)
 
     rb = round_bytes(layers=args.layers)
     value = rb * args.steps * world / elapsed / 1e9
@@ -411,16 +411,34 @@ def main():
     peak, peak_kind = load_peaks()
 
     # ---- dominant kernel, timed launch by launch on the same stream ---------
-    stats = per_kernel_durations(w4, lin, max(2, min(args.steps, 4)), stream)
-    top = max(stats, key=lambda r: stats[r][1])
-    n_l, t_l, b_l = stats[top]
-    achieved = (b_l / n_l) / (t_l / n_l) / 1e9
-    roofline = {"bound": "hbm", "kernel": f"gemv_kernel rung={w4.rung_name(top)}",
+    # A round of mma-rung linears is one launch of the fused round kernel:
+    # CUDA events around each launch on the launching stream.
+    per_round = launches // max(1, args.steps)
+    n_l = max(3, min(args.steps, 8))
+    evs = []
+    for _ in range(n_l):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    t_l = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    achieved = rb / (t_l / n_l) / 1e9
+    roofline = {"bound": "hbm",
+                "kernel": ("mma_kernel (fused decode round, one launch per round)"
+                           if per_round == 1 else f"decode round ({per_round} launches)"),
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
                 "traffic": None, "launches_timed": n_l,
                 "mean_launch_us": t_l / n_l * 1e6,
-                "mean_algorithmic_bytes_per_launch": b_l / n_l}
+                "mean_algorithmic_bytes_per_launch": rb}
+    # each linear launched alone (its own kernel), for the per-shape picture
+    stats = per_kernel_durations(w4, lin, 2, stream)
+    per_linear = {w4.rung_name(r): {"launches": n, "mean_us": t / n * 1e6,
+                                    "GBps": by / t / 1e9}
+                  for r, (n, t, by) in stats.items()}
 
     # ---- end to end through the C ABI with host buffers ----------------------
     e2e_s, h2d, d2h = time_e2e(w4, lin, xs, max(3, args.steps // 2), 2, stream)
@@ -445,7 +463,8 @@ def main():
     g.destroy()
 
     extra = {"round_graph_ms": graph_ms, "round_graph_GBps": rb / (graph_ms / 1e3) / 1e9,
-             "round_bytes": rb, "launches_per_round": launches // max(1, args.steps),
+             "round_bytes": rb, "launches_per_round": per_round,
+             "linears_launched_alone": per_linear,
              "rung_per_shape": {n: w4.rung_name(w4.w4a16_select_rung(M_ROUND, N, K))
                                 for n, K, N in ROUND_SHAPES}}
     del lin, descs

@@ -166,10 +166,15 @@ int w4a16_select_rung(int M, int N, int K, int group);
  * graphs captured earlier keep their rungs. */
 int w4a16_set_forced_rung(int rung);
 
-/* Copy min(n, W4A16_NUM_RUNGS) per-rung launch counts into counts (host);
- * returns the number written.  Counts are host-side dispatch decisions (a
- * graph replay does not re-count). */
+/* Copy min(n, W4A16_NUM_RUNGS) per-rung counts into counts (host); returns
+ * the number written.  A rung's count grows by one for every linear (every
+ * tile of up to its token limit) it computes: a fused decode round counts each
+ * of its linears under the rung that computes it.  Counts are host-side
+ * dispatch decisions (a graph replay does not re-count). */
 int w4a16_probe_counts(uint64_t *counts, int n);
+/* Kernels this library has launched (host count, all entry points, since the
+ * last w4a16_probe_reset; a graph replay does not re-count). */
+uint64_t w4a16_kernel_launches(void);
 void w4a16_probe_reset(void);
 
 /* Static strings; "?" for unknown values. */

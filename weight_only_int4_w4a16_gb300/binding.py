@@ -76,6 +76,7 @@ _sig("w4a16_select_rung", [_I, _I, _I, _I])
 _sig("w4a16_set_forced_rung", [_I])
 _sig("w4a16_probe_counts", [ctypes.POINTER(ctypes.c_uint64), _I])
 _sig("w4a16_probe_reset", [], None)
+_sig("w4a16_kernel_launches", [], ctypes.c_uint64)
 _sig("w4a16_rung_name", [_I], ctypes.c_char_p)
 _sig("w4a16_status_string", [_I], ctypes.c_char_p)
 _sig("w4a16_device_status", [_P, ctypes.POINTER(_I)])
@@ -86,7 +87,7 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
-            "w4a16_probe_reset", "w4a16_rung_name", "w4a16_status_string",
+            "w4a16_probe_reset", "w4a16_kernel_launches", "w4a16_rung_name", "w4a16_status_string",
             "w4a16_device_status", "w4a16_last_cuda_error", "w4a16_device_sm_count"]
 
 
@@ -250,6 +251,10 @@ def w4a16_probe_counts() -> list[int]:
 
 def w4a16_probe_reset() -> None:
     lib.w4a16_probe_reset()
+
+
+def w4a16_kernel_launches() -> int:
+    return int(lib.w4a16_kernel_launches())
 
 
 def w4a16_device_status(stream=None) -> int:

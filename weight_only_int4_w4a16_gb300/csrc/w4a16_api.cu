@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/w4a16.h"
 #include "w4a16_internal.h"
@@ -25,6 +26,8 @@ struct State {
     DeviceInfo dev{};
     Workspace ws{};
     void *ws_base = nullptr;
+    MmaLinDesc *round_descs = nullptr;     // device copy of the last fused round's descriptors
+    std::vector<MmaLinDesc> round_uploaded;  // what that copy holds
     int forced_rung = W4A16_RUNG_AUTO;
     bool log = false;
 };
@@ -32,10 +35,12 @@ struct State {
 State g_state;
 std::mutex g_mutex;
 std::atomic<unsigned long long> g_probe[W4A16_NUM_RUNGS];
+std::atomic<unsigned long long> g_launches{0};
 thread_local int t_last_cuda_error = 0;
 
 constexpr size_t kDefaultWorkspace = 64ull << 20;
-constexpr int kCounters = 1 << 16;
+constexpr int kCounters = 1 << 20;       // split-K arrival counters (and round completion counters)
+constexpr int kMaxRoundLinears = 4096;   // linears of one fused decode round
 constexpr int kMaxM = 65535;
 
 const char *const kRungNames[W4A16_NUM_RUNGS] = {"gemv", "gemv_splitk", "tc",
@@ -203,6 +208,7 @@ int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t s
             e = launch_gemv(t, p, st.ws, stream);
         }
         g_probe[rung].fetch_add(1, std::memory_order_relaxed);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
     }
     if (st.log)
         fprintf(stderr, "[w4a16] linear M=%d N=%d K=%d -> %s\n", a.M, a.N, a.K, kRungNames[rung]);
@@ -239,6 +245,111 @@ int linear_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
     return launch_linear(a, d.rung, s, (cudaStream_t)stream);
 }
 
+// ---- fused decode rounds ----------------------------------------------------
+// A round whose linears all take the mma rungs (auto dispatch, M <= 8) runs as
+// one launch of the mma kernel over the units of all its linears.  Each
+// linear gets its own slices of the split-K workspace, so linears in flight
+// at the same time never share partials or counters.  A linear that reads
+// what an earlier one writes, writes what an earlier one reads, or writes
+// what an earlier one writes waits (on per-linear completion counters) for
+// the latest such linear to finish: the results are those of running the
+// linears one after another.
+struct FusedRound {
+    std::vector<MmaLinDesc> descs;
+    MmaRound round{};
+    int counters_used = 0;  // split-K counters, then n + 1 completion counters if waits exist
+};
+
+size_t bytes_of(int rows, int cols) { return (size_t)rows * cols * 2; }
+
+// OK, UNSUPPORTED (the round is not eligible: launch linear by linear), or an error.
+int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &st,
+                     FusedRound *fr) {
+    if (st.forced_rung != W4A16_RUNG_AUTO || M > kMmaMaxTokens || n > kMaxRoundLinears)
+        return W4A16_ERR_UNSUPPORTED;
+    fr->descs.resize(n);
+    size_t partial_floats = 0;
+    int counters = 0, units = 0, smem = 0;
+    bool waits = false;
+    for (int l = 0; l < n; ++l) {
+        const w4a16_linear_desc &d = descs[l];
+        MmaPlan p = plan_mma(M, d.N, d.K, 2, st.dev);
+        if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+        float *part = nullptr;
+        unsigned *cnt = nullptr;
+        if (p.S > 1) {
+            part = st.ws.partials + partial_floats;
+            partial_floats += ((size_t)p.S * M * d.N + 63) / 64 * 64;
+            cnt = st.ws.counters + counters;
+            counters += p.n_strips;
+        }
+        int wait_for = -1;
+        for (int j = l - 1; j >= 0 && wait_for < 0; --j) {
+            const w4a16_linear_desc &e = descs[j];
+            if (overlaps(e.y, bytes_of(M, e.N), d.x, bytes_of(M, d.K)) ||
+                overlaps(e.x, bytes_of(M, e.K), d.y, bytes_of(M, d.N)) ||
+                overlaps(e.y, bytes_of(M, e.N), d.y, bytes_of(M, d.N)))
+                wait_for = j;
+        }
+        waits |= wait_for >= 0;
+        LinearArgs a{reinterpret_cast<const __half *>(d.x), d.qweight,
+                     reinterpret_cast<const __half *>(d.scales), d.zeros,
+                     reinterpret_cast<__half *>(d.y), M, d.N, d.K};
+        cudaError_t e = mma_describe(a, p, part, cnt, units, wait_for, &fr->descs[l]);
+        if (e != cudaSuccess) return cuda_fail(e);
+        units += p.units;
+        if (p.smem_bytes > smem) smem = p.smem_bytes;
+    }
+    if (partial_floats * sizeof(float) > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
+    if (counters + (waits ? n + 1 : 0) > st.ws.n_counters) return W4A16_ERR_WORKSPACE;
+    fr->round.n = n;
+    fr->round.total_units = units;
+    fr->round.smem_bytes = smem;
+    fr->round.done = waits ? st.ws.counters + counters : nullptr;
+    fr->counters_used = counters + (waits ? n + 1 : 0);
+    return W4A16_OK;
+}
+
+void count_fused_probes(const FusedRound &fr) {
+    for (const MmaLinDesc &d : fr.descs)
+        g_probe[d.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA].fetch_add(
+            1, std::memory_order_relaxed);
+}
+
+int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
+    if (!descs || n_descs < 1) return W4A16_ERR_INVALID_ARG;
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y);
+        if (st) return st;
+    }
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    return W4A16_OK;
+}
+
+// Linear by linear (rounds the fused kernel does not take).
+int round_per_linear(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung);
+        if (dec.status) return dec.status;
+        int st = check_workspace(dec.rung, M, d.N, d.K, g_state);
+        if (st) return st;
+    }
+    for (int i = 0; i < n_descs; ++i) {
+        const w4a16_linear_desc &d = descs[i];
+        int st = linear_impl(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y, stream,
+                             true);
+        if (st) return st;
+    }
+    return W4A16_OK;
+}
+
+struct RoundGraphHandle {
+    cudaGraphExec_t exec = nullptr;
+    void *buffer = nullptr;  // the fused round's descriptors and completion counters
+};
+
 }  // namespace
 
 extern "C" {
@@ -262,10 +373,12 @@ int w4a16_init(int device, size_t workspace_bytes) {
     if (e != cudaSuccess) return cuda_fail(e);
     if (workspace_bytes == 0) workspace_bytes = kDefaultWorkspace;
     workspace_bytes = (workspace_bytes + 255) & ~(size_t)255;
-    // counters, then one status word (kept 256-byte aligned)
+    // counters, then one status word (kept 256-byte aligned), then the fused
+    // round descriptors
     const size_t counter_bytes = (size_t)kCounters * sizeof(unsigned) + 256;
+    const size_t desc_bytes = (size_t)kMaxRoundLinears * sizeof(MmaLinDesc);
     void *base = nullptr;
-    e = cudaMalloc(&base, workspace_bytes + counter_bytes);
+    e = cudaMalloc(&base, workspace_bytes + counter_bytes + desc_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaMemset((char *)base + workspace_bytes, 0, counter_bytes);
     if (e == cudaSuccess) e = gemv_init_attributes(dev);
@@ -283,6 +396,8 @@ int w4a16_init(int device, size_t workspace_bytes) {
     s.ws.counters = (unsigned *)((char *)base + workspace_bytes);
     s.ws.n_counters = kCounters;
     s.ws.status = (int *)((char *)base + workspace_bytes + (size_t)kCounters * sizeof(unsigned));
+    s.round_descs = (MmaLinDesc *)((char *)base + workspace_bytes + counter_bytes);
+    s.round_uploaded.clear();
     s.forced_rung = parse_rung(getenv("W4A16_FORCE_RUNG"));
     const char *lg = getenv("W4A16_LOG");
     s.log = lg && *lg && strcmp(lg, "0") != 0;
@@ -321,6 +436,7 @@ int w4a16_pack(const uint8_t *q, const uint8_t *z, int N, int K, int group, uint
     if (!aligned(q, 16) || !aligned(qweight, 16) || !aligned(z, 4) || !aligned(zeros, 4))
         return W4A16_ERR_MISALIGNED;
     cudaError_t e = launch_pack(q, z, N, K, qweight, zeros, (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -332,6 +448,7 @@ int w4a16_unpack(const uint32_t *qweight, const uint32_t *zeros, int N, int K, i
     if (!aligned(q, 16) || !aligned(qweight, 16) || !aligned(z, 4) || !aligned(zeros, 4))
         return W4A16_ERR_MISALIGNED;
     cudaError_t e = launch_unpack(qweight, zeros, N, K, q, z, (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -343,6 +460,7 @@ int w4a16_dequant(const uint32_t *qweight, const uint16_t *scales, const uint32_
     if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(zeros, 4) ||
         (w_f32 && !aligned(w_f32, 16)) || (w_f16 && !aligned(w_f16, 16)))
         return W4A16_ERR_MISALIGNED;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = launch_dequant(qweight, reinterpret_cast<const __half *>(scales), zeros, N, K,
                                    w_f32, reinterpret_cast<__half *>(w_f16), (cudaStream_t)stream);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
@@ -355,68 +473,108 @@ int w4a16_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *sca
 }
 
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {
-    if (!descs || n_descs < 1) return W4A16_ERR_INVALID_ARG;
-    for (int i = 0; i < n_descs; ++i) {
-        const w4a16_linear_desc &d = descs[i];
-        int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y);
-        if (st) return st;
+    int st = validate_round(descs, n_descs, M);
+    if (st) return st;
+    State &s = g_state;
+    FusedRound fr;
+    st = plan_fused_round(descs, n_descs, M, s, &fr);
+    if (st == W4A16_ERR_UNSUPPORTED) return round_per_linear(descs, n_descs, M, stream);
+    if (st) return st;
+    // upload the descriptors unless the device copy already holds these
+    // (the copy is ordered on the stream after earlier rounds that read it)
+    const size_t bytes = fr.descs.size() * sizeof(MmaLinDesc);
+    if (s.round_uploaded.size() != fr.descs.size() ||
+        memcmp(s.round_uploaded.data(), fr.descs.data(), bytes) != 0) {
+        cudaError_t e = cudaMemcpyAsync(s.round_descs, fr.descs.data(), bytes,
+                                        cudaMemcpyHostToDevice, (cudaStream_t)stream);
+        if (e != cudaSuccess) {
+            s.round_uploaded.clear();
+            return cuda_fail(e);
+        }
+        s.round_uploaded = fr.descs;
     }
-    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    for (int i = 0; i < n_descs; ++i) {
-        const w4a16_linear_desc &d = descs[i];
-        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung);
-        if (dec.status) return dec.status;
-        int st = check_workspace(dec.rung, M, d.N, d.K, g_state);
-        if (st) return st;
-    }
-    for (int i = 0; i < n_descs; ++i) {
-        const w4a16_linear_desc &d = descs[i];
-        int st = linear_impl(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y, stream,
-                             true);
-        if (st) return st;
-    }
-    return W4A16_OK;
+    fr.round.descs = s.round_descs;
+    cudaError_t e = launch_mma_round(fr.round, s.ws, s.dev, (cudaStream_t)stream);
+    count_fused_probes(fr);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (s.log)
+        fprintf(stderr, "[w4a16] decode round of %d linears M=%d -> fused mma, %d units%s\n",
+                n_descs, M, fr.round.total_units, fr.round.done ? ", with waits" : "");
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
 int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M, void **graph) {
     if (!graph) return W4A16_ERR_INVALID_ARG;
     *graph = nullptr;
-    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    cudaStream_t s = nullptr;
-    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return cuda_fail(e);
-    e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    int st = validate_round(descs, n_descs, M);
+    if (st) return st;
+    State &s = g_state;
+    FusedRound fr;
+    st = plan_fused_round(descs, n_descs, M, s, &fr);
+    const bool fused = st == W4A16_OK;
+    if (st && st != W4A16_ERR_UNSUPPORTED) return st;
+    RoundGraphHandle *hd = new RoundGraphHandle();
+    cudaError_t e = cudaSuccess;
+    if (fused) {
+        // the graph owns its descriptors and completion counters
+        const size_t dbytes = fr.descs.size() * sizeof(MmaLinDesc);
+        const size_t cbytes = fr.round.done ? (size_t)(n_descs + 1) * sizeof(unsigned) : 0;
+        e = cudaMalloc(&hd->buffer, dbytes + cbytes);
+        if (e == cudaSuccess)
+            e = cudaMemcpy(hd->buffer, fr.descs.data(), dbytes, cudaMemcpyHostToDevice);
+        if (e == cudaSuccess && cbytes) e = cudaMemset((char *)hd->buffer + dbytes, 0, cbytes);
+        fr.round.descs = (const MmaLinDesc *)hd->buffer;
+        if (fr.round.done) fr.round.done = (unsigned *)((char *)hd->buffer + dbytes);
+    }
+    cudaStream_t cs = nullptr;
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) {
-        cudaStreamDestroy(s);
+        if (cs) cudaStreamDestroy(cs);
+        if (hd->buffer) cudaFree(hd->buffer);
+        delete hd;
         return cuda_fail(e);
     }
-    int st = w4a16_decode_round(descs, n_descs, M, s);
+    if (fused) {
+        cudaError_t le = launch_mma_round(fr.round, s.ws, s.dev, cs);
+        st = le == cudaSuccess ? W4A16_OK : cuda_fail(le);
+        if (!st) count_fused_probes(fr);
+    } else {
+        st = round_per_linear(descs, n_descs, M, cs);
+    }
     cudaGraph_t g = nullptr;
-    e = cudaStreamEndCapture(s, &g);
-    cudaStreamDestroy(s);
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (!st && e != cudaSuccess) st = cuda_fail(e);
+    if (!st) {
+        e = cudaGraphInstantiate(&hd->exec, g, 0);
+        if (e != cudaSuccess) st = cuda_fail(e);
+    }
+    if (g) cudaGraphDestroy(g);
     if (st) {
-        if (g) cudaGraphDestroy(g);
+        if (hd->buffer) cudaFree(hd->buffer);
+        delete hd;
         return st;
     }
-    if (e != cudaSuccess) return cuda_fail(e);
-    cudaGraphExec_t exec = nullptr;
-    e = cudaGraphInstantiate(&exec, g, 0);
-    cudaGraphDestroy(g);
-    if (e != cudaSuccess) return cuda_fail(e);
-    *graph = (void *)exec;
+    *graph = (void *)hd;
     return W4A16_OK;
 }
 
 int w4a16_round_graph_launch(void *graph, void *stream) {
     if (!graph) return W4A16_ERR_INVALID_ARG;
-    cudaError_t e = cudaGraphLaunch((cudaGraphExec_t)graph, (cudaStream_t)stream);
+    RoundGraphHandle *hd = (RoundGraphHandle *)graph;
+    cudaError_t e = cudaGraphLaunch(hd->exec, (cudaStream_t)stream);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
 int w4a16_round_graph_destroy(void *graph) {
     if (!graph) return W4A16_ERR_INVALID_ARG;
-    cudaError_t e = cudaGraphExecDestroy((cudaGraphExec_t)graph);
-    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+    RoundGraphHandle *hd = (RoundGraphHandle *)graph;
+    cudaError_t e = cudaGraphExecDestroy(hd->exec);
+    cudaError_t f = hd->buffer ? cudaFree(hd->buffer) : cudaSuccess;
+    delete hd;
+    if (e != cudaSuccess) return cuda_fail(e);
+    return f == cudaSuccess ? W4A16_OK : cuda_fail(f);
 }
 
 int w4a16_select_rung(int M, int N, int K, int group) {
@@ -442,8 +600,11 @@ int w4a16_probe_counts(uint64_t *counts, int n) {
     return k;
 }
 
+uint64_t w4a16_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
 void w4a16_probe_reset(void) {
     for (auto &c : g_probe) c.store(0, std::memory_order_relaxed);
+    g_launches.store(0, std::memory_order_relaxed);
 }
 
 const char *w4a16_rung_name(int rung) {

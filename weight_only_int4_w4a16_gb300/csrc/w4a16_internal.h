@@ -2,6 +2,7 @@
 // Nothing here is exported from the shared library.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -83,21 +84,61 @@ cudaError_t tc_init(const DeviceInfo &dev);
 // ---- warp-level tensor-core MMA rungs (w4a16_mma.cu) ----------------------
 constexpr int kMmaMaxTokens = 8;  // tokens per launch (the MMA's N = 8)
 
+// The work of one linear is cut into units: one K slice of 8 strips of 16
+// rows (one strip per warp of a CTA).  CTAs take units round-robin.
 struct MmaPlan {
     bool ok;
     int M;             // tokens (1..8)
     int S;             // K slices
-    int slice_groups;  // groups per slice
-    int n_strips;      // 16-row strips (one warp's unit of work)
-    int ctas_per_slice;  // persistent CTAs working on each slice
-    int grid;          // ctas_per_slice * S
-    int smem_bytes;    // copy ring + staged activations
+    int slice_groups;  // groups per slice (a multiple of 4; the last slice may hold fewer)
+    int n_strips;      // 16-row strips
+    int n_blocks;      // units per slice: ceil(n_strips / 8)
+    int units;         // S * n_blocks
+    int grid;          // CTAs of a launch of this linear alone
+    int smem_bytes;    // dynamic shared memory of such a launch
     size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
 };
 
+// One linear as the kernel reads it: in the kernel's parameters for a launch
+// of one linear, in device memory for a fused round.
+struct MmaLinDesc {
+    CUtensorMap tmap;  // qweight as a 3-D tensor: (word in group, row, group)
+    const __half *x;
+    const __half *scales;
+    const uint32_t *zeros;
+    __half *y;
+    float *partials;      // this linear's split-K partials (S > 1)
+    unsigned *counters;   // this linear's per-strip arrival counters (S > 1)
+    uintptr_t scales_first;  // the aligned word holding the first scale
+    uintptr_t scales_end;    // one past the last byte of the scales array
+    int N, K, G, ZW, M, S, slice_groups, n_strips, n_blocks;
+    int unit_start;  // index of the linear's first unit in the fused list
+    int xstride;     // bytes per staged token row
+    int wait_for;    // fused round: linear that must be complete before this one reads x (-1: none)
+};
+
+// split: 0 = never split K, 1 = split K, -1 = planner balances the warps,
+// 2 = fewest slices the staged activations allow (fused rounds).
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev);
+cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
+                         unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
                        cudaStream_t stream);
+
+// A fused round: n linears in one launch, their units in order.  done points
+// at n + 1 zeroed counters when some linear waits for another (else null);
+// the kernel leaves them zeroed again.
+struct MmaRound {
+    const MmaLinDesc *descs;  // device array of n descriptors
+    int n;
+    int total_units;
+    int smem_bytes;
+    unsigned *done;
+};
+int mma_round_grid(const DeviceInfo &dev);
+int mma_smem_bytes(int M, int slice_groups);
+cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const DeviceInfo &dev,
+                             cudaStream_t stream);
 cudaError_t mma_init(const DeviceInfo &dev);
 
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------

@@ -41,11 +41,19 @@
 //     when x is staged).  Per group
 //         acc += s * (16 * D_lo + D_hi - z * S * 2^-20)
 //     and y = 2^20 * acc, which is sum_g s_g * sum_k (q - z) x;
-//   * CTAs are persistent: a CTA owns one K slice, stages that slice of x
-//     once, then each warp walks its strips with one continuous copy stream;
+//   * work comes in units: one K slice of 8 strips, a strip per warp.  CTAs
+//     are persistent and take units round-robin; per unit a CTA stages that
+//     slice of x (with each group's sums of x) and its warps stream their
+//     strips, while each warp's copy stream already runs ahead into its next
+//     unit;
+//   * a fused decode round is one launch over the units of all its linears
+//     in order: the weight stream does not stop between linears.  Where a
+//     linear reads activations an earlier one writes (or the like), it waits
+//     on per-linear completion counters before staging them;
 //   * split K: fp32 partials and a last-arriving-warp reduction in slice
 //     order (deterministic, no warp waits for another).
 #include <cuda.h>
+#include <string.h>
 
 #include "w4a16_device.cuh"
 #include "w4a16_internal.h"
@@ -62,30 +70,14 @@ constexpr int kStageW = kStageGroups * 16 * 64;  // 4 KB of weights
 constexpr int kStageMeta = 16 * 16;             // per row: 3 scale words, 1 zeros word
 constexpr int kStageBytes = kStageW + kStageMeta;
 constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
-constexpr int kBarBytes = kWarps * kDepth * 8;
+constexpr int kBarBytes = kWarps * kDepth * 8 + 16;  // ring barriers, then a CTA flag
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr int kErrMmaWait = 128;  // device status bit: a ring wait expired
+constexpr int kErrMmaDep = 256;   // device status bit: a wait for an earlier linear expired
 constexpr float kTwo20 = 1048576.f;
 constexpr float kTwoM20 = 1.f / 1048576.f;
-
-struct MmaParams {
-    const __half *x;
-    const __half *scales;
-    const uint32_t *zeros;
-    __half *y;
-    float *partials;
-    unsigned *counters;
-    int *status;
-    uintptr_t scales_first;  // the aligned word holding the first scale
-    uintptr_t scales_end;    // one past the last byte of the scales array
-    int N, K, G, ZW;
-    int M;  // tokens, 1..8
-    int S, slice_groups;
-    int n_strips, ctas_per_slice;  // 16-row strips; persistent CTAs per slice
-    int xstride;                   // bytes per staged token row
-};
 
 // Staged x: 16-byte unit J of a token row lives at unit J ^ (bit 3 of J moved
 // to bit 1).  With a row stride of 16 (mod 128) bytes the 16-byte reads of a
@@ -171,26 +163,46 @@ __device__ __forceinline__ uint4 mma_pair_order(uint4 v) {
     return o;
 }
 
+
+struct MmaKernelParams {
+    MmaLinDesc single;         // the linear of a one-linear launch
+    const MmaLinDesc *descs;   // fused round: device array of n_lin linears
+    unsigned *done;            // fused round with waits: n_lin + 1 counters, else null
+    int *status;
+    int n_lin;
+    int total_units;
+};
+
+// Bounded wait until *p >= target (acquire); false once kWaitNs has passed.
+__device__ __forceinline__ bool wait_counter(const unsigned *p, unsigned target) {
+    const unsigned long long t0 = dev::globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if ((i & 15) == 15) {
+            if (dev::globaltimer() - t0 > kWaitNs) return false;
+            __nanosleep(256);
+        }
+    }
+}
+
+template <bool kRound>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    mma_kernel(const __grid_constant__ CUtensorMap tmap, const MmaParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    mma_kernel(const __grid_constant__ MmaKernelParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     uint8_t *wring = smem + (size_t)warp * kDepth * kStageBytes;  // this warp's two slots
     uint8_t *xs = smem + kRingBytes + kBarBytes;                   // staged x, then the sums
+    // set when a wait expired: the CTA's warps stop at their next unit
+    volatile int &abort_flag = *reinterpret_cast<int *>(smem + kRingBytes + kBarBytes - 16);
     // the next kernel in the stream may be scheduled as SMs free up; it waits
     // for this grid to finish before it touches anything this grid writes
     grid_dependents_launch();
-
-    const int slice = blockIdx.x % p.S;
-    const int q = blockIdx.x / p.S;  // index among the CTAs of this slice
-    const int g0 = slice * p.slice_groups;  // a multiple of kStageGroups
-    const int ng = min(p.G, g0 + p.slice_groups) - g0;
-    const int nst = (ng + kStageGroups - 1) / kStageGroups;  // stages per strip
-    // this warp's strips: first, first + stride, ...
-    const int first = q * kWarps + warp;
-    const int stride = p.ctas_per_slice * kWarps;
-    const int my_strips = first < p.n_strips ? (p.n_strips - 1 - first) / stride + 1 : 0;
+    const int total = P.total_units;
+    const int grid = gridDim.x;
+    auto desc = [&](int l) -> const MmaLinDesc & { return kRound ? P.descs[l] : P.single; };
 
     const uint32_t bar0 = dev::smem_u32(smem + kRingBytes) + 8 * kDepth * warp;
     const uint32_t ring0 = dev::smem_u32(wring);
@@ -200,165 +212,232 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int s = 0; s < kDepth; ++s) mbar_init(bar0 + 8 * s, 1 + 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (threadIdx.x == 0) abort_flag = 0;
     __syncwarp();
 
-    // ---- copy stream: the issue cursor runs kDepth stages ahead of the
-    // consume cursor.  Weights, scales and zeros are parameters (never written
-    // by a preceding kernel), so the stream starts before the grid-dependency
-    // wait.  Metadata: lane (r = lane % 16, h = lane / 16) copies, for row r
-    // of the strip, scale words 0 and 1 of the stage (h = 0) or scale word 2
-    // and the zeros word (h = 1); the scale words are the three aligned words
-    // that hold the stage's four (2-byte aligned) scales.
-    int is_k = 0, is_j = 0, is_slot = 0;
+    // ---- copy stream.  The issue cursor walks this warp's stages (unit by
+    // unit, linear by linear) kDepth stages ahead of the consume cursor.
+    // Weights, scales and zeros are never written by a preceding kernel, so
+    // the stream starts before the grid-dependency wait.  Metadata: lane
+    // (r = lane % 16, h = lane / 16) copies, for row r of the strip, scale
+    // words 0 and 1 of the stage (h = 0) or scale word 2 and the zeros word
+    // (h = 1): the three aligned words that hold the stage's four (2-byte
+    // aligned) scales, and the zeros word of its groups.
     const int r = lane & 15, h = lane >> 4;
-    // this lane's copy sources in the issue cursor's strip, set on entering it
-    int is_row16 = 0;    // first row of the strip
-    uintptr_t is_s = 0;  // next scale word to copy (h = 0: it and the next; h = 1: word 2)
-    int is_avail = 0;    // bytes from is_s to the end of the scales array (0 past row N)
-    uintptr_t is_z = 0;  // zeros word of the next stage
+    int iu = blockIdx.x, il = 0;  // unit and linear of the issue cursor
+    int ij = 0, inst = 0;         // stage within the unit, stages of the unit
+    unsigned t_iss = 0;           // stages issued by this warp
+    uint64_t i_map = 0;           // tensor map of the unit's linear
+    int i_g0 = 0, i_row16 = 0;    // first group of the slice, first row of the strip
+    uintptr_t i_sfirst = 0;       // a valid source address for zero-byte copies
+    uintptr_t is_s = 0;           // next scale word to copy (h = 0: it and the next)
+    int is_avail = 0;             // bytes from is_s to the end of the scales (0 past row N)
+    uintptr_t is_z = 0;           // zeros word of the next stage
     uint32_t is_zbytes = 0;
-    auto enter_strip = [&]() {
-        is_row16 = (first + is_k * stride) * 16;
-        const int row = is_row16 + r;
-        const bool vr = row < p.N;
-        const size_t rr = (size_t)(vr ? row : 0);
-        is_s = (((uintptr_t)(p.scales + rr * p.G + g0)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
-        const uintptr_t rem = is_s < p.scales_end ? p.scales_end - is_s : 0;
-        is_avail = vr ? (int)(rem > (1u << 30) ? (1u << 30) : rem) : 0;
-        is_z = (uintptr_t)(p.zeros + rr * p.ZW + (g0 >> 3));
-        is_zbytes = vr ? 4u : 0u;
+    // move the issue cursor to the first unit at or after iu in which this
+    // warp has a strip (warp 0 always has one: it also asks L2 for the unit's
+    // slice of x)
+    auto i_enter = [&]() {
+        for (; iu < total; iu += grid) {
+            if (kRound)
+                while (il + 1 < P.n_lin && iu >= P.descs[il + 1].unit_start) ++il;
+            const MmaLinDesc &D = desc(il);
+            const int ul = iu - D.unit_start;
+            const int s = ul / D.n_blocks, sb = ul - s * D.n_blocks;
+            const int strip = sb * kWarps + warp;
+            if (strip >= D.n_strips) continue;
+            i_g0 = s * D.slice_groups;
+            const int ng = min(D.G, i_g0 + D.slice_groups) - i_g0;
+            inst = (ng + kStageGroups - 1) / kStageGroups;
+            if (warp == 0 && lane < D.M)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 D.x + (size_t)lane * D.K + (size_t)i_g0 * kGroup),
+                             "r"(ng * kGroup * 2)
+                             : "memory");
+            i_map = reinterpret_cast<uint64_t>(&D.tmap);
+            i_row16 = strip * 16;
+            i_sfirst = D.scales_first;
+            const int row = i_row16 + r;
+            const bool vr = row < D.N;
+            const size_t rr = (size_t)(vr ? row : 0);
+            is_s = (((uintptr_t)(D.scales + rr * D.G + i_g0)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
+            const uintptr_t rem = is_s < D.scales_end ? D.scales_end - is_s : 0;
+            is_avail = vr ? (int)(rem > (1u << 30) ? (1u << 30) : rem) : 0;
+            is_z = (uintptr_t)(D.zeros + rr * D.ZW + (i_g0 >> 3));
+            is_zbytes = vr ? 4u : 0u;
+            ij = 0;
+            return;
+        }
     };
-    if (my_strips > 0) enter_strip();
     auto issue_next = [&]() {
-        if (is_k >= my_strips) return;
-        const uint32_t bar = bar0 + 8 * is_slot;
-        const uint32_t dst = ring0 + is_slot * kStageBytes;
+        if (iu >= total) return;
+        const uint32_t slot = t_iss & 1u;  // kDepth == 2
+        const uint32_t bar = bar0 + 8 * slot;
+        const uint32_t dst = ring0 + slot * kStageBytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, kStageW);
-            tma_box(dst, &tmap, is_row16, g0 + is_j * kStageGroups, bar);
+            tma_box(dst, reinterpret_cast<const CUtensorMap *>(i_map), i_row16,
+                    i_g0 + ij * kStageGroups, bar);
         }
         // a scale word copies the part of it inside the array; a word past
         // the end, or of a row past N, becomes zeros, reads nothing and takes
-        // the array's first word as its (valid) source address
+        // a valid source address
         const uint32_t md = dst + kStageW + r * 16 + 8 * h;
         const int n0 = min(max(is_avail, 0), 4);
-        cp4(md, n0 ? is_s : p.scales_first, (uint32_t)n0);
+        cp4(md, n0 ? is_s : i_sfirst, (uint32_t)n0);
         if (h == 0) {
             const int n1 = min(max(is_avail - 4, 0), 4);
-            cp4(md + 4, n1 ? is_s + 4 : p.scales_first, (uint32_t)n1);
+            cp4(md + 4, n1 ? is_s + 4 : i_sfirst, (uint32_t)n1);
         } else {
             cp4(md + 4, is_z, is_zbytes);
         }
         cp_arrive_noinc(bar);
-        is_slot ^= 1;  // kDepth == 2
+        ++t_iss;
         is_s += 8;
         is_avail -= 8;
         // stage j covers groups g0 + 4j .. g0 + 4j + 3: a new zeros word
         // starts with every second stage
-        if (((g0 + (is_j + 1) * kStageGroups) & 7) == 0) is_z += 4;
-        if (++is_j == nst) {
-            is_j = 0;
-            if (++is_k < my_strips) enter_strip();
+        if (((i_g0 + (ij + 1) * kStageGroups) & 7) == 0) is_z += 4;
+        if (++ij == inst) {
+            iu += grid;
+            i_enter();
         }
     };
-    static_assert(kDepth == 2, "the slot and phase updates assume two slots");
-    // Ask L2 for this slice of x first: the staging loads below then hit L2
-    // instead of queueing behind the weight stream.  A prefetch changes no
-    // value a later load returns, so it may run before the dependency wait.
-    if (warp == 0 && lane < p.M)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         p.x + (size_t)lane * p.K + (size_t)g0 * kGroup),
-                     "r"(ng * kGroup * 2)
-                     : "memory");
+    static_assert(kDepth == 2, "the slot and phase arithmetic assumes two slots");
+    i_enter();
 #pragma unroll
     for (int s = 0; s < kDepth; ++s) issue_next();
 
-    // ---- from here on: x, y and the split-K workspace may belong to the
-    // preceding kernel
+    // ---- from here on: activations, outputs, the split-K workspace and the
+    // completion counters may belong to the preceding kernel
     grid_dependency_wait();
 
-    // ---- stage x[:, slice] in MMA pair order, and each (group, token)'s sum
-    // S of x (kept as S * 2^-20): the 16 lanes of a half warp hold the 16 units
-    // of one group of one token and add theirs with shuffles
-    const int M = p.M;
-    float *sums = reinterpret_cast<float *>(xs + (size_t)M * p.xstride);  // [group][8] S * 2^-20
-    {
-        // kXBatch loads in flight per thread: the staging costs two or three
-        // L2 round trips instead of one per unit
-        constexpr int kXBatch = 8;
-        const int nunits = ng * (kGroup / 8);
-        const int xtotal = M * nunits;  // a multiple of 16
-        const int k0 = g0 * kGroup;
-        for (int base = warp * 32; base < xtotal; base += kThreads * kXBatch) {
-            uint4 v[kXBatch];
-#pragma unroll
-            for (int b = 0; b < kXBatch; ++b) {
-                const int i = base + b * kThreads + lane;
-                v[b] = make_uint4(0, 0, 0, 0);
-                if (i < xtotal) {
-                    const int t = i / nunits, J = i - t * nunits;
-                    v[b] = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * p.K + k0 + 8 * J));
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < kXBatch; ++b) {
-                const int i = base + b * kThreads + lane;
-                const bool valid = i < xtotal;
-                const int t = i / nunits, J = i - t * nunits;
-                if (valid)
-                    *reinterpret_cast<uint4 *>(xs + (size_t)t * p.xstride + 16 * x_unit(J)) =
-                        mma_pair_order(v[b]);
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].x));
-                const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].y));
-                const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].z));
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].w));
-                float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                if (valid && (J & 15) == 0) sums[(J >> 4) * 8 + t] = sum * kTwoM20;
-            }
-        }
-        // tokens M..7 have no x: their sums are zero
-        for (int i = threadIdx.x; i < ng * (8 - M); i += kThreads)
-            sums[(i / (8 - M)) * 8 + M + i % (8 - M)] = 0.f;
-    }
-    __syncthreads();
-
-    // lanes of tokens >= M compute a column nobody stores: they read token 0
-    const int tok = g < M ? g : 0;
-    const uint8_t *xrow = xs + (size_t)tok * p.xstride;
     // unit of word u of this lane's chunk in a group: x_unit(4c + u)
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
     const int xo2 = 16 * x_unit(4 * c + 2), xo3 = 16 * x_unit(4 * c + 3);
-    int cs_slot = 0;
-    uint32_t cs_par = 0;
+    unsigned t_cons = 0;  // stages consumed by this warp
+    int cl = 0;           // linear of the consumer's unit
+    int passed = 0;       // linears below this one are counted in P.done
+    int staged_l = -1, staged_slice = -1;  // the (linear, slice) whose x is staged
+    bool dead = false;
 
-    for (int k = 0; k < my_strips; ++k) {
-        const int strip = first + k * stride;
+    for (int u = blockIdx.x; u < total; u += grid) {
+        if (kRound)
+            while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
+        const MmaLinDesc &D = desc(cl);
+        const int M = D.M;
+        const int ul = u - D.unit_start;
+        const int slice = ul / D.n_blocks, sb = ul - slice * D.n_blocks;
+        const int g0 = slice * D.slice_groups;  // a multiple of kStageGroups
+        const int ng = min(D.G, g0 + D.slice_groups) - g0;
+        const int nst = (ng + kStageGroups - 1) / kStageGroups;
+
+        float *sums = reinterpret_cast<float *>(xs + (size_t)M * D.xstride);  // [group][8]
+        if (cl == staged_l && slice == staged_slice) goto staged;  // same x as the last unit
+        __syncthreads();  // the previous unit's staged x is no longer read
+        if (abort_flag) {
+            dead = true;
+            break;
+        }
+        if (kRound && P.done) {
+            if (threadIdx.x == 0) {
+                // this CTA has finished every unit of the linears below cl
+                if (passed < cl) {
+                    __threadfence();
+                    for (; passed < cl; ++passed) atomicAdd(P.done + passed, 1u);
+                }
+                if (D.wait_for >= 0 && !wait_counter(P.done + D.wait_for, (unsigned)grid)) {
+                    atomicOr(P.status, kErrMmaDep);
+                    abort_flag = 1;
+                }
+            }
+            __syncthreads();
+            if (abort_flag) {
+                dead = true;
+                break;
+            }
+        }
+
+        // ---- stage x[:, slice] in MMA pair order, and each (group, token)'s
+        // sum S of x (kept as S * 2^-20): the 16 lanes of a half warp hold the
+        // 16 units of one group of one token and add theirs with shuffles
+        {
+            // kXBatch loads in flight per thread: the staging costs a few L2
+            // round trips instead of one per unit of x
+            constexpr int kXBatch = 8;
+            const int nunits = ng * (kGroup / 8);
+            const int xtotal = M * nunits;  // a multiple of 16
+            const int k0 = g0 * kGroup;
+            for (int base = warp * 32; base < xtotal; base += kThreads * kXBatch) {
+                uint4 v[kXBatch];
+#pragma unroll
+                for (int b = 0; b < kXBatch; ++b) {
+                    const int i = base + b * kThreads + lane;
+                    v[b] = make_uint4(0, 0, 0, 0);
+                    if (i < xtotal) {
+                        const int t = i / nunits, J = i - t * nunits;
+                        v[b] = __ldg(reinterpret_cast<const uint4 *>(D.x + (size_t)t * D.K + k0 + 8 * J));
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kXBatch; ++b) {
+                    const int i = base + b * kThreads + lane;
+                    const bool valid = i < xtotal;
+                    const int t = i / nunits, J = i - t * nunits;
+                    if (valid)
+                        *reinterpret_cast<uint4 *>(xs + (size_t)t * D.xstride + 16 * x_unit(J)) =
+                            mma_pair_order(v[b]);
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].x));
+                    const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].y));
+                    const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].z));
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].w));
+                    float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1)
+                        sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                    if (valid && (J & 15) == 0) sums[(J >> 4) * 8 + t] = sum * kTwoM20;
+                }
+            }
+            // tokens M..7 have no x: their sums are zero
+            for (int i = threadIdx.x; i < ng * (8 - M); i += kThreads)
+                sums[(i / (8 - M)) * 8 + M + i % (8 - M)] = 0.f;
+        }
+        __syncthreads();
+        staged_l = cl;
+        staged_slice = slice;
+    staged:
+        const int strip = sb * kWarps + warp;
+        if (strip >= D.n_strips) continue;  // the tail block of a slice
+        // lanes of tokens >= M compute a column nobody stores: they read token 0
+        const int tok = g < M ? g : 0;
+        const uint8_t *xrow = xs + (size_t)tok * D.xstride;
         const int ra = strip * 16 + g, rb = ra + 8;
-        const bool va = ra < p.N, vb = rb < p.N;
+        const bool va = ra < D.N, vb = rb < D.N;
         // where the slice's first scale of each row sits in its aligned word
         // (the same in every stage: a stage advances 8 bytes)
         const uint32_t offA =
-            (uint32_t)(((uintptr_t)(p.scales + (size_t)(va ? ra : 0) * p.G + g0)) >> 1) & 1u;
+            (uint32_t)(((uintptr_t)(D.scales + (size_t)(va ? ra : 0) * D.G + g0)) >> 1) & 1u;
         const uint32_t offB =
-            (uint32_t)(((uintptr_t)(p.scales + (size_t)(vb ? rb : 0) * p.G + g0)) >> 1) & 1u;
+            (uint32_t)(((uintptr_t)(D.scales + (size_t)(vb ? rb : 0) * D.G + g0)) >> 1) & 1u;
         const uint32_t shA = 16u * offA, shB = 16u * offB;
         const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < nst; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * cs_slot, cs_par))) {
-                if (lane == 0) atomicOr(p.status, kErrMmaWait);
-                cp_wait_all();
-                return;
+            const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
+                if (lane == 0) {
+                    atomicOr(P.status, kErrMmaWait);
+                    abort_flag = 1;  // the other warps stop at their next unit
+                }
+                dead = true;
+                break;
             }
             // this lane's part of the stage: 16 bytes of rows g and g + 8 of
             // each group (read just before the group), the metadata of both rows
-            const uint8_t *st = wring + cs_slot * kStageBytes;
+            const uint8_t *st = wring + slot * kStageBytes;
             const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
             const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
             const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
-
             // zero nibbles of the stage's groups: the stage starts at group
             // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
             const uint32_t zsh = ((g0 + j * kStageGroups) & 4) ? 16u : 0u;
@@ -381,8 +460,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const float sA = __half2float(__ushort_as_half((unsigned short)hA));
                 const float sB = __half2float(__ushort_as_half((unsigned short)hB));
                 // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
-                const float zA = __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
-                const float zB = __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
+                const float zA =
+                    __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
+                const float zB =
+                    __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
                 const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);  // S * 2^-20
                 const uint8_t *xi = xg + i * 256;
                 uint4 xv[4];
@@ -396,12 +477,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
                 float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t a = wA[u], b = wB[u], a8 = a >> 8, b8 = b >> 8;
+                for (int uu = 0; uu < 4; ++uu) {
+                    const uint32_t a = wA[uu], b = wB[uu], a8 = a >> 8, b8 = b >> 8;
                     mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
-                             b8 & 0x000f000fu, xv[u].x, xv[u].y);
+                             b8 & 0x000f000fu, xv[uu].x, xv[uu].y);
                     mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
-                             b8 & 0x00f000f0u, xv[u].z, xv[u].w);
+                             b8 & 0x00f000f0u, xv[uu].z, xv[uu].w);
                 }
                 // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
                 acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
@@ -423,27 +504,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // reads before the new box's writes.
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            ++t_cons;
             issue_next();
-            cs_slot ^= 1;
-            if (cs_slot == 0) cs_par ^= 1;
         }
+        if (dead) break;
 
         // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
         const int t0 = 2 * c, t1 = 2 * c + 1;
-        if (p.S == 1) {
-            if (va && t0 < M) p.y[(size_t)t0 * p.N + ra] = __float2half_rn(acc[0]);
-            if (va && t1 < M) p.y[(size_t)t1 * p.N + ra] = __float2half_rn(acc[1]);
-            if (vb && t0 < M) p.y[(size_t)t0 * p.N + rb] = __float2half_rn(acc[2]);
-            if (vb && t1 < M) p.y[(size_t)t1 * p.N + rb] = __float2half_rn(acc[3]);
+        if (D.S == 1) {
+            if (va && t0 < M) D.y[(size_t)t0 * D.N + ra] = __float2half_rn(acc[0]);
+            if (va && t1 < M) D.y[(size_t)t1 * D.N + ra] = __float2half_rn(acc[1]);
+            if (vb && t0 < M) D.y[(size_t)t0 * D.N + rb] = __float2half_rn(acc[2]);
+            if (vb && t1 < M) D.y[(size_t)t1 * D.N + rb] = __float2half_rn(acc[3]);
             continue;
         }
-        float *part = p.partials + (size_t)slice * M * p.N;
-        if (va && t0 < M) part[(size_t)t0 * p.N + ra] = acc[0];
-        if (va && t1 < M) part[(size_t)t1 * p.N + ra] = acc[1];
-        if (vb && t0 < M) part[(size_t)t0 * p.N + rb] = acc[2];
-        if (vb && t1 < M) part[(size_t)t1 * p.N + rb] = acc[3];
+        float *part = D.partials + (size_t)slice * M * D.N;
+        if (va && t0 < M) part[(size_t)t0 * D.N + ra] = acc[0];
+        if (va && t1 < M) part[(size_t)t1 * D.N + ra] = acc[1];
+        if (vb && t0 < M) part[(size_t)t0 * D.N + rb] = acc[2];
+        if (vb && t1 < M) part[(size_t)t1 * D.N + rb] = acc[3];
         // count this slice's arrival for the strip with one release-acquire
         // atomic after a warp barrier (the barrier orders the other lanes'
         // partial writes before it); the warp that arrives last sums the
@@ -453,11 +534,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 0)
             asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                          : "=r"(prev)
-                         : "l"(p.counters + strip)
+                         : "l"(D.counters + strip)
                          : "memory");
         prev = __shfl_sync(0xffffffffu, prev, 0);
         __syncwarp();  // the other lanes' reads below come after lane 0's acquire
-        if (prev == (unsigned)(p.S - 1)) {
+        if (prev == (unsigned)(D.S - 1)) {
             const int rows[2] = {ra, rb};
             const bool ok[2] = {va, vb};
 #pragma unroll
@@ -467,24 +548,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const int t = 2 * c + e;
                     if (ok[hh] && t < M) {
                         float sum = 0.f;
-                        for (int s2 = 0; s2 < p.S; ++s2)
-                            sum += __ldcg(p.partials + ((size_t)s2 * M + t) * p.N + rows[hh]);
-                        p.y[(size_t)t * p.N + rows[hh]] = __float2half_rn(sum);
+                        for (int s2 = 0; s2 < D.S; ++s2)
+                            sum += __ldcg(D.partials + ((size_t)s2 * M + t) * D.N + rows[hh]);
+                        D.y[(size_t)t * D.N + rows[hh]] = __float2half_rn(sum);
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) p.counters[strip] = 0u;  // ready for the next launch
+            if (lane == 0) D.counters[strip] = 0u;  // ready for the next launch
         }
     }
+
+    if (dead) {
+        // a wait expired: let this warp's copies in flight land (bounded)
+        // before the CTA's shared memory goes away
+        for (; t_cons < t_iss; ++t_cons) mbar_wait(bar0 + 8 * (t_cons & 1u), (t_cons >> 1) & 1u);
+        cp_wait_all();
+        return;
+    }
     cp_wait_all();
+    if (kRound && P.done) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            for (; passed < P.n_lin; ++passed) atomicAdd(P.done + passed, 1u);
+            // the last CTA out leaves the counters zeroed for the next launch
+            const unsigned prev = atomicAdd(P.done + P.n_lin, 1u);
+            if (prev == (unsigned)grid - 1) {
+                __threadfence();
+                for (int l = 0; l <= P.n_lin; ++l) P.done[l] = 0u;
+            }
+        }
+    }
 }
 
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
-
-int smem_for(int M, int slice_groups) {
-    return kRingBytes + kBarBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 4;
-}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -492,13 +590,37 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode_mma = nullptr;
 
+cudaLaunchConfig_t launch_config(int grid, int smem, cudaStream_t stream,
+                                 cudaLaunchAttribute *attr) {
+    // programmatic dependent launch: the grid may start while the previous
+    // kernel in the stream drains; the kernel waits for it (griddepcontrol)
+    // before touching activations, outputs or the workspace
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 }  // namespace
+
+int mma_smem_bytes(int M, int slice_groups) {
+    return kRingBytes + kBarBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 4;
+}
+
+int mma_round_grid(const DeviceInfo &dev) { return kCtasPerSm * dev.sm_count; }
 
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     MmaPlan pl{};
     pl.M = M;
     const int G = K / kGroup;
     pl.n_strips = (N + 15) / 16;
+    pl.n_blocks = (pl.n_strips + kWarps - 1) / kWarps;
     // largest slice (a whole number of stages) whose staged x and sums fit
     const int budget = kSmemPerCta - kRingBytes - kBarBytes;
     int max_groups = (budget - 16 * M) / (kGroup * 2 * M + 32);
@@ -510,28 +632,35 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
         pl.ok = false;
         return pl;
     }
-    const int warps = kCtasPerSm * dev.sm_count * kWarps;
-    // Pick the number of K slices that minimises the work of the busiest warp
-    // (strips per warp x (groups per slice + a per-strip charge)), plus a
-    // charge per extra slice for the partial sums; slices are whole stages.
-    int s_lo = s_min;
-    if (split == 1 && s_lo < 2 && G > kStageGroups) s_lo = 2;
-    int s_hi = split == 0 ? 1 : (G + kStageGroups - 1) / kStageGroups;
-    if (s_hi < s_lo) s_hi = s_lo;
+    const int grid_max = kCtasPerSm * dev.sm_count;
     int best_sg = 0;
-    double best_cost = 1e30;
-    for (int S = s_lo; S <= s_hi; ++S) {
-        int sg = (G + S - 1) / S;
-        sg = (sg + kStageGroups - 1) / kStageGroups * kStageGroups;
-        if (sg > max_groups) continue;
-        const int S_eff = (G + sg - 1) / sg;
-        if (split == 1 && S_eff < 2 && G > kStageGroups) continue;
-        const long long units = (long long)pl.n_strips * S_eff;
-        const long long per_warp = (units + warps - 1) / warps;
-        const double cost = (double)per_warp * (sg + 2) + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best_sg = sg;
+    if (split == 2) {
+        // fewest slices: spread evenly over whole stages
+        best_sg = (G + s_min - 1) / s_min;
+        best_sg = (best_sg + kStageGroups - 1) / kStageGroups * kStageGroups;
+    } else {
+        // Pick the number of K slices that minimises the work of the busiest
+        // CTA (units per CTA x (groups per slice + a per-unit charge)), plus a
+        // charge per extra slice for the partial sums; slices are whole stages.
+        int s_lo = s_min;
+        if (split == 1 && s_lo < 2 && G > kStageGroups) s_lo = 2;
+        int s_hi = split == 0 ? 1 : (G + kStageGroups - 1) / kStageGroups;
+        if (s_hi < s_lo) s_hi = s_lo;
+        double best_cost = 1e30;
+        for (int S = s_lo; S <= s_hi; ++S) {
+            int sg = (G + S - 1) / S;
+            sg = (sg + kStageGroups - 1) / kStageGroups * kStageGroups;
+            if (sg > max_groups) continue;
+            const int S_eff = (G + sg - 1) / sg;
+            if (split == 1 && S_eff < 2 && G > kStageGroups) continue;
+            const long long units = (long long)pl.n_blocks * S_eff;
+            const long long per_cta = (units + grid_max - 1) / grid_max;
+            const double cost =
+                (double)per_cta * (sg + 2) + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
+            if (cost < best_cost - 1e-9) {
+                best_cost = cost;
+                best_sg = sg;
+            }
         }
     }
     if (best_sg == 0) {  // split == 1 and too few groups to split along stage lines
@@ -540,67 +669,87 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     }
     pl.slice_groups = best_sg;
     pl.S = (G + best_sg - 1) / best_sg;
-    int per_slice = kCtasPerSm * dev.sm_count / pl.S;
-    const int need = (pl.n_strips + kWarps - 1) / kWarps;  // CTAs to give every strip a warp
-    if (per_slice > need) per_slice = need;
-    if (per_slice < 1) per_slice = 1;
-    pl.ctas_per_slice = per_slice;
-    pl.grid = per_slice * pl.S;
-    pl.smem_bytes = smem_for(M, pl.slice_groups);
+    pl.units = pl.S * pl.n_blocks;
+    pl.grid = pl.units < grid_max ? pl.units : grid_max;
+    pl.smem_bytes = mma_smem_bytes(M, pl.slice_groups);
     pl.ws_bytes = pl.S > 1 ? (size_t)pl.S * M * N * sizeof(float) : 0;
-    pl.ok = pl.S <= 65535;
+    pl.ok = true;
     return pl;
 }
 
-cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
-                       cudaStream_t stream) {
+cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
+                         unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d) {
     if (!g_encode_mma) return cudaErrorInitializationError;
+    memset(d, 0, sizeof(*d));
     const int G = a.K / kGroup;
     // qweight as a 3-D tensor of uint32: (word in group, row, group), so one
     // box brings a strip's 16 rows x 4 groups, group-major
-    CUtensorMap tmap;
     const cuuint64_t dims[3] = {16, (cuuint64_t)a.N, (cuuint64_t)G};
     const cuuint64_t strides[2] = {(cuuint64_t)a.K / 2, 64};
     const cuuint32_t box[3] = {16, 16, (cuuint32_t)kStageGroups};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode_mma(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims, strides,
-                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode_mma(&d->tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    MmaParams p;
-    p.x = a.x;
-    p.scales = a.scales;
-    p.zeros = a.zeros;
-    p.y = a.y;
-    p.partials = ws.partials;
-    p.counters = ws.counters;
-    p.status = ws.status;
-    p.scales_first = (uintptr_t)a.scales & ~(uintptr_t)3;
-    p.scales_end = (uintptr_t)(a.scales + (size_t)a.N * G);
-    p.N = a.N;
-    p.K = a.K;
-    p.G = G;
-    p.ZW = (G + 7) / 8;
-    p.M = a.M;
-    p.S = plan.S;
-    p.slice_groups = plan.slice_groups;
-    p.n_strips = plan.n_strips;
-    p.ctas_per_slice = plan.ctas_per_slice;
-    p.xstride = xstride_for(plan.slice_groups);
-    // programmatic dependent launch: the grid may start while the previous
-    // kernel in the stream drains; the kernel waits for it (griddepcontrol)
-    // before touching x, y or the workspace
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = plan.smem_bytes;
-    cfg.stream = stream;
+    d->x = a.x;
+    d->scales = a.scales;
+    d->zeros = a.zeros;
+    d->y = a.y;
+    d->partials = partials;
+    d->counters = counters;
+    d->scales_first = (uintptr_t)a.scales & ~(uintptr_t)3;
+    d->scales_end = (uintptr_t)(a.scales + (size_t)a.N * G);
+    d->N = a.N;
+    d->K = a.K;
+    d->G = G;
+    d->ZW = (G + 7) / 8;
+    d->M = a.M;
+    d->S = plan.S;
+    d->slice_groups = plan.slice_groups;
+    d->n_strips = plan.n_strips;
+    d->n_blocks = plan.n_blocks;
+    d->unit_start = unit_start;
+    d->xstride = xstride_for(plan.slice_groups);
+    d->wait_for = wait_for;
+    return cudaSuccess;
+}
+
+cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
+                       cudaStream_t stream) {
+    MmaKernelParams P;
+    memset(&P, 0, sizeof(P));
+    cudaError_t e = mma_describe(a, plan, ws.partials, ws.counters, 0, -1, &P.single);
+    if (e != cudaSuccess) return e;
+    P.status = ws.status;
+    P.n_lin = 1;
+    P.total_units = plan.units;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel, tmap, p);
+    cudaLaunchConfig_t cfg = launch_config(plan.grid, plan.smem_bytes, stream, attr);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<false>, P);
+}
+
+cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const DeviceInfo &dev,
+                             cudaStream_t stream) {
+    MmaKernelParams P;
+    memset(&P, 0, sizeof(P));
+    P.descs = r.descs;
+    P.done = r.done;
+    P.status = ws.status;
+    P.n_lin = r.n;
+    P.total_units = r.total_units;
+    int grid = mma_round_grid(dev);
+    if (grid > r.total_units) grid = r.total_units;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config(grid, r.smem_bytes, stream, attr);
+    if (r.done) {
+        // linears wait for earlier ones: every CTA must be resident at once
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+    }
+    return cudaLaunchKernelEx(&cfg, mma_kernel<true>, P);
 }
 
 cudaError_t mma_init(const DeviceInfo &dev) {
@@ -615,10 +764,14 @@ cudaError_t mma_init(const DeviceInfo &dev) {
     }
     int dyn = kSmemPerCta;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
-    cudaError_t e = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        const void *fn = k ? (const void *)mma_kernel<true> : (const void *)mma_kernel<false>;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+    }
     return e;
 }
 
