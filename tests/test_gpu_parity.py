@@ -312,6 +312,62 @@ def test_decode_round_eager_and_graph(w4):
         assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, f"round layer j={L['j']}")
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_decode_round_chained_waits(w4, graph):
+    # Each linear reads the previous one's output (x_l = y_{l-1}), one writes
+    # over an earlier one's input (write after read) and the last two write
+    # the same output (write after write): the fused round must wait where
+    # the results of running the linears one after another require it.
+    # Every output is checked against the oracle applied to the input the GPU
+    # actually used; the round runs twice (the completion counters must be
+    # left zeroed for the next launch).
+    M = 4
+    dims = [1024, 2048, 1536, 1024, 3072, 2048]
+    acts = [torch.zeros((M, d), dtype=torch.float16, device=DEV) for d in dims]
+    acts[0].copy_(si.x(si.config_seed(60), M, dims[0]).to(DEV))
+    layers = []
+    for l in range(len(dims) - 1):
+        K, N = dims[l], dims[l + 1]
+        seed = si.config_seed(61, l)
+        qw, s, zw = si.layer(seed, N, K, device=DEV)
+        layers.append(dict(x=acts[l], qweight=qw, scales=s, zeros=zw, y=acts[l + 1], N=N, K=K,
+                           seed=seed))
+    # write after read: overwrite the first input once the chain has read it
+    qw, s, zw = si.layer(si.config_seed(62), dims[0], dims[-1], device=DEV)
+    layers.append(dict(x=acts[-1], qweight=qw, scales=s, zeros=zw, y=acts[0], N=dims[0],
+                       K=dims[-1], seed=si.config_seed(62)))
+    # write after write: a later linear writes the same output; only its
+    # result may remain
+    qw, s, zw = si.layer(si.config_seed(63), dims[0], dims[2], device=DEV)
+    layers.append(dict(x=acts[2], qweight=qw, scales=s, zeros=zw, y=acts[0], N=dims[0],
+                       K=dims[2], seed=si.config_seed(63)))
+    descs = w4.make_descs(layers)
+    x0 = acts[0].clone()
+    for rep in range(2):
+        acts[0].copy_(x0)
+        for a in acts[1:]:
+            a.fill_(float("nan"))
+        if graph:
+            g = w4.RoundGraph(descs, M)
+            g.launch()
+            torch.cuda.synchronize()
+            g.destroy()
+        else:
+            w4.w4a16_decode_round(descs, M)
+            torch.cuda.synchronize()
+        assert w4.w4a16_device_status() == 0
+        chain = [x0] + [acts[l + 1].clone() for l in range(len(dims) - 1)]
+        # (input, output) of every linear whose output survives the round
+        checks = [(l, chain[l], chain[l + 1]) for l in range(len(dims) - 1)]
+        checks.append((len(layers) - 1, chain[2], acts[0].clone()))
+        for l, x_used, out in checks:
+            L = layers[l]
+            x_cpu = x_used.cpu()
+            qw_h, s_h, zw_h = si.layer(L["seed"], L["N"], L["K"])
+            ref = oracle.linear(si.as_u16(x_cpu), si.as_u32(qw_h), si.as_u16(s_h), si.as_u32(zw_h))
+            assert_close(out, ref, f"chained linear {l} rep {rep}")
+
+
 @pytest.mark.slow
 def test_decode_round_full_64_layers_sampled(w4):
     M = 4
