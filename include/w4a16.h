@@ -40,7 +40,7 @@
  *   - x, qweight and y must be 16-byte aligned, scales 2-byte, zeros 4-byte
  *     (W4A16_ERR_MISALIGNED).  x and y must not overlap (INVALID_ARG).
  *   - w4a16_linear and w4a16_decode_round allocate nothing, free nothing and
- *     never synchronise, so they may be captured into a CUDA graph.  They need
+ *     never synchronise the device, so they may be captured into a CUDA graph.  They need
  *     w4a16_init first (the split-K workspace and the kernel attributes).
  *   - The split-K workspace is shared by every call: calls that may use it must
  *     be ordered on one stream (or otherwise serialised).  Two such calls that
@@ -139,16 +139,31 @@ typedef struct {
 } w4a16_linear_desc;
 
 /* A decode round: the linears of `descs` (a HOST array of n_descs entries,
- * e.g. 64 layers x {qkv, o, gate+up, down}) run back to back on `stream`, all
- * at the same M, each reading its weights once (haowenji.com V100 decode
- * article: one round reads every weight once).  All descriptors are validated
- * before the first launch. */
+ * e.g. 64 layers x {qkv, o, gate+up, down}) run on `stream`, all at the same
+ * M, each reading its weights once (haowenji.com V100 decode article: one
+ * round reads every weight once).  All descriptors are validated before
+ * anything is launched.
+ *
+ * The results are those of running the linears one after another in array
+ * order.  When every linear takes the warp-MMA rungs (M <= 8, no forced rung)
+ * the round is ONE kernel launch: the weights of all linears stream without a
+ * break, each linear gets its own part of the split-K workspace, and a linear
+ * that reads an earlier linear's output, writes an earlier linear's input or
+ * output (overlapping device ranges) waits inside the kernel for that linear
+ * to complete.  Such a round needs n_descs <= 4096 and workspace for every
+ * split linear's partial sums at once (W4A16_ERR_WORKSPACE otherwise).  Its
+ * descriptors are copied to device memory on `stream` when they differ from
+ * the previous round's (the copy may briefly block the calling thread while
+ * it stages them).  Other rounds, and every round enqueued on a stream that is
+ * being captured, launch linear by linear; w4a16_round_graph_create captures
+ * the fused form. */
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream);
 
 /* Capture a decode round into an instantiated CUDA graph (an opaque handle in
- * *graph).  Allocates and captures on an internal stream: call after
- * w4a16_init, outside any other capture.  The graph keeps the descriptors'
- * device pointers and the dispatch decisions made at capture time. */
+ * *graph).  Allocates (the graph's own copy of a fused round's descriptors)
+ * and captures on an internal stream: call after w4a16_init, outside any other
+ * capture.  The graph keeps the descriptors' device pointers and the dispatch
+ * decisions made at capture time. */
 int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M,
                              void **graph);
 /* Replay a captured round on `stream`. */

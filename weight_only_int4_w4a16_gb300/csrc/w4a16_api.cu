@@ -476,6 +476,14 @@ int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void 
     int st = validate_round(descs, n_descs, M);
     if (st) return st;
     State &s = g_state;
+    // A graph captured from this call would keep pointing at the shared
+    // descriptor copy that later rounds overwrite: under capture, launch linear
+    // by linear (w4a16_round_graph_create captures a fused round with its own
+    // descriptors).
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    if (cap != cudaStreamCaptureStatusNone) return round_per_linear(descs, n_descs, M, stream);
     FusedRound fr;
     st = plan_fused_round(descs, n_descs, M, s, &fr);
     if (st == W4A16_ERR_UNSUPPORTED) return round_per_linear(descs, n_descs, M, stream);

@@ -84,15 +84,17 @@ cudaError_t tc_init(const DeviceInfo &dev);
 // ---- warp-level tensor-core MMA rungs (w4a16_mma.cu) ----------------------
 constexpr int kMmaMaxTokens = 8;  // tokens per launch (the MMA's N = 8)
 
-// The work of one linear is cut into units: one K slice of 8 strips of 16
-// rows (one strip per warp of a CTA).  CTAs take units round-robin.
+// The work of one linear is cut into units: one K slice of 8 * strips_per_warp
+// strips of 16 rows (strips_per_warp per warp of a CTA, which stages the
+// slice's activations once for all of them).  CTAs take units round-robin.
 struct MmaPlan {
     bool ok;
     int M;             // tokens (1..8)
     int S;             // K slices
     int slice_groups;  // groups per slice (a multiple of 4; the last slice may hold fewer)
     int n_strips;      // 16-row strips
-    int n_blocks;      // units per slice: ceil(n_strips / 8)
+    int strips_per_warp;
+    int n_blocks;      // units per slice: ceil(n_strips / (8 * strips_per_warp))
     int units;         // S * n_blocks
     int grid;          // CTAs of a launch of this linear alone
     int smem_bytes;    // dynamic shared memory of such a launch
@@ -111,14 +113,15 @@ struct MmaLinDesc {
     unsigned *counters;   // this linear's per-strip arrival counters (S > 1)
     uintptr_t scales_first;  // the aligned word holding the first scale
     uintptr_t scales_end;    // one past the last byte of the scales array
-    int N, K, G, ZW, M, S, slice_groups, n_strips, n_blocks;
+    int N, K, G, ZW, M, S, slice_groups, n_strips, strips_per_warp, n_blocks;
     int unit_start;  // index of the linear's first unit in the fused list
     int xstride;     // bytes per staged token row
     int wait_for;    // fused round: linear that must be complete before this one reads x (-1: none)
 };
 
 // split: 0 = never split K, 1 = split K, -1 = planner balances the warps,
-// 2 = fewest slices the staged activations allow (fused rounds).
+// 2 = fused rounds: fewest slices the staged activations allow, and units of
+// kRoundStripsPerWarp strips per warp (the round's units balance each other).
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev);
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);

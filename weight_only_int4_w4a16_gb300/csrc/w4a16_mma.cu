@@ -73,6 +73,7 @@ constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
 constexpr int kBarBytes = kWarps * kDepth * 8 + 16;  // ring barriers, then a CTA flag
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
+constexpr int kRoundStripsPerWarp = 4;  // fused rounds: strips per warp and unit
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr int kErrMmaWait = 128;  // device status bit: a ring wait expired
 constexpr int kErrMmaDep = 256;   // device status bit: a wait for an earlier linear expired
@@ -234,6 +235,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int is_avail = 0;             // bytes from is_s to the end of the scales (0 past row N)
     uintptr_t is_z = 0;           // zeros word of the next stage
     uint32_t is_zbytes = 0;
+    // this warp's strips in a unit: strip0 + 8r for r < strips per warp
+    int i_strip = 0, i_last = 0;  // current strip, last strip of the unit for this warp
+    const MmaLinDesc *iD = nullptr;
+    // copy sources of the issue cursor's strip
+    auto i_strip_enter = [&]() {
+        const MmaLinDesc &D = *iD;
+        i_row16 = i_strip * 16;
+        const int row = i_row16 + r;
+        const bool vr = row < D.N;
+        const size_t rr = (size_t)(vr ? row : 0);
+        is_s = (((uintptr_t)(D.scales + rr * D.G + i_g0)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
+        const uintptr_t rem = is_s < D.scales_end ? D.scales_end - is_s : 0;
+        is_avail = vr ? (int)(rem > (1u << 30) ? (1u << 30) : rem) : 0;
+        is_z = (uintptr_t)(D.zeros + rr * D.ZW + (i_g0 >> 3));
+        is_zbytes = vr ? 4u : 0u;
+        ij = 0;
+    };
     // move the issue cursor to the first unit at or after iu in which this
     // warp has a strip (warp 0 always has one: it also asks L2 for the unit's
     // slice of x)
@@ -244,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const MmaLinDesc &D = desc(il);
             const int ul = iu - D.unit_start;
             const int s = ul / D.n_blocks, sb = ul - s * D.n_blocks;
-            const int strip = sb * kWarps + warp;
-            if (strip >= D.n_strips) continue;
+            const int strip0 = sb * kWarps * D.strips_per_warp + warp;
+            if (strip0 >= D.n_strips) continue;
             i_g0 = s * D.slice_groups;
             const int ng = min(D.G, i_g0 + D.slice_groups) - i_g0;
             inst = (ng + kStageGroups - 1) / kStageGroups;
@@ -254,18 +272,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                  D.x + (size_t)lane * D.K + (size_t)i_g0 * kGroup),
                              "r"(ng * kGroup * 2)
                              : "memory");
+            iD = &D;
             i_map = reinterpret_cast<uint64_t>(&D.tmap);
-            i_row16 = strip * 16;
             i_sfirst = D.scales_first;
-            const int row = i_row16 + r;
-            const bool vr = row < D.N;
-            const size_t rr = (size_t)(vr ? row : 0);
-            is_s = (((uintptr_t)(D.scales + rr * D.G + i_g0)) & ~(uintptr_t)3) + 8 * (uintptr_t)h;
-            const uintptr_t rem = is_s < D.scales_end ? D.scales_end - is_s : 0;
-            is_avail = vr ? (int)(rem > (1u << 30) ? (1u << 30) : rem) : 0;
-            is_z = (uintptr_t)(D.zeros + rr * D.ZW + (i_g0 >> 3));
-            is_zbytes = vr ? 4u : 0u;
-            ij = 0;
+            const int nr = min(D.strips_per_warp, (D.n_strips - 1 - strip0) / kWarps + 1);
+            i_strip = strip0;
+            i_last = strip0 + kWarps * (nr - 1);
+            i_strip_enter();
             return;
         }
     };
@@ -299,8 +312,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // starts with every second stage
         if (((i_g0 + (ij + 1) * kStageGroups) & 7) == 0) is_z += 4;
         if (++ij == inst) {
-            iu += grid;
-            i_enter();
+            if (i_strip < i_last) {  // the warp's next strip of the unit
+                i_strip += kWarps;
+                i_strip_enter();
+            } else {
+                iu += grid;
+                i_enter();
+            }
         }
     };
     static_assert(kDepth == 2, "the slot and phase arithmetic assumes two slots");
@@ -406,157 +424,161 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         staged_l = cl;
         staged_slice = slice;
     staged:
-        const int strip = sb * kWarps + warp;
-        if (strip >= D.n_strips) continue;  // the tail block of a slice
-        // lanes of tokens >= M compute a column nobody stores: they read token 0
-        const int tok = g < M ? g : 0;
-        const uint8_t *xrow = xs + (size_t)tok * D.xstride;
-        const int ra = strip * 16 + g, rb = ra + 8;
-        const bool va = ra < D.N, vb = rb < D.N;
-        // where the slice's first scale of each row sits in its aligned word
-        // (the same in every stage: a stage advances 8 bytes)
-        const uint32_t offA =
-            (uint32_t)(((uintptr_t)(D.scales + (size_t)(va ? ra : 0) * D.G + g0)) >> 1) & 1u;
-        const uint32_t offB =
-            (uint32_t)(((uintptr_t)(D.scales + (size_t)(vb ? rb : 0) * D.G + g0)) >> 1) & 1u;
-        const uint32_t shA = 16u * offA, shB = 16u * offB;
-        const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < nst; ++j) {
-            const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
-                if (lane == 0) {
-                    atomicOr(P.status, kErrMmaWait);
-                    abort_flag = 1;  // the other warps stop at their next unit
+        // this warp's strips of the unit: strip0, strip0 + 8, ... (the tail
+        // block of a slice may hold fewer)
+        for (int strip = sb * kWarps * D.strips_per_warp + warp, rs = 0;
+             rs < D.strips_per_warp && strip < D.n_strips; ++rs, strip += kWarps) {
+            // lanes of tokens >= M compute a column nobody stores: they read token 0
+            const int tok = g < M ? g : 0;
+            const uint8_t *xrow = xs + (size_t)tok * D.xstride;
+            const int ra = strip * 16 + g, rb = ra + 8;
+            const bool va = ra < D.N, vb = rb < D.N;
+            // where the slice's first scale of each row sits in its aligned word
+            // (the same in every stage: a stage advances 8 bytes)
+            const uint32_t offA =
+                (uint32_t)(((uintptr_t)(D.scales + (size_t)(va ? ra : 0) * D.G + g0)) >> 1) & 1u;
+            const uint32_t offB =
+                (uint32_t)(((uintptr_t)(D.scales + (size_t)(vb ? rb : 0) * D.G + g0)) >> 1) & 1u;
+            const uint32_t shA = 16u * offA, shB = 16u * offB;
+            const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < nst; ++j) {
+                const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
+                    if (lane == 0) {
+                        atomicOr(P.status, kErrMmaWait);
+                        abort_flag = 1;  // the other warps stop at their next unit
+                    }
+                    dead = true;
+                    break;
                 }
-                dead = true;
-                break;
+                // this lane's part of the stage: 16 bytes of rows g and g + 8 of
+                // each group (read just before the group), the metadata of both rows
+                const uint8_t *st = wring + slot * kStageBytes;
+                const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
+                const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
+                const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
+                // zero nibbles of the stage's groups: the stage starts at group
+                // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
+                const uint32_t zsh = ((g0 + j * kStageGroups) & 4) ? 16u : 0u;
+                const uint32_t zwA = ma.w >> zsh, zwB = mb.w >> zsh;
+                const uint32_t mA[3] = {ma.x, ma.y, ma.z}, mB[3] = {mb.x, mb.y, mb.z};
+                const int n_in = min(kStageGroups, ng - j * kStageGroups);
+                const uint8_t *xg = xrow + (size_t)j * (kStageGroups * 256);
+                const float *sg = sums + (j * kStageGroups) * 8 + 2 * c;  // tokens 2c, 2c+1
+                // one group of the stage
+                auto group = [&](const int i) {
+                    // scales of rows ra and rb: half (off + i) of the words
+                    uint32_t hA, hB;
+                    if (i & 1) {
+                        hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
+                        hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
+                    } else {
+                        hA = mA[i >> 1] >> shA;
+                        hB = mB[i >> 1] >> shB;
+                    }
+                    const float sA = __half2float(__ushort_as_half((unsigned short)hA));
+                    const float sB = __half2float(__ushort_as_half((unsigned short)hB));
+                    // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
+                    const float zA =
+                        __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
+                    const float zB =
+                        __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
+                    const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);  // S * 2^-20
+                    const uint8_t *xi = xg + i * 256;
+                    uint4 xv[4];
+                    xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
+                    xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
+                    xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
+                    xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
+                    const uint4 wa = *reinterpret_cast<const uint4 *>(stA + i * 1024);
+                    const uint4 wb = *reinterpret_cast<const uint4 *>(stB + i * 1024);
+                    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+                    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+                    float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const uint32_t a = wA[uu], b = wB[uu], a8 = a >> 8, b8 = b >> 8;
+                        mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
+                                 b8 & 0x000f000fu, xv[uu].x, xv[uu].y);
+                        mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
+                                 b8 & 0x00f000f0u, xv[uu].z, xv[uu].w);
+                    }
+                    // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
+                    acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
+                    acc[1] = fmaf(sA, fmaf(-zA, sx.y, fmaf(16.f, dl[1], dh[1])), acc[1]);
+                    acc[2] = fmaf(sB, fmaf(-zB, sx.x, fmaf(16.f, dl[2], dh[2])), acc[2]);
+                    acc[3] = fmaf(sB, fmaf(-zB, sx.y, fmaf(16.f, dl[3], dh[3])), acc[3]);
+                };
+                if (n_in == kStageGroups) {
+    #pragma unroll
+                    for (int i = 0; i < kStageGroups; ++i) group(i);
+                } else {  // the last stage of a slice that ends at K
+    #pragma unroll
+                    for (int i = 0; i < kStageGroups; ++i)
+                        if (i < n_in) group(i);
+                }
+                // Refill the slot kDepth stages ahead once every lane is done with
+                // it.  The lanes read it through the generic proxy and the box
+                // lands through the async proxy: the proxy fence orders those
+                // reads before the new box's writes.
+                __syncwarp();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                ++t_cons;
+                issue_next();
             }
-            // this lane's part of the stage: 16 bytes of rows g and g + 8 of
-            // each group (read just before the group), the metadata of both rows
-            const uint8_t *st = wring + slot * kStageBytes;
-            const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
-            const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
-            const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
-            // zero nibbles of the stage's groups: the stage starts at group
-            // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
-            const uint32_t zsh = ((g0 + j * kStageGroups) & 4) ? 16u : 0u;
-            const uint32_t zwA = ma.w >> zsh, zwB = mb.w >> zsh;
-            const uint32_t mA[3] = {ma.x, ma.y, ma.z}, mB[3] = {mb.x, mb.y, mb.z};
-            const int n_in = min(kStageGroups, ng - j * kStageGroups);
-            const uint8_t *xg = xrow + (size_t)j * (kStageGroups * 256);
-            const float *sg = sums + (j * kStageGroups) * 8 + 2 * c;  // tokens 2c, 2c+1
-            // one group of the stage
-            auto group = [&](const int i) {
-                // scales of rows ra and rb: half (off + i) of the words
-                uint32_t hA, hB;
-                if (i & 1) {
-                    hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
-                    hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
-                } else {
-                    hA = mA[i >> 1] >> shA;
-                    hB = mB[i >> 1] >> shB;
-                }
-                const float sA = __half2float(__ushort_as_half((unsigned short)hA));
-                const float sB = __half2float(__ushort_as_half((unsigned short)hB));
-                // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
-                const float zA =
-                    __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
-                const float zB =
-                    __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
-                const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);  // S * 2^-20
-                const uint8_t *xi = xg + i * 256;
-                uint4 xv[4];
-                xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
-                xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
-                xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
-                xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
-                const uint4 wa = *reinterpret_cast<const uint4 *>(stA + i * 1024);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(stB + i * 1024);
-                const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-                const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-                float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const uint32_t a = wA[uu], b = wB[uu], a8 = a >> 8, b8 = b >> 8;
-                    mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
-                             b8 & 0x000f000fu, xv[uu].x, xv[uu].y);
-                    mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
-                             b8 & 0x00f000f0u, xv[uu].z, xv[uu].w);
-                }
-                // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
-                acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
-                acc[1] = fmaf(sA, fmaf(-zA, sx.y, fmaf(16.f, dl[1], dh[1])), acc[1]);
-                acc[2] = fmaf(sB, fmaf(-zB, sx.x, fmaf(16.f, dl[2], dh[2])), acc[2]);
-                acc[3] = fmaf(sB, fmaf(-zB, sx.y, fmaf(16.f, dl[3], dh[3])), acc[3]);
-            };
-            if (n_in == kStageGroups) {
-#pragma unroll
-                for (int i = 0; i < kStageGroups; ++i) group(i);
-            } else {  // the last stage of a slice that ends at K
-#pragma unroll
-                for (int i = 0; i < kStageGroups; ++i)
-                    if (i < n_in) group(i);
-            }
-            // Refill the slot kDepth stages ahead once every lane is done with
-            // it.  The lanes read it through the generic proxy and the box
-            // lands through the async proxy: the proxy fence orders those
-            // reads before the new box's writes.
-            __syncwarp();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            ++t_cons;
-            issue_next();
-        }
-        if (dead) break;
+            if (dead) break;
 
-        // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
-        const int t0 = 2 * c, t1 = 2 * c + 1;
-        if (D.S == 1) {
-            if (va && t0 < M) D.y[(size_t)t0 * D.N + ra] = __float2half_rn(acc[0]);
-            if (va && t1 < M) D.y[(size_t)t1 * D.N + ra] = __float2half_rn(acc[1]);
-            if (vb && t0 < M) D.y[(size_t)t0 * D.N + rb] = __float2half_rn(acc[2]);
-            if (vb && t1 < M) D.y[(size_t)t1 * D.N + rb] = __float2half_rn(acc[3]);
-            continue;
-        }
-        float *part = D.partials + (size_t)slice * M * D.N;
-        if (va && t0 < M) part[(size_t)t0 * D.N + ra] = acc[0];
-        if (va && t1 < M) part[(size_t)t1 * D.N + ra] = acc[1];
-        if (vb && t0 < M) part[(size_t)t0 * D.N + rb] = acc[2];
-        if (vb && t1 < M) part[(size_t)t1 * D.N + rb] = acc[3];
-        // count this slice's arrival for the strip with one release-acquire
-        // atomic after a warp barrier (the barrier orders the other lanes'
-        // partial writes before it); the warp that arrives last sums the
-        // slices in slice order.  No warp waits for another.
-        __syncwarp();
-        unsigned prev = 0;
-        if (lane == 0)
-            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                         : "=r"(prev)
-                         : "l"(D.counters + strip)
-                         : "memory");
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        __syncwarp();  // the other lanes' reads below come after lane 0's acquire
-        if (prev == (unsigned)(D.S - 1)) {
-            const int rows[2] = {ra, rb};
-            const bool ok[2] = {va, vb};
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 2 * c + e;
-                    if (ok[hh] && t < M) {
-                        float sum = 0.f;
-                        for (int s2 = 0; s2 < D.S; ++s2)
-                            sum += __ldcg(D.partials + ((size_t)s2 * M + t) * D.N + rows[hh]);
-                        D.y[(size_t)t * D.N + rows[hh]] = __float2half_rn(sum);
+            // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
+    #pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
+            const int t0 = 2 * c, t1 = 2 * c + 1;
+            if (D.S == 1) {
+                if (va && t0 < M) D.y[(size_t)t0 * D.N + ra] = __float2half_rn(acc[0]);
+                if (va && t1 < M) D.y[(size_t)t1 * D.N + ra] = __float2half_rn(acc[1]);
+                if (vb && t0 < M) D.y[(size_t)t0 * D.N + rb] = __float2half_rn(acc[2]);
+                if (vb && t1 < M) D.y[(size_t)t1 * D.N + rb] = __float2half_rn(acc[3]);
+                continue;
+            }
+            float *part = D.partials + (size_t)slice * M * D.N;
+            if (va && t0 < M) part[(size_t)t0 * D.N + ra] = acc[0];
+            if (va && t1 < M) part[(size_t)t1 * D.N + ra] = acc[1];
+            if (vb && t0 < M) part[(size_t)t0 * D.N + rb] = acc[2];
+            if (vb && t1 < M) part[(size_t)t1 * D.N + rb] = acc[3];
+            // count this slice's arrival for the strip with one release-acquire
+            // atomic after a warp barrier (the barrier orders the other lanes'
+            // partial writes before it); the warp that arrives last sums the
+            // slices in slice order.  No warp waits for another.
+            __syncwarp();
+            unsigned prev = 0;
+            if (lane == 0)
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(prev)
+                             : "l"(D.counters + strip)
+                             : "memory");
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            __syncwarp();  // the other lanes' reads below come after lane 0's acquire
+            if (prev == (unsigned)(D.S - 1)) {
+                const int rows[2] = {ra, rb};
+                const bool ok[2] = {va, vb};
+    #pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 2 * c + e;
+                        if (ok[hh] && t < M) {
+                            float sum = 0.f;
+                            for (int s2 = 0; s2 < D.S; ++s2)
+                                sum += __ldcg(D.partials + ((size_t)s2 * M + t) * D.N + rows[hh]);
+                            D.y[(size_t)t * D.N + rows[hh]] = __float2half_rn(sum);
+                        }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) D.counters[strip] = 0u;  // ready for the next launch
             }
-            __syncwarp();
-            if (lane == 0) D.counters[strip] = 0u;  // ready for the next launch
         }
+        if (dead) break;
     }
 
     if (dead) {
@@ -620,7 +642,8 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.M = M;
     const int G = K / kGroup;
     pl.n_strips = (N + 15) / 16;
-    pl.n_blocks = (pl.n_strips + kWarps - 1) / kWarps;
+    pl.strips_per_warp = split == 2 ? kRoundStripsPerWarp : 1;
+    pl.n_blocks = (pl.n_strips + kWarps * pl.strips_per_warp - 1) / (kWarps * pl.strips_per_warp);
     // largest slice (a whole number of stages) whose staged x and sums fit
     const int budget = kSmemPerCta - kRingBytes - kBarBytes;
     int max_groups = (budget - 16 * M) / (kGroup * 2 * M + 32);
@@ -709,6 +732,7 @@ cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partia
     d->S = plan.S;
     d->slice_groups = plan.slice_groups;
     d->n_strips = plan.n_strips;
+    d->strips_per_warp = plan.strips_per_warp;
     d->n_blocks = plan.n_blocks;
     d->unit_start = unit_start;
     d->xstride = xstride_for(plan.slice_groups);
