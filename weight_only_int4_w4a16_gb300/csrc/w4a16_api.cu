@@ -151,7 +151,7 @@ bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t 
     if (is_mma(rung)) {
         MmaPlan p = plan_mma(Mt, N, K, split_rule(rung), dev);
         *bytes = p.ws_bytes;
-        *counters = p.S > 1 ? p.n_strips : 0;
+        *counters = p.S > 1 ? p.n_blocks : 0;
         return p.ok;
     }
     GemvPlan p = plan_gemv(Mt, N, K, split_rule(rung), dev);
@@ -175,7 +175,7 @@ size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *
             return 0;
         }
         if (b > need) need = b;
-        if (c > kCounters) *status = W4A16_ERR_WORKSPACE;
+        if (c > kCounters - kMmaSchedWords) *status = W4A16_ERR_WORKSPACE;
     }
     return need;
 }
@@ -281,7 +281,7 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
             part = st.ws.partials + partial_floats;
             partial_floats += ((size_t)p.S * M * d.N + 63) / 64 * 64;
             cnt = st.ws.counters + counters;
-            counters += p.n_strips;
+            counters += p.n_blocks;
         }
         int wait_for = -1;
         for (int j = l - 1; j >= 0 && wait_for < 0; --j) {
@@ -301,12 +301,12 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
         if (p.smem_bytes > smem) smem = p.smem_bytes;
     }
     if (partial_floats * sizeof(float) > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
-    if (counters + (waits ? n + 1 : 0) > st.ws.n_counters) return W4A16_ERR_WORKSPACE;
+    if (counters + (waits ? n : 0) > st.ws.n_counters - kMmaSchedWords) return W4A16_ERR_WORKSPACE;
     fr->round.n = n;
     fr->round.total_units = units;
     fr->round.smem_bytes = smem;
     fr->round.done = waits ? st.ws.counters + counters : nullptr;
-    fr->counters_used = counters + (waits ? n + 1 : 0);
+    fr->counters_used = counters + (waits ? n : 0);
     return W4A16_OK;
 }
 
@@ -526,7 +526,7 @@ int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M,
     if (fused) {
         // the graph owns its descriptors and completion counters
         const size_t dbytes = fr.descs.size() * sizeof(MmaLinDesc);
-        const size_t cbytes = fr.round.done ? (size_t)(n_descs + 1) * sizeof(unsigned) : 0;
+        const size_t cbytes = fr.round.done ? (size_t)n_descs * sizeof(unsigned) : 0;
         e = cudaMalloc(&hd->buffer, dbytes + cbytes);
         if (e == cudaSuccess)
             e = cudaMemcpy(hd->buffer, fr.descs.data(), dbytes, cudaMemcpyHostToDevice);

@@ -129,8 +129,12 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
                        cudaStream_t stream);
 
 // A fused round: n linears in one launch, their units in order.  done points
-// at n + 1 zeroed counters when some linear waits for another (else null);
-// the kernel leaves them zeroed again.
+// at n zeroed counters when some linear waits for another (else null); the
+// kernel leaves them zeroed again.
+// The mma kernels take their scheduling counters from the last
+// kMmaSchedWords words of the workspace counters.
+constexpr int kMmaSchedWords = 2;
+
 struct MmaRound {
     const MmaLinDesc *descs;  // device array of n descriptors
     int n;

@@ -70,7 +70,7 @@ constexpr int kStageW = kStageGroups * 16 * 64;  // 4 KB of weights
 constexpr int kStageMeta = 16 * 16;             // per row: 3 scale words, 1 zeros word
 constexpr int kStageBytes = kStageW + kStageMeta;
 constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
-constexpr int kBarBytes = kWarps * kDepth * 8 + 16;  // ring barriers, then a CTA flag
+constexpr int kBarBytes = kWarps * kDepth * 8 + 64;  // ring barriers, then 16 flag ints
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
 constexpr int kRoundStripsPerWarp = 4;  // fused rounds: strips per warp and unit
@@ -168,7 +168,8 @@ __device__ __forceinline__ uint4 mma_pair_order(uint4 v) {
 struct MmaKernelParams {
     MmaLinDesc single;         // the linear of a one-linear launch
     const MmaLinDesc *descs;   // fused round: device array of n_lin linears
-    unsigned *done;            // fused round with waits: n_lin + 1 counters, else null
+    unsigned *done;            // fused round with waits: n_lin completion counters, else null
+    unsigned *sched;           // 2 zeroed words: next dynamic unit, CTAs finished
     int *status;
     int n_lin;
     int total_units;
@@ -188,6 +189,39 @@ __device__ __forceinline__ bool wait_counter(const unsigned *p, unsigned target)
     }
 }
 
+__device__ __forceinline__ int ld_acquire_cta(const int *p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(dev::smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta(int *p, int v) {
+    asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(dev::smem_u32(p)), "r"(v) : "memory");
+}
+
+// Ints of the CTA's flag area in shared memory
+constexpr int kFlagAbort = 0;   // a wait expired: the CTA's warps stop at their next unit
+constexpr int kFlagQKnown = 1;  // highest sequence index whose unit is in the queue
+constexpr int kFlagRed = 2;     // this CTA reduces the block (kFlagRedL, kFlagRedSb)
+constexpr int kFlagRedL = 3;
+constexpr int kFlagRedSb = 4;
+constexpr int kFlagQueue = 8;   // 8 ints: the CTA's units by sequence index (mod 8)
+constexpr int kQueueAhead = 5;  // units fetched ahead of the one being consumed
+
+// y = the sum of the S partial slices of block sb of a linear, by the whole CTA
+__device__ __forceinline__ void reduce_block(const MmaLinDesc &R, int sb) {
+    const int rows_per_block = kWarps * R.strips_per_warp * 16;
+    const int row0 = sb * rows_per_block;
+    const int nrows = min(R.N - row0, rows_per_block);
+    for (int i = threadIdx.x; i < R.M * nrows; i += kThreads) {
+        const int t = i / nrows, row = row0 + i - t * nrows;
+        float sum = 0.f;
+        for (int s2 = 0; s2 < R.S; ++s2)
+            sum += __ldcg(R.partials + ((size_t)s2 * R.M + t) * R.N + row);
+        R.y[(size_t)t * R.N + row] = __float2half_rn(sum);
+    }
+    if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
+}
+
 template <bool kRound>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mma_kernel(const __grid_constant__ MmaKernelParams P) {
@@ -196,8 +230,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int g = lane >> 2, c = lane & 3;
     uint8_t *wring = smem + (size_t)warp * kDepth * kStageBytes;  // this warp's two slots
     uint8_t *xs = smem + kRingBytes + kBarBytes;                   // staged x, then the sums
-    // set when a wait expired: the CTA's warps stop at their next unit
-    volatile int &abort_flag = *reinterpret_cast<int *>(smem + kRingBytes + kBarBytes - 16);
+    int *flags = reinterpret_cast<int *>(smem + kRingBytes + kWarps * kDepth * 8);
+    volatile int *vflags = flags;
+    volatile int *unit_q = flags + kFlagQueue;
     // the next kernel in the stream may be scheduled as SMs free up; it waits
     // for this grid to finish before it touches anything this grid writes
     grid_dependents_launch();
@@ -213,8 +248,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int s = 0; s < kDepth; ++s) mbar_init(bar0 + 8 * s, 1 + 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (threadIdx.x == 0) abort_flag = 0;
-    __syncwarp();
+    if (threadIdx.x == 0) {
+        // the CTA's first two units are fixed; the rest come from a counter
+        vflags[kFlagAbort] = 0;
+        vflags[kFlagRed] = 0;
+        unit_q[0] = blockIdx.x;
+        unit_q[1] = blockIdx.x + grid < total ? blockIdx.x + grid : total;
+        vflags[kFlagQKnown] = 1;
+    }
+    __syncthreads();
 
     // ---- copy stream.  The issue cursor walks this warp's stages (unit by
     // unit, linear by linear) kDepth stages ahead of the consume cursor.
@@ -225,8 +267,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // (h = 1): the three aligned words that hold the stage's four (2-byte
     // aligned) scales, and the zeros word of its groups.
     const int r = lane & 15, h = lane >> 4;
-    int iu = blockIdx.x, il = 0;  // unit and linear of the issue cursor
-    int ij = 0, inst = 0;         // stage within the unit, stages of the unit
+    int ik = 0, il = 0;           // sequence index of the issue cursor's unit, its linear
+    int ij = 0, inst = 0;         // stage within the strip, stages per strip
+    bool i_wait = false;          // the next unit is not in the queue yet
+    bool i_done = false;          // no units left
     unsigned t_iss = 0;           // stages issued by this warp
     uint64_t i_map = 0;           // tensor map of the unit's linear
     int i_g0 = 0, i_row16 = 0;    // first group of the slice, first row of the strip
@@ -252,11 +296,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         is_zbytes = vr ? 4u : 0u;
         ij = 0;
     };
-    // move the issue cursor to the first unit at or after iu in which this
-    // warp has a strip (warp 0 always has one: it also asks L2 for the unit's
-    // slice of x)
+    // move the issue cursor to the first unit, at or after sequence index ik,
+    // in which this warp has a strip (warp 0 always has one: it also asks L2
+    // for the unit's slice of x); stop at a unit the queue does not hold yet
     auto i_enter = [&]() {
-        for (; iu < total; iu += grid) {
+        for (;; ++ik) {
+            if (ik > ld_acquire_cta(flags + kFlagQKnown)) {
+                i_wait = true;
+                return;
+            }
+            i_wait = false;
+            const int iu = unit_q[ik & 7];
+            if (iu >= total) {
+                i_done = true;
+                return;
+            }
             if (kRound)
                 while (il + 1 < P.n_lin && iu >= P.descs[il + 1].unit_start) ++il;
             const MmaLinDesc &D = desc(il);
@@ -283,7 +337,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
     };
     auto issue_next = [&]() {
-        if (iu >= total) return;
+        if (i_done) return;
+        if (i_wait) {
+            i_enter();
+            if (i_wait || i_done) return;
+        }
         const uint32_t slot = t_iss & 1u;  // kDepth == 2
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t dst = ring0 + slot * kStageBytes;
@@ -316,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 i_strip += kWarps;
                 i_strip_enter();
             } else {
-                iu += grid;
+                ++ik;
                 i_enter();
             }
         }
@@ -327,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kDepth; ++s) issue_next();
 
     // ---- from here on: activations, outputs, the split-K workspace and the
-    // completion counters may belong to the preceding kernel
+    // counters may belong to the preceding kernel
     grid_dependency_wait();
 
     // unit of word u of this lane's chunk in a group: x_unit(4c + u)
@@ -338,8 +396,78 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int passed = 0;       // linears below this one are counted in P.done
     int staged_l = -1, staged_slice = -1;  // the (linear, slice) whose x is staged
     bool dead = false;
+    // split K, one arrival per unit and CTA: the CTA that brings the last
+    // slice of a block reduces it.  Thread 0 counts the arrival of the
+    // previous unit at a unit boundary and reads the count's result at the
+    // next boundary, so the atomic's latency hides behind a unit of work.
+    int arr_l = -1, arr_sb = 0;  // split unit whose arrival is still to count
+    int red_l = -1, red_sb = 0;  // arrival counted, its result in red_prev (thread 0)
+    unsigned red_prev = 0;
+    unsigned fetched = 0;        // thread 0: counter value for sequence index k + kQueueAhead + 1
+    if (threadIdx.x == 0) {
+        const unsigned f = atomicAdd(P.sched, 4u);
+        for (int i = 0; i < 4; ++i) {
+            const unsigned u = 2u * grid + f + i;
+            unit_q[2 + i] = u < (unsigned)total ? (int)u : total;
+        }
+        st_release_cta(flags + kFlagQKnown, kQueueAhead);
+        fetched = atomicAdd(P.sched, 1u);
+    }
+    // thread 0: publish whether this CTA reduces the block whose arrival it
+    // counted (the result is read here, a unit after the atomic), into the
+    // flag slot of the boundary that reads it (two slots by parity: a slot is
+    // rewritten only after every warp has passed the barrier after its read)
+    auto publish_reduction = [&](int boundary) {
+        if (threadIdx.x != 0) return;
+        volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
+        f[0] = red_l >= 0 && red_prev == (unsigned)(desc(red_l).S - 1);
+        f[1] = red_l;
+        f[2] = red_sb;
+        red_l = -1;
+    };
+    // thread 0: count the arrival of the pending split unit (all warps have
+    // stored their partials: call after a CTA barrier)
+    auto count_arrival = [&]() {
+        if (threadIdx.x != 0 || arr_l < 0) return;
+        unsigned prev;
+        asm volatile("fence.acq_rel.gpu;\n\tatom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(desc(arr_l).counters + arr_sb)
+                     : "memory");
+        red_prev = prev;
+        red_l = arr_l;
+        red_sb = arr_sb;
+        arr_l = -1;
+    };
+    // all threads, after the barrier that follows publish_reduction(boundary)
+    auto maybe_reduce = [&](int boundary) {
+        volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
+        if (f[0]) reduce_block(desc(f[1]), f[2]);
+    };
 
-    for (int u = blockIdx.x; u < total; u += grid) {
+    // boundary b: the barrier at the top of iteration b (b = k), or an extra
+    // one inside it (b = k + 1 ... ); `bnd` counts them
+    int bnd = 0;
+    for (int k = 0;; ++k) {
+        if (threadIdx.x == 0) {
+            publish_reduction(bnd);
+            if (k >= 1) {
+                // the unit fetched at the previous boundary joins the queue
+                const unsigned u = 2u * grid + fetched;
+                unit_q[(k + kQueueAhead) & 7] = u < (unsigned)total ? (int)u : total;
+                st_release_cta(flags + kFlagQKnown, k + kQueueAhead);
+                fetched = atomicAdd(P.sched, 1u);
+            }
+        }
+        __syncthreads();  // the previous unit's staged x is no longer read
+        if (vflags[kFlagAbort]) {
+            dead = true;
+            break;
+        }
+        maybe_reduce(bnd++);
+        const int u = unit_q[k & 7];
+        if (u >= total) break;
+        count_arrival();
         if (kRound)
             while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
         const MmaLinDesc &D = desc(cl);
@@ -349,39 +477,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int g0 = slice * D.slice_groups;  // a multiple of kStageGroups
         const int ng = min(D.G, g0 + D.slice_groups) - g0;
         const int nst = (ng + kStageGroups - 1) / kStageGroups;
-
         float *sums = reinterpret_cast<float *>(xs + (size_t)M * D.xstride);  // [group][8]
-        if (cl == staged_l && slice == staged_slice) goto staged;  // same x as the last unit
-        __syncthreads();  // the previous unit's staged x is no longer read
-        if (abort_flag) {
-            dead = true;
-            break;
-        }
-        if (kRound && P.done) {
+
+        if (kRound && P.done && passed < cl) {
+            // A new linear.  Settle this CTA's pending split arrival now (its
+            // linear may be one that others wait for), count the linears this
+            // CTA is done with, then wait for the linear this one depends on.
+            publish_reduction(bnd);
+            __syncthreads();
+            maybe_reduce(bnd++);
+            __syncthreads();
             if (threadIdx.x == 0) {
-                // this CTA has finished every unit of the linears below cl
-                if (passed < cl) {
-                    __threadfence();
-                    for (; passed < cl; ++passed) atomicAdd(P.done + passed, 1u);
-                }
+                __threadfence();
+                for (; passed < cl; ++passed) atomicAdd(P.done + passed, 1u);
                 if (D.wait_for >= 0 && !wait_counter(P.done + D.wait_for, (unsigned)grid)) {
                     atomicOr(P.status, kErrMmaDep);
-                    abort_flag = 1;
+                    vflags[kFlagAbort] = 1;
                 }
             }
             __syncthreads();
-            if (abort_flag) {
+            if (vflags[kFlagAbort]) {
                 dead = true;
                 break;
             }
         }
-
-        // ---- stage x[:, slice] in MMA pair order, and each (group, token)'s
-        // sum S of x (kept as S * 2^-20): the 16 lanes of a half warp hold the
-        // 16 units of one group of one token and add theirs with shuffles
-        {
-            // kXBatch loads in flight per thread: the staging costs a few L2
-            // round trips instead of one per unit of x
+        if (cl != staged_l || slice != staged_slice) {
+            // ---- stage x[:, slice] in MMA pair order, and each (group,
+            // token)'s sum S of x (kept as S * 2^-20): the 16 lanes of a half
+            // warp hold the 16 units of one group of one token and add theirs
+            // with shuffles.  kXBatch loads in flight per thread: a few L2
+            // round trips instead of one per unit of x.
             constexpr int kXBatch = 8;
             const int nunits = ng * (kGroup / 8);
             const int xtotal = M * nunits;  // a multiple of 16
@@ -419,11 +544,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // tokens M..7 have no x: their sums are zero
             for (int i = threadIdx.x; i < ng * (8 - M); i += kThreads)
                 sums[(i / (8 - M)) * 8 + M + i % (8 - M)] = 0.f;
+            __syncthreads();
+            staged_l = cl;
+            staged_slice = slice;
         }
-        __syncthreads();
-        staged_l = cl;
-        staged_slice = slice;
-    staged:
         // this warp's strips of the unit: strip0, strip0 + 8, ... (the tail
         // block of a slice may hold fewer)
         for (int strip = sb * kWarps * D.strips_per_warp + warp, rs = 0;
@@ -443,11 +567,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int j = 0; j < nst; ++j) {
+                // the issue cursor may have stopped at a unit the queue did not
+                // hold yet: this stage belongs to a unit it holds
+                if (t_iss == t_cons) issue_next();
                 const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
                 if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
                     if (lane == 0) {
                         atomicOr(P.status, kErrMmaWait);
-                        abort_flag = 1;  // the other warps stop at their next unit
+                        vflags[kFlagAbort] = 1;  // the other warps stop at their next unit
                     }
                     dead = true;
                     break;
@@ -545,41 +672,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (va && t1 < M) part[(size_t)t1 * D.N + ra] = acc[1];
             if (vb && t0 < M) part[(size_t)t0 * D.N + rb] = acc[2];
             if (vb && t1 < M) part[(size_t)t1 * D.N + rb] = acc[3];
-            // count this slice's arrival for the strip with one release-acquire
-            // atomic after a warp barrier (the barrier orders the other lanes'
-            // partial writes before it); the warp that arrives last sums the
-            // slices in slice order.  No warp waits for another.
-            __syncwarp();
-            unsigned prev = 0;
-            if (lane == 0)
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                             : "=r"(prev)
-                             : "l"(D.counters + strip)
-                             : "memory");
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            __syncwarp();  // the other lanes' reads below come after lane 0's acquire
-            if (prev == (unsigned)(D.S - 1)) {
-                const int rows[2] = {ra, rb};
-                const bool ok[2] = {va, vb};
-    #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-    #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 2 * c + e;
-                        if (ok[hh] && t < M) {
-                            float sum = 0.f;
-                            for (int s2 = 0; s2 < D.S; ++s2)
-                                sum += __ldcg(D.partials + ((size_t)s2 * M + t) * D.N + rows[hh]);
-                            D.y[(size_t)t * D.N + rows[hh]] = __float2half_rn(sum);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) D.counters[strip] = 0u;  // ready for the next launch
-            }
         }
         if (dead) break;
+        if (D.S > 1) {  // count this unit's arrival at the next boundary
+            arr_l = cl;
+            arr_sb = sb;
+        }
     }
+
 
     if (dead) {
         // a wait expired: let this warp's copies in flight land (bounded)
@@ -589,17 +689,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         return;
     }
     cp_wait_all();
-    if (kRound && P.done) {
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
+    // split K still pending: the decision on the arrival counted at the last
+    // boundary, then the arrival of the last unit
+    publish_reduction(bnd);
+    __syncthreads();
+    maybe_reduce(bnd++);
+    count_arrival();
+    publish_reduction(bnd);
+    __syncthreads();
+    maybe_reduce(bnd++);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (kRound && P.done)
             for (; passed < P.n_lin; ++passed) atomicAdd(P.done + passed, 1u);
-            // the last CTA out leaves the counters zeroed for the next launch
-            const unsigned prev = atomicAdd(P.done + P.n_lin, 1u);
-            if (prev == (unsigned)grid - 1) {
-                __threadfence();
-                for (int l = 0; l <= P.n_lin; ++l) P.done[l] = 0u;
-            }
+        // the last CTA out leaves the counters zeroed for the next launch
+        const unsigned prev = atomicAdd(P.sched + 1, 1u);
+        if (prev == (unsigned)grid - 1) {
+            __threadfence();
+            P.sched[0] = 0u;
+            P.sched[1] = 0u;
+            if (kRound && P.done)
+                for (int l = 0; l < P.n_lin; ++l) P.done[l] = 0u;
         }
     }
 }
@@ -747,6 +858,7 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     cudaError_t e = mma_describe(a, plan, ws.partials, ws.counters, 0, -1, &P.single);
     if (e != cudaSuccess) return e;
     P.status = ws.status;
+    P.sched = ws.counters + ws.n_counters - kMmaSchedWords;
     P.n_lin = 1;
     P.total_units = plan.units;
     cudaLaunchAttribute attr[1];
@@ -761,6 +873,7 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
     P.descs = r.descs;
     P.done = r.done;
     P.status = ws.status;
+    P.sched = ws.counters + ws.n_counters - kMmaSchedWords;
     P.n_lin = r.n;
     P.total_units = r.total_units;
     int grid = mma_round_grid(dev);
