@@ -171,6 +171,25 @@ int w4a16_round_graph_launch(void *graph, void *stream);
 /* Destroy a captured round (after its last replay has finished). */
 int w4a16_round_graph_destroy(void *graph);
 
+/* y = x @ W^T like w4a16_linear, for M <= 8 on the warp-MMA rungs, with no
+ * allocation and no w4a16_init: the pages have no counterpart; this serves
+ * callers that cannot allocate device memory (a process whose memory a
+ * caching allocator has wholly reserved, a serving loop that must not call
+ * cudaMalloc, which synchronises the device).  Its split-K scratch is a
+ * statically sized device array of the library (2 MiB of fp32 partial sums and
+ * 4096 block counters): shapes whose split needs more return
+ * W4A16_ERR_WORKSPACE before anything is launched; M > 8 returns
+ * W4A16_ERR_UNSUPPORTED.  The first call on a device (the current device at
+ * the call) sets up that device: it looks up the scratch's device address,
+ * zeroes its counters and sets the kernel attributes; make that first call
+ * before any stream capture.  Every call shares the one scratch array: calls
+ * that overlap on the GPU race on it.  Bounded-wait errors of its kernel are
+ * recorded in the scratch, not in the word w4a16_device_status reads.
+ * Argument rules as for w4a16_linear. */
+int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                         const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
+                         void *stream);
+
 /* The rung the dispatch table picks for a shape (honouring a forced rung), or
  * -1 for an invalid shape.  Pure host query. */
 int w4a16_select_rung(int M, int N, int K, int group);

@@ -68,6 +68,7 @@ _sig("w4a16_pack", [_P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_unpack", [_P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_dequant", [_P, _P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -84,7 +85,8 @@ _sig("w4a16_last_cuda_error", [])
 _sig("w4a16_device_sm_count", [])
 
 EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
-            "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_decode_round",
+            "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_linear_noalloc",
+            "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
             "w4a16_probe_reset", "w4a16_kernel_launches", "w4a16_rung_name", "w4a16_status_string",
@@ -192,6 +194,22 @@ def w4a16_linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
                             _dev(scales, torch.float16, "scales"), _dev(zeros, torch.int32, "zeros"),
                             M, N, K, group, _dev(y, torch.float16, "y"), _stream_ptr(stream)),
            "w4a16_linear")
+    return y
+
+
+def w4a16_linear_noalloc(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                         zeros: torch.Tensor, y: torch.Tensor, group: int = GROUP,
+                         stream=None) -> torch.Tensor:
+    """w4a16_linear for M <= 8 that allocates nothing (y must be given) and needs
+    no w4a16_init: its split-K scratch is static device memory of the library."""
+    M, K = x.shape
+    N = qweight.shape[0]
+    _check(lib.w4a16_linear_noalloc(_dev(x, torch.float16, "x"),
+                                    _dev(qweight, torch.int32, "qweight"),
+                                    _dev(scales, torch.float16, "scales"),
+                                    _dev(zeros, torch.int32, "zeros"), M, N, K, group,
+                                    _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+           "w4a16_linear_noalloc")
     return y
 
 

@@ -55,6 +55,9 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <mutex>
+
+#include "../../include/w4a16.h"
 #include "w4a16_device.cuh"
 #include "w4a16_internal.h"
 
@@ -913,3 +916,101 @@ cudaError_t mma_init(const DeviceInfo &dev) {
 }
 
 }  // namespace w4a16
+
+// ---- allocation-free entry point ------------------------------------------
+// Callers that cannot allocate device memory: a process whose device memory
+// is wholly reserved by its own caching allocator, or a serving loop that must
+// not call cudaMalloc (which synchronises the device and can fail when memory
+// is reserved).  w4a16_linear_noalloc needs neither w4a16_init nor any
+// allocation: its split-K scratch is this statically sized device array.
+namespace {
+constexpr size_t kNoAllocPartialFloats = size_t(1) << 19;  // 2 MB of fp32 partial sums
+constexpr int kNoAllocCounters = 4096;                      // per-block arrival counters
+// partials, then the counters, the kernel's scheduling words and a status word
+constexpr size_t kNoAllocBytes =
+    kNoAllocPartialFloats * sizeof(float) +
+    (size_t)(kNoAllocCounters + w4a16::kMmaSchedWords + 4) * sizeof(unsigned);
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch
+    w4a16::DeviceInfo dev{};
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: the scratch's device address
+// (cudaGetSymbolAddress), zeroed counters and status, the kernel attributes.
+int noalloc_setup(int device, NoAllocDevice **out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice &d = g_noalloc[device];
+    if (!d.ready) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return (int)e;
+        unsigned char *base = (unsigned char *)ptr;
+        // the counters, scheduling words and status word must start at zero
+        // (the kernels leave them zeroed after each launch)
+        e = cudaMemset(base + kNoAllocPartialFloats * sizeof(float), 0,
+                       kNoAllocBytes - kNoAllocPartialFloats * sizeof(float));
+        w4a16::DeviceInfo info{};
+        info.device = device;
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, device);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&info.max_smem_optin,
+                                       cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+        if (e == cudaSuccess) e = w4a16::mma_init(info);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return (int)e;
+        d.scratch = base;
+        d.dev = info;
+        d.ready = true;
+    }
+    *out = &d;
+    return 0;
+}
+}  // namespace
+
+extern "C" int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight,
+                                    const uint16_t *scales, const uint32_t *zeros, int M, int N,
+                                    int K, int group, uint16_t *y, void *stream) {
+    using namespace w4a16;
+    if (!x || !qweight || !scales || !zeros || !y) return W4A16_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || K > (1 << 22) || K % kGroup != 0) return W4A16_ERR_INVALID_ARG;
+    if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+    if (M > kMmaMaxTokens) return W4A16_ERR_UNSUPPORTED;
+    if ((uintptr_t)x % 16 || (uintptr_t)qweight % 16 || (uintptr_t)y % 16 ||
+        (uintptr_t)scales % 2 || (uintptr_t)zeros % 4)
+        return W4A16_ERR_MISALIGNED;
+    const uintptr_t x0 = (uintptr_t)x, y0 = (uintptr_t)y;
+    if (x0 < y0 + (size_t)M * N * 2 && y0 < x0 + (size_t)M * K * 2) return W4A16_ERR_INVALID_ARG;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+    if (device < 0 || device >= kNoAllocMaxDevices) return W4A16_ERR_UNSUPPORTED;
+    NoAllocDevice *nd = nullptr;
+    if (noalloc_setup(device, &nd)) return W4A16_ERR_CUDA;
+    MmaPlan plan = plan_mma(M, N, K, -1, nd->dev);
+    if (!plan.ok) return W4A16_ERR_UNSUPPORTED;
+    // sizes over the scratch are rejected before anything is launched
+    if (plan.ws_bytes > kNoAllocPartialFloats * sizeof(float) ||
+        (plan.S > 1 && plan.n_blocks > kNoAllocCounters))
+        return W4A16_ERR_WORKSPACE;
+    Workspace ws{};
+    ws.partials = reinterpret_cast<float *>(nd->scratch);
+    ws.partial_bytes = kNoAllocPartialFloats * sizeof(float);
+    ws.counters = reinterpret_cast<unsigned *>(nd->scratch + kNoAllocPartialFloats * sizeof(float));
+    ws.n_counters = kNoAllocCounters + kMmaSchedWords;
+    ws.status = reinterpret_cast<int *>(ws.counters + ws.n_counters);
+    LinearArgs a{reinterpret_cast<const __half *>(x), qweight,
+                 reinterpret_cast<const __half *>(scales), zeros, reinterpret_cast<__half *>(y), M,
+                 N, K};
+    e = launch_mma(a, plan, ws, (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
