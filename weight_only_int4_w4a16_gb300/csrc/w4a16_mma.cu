@@ -208,19 +208,40 @@ constexpr int kFlagRed = 2;     // this CTA reduces the block (kFlagRedL, kFlagR
 constexpr int kFlagRedL = 3;
 constexpr int kFlagRedSb = 4;
 constexpr int kFlagQueue = 8;   // 8 ints: the CTA's units by sequence index (mod 8)
-constexpr int kQueueAhead = 5;  // units fetched ahead of the one being consumed
+constexpr int kQueueAhead = 2;  // units fetched ahead of the one being consumed
 
 // y = the sum of the S partial slices of block sb of a linear, by the whole CTA
-__device__ __forceinline__ void reduce_block(const MmaLinDesc &R, int sb) {
+__device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
     const int nrows = min(R.N - row0, rows_per_block);
-    for (int i = threadIdx.x; i < R.M * nrows; i += kThreads) {
-        const int t = i / nrows, row = row0 + i - t * nrows;
-        float sum = 0.f;
-        for (int s2 = 0; s2 < R.S; ++s2)
-            sum += __ldcg(R.partials + ((size_t)s2 * R.M + t) * R.N + row);
-        R.y[(size_t)t * R.N + row] = __float2half_rn(sum);
+    const int n_out = R.M * nrows;
+    // each thread sums up to 8 outputs at a time, the 8 loads of one slice in
+    // flight together (slices in order: the sum is the same every launch)
+    constexpr int kR = 8;
+    for (int base = 0; base < n_out; base += kThreads * kR) {
+        float sum[kR];
+        size_t off[kR];
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            const int i = base + j * kThreads + threadIdx.x;
+            const int t = i / nrows, row = row0 + i - t * nrows;
+            off[j] = i < n_out ? (size_t)t * R.N + row : 0;
+            sum[j] = 0.f;
+        }
+        for (int s2 = 0; s2 < R.S; ++s2) {
+            const float *ps = R.partials + (size_t)s2 * R.M * R.N;
+            float v[kR];
+#pragma unroll
+            for (int j = 0; j < kR; ++j) v[j] = __ldcg(ps + off[j]);
+#pragma unroll
+            for (int j = 0; j < kR; ++j) sum[j] += v[j];
+        }
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            const int i = base + j * kThreads + threadIdx.x;
+            if (i < n_out) R.y[off[j]] = __float2half_rn(sum[j]);
+        }
     }
     if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
 }
@@ -408,8 +429,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     unsigned red_prev = 0;
     unsigned fetched = 0;        // thread 0: counter value for sequence index k + kQueueAhead + 1
     if (threadIdx.x == 0) {
-        const unsigned f = atomicAdd(P.sched, 4u);
-        for (int i = 0; i < 4; ++i) {
+        // sequence indices 2 .. kQueueAhead
+        const unsigned f = atomicAdd(P.sched, (unsigned)(kQueueAhead - 1));
+        for (int i = 0; i < kQueueAhead - 1; ++i) {
             const unsigned u = 2u * grid + f + i;
             unit_q[2 + i] = u < (unsigned)total ? (int)u : total;
         }
@@ -470,7 +492,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         maybe_reduce(bnd++);
         const int u = unit_q[k & 7];
         if (u >= total) break;
-        count_arrival();
         if (kRound)
             while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
         const MmaLinDesc &D = desc(cl);
@@ -486,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             // A new linear.  Settle this CTA's pending split arrival now (its
             // linear may be one that others wait for), count the linears this
             // CTA is done with, then wait for the linear this one depends on.
+            count_arrival();
             publish_reduction(bnd);
             __syncthreads();
             maybe_reduce(bnd++);
@@ -551,6 +573,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             staged_l = cl;
             staged_slice = slice;
         }
+        // after the staging: thread 0's release fence and atomic would
+        // otherwise hold up warp 0, and with it the staging
+        count_arrival();
         // this warp's strips of the unit: strip0, strip0 + 8, ... (the tail
         // block of a slice may hold fewer)
         for (int strip = sb * kWarps * D.strips_per_warp + warp, rs = 0;
