@@ -41,6 +41,7 @@ thread_local int t_last_cuda_error = 0;
 constexpr size_t kDefaultWorkspace = 64ull << 20;
 constexpr int kCounters = 1 << 20;       // split-K arrival counters (and round completion counters)
 constexpr int kMaxRoundLinears = 4096;   // linears of one fused decode round
+constexpr int kRoundTailLinears = 24;    // a round's last linears, planned with small units
 constexpr int kMaxM = 65535;
 
 const char *const kRungNames[W4A16_NUM_RUNGS] = {"gemv", "gemv_splitk", "tc",
@@ -273,7 +274,9 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
     bool waits = false;
     for (int l = 0; l < n; ++l) {
         const w4a16_linear_desc &d = descs[l];
-        MmaPlan p = plan_mma(M, d.N, d.K, 2, st.dev);
+        // the last linears of a round come in small units: the CTAs then
+        // run out of work within a small unit of each other
+        MmaPlan p = plan_mma(M, d.N, d.K, l >= n - kRoundTailLinears ? 3 : 2, st.dev);
         if (!p.ok) return W4A16_ERR_UNSUPPORTED;
         float *part = nullptr;
         unsigned *cnt = nullptr;

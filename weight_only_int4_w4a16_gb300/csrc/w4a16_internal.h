@@ -121,7 +121,9 @@ struct MmaLinDesc {
 
 // split: 0 = never split K, 1 = split K, -1 = planner balances the warps,
 // 2 = fused rounds: fewest slices the staged activations allow, and units of
-// kRoundStripsPerWarp strips per warp (the round's units balance each other).
+// kRoundStripsPerWarp strips per warp (the round's units balance each other),
+// 3 = the same slices with one strip per warp (the round's last linears, so
+// that the CTAs finish together).
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev);
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);

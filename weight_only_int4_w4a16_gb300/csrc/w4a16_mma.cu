@@ -76,7 +76,7 @@ constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
 constexpr int kBarBytes = kWarps * kDepth * 8 + 64;  // ring barriers, then 16 flag ints
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
-constexpr int kRoundStripsPerWarp = 4;  // fused rounds: strips per warp and unit
+constexpr int kRoundStripsPerWarp = 8;  // fused rounds: strips per warp and unit
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 constexpr int kErrMmaWait = 128;  // device status bit: a ring wait expired
 constexpr int kErrMmaDep = 256;   // device status bit: a wait for an earlier linear expired
@@ -782,6 +782,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     const int G = K / kGroup;
     pl.n_strips = (N + 15) / 16;
     pl.strips_per_warp = split == 2 ? kRoundStripsPerWarp : 1;
+    if (split == 3) split = 2;  // a round's last linears: fewest slices, small units
     pl.n_blocks = (pl.n_strips + kWarps * pl.strips_per_warp - 1) / (kWarps * pl.strips_per_warp);
     // largest slice (a whole number of stages) whose staged x and sums fit
     const int budget = kSmemPerCta - kRingBytes - kBarBytes;
