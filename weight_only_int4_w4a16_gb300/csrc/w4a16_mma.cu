@@ -73,7 +73,8 @@ constexpr int kStageW = kStageGroups * 16 * 64;  // 4 KB of weights
 constexpr int kStageMeta = 16 * 16;             // per row: 3 scale words, 1 zeros word
 constexpr int kStageBytes = kStageW + kStageMeta;
 constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
-constexpr int kBarBytes = kWarps * kDepth * 8 + 64;  // ring barriers, then 16 flag ints
+// ring barriers, then 16 flag ints, then the barrier of the x copies
+constexpr int kBarBytes = kWarps * kDepth * 8 + 64 + 16;
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
 constexpr int kRoundStripsPerWarp = 8;  // fused rounds: strips per warp and unit
@@ -176,6 +177,7 @@ struct MmaKernelParams {
     int *status;
     int n_lin;
     int total_units;
+    int dynamic;  // units after the first two: 0 = every grid-th, 1 = from *sched
 };
 
 // Bounded wait until *p >= target (acquire); false once kWaitNs has passed.
@@ -208,7 +210,7 @@ constexpr int kFlagRed = 2;     // this CTA reduces the block (kFlagRedL, kFlagR
 constexpr int kFlagRedL = 3;
 constexpr int kFlagRedSb = 4;
 constexpr int kFlagQueue = 8;   // 8 ints: the CTA's units by sequence index (mod 8)
-constexpr int kQueueAhead = 2;  // units fetched ahead of the one being consumed
+constexpr int kQueueAhead = 1;  // units fetched ahead of the one being consumed
 
 // y = the sum of the S partial slices of block sb of a linear, by the whole CTA
 __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
@@ -255,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint8_t *wring = smem + (size_t)warp * kDepth * kStageBytes;  // this warp's two slots
     uint8_t *xs = smem + kRingBytes + kBarBytes;                   // staged x, then the sums
     int *flags = reinterpret_cast<int *>(smem + kRingBytes + kWarps * kDepth * 8);
+    const uint32_t x_bar = dev::smem_u32(smem + kRingBytes + kWarps * kDepth * 8 + 64);
     volatile int *vflags = flags;
     volatile int *unit_q = flags + kFlagQueue;
     // the next kernel in the stream may be scheduled as SMs free up; it waits
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // one arrival with the box's byte count, plus one per lane once its
         // metadata copies have landed
         for (int s = 0; s < kDepth; ++s) mbar_init(bar0 + 8 * s, 1 + 32);
+        if (warp == 0) mbar_init(x_bar, 1);  // the x copies: bytes only
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (threadIdx.x == 0) {
@@ -405,12 +409,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
     static_assert(kDepth == 2, "the slot and phase arithmetic assumes two slots");
     i_enter();
-#pragma unroll
-    for (int s = 0; s < kDepth; ++s) issue_next();
+    issue_next();
 
     // ---- from here on: activations, outputs, the split-K workspace and the
     // counters may belong to the preceding kernel
     grid_dependency_wait();
+
+    // x of the CTA's first unit goes out before the second weight stage, so
+    // that it does not queue behind the weights
+    int xpend_l = -1, xpend_slice = -1;  // the x copy in flight (-1: none)
+    uint32_t x_par = 0;
+    // thread 0: bulk-copy groups xg0 .. xg0 + xng - 1 of every token's x into
+    // its staged row (raw order; rewritten in place once it lands)
+    auto issue_x = [&](const MmaLinDesc &L, int xg0, int xng) {
+        const uint32_t row_bytes = (uint32_t)xng * kGroup * 2;
+        mbar_arrive_expect_tx(x_bar, row_bytes * L.M);
+        for (int t = 0; t < L.M; ++t)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+                " [%0], [%1], %2, [%3];" ::"r"(dev::smem_u32(xs) + t * L.xstride),
+                "l"(L.x + (size_t)t * L.K + (size_t)xg0 * kGroup), "r"(row_bytes), "r"(x_bar)
+                : "memory");
+    };
+    {
+        const int u0 = unit_q[0];  // a fixed unit, below total
+        int l0 = 0;
+        if (kRound)
+            while (l0 + 1 < P.n_lin && u0 >= P.descs[l0 + 1].unit_start) ++l0;
+        const MmaLinDesc &D0 = desc(l0);
+        const int s0 = (u0 - D0.unit_start) / D0.n_blocks;
+        if (!(kRound && P.done && D0.wait_for >= 0)) {
+            const int xg0 = s0 * D0.slice_groups;
+            if (threadIdx.x == 0) issue_x(D0, xg0, min(D0.G, xg0 + D0.slice_groups) - xg0);
+            xpend_l = l0;
+            xpend_slice = s0;
+        }
+    }
+    issue_next();
 
     // unit of word u of this lane's chunk in a group: x_unit(4c + u)
     const int xo0 = 16 * x_unit(4 * c + 0), xo1 = 16 * x_unit(4 * c + 1);
@@ -427,16 +462,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int arr_l = -1, arr_sb = 0;  // split unit whose arrival is still to count
     int red_l = -1, red_sb = 0;  // arrival counted, its result in red_prev (thread 0)
     unsigned red_prev = 0;
-    unsigned fetched = 0;        // thread 0: counter value for sequence index k + kQueueAhead + 1
+    // The CTA's units after the first two: every grid-th unit (a launch of
+    // one linear, whose few units per CTA are balanced best that way), or
+    // from a shared counter (a fused round: CTAs that run faster take more).
+    unsigned fetched = 0;  // thread 0, dynamic: counter value for sequence index k + kQueueAhead + 1
+    auto seq_unit = [&](int seq, unsigned counter_value) -> int {
+        const unsigned un = P.dynamic ? 2u * grid + counter_value
+                                      : (unsigned)blockIdx.x + (unsigned)seq * grid;
+        return un < (unsigned)total ? (int)un : total;
+    };
     if (threadIdx.x == 0) {
         // sequence indices 2 .. kQueueAhead
-        const unsigned f = atomicAdd(P.sched, (unsigned)(kQueueAhead - 1));
-        for (int i = 0; i < kQueueAhead - 1; ++i) {
-            const unsigned u = 2u * grid + f + i;
-            unit_q[2 + i] = u < (unsigned)total ? (int)u : total;
-        }
+        const unsigned f = P.dynamic ? atomicAdd(P.sched, (unsigned)(kQueueAhead - 1)) : 0u;
+        for (int i = 0; i < kQueueAhead - 1; ++i) unit_q[2 + i] = seq_unit(2 + i, f + i);
         st_release_cta(flags + kFlagQKnown, kQueueAhead);
-        fetched = atomicAdd(P.sched, 1u);
+        if (P.dynamic) fetched = atomicAdd(P.sched, 1u);
     }
     // thread 0: publish whether this CTA reduces the block whose arrival it
     // counted (the result is read here, a unit after the atomic), into the
@@ -450,18 +490,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         f[2] = red_sb;
         red_l = -1;
     };
-    // thread 0: count the arrival of the pending split unit (all warps have
-    // stored their partials: call after a CTA barrier)
+    // count the arrival of the pending split unit (thread 0's atomic; all
+    // warps have stored their partials: call after a CTA barrier).  arr_l and
+    // red_pending are the same in every thread.
+    bool red_pending = false;  // an arrival is counted, its result not yet published
     auto count_arrival = [&]() {
-        if (threadIdx.x != 0 || arr_l < 0) return;
-        unsigned prev;
-        asm volatile("fence.acq_rel.gpu;\n\tatom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                     : "=r"(prev)
-                     : "l"(desc(arr_l).counters + arr_sb)
-                     : "memory");
-        red_prev = prev;
-        red_l = arr_l;
-        red_sb = arr_sb;
+        if (arr_l < 0) return;
+        if (threadIdx.x == 0) {
+            unsigned prev;
+            asm volatile("fence.acq_rel.gpu;\n\tatom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(prev)
+                         : "l"(desc(arr_l).counters + arr_sb)
+                         : "memory");
+            red_prev = prev;
+            red_l = arr_l;
+            red_sb = arr_sb;
+        }
+        red_pending = true;
         arr_l = -1;
     };
     // all threads, after the barrier that follows publish_reduction(boundary)
@@ -474,30 +519,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // one inside it (b = k + 1 ... ); `bnd` counts them
     int bnd = 0;
     for (int k = 0;; ++k) {
-        if (threadIdx.x == 0) {
-            publish_reduction(bnd);
-            if (k >= 1) {
-                // the unit fetched at the previous boundary joins the queue
-                const unsigned u = 2u * grid + fetched;
-                unit_q[(k + kQueueAhead) & 7] = u < (unsigned)total ? (int)u : total;
-                st_release_cta(flags + kFlagQKnown, k + kQueueAhead);
-                fetched = atomicAdd(P.sched, 1u);
+        if (threadIdx.x == 0 && k >= 1) {
+            // the unit fetched at the previous boundary joins the queue
+            unit_q[(k + kQueueAhead) & 7] = seq_unit(k + kQueueAhead, fetched);
+            st_release_cta(flags + kFlagQKnown, k + kQueueAhead);
+            if (P.dynamic) fetched = atomicAdd(P.sched, 1u);
+        }
+        // this unit's queue entry (thread 0 wrote it kQueueAhead units ago;
+        // warps that run ahead of warp 0 wait for it here)
+        if (ld_acquire_cta(flags + kFlagQKnown) < k) {
+            const unsigned long long tq = dev::globaltimer();
+            while (ld_acquire_cta(flags + kFlagQKnown) < k) {
+                if (vflags[kFlagAbort] || dev::globaltimer() - tq > kWaitNs) {
+                    if (lane == 0) atomicOr(P.status, kErrMmaWait);
+                    vflags[kFlagAbort] = 1;
+                    break;
+                }
             }
         }
-        __syncthreads();  // the previous unit's staged x is no longer read
-        if (vflags[kFlagAbort]) {
+        const int u = vflags[kFlagAbort] ? total : unit_q[k & 7];
+        if (kRound && u < total)
+            while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
+        const MmaLinDesc &D = desc(cl);
+        const int ul = u - D.unit_start;
+        const int slice = ul / D.n_blocks, sb = ul - slice * D.n_blocks;
+        // A CTA barrier is needed to restage x, for the split-K arrival and
+        // reduction protocol and for a new linear of a round with waits;
+        // otherwise the warps go on without one, but at least every fourth
+        // unit, so that no warp falls far enough behind warp 0 for the queue
+        // (8 entries) to overwrite a unit it has still to read.
+        const bool restage = u < total && (cl != staged_l || slice != staged_slice);
+        if (restage || arr_l >= 0 || red_pending || (k & 3) == 0 ||
+            (kRound && P.done && passed < cl && u < total)) {
+            publish_reduction(bnd);
+            red_pending = false;
+            __syncthreads();  // the previous unit's staged x is no longer read
+            if (vflags[kFlagAbort]) {
+                dead = true;
+                break;
+            }
+            maybe_reduce(bnd++);
+        } else if (vflags[kFlagAbort]) {
             dead = true;
             break;
         }
-        maybe_reduce(bnd++);
-        const int u = unit_q[k & 7];
         if (u >= total) break;
-        if (kRound)
-            while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
-        const MmaLinDesc &D = desc(cl);
         const int M = D.M;
-        const int ul = u - D.unit_start;
-        const int slice = ul / D.n_blocks, sb = ul - slice * D.n_blocks;
         const int g0 = slice * D.slice_groups;  // a multiple of kStageGroups
         const int ng = min(D.G, g0 + D.slice_groups) - g0;
         const int nst = (ng + kStageGroups - 1) / kStageGroups;
@@ -526,45 +593,53 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 break;
             }
         }
-        if (cl != staged_l || slice != staged_slice) {
-            // ---- stage x[:, slice] in MMA pair order, and each (group,
-            // token)'s sum S of x (kept as S * 2^-20): the 16 lanes of a half
-            // warp hold the 16 units of one group of one token and add theirs
-            // with shuffles.  kXBatch loads in flight per thread: a few L2
-            // round trips instead of one per unit of x.
-            constexpr int kXBatch = 8;
+        if (restage) {
+            // ---- stage x[:, slice]: the slice lands by bulk copy in its rows
+            // in raw order; then each lane rewrites its 16-byte unit J in MMA
+            // pair order at unit x_unit(J) (a unit and its partner sit in the
+            // same half warp: all of a warp's reads come before its writes),
+            // and each (group, token)'s sum S of x is formed (kept as S *
+            // 2^-20): the 16 lanes of a half warp hold the 16 units of one
+            // group of one token and add theirs with shuffles
+            if (xpend_l != cl || xpend_slice != slice) {  // not copied ahead
+                if (threadIdx.x == 0) {
+                    // the previous unit's reads of these rows are behind the
+                    // barrier above; order them before the copy's writes
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_x(D, g0, ng);
+                }
+            }
+            xpend_l = cl;  // in flight until the wait below
+            xpend_slice = slice;
+            if (!__all_sync(0xffffffffu, mbar_wait(x_bar, x_par))) {
+                if (lane == 0) {
+                    atomicOr(P.status, kErrMmaWait);
+                    vflags[kFlagAbort] = 1;
+                }
+                dead = true;
+                break;
+            }
+            x_par ^= 1u;
+            xpend_l = -1;
             const int nunits = ng * (kGroup / 8);
             const int xtotal = M * nunits;  // a multiple of 16
-            const int k0 = g0 * kGroup;
-            for (int base = warp * 32; base < xtotal; base += kThreads * kXBatch) {
-                uint4 v[kXBatch];
+            for (int base = warp * 32; base < xtotal; base += kThreads) {
+                const int i = base + lane;
+                const bool valid = i < xtotal;
+                const int t = i / nunits, J = i - t * nunits;
+                uint8_t *row = xs + (size_t)t * D.xstride;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid) v = *reinterpret_cast<const uint4 *>(row + 16 * J);
+                __syncwarp();
+                if (valid) *reinterpret_cast<uint4 *>(row + 16 * x_unit(J)) = mma_pair_order(v);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+                const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+                const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+                float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
 #pragma unroll
-                for (int b = 0; b < kXBatch; ++b) {
-                    const int i = base + b * kThreads + lane;
-                    v[b] = make_uint4(0, 0, 0, 0);
-                    if (i < xtotal) {
-                        const int t = i / nunits, J = i - t * nunits;
-                        v[b] = __ldg(reinterpret_cast<const uint4 *>(D.x + (size_t)t * D.K + k0 + 8 * J));
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < kXBatch; ++b) {
-                    const int i = base + b * kThreads + lane;
-                    const bool valid = i < xtotal;
-                    const int t = i / nunits, J = i - t * nunits;
-                    if (valid)
-                        *reinterpret_cast<uint4 *>(xs + (size_t)t * D.xstride + 16 * x_unit(J)) =
-                            mma_pair_order(v[b]);
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].x));
-                    const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].y));
-                    const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].z));
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v[b].w));
-                    float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1)
-                        sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                    if (valid && (J & 15) == 0) sums[(J >> 4) * 8 + t] = sum * kTwoM20;
-                }
+                for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if (valid && (J & 15) == 0) sums[(J >> 4) * 8 + t] = sum * kTwoM20;
             }
             // tokens M..7 have no x: their sums are zero
             for (int i = threadIdx.x; i < ng * (8 - M); i += kThreads)
@@ -713,32 +788,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // a wait expired: let this warp's copies in flight land (bounded)
         // before the CTA's shared memory goes away
         for (; t_cons < t_iss; ++t_cons) mbar_wait(bar0 + 8 * (t_cons & 1u), (t_cons >> 1) & 1u);
+        if (xpend_l >= 0) mbar_wait(x_bar, x_par);  // an x copy in flight
         cp_wait_all();
         return;
     }
     cp_wait_all();
     // split K still pending: the decision on the arrival counted at the last
-    // boundary, then the arrival of the last unit
-    publish_reduction(bnd);
-    __syncthreads();
-    maybe_reduce(bnd++);
-    count_arrival();
-    publish_reduction(bnd);
-    __syncthreads();
-    maybe_reduce(bnd++);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (kRound && P.done)
-            for (; passed < P.n_lin; ++passed) atomicAdd(P.done + passed, 1u);
-        // the last CTA out leaves the counters zeroed for the next launch
-        const unsigned prev = atomicAdd(P.sched + 1, 1u);
-        if (prev == (unsigned)grid - 1) {
+    // boundary, then the arrival of the last unit (arr_l and red_pending are
+    // the same in every thread)
+    if (red_pending || arr_l >= 0) {
+        publish_reduction(bnd);
+        red_pending = false;
+        __syncthreads();
+        maybe_reduce(bnd++);
+        count_arrival();
+        publish_reduction(bnd);
+        __syncthreads();
+        maybe_reduce(bnd++);
+    }
+    if (P.dynamic || (kRound && P.done)) {
+        __syncthreads();
+        if (threadIdx.x == 0) {
             __threadfence();
-            P.sched[0] = 0u;
-            P.sched[1] = 0u;
             if (kRound && P.done)
-                for (int l = 0; l < P.n_lin; ++l) P.done[l] = 0u;
+                for (; passed < P.n_lin; ++passed) atomicAdd(P.done + passed, 1u);
+            // the last CTA out leaves the counters zeroed for the next launch
+            const unsigned prev = atomicAdd(P.sched + 1, 1u);
+            if (prev == (unsigned)grid - 1) {
+                __threadfence();
+                P.sched[0] = 0u;
+                P.sched[1] = 0u;
+                if (kRound && P.done)
+                    for (int l = 0; l < P.n_lin; ++l) P.done[l] = 0u;
+            }
         }
     }
 }
@@ -890,6 +972,7 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     P.sched = ws.counters + ws.n_counters - kMmaSchedWords;
     P.n_lin = 1;
     P.total_units = plan.units;
+    P.dynamic = 0;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(plan.grid, plan.smem_bytes, stream, attr);
     return cudaLaunchKernelEx(&cfg, mma_kernel<false>, P);
@@ -905,6 +988,7 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
     P.sched = ws.counters + ws.n_counters - kMmaSchedWords;
     P.n_lin = r.n;
     P.total_units = r.total_units;
+    P.dynamic = 1;
     int grid = mma_round_grid(dev);
     if (grid > r.total_units) grid = r.total_units;
     cudaLaunchAttribute attr[2];
