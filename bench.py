@@ -124,6 +124,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload construction
 # ---------------------------------------------------------------------------
+# DRAM bytes (read + write) of one launch of the fused 64-layer round kernel,
+# from one ncu capture of the current kernel (profiles/
+# mma_kernel_decode_round_m4_launch_list.md); None once the kernel changes.
+ROUND_KERNEL_TRAFFIC = 11.57e9 + 0.098e9
+
+
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):
     import synthetic_inputs as si
     xs = [si.x(si.config_seed(3, 0, 8 + j), M, K) for j, (_, K, _) in enumerate(ROUND_SHAPES)]
@@ -431,7 +437,8 @@ def main():
                            if per_round == 1 else f"decode round ({per_round} launches)"),
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy)",
-                "traffic": None, "launches_timed": n_l,
+                "traffic": (ROUND_KERNEL_TRAFFIC if per_round == 1 and args.layers == N_LAYERS
+                            else None), "launches_timed": n_l,
                 "mean_launch_us": t_l / n_l * 1e6,
                 "mean_algorithmic_bytes_per_launch": rb}
     # each linear launched alone (its own kernel), for the per-shape picture
