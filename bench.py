@@ -124,9 +124,9 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload construction
 # ---------------------------------------------------------------------------
-# DRAM bytes (read + write) of one launch of the fused 64-layer round kernel,
-# from one ncu capture of the current kernel (profiles/
-# mma_kernel_decode_round_m4_launch_list.md); None once the kernel changes.
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the fused 64-layer round kernel, from one ncu capture of the current kernel;
+# None once the kernel changes.
 ROUND_KERNEL_TRAFFIC = 11.57e9 + 0.098e9
 
 

@@ -19,7 +19,7 @@
  *     y[m,n] = sum_k x[m,k] * w[n,k]
  * with q, z unsigned 4-bit, s and x IEEE binary16, y returned in binary64.
  *
- * Readings taken where the pages are silent (each one listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - packed layout [N, K/8] 32-bit words, rows = outputs (section 四 names
  *     "[N,K/8] int32"); element k sits in bits 4*(k%8)..4*(k%8)+3 of word k/8;
  *   - zeros are 4-bit too, packed 8 per word along the group axis with the
