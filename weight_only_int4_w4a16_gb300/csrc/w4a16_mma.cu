@@ -73,8 +73,27 @@ constexpr int kStageW = kStageGroups * 16 * 64;  // 4 KB of weights
 constexpr int kStageMeta = 16 * 16;             // per row: 3 scale words, 1 zeros word
 constexpr int kStageBytes = kStageW + kStageMeta;
 constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
-// ring barriers, then 16 flag ints, then the barrier of the x copies
-constexpr int kBarBytes = kWarps * kDepth * 8 + 64 + 16;
+// A unit of the CTA's queue, decoded once by thread 0 into shared memory:
+// everything the warps need of the unit and of its linear, so that none of
+// them reads a descriptor from global memory on its way.
+struct UnitInfo {
+    uint64_t tmap;  // address of the linear's tensor map
+    const __half *x;
+    const __half *scales;
+    const uint32_t *zeros;
+    __half *y;
+    float *partials;
+    unsigned *counters;
+    uintptr_t scales_first, scales_end;
+    int l, slice, sb;  // linear, K slice, strip block (l < 0: the queue has ended)
+    int N, K, G, ZW, M, S, slice_groups, n_strips, strips_per_warp, xstride, wait_for;
+    int seq;  // the queue position this entry holds (written last)
+};
+constexpr int kSlots = 8;  // one per queue position (mod 8)
+// ring barriers, then 16 flag ints, then the barrier of the x copies, then
+// the decoded units
+constexpr int kSlotOffset = kWarps * kDepth * 8 + 64 + 16;
+constexpr int kBarBytes = kSlotOffset + kSlots * (int)sizeof(UnitInfo);
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
 constexpr int kMaxSliceGroups = 128;
 constexpr int kRoundStripsPerWarp = 8;  // fused rounds: strips per warp and unit
@@ -205,10 +224,7 @@ __device__ __forceinline__ void st_release_cta(int *p, int v) {
 
 // Ints of the CTA's flag area in shared memory
 constexpr int kFlagAbort = 0;   // a wait expired: the CTA's warps stop at their next unit
-constexpr int kFlagQKnown = 1;  // highest sequence index whose unit is in the queue
-constexpr int kFlagRed = 2;     // this CTA reduces the block (kFlagRedL, kFlagRedSb)
-constexpr int kFlagRedL = 3;
-constexpr int kFlagRedSb = 4;
+constexpr int kFlagRed = 2;     // 2 x 3 ints: whether this CTA reduces a block, its linear and block
 constexpr int kFlagQueue = 8;   // 8 ints: the CTA's units by sequence index (mod 8)
 constexpr int kQueueAhead = 1;  // units fetched ahead of the one being consumed
 
@@ -260,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t x_bar = dev::smem_u32(smem + kRingBytes + kWarps * kDepth * 8 + 64);
     volatile int *vflags = flags;
     volatile int *unit_q = flags + kFlagQueue;
+    UnitInfo *slots = reinterpret_cast<UnitInfo *>(smem + kRingBytes + kSlotOffset);
     // the next kernel in the stream may be scheduled as SMs free up; it waits
     // for this grid to finish before it touches anything this grid writes
     grid_dependents_launch();
@@ -276,13 +293,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (warp == 0) mbar_init(x_bar, 1);  // the x copies: bytes only
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    // thread 0: decode queue position seq (its unit is in unit_q) into its
+    // slot; the descriptors are read-only inputs
+    int dl = 0;  // thread 0: the decoder's linear (units come in increasing order)
+    auto fill_slot = [&](int seq) {
+        UnitInfo &U = slots[seq & (kSlots - 1)];
+        const int u = unit_q[seq & 7];
+        if (u >= total) {
+            U.l = -1;
+        } else {
+            if (kRound)
+                while (dl + 1 < P.n_lin && u >= P.descs[dl + 1].unit_start) ++dl;
+            const MmaLinDesc &D = desc(dl);
+            const int ul = u - D.unit_start;
+            U.tmap = reinterpret_cast<uint64_t>(&D.tmap);
+            U.x = D.x;
+            U.scales = D.scales;
+            U.zeros = D.zeros;
+            U.y = D.y;
+            U.partials = D.partials;
+            U.counters = D.counters;
+            U.scales_first = D.scales_first;
+            U.scales_end = D.scales_end;
+            U.N = D.N;
+            U.K = D.K;
+            U.G = D.G;
+            U.ZW = D.ZW;
+            U.M = D.M;
+            U.S = D.S;
+            U.slice_groups = D.slice_groups;
+            U.n_strips = D.n_strips;
+            U.strips_per_warp = D.strips_per_warp;
+            U.xstride = D.xstride;
+            U.wait_for = D.wait_for;
+            U.l = dl;
+            U.slice = ul / D.n_blocks;
+            U.sb = ul - U.slice * D.n_blocks;
+        }
+        st_release_cta(&U.seq, seq);
+    };
     if (threadIdx.x == 0) {
-        // the CTA's first two units are fixed; the rest come from a counter
+        // the CTA's first two units are fixed; the rest come every grid-th or
+        // from a counter
         vflags[kFlagAbort] = 0;
         vflags[kFlagRed] = 0;
+        for (int i = 0; i < kSlots; ++i) slots[i].seq = -1;
         unit_q[0] = blockIdx.x;
         unit_q[1] = blockIdx.x + grid < total ? blockIdx.x + grid : total;
-        vflags[kFlagQKnown] = 1;
+        fill_slot(0);
+        fill_slot(1);
     }
     __syncthreads();
 
@@ -295,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // (h = 1): the three aligned words that hold the stage's four (2-byte
     // aligned) scales, and the zeros word of its groups.
     const int r = lane & 15, h = lane >> 4;
-    int ik = 0, il = 0;           // sequence index of the issue cursor's unit, its linear
+    int ik = 0;                   // queue position of the issue cursor's unit
     int ij = 0, inst = 0;         // stage within the strip, stages per strip
     bool i_wait = false;          // the next unit is not in the queue yet
     bool i_done = false;          // no units left
@@ -309,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t is_zbytes = 0;
     // this warp's strips in a unit: strip0 + 8r for r < strips per warp
     int i_strip = 0, i_last = 0;  // current strip, last strip of the unit for this warp
-    const MmaLinDesc *iD = nullptr;
+    const UnitInfo *iD = nullptr;
     // copy sources of the issue cursor's strip
     auto i_strip_enter = [&]() {
-        const MmaLinDesc &D = *iD;
+        const UnitInfo &D = *iD;
         i_row16 = i_strip * 16;
         const int row = i_row16 + r;
         const bool vr = row < D.N;
@@ -329,24 +388,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // for the unit's slice of x); stop at a unit the queue does not hold yet
     auto i_enter = [&]() {
         for (;; ++ik) {
-            if (ik > ld_acquire_cta(flags + kFlagQKnown)) {
+            const UnitInfo &D = slots[ik & (kSlots - 1)];
+            if (ld_acquire_cta(&D.seq) != ik) {  // not decoded yet
                 i_wait = true;
                 return;
             }
             i_wait = false;
-            const int iu = unit_q[ik & 7];
-            if (iu >= total) {
+            if (D.l < 0) {
                 i_done = true;
                 return;
             }
-            if (kRound)
-                while (il + 1 < P.n_lin && iu >= P.descs[il + 1].unit_start) ++il;
-            const MmaLinDesc &D = desc(il);
-            const int ul = iu - D.unit_start;
-            const int s = ul / D.n_blocks, sb = ul - s * D.n_blocks;
-            const int strip0 = sb * kWarps * D.strips_per_warp + warp;
+            const int strip0 = D.sb * kWarps * D.strips_per_warp + warp;
             if (strip0 >= D.n_strips) continue;
-            i_g0 = s * D.slice_groups;
+            i_g0 = D.slice * D.slice_groups;
             const int ng = min(D.G, i_g0 + D.slice_groups) - i_g0;
             inst = (ng + kStageGroups - 1) / kStageGroups;
             if (warp == 0 && lane < D.M)
@@ -355,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                              "r"(ng * kGroup * 2)
                              : "memory");
             iD = &D;
-            i_map = reinterpret_cast<uint64_t>(&D.tmap);
+            i_map = D.tmap;
             i_sfirst = D.scales_first;
             const int nr = min(D.strips_per_warp, (D.n_strips - 1 - strip0) / kWarps + 1);
             i_strip = strip0;
@@ -421,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t x_par = 0;
     // thread 0: bulk-copy groups xg0 .. xg0 + xng - 1 of every token's x into
     // its staged row (raw order; rewritten in place once it lands)
-    auto issue_x = [&](const MmaLinDesc &L, int xg0, int xng) {
+    auto issue_x = [&](const UnitInfo &L, int xg0, int xng) {
         const uint32_t row_bytes = (uint32_t)xng * kGroup * 2;
         mbar_arrive_expect_tx(x_bar, row_bytes * L.M);
         for (int t = 0; t < L.M; ++t)
@@ -432,17 +486,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 : "memory");
     };
     {
-        const int u0 = unit_q[0];  // a fixed unit, below total
-        int l0 = 0;
-        if (kRound)
-            while (l0 + 1 < P.n_lin && u0 >= P.descs[l0 + 1].unit_start) ++l0;
-        const MmaLinDesc &D0 = desc(l0);
-        const int s0 = (u0 - D0.unit_start) / D0.n_blocks;
+        const UnitInfo &D0 = slots[0];  // a fixed unit, decoded before the barrier above
         if (!(kRound && P.done && D0.wait_for >= 0)) {
-            const int xg0 = s0 * D0.slice_groups;
+            const int xg0 = D0.slice * D0.slice_groups;
             if (threadIdx.x == 0) issue_x(D0, xg0, min(D0.G, xg0 + D0.slice_groups) - xg0);
-            xpend_l = l0;
-            xpend_slice = s0;
+            xpend_l = D0.l;
+            xpend_slice = D0.slice;
         }
     }
     issue_next();
@@ -460,7 +509,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // previous unit at a unit boundary and reads the count's result at the
     // next boundary, so the atomic's latency hides behind a unit of work.
     int arr_l = -1, arr_sb = 0;  // split unit whose arrival is still to count
+    unsigned *arr_cnt = nullptr;  // its linear's counters
+    int arr_S = 0;                // its linear's slices
     int red_l = -1, red_sb = 0;  // arrival counted, its result in red_prev (thread 0)
+    int red_S = 0;
     unsigned red_prev = 0;
     // The CTA's units after the first two: every grid-th unit (a launch of
     // one linear, whose few units per CTA are balanced best that way), or
@@ -472,10 +524,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         return un < (unsigned)total ? (int)un : total;
     };
     if (threadIdx.x == 0) {
-        // sequence indices 2 .. kQueueAhead
-        const unsigned f = P.dynamic ? atomicAdd(P.sched, (unsigned)(kQueueAhead - 1)) : 0u;
-        for (int i = 0; i < kQueueAhead - 1; ++i) unit_q[2 + i] = seq_unit(2 + i, f + i);
-        st_release_cta(flags + kFlagQKnown, kQueueAhead);
+        // sequence indices 2 .. kQueueAhead (none when the queue runs one ahead)
+        if (kQueueAhead > 1) {
+            const unsigned f = P.dynamic ? atomicAdd(P.sched, (unsigned)(kQueueAhead - 1)) : 0u;
+            for (int i = 0; i < kQueueAhead - 1; ++i) unit_q[2 + i] = seq_unit(2 + i, f + i);
+        }
         if (P.dynamic) fetched = atomicAdd(P.sched, 1u);
     }
     // thread 0: publish whether this CTA reduces the block whose arrival it
@@ -485,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     auto publish_reduction = [&](int boundary) {
         if (threadIdx.x != 0) return;
         volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
-        f[0] = red_l >= 0 && red_prev == (unsigned)(desc(red_l).S - 1);
+        f[0] = red_l >= 0 && red_prev == (unsigned)(red_S - 1);
         f[1] = red_l;
         f[2] = red_sb;
         red_l = -1;
@@ -500,11 +553,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             unsigned prev;
             asm volatile("fence.acq_rel.gpu;\n\tatom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                          : "=r"(prev)
-                         : "l"(desc(arr_l).counters + arr_sb)
+                         : "l"(arr_cnt + arr_sb)
                          : "memory");
             red_prev = prev;
             red_l = arr_l;
             red_sb = arr_sb;
+            red_S = arr_S;
         }
         red_pending = true;
         arr_l = -1;
@@ -522,14 +576,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (threadIdx.x == 0 && k >= 1) {
             // the unit fetched at the previous boundary joins the queue
             unit_q[(k + kQueueAhead) & 7] = seq_unit(k + kQueueAhead, fetched);
-            st_release_cta(flags + kFlagQKnown, k + kQueueAhead);
             if (P.dynamic) fetched = atomicAdd(P.sched, 1u);
         }
-        // this unit's queue entry (thread 0 wrote it kQueueAhead units ago;
-        // warps that run ahead of warp 0 wait for it here)
-        if (ld_acquire_cta(flags + kFlagQKnown) < k) {
+        // this unit, decoded by thread 0 a unit ago (warps that run ahead of
+        // warp 0 wait for it here)
+        const UnitInfo &D = slots[k & (kSlots - 1)];
+        if (ld_acquire_cta(&D.seq) != k) {
             const unsigned long long tq = dev::globaltimer();
-            while (ld_acquire_cta(flags + kFlagQKnown) < k) {
+            while (ld_acquire_cta(&D.seq) != k) {
                 if (vflags[kFlagAbort] || dev::globaltimer() - tq > kWaitNs) {
                     if (lane == 0) atomicOr(P.status, kErrMmaWait);
                     vflags[kFlagAbort] = 1;
@@ -537,20 +591,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
             }
         }
-        const int u = vflags[kFlagAbort] ? total : unit_q[k & 7];
-        if (kRound && u < total)
-            while (cl + 1 < P.n_lin && u >= P.descs[cl + 1].unit_start) ++cl;
-        const MmaLinDesc &D = desc(cl);
-        const int ul = u - D.unit_start;
-        const int slice = ul / D.n_blocks, sb = ul - slice * D.n_blocks;
+        const bool have = !vflags[kFlagAbort] && D.l >= 0;
+        if (have) cl = D.l;
+        const int slice = D.slice, sb = D.sb;
         // A CTA barrier is needed to restage x, for the split-K arrival and
         // reduction protocol and for a new linear of a round with waits;
         // otherwise the warps go on without one, but at least every fourth
         // unit, so that no warp falls far enough behind warp 0 for the queue
         // (8 entries) to overwrite a unit it has still to read.
-        const bool restage = u < total && (cl != staged_l || slice != staged_slice);
+        const bool restage = have && (cl != staged_l || slice != staged_slice);
         if (restage || arr_l >= 0 || red_pending || (k & 3) == 0 ||
-            (kRound && P.done && passed < cl && u < total)) {
+            (kRound && P.done && passed < cl && have)) {
             publish_reduction(bnd);
             red_pending = false;
             __syncthreads();  // the previous unit's staged x is no longer read
@@ -563,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             dead = true;
             break;
         }
-        if (u >= total) break;
+        if (!have) break;
         const int M = D.M;
         const int g0 = slice * D.slice_groups;  // a multiple of kStageGroups
         const int ng = min(D.G, g0 + D.slice_groups) - g0;
@@ -609,6 +660,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     issue_x(D, g0, ng);
                 }
             }
+            // thread 0 decodes the next unit while the copy is in flight
+            if (threadIdx.x == 0 && k >= 1) fill_slot(k + 1);
             xpend_l = cl;  // in flight until the wait below
             xpend_slice = slice;
             if (!__all_sync(0xffffffffu, mbar_wait(x_bar, x_par))) {
@@ -647,6 +700,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             __syncthreads();
             staged_l = cl;
             staged_slice = slice;
+        } else if (threadIdx.x == 0 && k >= 1) {
+            fill_slot(k + 1);  // the next unit (slot 1 is decoded at the start)
         }
         // after the staging: thread 0's release fence and atomic would
         // otherwise hold up warp 0, and with it the staging
@@ -780,6 +835,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (D.S > 1) {  // count this unit's arrival at the next boundary
             arr_l = cl;
             arr_sb = sb;
+            arr_cnt = D.counters;
+            arr_S = D.S;
         }
     }
 
