@@ -58,6 +58,8 @@ def _bind(lib):
     lib.w4o_pack.argtypes = [P, P, I, I, I, P, P]
     lib.w4o_unpack.argtypes = [P, P, I, I, I, P, P]
     lib.w4o_dequant.argtypes = [P, P, P, I, I, I, P]
+    lib.w4o_silu_mul.argtypes = [P, I, I, P]
+    lib.w4o_add_residual.argtypes = [P, P, L, P]
     lib.w4o_linear.argtypes = [P, P, P, P, I, I, I, I, P, I]
     lib.w4o_linear_rows.argtypes = [P, P, P, P, I, I, I, I, P, I, P, I]
     lib.w4o_round_to_half.argtypes = [P, L, P]
@@ -196,3 +198,24 @@ def linear_rows(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
                             K, group, _ptr(rows), int(rows.size), _ptr(y), nt)
     return y
 
+
+
+def silu_mul(y: np.ndarray) -> np.ndarray:
+    """out[M, I] = silu(y[:, :I]) * y[:, I:] in binary64 (y is [M, 2I], gate
+    columns first): the epilogue of a fused gate+up projection."""
+    y = _c(y, np.float64)
+    M, N2 = y.shape
+    assert N2 % 2 == 0
+    out = np.empty((M, N2 // 2), dtype=np.float64)
+    _load().w4o_silu_mul(_ptr(y), M, N2 // 2, _ptr(out))
+    return out
+
+
+def add_residual(y: np.ndarray, residual: np.ndarray) -> np.ndarray:
+    """out = y + residual in binary64; residual as fp16 bits (uint16), same shape."""
+    y = _c(y, np.float64)
+    r = _c(residual, np.uint16)
+    assert r.shape == y.shape
+    out = np.empty_like(y)
+    _load().w4o_add_residual(_ptr(y), _ptr(r), int(y.size), _ptr(out))
+    return out

@@ -270,3 +270,28 @@ void w4o_half_array_to_double(const uint16_t *h, long n, double *out)
 {
     for (long i = 0; i < n; i++) out[i] = w4o_half_to_double(h[i]);
 }
+
+/* ---- epilogues: the steps right after the linear.  SiLU-and-mul follows
+ * the fused gate+up projection (Z100 thread, section 二, which lists it among
+ * the MLP operators); the residual add follows the output projections (V100
+ * article, third round of changes: the MLP's add-back of its input merged into
+ * the matmul's output stage).  TEST INFRASTRUCTURE ONLY.
+ *
+ * SiLU and multiply.  y is [M, 2I]: columns 0..I-1 are the gate g, columns
+ * I..2I-1 the up projection u (the fused gate+up layout, gate rows first).
+ * out[m, n] = silu(g) * u with silu(g) = g / (1 + exp(-g)), in binary64. */
+void w4o_silu_mul(const double *y, int M, int I, double *out)
+{
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < I; ++n) {
+            const double g = y[(long)m * 2 * I + n];
+            const double u = y[(long)m * 2 * I + I + n];
+            out[(long)m * I + n] = g / (1.0 + exp(-g)) * u;
+        }
+}
+
+/* Residual add: out[i] = y[i] + r[i], r given as binary16 bit patterns. */
+void w4o_add_residual(const double *y, const uint16_t *r, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = y[i] + w4o_half_to_double(r[i]);
+}

@@ -305,3 +305,70 @@ def test_golden_fixture_reproduces_bit_for_bit():
         y = oracle.linear(x, qw, s, zw, nthreads=2)
         want = np.array([float.fromhex(h) for h in c["y_f64_hex"]]).reshape(M, N)
         assert np.array_equal(y, want)
+
+
+# ----------------------------------------------------------------------------
+# epilogues: SiLU-and-mul after the fused gate+up projection (forum thread
+# "vLLM on Hygon Z100", section 二) and the residual add after an output
+# projection (V100 article, third round of changes)
+# ----------------------------------------------------------------------------
+def test_silu_mul_closed_forms():
+    # silu(g) = g * sigmoid(g); sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4,
+    # sigmoid(0) = 1/2: closed forms that need no exponential on this side.
+    import math
+    l3 = math.log(3.0)
+    gate = [0.0, l3, -l3, 0.0, l3]
+    up = [7.0, 1.0, 1.0, -3.0, -2.0]
+    got = oracle.silu_mul(np.array([gate + up]))[0]
+    want = [0.0, 0.75 * l3, -0.25 * l3, 0.0, -1.5 * l3]
+    assert np.allclose(got, want, rtol=4e-16, atol=0.0)
+    assert got[0] == 0.0 and got[3] == 0.0
+
+
+def test_silu_mul_odd_part_identity():
+    # silu(g) - silu(-g) = g * (sigmoid(g) + sigmoid(-g)) = g for every g
+    g = RNG.uniform(-30.0, 30.0, size=257)
+    one = np.ones_like(g)
+    pos = oracle.silu_mul(np.concatenate([g, one])[None, :])[0]
+    neg = oracle.silu_mul(np.concatenate([-g, one])[None, :])[0]
+    assert np.allclose(pos - neg, g, rtol=0.0, atol=1e-13)
+    # large gates saturate: silu(g) -> g, silu(-g) -> 0
+    assert np.allclose(pos[g > 25], g[g > 25], rtol=1e-10)
+
+
+def test_silu_mul_column_split_and_rows():
+    # gate is the first half of the columns, up the second; each output column
+    # sees only its own (gate, up) pair, each row only its own row; the output
+    # is linear in up
+    M, I = 3, 40
+    y = RNG.normal(size=(M, 2 * I))
+    out = oracle.silu_mul(y)
+    assert out.shape == (M, I)
+    perm = RNG.permutation(I)
+    yp = np.concatenate([y[:, :I][:, perm], y[:, I:][:, perm]], axis=1)
+    assert np.array_equal(oracle.silu_mul(yp), out[:, perm])
+    assert np.array_equal(oracle.silu_mul(y[::-1].copy()), out[::-1])
+    y2 = y.copy()
+    y2[:, I:] *= 2.0
+    assert np.array_equal(oracle.silu_mul(y2), 2.0 * out)
+    # up = 1 gives silu(gate) alone, which is positive for positive gates and
+    # never below its minimum (about -0.2785)
+    y1 = y.copy()
+    y1[:, I:] = 1.0
+    s = oracle.silu_mul(y1)
+    assert np.all((s > 0) == (y[:, :I] > 0))
+    assert s.min() > -0.2785
+
+
+def test_add_residual_exact():
+    # dyadic y and binary16 residuals: the binary64 sum is exact, so it must
+    # equal the rational sum
+    n = 500
+    y = RNG.integers(-2 ** 20, 2 ** 20, size=n) / 1024.0
+    rf = RNG.normal(size=n).astype(np.float16)
+    got = oracle.add_residual(y, rf.view(np.uint16))
+    want = [Fraction(float(a)) + Fraction(float(b)) for a, b in zip(y, rf)]
+    assert all(Fraction(float(g)) == w for g, w in zip(got, want))
+    # a residual of +0 changes nothing
+    z = oracle.add_residual(y, np.zeros(n, dtype=np.uint16))
+    assert np.array_equal(z, y)
