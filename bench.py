@@ -127,7 +127,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the fused 64-layer round kernel, from one ncu capture of the current kernel;
 # None once the kernel changes.
-ROUND_KERNEL_TRAFFIC = None
+ROUND_KERNEL_TRAFFIC = 11_624_143_104
 
 
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):
@@ -215,21 +215,39 @@ def flush_l2(buf):
     buf.sum()
 
 
-def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,)):
-    """Median single-launch time of one linear with L2 flushed before each
-    launch, per rung (-1 = the dispatch table's choice); None where a rung
-    cannot run the shape."""
+def epilogue_bytes(M: int, N: int, K: int, epi: int) -> int:
+    """Algorithmic bytes of a linear with an epilogue: y has N/2 columns after
+    SiLU-and-mul; the residual add reads M x N fp16 more."""
+    if epi == 2:
+        return linear_bytes(M, N, K) - M * N
+    if epi == 1:
+        return linear_bytes(M, N, K) + 2 * M * N
+    return linear_bytes(M, N, K)
+
+
+def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), epi=0):
+    """Median single-launch time of one linear (with epilogue `epi`) with L2
+    flushed before each launch, per rung (-1 = the dispatch table's choice);
+    None where a rung cannot run the shape."""
     import synthetic_inputs as si
-    qw, s, zw = si.layer(si.config_seed(seed_cfg, 0, M), N, K, device=dev)
-    x = si.x(si.config_seed(seed_cfg, 0, M), M, K).to(dev)
-    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    seed = si.config_seed(seed_cfg, 0, M)
+    qw, s, zw = si.layer(seed, N, K, device=dev)
+    x = si.x(seed, M, K).to(dev)
+    y = torch.empty((M, N // 2 if epi == 2 else N), dtype=torch.float16, device=dev)
+    res = si.residual(seed, M, N).to(dev) if epi == 1 else None
+
+    def call():
+        if epi:
+            w4.w4a16_linear_epilogue(x, qw, s, zw, epi, residual=res, y=y)
+        else:
+            w4.w4a16_linear(x, qw, s, zw, y=y)
     out = {}
     for rung in rungs:
         prev = w4.w4a16_set_forced_rung(rung)
         try:
             try:
                 for _ in range(3):
-                    w4.w4a16_linear(x, qw, s, zw, y=y)
+                    call()
             except w4.W4A16Error:
                 out[rung] = None
                 continue
@@ -239,7 +257,7 @@ def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,)):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
-                w4.w4a16_linear(x, qw, s, zw, y=y)
+                call()
                 b.record()
                 ts.append((a, b))
             torch.cuda.synchronize()
@@ -492,6 +510,19 @@ def main():
                               "us_per_rung": {w4.rung_name(r): (None if v is None else v * 1e6)
                                               for r, v in ts.items() if r >= 0}}
         extra["single_linear_l2_flushed"] = singles
+        # the fused epilogues against the same linear without one
+        epis = {}
+        for label, M, N, K, epi in [("gate_up_silu_M1_K5120_N34816", 1, 34816, 5120, 2),
+                                    ("gate_up_silu_M4_K5120_N34816", 4, 34816, 5120, 2),
+                                    ("gate_up_silu_M8_K5120_N34816", 8, 34816, 5120, 2),
+                                    ("down_residual_M4_K17408_N5120", 4, 5120, 17408, 1),
+                                    ("o_residual_M4_K6144_N5120", 4, 5120, 6144, 1)]:
+            t = time_single(w4, M, N, K, 5, dev, flush=flush, epi=epi)[-1]
+            t0 = time_single(w4, M, N, K, 5, dev, flush=flush)[-1]
+            by = epilogue_bytes(M, N, K, epi)
+            epis[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
+                           "us_without_epilogue": t0 * 1e6}
+        extra["epilogue_l2_flushed"] = epis
         del flush
 
     cpu = None

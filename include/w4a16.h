@@ -126,7 +126,26 @@ int w4a16_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *sca
                  const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
                  void *stream);
 
-/* One linear of a decode round.  x is [M, K] and y [M, N]; `group` must be 128. */
+/* What w4a16_linear_epilogue (and a decode round's linear) does with the
+ * linear's fp32 result h = x @ W^T before the single fp16 rounding of y.  The
+ * steps that follow the linear in a decoder layer, done in the same kernel so
+ * that h never goes to memory: the residual add after an output projection
+ * (haowenji.com V100 decode article, its third round of changes, which merged
+ * the add-back of the layer input into the matmul's output stage) and the
+ * SiLU-and-mul after a fused gate+up projection (forum.sourcefind.cn thread
+ * "vLLM on Hygon Z100", section 二, which names it among the MLP operators). */
+typedef enum {
+    W4A16_EPILOGUE_NONE = 0,     /* y[M, N] = h */
+    W4A16_EPILOGUE_RESIDUAL = 1, /* y[M, N] = h + residual[M, N] (fp16, read as fp32) */
+    W4A16_EPILOGUE_SILU_MUL = 2  /* y[M, N/2] = silu(h[:, :N/2]) * h[:, N/2:] with
+                                    silu(g) = g / (1 + e^-g): the weight's first N/2 rows are
+                                    the gate projection, the last N/2 the up projection; N must
+                                    be a multiple of 32 */
+} w4a16_epilogue;
+
+/* One linear of a decode round.  x is [M, K] and y [M, N] ([M, N/2] with
+ * SiLU-and-mul); `group` must be 128.  `epilogue` is a w4a16_epilogue;
+ * `residual` is [M, N] for W4A16_EPILOGUE_RESIDUAL and NULL otherwise. */
 typedef struct {
     const uint16_t *x;
     const uint32_t *qweight;
@@ -136,7 +155,27 @@ typedef struct {
     int N;
     int K;
     int group;
+    int epilogue;
+    const uint16_t *residual;
 } w4a16_linear_desc;
+
+/* y = epilogue(x @ W^T): w4a16_linear followed, in the same kernel, by the
+ * step `epilogue` names (w4a16_epilogue).  W4A16_EPILOGUE_NONE is exactly
+ * w4a16_linear.  The other epilogues run on the warp-MMA rungs only: M <= 8
+ * and no forced rung other than those (W4A16_ERR_UNSUPPORTED otherwise).
+ *   residual  [M, N] fp16, 2-byte aligned, for W4A16_EPILOGUE_RESIDUAL (NULL
+ *             otherwise: INVALID_ARG); it may be y itself (y += x @ W^T) but
+ *             must not otherwise overlap y.
+ *   y         [M, N], or [M, N/2] with W4A16_EPILOGUE_SILU_MUL (N a multiple
+ *             of 32: W4A16_ERR_UNSUPPORTED otherwise).
+ * With split K the partial sums of h are reduced first and the epilogue applied
+ * once to each output.  SiLU-and-mul always passes h through the split-K
+ * workspace (S x M x N fp32, S >= 1 K slices, and one arrival counter per
+ * block of rows) and applies the epilogue where a block's sums meet:
+ * W4A16_ERR_WORKSPACE if w4a16_init reserved too little. */
+int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                          const uint32_t *zeros, int M, int N, int K, int group, int epilogue,
+                          const uint16_t *residual, uint16_t *y, void *stream);
 
 /* A decode round: the linears of `descs` (a HOST array of n_descs entries,
  * e.g. 64 layers x {qkv, o, gate+up, down}) run on `stream`, all at the same
@@ -158,6 +197,9 @@ typedef struct {
  * being captured, launch linear by linear; w4a16_round_graph_create captures
  * the fused form. */
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream);
+/* Each linear of a round applies its own epilogue, with the rules of
+ * w4a16_linear_epilogue; a linear's residual counts as one of its inputs for
+ * the ordering above. */
 
 /* Capture a decode round into an instantiated CUDA graph (an opaque handle in
  * *graph).  Allocates (the graph's own copy of a fused round's descriptors)

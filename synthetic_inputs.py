@@ -20,7 +20,9 @@ weights with per-group fp16 scale and 4-bit zero, fp16 activations):
   * qweight: uniform random 32-bit words = 8 iid uniform nibbles 0..15;
   * zeros:   uniform random words, nibbles past the last group set to 0;
   * scales:  fp16 of U[0.002, 0.02];
-  * x:       fp16 of N(0, 1) (Box-Muller, computed on the host only).
+  * x:       fp16 of N(0, 1) (Box-Muller, computed on the host only);
+  * residual (the epilogue's second input): fp16 of N(0, 4^2), a spread like
+    that of the linear's outputs, so that a dropped residual shows.
 """
 from __future__ import annotations
 
@@ -38,6 +40,7 @@ T_QWEIGHT = 1
 T_ZEROS = 2
 T_SCALES = 3
 T_X = 4
+T_RESIDUAL = 5
 
 
 def _signed(c: int) -> int:
@@ -124,11 +127,10 @@ def scales(seed: int, N: int, K: int, group: int = 128, rows=None, device="cpu",
     return v.to(torch.float32).to(torch.float16)
 
 
-def x(seed: int, M: int, K: int) -> torch.Tensor:
-    """[M, K] float16 CPU tensor of N(0, 1) draws (Box-Muller on the host)."""
+def _normal_f16(seed: int, tensor_id: int, M: int, K: int, std: float) -> torch.Tensor:
     n = M * K
     idx = np.arange(2 * ((n + 1) // 2), dtype=np.uint64)
-    h = hash_u64_numpy(seed, T_X, idx)
+    h = hash_u64_numpy(seed, tensor_id, idx)
     u = (h >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
     u1 = 1.0 - u[0::2]          # (0, 1]
     u2 = u[1::2]
@@ -137,7 +139,19 @@ def x(seed: int, M: int, K: int) -> torch.Tensor:
     z = np.empty(u.size, dtype=np.float64)
     z[0::2] = r * np.cos(t)
     z[1::2] = r * np.sin(t)
+    if std != 1.0:
+        z *= std
     return torch.from_numpy(z[:n].astype(np.float32).astype(np.float16).reshape(M, K))
+
+
+def x(seed: int, M: int, K: int) -> torch.Tensor:
+    """[M, K] float16 CPU tensor of N(0, 1) draws (Box-Muller on the host)."""
+    return _normal_f16(seed, T_X, M, K, 1.0)
+
+
+def residual(seed: int, M: int, N: int, std: float = 4.0) -> torch.Tensor:
+    """[M, N] float16 CPU tensor of N(0, std^2) draws."""
+    return _normal_f16(seed, T_RESIDUAL, M, N, std)
 
 
 def as_u32(t: torch.Tensor) -> np.ndarray:

@@ -70,6 +70,32 @@ def test_linear_validation_codes(w4):
         assert _lin(w4) == w4.W4A16_ERR_NOT_INITIALIZED
 
 
+def _epi(w4, epi, res=None, M=1, N=64, K=256, y=5 * A, group=128):
+    return w4.lib.w4a16_linear_epilogue(A, 2 * A, 3 * A, 4 * A, M, N, K, group, epi, res, y, None)
+
+
+def test_linear_epilogue_validation_codes(w4):
+    R, S = w4.EPILOGUE_RESIDUAL, w4.EPILOGUE_SILU_MUL
+    assert _epi(w4, 3) == w4.W4A16_ERR_INVALID_ARG           # no such epilogue
+    assert _epi(w4, -1) == w4.W4A16_ERR_INVALID_ARG
+    assert _epi(w4, R) == w4.W4A16_ERR_INVALID_ARG           # residual epilogue without one
+    assert _epi(w4, 0, res=6 * A) == w4.W4A16_ERR_INVALID_ARG  # a residual nobody adds
+    assert _epi(w4, S, res=6 * A) == w4.W4A16_ERR_INVALID_ARG
+    assert _epi(w4, S, N=48) == w4.W4A16_ERR_UNSUPPORTED     # N/2 not a multiple of 16
+    assert _epi(w4, R, res=6 * A + 1) == w4.W4A16_ERR_MISALIGNED
+    # the residual partly over y (y itself is allowed)
+    assert _epi(w4, R, res=5 * A + 2) == w4.W4A16_ERR_INVALID_ARG
+    # y of SiLU-and-mul is [M, N/2]: 64 bytes just below x do not overlap it,
+    # the 128 bytes of a plain y do
+    assert _epi(w4, S, y=A - 64) == _epi(w4, S, y=5 * A)
+    assert _epi(w4, 0, y=A - 64) == w4.W4A16_ERR_INVALID_ARG
+    if w4.lib.w4a16_device_sm_count() == 0:
+        assert _epi(w4, R, res=5 * A) == w4.W4A16_ERR_NOT_INITIALIZED  # in place
+        assert _epi(w4, R, res=6 * A) == w4.W4A16_ERR_NOT_INITIALIZED
+        assert _epi(w4, S) == w4.W4A16_ERR_NOT_INITIALIZED
+        assert _epi(w4, 0) == w4.W4A16_ERR_NOT_INITIALIZED
+
+
 def test_pack_dequant_validation_codes(w4):
     L = w4.lib
     assert L.w4a16_pack(None, A, 4, 256, 128, A, A, None) == w4.W4A16_ERR_INVALID_ARG
@@ -85,6 +111,12 @@ def test_decode_round_validates_every_descriptor(w4):
     descs[0] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 64, 256, 128)
     descs[1] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 64, 250, 128)  # bad K
     assert w4.lib.w4a16_decode_round(descs, 2, 4, None) == w4.W4A16_ERR_INVALID_ARG
+    descs[1] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 64, 256, 128, w4.EPILOGUE_RESIDUAL,
+                             None)  # residual epilogue without a residual
+    assert w4.lib.w4a16_decode_round(descs, 2, 4, None) == w4.W4A16_ERR_INVALID_ARG
+    descs[1] = w4.LinearDesc(A, 2 * A, 3 * A, 4 * A, 5 * A, 48, 256, 128, w4.EPILOGUE_SILU_MUL,
+                             None)  # N/2 not a multiple of 16
+    assert w4.lib.w4a16_decode_round(descs, 2, 4, None) == w4.W4A16_ERR_UNSUPPORTED
     assert w4.lib.w4a16_decode_round(descs, 0, 4, None) == w4.W4A16_ERR_INVALID_ARG
     h = ctypes.c_void_p()
     assert w4.lib.w4a16_round_graph_create(descs, 2, 4, None) == w4.W4A16_ERR_INVALID_ARG

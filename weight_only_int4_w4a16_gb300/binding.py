@@ -43,6 +43,10 @@ RUNG_MMA = 4
 RUNG_MMA_SPLITK = 5
 NUM_RUNGS = 6
 
+EPILOGUE_NONE = 0
+EPILOGUE_RESIDUAL = 1
+EPILOGUE_SILU_MUL = 2
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
@@ -51,7 +55,7 @@ _SZ = ctypes.c_size_t
 class LinearDesc(ctypes.Structure):
     """Mirror of ``w4a16_linear_desc``."""
     _fields_ = [("x", _P), ("qweight", _P), ("scales", _P), ("zeros", _P), ("y", _P),
-                ("N", _I), ("K", _I), ("group", _I)]
+                ("N", _I), ("K", _I), ("group", _I), ("epilogue", _I), ("residual", _P)]
 
 
 def _sig(name, args, res=_I):
@@ -69,6 +73,7 @@ _sig("w4a16_unpack", [_P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_dequant", [_P, _P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_linear_epilogue", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -86,6 +91,7 @@ _sig("w4a16_device_sm_count", [])
 
 EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
             "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_linear_noalloc",
+            "w4a16_linear_epilogue",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -213,16 +219,40 @@ def w4a16_linear_noalloc(x: torch.Tensor, qweight: torch.Tensor, scales: torch.T
     return y
 
 
+def w4a16_linear_epilogue(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                          zeros: torch.Tensor, epilogue: int, residual=None, group: int = GROUP,
+                          y=None, stream=None) -> torch.Tensor:
+    """w4a16_linear followed in the same kernel by an epilogue: EPILOGUE_RESIDUAL
+    (y [M, N] = h + residual [M, N]; residual may be y itself) or EPILOGUE_SILU_MUL
+    (y [M, N/2] = silu(h[:, :N/2]) * h[:, N/2:]), h = x @ W^T in fp32."""
+    M, K = x.shape
+    N = qweight.shape[0]
+    cols = N // 2 if epilogue == EPILOGUE_SILU_MUL else N
+    if y is None:
+        y = torch.empty((M, cols), dtype=torch.float16, device=x.device)
+    r = _dev(residual, torch.float16, "residual") if residual is not None else None
+    _check(lib.w4a16_linear_epilogue(_dev(x, torch.float16, "x"),
+                                     _dev(qweight, torch.int32, "qweight"),
+                                     _dev(scales, torch.float16, "scales"),
+                                     _dev(zeros, torch.int32, "zeros"), M, N, K, group, epilogue,
+                                     r, _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+           "w4a16_linear_epilogue")
+    return y
+
+
 def make_descs(layers) -> ctypes.Array:
-    """layers: iterable of dicts with x, qweight, scales, zeros, y tensors -> host desc array."""
+    """layers: iterable of dicts with x, qweight, scales, zeros, y tensors (and
+    optionally an epilogue code and a residual tensor) -> host desc array."""
     layers = list(layers)
     arr = (LinearDesc * len(layers))()
     for i, L in enumerate(layers):
         N, K = L["qweight"].shape[0], L["x"].shape[1]
+        res = L.get("residual")
         arr[i] = LinearDesc(_dev(L["x"], torch.float16, "x"), _dev(L["qweight"], torch.int32, "qweight"),
                             _dev(L["scales"], torch.float16, "scales"),
                             _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], torch.float16, "y"),
-                            N, K, L.get("group", GROUP))
+                            N, K, L.get("group", GROUP), L.get("epilogue", EPILOGUE_NONE),
+                            _dev(res, torch.float16, "residual") if res is not None else None)
     return arr
 
 

@@ -60,6 +60,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 constexpr int kMaxK = 1 << 22;
+static_assert(kEpiNone == W4A16_EPILOGUE_NONE && kEpiResidual == W4A16_EPILOGUE_RESIDUAL &&
+                  kEpiSiluMul == W4A16_EPILOGUE_SILU_MUL,
+              "internal epilogue codes follow the ABI");
 
 int check_shape(int N, int K, int group) {
     if (N < 1 || K < 1 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
@@ -69,15 +72,26 @@ int check_shape(int N, int K, int group) {
 }
 
 int check_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
-                 const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y) {
+                 const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y,
+                 int epi = W4A16_EPILOGUE_NONE, const uint16_t *residual = nullptr) {
     if (!x || !qweight || !scales || !zeros || !y) return W4A16_ERR_INVALID_ARG;
     if (M < 1 || M > kMaxM) return W4A16_ERR_INVALID_ARG;
     int st = check_shape(N, K, group);
     if (st) return st;
+    if (epi != W4A16_EPILOGUE_NONE && epi != W4A16_EPILOGUE_RESIDUAL &&
+        epi != W4A16_EPILOGUE_SILU_MUL)
+        return W4A16_ERR_INVALID_ARG;
+    // a residual exactly when the epilogue adds one
+    if ((epi == W4A16_EPILOGUE_RESIDUAL) != (residual != nullptr)) return W4A16_ERR_INVALID_ARG;
+    if (epi == W4A16_EPILOGUE_SILU_MUL && N % 32 != 0) return W4A16_ERR_UNSUPPORTED;
     if (!aligned(x, 16) || !aligned(qweight, 16) || !aligned(y, 16) || !aligned(scales, 2) ||
-        !aligned(zeros, 4))
+        !aligned(zeros, 4) || (residual && !aligned(residual, 2)))
         return W4A16_ERR_MISALIGNED;
-    if (overlaps(x, (size_t)M * K * 2, y, (size_t)M * N * 2)) return W4A16_ERR_INVALID_ARG;
+    const size_t ybytes = (size_t)M * out_cols(N, epi) * 2;
+    if (overlaps(x, (size_t)M * K * 2, y, ybytes)) return W4A16_ERR_INVALID_ARG;
+    // the residual is y itself (y += x W^T) or lies apart from it
+    if (residual && residual != y && overlaps(residual, ybytes, y, ybytes))
+        return W4A16_ERR_INVALID_ARG;
     return W4A16_OK;
 }
 
@@ -97,9 +111,14 @@ int tile_tokens(int rung) {
     return is_tc(rung) ? kTcMaxTokens : (is_mma(rung) ? kMmaMaxTokens : kGemvMaxTokens);
 }
 
-Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
+Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi = kEpiNone) {
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
     const int G = K / kGroup;
+    if (epi != kEpiNone) {
+        // the epilogues run in the warp-MMA kernel only: up to 8 tokens
+        if (M > kMmaMaxTokens || (forced != W4A16_RUNG_AUTO && !is_mma(forced)))
+            return {forced, W4A16_ERR_UNSUPPORTED};
+    }
     switch (forced) {
         case W4A16_RUNG_GEMV: {
             GemvPlan p = plan_gemv(Mt, N, K, 0, dev);
@@ -112,14 +131,14 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced) {
         case W4A16_RUNG_TC:
             return {W4A16_RUNG_TC, W4A16_OK};
         case W4A16_RUNG_MMA: {
-            MmaPlan p = plan_mma(Mt, N, K, 0, dev);
+            MmaPlan p = plan_mma(Mt, N, K, 0, dev, epi);
             return {W4A16_RUNG_MMA, p.ok ? W4A16_OK : W4A16_ERR_UNSUPPORTED};
         }
         default:
             break;
     }
     if (M <= kMmaMaxTokens) {
-        MmaPlan p = plan_mma(Mt, N, K, -1, dev);
+        MmaPlan p = plan_mma(Mt, N, K, -1, dev, epi);
         return {p.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, W4A16_OK};
     }
     const int Mtc = M < kTcMaxTokens ? M : kTcMaxTokens;
@@ -142,7 +161,7 @@ int split_rule(int rung) {
 // Workspace bytes and counters one launch of `rung` needs for Mt tokens;
 // false if the rung cannot run the shape.
 bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t *bytes,
-                  int *counters) {
+                  int *counters, int epi) {
     if (is_tc(rung)) {
         TcPlan p = plan_tc(Mt, N, K, split_rule(rung), dev);
         *bytes = p.ws_bytes;
@@ -150,9 +169,9 @@ bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t 
         return p.ok;
     }
     if (is_mma(rung)) {
-        MmaPlan p = plan_mma(Mt, N, K, split_rule(rung), dev);
+        MmaPlan p = plan_mma(Mt, N, K, split_rule(rung), dev, epi);
         *bytes = p.ws_bytes;
-        *counters = p.S > 1 ? p.n_blocks : 0;
+        *counters = p.reduce ? p.n_blocks : 0;
         return p.ok;
     }
     GemvPlan p = plan_gemv(Mt, N, K, split_rule(rung), dev);
@@ -161,7 +180,8 @@ bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t 
     return p.ok;
 }
 
-size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *status) {
+size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *status,
+                     int epi = kEpiNone) {
     const int tt = tile_tokens(rung);
     size_t need = 0;
     *status = W4A16_OK;
@@ -171,7 +191,7 @@ size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *
         if (Mt == 0) continue;
         size_t b = 0;
         int c = 0;
-        if (!launch_needs(rung, Mt, N, K, dev, &b, &c)) {
+        if (!launch_needs(rung, Mt, N, K, dev, &b, &c, epi)) {
             *status = W4A16_ERR_UNSUPPORTED;
             return 0;
         }
@@ -181,9 +201,9 @@ size_t workspace_for(int rung, int M, int N, int K, const DeviceInfo &dev, int *
     return need;
 }
 
-int check_workspace(int rung, int M, int N, int K, const State &st) {
+int check_workspace(int rung, int M, int N, int K, const State &st, int epi = kEpiNone) {
     int status = W4A16_OK;
-    size_t need = workspace_for(rung, M, N, K, st.dev, &status);
+    size_t need = workspace_for(rung, M, N, K, st.dev, &status, epi);
     if (status) return status;
     if (need > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
     return W4A16_OK;
@@ -192,17 +212,19 @@ int check_workspace(int rung, int M, int N, int K, const State &st) {
 int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t stream) {
     cudaError_t e = cudaSuccess;
     const int tt = tile_tokens(rung);
+    const int ycols = out_cols(a.N, a.epi);
     for (int m0 = 0; m0 < a.M && e == cudaSuccess; m0 += tt) {
         const int Mt = a.M - m0 < tt ? a.M - m0 : tt;
         LinearArgs t = a;
         t.x = a.x + (size_t)m0 * a.K;
-        t.y = a.y + (size_t)m0 * a.N;
+        t.y = a.y + (size_t)m0 * ycols;
+        if (a.residual) t.residual = a.residual + (size_t)m0 * ycols;
         t.M = Mt;
         if (is_tc(rung)) {
             TcPlan p = plan_tc(Mt, a.N, a.K, split_rule(rung), st.dev);
             e = launch_tc(t, p, st.ws, st.ws.status, stream);
         } else if (is_mma(rung)) {
-            MmaPlan p = plan_mma(Mt, a.N, a.K, split_rule(rung), st.dev);
+            MmaPlan p = plan_mma(Mt, a.N, a.K, split_rule(rung), st.dev, a.epi);
             e = launch_mma(t, p, st.ws, stream);
         } else {
             GemvPlan p = plan_gemv(Mt, a.N, a.K, split_rule(rung), st.dev);
@@ -229,20 +251,22 @@ int parse_rung(const char *s) {
 
 int linear_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                 const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
-                void *stream, bool validated) {
+                void *stream, bool validated, int epi = kEpiNone,
+                const uint16_t *residual = nullptr) {
     if (!validated) {
-        int st = check_linear(x, qweight, scales, zeros, M, N, K, group, y);
+        int st = check_linear(x, qweight, scales, zeros, M, N, K, group, y, epi, residual);
         if (st) return st;
     }
     const State &s = g_state;
     if (!s.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    Decision d = decide(M, N, K, s.dev, s.forced_rung);
+    Decision d = decide(M, N, K, s.dev, s.forced_rung, epi);
     if (d.status) return d.status;
-    int st = check_workspace(d.rung, M, N, K, s);
+    int st = check_workspace(d.rung, M, N, K, s, epi);
     if (st) return st;
     LinearArgs a{reinterpret_cast<const __half *>(x), qweight,
                  reinterpret_cast<const __half *>(scales), zeros,
-                 reinterpret_cast<__half *>(y), M, N, K};
+                 reinterpret_cast<__half *>(y), M, N, K, epi,
+                 reinterpret_cast<const __half *>(residual)};
     return launch_linear(a, d.rung, s, (cudaStream_t)stream);
 }
 
@@ -276,28 +300,34 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
         const w4a16_linear_desc &d = descs[l];
         // the last linears of a round come in small units: the CTAs then
         // run out of work within a small unit of each other
-        MmaPlan p = plan_mma(M, d.N, d.K, l >= n - kRoundTailLinears ? 3 : 2, st.dev);
+        MmaPlan p = plan_mma(M, d.N, d.K, l >= n - kRoundTailLinears ? 3 : 2, st.dev, d.epilogue);
         if (!p.ok) return W4A16_ERR_UNSUPPORTED;
         float *part = nullptr;
         unsigned *cnt = nullptr;
-        if (p.S > 1) {
+        if (p.reduce) {  // split K, or SiLU-and-mul
             part = st.ws.partials + partial_floats;
-            partial_floats += ((size_t)p.S * M * d.N + 63) / 64 * 64;
+            partial_floats += (p.ws_bytes / sizeof(float) + 63) / 64 * 64;
             cnt = st.ws.counters + counters;
             counters += p.n_blocks;
         }
+        // what a linear reads (x, the residual) and writes (y)
         int wait_for = -1;
+        const size_t dy = bytes_of(M, out_cols(d.N, d.epilogue));
         for (int j = l - 1; j >= 0 && wait_for < 0; --j) {
             const w4a16_linear_desc &e = descs[j];
-            if (overlaps(e.y, bytes_of(M, e.N), d.x, bytes_of(M, d.K)) ||
-                overlaps(e.x, bytes_of(M, e.K), d.y, bytes_of(M, d.N)) ||
-                overlaps(e.y, bytes_of(M, e.N), d.y, bytes_of(M, d.N)))
+            const size_t ey = bytes_of(M, out_cols(e.N, e.epilogue));
+            if (overlaps(e.y, ey, d.x, bytes_of(M, d.K)) ||
+                (d.residual && overlaps(e.y, ey, d.residual, dy)) ||
+                overlaps(e.x, bytes_of(M, e.K), d.y, dy) ||
+                (e.residual && overlaps(e.residual, ey, d.y, dy)) ||
+                overlaps(e.y, ey, d.y, dy))
                 wait_for = j;
         }
         waits |= wait_for >= 0;
         LinearArgs a{reinterpret_cast<const __half *>(d.x), d.qweight,
                      reinterpret_cast<const __half *>(d.scales), d.zeros,
-                     reinterpret_cast<__half *>(d.y), M, d.N, d.K};
+                     reinterpret_cast<__half *>(d.y), M, d.N, d.K, d.epilogue,
+                     reinterpret_cast<const __half *>(d.residual)};
         cudaError_t e = mma_describe(a, p, part, cnt, units, wait_for, &fr->descs[l]);
         if (e != cudaSuccess) return cuda_fail(e);
         units += p.units;
@@ -323,7 +353,8 @@ int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
     if (!descs || n_descs < 1) return W4A16_ERR_INVALID_ARG;
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
-        int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y);
+        int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y,
+                              d.epilogue, d.residual);
         if (st) return st;
     }
     if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
@@ -334,15 +365,15 @@ int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
 int round_per_linear(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
-        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung);
+        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung, d.epilogue);
         if (dec.status) return dec.status;
-        int st = check_workspace(dec.rung, M, d.N, d.K, g_state);
+        int st = check_workspace(dec.rung, M, d.N, d.K, g_state, d.epilogue);
         if (st) return st;
     }
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
         int st = linear_impl(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y, stream,
-                             true);
+                             true, d.epilogue, d.residual);
         if (st) return st;
     }
     return W4A16_OK;
@@ -473,6 +504,13 @@ int w4a16_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *sca
                  const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
                  void *stream) {
     return linear_impl(x, qweight, scales, zeros, M, N, K, group, y, stream, false);
+}
+
+int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                          const uint32_t *zeros, int M, int N, int K, int group, int epilogue,
+                          const uint16_t *residual, uint16_t *y, void *stream) {
+    return linear_impl(x, qweight, scales, zeros, M, N, K, group, y, stream, false, epilogue,
+                       residual);
 }
 
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {

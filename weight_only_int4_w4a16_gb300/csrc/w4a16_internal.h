@@ -12,8 +12,15 @@ namespace w4a16 {
 
 constexpr int kGroup = 128;  // inputs per quantisation group
 
-// One W4A16 linear, device pointers.  x [M, K], y [M, N] fp16; qw [N, K/8];
-// scales [N, G] fp16; zeros [N, ceil(G/8)].
+// What follows the linear in the same kernel (the values of w4a16_epilogue):
+// nothing; y = h + residual; y = silu(h[:, :N/2]) * h[:, N/2:], h = x W^T.
+constexpr int kEpiNone = 0;
+constexpr int kEpiResidual = 1;
+constexpr int kEpiSiluMul = 2;
+
+// One W4A16 linear, device pointers.  x [M, K] fp16; qw [N, K/8]; scales
+// [N, G] fp16; zeros [N, ceil(G/8)]; y [M, N] fp16 ([M, N/2] for SiLU-and-mul);
+// residual [M, N] fp16 (the residual epilogue only).
 struct LinearArgs {
     const __half *x;
     const uint32_t *qw;
@@ -21,7 +28,12 @@ struct LinearArgs {
     const uint32_t *zeros;
     __half *y;
     int M, N, K;
+    int epi = kEpiNone;
+    const __half *residual = nullptr;
 };
+
+// Output columns of a linear with epilogue epi.
+inline int out_cols(int N, int epi) { return epi == kEpiSiluMul ? N / 2 : N; }
 
 // Library-owned scratch for the split-K rungs: fp32 partial outputs and one
 // arrival counter per output tile (zeroed at init, reset by the reducing CTA).
@@ -87,6 +99,8 @@ constexpr int kMmaMaxTokens = 8;  // tokens per launch (the MMA's N = 8)
 // The work of one linear is cut into units: one K slice of 8 * strips_per_warp
 // strips of 16 rows (strips_per_warp per warp of a CTA, which stages the
 // slice's activations once for all of them).  CTAs take units round-robin.
+// With SiLU-and-mul a strip is logical: 16 gate rows and the 16 up rows N/2
+// below them, computed one after the other by the same warp.
 struct MmaPlan {
     bool ok;
     int M;             // tokens (1..8)
@@ -96,6 +110,8 @@ struct MmaPlan {
     int strips_per_warp;
     int n_blocks;      // units per slice: ceil(n_strips / (8 * strips_per_warp))
     int units;         // S * n_blocks
+    bool reduce;       // sums go to the workspace, a block's last CTA reduces them
+                       // (S > 1, or SiLU-and-mul); n_blocks arrival counters
     int grid;          // CTAs of a launch of this linear alone
     int smem_bytes;    // dynamic shared memory of such a launch
     size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
@@ -109,10 +125,15 @@ struct MmaLinDesc {
     const __half *scales;
     const uint32_t *zeros;
     __half *y;
-    float *partials;      // this linear's split-K partials (S > 1)
-    unsigned *counters;   // this linear's per-strip arrival counters (S > 1)
+    float *partials;      // this linear's partial sums (S > 1 or SiLU-and-mul)
+    unsigned *counters;   // this linear's per-block arrival counters (the same)
     uintptr_t scales_first;  // the aligned word holding the first scale
     uintptr_t scales_end;    // one past the last byte of the scales array
+    const __half *residual;  // kEpiResidual: [M, N], read before y is written
+    int epi;                 // kEpiNone, kEpiResidual or kEpiSiluMul
+    int ycols;               // columns of y (and of the residual)
+    int half_strips;         // kEpiSiluMul: strips of the gate half (the up strip of
+                             // logical strip s is strip s + half_strips)
     int N, K, G, ZW, M, S, slice_groups, n_strips, strips_per_warp, n_blocks;
     int unit_start;  // index of the linear's first unit in the fused list
     int xstride;     // bytes per staged token row
@@ -124,7 +145,7 @@ struct MmaLinDesc {
 // kRoundStripsPerWarp strips per warp (the round's units balance each other),
 // 3 = the same slices with one strip per warp (the round's last linears, so
 // that the CTAs finish together).
-MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev);
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi = kEpiNone);
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,

@@ -85,8 +85,10 @@ struct UnitInfo {
     float *partials;
     unsigned *counters;
     uintptr_t scales_first, scales_end;
+    const __half *residual;
     int l, slice, sb;  // linear, K slice, strip block (l < 0: the queue has ended)
     int N, K, G, ZW, M, S, slice_groups, n_strips, strips_per_warp, xstride, wait_for;
+    int epi, ycols, half_strips;
     int seq;  // the queue position this entry holds (written last)
 };
 constexpr int kSlots = 8;  // one per queue position (mod 8)
@@ -228,23 +230,40 @@ constexpr int kFlagRed = 2;     // 2 x 3 ints: whether this CTA reduces a block,
 constexpr int kFlagQueue = 8;   // 8 ints: the CTA's units by sequence index (mod 8)
 constexpr int kQueueAhead = 1;  // units fetched ahead of the one being consumed
 
-// y = the sum of the S partial slices of block sb of a linear, by the whole CTA
+// The epilogue of one output: y = h, h + residual, or silu(gate) * h (the
+// up projection h and its gate both in fp32; silu(g) = g / (1 + e^-g)).
+template <class Lin>
+__device__ __forceinline__ void epilogue_store(const Lin &R, size_t o, float h, float gate) {
+    if (R.epi == kEpiResidual) h += __half2float(R.residual[o]);
+    else if (R.epi == kEpiSiluMul) h *= gate / (1.f + expf(-gate));
+    R.y[o] = __float2half_rn(h);
+}
+
+// y = the epilogue of the sum of the S partial slices of block sb of a linear,
+// by the whole CTA.  With SiLU-and-mul an output needs its gate row and its up
+// row: half of the sums a thread keeps are gate rows, the other half the up
+// rows of the same outputs (the register footprint stays that of 8 sums: the
+// callers keep their registers across this call).
 __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
-    const int nrows = min(R.N - row0, rows_per_block);
+    const int nrows = min(R.ycols - row0, rows_per_block);
     const int n_out = R.M * nrows;
-    // each thread sums up to 8 outputs at a time, the 8 loads of one slice in
+    const bool silu = R.epi == kEpiSiluMul;
+    const size_t up = (size_t)R.half_strips * 16;  // the up rows sit N/2 below the gate rows
+    // each thread sums up to 8 rows at a time, the 8 loads of one slice in
     // flight together (slices in order: the sum is the same every launch)
-    constexpr int kR = 8;
-    for (int base = 0; base < n_out; base += kThreads * kR) {
+    constexpr int kR = 8, kH = kR / 2;
+    const int per = silu ? kH : kR;  // outputs per thread and pass
+    for (int base = 0; base < n_out; base += kThreads * per) {
         float sum[kR];
         size_t off[kR];
 #pragma unroll
         for (int j = 0; j < kR; ++j) {
-            const int i = base + j * kThreads + threadIdx.x;
+            const int jo = silu ? (j & (kH - 1)) : j;  // the output of sum j
+            const int i = base + jo * kThreads + threadIdx.x;
             const int t = i / nrows, row = row0 + i - t * nrows;
-            off[j] = i < n_out ? (size_t)t * R.N + row : 0;
+            off[j] = i < n_out ? (size_t)t * R.N + row + (silu && j >= kH ? up : 0) : 0;
             sum[j] = 0.f;
         }
         for (int s2 = 0; s2 < R.S; ++s2) {
@@ -258,7 +277,11 @@ __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
 #pragma unroll
         for (int j = 0; j < kR; ++j) {
             const int i = base + j * kThreads + threadIdx.x;
-            if (i < n_out) R.y[off[j]] = __float2half_rn(sum[j]);
+            if ((silu && j >= kH) || i >= n_out) continue;
+            const int t = i / nrows, row = row0 + i - t * nrows;
+            const size_t o = (size_t)t * R.ycols + row;
+            if (silu) epilogue_store(R, o, sum[j + kH], sum[j]);
+            else epilogue_store(R, o, sum[j], 0.f);
         }
     }
     if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
@@ -315,6 +338,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             U.counters = D.counters;
             U.scales_first = D.scales_first;
             U.scales_end = D.scales_end;
+            U.residual = D.residual;
+            U.epi = D.epi;
+            U.ycols = D.ycols;
+            U.half_strips = D.half_strips;
             U.N = D.N;
             U.K = D.K;
             U.G = D.G;
@@ -366,8 +393,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int is_avail = 0;             // bytes from is_s to the end of the scales (0 past row N)
     uintptr_t is_z = 0;           // zeros word of the next stage
     uint32_t is_zbytes = 0;
-    // this warp's strips in a unit: strip0 + 8r for r < strips per warp
-    int i_strip = 0, i_last = 0;  // current strip, last strip of the unit for this warp
+    // this warp's strips in a unit: strip0 + 8r for r < strips per warp; with
+    // SiLU-and-mul the gate strip s, then the up strip s + half_strips
+    int i_strip = 0, i_last = 0;  // current strip (of weight rows), the unit's last gate strip
     const UnitInfo *iD = nullptr;
     // copy sources of the issue cursor's strip
     auto i_strip_enter = [&]() {
@@ -452,8 +480,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // starts with every second stage
         if (((i_g0 + (ij + 1) * kStageGroups) & 7) == 0) is_z += 4;
         if (++ij == inst) {
-            if (i_strip < i_last) {  // the warp's next strip of the unit
-                i_strip += kWarps;
+            // gate strip: its up strip next; then the next gate strip
+            const int up = iD->epi == kEpiSiluMul ? iD->half_strips : 0;
+            if (up && i_strip < up) {
+                i_strip += up;
+                i_strip_enter();
+            } else if (i_strip - up < i_last) {  // the warp's next strip of the unit
+                i_strip += kWarps - up;
                 i_strip_enter();
             } else {
                 ++ik;
@@ -707,132 +740,153 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // otherwise hold up warp 0, and with it the staging
         count_arrival();
         // this warp's strips of the unit: strip0, strip0 + 8, ... (the tail
-        // block of a slice may hold fewer)
+        // block of a slice may hold fewer); with SiLU-and-mul each is the
+        // strip's gate rows, then its up rows
+        const int nparts = D.epi == kEpiSiluMul ? 2 : 1;
+        // The block's sums go to the workspace and the CTA that brings the
+        // last slice reduces them (reduce_block, which applies the epilogue)
+        // with split K, and always with SiLU-and-mul: its gate and up sums
+        // meet there, so that no warp keeps the gate sums in registers
+        // across the up rows (registers every linear would pay for).
+        const bool to_ws = D.S > 1 || nparts == 2;
         for (int strip = sb * kWarps * D.strips_per_warp + warp, rs = 0;
              rs < D.strips_per_warp && strip < D.n_strips; ++rs, strip += kWarps) {
             // lanes of tokens >= M compute a column nobody stores: they read token 0
             const int tok = g < M ? g : 0;
             const uint8_t *xrow = xs + (size_t)tok * D.xstride;
-            const int ra = strip * 16 + g, rb = ra + 8;
-            const bool va = ra < D.N, vb = rb < D.N;
-            // where the slice's first scale of each row sits in its aligned word
-            // (the same in every stage: a stage advances 8 bytes)
-            const uint32_t offA =
-                (uint32_t)(((uintptr_t)(D.scales + (size_t)(va ? ra : 0) * D.G + g0)) >> 1) & 1u;
-            const uint32_t offB =
-                (uint32_t)(((uintptr_t)(D.scales + (size_t)(vb ? rb : 0) * D.G + g0)) >> 1) & 1u;
-            const uint32_t shA = 16u * offA, shB = 16u * offB;
-            const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < nst; ++j) {
-                // the issue cursor may have stopped at a unit the queue did not
-                // hold yet: this stage belongs to a unit it holds
-                if (t_iss == t_cons) issue_next();
-                const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
-                    if (lane == 0) {
-                        atomicOr(P.status, kErrMmaWait);
-                        vflags[kFlagAbort] = 1;  // the other warps stop at their next unit
+            float acc[4];
+            for (int part = 0; part < nparts; ++part) {
+                const int ra = (strip + (part ? D.half_strips : 0)) * 16 + g, rb = ra + 8;
+                const bool va = ra < D.N, vb = rb < D.N;
+                // where the slice's first scale of each row sits in its aligned word
+                // (the same in every stage: a stage advances 8 bytes)
+                const uintptr_t s0A = (uintptr_t)(D.scales + (size_t)(va ? ra : 0) * D.G + g0);
+                const uintptr_t s0B = (uintptr_t)(D.scales + (size_t)(vb ? rb : 0) * D.G + g0);
+                const uint32_t offA = (uint32_t)(s0A >> 1) & 1u, offB = (uint32_t)(s0B >> 1) & 1u;
+                const uint32_t shA = 16u * offA, shB = 16u * offB;
+                const uint32_t selA = offA ? 0x54u : 0x32u, selB = offB ? 0x54u : 0x32u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+                for (int j = 0; j < nst; ++j) {
+                    // the issue cursor may have stopped at a unit the queue did not
+                    // hold yet: this stage belongs to a unit it holds
+                    if (t_iss == t_cons) issue_next();
+                    const uint32_t slot = t_cons & 1u, par = (t_cons >> 1) & 1u;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * slot, par))) {
+                        if (lane == 0) {
+                            atomicOr(P.status, kErrMmaWait);
+                            vflags[kFlagAbort] = 1;  // the other warps stop at their next unit
+                        }
+                        dead = true;
+                        break;
                     }
-                    dead = true;
-                    break;
+                    // this lane's part of the stage: 16 bytes of rows g and g + 8 of
+                    // each group (read just before the group), the metadata of both rows
+                    const uint8_t *st = wring + slot * kStageBytes;
+                    const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
+                    const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
+                    const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
+                    // zero nibbles of the stage's groups: the stage starts at group
+                    // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
+                    const uint32_t zsh = ((g0 + j * kStageGroups) & 4) ? 16u : 0u;
+                    const uint32_t zwA = ma.w >> zsh, zwB = mb.w >> zsh;
+                    const uint32_t mA[3] = {ma.x, ma.y, ma.z}, mB[3] = {mb.x, mb.y, mb.z};
+                    const int n_in = min(kStageGroups, ng - j * kStageGroups);
+                    const uint8_t *xg = xrow + (size_t)j * (kStageGroups * 256);
+                    const float *sg = sums + (j * kStageGroups) * 8 + 2 * c;  // tokens 2c, 2c+1
+                    // one group of the stage
+                    auto group = [&](const int i) {
+                        // scales of rows ra and rb: half (off + i) of the words
+                        uint32_t hA, hB;
+                        if (i & 1) {
+                            hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
+                            hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
+                        } else {
+                            hA = mA[i >> 1] >> shA;
+                            hB = mB[i >> 1] >> shB;
+                        }
+                        const float sA = __half2float(__ushort_as_half((unsigned short)hA));
+                        const float sB = __half2float(__ushort_as_half((unsigned short)hB));
+                        // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
+                        const float zA =
+                            __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
+                        const float zB =
+                            __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
+                        // S * 2^-20 of tokens 2c, 2c + 1
+                        const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);
+                        const uint8_t *xi = xg + i * 256;
+                        uint4 xv[4];
+                        xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
+                        xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
+                        xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
+                        xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
+                        const uint4 wa = *reinterpret_cast<const uint4 *>(stA + i * 1024);
+                        const uint4 wb = *reinterpret_cast<const uint4 *>(stB + i * 1024);
+                        const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+                        const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+                        float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int uu = 0; uu < 4; ++uu) {
+                            const uint32_t a = wA[uu], b = wB[uu], a8 = a >> 8, b8 = b >> 8;
+                            mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
+                                     b8 & 0x000f000fu, xv[uu].x, xv[uu].y);
+                            mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
+                                     b8 & 0x00f000f0u, xv[uu].z, xv[uu].w);
+                        }
+                        // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
+                        acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
+                        acc[1] = fmaf(sA, fmaf(-zA, sx.y, fmaf(16.f, dl[1], dh[1])), acc[1]);
+                        acc[2] = fmaf(sB, fmaf(-zB, sx.x, fmaf(16.f, dl[2], dh[2])), acc[2]);
+                        acc[3] = fmaf(sB, fmaf(-zB, sx.y, fmaf(16.f, dl[3], dh[3])), acc[3]);
+                    };
+                    if (n_in == kStageGroups) {
+#pragma unroll
+                        for (int i = 0; i < kStageGroups; ++i) group(i);
+                    } else {  // the last stage of a slice that ends at K
+#pragma unroll
+                        for (int i = 0; i < kStageGroups; ++i)
+                            if (i < n_in) group(i);
+                    }
+                    // Refill the slot kDepth stages ahead once every lane is done with
+                    // it.  The lanes read it through the generic proxy and the box
+                    // lands through the async proxy: the proxy fence orders those
+                    // reads before the new box's writes.
+                    __syncwarp();
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    ++t_cons;
+                    issue_next();
                 }
-                // this lane's part of the stage: 16 bytes of rows g and g + 8 of
-                // each group (read just before the group), the metadata of both rows
-                const uint8_t *st = wring + slot * kStageBytes;
-                const uint8_t *stA = st + g * 64 + 16 * c, *stB = st + (g + 8) * 64 + 16 * c;
-                const uint4 ma = *reinterpret_cast<const uint4 *>(st + kStageW + g * 16);
-                const uint4 mb = *reinterpret_cast<const uint4 *>(st + kStageW + (g + 8) * 16);
-                // zero nibbles of the stage's groups: the stage starts at group
-                // g0 + 4j, nibble (g0 + 4j) % 8 of its zeros word
-                const uint32_t zsh = ((g0 + j * kStageGroups) & 4) ? 16u : 0u;
-                const uint32_t zwA = ma.w >> zsh, zwB = mb.w >> zsh;
-                const uint32_t mA[3] = {ma.x, ma.y, ma.z}, mB[3] = {mb.x, mb.y, mb.z};
-                const int n_in = min(kStageGroups, ng - j * kStageGroups);
-                const uint8_t *xg = xrow + (size_t)j * (kStageGroups * 256);
-                const float *sg = sums + (j * kStageGroups) * 8 + 2 * c;  // tokens 2c, 2c+1
-                // one group of the stage
-                auto group = [&](const int i) {
-                    // scales of rows ra and rb: half (off + i) of the words
-                    uint32_t hA, hB;
-                    if (i & 1) {
-                        hA = dev::prmt(mA[i >> 1], mA[(i >> 1) + 1], selA);
-                        hB = dev::prmt(mB[i >> 1], mB[(i >> 1) + 1], selB);
-                    } else {
-                        hA = mA[i >> 1] >> shA;
-                        hB = mB[i >> 1] >> shB;
-                    }
-                    const float sA = __half2float(__ushort_as_half((unsigned short)hA));
-                    const float sB = __half2float(__ushort_as_half((unsigned short)hB));
-                    // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
-                    const float zA =
-                        __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
-                    const float zB =
-                        __uint_as_float(0x4b000000u | ((zwB >> (4 * i)) & 0xfu)) - 8388608.f;
-                    const float2 sx = *reinterpret_cast<const float2 *>(sg + i * 8);  // S * 2^-20
-                    const uint8_t *xi = xg + i * 256;
-                    uint4 xv[4];
-                    xv[0] = *reinterpret_cast<const uint4 *>(xi + xo0);
-                    xv[1] = *reinterpret_cast<const uint4 *>(xi + xo1);
-                    xv[2] = *reinterpret_cast<const uint4 *>(xi + xo2);
-                    xv[3] = *reinterpret_cast<const uint4 *>(xi + xo3);
-                    const uint4 wa = *reinterpret_cast<const uint4 *>(stA + i * 1024);
-                    const uint4 wb = *reinterpret_cast<const uint4 *>(stB + i * 1024);
-                    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
-                    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
-                    float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
-    #pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        const uint32_t a = wA[uu], b = wB[uu], a8 = a >> 8, b8 = b >> 8;
-                        mma16816(dl, a & 0x000f000fu, b & 0x000f000fu, a8 & 0x000f000fu,
-                                 b8 & 0x000f000fu, xv[uu].x, xv[uu].y);
-                        mma16816(dh, a & 0x00f000f0u, b & 0x00f000f0u, a8 & 0x00f000f0u,
-                                 b8 & 0x00f000f0u, xv[uu].z, xv[uu].w);
-                    }
-                    // 2^-20 sum (q - z) x = 16 D_lo + D_hi - z S 2^-20
-                    acc[0] = fmaf(sA, fmaf(-zA, sx.x, fmaf(16.f, dl[0], dh[0])), acc[0]);
-                    acc[1] = fmaf(sA, fmaf(-zA, sx.y, fmaf(16.f, dl[1], dh[1])), acc[1]);
-                    acc[2] = fmaf(sB, fmaf(-zB, sx.x, fmaf(16.f, dl[2], dh[2])), acc[2]);
-                    acc[3] = fmaf(sB, fmaf(-zB, sx.y, fmaf(16.f, dl[3], dh[3])), acc[3]);
-                };
-                if (n_in == kStageGroups) {
-    #pragma unroll
-                    for (int i = 0; i < kStageGroups; ++i) group(i);
-                } else {  // the last stage of a slice that ends at K
-    #pragma unroll
-                    for (int i = 0; i < kStageGroups; ++i)
-                        if (i < n_in) group(i);
+                if (dead) break;
+
+                // ---- end of the rows: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
+                const int t0 = 2 * c, t1 = 2 * c + 1;
+                if (to_ws) {  // this slice's partial sums, by weight row
+                    float *ps = D.partials + (size_t)slice * M * D.N;
+                    if (va && t0 < M) ps[(size_t)t0 * D.N + ra] = acc[0];
+                    if (va && t1 < M) ps[(size_t)t1 * D.N + ra] = acc[1];
+                    if (vb && t0 < M) ps[(size_t)t0 * D.N + rb] = acc[2];
+                    if (vb && t1 < M) ps[(size_t)t1 * D.N + rb] = acc[3];
+                    continue;
                 }
-                // Refill the slot kDepth stages ahead once every lane is done with
-                // it.  The lanes read it through the generic proxy and the box
-                // lands through the async proxy: the proxy fence orders those
-                // reads before the new box's writes.
-                __syncwarp();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                ++t_cons;
-                issue_next();
+                // y, or y + residual (read as fp32, one rounding)
+                const size_t ya = (size_t)t0 * D.ycols + ra, yb = (size_t)t0 * D.ycols + rb;
+                if (D.epi == kEpiResidual) {
+                    if (va && t0 < M) acc[0] += __half2float(D.residual[ya]);
+                    if (va && t1 < M) acc[1] += __half2float(D.residual[ya + D.ycols]);
+                    if (vb && t0 < M) acc[2] += __half2float(D.residual[yb]);
+                    if (vb && t1 < M) acc[3] += __half2float(D.residual[yb + D.ycols]);
+                }
+                if (va && t0 < M) D.y[ya] = __float2half_rn(acc[0]);
+                if (va && t1 < M) D.y[ya + D.ycols] = __float2half_rn(acc[1]);
+                if (vb && t0 < M) D.y[yb] = __float2half_rn(acc[2]);
+                if (vb && t1 < M) D.y[yb + D.ycols] = __float2half_rn(acc[3]);
             }
             if (dead) break;
-
-            // ---- end of strip: acc[0..1] row ra, tokens 2c, 2c+1; acc[2..3] row rb
-    #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
-            const int t0 = 2 * c, t1 = 2 * c + 1;
-            if (D.S == 1) {
-                if (va && t0 < M) D.y[(size_t)t0 * D.N + ra] = __float2half_rn(acc[0]);
-                if (va && t1 < M) D.y[(size_t)t1 * D.N + ra] = __float2half_rn(acc[1]);
-                if (vb && t0 < M) D.y[(size_t)t0 * D.N + rb] = __float2half_rn(acc[2]);
-                if (vb && t1 < M) D.y[(size_t)t1 * D.N + rb] = __float2half_rn(acc[3]);
-                continue;
-            }
-            float *part = D.partials + (size_t)slice * M * D.N;
-            if (va && t0 < M) part[(size_t)t0 * D.N + ra] = acc[0];
-            if (va && t1 < M) part[(size_t)t1 * D.N + ra] = acc[1];
-            if (vb && t0 < M) part[(size_t)t0 * D.N + rb] = acc[2];
-            if (vb && t1 < M) part[(size_t)t1 * D.N + rb] = acc[3];
         }
         if (dead) break;
-        if (D.S > 1) {  // count this unit's arrival at the next boundary
+        if (to_ws) {  // count this unit's arrival at the next boundary
             arr_l = cl;
             arr_sb = sb;
             arr_cnt = D.counters;
@@ -915,12 +969,15 @@ int mma_smem_bytes(int M, int slice_groups) {
 
 int mma_round_grid(const DeviceInfo &dev) { return kCtasPerSm * dev.sm_count; }
 
-MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
     MmaPlan pl{};
     pl.M = M;
     const int G = K / kGroup;
-    pl.n_strips = (N + 15) / 16;
-    pl.strips_per_warp = split == 2 ? kRoundStripsPerWarp : 1;
+    // SiLU-and-mul: a logical strip is a gate strip and its up strip (N/2 a
+    // multiple of 16), twice the work of a strip
+    const int work = epi == kEpiSiluMul ? 2 : 1;
+    pl.n_strips = (out_cols(N, epi) + 15) / 16;
+    pl.strips_per_warp = split == 2 ? kRoundStripsPerWarp / work : 1;
     if (split == 3) split = 2;  // a round's last linears: fewest slices, small units
     pl.n_blocks = (pl.n_strips + kWarps * pl.strips_per_warp - 1) / (kWarps * pl.strips_per_warp);
     // largest slice (a whole number of stages) whose staged x and sums fit
@@ -958,7 +1015,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
             const long long units = (long long)pl.n_blocks * S_eff;
             const long long per_cta = (units + grid_max - 1) / grid_max;
             const double cost =
-                (double)per_cta * (sg + 2) + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
+                (double)per_cta * (sg * work + 2) + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
             if (cost < best_cost - 1e-9) {
                 best_cost = cost;
                 best_sg = sg;
@@ -974,7 +1031,9 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.units = pl.S * pl.n_blocks;
     pl.grid = pl.units < grid_max ? pl.units : grid_max;
     pl.smem_bytes = mma_smem_bytes(M, pl.slice_groups);
-    pl.ws_bytes = pl.S > 1 ? (size_t)pl.S * M * N * sizeof(float) : 0;
+    // split K, and SiLU-and-mul with any number of slices: the partial sums
+    pl.reduce = pl.S > 1 || epi == kEpiSiluMul;
+    pl.ws_bytes = pl.reduce ? (size_t)pl.S * M * N * sizeof(float) : 0;
     pl.ok = true;
     return pl;
 }
@@ -1003,6 +1062,10 @@ cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partia
     d->counters = counters;
     d->scales_first = (uintptr_t)a.scales & ~(uintptr_t)3;
     d->scales_end = (uintptr_t)(a.scales + (size_t)a.N * G);
+    d->residual = a.epi == kEpiResidual ? a.residual : nullptr;
+    d->epi = a.epi;
+    d->ycols = out_cols(a.N, a.epi);
+    d->half_strips = a.epi == kEpiSiluMul ? a.N / 32 : 0;
     d->N = a.N;
     d->K = a.K;
     d->G = G;
