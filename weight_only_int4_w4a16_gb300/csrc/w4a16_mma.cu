@@ -998,27 +998,43 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi)
         best_sg = (G + s_min - 1) / s_min;
         best_sg = (best_sg + kStageGroups - 1) / kStageGroups * kStageGroups;
     } else {
-        // Pick the number of K slices that minimises the work of the busiest
-        // CTA (units per CTA x (groups per slice + a per-unit charge)), plus a
-        // charge per extra slice for the partial sums; slices are whole stages.
+        // Pick the strips per warp and the K slices (whole stages) with the
+        // least cost in a model tuned on single-launch times measured on
+        // GB300 (one linear, L2 evicted, 14 shapes with K 5120..17408,
+        // N 5120..139264, M 1..8, every feasible plan; the model's pick is
+        // within 1.5% of the best plan on average): per unit a CTA pays
+        // ~2.2 us (barrier, x staging) plus its stages, a stage per warp
+        // 0.85 us plus 0.45 us at full load (16 warps share an SM's issue
+        // slots); a split adds ~4.5 us plus 2 us per slice (partials, the
+        // reducing CTA on the critical path).  Fewer, longer units win unless
+        // the staged x needs the slices or many SMs would sit idle.
         int s_lo = s_min;
         if (split == 1 && s_lo < 2 && G > kStageGroups) s_lo = 2;
         int s_hi = split == 0 ? 1 : (G + kStageGroups - 1) / kStageGroups;
         if (s_hi < s_lo) s_hi = s_lo;
         double best_cost = 1e30;
-        for (int S = s_lo; S <= s_hi; ++S) {
-            int sg = (G + S - 1) / S;
-            sg = (sg + kStageGroups - 1) / kStageGroups * kStageGroups;
-            if (sg > max_groups) continue;
-            const int S_eff = (G + sg - 1) / sg;
-            if (split == 1 && S_eff < 2 && G > kStageGroups) continue;
-            const long long units = (long long)pl.n_blocks * S_eff;
-            const long long per_cta = (units + grid_max - 1) / grid_max;
-            const double cost =
-                (double)per_cta * (sg * work + 2) + (S_eff > 1 ? 2.0 + 0.5 * S_eff : 0.0);
-            if (cost < best_cost - 1e-9) {
-                best_cost = cost;
-                best_sg = sg;
+        for (int spw = 1; spw <= kRoundStripsPerWarp; spw *= 2) {
+            const int nb = (pl.n_strips + kWarps * spw - 1) / (kWarps * spw);
+            for (int S = s_lo; S <= s_hi; ++S) {
+                int sg = (G + S - 1) / S;
+                sg = (sg + kStageGroups - 1) / kStageGroups * kStageGroups;
+                if (sg > max_groups) continue;
+                const int S_eff = (G + sg - 1) / sg;
+                if (split == 1 && S_eff < 2 && G > kStageGroups) continue;
+                const long long units = (long long)nb * S_eff;
+                const long long per_cta = (units + grid_max - 1) / grid_max;
+                const double load = (double)(units < grid_max ? units : grid_max) / grid_max;
+                const double stages = (double)spw * work * ((sg + kStageGroups - 1) / kStageGroups);
+                // (SiLU-and-mul reduces through the workspace at any S)
+                const bool reduces = S_eff > 1 || epi == kEpiSiluMul;
+                const double cost = (double)per_cta * (2.2 + stages * (0.85 + 0.45 * load)) +
+                                    (reduces ? 4.5 + 2.0 * S_eff : 0.0);
+                if (cost < best_cost - 1e-9) {
+                    best_cost = cost;
+                    best_sg = sg;
+                    pl.strips_per_warp = spw;
+                    pl.n_blocks = nb;
+                }
             }
         }
     }
