@@ -60,6 +60,8 @@ def _bind(lib):
     lib.w4o_dequant.argtypes = [P, P, P, I, I, I, P]
     lib.w4o_silu_mul.argtypes = [P, I, I, P]
     lib.w4o_add_residual.argtypes = [P, P, L, P]
+    lib.w4o_transpose_u4.argtypes = [P, L, L, ctypes.c_uint32, P]
+    lib.w4o_transpose_u16.argtypes = [P, L, L, P]
     lib.w4o_linear.argtypes = [P, P, P, P, I, I, I, I, P, I]
     lib.w4o_linear_rows.argtypes = [P, P, P, P, I, I, I, I, P, I, P, I]
     lib.w4o_round_to_half.argtypes = [P, L, P]
@@ -219,3 +221,25 @@ def add_residual(y: np.ndarray, residual: np.ndarray) -> np.ndarray:
     out = np.empty_like(y)
     _load().w4o_add_residual(_ptr(y), _ptr(r), int(y.size), _ptr(out))
     return out
+
+
+SEQUENTIAL_ORDER = 0x76543210
+
+
+def transpose_u4(src: np.ndarray, rows: int, cols: int, order: int = SEQUENTIAL_ORDER) -> np.ndarray:
+    """Packed 4-bit transpose: src [rows, cols/8] uint32 packed along cols (nibble
+    order `order`) -> [cols, ceil(rows/8)] uint32 packed along rows, sequential."""
+    src = _c(src, np.uint32)
+    assert cols % 8 == 0 and src.size == rows * cols // 8
+    dst = np.empty((cols, (rows + 7) // 8), dtype=np.uint32)
+    _load().w4o_transpose_u4(_ptr(src), rows, cols, order, _ptr(dst))
+    return dst
+
+
+def transpose_u16(src: np.ndarray) -> np.ndarray:
+    """[rows, cols] uint16 (fp16 bits) -> [cols, rows]."""
+    src = _c(src, np.uint16)
+    rows, cols = src.shape
+    dst = np.empty((cols, rows), dtype=np.uint16)
+    _load().w4o_transpose_u16(_ptr(src), rows, cols, _ptr(dst))
+    return dst

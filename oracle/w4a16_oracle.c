@@ -35,7 +35,10 @@
  *   position; dequant against exact rationals for all 256 (q, z) pairs and a
  *   set of scales; linear against exact-rational brute force on tiny shapes,
  *   q == z gives 0, one nonzero group, linearity, and an integer special case
- *   that reduces to an int64 matrix product.
+ *   that reduces to an int64 matrix product; the epilogues against closed
+ *   forms (sigmoid at ln 3), the odd-part identity and exact sums; the repack
+ *   transpose against the pinned pack/unpack, a hand 8 x 8 block, ragged rows
+ *   and a nibble-order permutation.
  */
 #include <math.h>
 #include <pthread.h>
@@ -294,4 +297,37 @@ void w4o_silu_mul(const double *y, int M, int I, double *out)
 void w4o_add_residual(const double *y, const uint16_t *r, long n, double *out)
 {
     for (long i = 0; i < n; ++i) out[i] = y[i] + w4o_half_to_double(r[i]);
+}
+
+/* ---- load-time repack (Z100 thread, section 四: checkpoint INT4 layouts are
+ * transposed and repacked at load time, now at nibble level in 8 x 8 blocks,
+ * without unpacking the whole matrix to int32).  TEST INFRASTRUCTURE ONLY.
+ *
+ * Transpose of a packed 4-bit matrix A [rows, cols]:
+ *   src [rows, cols/8] words, packed along cols; element (r, c) sits at nibble
+ *       position ((order >> 4*(c%8)) & 7) of word src[r][c/8] (order: eight
+ *       nibbles, entry j = the position holding element j of a word's group of
+ *       eight; 0x76543210 is the sequential order used everywhere else);
+ *   dst [cols, ceil(rows/8)] words, packed along rows in sequential order:
+ *       element (c, r) of A^T at nibble r%8 of word dst[c][r/8]; pad nibbles 0.
+ * Written element by element from that definition. */
+void w4o_transpose_u4(const uint32_t *src, long rows, long cols, uint32_t order,
+                      uint32_t *dst)
+{
+    const long sw = cols / 8, dw = (rows + 7) / 8;
+    memset(dst, 0, sizeof(uint32_t) * (size_t)(cols * dw));
+    for (long r = 0; r < rows; ++r)
+        for (long c = 0; c < cols; ++c) {
+            const unsigned pos = (order >> (4 * (c % 8))) & 7u;
+            const unsigned v = (src[r * sw + c / 8] >> (4 * pos)) & 15u;
+            dst[c * dw + r / 8] |= (uint32_t)v << (4 * (r % 8));
+        }
+}
+
+/* Transpose of a binary16 matrix (the per-group scales of a checkpoint laid
+ * out [G, N], to this layout's [N, G]): dst[c][r] = src[r][c]. */
+void w4o_transpose_u16(const uint16_t *src, long rows, long cols, uint16_t *dst)
+{
+    for (long r = 0; r < rows; ++r)
+        for (long c = 0; c < cols; ++c) dst[c * rows + r] = src[r * cols + c];
 }

@@ -34,6 +34,15 @@ MUTANTS = {
     "subnormal_exponent": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;",
                             "if (frac >= 0.5) m++;"),
+    "silu_sign": ("out[(long)m * I + n] = g / (1.0 + exp(-g)) * u;",
+                  "out[(long)m * I + n] = g / (1.0 + exp(g)) * u;"),
+    "silu_halves_swapped": ("const double g = y[(long)m * 2 * I + n];\n            const double u = y[(long)m * 2 * I + I + n];",
+                            "const double u = y[(long)m * 2 * I + n];\n            const double g = y[(long)m * 2 * I + I + n];"),
+    "residual_dropped": ("out[i] = y[i] + w4o_half_to_double(r[i]);", "out[i] = y[i];"),
+    "transpose_order_inverted": ("const unsigned pos = (order >> (4 * (c % 8))) & 7u;",
+                                 "unsigned pos = 0;\n            while (((order >> (4 * pos)) & 7u) != (unsigned)(c % 8) && pos < 7) ++pos;"),
+    "transpose_dst_word_index": ("dst[c * dw + r / 8] |= (uint32_t)v << (4 * (r % 8));",
+                                 "dst[c * dw + r / 8] |= (uint32_t)v << (4 * (7 - r % 8));"),
     "pack_zero_pad_dirty": ("if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);",
                             "word |= (uint32_t)(z[n * G + (g < G ? g : G - 1)] & 0xfu) << (4 * j);"),
 }
@@ -56,6 +65,14 @@ def _pin_calls():
         pins.test_linearity_in_x,
         lambda: pins.test_integer_case_equals_int64_matmul(0x2C00, 1 / 16),
         pins.test_hand_worked_example,
+        pins.test_silu_mul_closed_forms,
+        pins.test_silu_mul_odd_part_identity,
+        pins.test_silu_mul_column_split_and_rows,
+        pins.test_add_residual_exact,
+        pins.test_transpose_u4_hand_block,
+        pins.test_transpose_u4_against_pinned_pack_unpack,
+        pins.test_transpose_u4_ragged_rows_pad_with_zero,
+        pins.test_transpose_u4_nibble_order,
     ]
 
 

@@ -372,3 +372,63 @@ def test_add_residual_exact():
     # a residual of +0 changes nothing
     z = oracle.add_residual(y, np.zeros(n, dtype=np.uint16))
     assert np.array_equal(z, y)
+
+
+# ----------------------------------------------------------------------------
+# load-time repack: the nibble-level transpose of a packed 4-bit matrix
+# (forum thread "vLLM on Hygon Z100", section 四: checkpoint INT4 layouts
+# transposed and repacked in 8 x 8 nibble blocks)
+# ----------------------------------------------------------------------------
+def test_transpose_u4_hand_block():
+    # A[r][c] = r: every source word of row r is r repeated (r * 0x11111111);
+    # every column of A is 0, 1, ..., 7, i.e. the word 0x76543210.  And the
+    # other way round for A[r][c] = c.
+    rows_const = np.array([r * 0x11111111 for r in range(8)], dtype=np.uint32)
+    assert np.array_equal(oracle.transpose_u4(rows_const, 8, 8)[:, 0],
+                          np.full(8, 0x76543210, dtype=np.uint32))
+    cols_const = np.full(8, 0x76543210, dtype=np.uint32)
+    assert np.array_equal(oracle.transpose_u4(cols_const, 8, 8)[:, 0],
+                          np.array([c * 0x11111111 for c in range(8)], dtype=np.uint32))
+
+
+def test_transpose_u4_against_pinned_pack_unpack():
+    # A [128, 256] of random nibbles: pack it along its columns (the pinned
+    # packer), transpose, unpack along the new rows: A^T exactly
+    A = RNG.integers(0, 16, size=(128, 256), dtype=np.uint8)
+    zq = np.zeros((128, 2), dtype=np.uint8)
+    src, _ = oracle.pack(A, zq)
+    dst = oracle.transpose_u4(src, 128, 256)
+    assert dst.shape == (256, 16)
+    back, _ = oracle.unpack(dst, np.zeros((256, 1), dtype=np.uint32), 128)
+    assert np.array_equal(back, A.T)
+    # twice is the identity
+    assert np.array_equal(oracle.transpose_u4(dst, 256, 128), src)
+
+
+def test_transpose_u4_ragged_rows_pad_with_zero():
+    # rows not a multiple of 8: the result equals that of the matrix padded
+    # with zero rows (pad nibbles are 0)
+    A = RNG.integers(0, 16, size=(128, 128), dtype=np.uint8)
+    A[101:] = 0
+    src, _ = oracle.pack(A, np.zeros((128, 1), dtype=np.uint8))
+    full = oracle.transpose_u4(src, 128, 128)
+    ragged = oracle.transpose_u4(src[:101], 101, 128)
+    assert ragged.shape == (128, 13)
+    assert np.array_equal(ragged, full[:, :13])
+
+
+def test_transpose_u4_nibble_order():
+    # one source word 0x76543210 holds the value p at position p; with order
+    # P (element j at position P[j]) column j of the one-row matrix reads P[j]
+    perm = [3, 7, 0, 4, 1, 5, 2, 6]
+    order = sum(p << (4 * j) for j, p in enumerate(perm))
+    dst = oracle.transpose_u4(np.array([0x76543210], dtype=np.uint32), 1, 8, order)
+    assert dst[:, 0].tolist() == perm
+    # the sequential order is the identity permutation
+    dst = oracle.transpose_u4(np.array([0x76543210], dtype=np.uint32), 1, 8)
+    assert dst[:, 0].tolist() == list(range(8))
+
+
+def test_transpose_u16_is_numpy_transpose():
+    a = RNG.integers(0, 1 << 16, size=(37, 130)).astype(np.uint16)
+    assert np.array_equal(oracle.transpose_u16(a), a.T)
