@@ -268,6 +268,32 @@ def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), ep
     return out
 
 
+def time_repack(w4, dev, flush, peak, reps=10):
+    """Load-time repack of a gate+up checkpoint stored transposed (qweight
+    [5120, 34816/8] packed along N): median time with L2 evicted, and GB/s
+    of bytes read + written."""
+    import synthetic_inputs as si
+    K, N = 5120, 34816
+    src = si.qweight(si.config_seed(6), K, N, device=dev)
+    dst = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        w4.w4a16_repack_transpose(src, K, N, dst=dst)
+    ts = []
+    for _ in range(reps):
+        flush_l2(flush)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        w4.w4a16_repack_transpose(src, K, N, dst=dst)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+    by = 2 * src.numel() * 4
+    return {"rows": K, "cols": N, "us": t * 1e6, "GBps": by / t / 1e9,
+            "frac_of_peak": by / t / 1e9 / peak}
+
+
 _LAYER0 = None
 
 
@@ -523,6 +549,7 @@ def main():
             epis[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
                            "us_without_epilogue": t0 * 1e6}
         extra["epilogue_l2_flushed"] = epis
+        extra["repack_transpose"] = time_repack(w4, dev, flush, peak)
         del flush
 
     cpu = None

@@ -118,6 +118,28 @@ int w4a16_unpack(const uint32_t *qweight, const uint32_t *zeros, int N, int K, i
 int w4a16_dequant(const uint32_t *qweight, const uint16_t *scales, const uint32_t *zeros,
                   int N, int K, int group, float *w_f32, uint16_t *w_f16, void *stream);
 
+/* Load-time repack of a checkpoint whose INT4 layout is transposed (the Z100
+ * thread, section 四: checkpoint layouts are transposed and repacked at load
+ * time, nibble by nibble in 8 x 8 blocks, with no full int32 copy of the
+ * matrix).  Transposes a packed 4-bit matrix A [rows, cols]:
+ *   src [rows, cols/8] uint32, packed along cols: element (r, c) is nibble
+ *       ((src_order >> 4*(c%8)) & 7) of word src[r][c/8].  src_order lists, in
+ *       nibble j, the position holding element j of each word's eight;
+ *       0x76543210 is this library's sequential order.  It must name each
+ *       position 0..7 once (INVALID_ARG otherwise).
+ *   dst [cols, ceil(rows/8)] uint32, packed along rows in sequential order;
+ *       pad nibbles past `rows` are 0.
+ * cols a multiple of 8; 1 <= rows, cols <= 2^24; src and dst 4-byte aligned
+ * and apart.  A checkpoint with qweight [K, N/8] and zeros [G, N/8] (packed
+ * along N) gives this library's qweight = repack(qweight, K, N) and zeros =
+ * repack(zeros, G, N); its scales [G, N] go through w4a16_transpose_f16. */
+int w4a16_repack_transpose(const uint32_t *src, int rows, int cols, uint32_t src_order,
+                           uint32_t *dst, void *stream);
+
+/* dst [cols, rows] = src [rows, cols]^T for 16-bit elements (fp16 bit patterns);
+ * 1 <= rows, cols <= 2^24, 2-byte aligned, apart. */
+int w4a16_transpose_f16(const uint16_t *src, int rows, int cols, uint16_t *dst, void *stream);
+
 /* y = x @ W^T for one W4A16 linear layer (the operation at the top of this
  * file).  Enqueues one kernel for the rung w4a16_select_rung picks (the
  * split-K rungs reduce inside the same kernel); the CUDA-core rungs enqueue one

@@ -96,6 +96,20 @@ def test_linear_epilogue_validation_codes(w4):
         assert _epi(w4, 0) == w4.W4A16_ERR_NOT_INITIALIZED
 
 
+def test_repack_validation_codes(w4):
+    L, seq = w4.lib, 0x76543210
+    assert L.w4a16_repack_transpose(None, 8, 8, seq, A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_transpose(A, 0, 8, seq, 2 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_transpose(A, 8, 12, seq, 2 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_transpose(A, 8, 8, 0x76543211, 2 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_transpose(A, 8, 8, 0x86543210, 2 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_repack_transpose(A + 2, 8, 8, seq, 2 * A, None) == w4.W4A16_ERR_MISALIGNED
+    assert L.w4a16_repack_transpose(A, 64, 64, seq, A + 64, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_transpose_f16(A, 0, 4, 2 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_transpose_f16(A + 1, 4, 4, 2 * A, None) == w4.W4A16_ERR_MISALIGNED
+    assert L.w4a16_transpose_f16(A, 4, 4, A + 8, None) == w4.W4A16_ERR_INVALID_ARG
+
+
 def test_pack_dequant_validation_codes(w4):
     L = w4.lib
     assert L.w4a16_pack(None, A, 4, 256, 128, A, A, None) == w4.W4A16_ERR_INVALID_ARG

@@ -71,6 +71,8 @@ _sig("w4a16_workspace_bytes", [_I, _I, _I, _I], _SZ)
 _sig("w4a16_pack", [_P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_unpack", [_P, _P, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_dequant", [_P, _P, _P, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_repack_transpose", [_P, _I, _I, ctypes.c_uint32, _P, _P])
+_sig("w4a16_transpose_f16", [_P, _I, _I, _P, _P])
 _sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_epilogue", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P])
@@ -90,7 +92,8 @@ _sig("w4a16_last_cuda_error", [])
 _sig("w4a16_device_sm_count", [])
 
 EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
-            "w4a16_unpack", "w4a16_dequant", "w4a16_linear", "w4a16_linear_noalloc",
+            "w4a16_unpack", "w4a16_dequant", "w4a16_repack_transpose", "w4a16_transpose_f16",
+            "w4a16_linear", "w4a16_linear_noalloc",
             "w4a16_linear_epilogue",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
@@ -187,6 +190,32 @@ def w4a16_dequant(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tens
                              N, K, group, w32.data_ptr() if f32 else None,
                              w16.data_ptr() if f16 else None, _stream_ptr(stream)), "w4a16_dequant")
     return w32, w16
+
+
+SEQUENTIAL_ORDER = 0x76543210
+
+
+def w4a16_repack_transpose(src: torch.Tensor, rows: int, cols: int,
+                           src_order: int = SEQUENTIAL_ORDER, dst=None, stream=None) -> torch.Tensor:
+    """src [rows, cols/8] int32 (4-bit values packed along cols, nibble order
+    src_order) -> [cols, ceil(rows/8)] int32 packed along rows (sequential)."""
+    if dst is None:
+        dst = torch.empty((cols, (rows + 7) // 8), dtype=torch.int32, device=src.device)
+    _check(lib.w4a16_repack_transpose(_dev(src, torch.int32, "src"), rows, cols, src_order,
+                                      _dev(dst, torch.int32, "dst"), _stream_ptr(stream)),
+           "w4a16_repack_transpose")
+    return dst
+
+
+def w4a16_transpose_f16(src: torch.Tensor, dst=None, stream=None) -> torch.Tensor:
+    """[rows, cols] fp16 -> [cols, rows]."""
+    rows, cols = src.shape
+    if dst is None:
+        dst = torch.empty((cols, rows), dtype=torch.float16, device=src.device)
+    _check(lib.w4a16_transpose_f16(_dev(src, torch.float16, "src"), rows, cols,
+                                   _dev(dst, torch.float16, "dst"), _stream_ptr(stream)),
+           "w4a16_transpose_f16")
+    return dst
 
 
 def w4a16_linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,

@@ -60,6 +60,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 }
 
 constexpr int kMaxK = 1 << 22;
+constexpr int kMaxRepackDim = 1 << 24;  // rows and columns of a repacked matrix
 static_assert(kEpiNone == W4A16_EPILOGUE_NONE && kEpiResidual == W4A16_EPILOGUE_RESIDUAL &&
                   kEpiSiluMul == W4A16_EPILOGUE_SILU_MUL,
               "internal epilogue codes follow the ABI");
@@ -497,6 +498,34 @@ int w4a16_dequant(const uint32_t *qweight, const uint16_t *scales, const uint32_
     g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = launch_dequant(qweight, reinterpret_cast<const __half *>(scales), zeros, N, K,
                                    w_f32, reinterpret_cast<__half *>(w_f16), (cudaStream_t)stream);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_repack_transpose(const uint32_t *src, int rows, int cols, uint32_t src_order,
+                           uint32_t *dst, void *stream) {
+    if (!src || !dst || rows < 1 || cols < 8 || cols % 8 != 0 || rows > kMaxRepackDim ||
+        cols > kMaxRepackDim)
+        return W4A16_ERR_INVALID_ARG;
+    // the order must name each of the 8 nibble positions once
+    unsigned seen = 0;
+    for (int j = 0; j < 8; ++j) seen |= 1u << ((src_order >> (4 * j)) & 0xfu);
+    if (seen != 0xffu) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(src, 4) || !aligned(dst, 4)) return W4A16_ERR_MISALIGNED;
+    if (overlaps(src, (size_t)rows * (cols / 8) * 4, dst, (size_t)cols * ((rows + 7) / 8) * 4))
+        return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = launch_transpose_u4(src, rows, cols, src_order, dst, (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_transpose_f16(const uint16_t *src, int rows, int cols, uint16_t *dst, void *stream) {
+    if (!src || !dst || rows < 1 || cols < 1 || rows > kMaxRepackDim || cols > kMaxRepackDim)
+        return W4A16_ERR_INVALID_ARG;
+    if (!aligned(src, 2) || !aligned(dst, 2)) return W4A16_ERR_MISALIGNED;
+    if (overlaps(src, (size_t)rows * cols * 2, dst, (size_t)rows * cols * 2))
+        return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = launch_transpose_u16(src, rows, cols, dst, (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

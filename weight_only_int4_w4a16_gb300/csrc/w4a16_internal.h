@@ -178,5 +178,12 @@ cudaError_t launch_unpack(const uint32_t *qw, const uint32_t *zeros, int N, int 
                           uint8_t *z, cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t *qw, const __half *scales, const uint32_t *zeros,
                            int N, int K, float *w_f32, __half *w_f16, cudaStream_t stream);
+// src [rows, cols/8] words packed along cols (nibble order `order`) ->
+// dst [cols, ceil(rows/8)] words packed along rows, sequential, pad nibbles 0.
+cudaError_t launch_transpose_u4(const uint32_t *src, int rows, int cols, uint32_t order,
+                                uint32_t *dst, cudaStream_t stream);
+// src [rows, cols] -> dst [cols, rows], 16-bit elements.
+cudaError_t launch_transpose_u16(const uint16_t *src, int rows, int cols, uint16_t *dst,
+                                 cudaStream_t stream);
 
 }  // namespace w4a16

@@ -110,6 +110,93 @@ __global__ void dequant_kernel(const uint32_t *__restrict__ qw, const __half *__
     }
 }
 
+// ---- checkpoint repack: transpose a packed 4-bit matrix at nibble level ----
+// The Z100 thread (section 四) transposes and repacks INT4 checkpoint layouts
+// at load time in 8 x 8 nibble blocks, without unpacking the whole matrix to
+// int32.  Here a CTA moves a tile of 32 x 32 blocks (256 source rows x 256
+// source columns): each thread loads the 8 words of a block (8 source rows,
+// coalesced across the warp), brings their nibbles into sequential order,
+// transposes the block in registers (three exchange stages: 4 x 4 quadrants
+// between words e and e + 4, 2 x 2 within them between e and e + 2, single
+// nibbles between e and e + 1) and parks the 8 result words in shared memory;
+// the CTA then writes whole destination rows, coalesced.
+constexpr int kTile = 32;  // blocks per tile side
+
+__device__ __forceinline__ void swap_bits(uint32_t &lo, uint32_t &hi, int shift, uint32_t mask) {
+    const uint32_t t = ((lo >> shift) ^ hi) & mask;
+    lo ^= t << shift;
+    hi ^= t;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    transpose_u4_kernel(const uint32_t *__restrict__ src, int rows, int SW, uint32_t order,
+                        int sequential, uint32_t *__restrict__ dst, int cols, int DW) {
+    // [nibble j][column word in tile][row block in tile], padded against bank conflicts
+    __shared__ uint32_t tile[8][kTile][kTile + 1];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int cw0 = blockIdx.x * kTile, rb0 = blockIdx.y * kTile;
+    const int cw = cw0 + tx;
+    for (int i = 0; i < kTile / 8; ++i) {
+        const int rbl = ty + 8 * i;
+        const long long r0 = 8LL * (rb0 + rbl);
+        uint32_t a[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const long long r = r0 + e;
+            a[e] = (cw < SW && r < rows) ? src[r * SW + cw] : 0u;
+        }
+        if (!sequential) {  // element j of a word sits at nibble (order >> 4j) & 7
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t pos = (order >> (4 * j)) & 7u;
+                    w |= ((a[e] >> (4 * pos)) & 0xfu) << (4 * j);
+                }
+                a[e] = w;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) swap_bits(a[e], a[e + 4], 16, 0x0000ffffu);
+        swap_bits(a[0], a[2], 8, 0x00ff00ffu);
+        swap_bits(a[1], a[3], 8, 0x00ff00ffu);
+        swap_bits(a[4], a[6], 8, 0x00ff00ffu);
+        swap_bits(a[5], a[7], 8, 0x00ff00ffu);
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) swap_bits(a[e], a[e + 1], 4, 0x0f0f0f0fu);
+        // a[j] is now column 8 * cw + j of the source over the block's 8 rows
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tile[j][tx][rbl] = a[j];
+    }
+    __syncthreads();
+    // destination row 8 * (cw0 + c) + j, words rb0 .. rb0 + 31 (one per lane)
+    for (int d = ty; d < 8 * kTile; d += kThreads / 32) {
+        const int c = d >> 3, j = d & 7;
+        const long long row = 8LL * (cw0 + c) + j;
+        if (row < cols && rb0 + tx < DW) dst[row * DW + rb0 + tx] = tile[j][c][tx];
+    }
+}
+
+// Transpose of a 16-bit matrix by 32 x 32 tiles (the scales of a checkpoint
+// stored [G, N] into this layout's [N, G]).
+__global__ void __launch_bounds__(kThreads)
+    transpose_u16_kernel(const uint16_t *__restrict__ src, int rows, int cols,
+                         uint16_t *__restrict__ dst) {
+    __shared__ uint16_t tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = ty; i < 32; i += 8) {
+        const int r = r0 + i, c = c0 + tx;
+        if (r < rows && c < cols) tile[i][tx] = src[(long long)r * cols + c];
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int c = c0 + i, r = r0 + tx;
+        if (c < cols && r < rows) dst[(long long)c * rows + r] = tile[tx][i];
+    }
+}
+
 int grid_for(long long items) {
     long long b = (items + kThreads - 1) / kThreads;
     if (b < 1) b = 1;
@@ -143,6 +230,22 @@ cudaError_t launch_dequant(const uint32_t *qw, const __half *scales, const uint3
     long long n_words = (long long)N * (K / 8);
     dequant_kernel<<<grid_for(n_words), kThreads, 0, stream>>>(qw, scales, zeros, N, K, G, ZW,
                                                                w_f32, w_f16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_u4(const uint32_t *src, int rows, int cols, uint32_t order,
+                                uint32_t *dst, cudaStream_t stream) {
+    const int SW = cols / 8, DW = (rows + 7) / 8;
+    const dim3 grid((SW + kTile - 1) / kTile, (DW + kTile - 1) / kTile);
+    transpose_u4_kernel<<<grid, kThreads, 0, stream>>>(src, rows, SW, order,
+                                                       order == 0x76543210u, dst, cols, DW);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_u16(const uint16_t *src, int rows, int cols, uint16_t *dst,
+                                 cudaStream_t stream) {
+    const dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+    transpose_u16_kernel<<<grid, kThreads, 0, stream>>>(src, rows, cols, dst);
     return cudaGetLastError();
 }
 
