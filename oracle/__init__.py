@@ -59,16 +59,24 @@ def _bind(lib):
     lib.w4o_unpack.argtypes = [P, P, I, I, I, P, P]
     lib.w4o_dequant.argtypes = [P, P, P, I, I, I, P]
     lib.w4o_silu_mul.argtypes = [P, I, I, P]
-    lib.w4o_add_residual.argtypes = [P, P, L, P]
     lib.w4o_transpose_u4.argtypes = [P, L, L, ctypes.c_uint32, P]
     lib.w4o_transpose_u16.argtypes = [P, L, L, P]
-    lib.w4o_linear.argtypes = [P, P, P, P, I, I, I, I, P, I]
-    lib.w4o_linear_rows.argtypes = [P, P, P, P, I, I, I, I, P, I, P, I]
     lib.w4o_round_to_half.argtypes = [P, L, P]
     lib.w4o_half_array_to_double.argtypes = [P, L, P]
-    for f in (lib.w4o_pack, lib.w4o_unpack, lib.w4o_dequant, lib.w4o_linear,
-              lib.w4o_linear_rows, lib.w4o_round_to_half,
-              lib.w4o_half_array_to_double):
+    lib.w4o_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.w4o_bf16_to_double.restype = ctypes.c_double
+    lib.w4o_double_to_bf16.argtypes = [ctypes.c_double]
+    lib.w4o_double_to_bf16.restype = ctypes.c_uint16
+    lib.w4o_round_to_bf16.argtypes = [P, L, P]
+    lib.w4o_bf16_array_to_double.argtypes = [P, L, P]
+    lib.w4o_linear_dt.argtypes = [P, P, P, P, I, I, I, I, I, P, I]
+    lib.w4o_linear_rows_dt.argtypes = [P, P, P, P, I, I, I, I, I, P, I, P, I]
+    lib.w4o_add_residual_dt.argtypes = [P, P, L, I, P]
+    for f in (lib.w4o_pack, lib.w4o_unpack, lib.w4o_dequant, lib.w4o_round_to_half,
+              lib.w4o_half_array_to_double, lib.w4o_round_to_bf16,
+              lib.w4o_bf16_array_to_double, lib.w4o_linear_dt, lib.w4o_linear_rows_dt,
+              lib.w4o_silu_mul, lib.w4o_add_residual_dt,
+              lib.w4o_transpose_u4, lib.w4o_transpose_u16):
         f.restype = None
     return lib
 
@@ -115,6 +123,23 @@ def double_to_half(v) -> np.ndarray:
     return out.reshape(np.shape(v))
 
 
+def bf16_to_double(bits) -> np.ndarray:
+    b = _c(np.asarray(bits, dtype=np.uint16).reshape(-1), np.uint16)
+    out = np.empty(b.size, dtype=np.float64)
+    _load().w4o_bf16_array_to_double(_ptr(b), b.size, _ptr(out))
+    return out.reshape(np.shape(bits))
+
+
+def double_to_bf16(v) -> np.ndarray:
+    d = _c(np.asarray(v, dtype=np.float64).reshape(-1), np.float64)
+    out = np.empty(d.size, dtype=np.uint16)
+    _load().w4o_round_to_bf16(_ptr(d), d.size, _ptr(out))
+    return out.reshape(np.shape(v))
+
+
+_DTYPES = {"f16": 0, "bf16": 1}
+
+
 def pack(q: np.ndarray, z: np.ndarray, group: int = 128):
     """q [N, K] uint8 (0..15), z [N, K/group] uint8 -> (qweight [N, K/8], zeros [N, ceil(G/8)]) uint32."""
     q = _c(q, np.uint8)
@@ -158,8 +183,9 @@ def dequant(qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray, K: int,
 
 
 def linear(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
-           group: int = 128, nthreads: int | None = None) -> np.ndarray:
-    """y[M, N] = x @ dequant(W)^T in binary64.  x is [M, K] fp16 bits (uint16)."""
+           group: int = 128, nthreads: int | None = None, dtype: str = "f16") -> np.ndarray:
+    """y[M, N] = x @ dequant(W)^T in binary64.  x is [M, K] and scales [N, G]
+    16-bit bit patterns (uint16) of type dtype: "f16" (IEEE binary16) or "bf16"."""
     x = _c(x, np.uint16)
     qweight = _c(qweight, np.uint32)
     scales = _c(scales, np.uint16)
@@ -172,14 +198,14 @@ def linear(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray, zeros: np.nda
     assert zeros.shape == (N, zero_words(G))
     y = np.empty((M, N), dtype=np.float64)
     nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
-    _load().w4o_linear(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N, K,
-                       group, _ptr(y), nt)
+    _load().w4o_linear_dt(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N, K,
+                          group, _DTYPES[dtype], _ptr(y), nt)
     return y
 
 
 def linear_rows(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
                 zeros: np.ndarray, rows, group: int = 128,
-                nthreads: int | None = None) -> np.ndarray:
+                nthreads: int | None = None, dtype: str = "f16") -> np.ndarray:
     """y[M, len(rows)] for the listed output rows; the weight arrays hold all N rows."""
     x = _c(x, np.uint16)
     qweight = _c(qweight, np.uint32)
@@ -196,8 +222,8 @@ def linear_rows(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray,
         raise IndexError("row index out of range")
     y = np.empty((M, rows.size), dtype=np.float64)
     nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
-    _load().w4o_linear_rows(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N,
-                            K, group, _ptr(rows), int(rows.size), _ptr(y), nt)
+    _load().w4o_linear_rows_dt(_ptr(x), _ptr(qweight), _ptr(scales), _ptr(zeros), M, N,
+                               K, group, _DTYPES[dtype], _ptr(rows), int(rows.size), _ptr(y), nt)
     return y
 
 
@@ -213,13 +239,14 @@ def silu_mul(y: np.ndarray) -> np.ndarray:
     return out
 
 
-def add_residual(y: np.ndarray, residual: np.ndarray) -> np.ndarray:
-    """out = y + residual in binary64; residual as fp16 bits (uint16), same shape."""
+def add_residual(y: np.ndarray, residual: np.ndarray, dtype: str = "f16") -> np.ndarray:
+    """out = y + residual in binary64; residual as 16-bit bits (uint16) of type
+    dtype ("f16" or "bf16"), same shape."""
     y = _c(y, np.float64)
     r = _c(residual, np.uint16)
     assert r.shape == y.shape
     out = np.empty_like(y)
-    _load().w4o_add_residual(_ptr(y), _ptr(r), int(y.size), _ptr(out))
+    _load().w4o_add_residual_dt(_ptr(y), _ptr(r), int(y.size), _DTYPES[dtype], _ptr(out))
     return out
 
 

@@ -17,7 +17,9 @@
  * Written out for m < M, n < N, k < K, g = floor(k / group):
  *     w[n,k] = (q[n,k] - z[n,g]) * s[n,g]
  *     y[m,n] = sum_k x[m,k] * w[n,k]
- * with q, z unsigned 4-bit, s and x IEEE binary16, y returned in binary64.
+ * with q, z unsigned 4-bit, s and x IEEE binary16 or bfloat16 (the pages'
+ * activations are "fp16 or bf16"; a bf16 layer keeps its scales in bf16 too),
+ * y returned in binary64.
  *
  * Readings taken where the pages are silent:
  *   - packed layout [N, K/8] 32-bit words, rows = outputs (section 四 names
@@ -38,7 +40,9 @@
  *   that reduces to an int64 matrix product; the epilogues against closed
  *   forms (sigmoid at ln 3), the odd-part identity and exact sums; the repack
  *   transpose against the pinned pack/unpack, a hand 8 x 8 block, ragged rows
- *   and a nibble-order permutation.
+ *   and a nibble-order permutation; bfloat16 conversions against numpy's
+ *   binary32 decoder over every pattern, neighbours and ties; the bf16 linear
+ *   against exact rationals and an int64 matrix product.
  */
 #include <math.h>
 #include <pthread.h>
@@ -100,6 +104,76 @@ uint16_t w4o_double_to_half(double v)
     int field = E + 15;
     if (field >= 31) return (uint16_t)(sign | 0x7c00u);
     return (uint16_t)(sign | (uint16_t)(field << 10) | (uint16_t)(m - 1024));
+}
+
+/* ---------------------------------------------------------------------------
+ * bfloat16 <-> binary64 (the 16-bit activation type the pages name beside
+ * fp16, "fp16 or bf16"), written from the format's definition: 1 sign bit,
+ * 8 exponent bits (bias 127), 7 fraction bits -- the top half of an IEEE
+ * binary32.  Exponent field 0 holds zero and subnormals (fraction * 2^-133),
+ * field 255 holds inf / NaN.
+ * ------------------------------------------------------------------------- */
+double w4o_bf16_to_double(uint16_t b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133);
+    } else if (e == 255) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + f), e - 134);
+    }
+    return sign ? -v : v;
+}
+
+/* Round to nearest, ties to even, by the same exact scaling as for binary16:
+ * 8 significant bits, binades 2^-126 .. 2^127, subnormal quantum 2^-133. */
+uint16_t w4o_double_to_bf16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7fc0u);
+    double a = fabs(v);
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80u);
+    if (a == 0.0) return sign;
+    int e2;
+    (void)frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;               /* a in [2^E, 2^(E+1)) */
+    if (E < -126) E = -126;       /* subnormal range shares the 2^-133 quantum */
+    if (E > 127) return (uint16_t)(sign | 0x7f80u);
+    double r = ldexp(a, 7 - E);   /* a / 2^(E-7), exact */
+    double fl = floor(r);
+    double frac = r - fl;
+    uint64_t m = (uint64_t)fl;
+    if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;
+    if (m == 0) return sign;
+    if (m < 128) return (uint16_t)(sign | (uint16_t)m);  /* subnormal */
+    if (m == 256) {               /* rounding carried into the next binade */
+        m = 128;
+        E++;
+    }
+    int field = E + 127;
+    if (field >= 255) return (uint16_t)(sign | 0x7f80u);
+    return (uint16_t)(sign | (uint16_t)(field << 7) | (uint16_t)(m - 128));
+}
+
+void w4o_round_to_bf16(const double *v, long n, uint16_t *out)
+{
+    for (long i = 0; i < n; i++) out[i] = w4o_double_to_bf16(v[i]);
+}
+
+void w4o_bf16_array_to_double(const uint16_t *b, long n, double *out)
+{
+    for (long i = 0; i < n; i++) out[i] = w4o_bf16_to_double(b[i]);
+}
+
+/* The 16-bit type of activations and scales: 0 = IEEE binary16, 1 = bfloat16. */
+typedef double (*decode16_fn)(uint16_t);
+static decode16_fn decoder_for(int dtype)
+{
+    return dtype == 1 ? w4o_bf16_to_double : w4o_half_to_double;
 }
 
 /* ---------------------------------------------------------------------------
@@ -171,15 +245,15 @@ void w4o_dequant(const uint32_t *qweight, const uint16_t *scales,
  * multiply by the activation, add in increasing k. */
 static double linear_one(const uint16_t *x_row, const uint32_t *q_row,
                          const uint16_t *s_row, const uint32_t *z_row, int K,
-                         int group)
+                         int group, decode16_fn dec)
 {
     double acc = 0.0;
     for (long k = 0; k < K; k++) {
         long g = k / group;
         int qv = (int)nibble_at(q_row, k);
         int zv = (int)nibble_at(z_row, g);
-        double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);
-        acc += w4o_half_to_double(x_row[k]) * w;
+        double w = (double)(qv - zv) * dec(s_row[g]);
+        acc += dec(x_row[k]) * w;
     }
     return acc;
 }
@@ -190,7 +264,7 @@ typedef struct {
     const uint16_t *scales;
     const uint32_t *zeros;
     const int64_t *rows; /* NULL: all rows */
-    int M, N, K, group, nrows;
+    int M, N, K, group, nrows, dtype;
     double *y; /* [M, nrows] */
     int t, nthreads;
 } linear_job;
@@ -205,7 +279,8 @@ static void *linear_worker(void *arg)
         for (long m = 0; m < j->M; m++) {
             j->y[m * j->nrows + i] =
                 linear_one(j->x + m * (long)j->K, j->qweight + n * KW,
-                           j->scales + n * G, j->zeros + n * ZW, j->K, j->group);
+                           j->scales + n * G, j->zeros + n * ZW, j->K, j->group,
+                           decoder_for(j->dtype));
         }
     }
     return NULL;
@@ -243,23 +318,24 @@ static void run_linear(linear_job base, int nthreads)
     free(th);
 }
 
-/* y[M, N] in binary64, rows split over nthreads host threads. */
-void w4o_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
-                const uint32_t *zeros, int M, int N, int K, int group, double *y,
-                int nthreads)
+/* y[M, N] in binary64, rows split over nthreads host threads; x and scales
+ * are 16-bit bit patterns of type dtype (0 binary16, 1 bfloat16). */
+void w4o_linear_dt(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                   const uint32_t *zeros, int M, int N, int K, int group, int dtype,
+                   double *y, int nthreads)
 {
-    linear_job j = {x, qweight, scales, zeros, NULL, M, N, K, group, N, y, 0, 1};
+    linear_job j = {x, qweight, scales, zeros, NULL, M, N, K, group, N, dtype, y, 0, 1};
     run_linear(j, nthreads);
 }
 
 /* Sampled outputs: y[M, nrows] for the listed output rows only.  The weight
  * arrays still describe all N rows (row n starts at n * K/8 words). */
-void w4o_linear_rows(const uint16_t *x, const uint32_t *qweight,
-                     const uint16_t *scales, const uint32_t *zeros, int M, int N,
-                     int K, int group, const int64_t *rows, int nrows, double *y,
-                     int nthreads)
+void w4o_linear_rows_dt(const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, const uint32_t *zeros, int M, int N,
+                        int K, int group, int dtype, const int64_t *rows, int nrows,
+                        double *y, int nthreads)
 {
-    linear_job j = {x, qweight, scales, zeros, rows, M, N, K, group, nrows, y, 0, 1};
+    linear_job j = {x, qweight, scales, zeros, rows, M, N, K, group, nrows, dtype, y, 0, 1};
     run_linear(j, nthreads);
 }
 
@@ -293,10 +369,12 @@ void w4o_silu_mul(const double *y, int M, int I, double *out)
         }
 }
 
-/* Residual add: out[i] = y[i] + r[i], r given as binary16 bit patterns. */
-void w4o_add_residual(const double *y, const uint16_t *r, long n, double *out)
+/* Residual add: out[i] = y[i] + r[i], r given as 16-bit bit patterns of type
+ * dtype (0 binary16, 1 bfloat16). */
+void w4o_add_residual_dt(const double *y, const uint16_t *r, long n, int dtype, double *out)
 {
-    for (long i = 0; i < n; ++i) out[i] = y[i] + w4o_half_to_double(r[i]);
+    decode16_fn dec = decoder_for(dtype);
+    for (long i = 0; i < n; ++i) out[i] = y[i] + dec(r[i]);
 }
 
 /* ---- load-time repack (Z100 thread, section 四: checkpoint INT4 layouts are

@@ -21,10 +21,10 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
 MUTANTS = {
     "nibble_order_reversed": ("return (row_words[idx / 8] >> (4 * (idx % 8))) & 0xfu;",
                               "return (row_words[idx / 8] >> (4 * (7 - idx % 8))) & 0xfu;"),
-    "sign_flipped": ("double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);",
-                     "double w = (double)(zv - qv) * w4o_half_to_double(s_row[g]);"),
-    "scale_group_ignored": ("double w = (double)(qv - zv) * w4o_half_to_double(s_row[g]);",
-                            "double w = (double)(qv - zv) * w4o_half_to_double(s_row[0]);"),
+    "sign_flipped": ("double w = (double)(qv - zv) * dec(s_row[g]);",
+                     "double w = (double)(zv - qv) * dec(s_row[g]);"),
+    "scale_group_ignored": ("double w = (double)(qv - zv) * dec(s_row[g]);",
+                            "double w = (double)(qv - zv) * dec(s_row[0]);"),
     "zero_group_off_by_one": ("int zv = (int)nibble_at(z_row, g);",
                               "int zv = (int)nibble_at(z_row, g ? g - 1 : 0);"),
     "last_term_dropped": ("for (long k = 0; k < K; k++) {\n        long g = k / group;\n        int qv = (int)nibble_at(q_row, k);\n        int zv",
@@ -32,17 +32,23 @@ MUTANTS = {
     "operands_transposed": ("linear_one(j->x + m * (long)j->K, j->qweight + n * KW,",
                             "linear_one(j->x + (n % j->M) * (long)j->K, j->qweight + (m % j->N) * KW,"),
     "subnormal_exponent": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
-    "ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;",
-                            "if (frac >= 0.5) m++;"),
+    "ties_away_from_zero": ("if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;\n    if (m == 0) return sign;\n    if (m < 1024)",
+                            "if (frac >= 0.5) m++;\n    if (m == 0) return sign;\n    if (m < 1024)"),
     "silu_sign": ("out[(long)m * I + n] = g / (1.0 + exp(-g)) * u;",
                   "out[(long)m * I + n] = g / (1.0 + exp(g)) * u;"),
     "silu_halves_swapped": ("const double g = y[(long)m * 2 * I + n];\n            const double u = y[(long)m * 2 * I + I + n];",
                             "const double u = y[(long)m * 2 * I + n];\n            const double g = y[(long)m * 2 * I + I + n];"),
-    "residual_dropped": ("out[i] = y[i] + w4o_half_to_double(r[i]);", "out[i] = y[i];"),
+    "residual_dropped": ("out[i] = y[i] + dec(r[i]);", "out[i] = y[i];"),
     "transpose_order_inverted": ("const unsigned pos = (order >> (4 * (c % 8))) & 7u;",
                                  "unsigned pos = 0;\n            while (((order >> (4 * pos)) & 7u) != (unsigned)(c % 8) && pos < 7) ++pos;"),
     "transpose_dst_word_index": ("dst[c * dw + r / 8] |= (uint32_t)v << (4 * (r % 8));",
                                  "dst[c * dw + r / 8] |= (uint32_t)v << (4 * (7 - r % 8));"),
+    "bf16_bias_off_by_one": ("v = ldexp((double)(128 + f), e - 134);", "v = ldexp((double)(128 + f), e - 133);"),
+    "bf16_subnormal_exponent": ("v = ldexp((double)f, -133);", "v = ldexp((double)f, -132);"),
+    "bf16_truncates": ("    if (frac > 0.5 || (frac == 0.5 && (m & 1u))) m++;\n    if (m == 0) return sign;\n    if (m < 128)",
+                       "    if (m == 0) return sign;\n    if (m < 128)"),
+    "bf16_read_as_half": ("return dtype == 1 ? w4o_bf16_to_double : w4o_half_to_double;",
+                          "return w4o_half_to_double;"),
     "pack_zero_pad_dirty": ("if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);",
                             "word |= (uint32_t)(z[n * G + (g < G ? g : G - 1)] & 0xfu) << (4 * j);"),
 }
@@ -73,6 +79,12 @@ def _pin_calls():
         pins.test_transpose_u4_against_pinned_pack_unpack,
         pins.test_transpose_u4_ragged_rows_pad_with_zero,
         pins.test_transpose_u4_nibble_order,
+        pins.test_bf16_to_double_every_pattern,
+        pins.test_double_to_bf16_neighbours_and_ties,
+        pins.test_double_to_bf16_closed_form,
+        lambda: pins.test_linear_bf16_matches_exact_rationals(2, 3, 256),
+        pins.test_linear_bf16_integer_case_equals_int64_matmul,
+        pins.test_add_residual_bf16_exact,
     ]
 
 

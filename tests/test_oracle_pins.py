@@ -432,3 +432,121 @@ def test_transpose_u4_nibble_order():
 def test_transpose_u16_is_numpy_transpose():
     a = RNG.integers(0, 1 << 16, size=(37, 130)).astype(np.uint16)
     assert np.array_equal(oracle.transpose_u16(a), a.T)
+
+
+# ----------------------------------------------------------------------------
+# bfloat16 (activations "fp16 or bf16"): conversions and the linear
+# ----------------------------------------------------------------------------
+def _bf16_value(bits):
+    """bfloat16 is the top half of an IEEE binary32: decode with numpy's float32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def _bf16_bits(a):
+    """Inputs only: the top 16 bits of the float32 (any pattern is a valid bf16)."""
+    return (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_bf16_to_double_every_pattern():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_to_double(bits)
+    with np.errstate(invalid="ignore"):
+        ref = _bf16_value(bits)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_double_to_bf16_neighbours_and_ties():
+    # a and its successor b (consecutive finite positive patterns): values
+    # exactly a and b map to themselves; their midpoint (exact in binary64)
+    # to whichever has an even last bit; points just off the midpoint to the
+    # nearer one; negative values mirror positive ones
+    a = RNG.integers(1, 0x7F7F, size=20000).astype(np.uint16)
+    b = (a + 1).astype(np.uint16)
+    va, vb = _bf16_value(a), _bf16_value(b)
+    mid = (va + vb) / 2
+    assert np.array_equal(oracle.double_to_bf16(va), a)
+    assert np.array_equal(oracle.double_to_bf16(vb), b)
+    even = np.where(a % 2 == 0, a, b)
+    assert np.array_equal(oracle.double_to_bf16(mid), even)
+    eps = (vb - va) * 2.0 ** -20
+    assert np.array_equal(oracle.double_to_bf16(mid - eps), a)
+    assert np.array_equal(oracle.double_to_bf16(mid + eps), b)
+    assert np.array_equal(oracle.double_to_bf16(-mid), even | 0x8000)
+
+
+def test_double_to_bf16_closed_form():
+    # 1 + 2^-8 ties between 1 and 1 + 2^-7: to even (1.0); 1 + 3 * 2^-8 ties
+    # between 1 + 2^-7 (odd) and 1 + 2^-6 (even)
+    assert oracle.double_to_bf16([1 + 2 ** -8])[0] == 0x3F80
+    assert oracle.double_to_bf16([1 + 3 * 2 ** -8])[0] == 0x3F82
+    # largest finite (2 - 2^-7) * 2^127; the midpoint to 2^128 rounds up to inf
+    big = (2 - 2 ** -7) * 2.0 ** 127
+    assert oracle.double_to_bf16([big])[0] == 0x7F7F
+    assert oracle.double_to_bf16([(2 - 2 ** -8) * 2.0 ** 127])[0] == 0x7F80
+    # subnormals: quantum 2^-133; half of it ties to zero, 1.5 of it to 2 quanta
+    assert oracle.double_to_bf16([2.0 ** -134])[0] == 0x0000
+    assert oracle.double_to_bf16([3 * 2.0 ** -134])[0] == 0x0002
+    assert oracle.double_to_bf16([-0.0])[0] == 0x8000
+
+
+def _brute_force_exact_bf16(xb, q, z, sb, group):
+    M, K = xb.shape
+    N = q.shape[0]
+    xf = [[Fraction(float(v)) for v in row] for row in _bf16_value(xb)]
+    sf = [[Fraction(float(v)) for v in row] for row in _bf16_value(sb)]
+    y = [[Fraction(0)] * N for _ in range(M)]
+    mag = [[Fraction(0)] * N for _ in range(M)]
+    for m in range(M):
+        for n in range(N):
+            for k in range(K):
+                t = xf[m][k] * (int(q[n, k]) - int(z[n, k // group])) * sf[n][k // group]
+                y[m][n] += t
+                mag[m][n] += abs(t)
+    return y, mag
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (2, 3, 256)])
+def test_linear_bf16_matches_exact_rationals(M, N, K):
+    G = K // 128
+    q = RNG.integers(0, 16, (N, K)).astype(np.uint8)
+    z = RNG.integers(0, 16, (N, G)).astype(np.uint8)
+    sb = _bf16_bits(RNG.uniform(0.002, 0.02, (N, G)))
+    xb = _bf16_bits(RNG.standard_normal((M, K)))
+    qw, zw = oracle.pack(q, z)
+    y = oracle.linear(xb, qw, sb, zw, dtype="bf16")
+    ye, mag = _brute_force_exact_bf16(xb, q, z, sb, 128)
+    for m in range(M):
+        for n in range(N):
+            err = abs(Fraction(y[m, n]) - ye[m][n])
+            assert err <= Fraction(1, 10 ** 12) * (mag[m][n] + Fraction(1, 10 ** 30))
+    rows = np.array([N - 1, 0] if N > 1 else [0])
+    assert np.array_equal(oracle.linear_rows(xb, qw, sb, zw, rows, dtype="bf16"), y[:, rows])
+    # the same bits read as fp16 give a different product: the type is honoured
+    assert not np.array_equal(oracle.linear(xb, qw, sb, zw), y)
+
+
+def test_linear_bf16_integer_case_equals_int64_matmul():
+    # x in {-1, 0, 1} (bf16 0xBF80, 0, 0x3F80), s = 2^-4 (bf16 0x3D80)
+    M, N, K = 3, 7, 512
+    q = RNG.integers(0, 16, (N, K)).astype(np.uint8)
+    z = RNG.integers(0, 16, (N, K // 128)).astype(np.uint8)
+    X = RNG.integers(-1, 2, (M, K)).astype(np.int64)
+    xb = np.where(X == 1, 0x3F80, np.where(X == -1, 0xBF80, 0)).astype(np.uint16)
+    sb = np.full((N, K // 128), 0x3D80, dtype=np.uint16)
+    qw, zw = oracle.pack(q, z)
+    W = q.astype(np.int64) - np.repeat(z.astype(np.int64), 128, axis=1)
+    assert np.array_equal(oracle.linear(xb, qw, sb, zw, dtype="bf16"),
+                          (X @ W.T).astype(np.float64) / 16)
+
+
+def test_add_residual_bf16_exact():
+    n = 300
+    y = RNG.integers(-2 ** 20, 2 ** 20, size=n) / 1024.0
+    rb = _bf16_bits(RNG.normal(size=n) * 4)
+    got = oracle.add_residual(y, rb, dtype="bf16")
+    assert all(Fraction(float(g)) == Fraction(float(a)) + Fraction(float(b))
+               for g, a, b in zip(got, y, _bf16_value(rb)))
