@@ -518,6 +518,20 @@ def main():
              "linears_launched_alone": per_linear,
              "rung_per_shape": {n: w4.rung_name(w4.w4a16_select_rung(M_ROUND, N, K))
                                 for n, K, N in ROUND_SHAPES}}
+    if not args.no_extra and rank == 0:
+        # the same round with bf16 activations and scales (the same packed
+        # weights and zeros; bf16 copies of x and the scales, bf16 outputs)
+        bxs = {id(L["x"]): L["x"].to(torch.bfloat16) for L in lin}
+        blin = [dict(x=bxs[id(L["x"])], qweight=L["qweight"], zeros=L["zeros"],
+                     scales=L["scales"].to(torch.bfloat16),
+                     y=torch.empty_like(L["y"], dtype=torch.bfloat16)) for L in lin]
+        bdescs = w4.make_descs(blin)
+        t = time_round(w4, bdescs, args.steps, args.warmup, stream)
+        bms = t / args.steps * 1e3
+        extra["round_bf16_ms"] = bms
+        extra["round_bf16_GBps"] = rb / (bms / 1e3) / 1e9
+        extra["round_bf16_frac_of_peak"] = rb / (bms / 1e3) / 1e9 / peak
+        del blin, bdescs, bxs
     del lin, descs
     torch.cuda.empty_cache()
 

@@ -165,9 +165,18 @@ typedef enum {
                                     be a multiple of 32 */
 } w4a16_epilogue;
 
+/* The 16-bit type of x, scales, y and the residual.  The pages name fp16 or
+ * bf16 activations; a bf16 layer keeps its scales in bf16 too.  Weights and
+ * zeros are 4-bit either way; accumulation is fp32 either way. */
+typedef enum {
+    W4A16_DTYPE_F16 = 0,  /* IEEE binary16 */
+    W4A16_DTYPE_BF16 = 1  /* bfloat16 (the top half of an IEEE binary32) */
+} w4a16_dtype;
+
 /* One linear of a decode round.  x is [M, K] and y [M, N] ([M, N/2] with
  * SiLU-and-mul); `group` must be 128.  `epilogue` is a w4a16_epilogue;
- * `residual` is [M, N] for W4A16_EPILOGUE_RESIDUAL and NULL otherwise. */
+ * `residual` is [M, N] for W4A16_EPILOGUE_RESIDUAL and NULL otherwise;
+ * `dtype` is a w4a16_dtype (0: fp16). */
 typedef struct {
     const uint16_t *x;
     const uint32_t *qweight;
@@ -179,12 +188,14 @@ typedef struct {
     int group;
     int epilogue;
     const uint16_t *residual;
+    int dtype;
 } w4a16_linear_desc;
 
 /* y = epilogue(x @ W^T): w4a16_linear followed, in the same kernel, by the
  * step `epilogue` names (w4a16_epilogue).  W4A16_EPILOGUE_NONE is exactly
- * w4a16_linear.  The other epilogues run on the warp-MMA rungs only: M <= 8
- * and no forced rung other than those (W4A16_ERR_UNSUPPORTED otherwise).
+ * w4a16_linear.  The other epilogues run on the warp-MMA rungs only (a forced
+ * rung other than those: W4A16_ERR_UNSUPPORTED); more than 8 tokens run as
+ * tiles of 8, each of which reads the weights.
  *   residual  [M, N] fp16, 2-byte aligned, for W4A16_EPILOGUE_RESIDUAL (NULL
  *             otherwise: INVALID_ARG); it may be y itself (y += x @ W^T) but
  *             must not otherwise overlap y.
@@ -198,6 +209,19 @@ typedef struct {
 int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                           const uint32_t *zeros, int M, int N, int K, int group, int epilogue,
                           const uint16_t *residual, uint16_t *y, void *stream);
+
+/* w4a16_linear_epilogue with the 16-bit type `dtype` (w4a16_dtype) of x,
+ * scales, residual and y.  bf16 runs on the warp-MMA rungs only, with the
+ * same rules as the epilogues.  Each token's slice of x is staged as fp16
+ * scaled by a power of two chosen from its largest exponent (so any bf16
+ * magnitude fits; bf16's 8 significant bits fit fp16's 11, so the staged
+ * values are exact but for those 2^29 below the token's largest), the fp16
+ * tensor-core path runs unchanged, and the scale is removed in fp32 before
+ * the one rounding of y to bf16.  W4A16_DTYPE_F16 is exactly
+ * w4a16_linear_epilogue.  An invalid dtype is INVALID_ARG. */
+int w4a16_linear_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                    const uint32_t *zeros, int M, int N, int K, int group, int dtype,
+                    int epilogue, const uint16_t *residual, uint16_t *y, void *stream);
 
 /* A decode round: the linears of `descs` (a HOST array of n_descs entries,
  * e.g. 64 layers x {qkv, o, gate+up, down}) run on `stream`, all at the same
@@ -219,9 +243,10 @@ int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint
  * being captured, launch linear by linear; w4a16_round_graph_create captures
  * the fused form. */
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream);
-/* Each linear of a round applies its own epilogue, with the rules of
- * w4a16_linear_epilogue; a linear's residual counts as one of its inputs for
- * the ordering above. */
+/* Each linear of a round applies its own epilogue and 16-bit type, with the
+ * rules of w4a16_linear_ex; a linear's residual counts as one of its inputs for
+ * the ordering above.  A round whose linears mix fp16 and bf16 launches linear
+ * by linear. */
 
 /* Capture a decode round into an instantiated CUDA graph (an opaque handle in
  * *graph).  Allocates (the graph's own copy of a fused round's descriptors)

@@ -96,6 +96,18 @@ def test_linear_epilogue_validation_codes(w4):
         assert _epi(w4, 0) == w4.W4A16_ERR_NOT_INITIALIZED
 
 
+def test_linear_ex_validation_codes(w4):
+    L = w4.lib
+    args = (A, 2 * A, 3 * A, 4 * A, 1, 64, 256, 128)
+    assert L.w4a16_linear_ex(*args, 2, 0, None, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_linear_ex(*args, -1, 0, None, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_linear_ex(*args, 1, 3, None, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_linear_ex(*args, 1, 1, None, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    if w4.lib.w4a16_device_sm_count() == 0:
+        assert L.w4a16_linear_ex(*args, 1, 0, None, 5 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
+        assert L.w4a16_linear_ex(*args, 1, 1, 6 * A, 5 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
+
+
 def test_repack_validation_codes(w4):
     L, seq = w4.lib, 0x76543210
     assert L.w4a16_repack_transpose(None, 8, 8, seq, A, None) == w4.W4A16_ERR_INVALID_ARG

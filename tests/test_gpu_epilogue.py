@@ -128,12 +128,24 @@ def test_silu_mul_full_gate_up_sampled(w4, rung, M):
     assert torch.isfinite(y).all()
 
 
+@pytest.mark.parametrize("M", [9, 20])
+def test_epilogues_beyond_8_tokens_run_in_tiles(w4, M):
+    # more than 8 tokens: tiles of 8 on the warp-MMA rungs (the residual and
+    # the output rows offset per tile)
+    N, K = 1024, 2048
+    seed = si.config_seed(86, 0, M)
+    x = si.x(seed, M, K)
+    r = si.residual(seed, M, N)
+    qw, s, zw = si.layer(seed, N, K, device=DEV)
+    y = _epilogue(w4, AUTO, x.to(DEV), qw, s, zw, w4.EPILOGUE_RESIDUAL, r.to(DEV), _nan(M, N))
+    h = _oracle_linear(seed, x, N, K)
+    assert_close(y, oracle.add_residual(h, si.as_u16(r)), f"residual M={M}")
+    y = _epilogue(w4, AUTO, x.to(DEV), qw, s, zw, w4.EPILOGUE_SILU_MUL, None, _nan(M, N // 2))
+    assert_close(y, oracle.silu_mul(h), f"silu_mul M={M}")
+
+
 def test_epilogue_rejections_on_device(w4):
     qw, s, zw = si.layer(1, 64, 256, device=DEV)
-    x9 = torch.zeros((9, 256), dtype=torch.float16, device=DEV)
-    with pytest.raises(w4.W4A16Error) as e:  # more than 8 tokens
-        w4.w4a16_linear_epilogue(x9, qw, s, zw, w4.EPILOGUE_SILU_MUL)
-    assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
     x = torch.zeros((2, 256), dtype=torch.float16, device=DEV)
     prev = w4.w4a16_set_forced_rung(0)  # a CUDA-core rung has no epilogue
     try:

@@ -47,6 +47,10 @@ EPILOGUE_NONE = 0
 EPILOGUE_RESIDUAL = 1
 EPILOGUE_SILU_MUL = 2
 
+DTYPE_F16 = 0
+DTYPE_BF16 = 1
+_DTYPE_OF = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
@@ -55,7 +59,8 @@ _SZ = ctypes.c_size_t
 class LinearDesc(ctypes.Structure):
     """Mirror of ``w4a16_linear_desc``."""
     _fields_ = [("x", _P), ("qweight", _P), ("scales", _P), ("zeros", _P), ("y", _P),
-                ("N", _I), ("K", _I), ("group", _I), ("epilogue", _I), ("residual", _P)]
+                ("N", _I), ("K", _I), ("group", _I), ("epilogue", _I), ("residual", _P),
+                ("dtype", _I)]
 
 
 def _sig(name, args, res=_I):
@@ -76,6 +81,7 @@ _sig("w4a16_transpose_f16", [_P, _I, _I, _P, _P])
 _sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_epilogue", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_linear_ex", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -94,7 +100,7 @@ _sig("w4a16_device_sm_count", [])
 EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
             "w4a16_unpack", "w4a16_dequant", "w4a16_repack_transpose", "w4a16_transpose_f16",
             "w4a16_linear", "w4a16_linear_noalloc",
-            "w4a16_linear_epilogue",
+            "w4a16_linear_epilogue", "w4a16_linear_ex",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -269,6 +275,28 @@ def w4a16_linear_epilogue(x: torch.Tensor, qweight: torch.Tensor, scales: torch.
     return y
 
 
+def w4a16_linear_ex(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                    zeros: torch.Tensor, epilogue: int = EPILOGUE_NONE, residual=None,
+                    group: int = GROUP, y=None, stream=None) -> torch.Tensor:
+    """w4a16_linear_epilogue for fp16 or bf16 data: x, scales, residual and y
+    share one dtype (torch.float16 or torch.bfloat16)."""
+    M, K = x.shape
+    N = qweight.shape[0]
+    if x.dtype not in _DTYPE_OF:
+        raise TypeError(f"x must be float16 or bfloat16, got {x.dtype}")
+    dt = x.dtype
+    cols = N // 2 if epilogue == EPILOGUE_SILU_MUL else N
+    if y is None:
+        y = torch.empty((M, cols), dtype=dt, device=x.device)
+    r = _dev(residual, dt, "residual") if residual is not None else None
+    _check(lib.w4a16_linear_ex(_dev(x, dt, "x"), _dev(qweight, torch.int32, "qweight"),
+                               _dev(scales, dt, "scales"), _dev(zeros, torch.int32, "zeros"),
+                               M, N, K, group, _DTYPE_OF[dt], epilogue, r, _dev(y, dt, "y"),
+                               _stream_ptr(stream)),
+           "w4a16_linear_ex")
+    return y
+
+
 def make_descs(layers) -> ctypes.Array:
     """layers: iterable of dicts with x, qweight, scales, zeros, y tensors (and
     optionally an epilogue code and a residual tensor) -> host desc array."""
@@ -277,11 +305,15 @@ def make_descs(layers) -> ctypes.Array:
     for i, L in enumerate(layers):
         N, K = L["qweight"].shape[0], L["x"].shape[1]
         res = L.get("residual")
-        arr[i] = LinearDesc(_dev(L["x"], torch.float16, "x"), _dev(L["qweight"], torch.int32, "qweight"),
-                            _dev(L["scales"], torch.float16, "scales"),
-                            _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], torch.float16, "y"),
+        dt = L["x"].dtype
+        if dt not in _DTYPE_OF:
+            raise TypeError(f"x must be float16 or bfloat16, got {dt}")
+        arr[i] = LinearDesc(_dev(L["x"], dt, "x"), _dev(L["qweight"], torch.int32, "qweight"),
+                            _dev(L["scales"], dt, "scales"),
+                            _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], dt, "y"),
                             N, K, L.get("group", GROUP), L.get("epilogue", EPILOGUE_NONE),
-                            _dev(res, torch.float16, "residual") if res is not None else None)
+                            _dev(res, dt, "residual") if res is not None else None,
+                            _DTYPE_OF[dt])
     return arr
 
 

@@ -64,6 +64,8 @@ constexpr int kMaxRepackDim = 1 << 24;  // rows and columns of a repacked matrix
 static_assert(kEpiNone == W4A16_EPILOGUE_NONE && kEpiResidual == W4A16_EPILOGUE_RESIDUAL &&
                   kEpiSiluMul == W4A16_EPILOGUE_SILU_MUL,
               "internal epilogue codes follow the ABI");
+static_assert(kDtypeF16 == W4A16_DTYPE_F16 && kDtypeBf16 == W4A16_DTYPE_BF16,
+              "internal 16-bit type codes follow the ABI");
 
 int check_shape(int N, int K, int group) {
     if (N < 1 || K < 1 || K > kMaxK) return W4A16_ERR_INVALID_ARG;
@@ -74,9 +76,11 @@ int check_shape(int N, int K, int group) {
 
 int check_linear(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                  const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y,
-                 int epi = W4A16_EPILOGUE_NONE, const uint16_t *residual = nullptr) {
+                 int epi = W4A16_EPILOGUE_NONE, const uint16_t *residual = nullptr,
+                 int dtype = W4A16_DTYPE_F16) {
     if (!x || !qweight || !scales || !zeros || !y) return W4A16_ERR_INVALID_ARG;
     if (M < 1 || M > kMaxM) return W4A16_ERR_INVALID_ARG;
+    if (dtype != W4A16_DTYPE_F16 && dtype != W4A16_DTYPE_BF16) return W4A16_ERR_INVALID_ARG;
     int st = check_shape(N, K, group);
     if (st) return st;
     if (epi != W4A16_EPILOGUE_NONE && epi != W4A16_EPILOGUE_RESIDUAL &&
@@ -112,13 +116,18 @@ int tile_tokens(int rung) {
     return is_tc(rung) ? kTcMaxTokens : (is_mma(rung) ? kMmaMaxTokens : kGemvMaxTokens);
 }
 
-Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi = kEpiNone) {
+Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi = kEpiNone,
+                int dtype = kDtypeF16) {
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
     const int G = K / kGroup;
-    if (epi != kEpiNone) {
-        // the epilogues run in the warp-MMA kernel only: up to 8 tokens
-        if (M > kMmaMaxTokens || (forced != W4A16_RUNG_AUTO && !is_mma(forced)))
-            return {forced, W4A16_ERR_UNSUPPORTED};
+    if (epi != kEpiNone || dtype != kDtypeF16) {
+        // the epilogues and bf16 data run in the warp-MMA kernel only (tiles
+        // of up to 8 tokens, each reading the weights)
+        if (forced != W4A16_RUNG_AUTO && !is_mma(forced)) return {forced, W4A16_ERR_UNSUPPORTED};
+        if (forced == W4A16_RUNG_AUTO) {
+            MmaPlan p = plan_mma(Mt, N, K, -1, dev, epi);
+            return {p.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, W4A16_OK};
+        }
     }
     switch (forced) {
         case W4A16_RUNG_GEMV: {
@@ -253,21 +262,21 @@ int parse_rung(const char *s) {
 int linear_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                 const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
                 void *stream, bool validated, int epi = kEpiNone,
-                const uint16_t *residual = nullptr) {
+                const uint16_t *residual = nullptr, int dtype = kDtypeF16) {
     if (!validated) {
-        int st = check_linear(x, qweight, scales, zeros, M, N, K, group, y, epi, residual);
+        int st = check_linear(x, qweight, scales, zeros, M, N, K, group, y, epi, residual, dtype);
         if (st) return st;
     }
     const State &s = g_state;
     if (!s.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    Decision d = decide(M, N, K, s.dev, s.forced_rung, epi);
+    Decision d = decide(M, N, K, s.dev, s.forced_rung, epi, dtype);
     if (d.status) return d.status;
     int st = check_workspace(d.rung, M, N, K, s, epi);
     if (st) return st;
     LinearArgs a{reinterpret_cast<const __half *>(x), qweight,
                  reinterpret_cast<const __half *>(scales), zeros,
                  reinterpret_cast<__half *>(y), M, N, K, epi,
-                 reinterpret_cast<const __half *>(residual)};
+                 reinterpret_cast<const __half *>(residual), dtype};
     return launch_linear(a, d.rung, s, (cudaStream_t)stream);
 }
 
@@ -294,6 +303,9 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
     if (st.forced_rung != W4A16_RUNG_AUTO || M > kMmaMaxTokens || n > kMaxRoundLinears)
         return W4A16_ERR_UNSUPPORTED;
     fr->descs.resize(n);
+    // one launch instantiates one 16-bit type
+    for (int l = 1; l < n; ++l)
+        if (descs[l].dtype != descs[0].dtype) return W4A16_ERR_UNSUPPORTED;
     size_t partial_floats = 0;
     int counters = 0, units = 0, smem = 0;
     bool waits = false;
@@ -328,7 +340,7 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
         LinearArgs a{reinterpret_cast<const __half *>(d.x), d.qweight,
                      reinterpret_cast<const __half *>(d.scales), d.zeros,
                      reinterpret_cast<__half *>(d.y), M, d.N, d.K, d.epilogue,
-                     reinterpret_cast<const __half *>(d.residual)};
+                     reinterpret_cast<const __half *>(d.residual), d.dtype};
         cudaError_t e = mma_describe(a, p, part, cnt, units, wait_for, &fr->descs[l]);
         if (e != cudaSuccess) return cuda_fail(e);
         units += p.units;
@@ -340,6 +352,7 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
     fr->round.total_units = units;
     fr->round.smem_bytes = smem;
     fr->round.done = waits ? st.ws.counters + counters : nullptr;
+    fr->round.bf16 = descs[0].dtype == W4A16_DTYPE_BF16;
     fr->counters_used = counters + (waits ? n : 0);
     return W4A16_OK;
 }
@@ -355,7 +368,7 @@ int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
         int st = check_linear(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y,
-                              d.epilogue, d.residual);
+                              d.epilogue, d.residual, d.dtype);
         if (st) return st;
     }
     if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
@@ -366,7 +379,7 @@ int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
 int round_per_linear(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
-        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung, d.epilogue);
+        Decision dec = decide(M, d.N, d.K, g_state.dev, g_state.forced_rung, d.epilogue, d.dtype);
         if (dec.status) return dec.status;
         int st = check_workspace(dec.rung, M, d.N, d.K, g_state, d.epilogue);
         if (st) return st;
@@ -374,7 +387,7 @@ int round_per_linear(const w4a16_linear_desc *descs, int n_descs, int M, void *s
     for (int i = 0; i < n_descs; ++i) {
         const w4a16_linear_desc &d = descs[i];
         int st = linear_impl(d.x, d.qweight, d.scales, d.zeros, M, d.N, d.K, d.group, d.y, stream,
-                             true, d.epilogue, d.residual);
+                             true, d.epilogue, d.residual, d.dtype);
         if (st) return st;
     }
     return W4A16_OK;
@@ -540,6 +553,13 @@ int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint
                           const uint16_t *residual, uint16_t *y, void *stream) {
     return linear_impl(x, qweight, scales, zeros, M, N, K, group, y, stream, false, epilogue,
                        residual);
+}
+
+int w4a16_linear_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                    const uint32_t *zeros, int M, int N, int K, int group, int dtype,
+                    int epilogue, const uint16_t *residual, uint16_t *y, void *stream) {
+    return linear_impl(x, qweight, scales, zeros, M, N, K, group, y, stream, false, epilogue,
+                       residual, dtype);
 }
 
 int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void *stream) {

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -17,6 +18,9 @@ constexpr int kGroup = 128;  // inputs per quantisation group
 constexpr int kEpiNone = 0;
 constexpr int kEpiResidual = 1;
 constexpr int kEpiSiluMul = 2;
+// The 16-bit type of x, scales, y and the residual (the values of w4a16_dtype).
+constexpr int kDtypeF16 = 0;
+constexpr int kDtypeBf16 = 1;
 
 // One W4A16 linear, device pointers.  x [M, K] fp16; qw [N, K/8]; scales
 // [N, G] fp16; zeros [N, ceil(G/8)]; y [M, N] fp16 ([M, N/2] for SiLU-and-mul);
@@ -30,6 +34,7 @@ struct LinearArgs {
     int M, N, K;
     int epi = kEpiNone;
     const __half *residual = nullptr;
+    int dtype = kDtypeF16;  // bf16 data travels in __half storage, reinterpreted
 };
 
 // Output columns of a linear with epilogue epi.
@@ -164,6 +169,7 @@ struct MmaRound {
     int total_units;
     int smem_bytes;
     unsigned *done;
+    bool bf16;  // every linear of the round has bf16 data
 };
 int mma_round_grid(const DeviceInfo &dev);
 int mma_smem_bytes(int M, int slice_groups);

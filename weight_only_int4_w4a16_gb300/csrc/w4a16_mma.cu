@@ -110,6 +110,40 @@ constexpr float kTwoM20 = 1.f / 1048576.f;
 // quarter warp (two tokens x four lanes) fall on distinct banks.
 __device__ __forceinline__ int x_unit(int J) { return J ^ (((J >> 3) & 1) << 1); }
 
+// bf16 activations are staged as fp16 for the fp16 MMA: token t's values are
+// scaled by 2^k_t, k_t chosen from the largest exponent field E_t among them so
+// that every scaled value is below 2^15 (fp16's range); the scale leaves at
+// the end of each strip.  Values 2^29 below the token's largest lose bits to
+// fp16's subnormals (an error under 2^-39 of the largest).  The exponents sit
+// in 8 ints after the staged x and its sums.
+__device__ __forceinline__ int *token_exps(uint8_t *xs, int M, int xstride, int slice_groups) {
+    return reinterpret_cast<int *>(xs + (size_t)M * xstride + (size_t)slice_groups * 8 * 4);
+}
+// k_t for a largest biased exponent E (values below 2^(E - 126)), kept within
+// the float exponent range so that 2^k and 2^-k are finite
+__device__ __forceinline__ int bf16_stage_shift(int E) { return max(-126, min(126, 141 - E)); }
+__device__ __forceinline__ float pow2(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+// largest exponent field among the 8 bf16 values of a 16-byte unit
+__device__ __forceinline__ int max_bf16_exp(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int e = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e = max(e, max((int)((w[i] >> 7) & 0xffu), (int)((w[i] >> 23) & 0xffu)));
+    return e;
+}
+// 8 bf16 values times 2^k, rounded to fp16 (exact but for the subnormal tail)
+__device__ __forceinline__ uint4 bf16_to_scaled_f16(uint4 v, float scale) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * scale,
+                                            __uint_as_float(w[i] & 0xffff0000u) * scale);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -117,6 +151,29 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         "{%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16-bit activations, scales and outputs are IEEE binary16 or bfloat16 (the
+// top half of a binary32); storage is 16-bit either way.
+template <bool kBf16>
+__device__ __forceinline__ float to_float(__half h) {
+    if constexpr (kBf16) return __uint_as_float((uint32_t)__half_as_ushort(h) << 16);
+    else return __half2float(h);
+}
+template <bool kBf16>
+__device__ __forceinline__ float bits_to_float(uint32_t bits16) {  // low 16 bits
+    if constexpr (kBf16) return __uint_as_float(bits16 << 16);
+    else return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+template <bool kBf16>
+__device__ __forceinline__ __half from_float(float v) {  // round to nearest even
+    if constexpr (kBf16) return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    else return __float2half_rn(v);
+}
+template <bool kBf16>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t v) {
+    if constexpr (kBf16) return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+    else return __half22float2(*reinterpret_cast<const __half2 *>(&v));
 }
 
 // ---- copies and barriers ----------------------------------------------------
@@ -232,11 +289,11 @@ constexpr int kQueueAhead = 1;  // units fetched ahead of the one being consumed
 
 // The epilogue of one output: y = h, h + residual, or silu(gate) * h (the
 // up projection h and its gate both in fp32; silu(g) = g / (1 + e^-g)).
-template <class Lin>
+template <bool kBf16, class Lin>
 __device__ __forceinline__ void epilogue_store(const Lin &R, size_t o, float h, float gate) {
-    if (R.epi == kEpiResidual) h += __half2float(R.residual[o]);
+    if (R.epi == kEpiResidual) h += to_float<kBf16>(R.residual[o]);
     else if (R.epi == kEpiSiluMul) h *= gate / (1.f + expf(-gate));
-    R.y[o] = __float2half_rn(h);
+    R.y[o] = from_float<kBf16>(h);
 }
 
 // y = the epilogue of the sum of the S partial slices of block sb of a linear,
@@ -244,6 +301,7 @@ __device__ __forceinline__ void epilogue_store(const Lin &R, size_t o, float h, 
 // row: half of the sums a thread keeps are gate rows, the other half the up
 // rows of the same outputs (the register footprint stays that of 8 sums: the
 // callers keep their registers across this call).
+template <bool kBf16>
 __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
@@ -280,14 +338,14 @@ __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
             if ((silu && j >= kH) || i >= n_out) continue;
             const int t = i / nrows, row = row0 + i - t * nrows;
             const size_t o = (size_t)t * R.ycols + row;
-            if (silu) epilogue_store(R, o, sum[j + kH], sum[j]);
-            else epilogue_store(R, o, sum[j], 0.f);
+            if (silu) epilogue_store<kBf16>(R, o, sum[j + kH], sum[j]);
+            else epilogue_store<kBf16>(R, o, sum[j], 0.f);
         }
     }
     if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
 }
 
-template <bool kRound>
+template <bool kRound, bool kBf16>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     mma_kernel(const __grid_constant__ MmaKernelParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -510,6 +568,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // its staged row (raw order; rewritten in place once it lands)
     auto issue_x = [&](const UnitInfo &L, int xg0, int xng) {
         const uint32_t row_bytes = (uint32_t)xng * kGroup * 2;
+        if (kBf16) {
+            // the tokens' largest exponents, gathered once the copy lands:
+            // cleared before the arrival, which releases the stores to every
+            // thread that waits on the barrier
+            int *xe = token_exps(xs, L.M, L.xstride, L.slice_groups);
+            for (int t = 0; t < kMmaMaxTokens; ++t) xe[t] = 0;
+        }
         mbar_arrive_expect_tx(x_bar, row_bytes * L.M);
         for (int t = 0; t < L.M; ++t)
             asm volatile(
@@ -599,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // all threads, after the barrier that follows publish_reduction(boundary)
     auto maybe_reduce = [&](int boundary) {
         volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
-        if (f[0]) reduce_block(desc(f[1]), f[2]);
+        if (f[0]) reduce_block<kBf16>(desc(f[1]), f[2]);
     };
 
     // boundary b: the barrier at the top of iteration b (b = k), or an extra
@@ -709,6 +774,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             xpend_l = -1;
             const int nunits = ng * (kGroup / 8);
             const int xtotal = M * nunits;  // a multiple of 16
+            int *xexp = token_exps(xs, M, D.xstride, D.slice_groups);
+            if (kBf16) {
+                // each token's largest exponent: a half warp holds 16 units of
+                // one token (nunits is a multiple of 16)
+                for (int base = warp * 32; base < xtotal; base += kThreads) {
+                    const int i = base + lane;
+                    const int t = i / nunits, J = i - t * nunits;
+                    int e = 0;
+                    if (i < xtotal)
+                        e = max_bf16_exp(*reinterpret_cast<const uint4 *>(
+                            xs + (size_t)t * D.xstride + 16 * J));
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, off));
+                    if (i < xtotal && (J & 15) == 0) atomicMax(xexp + t, e);
+                }
+                __syncthreads();
+            }
             for (int base = warp * 32; base < xtotal; base += kThreads) {
                 const int i = base + lane;
                 const bool valid = i < xtotal;
@@ -716,12 +798,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 uint8_t *row = xs + (size_t)t * D.xstride;
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid) v = *reinterpret_cast<const uint4 *>(row + 16 * J);
+                if (kBf16 && valid) v = bf16_to_scaled_f16(v, pow2(bf16_stage_shift(xexp[t])));
                 __syncwarp();
                 if (valid) *reinterpret_cast<uint4 *>(row + 16 * x_unit(J)) = mma_pair_order(v);
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-                const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-                const float2 e = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
-                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+                const float2 a = pair_to_float2<false>(v.x), bb = pair_to_float2<false>(v.y);
+                const float2 e = pair_to_float2<false>(v.z), f = pair_to_float2<false>(v.w);
                 float sum = ((a.x + a.y) + (bb.x + bb.y)) + ((e.x + e.y) + (f.x + f.y));
 #pragma unroll
                 for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
@@ -805,8 +886,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             hA = mA[i >> 1] >> shA;
                             hB = mB[i >> 1] >> shB;
                         }
-                        const float sA = __half2float(__ushort_as_half((unsigned short)hA));
-                        const float sB = __half2float(__ushort_as_half((unsigned short)hB));
+                        const float sA = bits_to_float<kBf16>(hA & 0xffffu);
+                        const float sB = bits_to_float<kBf16>(hB & 0xffffu);
+                        // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
                         // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
                         const float zA =
                             __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;
@@ -862,6 +944,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[e] *= kTwo20;
                 const int t0 = 2 * c, t1 = 2 * c + 1;
+                if (kBf16) {  // undo the tokens' staging scales
+                    const int *xexp = token_exps(xs, M, D.xstride, D.slice_groups);
+                    const float u0 = pow2(-bf16_stage_shift(xexp[t0]));
+                    const float u1 = pow2(-bf16_stage_shift(xexp[t1]));
+                    acc[0] *= u0;
+                    acc[1] *= u1;
+                    acc[2] *= u0;
+                    acc[3] *= u1;
+                }
                 if (to_ws) {  // this slice's partial sums, by weight row
                     float *ps = D.partials + (size_t)slice * M * D.N;
                     if (va && t0 < M) ps[(size_t)t0 * D.N + ra] = acc[0];
@@ -873,15 +964,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 // y, or y + residual (read as fp32, one rounding)
                 const size_t ya = (size_t)t0 * D.ycols + ra, yb = (size_t)t0 * D.ycols + rb;
                 if (D.epi == kEpiResidual) {
-                    if (va && t0 < M) acc[0] += __half2float(D.residual[ya]);
-                    if (va && t1 < M) acc[1] += __half2float(D.residual[ya + D.ycols]);
-                    if (vb && t0 < M) acc[2] += __half2float(D.residual[yb]);
-                    if (vb && t1 < M) acc[3] += __half2float(D.residual[yb + D.ycols]);
+                    if (va && t0 < M) acc[0] += to_float<kBf16>(D.residual[ya]);
+                    if (va && t1 < M) acc[1] += to_float<kBf16>(D.residual[ya + D.ycols]);
+                    if (vb && t0 < M) acc[2] += to_float<kBf16>(D.residual[yb]);
+                    if (vb && t1 < M) acc[3] += to_float<kBf16>(D.residual[yb + D.ycols]);
                 }
-                if (va && t0 < M) D.y[ya] = __float2half_rn(acc[0]);
-                if (va && t1 < M) D.y[ya + D.ycols] = __float2half_rn(acc[1]);
-                if (vb && t0 < M) D.y[yb] = __float2half_rn(acc[2]);
-                if (vb && t1 < M) D.y[yb + D.ycols] = __float2half_rn(acc[3]);
+                if (va && t0 < M) D.y[ya] = from_float<kBf16>(acc[0]);
+                if (va && t1 < M) D.y[ya + D.ycols] = from_float<kBf16>(acc[1]);
+                if (vb && t0 < M) D.y[yb] = from_float<kBf16>(acc[2]);
+                if (vb && t1 < M) D.y[yb + D.ycols] = from_float<kBf16>(acc[3]);
             }
             if (dead) break;
         }
@@ -964,7 +1055,8 @@ cudaLaunchConfig_t launch_config(int grid, int smem, cudaStream_t stream,
 }  // namespace
 
 int mma_smem_bytes(int M, int slice_groups) {
-    return kRingBytes + kBarBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 4;
+    return kRingBytes + kBarBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 4 +
+           kMmaMaxTokens * 4;
 }
 
 int mma_round_grid(const DeviceInfo &dev) { return kCtasPerSm * dev.sm_count; }
@@ -982,7 +1074,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi)
     pl.n_blocks = (pl.n_strips + kWarps * pl.strips_per_warp - 1) / (kWarps * pl.strips_per_warp);
     // largest slice (a whole number of stages) whose staged x and sums fit
     const int budget = kSmemPerCta - kRingBytes - kBarBytes;
-    int max_groups = (budget - 16 * M) / (kGroup * 2 * M + 32);
+    int max_groups = (budget - 16 * M - kMmaMaxTokens * 4) / (kGroup * 2 * M + 32);
     max_groups = max_groups / kStageGroups * kStageGroups;
     if (max_groups > kMaxSliceGroups) max_groups = kMaxSliceGroups;
     if (max_groups < kStageGroups) max_groups = kStageGroups;
@@ -1100,6 +1192,7 @@ cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partia
 
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
                        cudaStream_t stream) {
+    const bool bf16 = a.dtype == kDtypeBf16;
     MmaKernelParams P;
     memset(&P, 0, sizeof(P));
     cudaError_t e = mma_describe(a, plan, ws.partials, ws.counters, 0, -1, &P.single);
@@ -1111,7 +1204,8 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     P.dynamic = 0;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config(plan.grid, plan.smem_bytes, stream, attr);
-    return cudaLaunchKernelEx(&cfg, mma_kernel<false>, P);
+    return bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<false, true>, P)
+                : cudaLaunchKernelEx(&cfg, mma_kernel<false, false>, P);
 }
 
 cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const DeviceInfo &dev,
@@ -1135,7 +1229,8 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
         attr[1].val.cooperative = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, mma_kernel<true>, P);
+    return r.bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<true, true>, P)
+                  : cudaLaunchKernelEx(&cfg, mma_kernel<true, false>, P);
 }
 
 cudaError_t mma_init(const DeviceInfo &dev) {
@@ -1151,8 +1246,12 @@ cudaError_t mma_init(const DeviceInfo &dev) {
     int dyn = kSmemPerCta;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     cudaError_t e = cudaSuccess;
-    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
-        const void *fn = k ? (const void *)mma_kernel<true> : (const void *)mma_kernel<false>;
+    const void *fns[4] = {(const void *)mma_kernel<false, false>,
+                          (const void *)mma_kernel<true, false>,
+                          (const void *)mma_kernel<false, true>,
+                          (const void *)mma_kernel<true, true>};
+    for (int k = 0; k < 4 && e == cudaSuccess; ++k) {
+        const void *fn = fns[k];
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
