@@ -209,6 +209,18 @@ def time_e2e(w4, lin, xs, steps, warmup, stream):
     return (t1 - t0), h2d, d2h
 
 
+def job_rate(elapsed_s: float, bytes_per_step: int, steps: int, world: int, device=None):
+    """Whole-job GB/s of `world` replicas that each moved bytes_per_step * steps:
+    the job's time is the slowest rank's (max over ranks, one all-reduce when
+    world > 1).  Returns (GB/s, that time)."""
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    return bytes_per_step * steps * world / elapsed_s / 1e9, elapsed_s
+
+
 def flush_l2(buf):
     # read-only sweep of a buffer larger than L2: evicts the weights without
     # leaving dirty lines whose write-back would slow the timed kernel
@@ -449,14 +461,10 @@ def main():
     launches1 = w4.w4a16_kernel_launches()
     elapsed = ev0.elapsed_time(ev1) / 1e3
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
     launches = int(launches1 - launches0)
 
     rb = round_bytes(layers=args.layers)
-    value = rb * args.steps * world / elapsed / 1e9
+    value, elapsed = job_rate(elapsed, rb, args.steps, world, dev)
     ms = elapsed / args.steps * 1e3
     peak, peak_kind = load_peaks()
 
@@ -494,7 +502,8 @@ def main():
     # ---- end to end through the C ABI with host buffers ----------------------
     e2e_s, h2d, d2h = time_e2e(w4, lin, xs, max(3, args.steps // 2), 2, stream)
     e2e_steps = max(3, args.steps // 2)
-    e2e = {"value": rb * e2e_steps * world / e2e_s / 1e9, "unit": "GB/s",
+    e2e_value, e2e_s = job_rate(e2e_s, rb, e2e_steps, world, dev)
+    e2e = {"value": e2e_value, "unit": "GB/s",
            "ms_per_step": e2e_s / e2e_steps * 1e3, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
