@@ -61,6 +61,8 @@ def _bind(lib):
     lib.w4o_silu_mul.argtypes = [P, I, I, P]
     lib.w4o_transpose_u4.argtypes = [P, L, L, ctypes.c_uint32, P]
     lib.w4o_transpose_u16.argtypes = [P, L, L, P]
+    lib.w4o_dense_linear.argtypes = [P, P, I, I, I, I, P]
+    lib.w4o_dense_linear_rows.argtypes = [P, P, I, I, I, I, P, I, P]
     lib.w4o_round_to_half.argtypes = [P, L, P]
     lib.w4o_half_array_to_double.argtypes = [P, L, P]
     lib.w4o_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -76,7 +78,8 @@ def _bind(lib):
               lib.w4o_half_array_to_double, lib.w4o_round_to_bf16,
               lib.w4o_bf16_array_to_double, lib.w4o_linear_dt, lib.w4o_linear_rows_dt,
               lib.w4o_silu_mul, lib.w4o_add_residual_dt,
-              lib.w4o_transpose_u4, lib.w4o_transpose_u16):
+              lib.w4o_transpose_u4, lib.w4o_transpose_u16, lib.w4o_dense_linear,
+              lib.w4o_dense_linear_rows):
         f.restype = None
     return lib
 
@@ -270,3 +273,24 @@ def transpose_u16(src: np.ndarray) -> np.ndarray:
     dst = np.empty((cols, rows), dtype=np.uint16)
     _load().w4o_transpose_u16(_ptr(src), rows, cols, _ptr(dst))
     return dst
+
+
+def dense_linear(x: np.ndarray, w: np.ndarray, dtype: str = "f16", rows=None) -> np.ndarray:
+    """y[M, N] = x @ w^T in binary64 for 16-bit x [M, K] and w [N, K] (bit
+    patterns, type dtype); with rows, only those output rows: y[M, len(rows)]."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    assert w.shape == (N, K)
+    if rows is None:
+        y = np.empty((M, N), dtype=np.float64)
+        _load().w4o_dense_linear(_ptr(x), _ptr(w), M, N, K, _DTYPES[dtype], _ptr(y))
+        return y
+    rows = _c(np.asarray(rows, dtype=np.int64), np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= N):
+        raise IndexError("row index out of range")
+    y = np.empty((M, rows.size), dtype=np.float64)
+    _load().w4o_dense_linear_rows(_ptr(x), _ptr(w), M, N, K, _DTYPES[dtype], _ptr(rows),
+                                  int(rows.size), _ptr(y))
+    return y

@@ -42,7 +42,9 @@
  *   transpose against the pinned pack/unpack, a hand 8 x 8 block, ragged rows
  *   and a nibble-order permutation; bfloat16 conversions against numpy's
  *   binary32 decoder over every pattern, neighbours and ties; the bf16 linear
- *   against exact rationals and an int64 matrix product.
+ *   against exact rationals and an int64 matrix product; the dense 16-bit
+ *   linear against exact rationals, an int64 product and, bit for bit, the
+ *   4-bit linear over its own exactly representable dequantised weights.
  */
 #include <math.h>
 #include <pthread.h>
@@ -408,4 +410,37 @@ void w4o_transpose_u16(const uint16_t *src, long rows, long cols, uint16_t *dst)
 {
     for (long r = 0; r < rows; ++r)
         for (long c = 0; c < cols; ++c) dst[c * rows + r] = src[r * cols + c];
+}
+
+/* ---- dense 16-bit linear (Z100 thread, section 六: weights dequantised to
+ * fp16/bf16 once at load time, then a large-K, small-M GEMV with fp32
+ * products and sums).  TEST INFRASTRUCTURE ONLY.
+ * y[m, n] = sum_k x[m, k] * w[n, k] in binary64, increasing k; x [M, K] and
+ * w [N, K] are 16-bit bit patterns of type dtype (0 binary16, 1 bfloat16).
+ * Each product is exact in binary64 (at most 11 + 11 significant bits). */
+void w4o_dense_linear(const uint16_t *x, const uint16_t *w, int M, int N, int K, int dtype,
+                      double *y)
+{
+    decode16_fn dec = decoder_for(dtype);
+    for (long m = 0; m < M; ++m)
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);
+            y[m * N + n] = acc;
+        }
+}
+
+/* The same for the listed output rows only: y[M, nrows]. */
+void w4o_dense_linear_rows(const uint16_t *x, const uint16_t *w, int M, int N, int K,
+                           int dtype, const int64_t *rows, int nrows, double *y)
+{
+    decode16_fn dec = decoder_for(dtype);
+    (void)N;
+    for (long m = 0; m < M; ++m)
+        for (long i = 0; i < nrows; ++i) {
+            const long n = (long)rows[i];
+            double acc = 0.0;
+            for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);
+            y[m * nrows + i] = acc;
+        }
 }

@@ -49,6 +49,10 @@ MUTANTS = {
                        "    if (m == 0) return sign;\n    if (m < 128)"),
     "bf16_read_as_half": ("return dtype == 1 ? w4o_bf16_to_double : w4o_half_to_double;",
                           "return w4o_half_to_double;"),
+    "dense_transposed_weight": ("for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);\n            y[m * N + n] = acc;",
+                                "for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[(k % N) * K + n % K]);\n            y[m * N + n] = acc;"),
+    "dense_last_term_dropped": ("for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);\n            y[m * N + n] = acc;",
+                                "for (long k = 0; k < K - 1; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);\n            y[m * N + n] = acc;"),
     "pack_zero_pad_dirty": ("if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);",
                             "word |= (uint32_t)(z[n * G + (g < G ? g : G - 1)] & 0xfu) << (4 * j);"),
 }
@@ -85,6 +89,10 @@ def _pin_calls():
         lambda: pins.test_linear_bf16_matches_exact_rationals(2, 3, 256),
         pins.test_linear_bf16_integer_case_equals_int64_matmul,
         pins.test_add_residual_bf16_exact,
+        lambda: pins.test_dense_linear_matches_exact_rationals("f16"),
+        lambda: pins.test_dense_linear_matches_exact_rationals("bf16"),
+        pins.test_dense_linear_equals_the_4bit_linear_on_its_dequantised_weights,
+        pins.test_dense_linear_integer_case_equals_int64_matmul,
     ]
 
 

@@ -550,3 +550,50 @@ def test_add_residual_bf16_exact():
     got = oracle.add_residual(y, rb, dtype="bf16")
     assert all(Fraction(float(g)) == Fraction(float(a)) + Fraction(float(b))
                for g, a, b in zip(got, y, _bf16_value(rb)))
+
+
+# ----------------------------------------------------------------------------
+# dense 16-bit linear (weights dequantised at load time; Z100 thread, section 六)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_dense_linear_matches_exact_rationals(dtype):
+    M, N, K = 2, 3, 96
+    if dtype == "f16":
+        xb = _f16_bits(RNG.standard_normal((M, K)))
+        wb = _f16_bits(RNG.standard_normal((N, K)) * 0.05)
+        dec = lambda b: b.view(np.float16).astype(np.float64)  # noqa: E731
+    else:
+        xb = _bf16_bits(RNG.standard_normal((M, K)))
+        wb = _bf16_bits(RNG.standard_normal((N, K)) * 0.05)
+        dec = _bf16_value
+    y = oracle.dense_linear(xb, wb, dtype)
+    xf, wf = dec(xb), dec(wb)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(xf[m], wf[n]))
+            mag = sum(abs(Fraction(float(a)) * Fraction(float(b))) for a, b in zip(xf[m], wf[n]))
+            assert abs(Fraction(y[m, n]) - exact) <= Fraction(1, 10 ** 12) * (mag + Fraction(1, 10 ** 30))
+    rows = np.array([2, 0])
+    assert np.array_equal(oracle.dense_linear(xb, wb, dtype, rows=rows), y[:, rows])
+
+
+def test_dense_linear_equals_the_4bit_linear_on_its_dequantised_weights():
+    # s a power of two: every (q - z) * s is exact in fp16, so the dense product
+    # over those weights adds the same binary64 terms in the same order as the
+    # (pinned) 4-bit oracle: bit-identical
+    M, N, K = 3, 5, 512
+    q = RNG.integers(0, 16, (N, K)).astype(np.uint8)
+    z = RNG.integers(0, 16, (N, K // 128)).astype(np.uint8)
+    sb = np.full((N, K // 128), 0x2C00, dtype=np.uint16)  # 1/16
+    xb = _f16_bits(RNG.standard_normal((M, K)))
+    qw, zw = oracle.pack(q, z)
+    w = (q.astype(np.float64) - np.repeat(z, 128, axis=1)) / 16
+    assert np.array_equal(oracle.dense_linear(xb, _f16_bits(w)), oracle.linear(xb, qw, sb, zw))
+
+
+def test_dense_linear_integer_case_equals_int64_matmul():
+    M, N, K = 4, 7, 300
+    X = RNG.integers(-1, 2, (M, K)).astype(np.int64)
+    W = RNG.integers(-50, 51, (N, K)).astype(np.int64)
+    y = oracle.dense_linear(_f16_bits(X), _f16_bits(W))
+    assert np.array_equal(y, (X @ W.T).astype(np.float64))
