@@ -306,6 +306,41 @@ def time_repack(w4, dev, flush, peak, reps=10):
             "frac_of_peak": by / t / 1e9 / peak}
 
 
+def time_dense(w4, dev, flush, peak, reps=20):
+    """The dense 16-bit linear on the pages' shape (N 8192, K 5120, M 2/4/8) and
+    on a gate+up-sized layer (N 34816): median single launch, L2 evicted."""
+    import synthetic_inputs as si
+    out = {}
+    for N, K in ((8192, 5120), (34816, 5120)):
+        qw, s, zw = si.layer(si.config_seed(7), N, K, device=dev)
+        _, w16 = w4.w4a16_dequant(qw, s, zw, K, f32=False)  # seeded weights made on the device
+        del qw, s, zw
+        for dt in (torch.float16, torch.bfloat16):
+            w = w16 if dt == torch.float16 else w16.to(dt)
+            for M in (1, 2, 4, 8):
+                x = si.x(si.config_seed(7, 0, M), M, K).to(dev).to(dt)
+                y = torch.empty((M, N), dtype=dt, device=dev)
+                for _ in range(3):
+                    w4.w4a16_dense_linear(x, w, y=y)
+                ts = []
+                for _ in range(reps):
+                    flush_l2(flush)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    w4.w4a16_dense_linear(x, w, y=y)
+                    b.record()
+                    ts.append((a, b))
+                torch.cuda.synchronize()
+                t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+                by = 2 * N * K + 2 * M * K + 2 * M * N
+                out[f"{'bf16' if dt == torch.bfloat16 else 'f16'}_M{M}_K{K}_N{N}"] = {
+                    "us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak}
+            del w
+        del w16
+    return out
+
+
 _LAYER0 = None
 
 
@@ -573,6 +608,7 @@ def main():
                            "us_without_epilogue": t0 * 1e6}
         extra["epilogue_l2_flushed"] = epis
         extra["repack_transpose"] = time_repack(w4, dev, flush, peak)
+        extra["dense_linear_l2_flushed"] = time_dense(w4, dev, flush, peak)
         del flush
 
     cpu = None

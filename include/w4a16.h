@@ -279,6 +279,18 @@ int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight, const uint1
                          const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
                          void *stream);
 
+/* Dense 16-bit linear y [M, N] = x [M, K] @ w [N, K]^T for weights already
+ * dequantised to fp16 or bf16 (the Z100 thread, section 六: FP8 weights
+ * dequantised at load time to FP16/BF16 run through a large-K, small-M GEMV
+ * with fp32 products and sums).  x, w and y share the 16-bit type `dtype`
+ * (w4a16_dtype); accumulation is fp32, y rounded once (nearest even).
+ * Streams w once per tile of up to 8 tokens on the warp MMA (split K through
+ * the w4a16_init workspace when the plan splits; W4A16_ERR_WORKSPACE if it is
+ * too small).  K a multiple of 128 (128..2^22), 1 <= N < 2^31, 1 <= M <=
+ * 65535; x, w, y 16-byte aligned; y apart from x and w.  Needs w4a16_init. */
+int w4a16_dense_linear(const uint16_t *x, const uint16_t *w, int M, int N, int K, int dtype,
+                       uint16_t *y, void *stream);
+
 /* The rung the dispatch table picks for a shape (honouring a forced rung), or
  * -1 for an invalid shape.  Pure host query. */
 int w4a16_select_rung(int M, int N, int K, int group);

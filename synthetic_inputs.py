@@ -22,7 +22,9 @@ weights with per-group fp16 scale and 4-bit zero, fp16 activations):
   * scales:  fp16 of U[0.002, 0.02];
   * x:       fp16 of N(0, 1) (Box-Muller, computed on the host only);
   * residual (the epilogue's second input): fp16 of N(0, 4^2), a spread like
-    that of the linear's outputs, so that a dropped residual shows.
+    that of the linear's outputs, so that a dropped residual shows;
+  * dense 16-bit weights: fp16 of N(0, 0.05^2), the spread of the dequantised
+    4-bit weights above.
 """
 from __future__ import annotations
 
@@ -41,6 +43,7 @@ T_ZEROS = 2
 T_SCALES = 3
 T_X = 4
 T_RESIDUAL = 5
+T_DENSE_W = 6
 
 
 def _signed(c: int) -> int:
@@ -147,6 +150,12 @@ def _normal_f16(seed: int, tensor_id: int, M: int, K: int, std: float) -> torch.
 def x(seed: int, M: int, K: int) -> torch.Tensor:
     """[M, K] float16 CPU tensor of N(0, 1) draws (Box-Muller on the host)."""
     return _normal_f16(seed, T_X, M, K, 1.0)
+
+
+def dense_weight(seed: int, N: int, K: int, std: float = 0.05) -> torch.Tensor:
+    """[N, K] float16 CPU tensor of N(0, std^2) draws: 16-bit weights of the
+    dense linear (the spread of dequantised 4-bit weights here)."""
+    return _normal_f16(seed, T_DENSE_W, N, K, std)
 
 
 def residual(seed: int, M: int, N: int, std: float = 4.0) -> torch.Tensor:

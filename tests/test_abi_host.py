@@ -108,6 +108,18 @@ def test_linear_ex_validation_codes(w4):
         assert L.w4a16_linear_ex(*args, 1, 1, 6 * A, 5 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
 
 
+def test_dense_linear_validation_codes(w4):
+    L = w4.lib
+    assert L.w4a16_dense_linear(None, 2 * A, 1, 64, 256, 0, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dense_linear(A, 2 * A, 0, 64, 256, 0, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dense_linear(A, 2 * A, 1, 64, 200, 0, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dense_linear(A, 2 * A, 1, 64, 256, 2, 5 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_dense_linear(A + 8, 2 * A, 1, 64, 256, 0, 5 * A, None) == w4.W4A16_ERR_MISALIGNED
+    assert L.w4a16_dense_linear(A, 2 * A, 1, 64, 256, 0, 2 * A + 64, None) == w4.W4A16_ERR_INVALID_ARG
+    if w4.lib.w4a16_device_sm_count() == 0:
+        assert L.w4a16_dense_linear(A, 2 * A, 1, 64, 256, 1, 5 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
+
+
 def test_repack_validation_codes(w4):
     L, seq = w4.lib, 0x76543210
     assert L.w4a16_repack_transpose(None, 8, 8, seq, A, None) == w4.W4A16_ERR_INVALID_ARG

@@ -82,6 +82,7 @@ _sig("w4a16_linear", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_epilogue", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_linear_ex", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P])
+_sig("w4a16_dense_linear", [_P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -100,7 +101,7 @@ _sig("w4a16_device_sm_count", [])
 EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack",
             "w4a16_unpack", "w4a16_dequant", "w4a16_repack_transpose", "w4a16_transpose_f16",
             "w4a16_linear", "w4a16_linear_noalloc",
-            "w4a16_linear_epilogue", "w4a16_linear_ex",
+            "w4a16_linear_epilogue", "w4a16_linear_ex", "w4a16_dense_linear",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -294,6 +295,22 @@ def w4a16_linear_ex(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor
                                M, N, K, group, _DTYPE_OF[dt], epilogue, r, _dev(y, dt, "y"),
                                _stream_ptr(stream)),
            "w4a16_linear_ex")
+    return y
+
+
+def w4a16_dense_linear(x: torch.Tensor, w: torch.Tensor, y=None, stream=None) -> torch.Tensor:
+    """y [M, N] = x [M, K] @ w [N, K]^T for fp16 or bf16 weights (x, w and y of
+    one dtype), fp32 accumulation."""
+    M, K = x.shape
+    N = w.shape[0]
+    if x.dtype not in _DTYPE_OF:
+        raise TypeError(f"x must be float16 or bfloat16, got {x.dtype}")
+    dt = x.dtype
+    if y is None:
+        y = torch.empty((M, N), dtype=dt, device=x.device)
+    _check(lib.w4a16_dense_linear(_dev(x, dt, "x"), _dev(w, dt, "w"), M, N, K, _DTYPE_OF[dt],
+                                  _dev(y, dt, "y"), _stream_ptr(stream)),
+           "w4a16_dense_linear")
     return y
 
 

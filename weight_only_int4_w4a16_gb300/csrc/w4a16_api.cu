@@ -432,6 +432,7 @@ int w4a16_init(int device, size_t workspace_bytes) {
     if (e == cudaSuccess) e = gemv_init_attributes(dev);
     if (e == cudaSuccess) e = tc_init(dev);
     if (e == cudaSuccess) e = mma_init(dev);
+    if (e == cudaSuccess) e = dense_init(dev);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(base);
@@ -539,6 +540,42 @@ int w4a16_transpose_f16(const uint16_t *src, int rows, int cols, uint16_t *dst, 
         return W4A16_ERR_INVALID_ARG;
     cudaError_t e = launch_transpose_u16(src, rows, cols, dst, (cudaStream_t)stream);
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_dense_linear(const uint16_t *x, const uint16_t *w, int M, int N, int K, int dtype,
+                       uint16_t *y, void *stream) {
+    if (!x || !w || !y || M < 1 || M > kMaxM || N < 1 || K < kGroup || K > kMaxK ||
+        K % kGroup != 0)
+        return W4A16_ERR_INVALID_ARG;
+    if (dtype != W4A16_DTYPE_F16 && dtype != W4A16_DTYPE_BF16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
+    const size_t ybytes = (size_t)M * N * 2;
+    if (overlaps(x, (size_t)M * K * 2, y, ybytes) || overlaps(w, (size_t)N * K * 2, y, ybytes))
+        return W4A16_ERR_INVALID_ARG;
+    const State &st = g_state;
+    if (!st.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    // tiles of up to 8 tokens, each streaming the weights once
+    for (int m0 = 0; m0 < M; m0 += kMmaMaxTokens) {
+        const int Mt = M - m0 < kMmaMaxTokens ? M - m0 : kMmaMaxTokens;
+        DensePlan p = plan_dense(Mt, N, K, st.dev);
+        if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+        if (p.ws_bytes > st.ws.partial_bytes ||
+            (p.S > 1 && p.n_blocks > st.ws.n_counters - kMmaSchedWords))
+            return W4A16_ERR_WORKSPACE;
+    }
+    cudaError_t e = cudaSuccess;
+    for (int m0 = 0; m0 < M && e == cudaSuccess; m0 += kMmaMaxTokens) {
+        const int Mt = M - m0 < kMmaMaxTokens ? M - m0 : kMmaMaxTokens;
+        DensePlan p = plan_dense(Mt, N, K, st.dev);
+        e = launch_dense(reinterpret_cast<const __half *>(x) + (size_t)m0 * K,
+                         reinterpret_cast<const __half *>(w),
+                         reinterpret_cast<__half *>(y) + (size_t)m0 * N, Mt, N, K,
+                         dtype == W4A16_DTYPE_BF16, p, st.ws, (cudaStream_t)stream);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (st.log)
+        fprintf(stderr, "[w4a16] dense linear M=%d N=%d K=%d dtype=%d\n", M, N, K, dtype);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

@@ -177,6 +177,27 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
                              cudaStream_t stream);
 cudaError_t mma_init(const DeviceInfo &dev);
 
+// ---- dense 16-bit linear (w4a16_dense.cu) ---------------------------------
+struct DensePlan {
+    bool ok;
+    int M;               // tokens (1..8)
+    int S;               // K slices
+    int slice_stages;    // 128-k stages per slice
+    int n_strips;        // 16-row strips
+    int strips_per_warp;
+    int n_blocks;        // blocks of 8 * strips_per_warp strips
+    int units;           // S * n_blocks
+    int grid;
+    int smem_bytes;
+    size_t ws_bytes;     // split-K partial bytes (0 when S == 1)
+};
+DensePlan plan_dense(int M, int N, int K, const DeviceInfo &dev);
+// y [M, N] = x [M, K] @ w [N, K]^T, 16-bit data (bf16: bfloat16 in __half storage)
+cudaError_t launch_dense(const __half *x, const __half *w, __half *y, int M, int N, int K,
+                         bool bf16, const DensePlan &plan, const Workspace &ws,
+                         cudaStream_t stream);
+cudaError_t dense_init(const DeviceInfo &dev);
+
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,
                         uint32_t *zeros, cudaStream_t stream);
