@@ -63,6 +63,9 @@ def _bind(lib):
     lib.w4o_transpose_u16.argtypes = [P, L, L, P]
     lib.w4o_dense_linear.argtypes = [P, P, I, I, I, I, P]
     lib.w4o_dense_linear_rows.argtypes = [P, P, I, I, I, I, P, I, P]
+    lib.w4o_moe_align.argtypes = [P, I, I, P, P, P]
+    lib.w4o_moe_linear.argtypes = [P, I, P, P, P, P, I, I, I, I, I, I, I, P]
+    lib.w4o_moe_sum.argtypes = [P, P, I, I, I, P]
     lib.w4o_round_to_half.argtypes = [P, L, P]
     lib.w4o_half_array_to_double.argtypes = [P, L, P]
     lib.w4o_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -79,7 +82,8 @@ def _bind(lib):
               lib.w4o_bf16_array_to_double, lib.w4o_linear_dt, lib.w4o_linear_rows_dt,
               lib.w4o_silu_mul, lib.w4o_add_residual_dt,
               lib.w4o_transpose_u4, lib.w4o_transpose_u16, lib.w4o_dense_linear,
-              lib.w4o_dense_linear_rows):
+              lib.w4o_dense_linear_rows, lib.w4o_moe_align, lib.w4o_moe_linear,
+              lib.w4o_moe_sum):
         f.restype = None
     return lib
 
@@ -294,3 +298,49 @@ def dense_linear(x: np.ndarray, w: np.ndarray, dtype: str = "f16", rows=None) ->
     _load().w4o_dense_linear_rows(_ptr(x), _ptr(w), M, N, K, _DTYPES[dtype], _ptr(rows),
                                   int(rows.size), _ptr(y))
     return y
+
+
+def moe_align(ids: np.ndarray, E: int):
+    """Slots grouped by expert (stable): (sorted [S], pos [S], offsets [E+1]) int32."""
+    ids = _c(np.asarray(ids, dtype=np.int32).reshape(-1), np.int32)
+    assert ids.size == 0 or (ids.min() >= 0 and ids.max() < E)
+    S = ids.size
+    srt = np.empty(S, dtype=np.int32)
+    pos = np.empty(S, dtype=np.int32)
+    off = np.empty(E + 1, dtype=np.int32)
+    _load().w4o_moe_align(_ptr(ids), S, E, _ptr(srt), _ptr(pos), _ptr(off))
+    return srt, pos, off
+
+
+def moe_linear(x: np.ndarray, qweight: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+               ids: np.ndarray, per_slot: bool = False, group: int = 128,
+               dtype: str = "f16") -> np.ndarray:
+    """Expert linears per slot: y [T*k, N] (binary64).  qweight [E, N, K/8],
+    scales [E, N, G], zeros [E, N, ceil(G/8)]; ids [T, k]; x [T, K] by token,
+    or [T*k, K] by slot when per_slot."""
+    ids = _c(np.asarray(ids, dtype=np.int32), np.int32)
+    T, k = ids.shape
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    zeros = _c(zeros, np.uint32)
+    E, N, KW = qweight.shape
+    K = KW * 8
+    x = _c(x, np.uint16)
+    assert x.shape == ((T * k if per_slot else T), K)
+    assert ids.size == 0 or (ids.min() >= 0 and ids.max() < E)
+    y = np.empty((T * k, N), dtype=np.float64)
+    _load().w4o_moe_linear(_ptr(x), int(per_slot), _ptr(qweight), _ptr(scales), _ptr(zeros),
+                           _ptr(ids), T, k, E, N, K, group, _DTYPES[dtype], _ptr(y))
+    return y
+
+
+def moe_sum(y: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """out [T, N] = sum_j weights[t, j] * y[t*k + j] in binary64."""
+    w = _c(np.asarray(weights, dtype=np.float64), np.float64)
+    T, k = w.shape
+    y = _c(y, np.float64)
+    N = y.shape[1]
+    assert y.shape == (T * k, N)
+    out = np.empty((T, N), dtype=np.float64)
+    _load().w4o_moe_sum(_ptr(y), _ptr(w), T, k, N, _ptr(out))
+    return out

@@ -44,7 +44,9 @@
  *   binary32 decoder over every pattern, neighbours and ties; the bf16 linear
  *   against exact rationals and an int64 matrix product; the dense 16-bit
  *   linear against exact rationals, an int64 product and, bit for bit, the
- *   4-bit linear over its own exactly representable dequantised weights.
+ *   4-bit linear over its own exactly representable dequantised weights; the
+ *   MoE alignment against a stable sort, the expert linears against the
+ *   pinned linear of each slot's expert, the weighted sum exact.
  */
 #include <math.h>
 #include <pthread.h>
@@ -442,5 +444,68 @@ void w4o_dense_linear_rows(const uint16_t *x, const uint16_t *w, int M, int N, i
             double acc = 0.0;
             for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);
             y[m * nrows + i] = acc;
+        }
+}
+
+/* ---- mixture of experts (Z100 thread, section 七: tokens rearranged by
+ * expert, the W4A16 expert small-M GEMV over packed INT4 experts, and the
+ * weighted sum of each token's expert outputs).  TEST INFRASTRUCTURE ONLY.
+ *
+ * Slots: token t's j-th choice is slot s = t*k + j, routed to expert
+ * ids[s] (0 <= ids[s] < E).
+ *
+ * Alignment: the slots grouped by expert, in increasing slot order within
+ * an expert (a stable counting sort).  offsets[e] is the first sorted
+ * position of expert e (offsets[E] = T*k), sorted[p] the slot at position
+ * p, pos[s] the position of slot s. */
+void w4o_moe_align(const int32_t *ids, int n_slots, int E, int32_t *sorted, int32_t *pos,
+                   int32_t *offsets)
+{
+    for (int e = 0; e <= E; ++e) offsets[e] = 0;
+    for (int s = 0; s < n_slots; ++s) offsets[ids[s] + 1]++;
+    for (int e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E > 0 ? E : 1));
+    for (int e = 0; e < E; ++e) fill[e] = offsets[e];
+    for (int s = 0; s < n_slots; ++s) {
+        const int p = fill[ids[s]]++;
+        sorted[p] = s;
+        pos[s] = p;
+    }
+    free(fill);
+}
+
+/* Expert linears: y[s, n] = sum_k xs[m(s), k] * w_e[n, k], e = ids[s], with
+ * the experts' packed layers stacked ([E, N, K/8] words, [E, N, G] scales,
+ * [E, N, ceil(G/8)] zeros words).  The input row m(s) is the slot's token
+ * t = s / k when per_slot is 0 (the first linear of an expert MLP), the slot
+ * itself when per_slot is 1 (a later linear, fed by the slot's own
+ * activations).  y is [T*k, N] in slot order, binary64. */
+void w4o_moe_linear(const uint16_t *x, int per_slot, const uint32_t *qweight,
+                    const uint16_t *scales, const uint32_t *zeros, const int32_t *ids, int T,
+                    int k, int E, int N, int K, int group, int dtype, double *y)
+{
+    const int G = K / group;
+    const long KW = K / 8, ZW = zero_words_per_row(G);
+    decode16_fn dec = decoder_for(dtype);
+    (void)E;
+    for (long s = 0; s < (long)T * k; ++s) {
+        const long e = ids[s], m = per_slot ? s : s / k;
+        for (long n = 0; n < N; ++n) {
+            const long row = e * N + n;
+            y[s * N + n] = linear_one(x + m * K, qweight + row * KW, scales + row * G,
+                                      zeros + row * ZW, K, group, dec);
+        }
+    }
+}
+
+/* Weighted sum per token: out[t, n] = sum_j wts[t*k + j] * y[t*k + j, n],
+ * in binary64, j increasing. */
+void w4o_moe_sum(const double *y, const double *wts, int T, int k, int N, double *out)
+{
+    for (long t = 0; t < T; ++t)
+        for (long n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (long j = 0; j < k; ++j) acc += wts[t * k + j] * y[(t * k + j) * N + n];
+            out[t * N + n] = acc;
         }
 }

@@ -53,6 +53,13 @@ MUTANTS = {
                                 "for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[(k % N) * K + n % K]);\n            y[m * N + n] = acc;"),
     "dense_last_term_dropped": ("for (long k = 0; k < K; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);\n            y[m * N + n] = acc;",
                                 "for (long k = 0; k < K - 1; ++k) acc += dec(x[m * K + k]) * dec(w[n * K + k]);\n            y[m * N + n] = acc;"),
+    "moe_align_unstable": ("    for (int s = 0; s < n_slots; ++s) {\n        const int p = fill[ids[s]]++;",
+                           "    for (int s = n_slots - 1; s >= 0; --s) {\n        const int p = fill[ids[s]]++;"),
+    "moe_token_of_slot": ("const long e = ids[s], m = per_slot ? s : s / k;",
+                          "const long e = ids[s], m = per_slot ? s : s % T;"),
+    "moe_expert_offset": ("const long row = e * N + n;", "const long row = n;"),
+    "moe_sum_weight_index": ("acc += wts[t * k + j] * y[(t * k + j) * N + n];",
+                             "acc += wts[t * k] * y[(t * k + j) * N + n];"),
     "pack_zero_pad_dirty": ("if (g < G) word |= (uint32_t)(z[n * G + g] & 0xfu) << (4 * j);",
                             "word |= (uint32_t)(z[n * G + (g < G ? g : G - 1)] & 0xfu) << (4 * j);"),
 }
@@ -93,6 +100,9 @@ def _pin_calls():
         lambda: pins.test_dense_linear_matches_exact_rationals("bf16"),
         pins.test_dense_linear_equals_the_4bit_linear_on_its_dequantised_weights,
         pins.test_dense_linear_integer_case_equals_int64_matmul,
+        pins.test_moe_align_is_a_stable_sort_by_expert,
+        pins.test_moe_linear_is_the_pinned_linear_of_each_slots_expert,
+        pins.test_moe_sum_selects_and_is_exact,
     ]
 
 

@@ -597,3 +597,60 @@ def test_dense_linear_integer_case_equals_int64_matmul():
     W = RNG.integers(-50, 51, (N, K)).astype(np.int64)
     y = oracle.dense_linear(_f16_bits(X), _f16_bits(W))
     assert np.array_equal(y, (X @ W.T).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------
+# mixture of experts (Z100 thread, section 七): alignment by expert, the expert
+# linears, the weighted sum per token
+# ----------------------------------------------------------------------------
+def test_moe_align_is_a_stable_sort_by_expert():
+    E = 7
+    ids = RNG.integers(0, E, size=(9, 4)).astype(np.int32)
+    srt, pos, off = oracle.moe_align(ids, E)
+    flat = ids.reshape(-1)
+    assert np.array_equal(srt, np.argsort(flat, kind="stable"))
+    assert np.array_equal(pos[srt], np.arange(flat.size))
+    assert np.array_equal(off, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+    # an expert nobody chose has an empty range
+    srt1, _, off1 = oracle.moe_align(np.zeros((3, 2), dtype=np.int32), 3)
+    assert off1.tolist() == [0, 6, 6, 6] and srt1.tolist() == list(range(6))
+
+
+def _experts(E, N, K):
+    q = RNG.integers(0, 16, (E, N, K)).astype(np.uint8)
+    z = RNG.integers(0, 16, (E, N, K // 128)).astype(np.uint8)
+    s = _f16_bits(RNG.uniform(0.002, 0.02, (E, N, K // 128)))
+    packed = [oracle.pack(q[e], z[e]) for e in range(E)]
+    return np.stack([p[0] for p in packed]), s, np.stack([p[1] for p in packed])
+
+
+def test_moe_linear_is_the_pinned_linear_of_each_slots_expert():
+    E, N, K, T, k = 4, 6, 256, 5, 3
+    qw, s, zw = _experts(E, N, K)
+    ids = RNG.integers(0, E, size=(T, k)).astype(np.int32)
+    x = _f16_bits(RNG.standard_normal((T, K)))
+    y = oracle.moe_linear(x, qw, s, zw, ids)
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            assert np.array_equal(y[t * k + j], oracle.linear(x[t:t + 1], qw[e], s[e], zw[e])[0])
+    # per-slot inputs: slot s reads row s
+    xs = _f16_bits(RNG.standard_normal((T * k, K)))
+    ys = oracle.moe_linear(xs, qw, s, zw, ids, per_slot=True)
+    for slot in (0, 7, T * k - 1):
+        e = ids.reshape(-1)[slot]
+        assert np.array_equal(ys[slot], oracle.linear(xs[slot:slot + 1], qw[e], s[e], zw[e])[0])
+
+
+def test_moe_sum_selects_and_is_exact():
+    T, k, N = 3, 4, 5
+    y = RNG.integers(-2 ** 10, 2 ** 10, size=(T * k, N)) / 64.0
+    onehot = np.zeros((T, k))
+    onehot[np.arange(T), [1, 3, 0]] = 1.0
+    assert np.array_equal(oracle.moe_sum(y, onehot), y[[1, 7, 8]])
+    w = RNG.integers(0, 64, size=(T, k)) / 64.0  # dyadic: the binary64 sum is exact
+    out = oracle.moe_sum(y, w)
+    for t in range(T):
+        for n in range(N):
+            exact = sum(Fraction(float(w[t, j])) * Fraction(float(y[t * k + j, n])) for j in range(k))
+            assert Fraction(float(out[t, n])) == exact
