@@ -341,6 +341,56 @@ def time_dense(w4, dev, flush, peak, reps=20):
     return out
 
 
+def time_moe(w4, dev, peak, reps=20):
+    """A decode-time expert MLP of a Qwen3-MoE-like shape (E 128, top 8,
+    hidden 2048, intermediate 768): align, gate+up with SiLU-and-mul, down and
+    the weighted sum, timed as one step (all five launches) with L2 evicted;
+    GB/s counts the weights of the experts in use."""
+    import synthetic_inputs as si
+    E, k, H, I = 128, 8, 2048, 768
+    parts_g = [si.layer(si.config_seed(8, e, 0), 2 * I, H, device=dev) for e in range(E)]
+    parts_d = [si.layer(si.config_seed(8, e, 1), H, I, device=dev) for e in range(E)]
+    g = [torch.stack([p[i] for p in parts_g]) for i in range(3)]
+    d = [torch.stack([p[i] for p in parts_d]) for i in range(3)]
+    del parts_g, parts_d
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)
+    out = {}
+    for T in (1, 4, 8):
+        rng = np.random.default_rng(T)
+        ids = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(T)])
+                               .astype(np.int32)).to(dev)
+        wts = torch.full((T, k), 1.0 / k, dtype=torch.float32, device=dev)
+        x = si.x(si.config_seed(8, 0, 9), T, H).to(dev)
+        gu = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+        dn = w4.MoeExperts(*d, max_slots=T * k)
+
+        def step():
+            srt, pos, off = w4.w4a16_moe_align(ids, E)
+            h = gu.linear(x, srt, off, T * k, gather_k=k)
+            o = dn.linear(h, srt, off, T * k, gather_k=0)
+            return w4.w4a16_moe_sum(o, pos, wts)
+        for _ in range(3):
+            step()
+        ts = []
+        for _ in range(reps):
+            flush_l2(flush)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            step()
+            b.record()
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+        used = len(set(ids.cpu().numpy().reshape(-1).tolist()))
+        by = used * (linear_bytes(0, 2 * I, H) + linear_bytes(0, H, I))
+        out[f"T{T}"] = {"experts_used": used, "us": t * 1e6, "GBps": by / t / 1e9,
+                        "frac_of_peak": by / t / 1e9 / peak}
+        gu.destroy()
+        dn.destroy()
+    return out
+
+
 _LAYER0 = None
 
 
@@ -609,6 +659,7 @@ def main():
         extra["epilogue_l2_flushed"] = epis
         extra["repack_transpose"] = time_repack(w4, dev, flush, peak)
         extra["dense_linear_l2_flushed"] = time_dense(w4, dev, flush, peak)
+        extra["moe_expert_mlp_l2_flushed"] = time_moe(w4, dev, peak)
         del flush
 
     cpu = None

@@ -291,6 +291,50 @@ int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight, const uint1
 int w4a16_dense_linear(const uint16_t *x, const uint16_t *w, int M, int N, int K, int dtype,
                        uint16_t *y, void *stream);
 
+/* ---- mixture of experts (the Z100 thread, section 七: a router picks k of E
+ * experts per token; the tokens are regrouped by expert; a W4A16 small-M GEMV
+ * runs over the packed INT4 experts; each token's expert outputs are summed
+ * with the router's weights).  Token t's j-th choice is slot s = t*k + j.
+ * The router itself (its linear, softmax and top-k) is the caller's.
+ *
+ * w4a16_moe_align: topk_ids [n_slots] int32 (device) -> the slots grouped by
+ * expert, stable in slot order: offsets [E+1] (first sorted position of each
+ * expert; offsets[E] = the slots with a valid id), sorted [n_slots] (slot at
+ * each position), pos [n_slots] (position of each slot).  An id outside
+ * [0, E) gives its slot pos = -1 (left out of every expert and of the sum) and
+ * sets a bit that w4a16_device_status reports.  E <= 1024.  Needs w4a16_init. */
+int w4a16_moe_align(const int32_t *topk_ids, int n_slots, int E, int32_t *sorted, int32_t *pos,
+                    int32_t *offsets, void *stream);
+
+/* An expert layer: E experts stacked, qweight [E, N, K/8], scales [E, N, G],
+ * zeros [E, N, ceil(G/8)], each expert in this library's layout.  `epilogue`
+ * is W4A16_EPILOGUE_NONE or W4A16_EPILOGUE_SILU_MUL (the experts' fused
+ * gate+up); `dtype` the 16-bit type of activations, scales and outputs.
+ * max_slots bounds n_slots of later calls.  Allocates (call after w4a16_init,
+ * outside any capture); the weights must outlive the handle.  One plan serves
+ * every call: it assumes min(max_slots, E) experts in use side by side. */
+int w4a16_moe_create(int E, int N, int K, int group, const uint32_t *qweight,
+                     const uint16_t *scales, const uint32_t *zeros, int epilogue, int dtype,
+                     int max_slots, void **moe);
+int w4a16_moe_destroy(void *moe);
+
+/* y [n_slots, N] (N/2 with SiLU-and-mul), in sorted order (row p = slot
+ * sorted[p]): each slot's expert linear.  x is by token, [n_slots/gather_k, K]
+ * (slot s reads token s / gather_k, gathered on the device), when gather_k > 0;
+ * by sorted position, [n_slots, K] (e.g. the y of an earlier expert linear),
+ * when gather_k == 0.  sorted and offsets come from w4a16_moe_align.  Two
+ * kernels: the tile descriptors (and the gather), then every expert tile of up
+ * to 8 slots in one launch of the warp-MMA kernel.  Calls on one handle must
+ * not overlap on the GPU (it holds the descriptors and gathered rows). */
+int w4a16_moe_linear(void *moe, const uint16_t *x, int gather_k, const int32_t *sorted,
+                     const int32_t *offsets, int n_slots, uint16_t *y, void *stream);
+
+/* out [T, N] = sum_j weights[t*k + j] * y_sorted[pos[t*k + j]], fp32
+ * accumulation in j order, one rounding; weights fp32 [T, k]; y_sorted and
+ * out of type dtype. */
+int w4a16_moe_sum(const uint16_t *y_sorted, const int32_t *pos, const float *weights, int T,
+                  int k, int N, int dtype, uint16_t *out, void *stream);
+
 /* The rung the dispatch table picks for a shape (honouring a forced rung), or
  * -1 for an invalid shape.  Pure host query. */
 int w4a16_select_rung(int M, int N, int K, int group);

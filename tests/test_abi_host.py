@@ -120,6 +120,32 @@ def test_dense_linear_validation_codes(w4):
         assert L.w4a16_dense_linear(A, 2 * A, 1, 64, 256, 1, 5 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
 
 
+def test_moe_validation_codes(w4):
+    L = w4.lib
+    assert L.w4a16_moe_align(None, 8, 4, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_align(A, 8, 0, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_align(A, 8, 2000, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_align(A + 2, 8, 4, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_MISALIGNED
+    h = ctypes.c_void_p()
+    assert L.w4a16_moe_create(0, 64, 256, 128, A, 2 * A, 3 * A, 0, 0, 8,
+                              ctypes.byref(h)) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_create(4, 64, 256, 128, A, 2 * A, 3 * A, 1, 0, 8,
+                              ctypes.byref(h)) == w4.W4A16_ERR_UNSUPPORTED  # residual
+    assert L.w4a16_moe_create(4, 48, 256, 128, A, 2 * A, 3 * A, 2, 0, 8,
+                              ctypes.byref(h)) == w4.W4A16_ERR_UNSUPPORTED  # N/2 % 16
+    assert L.w4a16_moe_create(4, 64, 256, 64, A, 2 * A, 3 * A, 0, 0, 8,
+                              ctypes.byref(h)) == w4.W4A16_ERR_UNSUPPORTED  # group
+    assert L.w4a16_moe_linear(None, A, 1, A, A, 8, A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_destroy(None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 0, 2, 8, 0, 4 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 2, 2, 8, 5, 4 * A, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 2, 2, 8, 0, A + 8, None) == w4.W4A16_ERR_INVALID_ARG
+    if w4.lib.w4a16_device_sm_count() == 0:
+        assert L.w4a16_moe_align(A, 8, 4, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
+        assert L.w4a16_moe_create(4, 64, 256, 128, A, 2 * A, 3 * A, 2, 1, 8,
+                                  ctypes.byref(h)) == w4.W4A16_ERR_NOT_INITIALIZED
+
+
 def test_repack_validation_codes(w4):
     L, seq = w4.lib, 0x76543210
     assert L.w4a16_repack_transpose(None, 8, 8, seq, A, None) == w4.W4A16_ERR_INVALID_ARG

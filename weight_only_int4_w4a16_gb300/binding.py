@@ -83,6 +83,11 @@ _sig("w4a16_linear_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_linear_epilogue", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_linear_ex", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P])
 _sig("w4a16_dense_linear", [_P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_moe_align", [_P, _I, _I, _P, _P, _P, _P])
+_sig("w4a16_moe_create", [_I, _I, _I, _I, _P, _P, _P, _I, _I, _I, ctypes.POINTER(_P)])
+_sig("w4a16_moe_destroy", [_P])
+_sig("w4a16_moe_linear", [_P, _P, _I, _P, _P, _I, _P, _P])
+_sig("w4a16_moe_sum", [_P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -102,6 +107,8 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_unpack", "w4a16_dequant", "w4a16_repack_transpose", "w4a16_transpose_f16",
             "w4a16_linear", "w4a16_linear_noalloc",
             "w4a16_linear_epilogue", "w4a16_linear_ex", "w4a16_dense_linear",
+            "w4a16_moe_align", "w4a16_moe_create", "w4a16_moe_destroy", "w4a16_moe_linear",
+            "w4a16_moe_sum",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -312,6 +319,70 @@ def w4a16_dense_linear(x: torch.Tensor, w: torch.Tensor, y=None, stream=None) ->
                                   _dev(y, dt, "y"), _stream_ptr(stream)),
            "w4a16_dense_linear")
     return y
+
+
+def w4a16_moe_align(topk_ids: torch.Tensor, E: int, stream=None):
+    """topk_ids [T, k] int32 -> (sorted [T*k], pos [T*k], offsets [E+1]) int32."""
+    n = topk_ids.numel()
+    dev = topk_ids.device
+    srt = torch.empty(n, dtype=torch.int32, device=dev)
+    pos = torch.empty(n, dtype=torch.int32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    _check(lib.w4a16_moe_align(_dev(topk_ids, torch.int32, "topk_ids"), n, E, srt.data_ptr(),
+                               pos.data_ptr(), off.data_ptr(), _stream_ptr(stream)),
+           "w4a16_moe_align")
+    return srt, pos, off
+
+
+class MoeExperts:
+    """E stacked W4A16 experts (qweight [E, N, K/8], scales [E, N, G], zeros
+    [E, N, ceil(G/8)]) prepared for w4a16_moe_linear."""
+
+    def __init__(self, qweight, scales, zeros, epilogue: int = EPILOGUE_NONE,
+                 max_slots: int = 64, group: int = GROUP):
+        E, N, KW = qweight.shape
+        self.E, self.N, self.K, self.epilogue = E, N, KW * 8, epilogue
+        self.dtype = scales.dtype
+        self._keep = (qweight, scales, zeros)
+        h = _P()
+        _check(lib.w4a16_moe_create(E, N, self.K, group, _dev(qweight, torch.int32, "qweight"),
+                                    _dev(scales, self.dtype, "scales"),
+                                    _dev(zeros, torch.int32, "zeros"), epilogue,
+                                    _DTYPE_OF[self.dtype], max_slots, ctypes.byref(h)),
+               "w4a16_moe_create")
+        self.handle = h.value
+
+    def linear(self, x, sorted_slots, offsets, n_slots: int, gather_k: int = 0, y=None,
+               stream=None):
+        cols = self.N // 2 if self.epilogue == EPILOGUE_SILU_MUL else self.N
+        if y is None:
+            y = torch.empty((n_slots, cols), dtype=self.dtype, device=x.device)
+        _check(lib.w4a16_moe_linear(self.handle, _dev(x, self.dtype, "x"), gather_k,
+                                    _dev(sorted_slots, torch.int32, "sorted"),
+                                    _dev(offsets, torch.int32, "offsets"), n_slots,
+                                    _dev(y, self.dtype, "y"), _stream_ptr(stream)),
+               "w4a16_moe_linear")
+        return y
+
+    def destroy(self):
+        if self.handle:
+            _check(lib.w4a16_moe_destroy(self.handle), "w4a16_moe_destroy")
+            self.handle = None
+
+
+def w4a16_moe_sum(y_sorted: torch.Tensor, pos: torch.Tensor, weights: torch.Tensor, out=None,
+                  stream=None) -> torch.Tensor:
+    """out [T, N] = sum_j weights[t, j] * y_sorted[pos[t*k + j]] (weights fp32 [T, k])."""
+    T, k = weights.shape
+    N = y_sorted.shape[1]
+    dt = y_sorted.dtype
+    if out is None:
+        out = torch.empty((T, N), dtype=dt, device=y_sorted.device)
+    _check(lib.w4a16_moe_sum(_dev(y_sorted, dt, "y_sorted"), _dev(pos, torch.int32, "pos"),
+                             _dev(weights, torch.float32, "weights"), T, k, N, _DTYPE_OF[dt],
+                             _dev(out, dt, "out"), _stream_ptr(stream)),
+           "w4a16_moe_sum")
+    return out
 
 
 def make_descs(layers) -> ctypes.Array:

@@ -393,6 +393,19 @@ int round_per_linear(const w4a16_linear_desc *descs, int n_descs, int M, void *s
     return W4A16_OK;
 }
 
+// A mixture-of-experts layer: the experts' descriptor templates (tensor maps
+// written once here), room for the tile descriptors a call's prepare kernel
+// writes, and the gathered activations.
+struct MoeHandle {
+    int E, N, K, epi, dtype, max_slots, max_tiles;
+    MmaPlan plan;             // every tile's plan (M = 8 for the shared-memory budget)
+    MmaLinDesc *tmpl = nullptr;   // device [E]
+    MmaLinDesc *tiles = nullptr;  // device [max_tiles]
+    int *counts = nullptr;        // device [2]: tiles, units
+    __half *xs = nullptr;         // device [max_slots, K]
+    void *buffer = nullptr;
+};
+
 struct RoundGraphHandle {
     cudaGraphExec_t exec = nullptr;
     void *buffer = nullptr;  // the fused round's descriptors and completion counters
@@ -576,6 +589,164 @@ int w4a16_dense_linear(const uint16_t *x, const uint16_t *w, int M, int N, int K
     }
     if (st.log)
         fprintf(stderr, "[w4a16] dense linear M=%d N=%d K=%d dtype=%d\n", M, N, K, dtype);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_create(int E, int N, int K, int group, const uint32_t *qweight,
+                     const uint16_t *scales, const uint32_t *zeros, int epilogue, int dtype,
+                     int max_slots, void **moe) {
+    if (!moe) return W4A16_ERR_INVALID_ARG;
+    *moe = nullptr;
+    if (!qweight || !scales || !zeros || E < 1 || E > kMaxMoeExperts || max_slots < 1)
+        return W4A16_ERR_INVALID_ARG;
+    int st = check_shape(N, K, group);
+    if (st) return st;
+    if (dtype != W4A16_DTYPE_F16 && dtype != W4A16_DTYPE_BF16) return W4A16_ERR_INVALID_ARG;
+    if (epilogue != W4A16_EPILOGUE_NONE && epilogue != W4A16_EPILOGUE_SILU_MUL)
+        return epilogue == W4A16_EPILOGUE_RESIDUAL ? W4A16_ERR_UNSUPPORTED : W4A16_ERR_INVALID_ARG;
+    if (epilogue == W4A16_EPILOGUE_SILU_MUL && N % 32 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(zeros, 4))
+        return W4A16_ERR_MISALIGNED;
+    State &s = g_state;
+    if (!s.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    // tiles: one per expert that gets a slot, one more per further 8 slots
+    long long max_tiles = (long long)max_slots < E ? max_slots : E;
+    max_tiles += max_slots / kMmaMaxTokens;
+    if (max_tiles > max_slots) max_tiles = max_slots;
+    if (max_tiles > kMaxMoeTiles) return W4A16_ERR_UNSUPPORTED;
+    MoeHandle *h = new MoeHandle();
+    h->E = E;
+    h->N = N;
+    h->K = K;
+    h->epi = epilogue;
+    h->dtype = dtype;
+    h->max_slots = max_slots;
+    h->max_tiles = (int)max_tiles;
+    // one plan for every tile, weighing the tiles expected side by side (one
+    // per expert in use, up to the slots)
+    const int copies = max_slots < E ? max_slots : E;
+    h->plan = plan_mma(kMmaMaxTokens, N, K, -1, s.dev, epilogue, copies);
+    if (!h->plan.ok) {
+        delete h;
+        return W4A16_ERR_UNSUPPORTED;
+    }
+    const size_t part_floats = h->plan.reduce ? (size_t)h->plan.S * kMmaMaxTokens * N : 0;
+    if (part_floats * max_tiles * sizeof(float) > s.ws.partial_bytes ||
+        (h->plan.reduce &&
+         (long long)h->plan.n_blocks * max_tiles > s.ws.n_counters - kMmaSchedWords)) {
+        delete h;
+        return W4A16_ERR_WORKSPACE;
+    }
+    const int G = K / kGroup, ZW = (G + 7) / 8;
+    std::vector<MmaLinDesc> tmpl(E);
+    for (int e = 0; e < E; ++e) {
+        LinearArgs a{nullptr, qweight + (size_t)e * N * (K / 8),
+                     reinterpret_cast<const __half *>(scales) + (size_t)e * N * G,
+                     zeros + (size_t)e * N * ZW, nullptr, kMmaMaxTokens, N, K, epilogue,
+                     nullptr, dtype};
+        cudaError_t e2 = mma_describe(a, h->plan, nullptr, nullptr, 0, -1, &tmpl[e]);
+        if (e2 != cudaSuccess) {
+            delete h;
+            return cuda_fail(e2);
+        }
+    }
+    const size_t tb = sizeof(MmaLinDesc) * E, lb = sizeof(MmaLinDesc) * max_tiles;
+    const size_t xb = ((size_t)max_slots * K * 2 + 255) & ~(size_t)255;
+    cudaError_t e = cudaMalloc(&h->buffer, tb + lb + 256 + xb);
+    if (e == cudaSuccess) {
+        char *b = (char *)h->buffer;
+        h->tmpl = (MmaLinDesc *)b;
+        h->tiles = (MmaLinDesc *)(b + tb);
+        h->counts = (int *)(b + tb + lb);
+        h->xs = (__half *)(b + tb + lb + 256);
+        e = cudaMemcpy(h->tmpl, tmpl.data(), tb, cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) {
+        if (h->buffer) cudaFree(h->buffer);
+        delete h;
+        return cuda_fail(e);
+    }
+    *moe = h;
+    return W4A16_OK;
+}
+
+int w4a16_moe_destroy(void *moe) {
+    if (!moe) return W4A16_ERR_INVALID_ARG;
+    MoeHandle *h = (MoeHandle *)moe;
+    cudaError_t e = h->buffer ? cudaFree(h->buffer) : cudaSuccess;
+    delete h;
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_align(const int32_t *topk_ids, int n_slots, int E, int32_t *sorted, int32_t *pos,
+                    int32_t *offsets, void *stream) {
+    if (!topk_ids || !sorted || !pos || !offsets || n_slots < 1 || E < 1 || E > kMaxMoeExperts)
+        return W4A16_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(sorted, 4) || !aligned(pos, 4) || !aligned(offsets, 4))
+        return W4A16_ERR_MISALIGNED;
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    cudaError_t e = launch_moe_align(topk_ids, n_slots, E, sorted, pos, offsets, g_state.ws.status,
+                                     (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_linear(void *moe, const uint16_t *x, int gather_k, const int32_t *sorted,
+                     const int32_t *offsets, int n_slots, uint16_t *y, void *stream) {
+    if (!moe || !x || !sorted || !offsets || !y || n_slots < 1 || gather_k < 0)
+        return W4A16_ERR_INVALID_ARG;
+    MoeHandle *h = (MoeHandle *)moe;
+    if (n_slots > h->max_slots || (gather_k > 0 && n_slots % gather_k != 0))
+        return W4A16_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return W4A16_ERR_MISALIGNED;
+    const State &st = g_state;
+    if (!st.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    const int ycols = out_cols(h->N, h->epi);
+    const size_t xrows = gather_k > 0 ? (size_t)(n_slots / gather_k) : (size_t)n_slots;
+    if (overlaps(x, xrows * h->K * 2, y, (size_t)n_slots * ycols * 2)) return W4A16_ERR_INVALID_ARG;
+    MoeTileSpace sp{};
+    sp.y = reinterpret_cast<__half *>(y);
+    if (h->plan.reduce) {
+        sp.partials = st.ws.partials;
+        sp.partial_stride = (size_t)h->plan.S * kMmaMaxTokens * h->N;
+        sp.counters = st.ws.counters;
+        sp.counter_stride = (size_t)h->plan.n_blocks;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e = launch_moe_prepare(h->tmpl, offsets, sorted, h->E, gather_k > 0 ? gather_k : 1,
+                                       h->max_tiles, h->plan.units, sp,
+                                       reinterpret_cast<const __half *>(x), gather_k > 0, h->xs,
+                                       n_slots, h->K, h->tiles, h->counts, cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    MmaRound r{};
+    r.descs = h->tiles;
+    r.n = h->max_tiles;
+    r.total_units = h->max_tiles * h->plan.units;
+    r.smem_bytes = h->plan.smem_bytes;
+    r.done = nullptr;
+    r.bf16 = h->dtype == W4A16_DTYPE_BF16;
+    r.counts = h->counts;
+    e = launch_mma_round(r, st.ws, st.dev, cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_probe[h->plan.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA].fetch_add(
+        1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_sum(const uint16_t *y_sorted, const int32_t *pos, const float *weights, int T,
+                  int k, int N, int dtype, uint16_t *out, void *stream) {
+    if (!y_sorted || !pos || !weights || !out || T < 1 || k < 1 || N < 1)
+        return W4A16_ERR_INVALID_ARG;
+    if (dtype != W4A16_DTYPE_F16 && dtype != W4A16_DTYPE_BF16) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(y_sorted, 2) || !aligned(out, 2) || !aligned(pos, 4) || !aligned(weights, 4))
+        return W4A16_ERR_MISALIGNED;
+    if (overlaps(y_sorted, (size_t)T * k * N * 2, out, (size_t)T * N * 2))
+        return W4A16_ERR_INVALID_ARG;
+    cudaError_t e = launch_moe_sum(reinterpret_cast<const __half *>(y_sorted), pos, weights, T, k,
+                                   N, dtype == W4A16_DTYPE_BF16, reinterpret_cast<__half *>(out),
+                                   (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

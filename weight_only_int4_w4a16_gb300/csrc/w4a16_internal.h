@@ -126,6 +126,10 @@ struct MmaPlan {
 // of one linear, in device memory for a fused round.
 struct MmaLinDesc {
     CUtensorMap tmap;  // qweight as a 3-D tensor: (word in group, row, group)
+    // when set, the tensor map to use instead of tmap: one written by the host
+    // (expert tiles, whose descriptors a kernel writes, point at their
+    // expert's map; a tensor map is never written by a kernel)
+    const CUtensorMap *tmap_ref;
     const __half *x;
     const __half *scales;
     const uint32_t *zeros;
@@ -150,7 +154,11 @@ struct MmaLinDesc {
 // kRoundStripsPerWarp strips per warp (the round's units balance each other),
 // 3 = the same slices with one strip per warp (the round's last linears, so
 // that the CTAs finish together).
-MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi = kEpiNone);
+// copies: the number of such linears that run side by side in one launch
+// (the expert tiles of a mixture of experts); the one-linear cost model
+// weighs their units together
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi = kEpiNone,
+                 int copies = 1);
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
@@ -170,6 +178,10 @@ struct MmaRound {
     int smem_bytes;
     unsigned *done;
     bool bf16;  // every linear of the round has bf16 data
+    // expert groups: the descriptors come from the preceding kernel, which
+    // writes the linear count and total units here (n and total_units are
+    // then upper bounds, for the grid)
+    const int *counts = nullptr;
 };
 int mma_round_grid(const DeviceInfo &dev);
 int mma_smem_bytes(int M, int slice_groups);
@@ -197,6 +209,28 @@ cudaError_t launch_dense(const __half *x, const __half *w, __half *y, int M, int
                          bool bf16, const DensePlan &plan, const Workspace &ws,
                          cudaStream_t stream);
 cudaError_t dense_init(const DeviceInfo &dev);
+
+// ---- mixture of experts (w4a16_moe.cu) -------------------------------------
+constexpr int kMaxMoeExperts = 1024;
+constexpr int kMaxMoeTiles = 2048;  // tiles of up to 8 slots per launch
+// Where the tiles of one expert-group launch put their results: y rows in
+// sorted order, and per tile its own split-K partials and counters.
+struct MoeTileSpace {
+    __half *y;
+    float *partials;        // null when the plan needs none
+    size_t partial_stride;  // floats per tile
+    unsigned *counters;
+    size_t counter_stride;  // counters per tile
+};
+cudaError_t launch_moe_align(const int32_t *ids, int n_slots, int E, int32_t *sorted,
+                             int32_t *pos, int32_t *offsets, int *status, cudaStream_t stream);
+cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
+                               const int32_t *sorted, int E, int k, int max_tiles,
+                               int units_per_tile, const MoeTileSpace &sp, const __half *x,
+                               bool gather, __half *xs, int n_slots, int K, MmaLinDesc *tiles,
+                               int *counts, cudaStream_t stream);
+cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
+                           int N, bool bf16, __half *out, cudaStream_t stream);
 
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,

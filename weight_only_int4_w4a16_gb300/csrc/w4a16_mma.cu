@@ -256,6 +256,11 @@ struct MmaKernelParams {
     int n_lin;
     int total_units;
     int dynamic;  // units after the first two: 0 = every grid-th, 1 = from *sched
+    // descriptors written by the preceding kernel (expert groups): n_lin and
+    // total_units are upper bounds, counts[1] the units that exist (the
+    // unused descriptors start past every unit); such a launch starts after
+    // that kernel has finished
+    const int *counts;
 };
 
 // Bounded wait until *p >= target (acquire); false once kWaitNs has passed.
@@ -380,14 +385,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     auto fill_slot = [&](int seq) {
         UnitInfo &U = slots[seq & (kSlots - 1)];
         const int u = unit_q[seq & 7];
-        if (u >= total) {
+        if (u >= total || (kRound && P.counts && u >= P.counts[1])) {
             U.l = -1;
         } else {
             if (kRound)
                 while (dl + 1 < P.n_lin && u >= P.descs[dl + 1].unit_start) ++dl;
             const MmaLinDesc &D = desc(dl);
             const int ul = u - D.unit_start;
-            U.tmap = reinterpret_cast<uint64_t>(&D.tmap);
+            U.tmap = reinterpret_cast<uint64_t>(D.tmap_ref ? D.tmap_ref : &D.tmap);
             U.x = D.x;
             U.scales = D.scales;
             U.zeros = D.zeros;
@@ -585,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
     {
         const UnitInfo &D0 = slots[0];  // a fixed unit, decoded before the barrier above
-        if (!(kRound && P.done && D0.wait_for >= 0)) {
+        if (D0.l >= 0 && !(kRound && P.done && D0.wait_for >= 0)) {
             const int xg0 = D0.slice * D0.slice_groups;
             if (threadIdx.x == 0) issue_x(D0, xg0, min(D0.G, xg0 + D0.slice_groups) - xg0);
             xpend_l = D0.l;
@@ -1061,7 +1066,7 @@ int mma_smem_bytes(int M, int slice_groups) {
 
 int mma_round_grid(const DeviceInfo &dev) { return kCtasPerSm * dev.sm_count; }
 
-MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi, int copies) {
     MmaPlan pl{};
     pl.M = M;
     const int G = K / kGroup;
@@ -1113,7 +1118,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi)
                 if (sg > max_groups) continue;
                 const int S_eff = (G + sg - 1) / sg;
                 if (split == 1 && S_eff < 2 && G > kStageGroups) continue;
-                const long long units = (long long)nb * S_eff;
+                const long long units = (long long)nb * S_eff * copies;
                 const long long per_cta = (units + grid_max - 1) / grid_max;
                 const double load = (double)(units < grid_max ? units : grid_max) / grid_max;
                 const double stages = (double)spw * work * ((sg + kStageGroups - 1) / kStageGroups);
@@ -1218,16 +1223,20 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
     P.sched = ws.counters + ws.n_counters - kMmaSchedWords;
     P.n_lin = r.n;
     P.total_units = r.total_units;
+    P.counts = r.counts;
     P.dynamic = 1;
     int grid = mma_round_grid(dev);
     if (grid > r.total_units) grid = r.total_units;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config(grid, r.smem_bytes, stream, attr);
+    // descriptors from the preceding kernel: no early start (the kernel reads
+    // them, and the counts, before any dependency wait)
+    if (r.counts) cfg.numAttrs = 0;
     if (r.done) {
         // linears wait for earlier ones: every CTA must be resident at once
-        attr[1].id = cudaLaunchAttributeCooperative;
-        attr[1].val.cooperative = 1;
-        cfg.numAttrs = 2;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+        attr[cfg.numAttrs].val.cooperative = 1;
+        cfg.numAttrs += 1;
     }
     return r.bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<true, true>, P)
                   : cudaLaunchKernelEx(&cfg, mma_kernel<true, false>, P);

@@ -1,0 +1,215 @@
+// Mixture of experts on the W4A16 rungs (forum.sourcefind.cn thread "vLLM on
+// Hygon Z100", section 七: a router picks a few experts per token; the tokens
+// are rearranged by expert, aligned and padded; the W4A16 expert small-M GEMV
+// runs over packed INT4 experts; each token's expert outputs are summed with
+// the router's weights).
+//
+//   * align: a stable counting sort of the T*k slots (token t's j-th choice is
+//     slot t*k + j) by expert: per-expert offsets, the slot at each sorted
+//     position and the sorted position of each slot;
+//   * prepare: one CTA cuts every expert's range of slots into tiles of up to
+//     8 (the MMA's N) and writes one fused-round descriptor per tile (the
+//     expert's tensor map and arrays from a per-expert template, the tile's
+//     rows of the sorted activations and outputs, its own split-K partials
+//     and counters); the other CTAs gather each sorted slot's activation row
+//     from its token when the input is by token;
+//   * the tiles then run as one launch of the fused-round mma kernel, which
+//     reads the descriptors written just before it (the launch does not start
+//     early) and skips descriptor slots past the last tile;
+//   * sum: out[t] = sum_j w[t, j] * y[pos(t*k + j)] in fp32, j increasing,
+//     rounded once.
+#include <string.h>
+
+#include "../../include/w4a16.h"
+#include "w4a16_internal.h"
+
+namespace w4a16 {
+namespace {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kErrMoeIds = 1024;  // device status bit: an expert id outside [0, E)
+constexpr int kAlignChunk = 4096;  // slots staged in shared memory per pass
+
+// One CTA.  Thread e owns expert e: counts, the exclusive prefix, then a scan
+// over the slots in order that places expert e's slots (stable by slot).  A
+// slot whose id is outside [0, E) gets no position (pos = -1, it is left out
+// of every expert and of the sum) and sets a status bit.
+__global__ void __launch_bounds__(kAlignThreads)
+    moe_align_kernel(const int32_t *__restrict__ ids, int n_slots, int E,
+                     int32_t *__restrict__ sorted, int32_t *__restrict__ pos,
+                     int32_t *__restrict__ offsets, int *status) {
+    __shared__ int count[kMaxMoeExperts];
+    __shared__ int32_t chunk[kAlignChunk];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) count[e] = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
+        const int e = ids[s];
+        if (e >= 0 && e < E) {
+            atomicAdd(&count[e], 1);
+        } else {
+            pos[s] = -1;
+            atomicOr(status, kErrMoeIds);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            const int c = count[e];
+            offsets[e] = run;
+            count[e] = run;  // becomes the expert's fill cursor
+            run += c;
+        }
+        offsets[E] = run;
+    }
+    __syncthreads();
+    for (int base = 0; base < n_slots; base += kAlignChunk) {
+        const int n = min(kAlignChunk, n_slots - base);
+        for (int i = threadIdx.x; i < n; i += blockDim.x) chunk[i] = ids[base + i];
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            int p = count[e];
+            for (int i = 0; i < n; ++i)
+                if (chunk[i] == e) {
+                    sorted[p] = base + i;
+                    pos[base + i] = p;
+                    ++p;
+                }
+            count[e] = p;
+        }
+        __syncthreads();
+    }
+}
+
+// Block 0: the tile descriptors.  Blocks 1..: the gathered activation rows.
+__global__ void __launch_bounds__(256)
+    moe_prepare_kernel(const MmaLinDesc *__restrict__ tmpl, const int32_t *__restrict__ offsets,
+                       const int32_t *__restrict__ sorted, int E, int k, int max_tiles,
+                       int units_per_tile_block, MoeTileSpace sp, const __half *__restrict__ x,
+                       int gather, __half *__restrict__ xs, int n_slots, int K,
+                       MmaLinDesc *__restrict__ tiles, int *__restrict__ counts) {
+    if (blockIdx.x > 0) {
+        // sorted position p reads its token's row: x[sorted[p] / k] (positions
+        // up to offsets[E]: slots with an invalid id have none)
+        const int kw = K / 8;  // 16-byte words per row
+        const int n_valid = min(offsets[E], n_slots);
+        for (long long i = (blockIdx.x - 1) * (long long)blockDim.x + threadIdx.x;
+             i < (long long)n_valid * kw; i += (long long)(gridDim.x - 1) * blockDim.x) {
+            const int p = (int)(i / kw), w = (int)(i - (long long)p * kw);
+            const int t = sorted[p] / k;
+            reinterpret_cast<uint4 *>(xs + (size_t)p * K)[w] =
+                reinterpret_cast<const uint4 *>(x + (size_t)t * K)[w];
+        }
+        return;
+    }
+    __shared__ int tile_expert[kMaxMoeTiles];
+    __shared__ int tile_row[kMaxMoeTiles];
+    __shared__ int tile_m[kMaxMoeTiles];
+    __shared__ int tile_unit[kMaxMoeTiles];
+    __shared__ int n_tiles;
+    if (threadIdx.x == 0) {
+        int nt = 0, units = 0;
+        for (int e = 0; e < E; ++e)
+            for (int r = offsets[e]; r < offsets[e + 1] && nt < max_tiles; r += kMmaMaxTokens) {
+                tile_expert[nt] = e;
+                tile_row[nt] = r;
+                tile_m[nt] = min(kMmaMaxTokens, offsets[e + 1] - r);
+                tile_unit[nt] = units;
+                units += units_per_tile_block;
+                ++nt;
+            }
+        n_tiles = nt;
+        counts[0] = nt;
+        counts[1] = units;
+    }
+    __syncthreads();
+    // copy each tile's template, then its own fields; descriptor slots past
+    // the last tile start past every unit
+    const int words = (int)(sizeof(MmaLinDesc) / 4);
+    for (int i = threadIdx.x; i < max_tiles * words; i += blockDim.x) {
+        const int t = i / words, w = i - t * words;
+        const int e = t < n_tiles ? tile_expert[t] : 0;
+        reinterpret_cast<uint32_t *>(tiles + t)[w] = reinterpret_cast<const uint32_t *>(tmpl + e)[w];
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < max_tiles; t += blockDim.x) {
+        MmaLinDesc &d = tiles[t];
+        if (t < n_tiles) {
+            const int r = tile_row[t];
+            d.x = (gather ? xs : x) + (size_t)r * K;
+            d.y = sp.y + (size_t)r * d.ycols;
+            d.M = tile_m[t];
+            d.partials = sp.partials ? sp.partials + (size_t)t * sp.partial_stride : nullptr;
+            d.counters = sp.counters ? sp.counters + (size_t)t * sp.counter_stride : nullptr;
+            d.unit_start = tile_unit[t];
+            d.tmap_ref = &tmpl[tile_expert[t]].tmap;
+        } else {
+            d.M = 1;
+            d.unit_start = 0x7fffffff;
+        }
+        d.wait_for = -1;
+    }
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(256)
+    moe_sum_kernel(const __half *__restrict__ y, const int32_t *__restrict__ pos,
+                   const float *__restrict__ w, int T, int k, int N, __half *__restrict__ out) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * N;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / N), n = (int)(i - (long long)t * N);
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int s = t * k + j;
+            if (pos[s] < 0) continue;  // a slot with an invalid expert id
+            const __half v = y[(size_t)pos[s] * N + n];
+            const float f = kBf16 ? __uint_as_float((uint32_t)__half_as_ushort(v) << 16)
+                                  : __half2float(v);
+            acc = fmaf(w[s], f, acc);
+        }
+        out[i] = kBf16 ? __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(acc)))
+                       : __float2half_rn(acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_moe_align(const int32_t *ids, int n_slots, int E, int32_t *sorted,
+                             int32_t *pos, int32_t *offsets, int *status, cudaStream_t stream) {
+    moe_align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, n_slots, E, sorted, pos, offsets,
+                                                      status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
+                               const int32_t *sorted, int E, int k, int max_tiles,
+                               int units_per_tile, const MoeTileSpace &sp, const __half *x,
+                               bool gather, __half *xs, int n_slots, int K, MmaLinDesc *tiles,
+                               int *counts, cudaStream_t stream) {
+    int blocks = 1;
+    if (gather) {
+        const long long words = (long long)n_slots * (K / 8);
+        long long b = (words + 255) / 256;
+        if (b > 1024) b = 1024;
+        blocks += (int)(b < 1 ? 1 : b);
+    }
+    moe_prepare_kernel<<<blocks, 256, 0, stream>>>(tmpl, offsets, sorted, E, k, max_tiles,
+                                                   units_per_tile, sp, x, gather ? 1 : 0, xs,
+                                                   n_slots, K, tiles, counts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
+                           int N, bool bf16, __half *out, cudaStream_t stream) {
+    long long b = ((long long)T * N + 255) / 256;
+    if (b > 4096) b = 4096;
+    if (b < 1) b = 1;
+    if (bf16) {
+        moe_sum_kernel<true><<<(int)b, 256, 0, stream>>>(y, pos, w, T, k, N, out);
+    } else {
+        moe_sum_kernel<false><<<(int)b, 256, 0, stream>>>(y, pos, w, T, k, N, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace w4a16
