@@ -258,8 +258,8 @@ struct MmaKernelParams {
     int dynamic;  // units after the first two: 0 = every grid-th, 1 = from *sched
     // descriptors written by the preceding kernel (expert groups): n_lin and
     // total_units are upper bounds, counts[1] the units that exist (the
-    // unused descriptors start past every unit); such a launch starts after
-    // that kernel has finished
+    // unused descriptors start past every unit); thread 0 waits for that
+    // kernel before it reads them
     const int *counts;
 };
 
@@ -423,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         st_release_cta(&U.seq, seq);
     };
     if (threadIdx.x == 0) {
+        // descriptors written by the preceding kernel: wait for it before the
+        // first read (the other threads read them after the barrier below)
+        if (kRound && P.counts) grid_dependency_wait();
         // the CTA's first two units are fixed; the rest come every grid-th or
         // from a counter
         vflags[kFlagAbort] = 0;
@@ -1229,9 +1232,6 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
     if (grid > r.total_units) grid = r.total_units;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config(grid, r.smem_bytes, stream, attr);
-    // descriptors from the preceding kernel: no early start (the kernel reads
-    // them, and the counts, before any dependency wait)
-    if (r.counts) cfg.numAttrs = 0;
     if (r.done) {
         // linears wait for earlier ones: every CTA must be resident at once
         attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;

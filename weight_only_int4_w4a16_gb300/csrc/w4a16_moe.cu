@@ -14,8 +14,8 @@
 //     and counters); the other CTAs gather each sorted slot's activation row
 //     from its token when the input is by token;
 //   * the tiles then run as one launch of the fused-round mma kernel, which
-//     reads the descriptors written just before it (the launch does not start
-//     early) and skips descriptor slots past the last tile;
+//     reads the descriptors written just before it (after waiting for that
+//     kernel) and skips descriptor slots past the last tile;
 //   * sum: out[t] = sum_j w[t, j] * y[pos(t*k + j)] in fp32, j increasing,
 //     rounded once.
 #include <string.h>
@@ -27,6 +27,29 @@ namespace w4a16 {
 namespace {
 
 constexpr int kAlignThreads = 1024;
+
+// Each kernel here may start while the previous one in the stream drains
+// (programmatic dependent launch): it lets its own successor start early,
+// then waits for its predecessor before reading anything.
+__device__ __forceinline__ void chain_start() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_chained(void (*kernel)(Params...), int grid, int threads, cudaStream_t stream,
+                           Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 constexpr int kErrMoeIds = 1024;  // device status bit: an expert id outside [0, E)
 constexpr int kAlignChunk = 4096;  // slots staged in shared memory per pass
 
@@ -40,6 +63,7 @@ __global__ void __launch_bounds__(kAlignThreads)
                      int32_t *__restrict__ offsets, int *status) {
     __shared__ int count[kMaxMoeExperts];
     __shared__ int32_t chunk[kAlignChunk];
+    chain_start();
     for (int e = threadIdx.x; e < E; e += blockDim.x) count[e] = 0;
     __syncthreads();
     for (int s = threadIdx.x; s < n_slots; s += blockDim.x) {
@@ -88,6 +112,7 @@ __global__ void __launch_bounds__(256)
                        int units_per_tile_block, MoeTileSpace sp, const __half *__restrict__ x,
                        int gather, __half *__restrict__ xs, int n_slots, int K,
                        MmaLinDesc *__restrict__ tiles, int *__restrict__ counts) {
+    chain_start();
     if (blockIdx.x > 0) {
         // sorted position p reads its token's row: x[sorted[p] / k] (positions
         // up to offsets[E]: slots with an invalid id have none)
@@ -155,6 +180,7 @@ template <bool kBf16>
 __global__ void __launch_bounds__(256)
     moe_sum_kernel(const __half *__restrict__ y, const int32_t *__restrict__ pos,
                    const float *__restrict__ w, int T, int k, int N, __half *__restrict__ out) {
+    chain_start();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)T * N;
          i += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(i / N), n = (int)(i - (long long)t * N);
@@ -176,9 +202,8 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_moe_align(const int32_t *ids, int n_slots, int E, int32_t *sorted,
                              int32_t *pos, int32_t *offsets, int *status, cudaStream_t stream) {
-    moe_align_kernel<<<1, kAlignThreads, 0, stream>>>(ids, n_slots, E, sorted, pos, offsets,
-                                                      status);
-    return cudaGetLastError();
+    return launch_chained(moe_align_kernel, 1, kAlignThreads, stream, ids, n_slots, E, sorted, pos,
+                          offsets, status);
 }
 
 cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
@@ -193,10 +218,9 @@ cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
         if (b > 1024) b = 1024;
         blocks += (int)(b < 1 ? 1 : b);
     }
-    moe_prepare_kernel<<<blocks, 256, 0, stream>>>(tmpl, offsets, sorted, E, k, max_tiles,
-                                                   units_per_tile, sp, x, gather ? 1 : 0, xs,
-                                                   n_slots, K, tiles, counts);
-    return cudaGetLastError();
+    return launch_chained(moe_prepare_kernel, blocks, 256, stream, tmpl, offsets, sorted, E, k,
+                          max_tiles, units_per_tile, sp, x, gather ? 1 : 0, xs, n_slots, K, tiles,
+                          counts);
 }
 
 cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
@@ -204,12 +228,9 @@ cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, 
     long long b = ((long long)T * N + 255) / 256;
     if (b > 4096) b = 4096;
     if (b < 1) b = 1;
-    if (bf16) {
-        moe_sum_kernel<true><<<(int)b, 256, 0, stream>>>(y, pos, w, T, k, N, out);
-    } else {
-        moe_sum_kernel<false><<<(int)b, 256, 0, stream>>>(y, pos, w, T, k, N, out);
-    }
-    return cudaGetLastError();
+    return bf16 ? launch_chained(moe_sum_kernel<true>, (int)b, 256, stream, y, pos, w, T, k, N, out)
+                : launch_chained(moe_sum_kernel<false>, (int)b, 256, stream, y, pos, w, T, k, N,
+                                 out);
 }
 
 }  // namespace w4a16
