@@ -127,7 +127,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the fused 64-layer round kernel, from one ncu capture of the current kernel;
 # None once the kernel changes.
-ROUND_KERNEL_TRAFFIC = 11_624_143_104
+ROUND_KERNEL_TRAFFIC = 11_640_021_504
 
 
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):
@@ -481,6 +481,29 @@ def run_case(M: int, N: int, K: int, rung: int, reps: int):
         raise SystemExit(1)
 
 
+def run_dense_case(M: int, N: int, K: int, reps: int):
+    """One dense 16-bit linear (fp16 weights made on the device from a seeded
+    4-bit layer) launched `reps` times: the target of ncu captures."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import synthetic_inputs as si
+    import weight_only_int4_w4a16_gb300 as w4
+    dev = torch.device("cuda:0")
+    w4.w4a16_init(0, 512 << 20)
+    qw, s, zw = si.layer(si.config_seed(1), N, K, device=dev)
+    _, w = w4.w4a16_dequant(qw, s, zw, K, f32=False)
+    del qw, s, zw
+    x = si.x(si.config_seed(1), M, K).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    for _ in range(reps):
+        w4.w4a16_dense_linear(x, w, y=y)
+    torch.cuda.synchronize()
+    status = w4.w4a16_device_status()
+    print(f"dense case M={M} N={N} K={K} reps={reps} device_status={status}")
+    if status:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,12 +516,17 @@ def main():
     ap.add_argument("--case", type=int, nargs=5, metavar=("M", "N", "K", "RUNG", "REPS"),
                     help="profiling helper: run one seeded linear REPS times on a forced rung "
                          "(-1 = dispatch table) and exit; prints no benchmark line")
+    ap.add_argument("--dense-case", type=int, nargs=4, metavar=("M", "N", "K", "REPS"),
+                    help="profiling helper: run one dense fp16 linear REPS times and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
     if args.case:
         run_case(*args.case)
+        return
+    if args.dense_case:
+        run_dense_case(*args.dense_case)
         return
     if args.impl == "reference":
         run_reference(args)
