@@ -131,16 +131,26 @@ ROUND_KERNEL_TRAFFIC = 11_640_021_504
 
 
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):
+    """The round's linears.  The four inputs are views of one device buffer and
+    the 256 outputs views of another (one copy each way per end-to-end step);
+    each linear's x and y stay separate tensors to the library."""
     import synthetic_inputs as si
     xs = [si.x(si.config_seed(3, 0, 8 + j), M, K) for j, (_, K, _) in enumerate(ROUND_SHAPES)]
-    xs_dev = [x.to(dev) for x in xs]
-    lin = []
+    x_all = torch.cat([x.reshape(-1) for x in xs]).to(dev)
+    xs_dev, off = [], 0
+    for x in xs:
+        xs_dev.append(x_all[off:off + x.numel()].view(x.shape))
+        off += x.numel()
+    y_all = torch.empty(layers * sum(M * N for _, _, N in ROUND_SHAPES), dtype=torch.float16,
+                        device=dev)
+    lin, off = [], 0
     for l in range(layers):
         for j, (name, K, N) in enumerate(ROUND_SHAPES):
             qw, s, zw = si.layer(si.config_seed(3, l, j), N, K, device=dev)
-            y = torch.empty((M, N), dtype=torch.float16, device=dev)
+            y = y_all[off:off + M * N].view(M, N)
+            off += M * N
             lin.append(dict(name=name, x=xs_dev[j], qweight=qw, scales=s, zeros=zw, y=y, N=N, K=K,
-                            j=j))
+                            j=j, x_all=x_all, y_all=y_all))
     return lin, xs, xs_dev
 
 
@@ -180,22 +190,20 @@ def per_kernel_durations(w4, lin, steps, stream):
 
 
 def time_e2e(w4, lin, xs, steps, warmup, stream):
-    """x from pinned host memory in, decode round, every y back to pinned host memory."""
-    dev_x = {}
-    for L in lin:
-        dev_x[L["j"]] = L["x"]
-    pinned_x = [x.pin_memory() for x in xs]
-    pinned_y = [torch.empty(L["y"].shape, dtype=torch.float16).pin_memory() for L in lin]
+    """x from pinned host memory in, decode round, every y back to pinned host
+    memory: one copy each way per step (the inputs and the outputs each sit in
+    one buffer), waited for every step."""
+    x_all, y_all = lin[0]["x_all"], lin[0]["y_all"]
+    pinned_x = torch.cat([x.reshape(-1) for x in xs]).pin_memory()
+    pinned_y = torch.empty(y_all.shape, dtype=torch.float16).pin_memory()
     descs = w4.make_descs(lin)
-    h2d = sum(x.numel() * 2 for x in xs)
-    d2h = sum(L["y"].numel() * 2 for L in lin)
+    h2d = pinned_x.numel() * 2
+    d2h = pinned_y.numel() * 2
 
     def step():
-        for j, x in enumerate(pinned_x):
-            dev_x[j].copy_(x, non_blocking=True)
+        x_all.copy_(pinned_x, non_blocking=True)
         w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
-        for L, hy in zip(lin, pinned_y):
-            hy.copy_(L["y"], non_blocking=True)
+        pinned_y.copy_(y_all, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
