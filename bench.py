@@ -75,10 +75,13 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, log_dir: str | None = None):
+        """Samples go to clocks_rank<index>.csv in log_dir (default: the
+        system's temporary directory)."""
+        import tempfile
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.path = os.path.join(log_dir or tempfile.gettempdir(), f"clocks_rank{index}.csv")
 
     def start(self):
         try:
@@ -524,6 +527,8 @@ def main():
     ap.add_argument("--case", type=int, nargs=5, metavar=("M", "N", "K", "RUNG", "REPS"),
                     help="profiling helper: run one seeded linear REPS times on a forced rung "
                          "(-1 = dispatch table) and exit; prints no benchmark line")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where to keep the nvidia-smi samples of the timed region")
     ap.add_argument("--dense-case", type=int, nargs=4, metavar=("M", "N", "K", "REPS"),
                     help="profiling helper: run one dense fp16 linear REPS times and exit")
     args = ap.parse_args()
@@ -563,7 +568,7 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_dir)
     clocks.start()
     w4.w4a16_probe_reset()
     for _ in range(args.warmup):
