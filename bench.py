@@ -354,9 +354,10 @@ def time_dense(w4, dev, flush, peak, reps=20):
 
 def time_moe(w4, dev, peak, reps=20):
     """A decode-time expert MLP of a Qwen3-MoE-like shape (E 128, top 8,
-    hidden 2048, intermediate 768): align, gate+up with SiLU-and-mul, down and
-    the weighted sum, timed as one step (all five launches) with L2 evicted;
-    GB/s counts the weights of the experts in use."""
+    hidden 2048, intermediate 768) with L2 evicted: w4a16_moe_mlp (align,
+    prepare, one expert-MMA launch for gate+up with SiLU-and-mul and down, the
+    weighted sum), and the same chain call by call; GB/s counts the weights of
+    the experts in use."""
     import synthetic_inputs as si
     E, k, H, I = 128, 8, 2048, 768
     parts_g = [si.layer(si.config_seed(8, e, 0), 2 * I, H, device=dev) for e in range(E)]
@@ -374,29 +375,39 @@ def time_moe(w4, dev, peak, reps=20):
         x = si.x(si.config_seed(8, 0, 9), T, H).to(dev)
         gu = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
         dn = w4.MoeExperts(*d, max_slots=T * k)
+        mlp = w4.MoeMlp(gu, dn, T, k)
+        y = torch.empty((T, H), dtype=torch.float16, device=dev)
 
-        def step():
+        def chain():
             srt, pos, off = w4.w4a16_moe_align(ids, E)
             h = gu.linear(x, srt, off, T * k, gather_k=k)
             o = dn.linear(h, srt, off, T * k, gather_k=0)
             return w4.w4a16_moe_sum(o, pos, wts)
-        for _ in range(3):
-            step()
-        ts = []
-        for _ in range(reps):
-            flush_l2(flush)
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            step()
-            b.record()
-            ts.append((a, b))
-        torch.cuda.synchronize()
-        t = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+
+        def one():
+            return mlp(x, ids, wts, out=y)
+
+        def timed(step):
+            for _ in range(3):
+                step()
+            ts = []
+            for _ in range(reps):
+                flush_l2(flush)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                step()
+                b.record()
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+        t = timed(one)
+        t_chain = timed(chain)
         used = len(set(ids.cpu().numpy().reshape(-1).tolist()))
         by = used * (linear_bytes(0, 2 * I, H) + linear_bytes(0, H, I))
         out[f"T{T}"] = {"experts_used": used, "us": t * 1e6, "GBps": by / t / 1e9,
-                        "frac_of_peak": by / t / 1e9 / peak}
+                        "frac_of_peak": by / t / 1e9 / peak, "us_call_by_call": t_chain * 1e6}
+        mlp.destroy()
         gu.destroy()
         dn.destroy()
     return out

@@ -329,6 +329,26 @@ int w4a16_moe_destroy(void *moe);
 int w4a16_moe_linear(void *moe, const uint16_t *x, int gather_k, const int32_t *sorted,
                      const int32_t *offsets, int n_slots, uint16_t *y, void *stream);
 
+/* An expert MLP: gate+up (usually with SiLU-and-mul) then down over the same
+ * routing, made of two handles from w4a16_moe_create (down's K = gate+up's
+ * output columns, down's N = gate+up's K, same E and dtype, down without an
+ * epilogue).  Holds the chain's buffers for up to max_tokens tokens of k
+ * choices (max_tokens * k must not exceed either handle's max_slots).
+ * Allocates: call after w4a16_init, outside any capture.  Both split-K spaces
+ * must fit the workspace at once (W4A16_ERR_WORKSPACE). */
+int w4a16_moe_mlp_create(void *gate_up, void *down, int max_tokens, int k, void **mlp);
+int w4a16_moe_mlp_destroy(void *mlp);
+
+/* out [T, N_down] = sum_j weights[t, j] * down_e(gate_up_e(x[t])) with e the
+ * token's j-th expert: align, then one kernel preparing both linears' tiles
+ * (and gathering x), then ONE launch of the warp-MMA kernel over the gate+up
+ * tiles and the down tiles (a down tile waits inside the kernel for its
+ * gate+up tile), then the weighted sum.  x [T, K] by token; topk_ids [T, k]
+ * int32; weights [T, k] fp32 (device).  Calls on one handle must not overlap
+ * on the GPU. */
+int w4a16_moe_mlp(void *mlp, const uint16_t *x, const int32_t *topk_ids, const float *weights,
+                  int T, uint16_t *out, void *stream);
+
 /* out [T, N] = sum_j weights[t*k + j] * y_sorted[pos[t*k + j]], fp32
  * accumulation in j order, one rounding; weights fp32 [T, k]; y_sorted and
  * out of type dtype. */

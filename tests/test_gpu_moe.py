@@ -192,3 +192,36 @@ def test_moe_expert_mlp_step_by_step(w4, T):
     assert_close(o, o_ref[order], "expert down")
     o_slots = o.double().cpu().numpy()[slot_pos]
     assert_close(out, oracle.moe_sum(o_slots, w.astype(np.float64)), "weighted sum")
+
+
+@pytest.mark.parametrize("T,E,dt", [(1, 32, torch.float16), (4, 32, torch.float16),
+                                    (8, 128, torch.float16), (4, 16, torch.bfloat16)])
+def test_moe_mlp_one_launch_matches_the_chain(w4, T, E, dt):
+    # w4a16_moe_mlp (both linears in one expert-MMA launch, down tiles waiting
+    # for their gate+up tiles) against the call-by-call chain, which the test
+    # above checks against the oracle step by step; run twice (the completion
+    # counters must be left zeroed), bit-identical
+    k, H, I = 8, 1024, 768
+    ids, w = routing(800 + T + E, T, k, E)
+    g_qw, g_s, g_zw = experts(610, E, 2 * I, H)
+    d_qw, d_s, d_zw = experts(611, E, H, I)
+    if dt == torch.bfloat16:
+        g_s, d_s = g_s.float().to(dt), d_s.float().to(dt)
+    x = si.x(si.config_seed(612, T), T, H).float().to(dt).to(DEV)
+    ids_d, w_d = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
+    gate_up = w4.MoeExperts(g_qw, g_s, g_zw, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+    down = w4.MoeExperts(d_qw, d_s, d_zw, max_slots=T * k)
+    mlp = w4.MoeMlp(gate_up, down, T, k)
+    try:
+        outs = [mlp(x, ids_d, w_d) for _ in range(2)]
+        srt, pos, off = w4.w4a16_moe_align(ids_d, E)
+        h = gate_up.linear(x, srt, off, T * k, gather_k=k)
+        o = down.linear(h, srt, off, T * k, gather_k=0)
+        chain = w4.w4a16_moe_sum(o, pos, w_d)
+        torch.cuda.synchronize()
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert_close(outs[0], chain.double().cpu().numpy(), f"expert MLP T={T} E={E}")

@@ -88,6 +88,9 @@ _sig("w4a16_moe_create", [_I, _I, _I, _I, _P, _P, _P, _I, _I, _I, ctypes.POINTER
 _sig("w4a16_moe_destroy", [_P])
 _sig("w4a16_moe_linear", [_P, _P, _I, _P, _P, _I, _P, _P])
 _sig("w4a16_moe_sum", [_P, _P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_moe_mlp_create", [_P, _P, _I, _I, ctypes.POINTER(_P)])
+_sig("w4a16_moe_mlp_destroy", [_P])
+_sig("w4a16_moe_mlp", [_P, _P, _P, _P, _I, _P, _P])
 _sig("w4a16_decode_round", [ctypes.POINTER(LinearDesc), _I, _I, _P])
 _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_round_graph_launch", [_P, _P])
@@ -108,7 +111,7 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_linear", "w4a16_linear_noalloc",
             "w4a16_linear_epilogue", "w4a16_linear_ex", "w4a16_dense_linear",
             "w4a16_moe_align", "w4a16_moe_create", "w4a16_moe_destroy", "w4a16_moe_linear",
-            "w4a16_moe_sum",
+            "w4a16_moe_sum", "w4a16_moe_mlp_create", "w4a16_moe_mlp_destroy", "w4a16_moe_mlp",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -367,6 +370,32 @@ class MoeExperts:
     def destroy(self):
         if self.handle:
             _check(lib.w4a16_moe_destroy(self.handle), "w4a16_moe_destroy")
+            self.handle = None
+
+
+class MoeMlp:
+    """gate+up then down over one routing (two MoeExperts), one expert-MMA launch."""
+
+    def __init__(self, gate_up: MoeExperts, down: MoeExperts, max_tokens: int, k: int):
+        self.gate_up, self.down, self.k = gate_up, down, k
+        h = _P()
+        _check(lib.w4a16_moe_mlp_create(gate_up.handle, down.handle, max_tokens, k,
+                                        ctypes.byref(h)), "w4a16_moe_mlp_create")
+        self.handle = h.value
+
+    def __call__(self, x, topk_ids, weights, out=None, stream=None):
+        T = x.shape[0]
+        dt = self.gate_up.dtype
+        if out is None:
+            out = torch.empty((T, self.down.N), dtype=dt, device=x.device)
+        _check(lib.w4a16_moe_mlp(self.handle, _dev(x, dt, "x"), _dev(topk_ids, torch.int32, "topk_ids"),
+                                 _dev(weights, torch.float32, "weights"), T, _dev(out, dt, "out"),
+                                 _stream_ptr(stream)), "w4a16_moe_mlp")
+        return out
+
+    def destroy(self):
+        if self.handle:
+            _check(lib.w4a16_moe_mlp_destroy(self.handle), "w4a16_moe_mlp_destroy")
             self.handle = None
 
 

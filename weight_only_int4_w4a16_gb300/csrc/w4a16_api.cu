@@ -406,6 +406,20 @@ struct MoeHandle {
     void *buffer = nullptr;
 };
 
+// An expert MLP: gate+up and down expert layers and the per-call buffers of
+// their chain (alignment, the intermediate and output rows in sorted order,
+// both linears' tile descriptors, their completion counters).
+struct MoeMlpHandle {
+    MoeHandle *gu = nullptr, *dn = nullptr;
+    int max_tokens = 0, k = 0, max_slots = 0, max_tiles = 0;
+    int32_t *sorted = nullptr, *pos = nullptr, *offsets = nullptr;
+    __half *h = nullptr, *o = nullptr;
+    MmaLinDesc *tiles = nullptr;
+    unsigned *done = nullptr;
+    int *counts = nullptr;
+    void *buffer = nullptr;
+};
+
 struct RoundGraphHandle {
     cudaGraphExec_t exec = nullptr;
     void *buffer = nullptr;  // the fused round's descriptors and completion counters
@@ -713,10 +727,11 @@ int w4a16_moe_linear(void *moe, const uint16_t *x, int gather_k, const int32_t *
         sp.counter_stride = (size_t)h->plan.n_blocks;
     }
     cudaStream_t cs = (cudaStream_t)stream;
-    cudaError_t e = launch_moe_prepare(h->tmpl, offsets, sorted, h->E, gather_k > 0 ? gather_k : 1,
-                                       h->max_tiles, h->plan.units, sp,
-                                       reinterpret_cast<const __half *>(x), gather_k > 0, h->xs,
-                                       n_slots, h->K, h->tiles, h->counts, cs);
+    cudaError_t e = launch_moe_prepare(h->tmpl, nullptr, offsets, sorted, h->E,
+                                       gather_k > 0 ? gather_k : 1, h->max_tiles, h->plan.units, 0,
+                                       sp, MoeTileSpace{}, reinterpret_cast<const __half *>(x),
+                                       gather_k > 0, h->xs, n_slots, h->K, h->tiles, h->counts,
+                                       cs);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (e != cudaSuccess) return cuda_fail(e);
     MmaRound r{};
@@ -731,6 +746,139 @@ int w4a16_moe_linear(void *moe, const uint16_t *x, int gather_k, const int32_t *
     g_launches.fetch_add(1, std::memory_order_relaxed);
     g_probe[h->plan.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA].fetch_add(
         1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_mlp_create(void *gate_up, void *down, int max_tokens, int k, void **mlp) {
+    if (!mlp) return W4A16_ERR_INVALID_ARG;
+    *mlp = nullptr;
+    if (!gate_up || !down || max_tokens < 1 || k < 1) return W4A16_ERR_INVALID_ARG;
+    MoeHandle *gu = (MoeHandle *)gate_up, *dn = (MoeHandle *)down;
+    // down reads what gate+up writes, and gives back rows of gate+up's input width
+    if (gu->E != dn->E || gu->dtype != dn->dtype || dn->K != out_cols(gu->N, gu->epi) ||
+        dn->epi != W4A16_EPILOGUE_NONE || dn->N != gu->K)
+        return W4A16_ERR_INVALID_ARG;
+    const long long slots = (long long)max_tokens * k;
+    if (slots > gu->max_slots || slots > dn->max_slots) return W4A16_ERR_INVALID_ARG;
+    const State &st = g_state;
+    if (!st.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    // both linears' split-K spaces side by side in the workspace
+    const size_t part_a = gu->plan.reduce ? (size_t)gu->plan.S * kMmaMaxTokens * gu->N : 0;
+    const size_t part_b = dn->plan.reduce ? (size_t)dn->plan.S * kMmaMaxTokens * dn->N : 0;
+    const int tiles = gu->max_tiles;
+    const long long cnt_a = gu->plan.reduce ? (long long)gu->plan.n_blocks * tiles : 0;
+    const long long cnt_b = dn->plan.reduce ? (long long)dn->plan.n_blocks * tiles : 0;
+    if ((part_a + part_b) * tiles * sizeof(float) > st.ws.partial_bytes ||
+        cnt_a + cnt_b > st.ws.n_counters - kMmaSchedWords)
+        return W4A16_ERR_WORKSPACE;
+    MoeMlpHandle *m = new MoeMlpHandle();
+    m->gu = gu;
+    m->dn = dn;
+    m->max_tokens = max_tokens;
+    m->k = k;
+    m->max_slots = (int)slots;
+    m->max_tiles = tiles;
+    const size_t al = 256;
+    auto up = [&](size_t b) { return (b + al - 1) / al * al; };
+    const size_t b_sorted = up(slots * 4), b_pos = up(slots * 4), b_off = up((gu->E + 1) * 4);
+    const size_t b_h = up(slots * dn->K * 2), b_o = up(slots * dn->N * 2);
+    const size_t b_tiles = up(sizeof(MmaLinDesc) * 2 * tiles), b_done = up(2 * tiles * 4);
+    const size_t total = b_sorted + b_pos + b_off + b_h + b_o + b_tiles + b_done + al;
+    cudaError_t e = cudaMalloc(&m->buffer, total);
+    if (e == cudaSuccess) {
+        char *b = (char *)m->buffer;
+        m->sorted = (int32_t *)b;
+        b += b_sorted;
+        m->pos = (int32_t *)b;
+        b += b_pos;
+        m->offsets = (int32_t *)b;
+        b += b_off;
+        m->h = (__half *)b;
+        b += b_h;
+        m->o = (__half *)b;
+        b += b_o;
+        m->tiles = (MmaLinDesc *)b;
+        b += b_tiles;
+        m->done = (unsigned *)b;
+        b += b_done;
+        m->counts = (int *)b;
+        e = cudaMemset(m->done, 0, b_done);  // the kernel leaves them zeroed again
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (m->buffer) cudaFree(m->buffer);
+        delete m;
+        return cuda_fail(e);
+    }
+    *mlp = m;
+    return W4A16_OK;
+}
+
+int w4a16_moe_mlp_destroy(void *mlp) {
+    if (!mlp) return W4A16_ERR_INVALID_ARG;
+    MoeMlpHandle *m = (MoeMlpHandle *)mlp;
+    cudaError_t e = m->buffer ? cudaFree(m->buffer) : cudaSuccess;
+    delete m;
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
+int w4a16_moe_mlp(void *mlp, const uint16_t *x, const int32_t *topk_ids, const float *weights,
+                  int T, uint16_t *out, void *stream) {
+    if (!mlp || !x || !topk_ids || !weights || !out || T < 1) return W4A16_ERR_INVALID_ARG;
+    MoeMlpHandle *m = (MoeMlpHandle *)mlp;
+    if (T > m->max_tokens) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 2) || !aligned(topk_ids, 4) || !aligned(weights, 4))
+        return W4A16_ERR_MISALIGNED;
+    MoeHandle *gu = m->gu, *dn = m->dn;
+    if (overlaps(x, (size_t)T * gu->K * 2, out, (size_t)T * dn->N * 2)) return W4A16_ERR_INVALID_ARG;
+    const State &st = g_state;
+    if (!st.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    const int n_slots = T * m->k;
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e = launch_moe_align(topk_ids, n_slots, gu->E, m->sorted, m->pos, m->offsets,
+                                     st.ws.status, cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    MoeTileSpace sa{}, sb{};
+    sa.y = m->h;
+    sb.y = m->o;
+    size_t part_off = 0, cnt_off = 0;
+    if (gu->plan.reduce) {
+        sa.partials = st.ws.partials;
+        sa.partial_stride = (size_t)gu->plan.S * kMmaMaxTokens * gu->N;
+        sa.counters = st.ws.counters;
+        sa.counter_stride = (size_t)gu->plan.n_blocks;
+        part_off = sa.partial_stride * m->max_tiles;
+        cnt_off = sa.counter_stride * m->max_tiles;
+    }
+    if (dn->plan.reduce) {
+        sb.partials = st.ws.partials + part_off;
+        sb.partial_stride = (size_t)dn->plan.S * kMmaMaxTokens * dn->N;
+        sb.counters = st.ws.counters + cnt_off;
+        sb.counter_stride = (size_t)dn->plan.n_blocks;
+    }
+    e = launch_moe_prepare(gu->tmpl, dn->tmpl, m->offsets, m->sorted, gu->E, m->k, m->max_tiles,
+                           gu->plan.units, dn->plan.units, sa, sb,
+                           reinterpret_cast<const __half *>(x), true, gu->xs, n_slots, gu->K,
+                           m->tiles, m->counts, cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    // both linears in one launch: tile t of down waits for tile t of gate+up
+    MmaRound r{};
+    r.descs = m->tiles;
+    r.n = 2 * m->max_tiles;
+    r.total_units = m->max_tiles * (gu->plan.units + dn->plan.units);
+    r.smem_bytes = gu->plan.smem_bytes > dn->plan.smem_bytes ? gu->plan.smem_bytes
+                                                             : dn->plan.smem_bytes;
+    r.done = m->done;
+    r.bf16 = gu->dtype == W4A16_DTYPE_BF16;
+    r.counts = m->counts;
+    e = launch_mma_round(r, st.ws, st.dev, cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_moe_sum(m->o, m->pos, weights, T, m->k, dn->N, gu->dtype == W4A16_DTYPE_BF16,
+                       reinterpret_cast<__half *>(out), cs);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

@@ -224,11 +224,14 @@ struct MoeTileSpace {
 };
 cudaError_t launch_moe_align(const int32_t *ids, int n_slots, int E, int32_t *sorted,
                              int32_t *pos, int32_t *offsets, int *status, cudaStream_t stream);
-cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
-                               const int32_t *sorted, int E, int k, int max_tiles,
-                               int units_per_tile, const MoeTileSpace &sp, const __half *x,
-                               bool gather, __half *xs, int n_slots, int K, MmaLinDesc *tiles,
-                               int *counts, cudaStream_t stream);
+// tmpl2: null, or a second linear (the expert MLP's down projection) whose
+// tiles follow the first's, read its outputs and wait for them
+cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const MmaLinDesc *tmpl2,
+                               const int32_t *offsets, const int32_t *sorted, int E, int k,
+                               int max_tiles, int units1, int units2, const MoeTileSpace &sp,
+                               const MoeTileSpace &sp2, const __half *x, bool gather, __half *xs,
+                               int n_slots, int K, MmaLinDesc *tiles, int *counts,
+                               cudaStream_t stream);
 cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
                            int N, bool bf16, __half *out, cudaStream_t stream);
 

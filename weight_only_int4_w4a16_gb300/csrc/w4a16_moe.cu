@@ -106,11 +106,15 @@ __global__ void __launch_bounds__(kAlignThreads)
 }
 
 // Block 0: the tile descriptors.  Blocks 1..: the gathered activation rows.
+// With a second linear (tmpl2: an expert MLP's down projection) block 0 also
+// writes its tiles right after the first linear's: tile t of the second reads
+// the first's output rows of tile t and waits for that tile (wait_for).
 __global__ void __launch_bounds__(256)
-    moe_prepare_kernel(const MmaLinDesc *__restrict__ tmpl, const int32_t *__restrict__ offsets,
-                       const int32_t *__restrict__ sorted, int E, int k, int max_tiles,
-                       int units_per_tile_block, MoeTileSpace sp, const __half *__restrict__ x,
-                       int gather, __half *__restrict__ xs, int n_slots, int K,
+    moe_prepare_kernel(const MmaLinDesc *__restrict__ tmpl, const MmaLinDesc *__restrict__ tmpl2,
+                       const int32_t *__restrict__ offsets, const int32_t *__restrict__ sorted,
+                       int E, int k, int max_tiles, int units1, int units2, MoeTileSpace sp,
+                       MoeTileSpace sp2, const __half *__restrict__ x, int gather,
+                       __half *__restrict__ xs, int n_slots, int K,
                        MmaLinDesc *__restrict__ tiles, int *__restrict__ counts) {
     chain_start();
     if (blockIdx.x > 0) {
@@ -130,49 +134,65 @@ __global__ void __launch_bounds__(256)
     __shared__ int tile_expert[kMaxMoeTiles];
     __shared__ int tile_row[kMaxMoeTiles];
     __shared__ int tile_m[kMaxMoeTiles];
-    __shared__ int tile_unit[kMaxMoeTiles];
     __shared__ int n_tiles;
     if (threadIdx.x == 0) {
-        int nt = 0, units = 0;
+        int nt = 0;
         for (int e = 0; e < E; ++e)
             for (int r = offsets[e]; r < offsets[e + 1] && nt < max_tiles; r += kMmaMaxTokens) {
                 tile_expert[nt] = e;
                 tile_row[nt] = r;
                 tile_m[nt] = min(kMmaMaxTokens, offsets[e + 1] - r);
-                tile_unit[nt] = units;
-                units += units_per_tile_block;
                 ++nt;
             }
         n_tiles = nt;
-        counts[0] = nt;
-        counts[1] = units;
+        counts[0] = tmpl2 ? 2 * nt : nt;
+        counts[1] = nt * (units1 + (tmpl2 ? units2 : 0));
     }
     __syncthreads();
-    // copy each tile's template, then its own fields; descriptor slots past
-    // the last tile start past every unit
+    const int nt = n_tiles;
+    const int slots = (tmpl2 ? 2 : 1) * max_tiles;
+    // which linear (0, 1) and tile a descriptor slot holds (-1: unused)
+    auto role = [&](int i, int &lin, int &t) {
+        lin = i < nt ? 0 : (tmpl2 && i < 2 * nt ? 1 : -1);
+        t = lin == 0 ? i : i - nt;
+    };
+    // copy each slot's template, then its own fields; slots past the last
+    // tile start past every unit
     const int words = (int)(sizeof(MmaLinDesc) / 4);
-    for (int i = threadIdx.x; i < max_tiles * words; i += blockDim.x) {
-        const int t = i / words, w = i - t * words;
-        const int e = t < n_tiles ? tile_expert[t] : 0;
-        reinterpret_cast<uint32_t *>(tiles + t)[w] = reinterpret_cast<const uint32_t *>(tmpl + e)[w];
+    for (int i = threadIdx.x; i < slots * words; i += blockDim.x) {
+        const int d = i / words, w = i - d * words;
+        int lin, t;
+        role(d, lin, t);
+        const MmaLinDesc *src = lin == 1 ? tmpl2 + tile_expert[t] : tmpl + (lin == 0 ? tile_expert[t] : 0);
+        reinterpret_cast<uint32_t *>(tiles + d)[w] = reinterpret_cast<const uint32_t *>(src)[w];
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < max_tiles; t += blockDim.x) {
-        MmaLinDesc &d = tiles[t];
-        if (t < n_tiles) {
-            const int r = tile_row[t];
-            d.x = (gather ? xs : x) + (size_t)r * K;
-            d.y = sp.y + (size_t)r * d.ycols;
-            d.M = tile_m[t];
-            d.partials = sp.partials ? sp.partials + (size_t)t * sp.partial_stride : nullptr;
-            d.counters = sp.counters ? sp.counters + (size_t)t * sp.counter_stride : nullptr;
-            d.unit_start = tile_unit[t];
-            d.tmap_ref = &tmpl[tile_expert[t]].tmap;
-        } else {
+    for (int i = threadIdx.x; i < slots; i += blockDim.x) {
+        MmaLinDesc &d = tiles[i];
+        int lin, t;
+        role(i, lin, t);
+        d.wait_for = -1;
+        if (lin < 0) {
             d.M = 1;
             d.unit_start = 0x7fffffff;
+            continue;
         }
-        d.wait_for = -1;
+        const int r = tile_row[t], e = tile_expert[t];
+        const MoeTileSpace &q = lin == 0 ? sp : sp2;
+        d.M = tile_m[t];
+        d.y = q.y + (size_t)r * d.ycols;
+        d.partials = q.partials ? q.partials + (size_t)t * q.partial_stride : nullptr;
+        d.counters = q.counters ? q.counters + (size_t)t * q.counter_stride : nullptr;
+        if (lin == 0) {
+            d.x = (gather ? xs : x) + (size_t)r * K;
+            d.unit_start = t * units1;
+            d.tmap_ref = &tmpl[e].tmap;
+        } else {
+            d.x = sp.y + (size_t)r * tmpl[e].ycols;  // the first linear's rows of this tile
+            d.unit_start = nt * units1 + t * units2;
+            d.tmap_ref = &tmpl2[e].tmap;
+            d.wait_for = t;
+        }
     }
 }
 
@@ -206,11 +226,12 @@ cudaError_t launch_moe_align(const int32_t *ids, int n_slots, int E, int32_t *so
                           offsets, status);
 }
 
-cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
-                               const int32_t *sorted, int E, int k, int max_tiles,
-                               int units_per_tile, const MoeTileSpace &sp, const __half *x,
-                               bool gather, __half *xs, int n_slots, int K, MmaLinDesc *tiles,
-                               int *counts, cudaStream_t stream) {
+cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const MmaLinDesc *tmpl2,
+                               const int32_t *offsets, const int32_t *sorted, int E, int k,
+                               int max_tiles, int units1, int units2, const MoeTileSpace &sp,
+                               const MoeTileSpace &sp2, const __half *x, bool gather, __half *xs,
+                               int n_slots, int K, MmaLinDesc *tiles, int *counts,
+                               cudaStream_t stream) {
     int blocks = 1;
     if (gather) {
         const long long words = (long long)n_slots * (K / 8);
@@ -218,9 +239,9 @@ cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const int32_t *offsets,
         if (b > 1024) b = 1024;
         blocks += (int)(b < 1 ? 1 : b);
     }
-    return launch_chained(moe_prepare_kernel, blocks, 256, stream, tmpl, offsets, sorted, E, k,
-                          max_tiles, units_per_tile, sp, x, gather ? 1 : 0, xs, n_slots, K, tiles,
-                          counts);
+    return launch_chained(moe_prepare_kernel, blocks, 256, stream, tmpl, tmpl2, offsets, sorted, E,
+                          k, max_tiles, units1, units2, sp, sp2, x, gather ? 1 : 0, xs, n_slots,
+                          K, tiles, counts);
 }
 
 cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
