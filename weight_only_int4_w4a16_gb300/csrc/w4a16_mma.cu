@@ -388,8 +388,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (u >= total || (kRound && P.counts && u >= P.counts[1])) {
             U.l = -1;
         } else {
-            if (kRound)
-                while (dl + 1 < P.n_lin && u >= P.descs[dl + 1].unit_start) ++dl;
+            if (kRound) {
+                // the last linear starting at or before u, four descriptors
+                // per round trip (a CTA's first unit may lie many linears in)
+                for (;;) {
+                    int st[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st[i] = dl + 1 + i < P.n_lin ? P.descs[dl + 1 + i].unit_start : 0x7fffffff;
+                    int adv = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) adv += u >= st[i];
+                    dl += adv;
+                    if (adv < 4) break;
+                }
+            }
             const MmaLinDesc &D = desc(dl);
             const int ul = u - D.unit_start;
             U.tmap = reinterpret_cast<uint64_t>(D.tmap_ref ? D.tmap_ref : &D.tmap);

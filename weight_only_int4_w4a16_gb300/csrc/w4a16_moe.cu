@@ -76,15 +76,26 @@ __global__ void __launch_bounds__(kAlignThreads)
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int e = 0; e < E; ++e) {
-            const int c = count[e];
-            offsets[e] = run;
-            count[e] = run;  // becomes the expert's fill cursor
-            run += c;
+    {
+        // exclusive scan of the counts, one expert per thread (E <= 1024)
+        __shared__ int warp_sum[kAlignThreads / 32];
+        const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+        const int c = e < E ? count[e] : 0;
+        int incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
         }
-        offsets[E] = run;
+        if (lane == 31) warp_sum[wid] = incl;
+        __syncthreads();
+        int before = incl - c;
+        for (int w = 0; w < wid; ++w) before += warp_sum[w];
+        if (e < E) {
+            offsets[e] = before;
+            count[e] = before;  // becomes the expert's fill cursor
+        }
+        if (e == E - 1) offsets[E] = before + c;
     }
     __syncthreads();
     for (int base = 0; base < n_slots; base += kAlignChunk) {
@@ -134,19 +145,49 @@ __global__ void __launch_bounds__(256)
     __shared__ int tile_expert[kMaxMoeTiles];
     __shared__ int tile_row[kMaxMoeTiles];
     __shared__ int tile_m[kMaxMoeTiles];
+    __shared__ int warp_sum[8];
     __shared__ int n_tiles;
-    if (threadIdx.x == 0) {
-        int nt = 0;
-        for (int e = 0; e < E; ++e)
-            for (int r = offsets[e]; r < offsets[e + 1] && nt < max_tiles; r += kMmaMaxTokens) {
-                tile_expert[nt] = e;
-                tile_row[nt] = r;
-                tile_m[nt] = min(kMmaMaxTokens, offsets[e + 1] - r);
-                ++nt;
-            }
+    // the tiles of each expert (ceil(slots / 8)), numbered by an exclusive
+    // scan over the experts: each thread takes up to 4 consecutive experts
+    constexpr int kPer = kMaxMoeExperts / 256;
+    const int e0 = threadIdx.x * kPer;
+    int cnt[kPer], local = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = e0 + i;
+        cnt[i] = e < E ? (offsets[e + 1] - offsets[e] + kMmaMaxTokens - 1) / kMmaMaxTokens : 0;
+        local += cnt[i];
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    int before = incl - local;
+    for (int w = 0; w < wid; ++w) before += warp_sum[w];
+    if (threadIdx.x == blockDim.x - 1) {
+        const int total = before + local;
+        const int nt = total < max_tiles ? total : max_tiles;
         n_tiles = nt;
         counts[0] = tmpl2 ? 2 * nt : nt;
         counts[1] = nt * (units1 + (tmpl2 ? units2 : 0));
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = e0 + i;
+        for (int t = 0; t < cnt[i]; ++t) {
+            const int idx = before + t;
+            if (idx >= max_tiles) break;
+            const int r = offsets[e] + t * kMmaMaxTokens;
+            tile_expert[idx] = e;
+            tile_row[idx] = r;
+            tile_m[idx] = min(kMmaMaxTokens, offsets[e + 1] - r);
+        }
+        before += cnt[i];
     }
     __syncthreads();
     const int nt = n_tiles;
@@ -156,14 +197,15 @@ __global__ void __launch_bounds__(256)
         lin = i < nt ? 0 : (tmpl2 && i < 2 * nt ? 1 : -1);
         t = lin == 0 ? i : i - nt;
     };
-    // copy each slot's template, then its own fields; slots past the last
-    // tile start past every unit
+    // copy each tile's template, then its own fields; slots past the last
+    // tile only start past every unit
     const int words = (int)(sizeof(MmaLinDesc) / 4);
-    for (int i = threadIdx.x; i < slots * words; i += blockDim.x) {
+    const int used = (tmpl2 ? 2 : 1) * nt;
+    for (int i = threadIdx.x; i < used * words; i += blockDim.x) {
         const int d = i / words, w = i - d * words;
         int lin, t;
         role(d, lin, t);
-        const MmaLinDesc *src = lin == 1 ? tmpl2 + tile_expert[t] : tmpl + (lin == 0 ? tile_expert[t] : 0);
+        const MmaLinDesc *src = lin == 1 ? tmpl2 + tile_expert[t] : tmpl + tile_expert[t];
         reinterpret_cast<uint32_t *>(tiles + d)[w] = reinterpret_cast<const uint32_t *>(src)[w];
     }
     __syncthreads();
