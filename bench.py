@@ -354,10 +354,11 @@ def time_dense(w4, dev, flush, peak, reps=20):
 
 def time_moe(w4, dev, peak, reps=20):
     """A decode-time expert MLP of a Qwen3-MoE-like shape (E 128, top 8,
-    hidden 2048, intermediate 768) with L2 evicted: w4a16_moe_mlp (align,
-    prepare, one expert-MMA launch for gate+up with SiLU-and-mul and down, the
-    weighted sum), and the same chain call by call; GB/s counts the weights of
-    the experts in use."""
+    hidden 2048, intermediate 768) with L2 evicted: w4a16_moe_mlp on its
+    decode path (one launch: routing, gate+up with SiLU-and-mul, down, the
+    weighted sum), on its chain path (align, prepare, one expert-MMA launch for
+    both linears, the weighted sum), and the chain call by call; GB/s counts
+    the weights of the experts in use."""
     import synthetic_inputs as si
     E, k, H, I = 128, 8, 2048, 768
     parts_g = [si.layer(si.config_seed(8, e, 0), 2 * I, H, device=dev) for e in range(E)]
@@ -387,6 +388,12 @@ def time_moe(w4, dev, peak, reps=20):
         def one():
             return mlp(x, ids, wts, out=y)
 
+        def one_chain():
+            mlp.set_path(w4.MOE_PATH_CHAIN)
+            r = mlp(x, ids, wts, out=y)
+            mlp.set_path(w4.MOE_PATH_AUTO)
+            return r
+
         def timed(step):
             for _ in range(3):
                 step()
@@ -402,11 +409,14 @@ def time_moe(w4, dev, peak, reps=20):
             torch.cuda.synchronize()
             return float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
         t = timed(one)
+        t_mlp_chain = timed(one_chain)
         t_chain = timed(chain)
         used = len(set(ids.cpu().numpy().reshape(-1).tolist()))
         by = used * (linear_bytes(0, 2 * I, H) + linear_bytes(0, H, I))
-        out[f"T{T}"] = {"experts_used": used, "us": t * 1e6, "GBps": by / t / 1e9,
-                        "frac_of_peak": by / t / 1e9 / peak, "us_call_by_call": t_chain * 1e6}
+        out[f"T{T}"] = {"experts_used": used, "path": "decode" if mlp.path(T) == w4.MOE_PATH_DECODE
+                        else "chain", "us": t * 1e6, "GBps": by / t / 1e9,
+                        "frac_of_peak": by / t / 1e9 / peak, "us_chain_path": t_mlp_chain * 1e6,
+                        "us_call_by_call": t_chain * 1e6}
         mlp.destroy()
         gu.destroy()
         dn.destroy()

@@ -340,14 +340,42 @@ int w4a16_moe_mlp_create(void *gate_up, void *down, int max_tokens, int k, void 
 int w4a16_moe_mlp_destroy(void *mlp);
 
 /* out [T, N_down] = sum_j weights[t, j] * down_e(gate_up_e(x[t])) with e the
- * token's j-th expert: align, then one kernel preparing both linears' tiles
- * (and gathering x), then ONE launch of the warp-MMA kernel over the gate+up
- * tiles and the down tiles (a down tile waits inside the kernel for its
- * gate+up tile), then the weighted sum.  x [T, K] by token; topk_ids [T, k]
- * int32; weights [T, k] fp32 (device).  Calls on one handle must not overlap
- * on the GPU. */
+ * token's j-th expert.  x [T, K] by token; topk_ids [T, k] int32; weights
+ * [T, k] fp32 (device).  Two paths (w4a16_moe_path):
+ *   chain: align, then one kernel preparing both linears' tiles (and
+ *     gathering x), then ONE launch of the warp-MMA kernel over the gate+up
+ *     tiles and the down tiles (a down tile waits inside the kernel for its
+ *     gate+up tile), then the weighted sum;
+ *   decode: ONE launch for the whole MLP (routing in every CTA, gate+up with
+ *     SiLU-and-mul, down, and the weighted sum), for gate+up with
+ *     SiLU-and-mul, K and down's K multiples of 128, down's N a multiple of
+ *     128, T <= 8, T * k <= 128 and activation rows that fit on chip.
+ * The intermediate and each expert's output are rounded to the 16-bit type
+ * on both paths, and the sum runs over j in order in fp32.  Calls on one
+ * handle must not overlap on the GPU. */
 int w4a16_moe_mlp(void *mlp, const uint16_t *x, const int32_t *topk_ids, const float *weights,
                   int T, uint16_t *out, void *stream);
+
+typedef enum {
+    W4A16_MOE_PATH_AUTO = 0,   /* decode when the call fits it, else chain */
+    W4A16_MOE_PATH_CHAIN = 1,
+    W4A16_MOE_PATH_DECODE = 2  /* calls that do not fit return W4A16_ERR_UNSUPPORTED */
+} w4a16_moe_path;
+
+/* Choose the path of later w4a16_moe_mlp calls on this handle (host state;
+ * a graph captured earlier keeps its launches). */
+int w4a16_moe_mlp_set_path(void *mlp, int path);
+
+/* The path (W4A16_MOE_PATH_CHAIN or _DECODE) a call with T tokens takes, in
+ * *path; W4A16_ERR_UNSUPPORTED when the forced decode path cannot take T. */
+int w4a16_moe_mlp_path(void *mlp, int T, int *path);
+
+/* Device pointers to the handle's intermediate rows h [max_tokens * k, K_down]
+ * and expert outputs o [max_tokens * k, N_down] (16-bit), which every
+ * w4a16_moe_mlp call on either path writes in sorted order (the expert-major,
+ * slot-stable order of w4a16_moe_align; row p belongs to the slot at sorted
+ * position p).  Valid until w4a16_moe_mlp_destroy; for inspection and tests. */
+int w4a16_moe_mlp_buffers(void *mlp, uint16_t **h, uint16_t **o);
 
 /* out [T, N] = sum_j weights[t*k + j] * y_sorted[pos[t*k + j]], fp32
  * accumulation in j order, one rounding; weights fp32 [T, k]; y_sorted and

@@ -140,6 +140,10 @@ def test_moe_validation_codes(w4):
     assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 0, 2, 8, 0, 4 * A, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 2, 2, 8, 5, 4 * A, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a16_moe_sum(A, 2 * A, 3 * A, 2, 2, 8, 0, A + 8, None) == w4.W4A16_ERR_INVALID_ARG
+    p = ctypes.c_int()
+    assert L.w4a16_moe_mlp_set_path(None, 0) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_moe_mlp_path(None, 1, ctypes.byref(p)) == w4.W4A16_ERR_INVALID_ARG
+    assert (w4.MOE_PATH_AUTO, w4.MOE_PATH_CHAIN, w4.MOE_PATH_DECODE) == (0, 1, 2)
     if w4.lib.w4a16_device_sm_count() == 0:
         assert L.w4a16_moe_align(A, 8, 4, A, 2 * A, 3 * A, None) == w4.W4A16_ERR_NOT_INITIALIZED
         assert L.w4a16_moe_create(4, 64, 256, 128, A, 2 * A, 3 * A, 2, 1, 8,

@@ -225,3 +225,185 @@ def test_moe_mlp_one_launch_matches_the_chain(w4, T, E, dt):
         down.destroy()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     assert_close(outs[0], chain.double().cpu().numpy(), f"expert MLP T={T} E={E}")
+
+
+# ---- the one-launch decode path of w4a16_moe_mlp ---------------------------
+
+def mlp_experts(seed, E, H, I, dt):
+    g = experts(seed, E, 2 * I, H)
+    d = experts(seed + 1, E, H, I)
+    if dt == torch.bfloat16:
+        g = (g[0], g[1].float().to(dt), g[2])
+        d = (d[0], d[1].float().to(dt), d[2])
+    return g, d
+
+
+def run_mlp(w4, g, d, x, ids, w, path):
+    """One w4a16_moe_mlp call on a fresh handle: out, the path it took, and
+    copies of its intermediate rows and expert outputs (sorted order)."""
+    T, k = ids.shape
+    gate_up = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+    down = w4.MoeExperts(*d, max_slots=T * k)
+    mlp = w4.MoeMlp(gate_up, down, T, k, path=path)
+    try:
+        taken = mlp.path(T)
+        out = mlp(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV))
+        torch.cuda.synchronize()
+        h, o = (t.clone() for t in mlp.intermediates(T * k))
+        torch.cuda.synchronize()
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()
+    return out, taken, h, o
+
+
+def check_mlp_steps(g, d, x, ids, w, out, h, o, E, what):
+    # each step against the oracle on the GPU's own input to that step:
+    # h = silu(gate) * up in sorted order, o = down(h), out = the weighted sum
+    r_srt, r_pos, _ = oracle.moe_align(ids, E)
+    h_ref = oracle.silu_mul(oracle.moe_linear(bits16(x), host(g[0]).view(np.uint32), bits16(g[1]),
+                                              host(g[2]).view(np.uint32), ids,
+                                              dtype=name_of(x.dtype)))
+    assert_close(h, h_ref[r_srt], f"{what}: gate+up")
+    h_slots = bits16(h)[r_pos]
+    o_ref = oracle.moe_linear(h_slots, host(d[0]).view(np.uint32), bits16(d[1]),
+                              host(d[2]).view(np.uint32), ids, per_slot=True,
+                              dtype=name_of(x.dtype))
+    assert_close(o, o_ref[r_srt], f"{what}: down")
+    o_slots = o.double().cpu().numpy()[r_pos]
+    assert_close(out, oracle.moe_sum(o_slots, w.astype(np.float64)), f"{what}: weighted sum")
+
+
+def name_of(dt):
+    return "bf16" if dt == torch.bfloat16 else "f16"
+
+
+# (T, k, E, H, I, dtype): a Qwen3-MoE-like decode expert MLP (hidden 2048,
+# intermediate 768, top 8 of 128) at 1, 4 and 8 tokens; experts with several
+# slots; bf16; a partial last stage in both linears (H 1152: 9 groups, two
+# zeros words; I 384: 3 groups)
+DECODE_CASES = [(1, 8, 128, 2048, 768, torch.float16), (4, 8, 128, 2048, 768, torch.float16),
+                (8, 8, 64, 2048, 768, torch.float16), (2, 8, 16, 1024, 768, torch.bfloat16),
+                (8, 8, 128, 2048, 768, torch.bfloat16), (3, 2, 8, 1152, 384, torch.float16)]
+
+
+@pytest.mark.parametrize("T,k,E,H,I,dt", DECODE_CASES)
+def test_moe_mlp_decode_matches_oracle(w4, T, k, E, H, I, dt):
+    seed = 900 + 7 * T + E + I
+    ids, w = routing(seed, T, k, E)
+    g, d = mlp_experts(seed + 1, E, H, I, dt)
+    x = si.x(si.config_seed(seed, 5), T, H).float().to(dt)
+    out, taken, h, o = run_mlp(w4, g, d, x, ids, w, w4.MOE_PATH_AUTO)
+    assert taken == w4.MOE_PATH_DECODE
+    check_mlp_steps(g, d, x, ids, w, out, h, o, E, f"decode T={T} E={E} {name_of(dt)}")
+
+
+def test_moe_mlp_decode_experts_with_many_slots(w4):
+    # every token picks both experts twice: each expert has 16 slots (two
+    # tiles of 8), and a tile holds two slots of one token
+    T, k, E, H, I = 8, 4, 2, 1024, 512
+    ids = np.tile(np.array([[0, 1, 0, 1]], dtype=np.int32), (T, 1))
+    w = np.full((T, k), 0.25, dtype=np.float32)
+    g, d = mlp_experts(950, E, H, I, torch.float16)
+    x = si.x(si.config_seed(951), T, H)
+    out, taken, h, o = run_mlp(w4, g, d, x, ids, w, w4.MOE_PATH_DECODE)
+    assert taken == w4.MOE_PATH_DECODE
+    check_mlp_steps(g, d, x, ids, w, out, h, o, E, "decode, 16 slots per expert")
+
+
+def test_moe_mlp_decode_matches_chain_and_repeats(w4):
+    # the decode path against the chain (each checked against the oracle
+    # above), and three decode calls on one handle bit-identical (its
+    # counters are left zeroed)
+    T, k, E, H, I = 4, 8, 64, 2048, 768
+    ids, w = routing(960, T, k, E)
+    g, d = mlp_experts(961, E, H, I, torch.float16)
+    x = si.x(si.config_seed(962), T, H).to(DEV)
+    ids_d, w_d = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
+    gate_up = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+    down = w4.MoeExperts(*d, max_slots=T * k)
+    mlp = w4.MoeMlp(gate_up, down, T, k)
+    try:
+        outs = [mlp(x, ids_d, w_d) for _ in range(3)]
+        mlp.set_path(w4.MOE_PATH_CHAIN)
+        chain = mlp(x, ids_d, w_d)
+        torch.cuda.synchronize()
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()
+    for y in outs[1:]:
+        assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
+    assert_close(outs[0], chain.double().cpu().numpy(), "decode vs chain")
+
+
+def test_moe_mlp_decode_invalid_id_is_left_out(w4):
+    # a slot whose id is not an expert sets the status bit and drops out of
+    # the sum: out equals the call with that slot on expert 0 at weight 0
+    # (an MMA column does not depend on the tile's other columns)
+    T, k, E, H, I = 2, 4, 8, 1024, 512
+    ids, w = routing(970, T, k, E)
+    g, d = mlp_experts(971, E, H, I, torch.float16)
+    x = si.x(si.config_seed(972), T, H)
+    bad = ids.copy()
+    bad[1, 2] = E
+    out_bad, _, _, _ = run_mlp(w4, g, d, x, bad, w, w4.MOE_PATH_DECODE)
+    code = w4.w4a16_device_status()
+    assert code & 1024
+    fixed, w0 = ids.copy(), w.copy()
+    fixed[1, 2] = 0 if 0 not in fixed[1] else int(np.setdiff1d(np.arange(E), fixed[1])[0])
+    w0[1, 2] = 0.0
+    out_ref, _, _, _ = run_mlp(w4, g, d, x, fixed, w0, w4.MOE_PATH_DECODE)
+    assert torch.equal(out_bad.view(torch.int16), out_ref.view(torch.int16))
+
+
+def test_moe_mlp_decode_in_a_graph(w4):
+    # the decode launch captured in a CUDA graph: replays equal the eager call
+    T, k, E, H, I = 2, 8, 32, 2048, 768
+    ids, w = routing(980, T, k, E)
+    g, d = mlp_experts(981, E, H, I, torch.float16)
+    x = si.x(si.config_seed(982), T, H).to(DEV)
+    ids_d, w_d = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
+    gate_up = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+    down = w4.MoeExperts(*d, max_slots=T * k)
+    mlp = w4.MoeMlp(gate_up, down, T, k, path=w4.MOE_PATH_DECODE)
+    try:
+        eager = mlp(x, ids_d, w_d)
+        out = torch.empty_like(eager)
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            mlp(x, ids_d, w_d, out=out, stream=st)
+        for _ in range(3):
+            out.zero_()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()
+
+
+def test_moe_mlp_decode_path_rules(w4):
+    # more tokens than the decode kernel takes run the chain (AUTO) or are
+    # refused (forced DECODE); a gate+up without SiLU-and-mul never decodes
+    E, H, I = 8, 1024, 512
+    g, d = mlp_experts(990, E, H, I, torch.float16)
+    gate_up = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=16 * 2)
+    down = w4.MoeExperts(*d, max_slots=16 * 2)
+    mlp = w4.MoeMlp(gate_up, down, 16, 2)
+    try:
+        assert mlp.path(8) == w4.MOE_PATH_DECODE
+        assert mlp.path(9) == w4.MOE_PATH_CHAIN
+        mlp.set_path(w4.MOE_PATH_DECODE)
+        with pytest.raises(w4.W4A16Error):
+            mlp.path(9)
+        mlp.set_path(w4.MOE_PATH_CHAIN)
+        assert mlp.path(1) == w4.MOE_PATH_CHAIN
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()

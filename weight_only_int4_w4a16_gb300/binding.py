@@ -49,6 +49,10 @@ EPILOGUE_SILU_MUL = 2
 
 DTYPE_F16 = 0
 DTYPE_BF16 = 1
+
+MOE_PATH_AUTO = 0
+MOE_PATH_CHAIN = 1
+MOE_PATH_DECODE = 2
 _DTYPE_OF = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
 
 _P = ctypes.c_void_p
@@ -88,6 +92,9 @@ _sig("w4a16_moe_create", [_I, _I, _I, _I, _P, _P, _P, _I, _I, _I, ctypes.POINTER
 _sig("w4a16_moe_destroy", [_P])
 _sig("w4a16_moe_linear", [_P, _P, _I, _P, _P, _I, _P, _P])
 _sig("w4a16_moe_sum", [_P, _P, _P, _I, _I, _I, _I, _P, _P])
+_sig("w4a16_moe_mlp_set_path", [_P, _I])
+_sig("w4a16_moe_mlp_path", [_P, _I, ctypes.POINTER(_I)])
+_sig("w4a16_moe_mlp_buffers", [_P, ctypes.POINTER(_P), ctypes.POINTER(_P)])
 _sig("w4a16_moe_mlp_create", [_P, _P, _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_moe_mlp_destroy", [_P])
 _sig("w4a16_moe_mlp", [_P, _P, _P, _P, _I, _P, _P])
@@ -112,6 +119,7 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_linear_epilogue", "w4a16_linear_ex", "w4a16_dense_linear",
             "w4a16_moe_align", "w4a16_moe_create", "w4a16_moe_destroy", "w4a16_moe_linear",
             "w4a16_moe_sum", "w4a16_moe_mlp_create", "w4a16_moe_mlp_destroy", "w4a16_moe_mlp",
+            "w4a16_moe_mlp_set_path", "w4a16_moe_mlp_path", "w4a16_moe_mlp_buffers",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
@@ -337,6 +345,19 @@ def w4a16_moe_align(topk_ids: torch.Tensor, E: int, stream=None):
     return srt, pos, off
 
 
+class _DeviceRows:
+    """A device pointer seen as 16-bit rows (the CUDA array interface), for
+    torch.as_tensor: no copy, no ownership."""
+
+    def __init__(self, ptr: int, shape):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": "<i2",
+                                          "data": (ptr, False), "version": 3, "strides": None}
+
+
+def _view_device(ptr: int, shape, dt, dev) -> torch.Tensor:
+    return torch.as_tensor(_DeviceRows(ptr, shape), device=dev).view(dt)
+
+
 class MoeExperts:
     """E stacked W4A16 experts (qweight [E, N, K/8], scales [E, N, G], zeros
     [E, N, ceil(G/8)]) prepared for w4a16_moe_linear."""
@@ -374,14 +395,38 @@ class MoeExperts:
 
 
 class MoeMlp:
-    """gate+up then down over one routing (two MoeExperts), one expert-MMA launch."""
+    """gate+up then down over one routing (two MoeExperts): the one-launch
+    decode kernel when a call fits it, else the chain (path: MOE_PATH_*)."""
 
-    def __init__(self, gate_up: MoeExperts, down: MoeExperts, max_tokens: int, k: int):
+    def __init__(self, gate_up: MoeExperts, down: MoeExperts, max_tokens: int, k: int,
+                 path: int = 0):
         self.gate_up, self.down, self.k = gate_up, down, k
         h = _P()
         _check(lib.w4a16_moe_mlp_create(gate_up.handle, down.handle, max_tokens, k,
                                         ctypes.byref(h)), "w4a16_moe_mlp_create")
         self.handle = h.value
+        self.set_path(path)
+
+    def set_path(self, path: int):
+        _check(lib.w4a16_moe_mlp_set_path(self.handle, path), "w4a16_moe_mlp_set_path")
+
+    def path(self, T: int) -> int:
+        """The path (MOE_PATH_CHAIN or MOE_PATH_DECODE) a call with T tokens takes."""
+        p = _I()
+        _check(lib.w4a16_moe_mlp_path(self.handle, T, ctypes.byref(p)), "w4a16_moe_mlp_path")
+        return p.value
+
+    def intermediates(self, n_slots: int):
+        """The last call's intermediate rows h [n_slots, I] and expert outputs
+        o [n_slots, N] in sorted order, as views of the handle's device buffers."""
+        hp, op = _P(), _P()
+        _check(lib.w4a16_moe_mlp_buffers(self.handle, ctypes.byref(hp), ctypes.byref(op)),
+               "w4a16_moe_mlp_buffers")
+        dt = self.gate_up.dtype
+        dev = torch.device("cuda", torch.cuda.current_device())
+        I, N = self.down.K, self.down.N
+        return (_view_device(hp.value, (n_slots, I), dt, dev),
+                _view_device(op.value, (n_slots, N), dt, dev))
 
     def __call__(self, x, topk_ids, weights, out=None, stream=None):
         T = x.shape[0]

@@ -403,6 +403,9 @@ struct MoeHandle {
     MmaLinDesc *tiles = nullptr;  // device [max_tiles]
     int *counts = nullptr;        // device [2]: tiles, units
     __half *xs = nullptr;         // device [max_slots, K]
+    const uint32_t *qweight = nullptr;  // the experts, as given
+    const __half *scales = nullptr;
+    const uint32_t *zeros = nullptr;
     void *buffer = nullptr;
 };
 
@@ -417,8 +420,22 @@ struct MoeMlpHandle {
     MmaLinDesc *tiles = nullptr;
     unsigned *done = nullptr;
     int *counts = nullptr;
+    // the one-launch decode kernel (gate+up with SiLU-and-mul, whole groups)
+    bool dec_ok = false;
+    MoeDecodeWeights dec{};
+    unsigned *dec_counters = nullptr;
+    int path = W4A16_MOE_PATH_AUTO;
     void *buffer = nullptr;
 };
+
+// The path of an expert-MLP call with T tokens; -1 when the forced decode
+// path cannot take it.
+int mlp_path(const MoeMlpHandle *m, int T) {
+    const bool dec = m->dec_ok && moe_decode_smem(m->dec, T, m->k) >= 0;
+    if (m->path == W4A16_MOE_PATH_CHAIN) return W4A16_MOE_PATH_CHAIN;
+    if (m->path == W4A16_MOE_PATH_DECODE) return dec ? W4A16_MOE_PATH_DECODE : -1;
+    return dec ? W4A16_MOE_PATH_DECODE : W4A16_MOE_PATH_CHAIN;
+}
 
 struct RoundGraphHandle {
     cudaGraphExec_t exec = nullptr;
@@ -460,6 +477,7 @@ int w4a16_init(int device, size_t workspace_bytes) {
     if (e == cudaSuccess) e = tc_init(dev);
     if (e == cudaSuccess) e = mma_init(dev);
     if (e == cudaSuccess) e = dense_init(dev);
+    if (e == cudaSuccess) e = moe_decode_init(dev);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         cudaFree(base);
@@ -636,6 +654,9 @@ int w4a16_moe_create(int E, int N, int K, int group, const uint32_t *qweight,
     h->dtype = dtype;
     h->max_slots = max_slots;
     h->max_tiles = (int)max_tiles;
+    h->qweight = qweight;
+    h->scales = reinterpret_cast<const __half *>(scales);
+    h->zeros = zeros;
     // one plan for every tile, weighing the tiles expected side by side (one
     // per expert in use, up to the slots)
     const int copies = max_slots < E ? max_slots : E;
@@ -783,7 +804,16 @@ int w4a16_moe_mlp_create(void *gate_up, void *down, int max_tokens, int k, void 
     const size_t b_sorted = up(slots * 4), b_pos = up(slots * 4), b_off = up((gu->E + 1) * 4);
     const size_t b_h = up(slots * dn->K * 2), b_o = up(slots * dn->N * 2);
     const size_t b_tiles = up(sizeof(MmaLinDesc) * 2 * tiles), b_done = up(2 * tiles * 4);
-    const size_t total = b_sorted + b_pos + b_off + b_h + b_o + b_tiles + b_done + al;
+    // the decode kernel: gate+up rows [gate; up] with SiLU-and-mul over whole
+    // groups and 128-row blocks of down
+    if (gu->epi == W4A16_EPILOGUE_SILU_MUL && moe_decode_shape_ok(gu->E, gu->K, dn->K)) {
+        cudaError_t e0 = moe_decode_describe(gu->qweight, gu->scales, gu->zeros, dn->qweight,
+                                             dn->scales, dn->zeros, gu->E, gu->K, dn->K,
+                                             gu->dtype == W4A16_DTYPE_BF16, &m->dec);
+        m->dec_ok = e0 == cudaSuccess;
+    }
+    const size_t b_dec = m->dec_ok ? up(moe_decode_counter_words(m->dec) * 4) : 0;
+    const size_t total = b_sorted + b_pos + b_off + b_h + b_o + b_tiles + b_done + b_dec + al;
     cudaError_t e = cudaMalloc(&m->buffer, total);
     if (e == cudaSuccess) {
         char *b = (char *)m->buffer;
@@ -802,7 +832,10 @@ int w4a16_moe_mlp_create(void *gate_up, void *down, int max_tokens, int k, void 
         m->done = (unsigned *)b;
         b += b_done;
         m->counts = (int *)b;
+        b += al;
+        m->dec_counters = m->dec_ok ? (unsigned *)b : nullptr;
         e = cudaMemset(m->done, 0, b_done);  // the kernel leaves them zeroed again
+        if (e == cudaSuccess && m->dec_ok) e = cudaMemset(m->dec_counters, 0, b_dec);
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -822,6 +855,31 @@ int w4a16_moe_mlp_destroy(void *mlp) {
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
+int w4a16_moe_mlp_set_path(void *mlp, int path) {
+    if (!mlp || path < W4A16_MOE_PATH_AUTO || path > W4A16_MOE_PATH_DECODE)
+        return W4A16_ERR_INVALID_ARG;
+    ((MoeMlpHandle *)mlp)->path = path;
+    return W4A16_OK;
+}
+
+int w4a16_moe_mlp_path(void *mlp, int T, int *path) {
+    if (!mlp || !path || T < 1) return W4A16_ERR_INVALID_ARG;
+    const MoeMlpHandle *m = (const MoeMlpHandle *)mlp;
+    if (T > m->max_tokens) return W4A16_ERR_INVALID_ARG;
+    const int p = mlp_path(m, T);
+    if (p < 0) return W4A16_ERR_UNSUPPORTED;
+    *path = p;
+    return W4A16_OK;
+}
+
+int w4a16_moe_mlp_buffers(void *mlp, uint16_t **h, uint16_t **o) {
+    if (!mlp || !h || !o) return W4A16_ERR_INVALID_ARG;
+    const MoeMlpHandle *m = (const MoeMlpHandle *)mlp;
+    *h = reinterpret_cast<uint16_t *>(m->h);
+    *o = reinterpret_cast<uint16_t *>(m->o);
+    return W4A16_OK;
+}
+
 int w4a16_moe_mlp(void *mlp, const uint16_t *x, const int32_t *topk_ids, const float *weights,
                   int T, uint16_t *out, void *stream) {
     if (!mlp || !x || !topk_ids || !weights || !out || T < 1) return W4A16_ERR_INVALID_ARG;
@@ -833,8 +891,18 @@ int w4a16_moe_mlp(void *mlp, const uint16_t *x, const int32_t *topk_ids, const f
     if (overlaps(x, (size_t)T * gu->K * 2, out, (size_t)T * dn->N * 2)) return W4A16_ERR_INVALID_ARG;
     const State &st = g_state;
     if (!st.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    const int n_slots = T * m->k;
+    const int path = mlp_path(m, T);
+    if (path < 0) return W4A16_ERR_UNSUPPORTED;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (path == W4A16_MOE_PATH_DECODE) {
+        const MoeDecodeBuffers b{m->h, m->o, m->dec_counters};
+        cudaError_t e = launch_moe_decode(m->dec, reinterpret_cast<const __half *>(x), topk_ids,
+                                          weights, T, m->k, reinterpret_cast<__half *>(out), b,
+                                          st.ws.status, st.dev, cs);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+    }
+    const int n_slots = T * m->k;
     cudaError_t e = launch_moe_align(topk_ids, n_slots, gu->E, m->sorted, m->pos, m->offsets,
                                      st.ws.status, cs);
     g_launches.fetch_add(1, std::memory_order_relaxed);

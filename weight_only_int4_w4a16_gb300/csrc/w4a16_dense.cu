@@ -27,9 +27,12 @@
 #include "../../include/w4a16.h"
 #include "w4a16_device.cuh"
 #include "w4a16_internal.h"
+#include "w4a16_mma_common.cuh"
 
 namespace w4a16 {
 namespace {
+
+using namespace warp_mma;
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
@@ -41,7 +44,6 @@ constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 64 KB
 constexpr int kBarBytes = 256;  // ring barriers, the x barrier, flags
 constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;
 constexpr int kMaxSplit = 32;
-constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
 constexpr int kErrDenseWait = 512;  // device status bit: a wait of the dense kernel expired
 
 struct DenseParams {
@@ -71,48 +73,7 @@ __device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// true once the phase with this parity has completed; false after kWaitNs
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = dev::globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15) == 0 && dev::globaltimer() - t0 > kWaitNs) return false;
-    }
-}
-// box {32 elements, 16 rows, 4 chunks} at (0, row, chunk)
-__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, int row, int chunk,
-                                        uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(chunk), "r"(bar)
-        : "memory");
-}
-
-template <bool kBf16>
-__device__ __forceinline__ __half from_float(float v) {  // round to nearest even
-    if constexpr (kBf16) return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
-    else return __float2half_rn(v);
-}
+// weights: boxes {32 elements, 16 rows, 4 chunks} at (0, row, chunk) (tma_box)
 
 // y = the sum of the S partial slices of block sb, in slice order
 template <bool kBf16>

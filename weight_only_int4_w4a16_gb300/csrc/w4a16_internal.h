@@ -213,6 +213,7 @@ cudaError_t dense_init(const DeviceInfo &dev);
 // ---- mixture of experts (w4a16_moe.cu) -------------------------------------
 constexpr int kMaxMoeExperts = 1024;
 constexpr int kMaxMoeTiles = 2048;  // tiles of up to 8 slots per launch
+constexpr int kErrMoeIds = 1024;  // device status bit: an expert id outside [0, E)
 // Where the tiles of one expert-group launch put their results: y rows in
 // sorted order, and per tile its own split-K partials and counters.
 struct MoeTileSpace {
@@ -234,6 +235,39 @@ cudaError_t launch_moe_prepare(const MmaLinDesc *tmpl, const MmaLinDesc *tmpl2,
                                cudaStream_t stream);
 cudaError_t launch_moe_sum(const __half *y, const int32_t *pos, const float *w, int T, int k,
                            int N, bool bf16, __half *out, cudaStream_t stream);
+
+// ---- expert MLP decode kernel (w4a16_moe_decode.cu) ------------------------
+constexpr int kMoeDecodeMaxSlots = 128;  // T * k per launch
+constexpr int kMoeDecodeMaxTokens = 8;
+// The two expert layers of an MLP as the decode kernel reads them: gate+up
+// [E, 2I, H] (gate rows first, SiLU-and-mul) and down [E, H, I], stacked
+// experts, with the tensor maps written once.
+struct MoeDecodeWeights {
+    CUtensorMap map1, map2;
+    const __half *s1, *s2;
+    const uint32_t *z1, *z2;
+    uintptr_t s1_end, s2_end;
+    int E, I, H, G1, ZW1, G2, ZW2;
+    bool bf16;
+};
+// per call: intermediate rows [T*k, I] and expert outputs [T*k, H] (16-bit),
+// and moe_decode_counter_words zeroed counters (the kernel leaves them zeroed)
+struct MoeDecodeBuffers {
+    __half *h, *o;
+    unsigned *counters;
+};
+bool moe_decode_shape_ok(int E, int H, int I);
+cudaError_t moe_decode_describe(const uint32_t *qw1, const __half *s1, const uint32_t *z1,
+                                const uint32_t *qw2, const __half *s2, const uint32_t *z2, int E,
+                                int H, int I, bool bf16, MoeDecodeWeights *w);
+// dynamic shared memory of a launch for T tokens of k choices; -1: does not fit
+int moe_decode_smem(const MoeDecodeWeights &w, int T, int k);
+size_t moe_decode_counter_words(const MoeDecodeWeights &w);
+cudaError_t launch_moe_decode(const MoeDecodeWeights &w, const __half *x, const int32_t *ids,
+                              const float *wts, int T, int k, __half *out,
+                              const MoeDecodeBuffers &b, int *status, const DeviceInfo &dev,
+                              cudaStream_t stream);
+cudaError_t moe_decode_init(const DeviceInfo &dev);
 
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,

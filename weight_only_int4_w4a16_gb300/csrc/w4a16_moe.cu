@@ -50,7 +50,6 @@ cudaError_t launch_chained(void (*kernel)(Params...), int grid, int threads, cud
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
-constexpr int kErrMoeIds = 1024;  // device status bit: an expert id outside [0, E)
 constexpr int kAlignChunk = 4096;  // slots staged in shared memory per pass
 
 // One CTA.  Thread e owns expert e: counts, the exclusive prefix, then a scan
