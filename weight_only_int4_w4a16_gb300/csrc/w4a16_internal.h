@@ -246,7 +246,7 @@ struct MoeDecodeWeights {
     CUtensorMap map1, map2;
     const __half *s1, *s2;
     const uint32_t *z1, *z2;
-    uintptr_t s1_end, s2_end;
+    uintptr_t s1_end, s2_end, z1_end, z2_end;
     int E, I, H, G1, ZW1, G2, ZW2;
     bool bf16;
 };

@@ -18,13 +18,17 @@
 //     each lane holds a gate sum and its up sum for the same output and token
 //     and applies silu(gate) * up in registers.  Units go to warps
 //     interleaved across CTAs (warp w of CTA c takes units w * grid + c, ...),
-//     spreading the few strips of a decode step over every SM;
+//     spreading the few strips of a decode step over every SM.  x of every
+//     token is copied (cp.async) as soon as the kernel may read it, while the
+//     routing is worked out, and staged once per CTA;
 //   * phase 2, down: a unit is one tile and a block of 128 output rows, one
-//     16-row strip per warp of a CTA; it waits (bounded) for its tile's phase
-//     1 strips (a completion counter per tile), stages the tile's
-//     intermediate rows once, and writes its slots' outputs.  The CTA that
-//     brings a block's last tile sums the block's outputs over each token's
-//     experts (j in order, fp32, one rounding) into out;
+//     16-row strip per warp of a CTA, and a CTA takes a contiguous range of
+//     units (tile-major, so mostly blocks of one tile); for each new tile it
+//     waits (bounded) for the tile's phase-1 strips (a completion counter per
+//     tile) and stages the tile's intermediate rows once; it writes its
+//     slots' outputs.  The CTA that brings a block's last tile sums the
+//     block's outputs over each token's experts (j in order, fp32, one
+//     rounding) into out;
 //   * every warp streams its weights through its own two-slot ring of TMA
 //     boxes (two 8-row boxes per stage: 16 rows x 4 groups x 64 bytes, the
 //     rows' scale and zero words copied by the lanes onto the same
@@ -91,6 +95,7 @@ struct MoeDecodeParams {
     const __half *s1, *s2;  // scales [E * 2I, G1], [E * H, G2]
     const uint32_t *z1, *z2;
     uintptr_t s1_end, s2_end;  // one past each scales array
+    uintptr_t z1_end, z2_end;  // one past each zeros array
     __half *h;         // [T * k, I]: the intermediate rows by sorted position
     __half *o;         // [T * k, H]: each slot's down output by sorted position
     __half *out;       // [T, H]
@@ -104,29 +109,51 @@ struct MoeDecodeParams {
     int sums_off;            // bytes from the staged rows to their group sums, then 8 exponents
 };
 
-// Stage `rows` rows of 16-bit activations (row r at src + r * src_stride)
-// into the MMA's layout: 16-byte unit J of a row at unit x_unit(J), in MMA
-// pair order, bf16 as fp16 scaled by 2^shift(row) (shift from the row's
-// largest exponent, kept in exps[r]), and each group's sum of the staged
-// values times 2^-20 in sums[group * 8 + r].  Reads through L2 (the rows may
-// have been written by other CTAs of this grid).  Every thread of the CTA
-// calls this; it ends with a barrier.
+// Staging of activation rows for the MMA's B operand, in two steps so that
+// the copy overlaps other work:
+//   copy_rows_async: every thread issues 16-byte cp.async copies (L2 only:
+//     the rows may have been written by other CTAs of this grid) of `rows`
+//     rows (row r at src + r * src_stride) into the staged rows, raw order,
+//     committed as one group;
+//   permute_rows (after cp.async.wait_group 0 and a barrier): 16-byte unit J
+//     of a row moves to unit x_unit(J) in MMA pair order (bf16 as fp16 scaled
+//     by 2^shift(row), shift from the row's largest exponent, kept in
+//     exps[r]), and each group's sum of the staged values times 2^-20 goes to
+//     sums[group * 8 + r].  A unit and its destination sit in the same half
+//     warp, so a warp reads all its units before it writes.  Ends with a
+//     barrier.
+__device__ __forceinline__ void cp16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_committed() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void copy_rows_async(uint8_t *xs, int xstride, const __half *src,
+                                                size_t src_stride, int rows, int G) {
+    const int nunits = G * 16, total = rows * nunits;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int r = i / nunits, J = i - r * nunits;
+        cp16(dev::smem_u32(xs + (size_t)r * xstride + 16 * J), src + r * src_stride + 8 * J);
+    }
+    cp_commit();
+}
+
 template <bool kBf16>
-__device__ __forceinline__ void stage_rows(uint8_t *xs, int xstride, const __half *src,
-                                           size_t src_stride, int rows, int G, float *sums,
-                                           int *exps) {
+__device__ __forceinline__ void permute_rows(uint8_t *xs, int xstride, int rows, int G,
+                                             float *sums, int *exps) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nunits = G * 16;
     const int total = rows * nunits;  // a multiple of 16: a half warp holds one group
     if (kBf16) {
-        if (threadIdx.x < 8) exps[threadIdx.x] = 0;
-        __syncthreads();
+        // exps[] were cleared before the barrier that follows the copies
         for (int base = warp * 32; base < total; base += kThreads) {
             const int i = base + lane;
             const int r = i / nunits, J = i - r * nunits;
             int e = 0;
             if (i < total)
-                e = max_bf16_exp(__ldcg(reinterpret_cast<const uint4 *>(src + r * src_stride) + J));
+                e = max_bf16_exp(*reinterpret_cast<const uint4 *>(xs + (size_t)r * xstride + 16 * J));
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, off));
             if (i < total && (J & 15) == 0) atomicMax(exps + r, e);
@@ -137,11 +164,12 @@ __device__ __forceinline__ void stage_rows(uint8_t *xs, int xstride, const __hal
         const int i = base + lane;
         const bool valid = i < total;
         const int r = i / nunits, J = i - r * nunits;
+        uint8_t *row = xs + (size_t)r * xstride;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) v = __ldcg(reinterpret_cast<const uint4 *>(src + r * src_stride) + J);
+        if (valid) v = *reinterpret_cast<const uint4 *>(row + 16 * J);
         if (kBf16 && valid) v = bf16_to_scaled_f16(v, pow2(bf16_stage_shift(exps[r])));
-        if (valid)
-            *reinterpret_cast<uint4 *>(xs + (size_t)r * xstride + 16 * x_unit(J)) = mma_pair_order(v);
+        __syncwarp();
+        if (valid) *reinterpret_cast<uint4 *>(row + 16 * x_unit(J)) = mma_pair_order(v);
         const float2 a = pair_to_float2<false>(v.x), b = pair_to_float2<false>(v.y);
         const float2 e = pair_to_float2<false>(v.z), f = pair_to_float2<false>(v.w);
         float sum = ((a.x + a.y) + (b.x + b.y)) + ((e.x + e.y) + (f.x + f.y));
@@ -151,7 +179,6 @@ __device__ __forceinline__ void stage_rows(uint8_t *xs, int xstride, const __hal
     }
     __syncthreads();
 }
-
 
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -192,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // kernel; the intermediate rows, outputs and counters from the previous
     // launch of this kernel
     grid_dependency_wait();
+    // x of every token goes out first (raw order), to be staged once it lands
+    copy_rows_async(xs, P.xstride1, P.x, (size_t)P.H, P.T, P.G1);
+    if (kBf16 && threadIdx.x < 8) exps[threadIdx.x] = 0;
 
     // ---- routing: slots grouped by expert, stable in slot order.  A slot's
     // sorted position is the number of (expert, slot) keys below its own.
@@ -254,96 +284,89 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int S1 = P.I / 8;               // phase-1 strips per tile (8 outputs each)
     const int B2 = P.H / kBlockRows;      // phase-2 blocks per tile
     const int n_u1 = n_tiles * S1, n_u2 = n_tiles * B2;
+    // phase-2 units of this CTA: a contiguous range (units are tile-major, so
+    // a CTA waits for and stages few tiles)
+    const int u2_lo = (int)((long long)cta * n_u2 / grid);
+    const int u2_hi = (int)((long long)(cta + 1) * n_u2 / grid);
     const int nst1 = (P.G1 + kStageGroups - 1) / kStageGroups;
     const int nst2 = (P.G2 + kStageGroups - 1) / kStageGroups;
 
     // ---- copy stream: this warp's phase-1 strips, then its strips of the
-    // CTA's phase-2 units, kDepth stages ahead of the consumer.  Stage j of a
-    // strip: box A (rows rowA..rowA+7) and box B (rows rowB..rowB+7) of
-    // groups 4j..4j+3.  Metadata: lane (r = lane % 16, hh = lane / 16) copies,
-    // for row r of the stage (rows 0..7 box A's, 8..15 box B's), scale words
-    // 0 and 1 of the stage (hh = 0) or scale word 2 and the zeros word
-    // (hh = 1): the three aligned words that hold the stage's four scales.
+    // CTA's phase-2 units, stage by stage, kDepth stages ahead of the
+    // consumer.  Stage t of the stream: box A (rows rowA..rowA+7) and box B
+    // (rows rowB..rowB+7) of groups 4j..4j+3 of one strip.  Metadata: lane (r = lane % 16, hh = lane / 16) copies, for row r of the
+    // stage (rows 0..7 box A's, 8..15 box B's), scale words 0 and 1 of the
+    // stage (hh = 0) or scale word 2 and the zeros word (hh = 1): the three
+    // aligned words that hold the stage's four scales.
     const int r = lane & 15, hh = lane >> 4;
-    int i_ph = 1, i_q = 0, i_j = 0, i_nst = 0, i_rowA = 0, i_rowB = 0;
-    const CUtensorMap *i_map = nullptr;
-    uintptr_t is_s = 0, is_first = 0, is_z = 0;
-    int is_avail = 0;
-    unsigned t_iss = 0;  // stages issued by this warp
-    auto i_enter = [&]() {  // the strip at (i_ph, i_q), moving on to phase 2 / the end
-        for (;;) {
-            if (i_ph == 1) {
-                const int u = warp * grid + cta + i_q * grid * kWarps;
-                if (u < n_u1) {
-                    const int tile = u / S1, s = u - tile * S1;
-                    i_rowA = t_e[tile] * 2 * P.I + 8 * s;  // gate rows
-                    i_rowB = i_rowA + P.I;                 // their up rows
-                    break;
-                }
-                i_ph = 2;
-                i_q = 0;
-            } else if (i_ph == 2) {
-                const int u = cta + i_q * grid;
-                if (u < n_u2) {
-                    const int tile = u / B2, b = u - tile * B2;
-                    i_rowA = t_e[tile] * P.H + (b * kWarps + warp) * 16;
-                    i_rowB = i_rowA + 8;
-                    break;
-                }
-                i_ph = 3;
-                return;
-            } else {
-                return;
-            }
-        }
-        const bool p1 = i_ph == 1;
-        i_map = p1 ? &P.map1 : &P.map2;
-        i_nst = p1 ? nst1 : nst2;
-        const int G = p1 ? P.G1 : P.G2, ZW = p1 ? P.ZW1 : P.ZW2;
-        const size_t row = (size_t)(r < 8 ? i_rowA + r : i_rowB + (r - 8));
-        const __half *sc = p1 ? P.s1 : P.s2;
-        is_first = (uintptr_t)sc;
-        is_s = (((uintptr_t)(sc + row * G)) & ~(uintptr_t)3) + 8 * (uintptr_t)hh;
-        const uintptr_t end = p1 ? P.s1_end : P.s2_end;
-        const uintptr_t rem = is_s < end ? end - is_s : 0;
-        is_avail = (int)(rem > (1u << 30) ? (1u << 30) : rem);
-        is_z = (uintptr_t)((p1 ? P.z1 : P.z2) + row * ZW);
-        i_j = 0;
+    const int w_base = warp * grid + cta;  // this warp's first phase-1 unit
+    const int w_step = grid * kWarps;
+    const int n1w = w_base < n_u1 ? (n_u1 - 1 - w_base) / w_step + 1 : 0;
+    const unsigned n_st1 = (unsigned)(n1w * nst1);
+    const unsigned n_stages = n_st1 + (unsigned)((u2_hi - u2_lo) * nst2);
+    struct StageLoc {
+        int rowA, rowB, j;
+        bool p1;
     };
-    auto issue_next = [&]() {
-        if (i_ph == 3) return;
-        const uint32_t slot = t_iss & 1u;  // kDepth == 2
+    auto stage_at = [&](unsigned t) -> StageLoc {
+        StageLoc L;
+        if (t < n_st1) {
+            const int q = (int)t / nst1;
+            L.j = (int)t - q * nst1;
+            const int u = w_base + q * w_step;
+            const int tile = u / S1, st = u - tile * S1;
+            L.rowA = t_e[tile] * 2 * P.I + 8 * st;  // gate rows
+            L.rowB = L.rowA + P.I;                  // their up rows
+            L.p1 = true;
+        } else {
+            const int t2 = (int)(t - n_st1), q = t2 / nst2;
+            L.j = t2 - q * nst2;
+            const int u = u2_lo + q;
+            const int tile = u / B2, b = u - tile * B2;
+            L.rowA = t_e[tile] * P.H + (b * kWarps + warp) * 16;
+            L.rowB = L.rowA + 8;
+            L.p1 = false;
+        }
+        return L;
+    };
+    unsigned t_iss = 0;  // stages issued by this warp
+    auto issue_stage = [&](unsigned t) {
+        const StageLoc L = stage_at(t);
+        const CUtensorMap *map = L.p1 ? &P.map1 : &P.map2;
+        const int G = L.p1 ? P.G1 : P.G2, ZW = L.p1 ? P.ZW1 : P.ZW2;
+        const uint32_t slot = t & 1u;  // kDepth == 2
         const uint32_t bar = bar0 + 8 * slot;
         const uint32_t dst = ring0 + slot * kStageBytes;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, kStageW);
-            tma_box(dst, i_map, i_rowA, kStageGroups * i_j, bar);
-            tma_box(dst + kHalfBox, i_map, i_rowB, kStageGroups * i_j, bar);
+            tma_box(dst, map, L.rowA, kStageGroups * L.j, bar);
+            tma_box(dst + kHalfBox, map, L.rowB, kStageGroups * L.j, bar);
         }
         // a scale word copies the part of it inside the array; a word past the
         // end becomes zeros, reads nothing and takes a valid source address
+        const size_t row = (size_t)(r < 8 ? L.rowA + r : L.rowB + (r - 8));
+        const __half *sc = L.p1 ? P.s1 : P.s2;
+        const uintptr_t s_w = (((uintptr_t)(sc + row * G)) & ~(uintptr_t)3) + 8 * (uintptr_t)hh +
+                              8 * (uintptr_t)L.j;
+        const uintptr_t end = L.p1 ? P.s1_end : P.s2_end;
+        const int avail = s_w < end ? (int)min((uintptr_t)16, end - s_w) : 0;
         const uint32_t md = dst + kStageW + r * 16 + 8 * hh;
-        const int n0 = min(max(is_avail, 0), 4);
-        cp4(md, n0 ? is_s : is_first, (uint32_t)n0);
+        const int n0 = min(avail, 4);
+        cp4(md, n0 ? s_w : (uintptr_t)sc, (uint32_t)n0);
         if (hh == 0) {
-            const int n1 = min(max(is_avail - 4, 0), 4);
-            cp4(md + 4, n1 ? is_s + 4 : is_first, (uint32_t)n1);
+            const int n1 = min(max(avail - 4, 0), 4);
+            cp4(md + 4, n1 ? s_w + 4 : (uintptr_t)sc, (uint32_t)n1);
         } else {
-            cp4(md + 4, is_z, 4u);
+            cp4(md + 4, (uintptr_t)((L.p1 ? P.z1 : P.z2) + row * ZW + ((kStageGroups * L.j) >> 3)), 4u);
         }
         cp_arrive_noinc(bar);
+    };
+    auto issue_next = [&]() {
+        if (t_iss >= n_stages) return;
+        issue_stage(t_iss);
         ++t_iss;
-        is_s += 8;
-        is_avail -= 8;
-        // stage j covers groups 4j .. 4j + 3: a new zeros word every second stage
-        if (((i_j + 1) * kStageGroups & 7) == 0) is_z += 4;
-        if (++i_j == i_nst) {
-            ++i_q;
-            i_enter();
-        }
     };
     static_assert(kDepth == 2, "the slot and phase arithmetic assumes two slots");
-    i_enter();
     for (int s = 0; s < kDepth; ++s) issue_next();
 
     // ---- consumer.  One strip: MMA rows 0..7 from box A, rows 8..15 from box
@@ -447,11 +470,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
     };
 
-    // ---- phase 1: gate+up with SiLU-and-mul.  x of every token is staged
-    // once (only by CTAs with a phase-1 strip: warp 0 takes unit cta first).
+    // ---- phase 1: gate+up with SiLU-and-mul, on x staged once per CTA
     bool dead = false;
-    if (cta < n_u1) stage_rows<kBf16>(xs, P.xstride1, P.x, (size_t)P.H, P.T, P.G1, sums, exps);
-    for (int u = warp * grid + cta; u < n_u1; u += grid * kWarps) {
+    cp_wait_committed();
+    __syncthreads();
+    permute_rows<kBf16>(xs, P.xstride1, P.T, P.G1, sums, exps);
+    for (int u = w_base; u < n_u1; u += w_step) {
         const int tile = u / S1, s = u - tile * S1;
         const int p0 = t_p0[tile], n = t_n[tile];
         // lanes of columns >= n compute a column nobody stores: they read column 0
@@ -476,26 +500,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (2 * c + 1 < n)
             P.h[(size_t)(p0 + 2 * c + 1) * P.I + nout] =
                 from_float<kBf16>(acc[3] * (acc[1] / (1.f + expf(-acc[1]))));
-        __threadfence();  // this lane's rows before the strip's arrival
-        __syncwarp();
-        if (lane == 0) atomicAdd(P.tile_done + tile, 1u);
+        __syncwarp();  // the lanes' rows, then the strip's arrival
+        if (lane == 0) {
+            __threadfence();
+            atomicAdd(P.tile_done + tile, 1u);
+        }
     }
 
     // ---- phase 2: down, a tile and a block of 128 rows per unit, then the
     // weighted sum of a block by the CTA that finishes its last tile.  Every
     // warp reaches every barrier; an expired wait stops the CTA at the next.
-    for (int u = cta; u < n_u2; u += grid) {
-        __syncthreads();  // the previous unit's staged rows are free, the flags settled
+    int staged_tile = -1;
+    for (int u = u2_lo; u < u2_hi; ++u) {
+        __syncthreads();  // the staged rows and the flags are settled
         if (flags[kFlagAbortC]) break;
         const int tile = u / B2, b = u - tile * B2;
-        if (threadIdx.x == 0 && !wait_counter(P.tile_done + tile, (unsigned)S1)) {
-            atomicOr(P.status, kErrDecodeWait);
-            flags[kFlagAbortW] = 1;
-        }
-        __syncthreads();
-        if (flags[kFlagAbortW]) break;
         const int p0 = t_p0[tile], n = t_n[tile];
-        stage_rows<kBf16>(xs, P.xstride2, P.h + (size_t)p0 * P.I, (size_t)P.I, n, P.G2, sums, exps);
+        if (tile != staged_tile) {
+            // wait for the tile's phase-1 strips, then stage its intermediate rows
+            if (threadIdx.x == 0 && !wait_counter(P.tile_done + tile, (unsigned)S1)) {
+                atomicOr(P.status, kErrDecodeWait);
+                flags[kFlagAbortW] = 1;
+            }
+            if (kBf16 && threadIdx.x < 8) exps[threadIdx.x] = 0;
+            __syncthreads();
+            if (flags[kFlagAbortW]) break;
+            copy_rows_async(xs, P.xstride2, P.h + (size_t)p0 * P.I, (size_t)P.I, n, P.G2);
+            cp_wait_committed();
+            __syncthreads();
+            permute_rows<kBf16>(xs, P.xstride2, n, P.G2, sums, exps);
+            staged_tile = tile;
+        }
         const int cb = g < n ? g : 0, c0 = 2 * c < n ? 2 * c : 0, c1 = 2 * c + 1 < n ? 2 * c + 1 : 0;
         const int row = (b * kWarps + warp) * 16 + g;  // output row of MMA row g
         const size_t ra = (size_t)t_e[tile] * P.H + row, rb = ra + 8;
@@ -521,11 +556,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 o[row + 8] = from_float<kBf16>(acc[3]);
             }
         }
-        __threadfence();  // the outputs before the unit's arrival
-        __syncthreads();
+        __syncthreads();  // the CTA's outputs of the unit, then its arrival
         if (flags[kFlagAbortC]) break;
-        if (threadIdx.x == 0)
+        if (threadIdx.x == 0) {
+            __threadfence();
             flags[kFlagLast] = atomicAdd(P.blk + b, 1u) == (unsigned)n_tiles - 1u;
+        }
         __syncthreads();
         if (flags[kFlagLast]) {
             // every tile of block b is in: out[t, rows of b] = sum_j w[t, j] *
@@ -533,11 +569,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             __threadfence();
             for (int i = threadIdx.x; i < P.T * kBlockRows; i += kThreads) {
                 const int t = i / kBlockRows, nrow = b * kBlockRows + (i - t * kBlockRows);
+                // eight loads in flight at a time; a slot with an invalid
+                // expert id (no position) is left out
                 float a = 0.f;
-                for (int j = 0; j < P.k; ++j) {
-                    const int sl = t * P.k + j, p = spos[sl];
-                    if (p < 0) continue;  // a slot with an invalid expert id
-                    a = fmaf(wts[sl], to_float<kBf16>(__ldcg(P.o + (size_t)p * P.H + nrow)), a);
+                for (int j0 = 0; j0 < P.k; j0 += 8) {
+                    __half v[8];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = j0 + jj, p = j < P.k ? spos[t * P.k + j] : -1;
+                        v[jj] = p >= 0 ? __ldcg(P.o + (size_t)p * P.H + nrow) : __ushort_as_half(0);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = j0 + jj, sl = t * P.k + j;
+                        if (j < P.k && spos[sl] >= 0) a = fmaf(wts[sl], to_float<kBf16>(v[jj]), a);
+                    }
                 }
                 P.out[(size_t)t * P.H + nrow] = from_float<kBf16>(a);
             }
@@ -609,6 +655,8 @@ cudaError_t moe_decode_describe(const uint32_t *qw1, const __half *s1, const uin
     w->z2 = z2;
     w->s1_end = (uintptr_t)(s1 + (size_t)E * 2 * I * w->G1);
     w->s2_end = (uintptr_t)(s2 + (size_t)E * H * w->G2);
+    w->z1_end = (uintptr_t)(z1 + (size_t)E * 2 * I * w->ZW1);
+    w->z2_end = (uintptr_t)(z2 + (size_t)E * H * w->ZW2);
     w->bf16 = bf16;
     cudaError_t e = encode_experts(&w->map1, qw1, (long long)E * 2 * I, H);
     if (e == cudaSuccess) e = encode_experts(&w->map2, qw2, (long long)E * H, I);
@@ -655,6 +703,8 @@ cudaError_t launch_moe_decode(const MoeDecodeWeights &w, const __half *x, const 
     P.z2 = w.z2;
     P.s1_end = w.s1_end;
     P.s2_end = w.s2_end;
+    P.z1_end = w.z1_end;
+    P.z2_end = w.z2_end;
     P.h = b.h;
     P.o = b.o;
     P.out = out;
