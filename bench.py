@@ -130,7 +130,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the fused 64-layer round kernel, from one ncu capture of the current kernel;
 # None once the kernel changes.
-ROUND_KERNEL_TRAFFIC = None
+ROUND_KERNEL_TRAFFIC = 11_618_614_272
 
 
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):
@@ -536,6 +536,44 @@ def run_dense_case(M: int, N: int, K: int, reps: int):
         raise SystemExit(1)
 
 
+def run_moe_case(T: int, reps: int):
+    """The expert MLP of the bench's MoE entry (E 128, top 8, hidden 2048,
+    intermediate 768) for T tokens on its default path, `reps` calls: the
+    target of ncu captures."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import synthetic_inputs as si
+    import weight_only_int4_w4a16_gb300 as w4
+    dev = torch.device("cuda:0")
+    w4.w4a16_init(0, 512 << 20)
+    E, k, H, I = 128, 8, 2048, 768
+    parts_g = [si.layer(si.config_seed(8, e, 0), 2 * I, H, device=dev) for e in range(E)]
+    parts_d = [si.layer(si.config_seed(8, e, 1), H, I, device=dev) for e in range(E)]
+    g = [torch.stack([p[i] for p in parts_g]) for i in range(3)]
+    d = [torch.stack([p[i] for p in parts_d]) for i in range(3)]
+    del parts_g, parts_d
+    rng = np.random.default_rng(T)
+    ids = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(T)])
+                           .astype(np.int32)).to(dev)
+    wts = torch.full((T, k), 1.0 / k, dtype=torch.float32, device=dev)
+    x = si.x(si.config_seed(8, 0, 9), T, H).to(dev)
+    gu = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
+    dn = w4.MoeExperts(*d, max_slots=T * k)
+    mlp = w4.MoeMlp(gu, dn, T, k)
+    y = torch.empty((T, H), dtype=torch.float16, device=dev)
+    for _ in range(reps):
+        mlp(x, ids, wts, out=y)
+    torch.cuda.synchronize()
+    status = w4.w4a16_device_status()
+    path = "decode" if mlp.path(T) == w4.MOE_PATH_DECODE else "chain"
+    mlp.destroy()
+    gu.destroy()
+    dn.destroy()
+    print(f"moe case T={T} path={path} reps={reps} device_status={status}")
+    if status:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,6 +588,8 @@ def main():
                          "(-1 = dispatch table) and exit; prints no benchmark line")
     ap.add_argument("--clocks-dir", default=None,
                     help="where to keep the nvidia-smi samples of the timed region")
+    ap.add_argument("--moe-case", type=int, nargs=2, metavar=("T", "REPS"),
+                    help="run the expert MLP for T tokens REPS times and exit (for ncu)")
     ap.add_argument("--dense-case", type=int, nargs=4, metavar=("M", "N", "K", "REPS"),
                     help="profiling helper: run one dense fp16 linear REPS times and exit")
     args = ap.parse_args()
@@ -558,6 +598,9 @@ def main():
 
     if args.case:
         run_case(*args.case)
+        return
+    if args.moe_case:
+        run_moe_case(*args.moe_case)
         return
     if args.dense_case:
         run_dense_case(*args.dense_case)
