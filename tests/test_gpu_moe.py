@@ -407,3 +407,69 @@ def test_moe_mlp_decode_path_rules(w4):
         mlp.destroy()
         gate_up.destroy()
         down.destroy()
+
+
+# (T, k, E, H, I, dtype): the most slots a launch takes (T*k = 128), one
+# choice per token, 1024 experts, a one-group intermediate (I 128)
+DECODE_EDGE_CASES = [(8, 16, 128, 1024, 512, torch.float16), (8, 1, 4, 1024, 512, torch.float16),
+                     (1, 8, 1024, 1024, 256, torch.float16), (4, 4, 16, 1024, 128, torch.float16)]
+
+
+@pytest.mark.parametrize("T,k,E,H,I,dt", DECODE_EDGE_CASES)
+def test_moe_mlp_decode_edge_shapes(w4, T, k, E, H, I, dt):
+    seed = 1200 + T * 31 + k * 7 + E + I
+    ids, w = routing(seed, T, k, E)
+    g, d = mlp_experts(seed + 1, E, H, I, dt)
+    x = si.x(si.config_seed(seed, 5), T, H).float().to(dt)
+    out, taken, h, o = run_mlp(w4, g, d, x, ids, w, w4.MOE_PATH_DECODE)
+    assert taken == w4.MOE_PATH_DECODE
+    check_mlp_steps(g, d, x, ids, w, out, h, o, E, f"decode edge T={T} k={k} E={E} I={I}")
+
+
+def test_moe_mlp_decode_bf16_wide_range(w4):
+    # bf16 tokens 2^20 apart in magnitude: each staged row (x, and the
+    # intermediate rows) carries its own power-of-two scale
+    T, k, E, H, I = 4, 4, 16, 1024, 512
+    ids, w = routing(1300, T, k, E)
+    g, d = mlp_experts(1301, E, H, I, torch.bfloat16)
+    x = si.x(si.config_seed(1302), T, H).float()
+    x[1] *= 2.0 ** 20
+    x[3] *= 2.0 ** -20
+    x = x.to(torch.bfloat16)
+    out, _, h, o = run_mlp(w4, g, d, x, ids, w, w4.MOE_PATH_DECODE)
+    r_srt, r_pos, _ = oracle.moe_align(ids, E)
+    h_ref = oracle.silu_mul(oracle.moe_linear(bits16(x), host(g[0]).view(np.uint32), bits16(g[1]),
+                                              host(g[2]).view(np.uint32), ids, dtype="bf16"))[r_srt]
+    o_ref = oracle.moe_linear(bits16(h)[r_pos], host(d[0]).view(np.uint32), bits16(d[1]),
+                              host(d[2]).view(np.uint32), ids, per_slot=True, dtype="bf16")[r_srt]
+    out_ref = oracle.moe_sum(o.double().cpu().numpy()[r_pos], w.astype(np.float64))
+    # the rule is relative to each call's largest output: check the rows of
+    # each token (and their slots) on their own scale
+    tok = (r_srt // k)
+    for t in range(T):
+        rows = np.where(tok == t)[0]
+        assert_close(h[rows], h_ref[rows], f"bf16 wide range: gate+up, token {t}")
+        assert_close(o[rows], o_ref[rows], f"bf16 wide range: down, token {t}")
+        assert_close(out[t:t + 1], out_ref[t:t + 1], f"bf16 wide range: sum, token {t}")
+
+
+def test_moe_mlp_decode_varying_tokens_on_one_handle(w4):
+    # one handle, calls with 3, 8, 1 and 8 tokens: the counters a call leaves
+    # zeroed serve the next, whatever its number of tiles
+    E, k, H, I = 32, 8, 1024, 512
+    g, d = mlp_experts(1400, E, H, I, torch.float16)
+    gate_up = w4.MoeExperts(*g, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=8 * k)
+    down = w4.MoeExperts(*d, max_slots=8 * k)
+    mlp = w4.MoeMlp(gate_up, down, 8, k, path=w4.MOE_PATH_DECODE)
+    try:
+        for i, T in enumerate((3, 8, 1, 8)):
+            ids, w = routing(1401 + i, T, k, E)
+            x = si.x(si.config_seed(1402, i), T, H)
+            out = mlp(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV))
+            torch.cuda.synchronize()
+            h, o = (t.clone() for t in mlp.intermediates(T * k))
+            check_mlp_steps(g, d, x, ids, w, out, h, o, E, f"call {i} T={T}")
+    finally:
+        mlp.destroy()
+        gate_up.destroy()
+        down.destroy()
