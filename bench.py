@@ -130,7 +130,7 @@ class ClockSampler:
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
 # the fused 64-layer round kernel, from one ncu capture of the current kernel;
 # None once the kernel changes.
-ROUND_KERNEL_TRAFFIC = 11_618_614_272
+ROUND_KERNEL_TRAFFIC = 11_406_256_640
 
 
 def build_round(dev, M=M_ROUND, layers=N_LAYERS):

@@ -130,14 +130,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// box {16 words, 16 rows, 4 groups} at (word 0, row, group) of the qweight
-// tensor map (dims: word in group, row, group)
+// box of a 3-D tensor map at (word 0, row, group): the qweight boxes of the
+// warp-MMA kernels.  The weights are read once, so the copy carries an L2
+// evict-first policy: they do not push out what is read again (activations,
+// scale and zero words shared by neighbouring rows, split-K partials).
 __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap *map, int row, int grp,
                                         uint32_t bar) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(grp), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(grp), "r"(bar), "l"(pol)
         : "memory");
 }
 
