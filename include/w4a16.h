@@ -416,6 +416,15 @@ const char *w4a16_status_string(int status);
  * kernel reported one since the last call, and clears the word. */
 int w4a16_device_status(void *stream, int *code);
 
+/* Exercise the expired-wait report: one thread runs the library's bounded
+ * waits on a completion counter that nothing increments and on an mbarrier
+ * that nothing arrives at; each gives up after its limit (200 ms) and ORs a
+ * bit into the device status word (4096: the counter wait, 8192: the
+ * mbarrier wait), which the next w4a16_device_status returns.  Nothing
+ * faults or hangs; the stream is busy for about 0.4 s.  For tests of the
+ * error path.  Needs w4a16_init. */
+int w4a16_wait_probe(void *stream);
+
 /* The cudaError_t behind the calling thread's last W4A16_ERR_CUDA (0 if none). */
 int w4a16_last_cuda_error(void);
 

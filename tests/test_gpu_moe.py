@@ -473,3 +473,19 @@ def test_moe_mlp_decode_varying_tokens_on_one_handle(w4):
         mlp.destroy()
         gate_up.destroy()
         down.destroy()
+
+
+def test_moe_mlp_decode_no_valid_expert(w4):
+    # every id outside [0, E): the status bit is set and every output is an
+    # empty sum (zero), as on the chain path
+    T, k, E, H, I = 2, 4, 8, 1024, 512
+    g, d = mlp_experts(1500, E, H, I, torch.float16)
+    ids = np.full((T, k), E + 3, dtype=np.int32)
+    ids[1, 2] = -1
+    w = np.full((T, k), 0.25, dtype=np.float32)
+    x = si.x(si.config_seed(1501), T, H)
+    for path in (w4.MOE_PATH_DECODE, w4.MOE_PATH_CHAIN):
+        out, taken, _, _ = run_mlp(w4, g, d, x, ids, w, path)
+        assert taken == path
+        assert w4.w4a16_device_status() & 1024
+        assert torch.count_nonzero(out.float()) == 0

@@ -95,6 +95,7 @@ _sig("w4a16_moe_sum", [_P, _P, _P, _I, _I, _I, _I, _P, _P])
 _sig("w4a16_moe_mlp_set_path", [_P, _I])
 _sig("w4a16_moe_mlp_path", [_P, _I, ctypes.POINTER(_I)])
 _sig("w4a16_moe_mlp_buffers", [_P, ctypes.POINTER(_P), ctypes.POINTER(_P)])
+_sig("w4a16_wait_probe", [_P])
 _sig("w4a16_moe_mlp_create", [_P, _P, _I, _I, ctypes.POINTER(_P)])
 _sig("w4a16_moe_mlp_destroy", [_P])
 _sig("w4a16_moe_mlp", [_P, _P, _P, _P, _I, _P, _P])
@@ -124,7 +125,8 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
             "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
             "w4a16_probe_reset", "w4a16_kernel_launches", "w4a16_rung_name", "w4a16_status_string",
-            "w4a16_device_status", "w4a16_last_cuda_error", "w4a16_device_sm_count"]
+            "w4a16_device_status", "w4a16_wait_probe", "w4a16_last_cuda_error",
+            "w4a16_device_sm_count"]
 
 
 class W4A16Error(RuntimeError):
@@ -535,6 +537,13 @@ def w4a16_device_status(stream=None) -> int:
     if st not in (W4A16_OK, W4A16_ERR_DEVICE):
         _check(st, "w4a16_device_status")
     return int(code.value)
+
+
+def w4a16_wait_probe(stream=None):
+    """Run the library's bounded waits on a counter and an mbarrier that nothing
+    completes; each expires (200 ms) and sets its bit in the device status
+    word (4096, 8192)."""
+    _check(lib.w4a16_wait_probe(_stream_ptr(stream)), "w4a16_wait_probe")
 
 
 def w4a16_device_sm_count() -> int:

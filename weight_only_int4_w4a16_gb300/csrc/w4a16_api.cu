@@ -1164,6 +1164,13 @@ int w4a16_device_status(void *stream, int *code) {
     return h ? W4A16_ERR_DEVICE : W4A16_OK;
 }
 
+int w4a16_wait_probe(void *stream) {
+    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
+    cudaError_t e = launch_wait_probe(g_state.ws.status, (cudaStream_t)stream);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
+}
+
 int w4a16_last_cuda_error(void) { return t_last_cuda_error; }
 
 int w4a16_device_sm_count(void) { return g_state.initialized ? g_state.dev.sm_count : 0; }

@@ -269,6 +269,11 @@ cudaError_t launch_moe_decode(const MoeDecodeWeights &w, const __half *x, const 
                               cudaStream_t stream);
 cudaError_t moe_decode_init(const DeviceInfo &dev);
 
+// ---- expired-wait probe (w4a16_waitprobe.cu) -------------------------------
+constexpr int kErrProbeCounterWait = 4096;  // device status bit: the probe's counter wait expired
+constexpr int kErrProbeBarrierWait = 8192;  // device status bit: the probe's mbarrier wait expired
+cudaError_t launch_wait_probe(int *status, cudaStream_t stream);
+
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,
                         uint32_t *zeros, cudaStream_t stream);
