@@ -248,10 +248,11 @@ def epilogue_bytes(M: int, N: int, K: int, epi: int) -> int:
     return linear_bytes(M, N, K)
 
 
-def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), epi=0):
+def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), epi=0, spread=None):
     """Median single-launch time of one linear (with epilogue `epi`) with L2
     flushed before each launch, per rung (-1 = the dispatch table's choice);
-    None where a rung cannot run the shape."""
+    None where a rung cannot run the shape.  `spread`, a dict, receives each
+    rung's (p10, p90) times."""
     import synthetic_inputs as si
     seed = si.config_seed(seed_cfg, 0, M)
     qw, s, zw = si.layer(seed, N, K, device=dev)
@@ -284,7 +285,10 @@ def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), ep
                 b.record()
                 ts.append((a, b))
             torch.cuda.synchronize()
-            out[rung] = float(np.median([a.elapsed_time(b) for a, b in ts])) / 1e3
+            times = np.array([a.elapsed_time(b) for a, b in ts]) / 1e3
+            out[rung] = float(np.median(times))
+            if spread is not None:
+                spread[rung] = (float(np.percentile(times, 10)), float(np.percentile(times, 90)))
         finally:
             w4.w4a16_set_forced_rung(prev)
     del qw, s, zw
@@ -652,6 +656,15 @@ def main():
     elapsed = ev0.elapsed_time(ev1) / 1e3
     clk = clocks.stop()
     launches = int(launches1 - launches0)
+    # the rungs that ran (the library's per-rung counters) must be the ones
+    # the dispatch table names for the round's shapes
+    expect = [0] * w4.NUM_RUNGS
+    for L in lin:
+        expect[w4.w4a16_select_rung(M_ROUND, L["N"], L["K"])] += args.warmup + args.steps
+    ran = w4.w4a16_probe_counts()
+    if ran != expect:
+        raise SystemExit(f"the round ran rungs {ran}, the dispatch table names {expect}")
+    rungs_ran = {w4.rung_name(r): n for r, n in enumerate(ran) if n}
 
     rb = round_bytes(layers=args.layers)
     value, elapsed = job_rate(elapsed, rb, args.steps, world, dev)
@@ -716,7 +729,8 @@ def main():
              "round_bytes": rb, "launches_per_round": per_round,
              "linears_launched_alone": per_linear,
              "rung_per_shape": {n: w4.rung_name(w4.w4a16_select_rung(M_ROUND, N, K))
-                                for n, K, N in ROUND_SHAPES}}
+                                for n, K, N in ROUND_SHAPES},
+             "linears_per_rung_in_timed_and_warmup_rounds": rungs_ran}
     if not args.no_extra and rank == 0:
         # the same round with bf16 activations and scales (the same packed
         # weights and zeros; bf16 copies of x and the scales, bf16 outputs)
@@ -741,10 +755,14 @@ def main():
                                     ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
                                     ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] + \
                 [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)]:
-            ts = time_single(w4, M, N, K, cfg, dev, flush=flush, rungs=(-1, 0, 1, 2, 3, 4, 5))
+            spread = {}
+            ts = time_single(w4, M, N, K, cfg, dev, flush=flush, rungs=(-1, 0, 1, 2, 3, 4, 5),
+                             spread=spread)
             by = linear_bytes(M, N, K)
             t = ts[-1]
-            singles[label] = {"us": t * 1e6, "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
+            singles[label] = {"us": t * 1e6, "us_p10": spread[-1][0] * 1e6,
+                              "us_p90": spread[-1][1] * 1e6,
+                              "GBps": by / t / 1e9, "frac_of_peak": by / t / 1e9 / peak,
                               "rung": w4.rung_name(w4.w4a16_select_rung(M, N, K)),
                               "us_per_rung": {w4.rung_name(r): (None if v is None else v * 1e6)
                                               for r, v in ts.items() if r >= 0}}

@@ -278,11 +278,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode_dense = nullptr;
 
 int dense_xstride(int slice_stages) { return slice_stages * kStageK * 2 + 64; }
 
@@ -337,7 +332,8 @@ DensePlan plan_dense(int M, int N, int K, const DeviceInfo &dev) {
 cudaError_t launch_dense(const __half *x, const __half *w, __half *y, int M, int N, int K,
                          bool bf16, const DensePlan &plan, const Workspace &ws,
                          cudaStream_t stream) {
-    if (!g_encode_dense) return cudaErrorInitializationError;
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorInitializationError;
     DenseParams P;
     memset(&P, 0, sizeof(P));
     // W as a 3-D tensor of 16-bit elements: (element in a 32-k chunk, row,
@@ -346,7 +342,7 @@ cudaError_t launch_dense(const __half *x, const __half *w, __half *y, int M, int
     const cuuint64_t strides[2] = {(cuuint64_t)K * 2, 64};
     const cuuint32_t box[3] = {32, 16, (cuuint32_t)(kStageK / 32)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode_dense(&P.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, (void *)w, dims,
+    CUresult r = encode(&P.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, (void *)w, dims,
                                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -375,15 +371,7 @@ cudaError_t launch_dense(const __half *x, const __half *w, __half *y, int M, int
 }
 
 cudaError_t dense_init(const DeviceInfo &dev) {
-    if (!g_encode_dense) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-        g_encode_dense = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+    if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
     int dyn = kSmemPerCta;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     cudaError_t e = cudaSuccess;

@@ -50,6 +50,14 @@ struct Workspace {
     int *status;  // device word: kernels OR in an error code when a bounded wait expires
 };
 
+// cuTensorMapEncodeTiled from the driver, looked up once (null if the driver
+// lacks it); every kernel that reads through TMA encodes its maps with it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
 struct DeviceInfo {
     int device;
     int sm_count;

@@ -885,11 +885,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode_mma = nullptr;
 
 cudaLaunchConfig_t launch_config(int grid, int smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr) {
@@ -1004,7 +999,8 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi,
 
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d) {
-    if (!g_encode_mma) return cudaErrorInitializationError;
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorInitializationError;
     memset(d, 0, sizeof(*d));
     const int G = a.K / kGroup;
     // qweight as a 3-D tensor of uint32: (word in group, row, group), so one
@@ -1013,7 +1009,7 @@ cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partia
     const cuuint64_t strides[2] = {(cuuint64_t)a.K / 2, 64};
     const cuuint32_t box[3] = {16, 16, (cuuint32_t)kStageGroups};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode_mma(&d->tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims,
+    CUresult r = encode(&d->tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1090,16 +1086,21 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
                   : cudaLaunchKernelEx(&cfg, mma_kernel<true, false>, P);
 }
 
-cudaError_t mma_init(const DeviceInfo &dev) {
-    if (!g_encode_mma) {
-        void *fn = nullptr;
+EncodeTiledFn tensor_map_encoder() {
+    // looked up once, on first use (a function-local static: thread-safe)
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-        g_encode_mma = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+cudaError_t mma_init(const DeviceInfo &dev) {
+    if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
     int dyn = kSmemPerCta;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     cudaError_t e = cudaSuccess;

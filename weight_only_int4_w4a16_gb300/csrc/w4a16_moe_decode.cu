@@ -618,19 +618,16 @@ bool moe_decode_shape_ok(int E, int H, int I) {
            I > 0 && (long long)E * 2 * I < (1ll << 31) && (long long)E * H < (1ll << 31);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-static EncodeTiledFn g_encode_decode = nullptr;
 
 // qweight [rows, K/8] as (word in group, row, group), boxes of 8 rows x 4 groups
 static cudaError_t encode_experts(CUtensorMap *map, const uint32_t *qw, long long rows, int K) {
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorInitializationError;
     const cuuint64_t dims[3] = {16, (cuuint64_t)rows, (cuuint64_t)(K / kGroup)};
     const cuuint64_t strides[2] = {(cuuint64_t)K / 2, 64};
     const cuuint32_t box[3] = {16, 8, (cuuint32_t)kStageGroups};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode_decode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)qw, dims, strides,
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)qw, dims, strides,
                                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -640,7 +637,7 @@ static cudaError_t encode_experts(CUtensorMap *map, const uint32_t *qw, long lon
 cudaError_t moe_decode_describe(const uint32_t *qw1, const __half *s1, const uint32_t *z1,
                                 const uint32_t *qw2, const __half *s2, const uint32_t *z2, int E,
                                 int H, int I, bool bf16, MoeDecodeWeights *w) {
-    if (!g_encode_decode || !moe_decode_shape_ok(E, H, I)) return cudaErrorInvalidValue;
+    if (!tensor_map_encoder() || !moe_decode_shape_ok(E, H, I)) return cudaErrorInvalidValue;
     memset(w, 0, sizeof(*w));
     w->E = E;
     w->H = H;
@@ -743,15 +740,7 @@ cudaError_t launch_moe_decode(const MoeDecodeWeights &w, const __half *x, const 
 }
 
 cudaError_t moe_decode_init(const DeviceInfo &dev) {
-    if (!g_encode_decode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-        g_encode_decode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+    if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
     int dyn = kSmemPerCta;
     if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     const void *fns[2] = {(const void *)moe_decode_kernel<false>,

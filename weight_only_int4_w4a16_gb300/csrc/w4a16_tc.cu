@@ -638,11 +638,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn g_encode = nullptr;
 
 template <int T>
 cudaError_t launch_t(const TcParams &p, dim3 grid, cudaStream_t stream) {
@@ -679,15 +674,7 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
 
 cudaError_t tc_init(const DeviceInfo &dev) {
     (void)dev;
-    if (!g_encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorSymbolNotFound;
-        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-    }
+    if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TcConfig<16>::kSmemBytes);
     if (e == cudaSuccess)
@@ -708,14 +695,15 @@ extern "C" int w4a16_debug_trace(unsigned long long *out, int n) {
 
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream) {
-    if (!g_encode) return cudaErrorInitializationError;
+    const EncodeTiledFn encode = tensor_map_encoder();
+    if (!encode) return cudaErrorInitializationError;
     TcParams p;
     memset(&p, 0, sizeof(p));
     const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
     const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
     const cuuint32_t box[2] = {(cuuint32_t)kChunkWords, (cuuint32_t)kTileN};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, (void *)a.qw, dims, strides,
+    CUresult r = encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, (void *)a.qw, dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
