@@ -725,7 +725,48 @@ def main():
     graph_ms = a.elapsed_time(b) / args.steps
     g.destroy()
 
+    # the same round as 256 launches back to back (one w4a16_linear per
+    # linear, as a caller without the fused round would run it)
+    for L in lin:
+        w4.w4a16_linear(L["x"], L["qweight"], L["scales"], L["zeros"], y=L["y"], stream=stream)
+    torch.cuda.synchronize()
+    n_sep = 3
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n_sep):
+        for L in lin:
+            w4.w4a16_linear(L["x"], L["qweight"], L["scales"], L["zeros"], y=L["y"], stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    sep_ms = a.elapsed_time(b) / n_sep
+    # and those 256 launches captured into one CUDA graph (no host cost per
+    # launch; consecutive kernels overlap by programmatic dependent launch)
+    sep_graph_ms = None
+    try:
+        sg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(sg, stream=stream):
+            for L in lin:
+                w4.w4a16_linear(L["x"], L["qweight"], L["scales"], L["zeros"], y=L["y"],
+                                stream=stream)
+        with torch.cuda.stream(stream):  # a replay runs on the current stream
+            for _ in range(2):
+                sg.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(n_sep):
+                sg.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        sep_graph_ms = a.elapsed_time(b) / n_sep
+        sg.reset()
+    except RuntimeError as exc:  # reported, not fatal: the timed round is above
+        print(f"[bench] separate-launch graph not measured: {exc}", file=sys.stderr)
+
     extra = {"round_graph_ms": graph_ms, "round_graph_GBps": rb / (graph_ms / 1e3) / 1e9,
+             "round_as_separate_launches_ms": sep_ms,
+             "round_as_separate_launches_GBps": rb / (sep_ms / 1e3) / 1e9,
+             "round_as_separate_launches_graph_ms": sep_graph_ms,
              "round_bytes": rb, "launches_per_round": per_round,
              "linears_launched_alone": per_linear,
              "rung_per_shape": {n: w4.rung_name(w4.w4a16_select_rung(M_ROUND, N, K))
