@@ -381,3 +381,43 @@ def test_decode_round_full_64_layers_sampled(w4):
         assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, f"layer seed {L['seed']}")
     del layers
     torch.cuda.empty_cache()
+
+
+def test_random_sweep_every_path(w4):
+    # seeded random shapes across every dispatch path: M 1..64 (the mma rungs,
+    # 8-token tiles and the tcgen05 rung), ragged N, K from one group to 40,
+    # fp16 and bf16, each epilogue; all launched, then all checked (stale data
+    # between calls of different sizes shows only this way)
+    rng = np.random.default_rng(2026)
+    cases = []
+    for i in range(20):
+        M = int(rng.integers(1, 9)) if i % 2 == 0 else int(rng.integers(9, 65))
+        K = 128 * int(rng.integers(1, 41))
+        epi = int(rng.integers(0, 3))
+        dt = torch.bfloat16 if rng.random() < 0.4 else torch.float16
+        if epi == w4.EPILOGUE_SILU_MUL:
+            N = 32 * int(rng.integers(1, 60))
+        else:
+            N = int(rng.integers(1, 2000))
+        if M > 8 and N > 1024:  # keep the oracle's share of the test short
+            N = 1024  # (a multiple of 32, as SiLU-and-mul needs)
+        seed = si.config_seed(54, i)
+        qw, s, zw = si.layer(seed, N, K)
+        x = si.x(seed, M, K).float().to(dt)
+        s = s.float().to(dt) if dt == torch.bfloat16 else s
+        res = si.residual(seed, M, N).float().to(dt) if epi == w4.EPILOGUE_RESIDUAL else None
+        cols = N // 2 if epi == w4.EPILOGUE_SILU_MUL else N
+        y = torch.full((M, cols), float("nan"), dtype=dt, device=DEV)
+        w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV), epilogue=epi,
+                           residual=None if res is None else res.to(DEV), y=y)
+        cases.append((M, N, K, epi, dt, x, qw, s, zw, res, y))
+    torch.cuda.synchronize()
+    for M, N, K, epi, dt, x, qw, s, zw, res, y in cases:
+        name = "bf16" if dt == torch.bfloat16 else "f16"
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        ref = oracle.linear(bits(x), si.as_u32(qw), bits(s), si.as_u32(zw), dtype=name)
+        if epi == w4.EPILOGUE_RESIDUAL:
+            ref = oracle.add_residual(ref, bits(res), name)
+        elif epi == w4.EPILOGUE_SILU_MUL:
+            ref = oracle.silu_mul(ref)
+        assert_close(y, ref, f"M={M} N={N} K={K} epi={epi} {name}")
