@@ -248,11 +248,13 @@ def epilogue_bytes(M: int, N: int, K: int, epi: int) -> int:
     return linear_bytes(M, N, K)
 
 
-def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), epi=0, spread=None):
+def time_single(w4, M, N, K, seed_cfg, dev, reps=50, flush=None, rungs=(-1,), epi=0, spread=None,
+                warmup=10):
     """Median single-launch time of one linear (with epilogue `epi`) with L2
     flushed before each launch, per rung (-1 = the dispatch table's choice);
-    None where a rung cannot run the shape.  `spread`, a dict, receives each
-    rung's (p10, p90) times."""
+    None where a rung cannot run the shape.  After `warmup` launches per rung,
+    the rungs take turns launch by launch (A/B alternated, not one after the
+    other).  `spread`, a dict, receives each rung's (p10, p90) times."""
     import synthetic_inputs as si
     seed = si.config_seed(seed_cfg, 0, M)
     qw, s, zw = si.layer(seed, N, K, device=dev)
@@ -265,32 +267,37 @@ def time_single(w4, M, N, K, seed_cfg, dev, reps=20, flush=None, rungs=(-1,), ep
             w4.w4a16_linear_epilogue(x, qw, s, zw, epi, residual=res, y=y)
         else:
             w4.w4a16_linear(x, qw, s, zw, y=y)
-    out = {}
-    for rung in rungs:
-        prev = w4.w4a16_set_forced_rung(rung)
-        try:
+    out, runnable, events = {}, [], {}
+    prev = w4.w4a16_set_forced_rung(-1)
+    try:
+        for rung in rungs:
+            w4.w4a16_set_forced_rung(rung)
             try:
-                for _ in range(3):
+                for _ in range(warmup):
                     call()
             except w4.W4A16Error:
                 out[rung] = None
                 continue
-            ts = []
-            for _ in range(reps):
+            runnable.append(rung)
+            events[rung] = []
+        for _ in range(reps):
+            for rung in runnable:
+                w4.w4a16_set_forced_rung(rung)
                 flush_l2(flush)
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record()
                 call()
                 b.record()
-                ts.append((a, b))
-            torch.cuda.synchronize()
-            times = np.array([a.elapsed_time(b) for a, b in ts]) / 1e3
-            out[rung] = float(np.median(times))
-            if spread is not None:
-                spread[rung] = (float(np.percentile(times, 10)), float(np.percentile(times, 90)))
-        finally:
-            w4.w4a16_set_forced_rung(prev)
+                events[rung].append((a, b))
+        torch.cuda.synchronize()
+    finally:
+        w4.w4a16_set_forced_rung(prev)
+    for rung in runnable:
+        times = np.array([a.elapsed_time(b) for a, b in events[rung]]) / 1e3
+        out[rung] = float(np.median(times))
+        if spread is not None:
+            spread[rung] = (float(np.percentile(times, 10)), float(np.percentile(times, 90)))
     del qw, s, zw
     return out
 
