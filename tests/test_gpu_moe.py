@@ -197,9 +197,10 @@ def test_moe_expert_mlp_step_by_step(w4, T):
 @pytest.mark.parametrize("T,E,dt", [(1, 32, torch.float16), (4, 32, torch.float16),
                                     (8, 128, torch.float16), (4, 16, torch.bfloat16)])
 def test_moe_mlp_one_launch_matches_the_chain(w4, T, E, dt):
-    # w4a16_moe_mlp (both linears in one expert-MMA launch, down tiles waiting
-    # for their gate+up tiles) against the call-by-call chain, which the test
-    # above checks against the oracle step by step; run twice (the completion
+    # w4a16_moe_mlp on its chain path (both linears in one expert-MMA launch,
+    # down tiles waiting for their gate+up tiles) against the call-by-call
+    # chain, which the test above checks against the oracle step by step, and
+    # its intermediates against the oracle; run twice (the completion
     # counters must be left zeroed), bit-identical
     k, H, I = 8, 1024, 768
     ids, w = routing(800 + T + E, T, k, E)
@@ -211,9 +212,12 @@ def test_moe_mlp_one_launch_matches_the_chain(w4, T, E, dt):
     ids_d, w_d = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
     gate_up = w4.MoeExperts(g_qw, g_s, g_zw, epilogue=w4.EPILOGUE_SILU_MUL, max_slots=T * k)
     down = w4.MoeExperts(d_qw, d_s, d_zw, max_slots=T * k)
-    mlp = w4.MoeMlp(gate_up, down, T, k)
+    mlp = w4.MoeMlp(gate_up, down, T, k, path=w4.MOE_PATH_CHAIN)
     try:
+        assert mlp.path(T) == w4.MOE_PATH_CHAIN
         outs = [mlp(x, ids_d, w_d) for _ in range(2)]
+        torch.cuda.synchronize()
+        h_m, o_m = (t.clone() for t in mlp.intermediates(T * k))
         srt, pos, off = w4.w4a16_moe_align(ids_d, E)
         h = gate_up.linear(x, srt, off, T * k, gather_k=k)
         o = down.linear(h, srt, off, T * k, gather_k=0)
@@ -225,6 +229,8 @@ def test_moe_mlp_one_launch_matches_the_chain(w4, T, E, dt):
         down.destroy()
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
     assert_close(outs[0], chain.double().cpu().numpy(), f"expert MLP T={T} E={E}")
+    check_mlp_steps((g_qw, g_s, g_zw), (d_qw, d_s, d_zw), x.cpu(), ids, w, outs[0], h_m, o_m, E,
+                    f"chain path T={T} E={E}")
 
 
 # ---- the one-launch decode path of w4a16_moe_mlp ---------------------------
