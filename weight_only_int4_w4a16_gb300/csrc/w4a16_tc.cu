@@ -565,24 +565,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 tmem + ((uint32_t)(quarter * 32) << 16) + C::kDBase + d * kDCols;
             if constexpr (C::kChains == 1) {
 #pragma unroll
-                for (int t0 = 0; t0 < T; t0 += 16) {
-                    float v[16];
+                for (int t0 = 0; t0 < T; t0 += 32) {
+                    float v[16], w[16];
                     tmem_ld_x16(taddr + t0, v);
+                    tmem_ld_x16(taddr + t0 + 16, w);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) acc[t0 + i] = fmaf(sc, v[i], acc[t0 + i]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[t0 + 16 + i] = fmaf(sc, w[i], acc[t0 + 16 + i]);
                 }
             } else {
                 float sum[T];
 #pragma unroll
                 for (int t = 0; t < T; ++t) sum[t] = 0.f;
 #pragma unroll
-                for (int b = 0; b < kDCols / 16; ++b) {
-                    float v[16];
+                for (int b = 0; b < kDCols / 16; b += 2) {
+                    float v[16], w[16];
                     tmem_ld_x16(taddr + 16 * b, v);
+                    tmem_ld_x16(taddr + 16 * b + 16, w);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) sum[(16 * b + i) % T] += v[i];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) sum[(16 * b + 16 + i) % T] += w[i];
                 }
 #pragma unroll
                 for (int t = 0; t < T; ++t) acc[t] = fmaf(sc, sum[t], acc[t]);
