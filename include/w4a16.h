@@ -261,19 +261,24 @@ int w4a16_round_graph_launch(void *graph, void *stream);
 int w4a16_round_graph_destroy(void *graph);
 
 /* y = x @ W^T like w4a16_linear, for M <= 8 on the warp-MMA rungs, with no
- * allocation and no w4a16_init: the pages have no counterpart; this serves
+ * allocation and no w4a16_init.  The pages have no counterpart: this serves
  * callers that cannot allocate device memory (a process whose memory a
  * caching allocator has wholly reserved, a serving loop that must not call
  * cudaMalloc, which synchronises the device).  Its split-K scratch is a
- * statically sized device array of the library (2 MiB of fp32 partial sums and
- * 4096 block counters): shapes whose split needs more return
- * W4A16_ERR_WORKSPACE before anything is launched; M > 8 returns
+ * statically sized device array of the library, which every GPU that loads
+ * the library holds until the process exits: 4 MiB of fp32 partial sums and
+ * 4096 block counters.  That covers every M <= 8 linear of a 27B-class decode
+ * layer (qkv 5120 x 8192, o 6144 x 5120, gate+up 5120 x 34816, down
+ * 17408 x 5120, K x N); shapes whose split needs more return
+ * W4A16_ERR_WORKSPACE before anything is launched, and M > 8 returns
  * W4A16_ERR_UNSUPPORTED.  The first call on a device (the current device at
  * the call) sets up that device: it looks up the scratch's device address,
  * zeroes its counters and sets the kernel attributes; make that first call
  * before any stream capture.  Every call shares the one scratch array: calls
  * that overlap on the GPU race on it.  Bounded-wait errors of its kernel are
- * recorded in the scratch, not in the word w4a16_device_status reads.
+ * recorded in a status word of the scratch, which w4a16_device_status reads
+ * (that read also re-zeroes the scratch's counters when the word is set).
+ * Each call counts one launch and one linear of its rung in the probes.
  * Argument rules as for w4a16_linear. */
 int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                          const uint32_t *zeros, int M, int N, int K, int group, uint16_t *y,
@@ -413,15 +418,24 @@ const char *w4a16_status_string(int status);
  * word, drains its in-flight copies, frees its tensor memory and exits, so the
  * CUDA context stays usable.  This call synchronises `stream`, returns
  * W4A16_ERR_DEVICE with the accumulated code in *code (may be NULL) if any
- * kernel reported one since the last call, and clears the word. */
+ * kernel reported one since the last call, and clears the word.  It also
+ * reads the status word of w4a16_linear_noalloc's scratch on the current
+ * device (once a call has set that device up) and ORs it in; when that word
+ * is set it re-zeroes the scratch's block counters and scheduling words too,
+ * since a launch cut short by an expired wait can leave them nonzero (call it
+ * with no w4a16_linear_noalloc call in flight).  W4A16_ERR_NOT_INITIALIZED
+ * when neither w4a16_init nor a w4a16_linear_noalloc call has run. */
 int w4a16_device_status(void *stream, int *code);
 
 /* Exercise the expired-wait report: one thread runs the library's bounded
  * waits on a completion counter that nothing increments and on an mbarrier
  * that nothing arrives at; each gives up after its limit (200 ms) and ORs a
  * bit into the device status word (4096: the counter wait, 8192: the
- * mbarrier wait), which the next w4a16_device_status returns.  Nothing
- * faults or hangs; the stream is busy for about 0.4 s.  For tests of the
+ * mbarrier wait), which the next w4a16_device_status returns.  When a
+ * w4a16_linear_noalloc call has set up the current device, a second probe
+ * does the same on that scratch's status word after incrementing its first
+ * block counter, as a split-K launch cut short can leave it.  Nothing faults
+ * or hangs; the stream is busy for about 0.4 s per probe.  For tests of the
  * error path.  Needs w4a16_init. */
 int w4a16_wait_probe(void *stream);
 

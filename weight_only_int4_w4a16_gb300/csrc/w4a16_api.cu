@@ -444,6 +444,20 @@ struct RoundGraphHandle {
 
 }  // namespace
 
+namespace w4a16 {
+int check_linear_args(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                      const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y,
+                      int epi, const uint16_t *residual, int dtype) {
+    return check_linear(x, qweight, scales, zeros, M, N, K, group, y, epi, residual, dtype);
+}
+
+void count_launches(int rung, unsigned long long linears, unsigned long long kernels) {
+    if (rung >= 0 && rung < W4A16_NUM_RUNGS)
+        g_probe[rung].fetch_add(linears, std::memory_order_relaxed);
+    g_launches.fetch_add(kernels, std::memory_order_relaxed);
+}
+}  // namespace w4a16
+
 extern "C" {
 
 int w4a16_init(int device, size_t workspace_bytes) {
@@ -1151,23 +1165,48 @@ const char *w4a16_status_string(int status) {
 
 int w4a16_device_status(void *stream, int *code) {
     if (code) *code = 0;
-    if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    int h = 0;
-    cudaError_t e = cudaMemcpyAsync(&h, g_state.ws.status, sizeof(int), cudaMemcpyDeviceToHost,
-                                    (cudaStream_t)stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    // the allocation-free linear's scratch on the current device, if a call
+    // has set it up
+    NoAllocScratch na{};
+    int device = 0;
+    const bool have_na = cudaGetDevice(&device) == cudaSuccess && noalloc_scratch(device, &na);
+    if (!g_state.initialized && !have_na) return W4A16_ERR_NOT_INITIALIZED;
+    cudaStream_t st = (cudaStream_t)stream;
+    int h = 0, hn = 0;
+    cudaError_t e = cudaSuccess;
+    if (g_state.initialized)
+        e = cudaMemcpyAsync(&h, g_state.ws.status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && have_na)
+        e = cudaMemcpyAsync(&hn, na.status, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e == cudaSuccess && h != 0)
-        e = cudaMemsetAsync(g_state.ws.status, 0, sizeof(int), (cudaStream_t)stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+        e = cudaMemsetAsync(g_state.ws.status, 0, sizeof(int), st);
+    // an expired wait in the allocation-free kernel may have left a block's
+    // arrival counted and never reduced, or the scheduling words set: zero
+    // them with the word, so that later calls start clean
+    if (e == cudaSuccess && hn != 0) e = cudaMemsetAsync(na.counters, 0, na.counter_bytes, st);
+    if (e == cudaSuccess && hn != 0) e = cudaMemsetAsync(na.status, 0, sizeof(int), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
+    h |= hn;
     if (code) *code = h;
     return h ? W4A16_ERR_DEVICE : W4A16_OK;
 }
 
 int w4a16_wait_probe(void *stream) {
     if (!g_state.initialized) return W4A16_ERR_NOT_INITIALIZED;
-    cudaError_t e = launch_wait_probe(g_state.ws.status, (cudaStream_t)stream);
+    cudaError_t e = launch_wait_probe(g_state.ws.status, nullptr, (cudaStream_t)stream);
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    // the allocation-free linear's scratch, when set up on this device: the
+    // same expired waits report into its word, and its first block counter is
+    // left as a cut-short split-K launch can leave one
+    NoAllocScratch na{};
+    int device = 0;
+    if (e == cudaSuccess && cudaGetDevice(&device) == cudaSuccess &&
+        noalloc_scratch(device, &na)) {
+        e = launch_wait_probe(na.status, na.counters, (cudaStream_t)stream);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 

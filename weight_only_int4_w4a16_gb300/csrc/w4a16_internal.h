@@ -280,7 +280,34 @@ cudaError_t moe_decode_init(const DeviceInfo &dev);
 // ---- expired-wait probe (w4a16_waitprobe.cu) -------------------------------
 constexpr int kErrProbeCounterWait = 4096;  // device status bit: the probe's counter wait expired
 constexpr int kErrProbeBarrierWait = 8192;  // device status bit: the probe's mbarrier wait expired
-cudaError_t launch_wait_probe(int *status, cudaStream_t stream);
+// stale: null, or an arrival counter the probe increments first, leaving it as
+// a split-K launch cut short by an expired wait can leave one (an arrival
+// counted, the block never reduced)
+cudaError_t launch_wait_probe(int *status, unsigned *stale, cudaStream_t stream);
+
+// ---- shared by the entry points (w4a16_api.cu) -----------------------------
+// The argument rules of w4a16_linear (and of the epilogue and dtype variants):
+// a w4a16_status, W4A16_OK when the call may launch.
+int check_linear_args(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                      const uint32_t *zeros, int M, int N, int K, int group, const uint16_t *y,
+                      int epi = kEpiNone, const uint16_t *residual = nullptr,
+                      int dtype = kDtypeF16);
+// Record `linears` linears computed by `rung` and `kernels` kernel launches in
+// the per-rung probe counters and the launch count (w4a16_probe_counts,
+// w4a16_kernel_launches).
+void count_launches(int rung, unsigned long long linears, unsigned long long kernels);
+
+// ---- the allocation-free linear's scratch (w4a16_mma.cu) -------------------
+// Where a device's static scratch keeps its status word and its counters
+// (block arrival counters, then the kernel's scheduling words), once a
+// w4a16_linear_noalloc call has set that device up.
+struct NoAllocScratch {
+    int *status;
+    unsigned *counters;
+    size_t counter_bytes;  // the counters and scheduling words, all zero between launches
+};
+// false when no w4a16_linear_noalloc call has set up `device` yet
+bool noalloc_scratch(int device, NoAllocScratch *out);
 
 // ---- pack / unpack / dequant (w4a16_pack.cu) ------------------------------
 cudaError_t launch_pack(const uint8_t *q, const uint8_t *z, int N, int K, uint32_t *qw,

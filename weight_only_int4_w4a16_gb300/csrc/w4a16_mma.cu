@@ -1127,12 +1127,16 @@ cudaError_t mma_init(const DeviceInfo &dev) {
 // is reserved).  w4a16_linear_noalloc needs neither w4a16_init nor any
 // allocation: its split-K scratch is this statically sized device array.
 namespace {
-constexpr size_t kNoAllocPartialFloats = size_t(1) << 19;  // 2 MB of fp32 partial sums
-constexpr int kNoAllocCounters = 4096;                      // per-block arrival counters
+// 4 MiB of fp32 partial sums: enough for the split every M <= 8 linear of a
+// 27B-class decode layer takes (the largest, the fused gate+up projection
+// K 5120, N 34816 at M = 8, splits K in two: 2.2 MB)
+constexpr size_t kNoAllocPartialFloats = size_t(1) << 20;
+constexpr int kNoAllocCounters = 4096;  // per-block arrival counters
 // partials, then the counters, the kernel's scheduling words and a status word
+constexpr size_t kNoAllocCounterBytes =
+    (size_t)(kNoAllocCounters + w4a16::kMmaSchedWords) * sizeof(unsigned);
 constexpr size_t kNoAllocBytes =
-    kNoAllocPartialFloats * sizeof(float) +
-    (size_t)(kNoAllocCounters + w4a16::kMmaSchedWords + 4) * sizeof(unsigned);
+    kNoAllocPartialFloats * sizeof(float) + kNoAllocCounterBytes + 4 * sizeof(unsigned);
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
@@ -1146,6 +1150,14 @@ struct NoAllocDevice {
 constexpr int kNoAllocMaxDevices = 64;
 NoAllocDevice g_noalloc[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
+
+unsigned *noalloc_counters(unsigned char *scratch) {
+    return reinterpret_cast<unsigned *>(scratch + kNoAllocPartialFloats * sizeof(float));
+}
+int *noalloc_status(unsigned char *scratch) {
+    return reinterpret_cast<int *>(scratch + kNoAllocPartialFloats * sizeof(float) +
+                                   kNoAllocCounterBytes);
+}
 
 // Once per device, with that device current: the scratch's device address
 // (cudaGetSymbolAddress), zeroed counters and status, the kernel attributes.
@@ -1180,19 +1192,27 @@ int noalloc_setup(int device, NoAllocDevice **out) {
 }
 }  // namespace
 
+namespace w4a16 {
+bool noalloc_scratch(int device, NoAllocScratch *out) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    const NoAllocDevice &d = g_noalloc[device];
+    if (!d.ready) return false;
+    out->status = noalloc_status(d.scratch);
+    out->counters = noalloc_counters(d.scratch);
+    out->counter_bytes = kNoAllocCounterBytes;
+    return true;
+}
+}  // namespace w4a16
+
 extern "C" int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight,
                                     const uint16_t *scales, const uint32_t *zeros, int M, int N,
                                     int K, int group, uint16_t *y, void *stream) {
     using namespace w4a16;
-    if (!x || !qweight || !scales || !zeros || !y) return W4A16_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 1 || K > (1 << 22) || K % kGroup != 0) return W4A16_ERR_INVALID_ARG;
-    if (group != kGroup) return W4A16_ERR_UNSUPPORTED;
+    // the argument rules of w4a16_linear, then this entry point's own limit
+    int st = check_linear_args(x, qweight, scales, zeros, M, N, K, group, y);
+    if (st) return st;
     if (M > kMmaMaxTokens) return W4A16_ERR_UNSUPPORTED;
-    if ((uintptr_t)x % 16 || (uintptr_t)qweight % 16 || (uintptr_t)y % 16 ||
-        (uintptr_t)scales % 2 || (uintptr_t)zeros % 4)
-        return W4A16_ERR_MISALIGNED;
-    const uintptr_t x0 = (uintptr_t)x, y0 = (uintptr_t)y;
-    if (x0 < y0 + (size_t)M * N * 2 && y0 < x0 + (size_t)M * K * 2) return W4A16_ERR_INVALID_ARG;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return W4A16_ERR_CUDA;
@@ -1208,12 +1228,15 @@ extern "C" int w4a16_linear_noalloc(const uint16_t *x, const uint32_t *qweight,
     Workspace ws{};
     ws.partials = reinterpret_cast<float *>(nd->scratch);
     ws.partial_bytes = kNoAllocPartialFloats * sizeof(float);
-    ws.counters = reinterpret_cast<unsigned *>(nd->scratch + kNoAllocPartialFloats * sizeof(float));
+    ws.counters = noalloc_counters(nd->scratch);
     ws.n_counters = kNoAllocCounters + kMmaSchedWords;
-    ws.status = reinterpret_cast<int *>(ws.counters + ws.n_counters);
+    ws.status = noalloc_status(nd->scratch);
     LinearArgs a{reinterpret_cast<const __half *>(x), qweight,
                  reinterpret_cast<const __half *>(scales), zeros, reinterpret_cast<__half *>(y), M,
                  N, K};
     e = launch_mma(a, plan, ws, (cudaStream_t)stream);
-    return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+    if (e != cudaSuccess) return W4A16_ERR_CUDA;
+    // one kernel, one linear, under the rung that computed it
+    count_launches(plan.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, 1, 1);
+    return W4A16_OK;
 }

@@ -4,7 +4,10 @@
 // nothing arrives at.  Each wait gives up after its time limit and the thread
 // ORs a status bit into the library's device status word, the same report an
 // expired wait in a production kernel makes; nothing faults, traps or hangs,
-// and the context stays usable.
+// and the context stays usable.  Given an arrival counter, the probe first
+// increments it: what a split-K launch cut short by an expired wait can leave
+// behind (an arrival counted, its block never reduced), so that a test can
+// check that the report of the expiry also clears such counters.
 #include <cuda.h>
 
 #include "w4a16_internal.h"
@@ -17,8 +20,9 @@ using namespace warp_mma;
 
 __device__ unsigned g_never_incremented;  // zero for the life of the module
 
-__global__ void wait_probe_kernel(int *status) {
+__global__ void wait_probe_kernel(int *status, unsigned *stale) {
     __shared__ __align__(8) uint64_t bar;
+    if (stale) atomicAdd(stale, 1u);
     const uint32_t b = dev::smem_u32(&bar);
     mbar_init(b, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -28,8 +32,8 @@ __global__ void wait_probe_kernel(int *status) {
 
 }  // namespace
 
-cudaError_t launch_wait_probe(int *status, cudaStream_t stream) {
-    wait_probe_kernel<<<1, 1, 0, stream>>>(status);
+cudaError_t launch_wait_probe(int *status, unsigned *stale, cudaStream_t stream) {
+    wait_probe_kernel<<<1, 1, 0, stream>>>(status, stale);
     return cudaGetLastError();
 }
 
