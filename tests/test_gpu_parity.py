@@ -230,12 +230,27 @@ def test_varying_sizes_back_to_back(w4):
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, sampled rows
+# full-size workloads, every output compared
 # ---------------------------------------------------------------------------
+# The weights are generated on the device by the seeded generator (equal to the
+# host's, test_synthetic_generator_device_equals_host) and copied to the host
+# for the oracle; the oracle's output for a workload is computed once and
+# shared by every rung that runs it.
+_FULL_REFS = {}
+
+
+def _full_reference(key, x_cpu, qw, s, zw):
+    if key not in _FULL_REFS:
+        _FULL_REFS.clear()  # one workload's reference at a time
+        _FULL_REFS[key] = oracle.linear(si.as_u16(x_cpu), si.as_u32(qw), si.as_u16(s),
+                                        si.as_u32(zw))
+    return _FULL_REFS[key]
+
+
 @pytest.mark.parametrize("rung", [-1] + ALL_RUNGS)
 @pytest.mark.parametrize("M,N,K,cfg", [(1, 34816, 5120, 1), (4, 5120, 17408, 2),
                                        (8, 5120, 17408, 2)])
-def test_full_size_sampled(w4, M, N, K, cfg, rung):
+def test_full_size_full_output(w4, M, N, K, cfg, rung):
     seed = si.config_seed(cfg, 0, M)
     qw, s, zw = si.layer(seed, N, K, device=DEV)
     x = si.x(seed, M, K)
@@ -247,16 +262,13 @@ def test_full_size_sampled(w4, M, N, K, cfg, rung):
                 pytest.skip("rung cannot run this shape")
             raise
     torch.cuda.synchronize()
-    rows = sample_rows(N, 48, seed=cfg)
-    ref = sampled_reference(seed, x, N, K, rows)
-    # max|y_ref| is taken over the sampled rows only: at most the whole
-    # output's maximum, so this bound is the stricter one
-    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"cfg{cfg} M={M}")
+    ref = _full_reference((cfg, M), x, qw, s, zw)
+    assert_close(y, ref, f"cfg{cfg} M={M} rung {rung}")
 
 
 @pytest.mark.parametrize("rung", [-1, 2, 5])
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
-def test_m_sweep_sampled(w4, M, rung):
+def test_m_sweep_full_output(w4, M, rung):
     N, K = 27648, 5120
     seed = si.config_seed(4)
     qw, s, zw = si.layer(seed, N, K, device=DEV)
@@ -269,9 +281,8 @@ def test_m_sweep_sampled(w4, M, rung):
                 pytest.skip("rung cannot run this shape")
             raise
     torch.cuda.synchronize()
-    rows = sample_rows(N, 16, seed=M)
-    ref = sampled_reference(seed, x, N, K, rows)
-    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, f"sweep M={M}")
+    ref = _full_reference((4, M), x, qw, s, zw)
+    assert_close(y, ref, f"sweep M={M} rung {rung}")
 
 
 ROUND_SHAPES = [(5120, 8192), (6144, 5120), (5120, 34816), (17408, 5120)]  # (K, N)
@@ -368,17 +379,45 @@ def test_decode_round_chained_waits(w4, graph):
             assert_close(out, ref, f"chained linear {l} rep {rep}")
 
 
+def _round_reference(L, x_cpu):
+    """The oracle's output of one round linear, from its device weights."""
+    return oracle.linear(si.as_u16(x_cpu), si.as_u32(L["qweight"]), si.as_u16(L["scales"]),
+                         si.as_u32(L["zeros"]))
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_round_m1_m8_full_output(w4, M):
+    # the round at the other ends of the verify range (M = 4 runs below and
+    # in the benchmark): two layers, one fused launch, every output compared
+    layers, xs = _round(w4, 2, M)
+    descs = w4.make_descs(layers)
+    w4.w4a16_probe_reset()
+    w4.w4a16_decode_round(descs, M)
+    torch.cuda.synchronize()
+    assert w4.w4a16_kernel_launches() == 1
+    for L in layers:
+        assert_close(L["y"], _round_reference(L, xs[L["j"]]), f"M={M} round linear j={L['j']}")
+
+
 @pytest.mark.slow
-def test_decode_round_full_64_layers_sampled(w4):
+def test_decode_round_full_64_layers_full_output(w4):
+    # the whole 64-layer round at M = 4: all 256 outputs against the oracle
     M = 4
     layers, xs = _round(w4, 64, M)
     descs = w4.make_descs(layers)
     w4.w4a16_decode_round(descs, M)
     torch.cuda.synchronize()
-    for L in layers:
-        rows = sample_rows(L["N"], 4, seed=L["seed"] & 0xFFFF)
-        ref = sampled_reference(L["seed"], xs[L["j"]], L["N"], L["K"], rows)
-        assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, f"layer seed {L['seed']}")
+    # the premise of copying the device weights to the host: the device
+    # generator gives the host's bits (checked here on one linear's rows)
+    L = layers[-1]
+    rows = sample_rows(L["N"], 8, seed=5)
+    qh, sh, zh = si.layer(L["seed"], L["N"], L["K"], rows=rows)
+    idx = torch.from_numpy(rows).to(DEV)
+    assert torch.equal(L["qweight"][idx].cpu(), qh) and torch.equal(L["zeros"][idx].cpu(), zh)
+    assert torch.equal(L["scales"][idx].cpu().view(torch.int16), sh.view(torch.int16))
+    for i, L in enumerate(layers):
+        assert_close(L["y"], _round_reference(L, xs[L["j"]]), f"round linear {i} (j={L['j']})")
+        layers[i] = None  # release the layer's weights as we go
     del layers
     torch.cuda.empty_cache()
 
