@@ -157,18 +157,63 @@ def build_round(dev, M=M_ROUND, layers=N_LAYERS):
     return lin, xs, xs_dev
 
 
-def time_round(w4, descs, steps, warmup, stream):
+def time_round(w4, descs, steps, warmup, stream, M=M_ROUND):
     for _ in range(warmup):
-        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+        w4.w4a16_decode_round(descs, M, stream=stream)
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(steps):
-        w4.w4a16_decode_round(descs, M_ROUND, stream=stream)
+        w4.w4a16_decode_round(descs, M, stream=stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     return ev0.elapsed_time(ev1) / 1e3
+
+
+def round_at(w4, lin, M, dev):
+    """The same round's weights with x [M, K] and y [M, N] buffers of their own
+    (x drawn from the same seeds as the M = 4 round's)."""
+    import synthetic_inputs as si
+    xs = {j: si.x(si.config_seed(3, 0, 8 + j), M, K).to(dev)
+          for j, (_, K, _) in enumerate(ROUND_SHAPES)}
+    out = []
+    for L in lin:
+        out.append(dict(x=xs[L["j"]], qweight=L["qweight"], scales=L["scales"], zeros=L["zeros"],
+                        y=torch.empty((M, L["N"]), dtype=torch.float16, device=dev)))
+    return out
+
+
+def time_rounds_at(w4, lin, dev, stream, steps, warmup, peak, layers, Ms=(1, 8)):
+    """The decode round at other token counts (the ends of the verify range):
+    ms per round over `steps` back-to-back rounds, GB/s of the round's
+    algorithmic bytes at that M, the fraction of the measured HBM copy rate,
+    and the mean per-launch CUDA-event time of the fused kernel."""
+    out = {}
+    for M in Ms:
+        rl = round_at(w4, lin, M, dev)
+        d = w4.make_descs(rl)
+        w4.w4a16_probe_reset()
+        t = time_round(w4, d, steps, warmup, stream, M=M)
+        launches = w4.w4a16_kernel_launches() // (steps + warmup)
+        evs = []
+        for _ in range(4):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            w4.w4a16_decode_round(d, M, stream=stream)
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        t_l = float(np.mean([a.elapsed_time(b) for a, b in evs])) / 1e3
+        by = round_bytes(M, layers)
+        out[f"M{M}"] = {"ms_per_round": t / steps * 1e3, "GBps": by / (t / steps) / 1e9,
+                        "frac_of_peak": by / (t / steps) / 1e9 / peak,
+                        "mean_launch_us": t_l * 1e6,
+                        "launch_frac_of_peak": by / t_l / 1e9 / peak,
+                        "launches_per_round": int(launches), "round_bytes": by}
+        del rl, d
+    return out
 
 
 def per_kernel_durations(w4, lin, steps, stream):
@@ -474,6 +519,22 @@ def _layer0_host():
     return _LAYER0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (or its implementer / part on Arm)."""
+    try:
+        fields = {}
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+        for k in ("model name", "Model"):
+            if k in fields:
+                return fields[k]
+        return f"implementer {fields.get('CPU implementer', '?')} part {fields.get('CPU part', '?')}"
+    except OSError:
+        return "unknown"
+
+
 def cpu_baseline(seconds_target: float = 12.0):
     """The oracle, as it stands, on all host cores, over a bounded sample of the
     decode round: layer 0's four linears (all rows, M = 4), passed over
@@ -498,6 +559,38 @@ def cpu_baseline(seconds_target: float = 12.0):
             "seconds": t_total}
 
 
+ORACLE_CONFIGS = ([("cfg0_M1_K512_N1024", 1, 1024, 512, 0), ("cfg1_M1_K5120_N34816", 1, 34816, 5120, 1),
+                   ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
+                   ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] +
+                  [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)])
+
+
+def oracle_legs(cores: int):
+    """The oracle, as it stands, on every single-linear workload in full (all
+    outputs), on `cores` host threads, and once more on one thread for the
+    M = 1 gate+up shape: milliseconds and GB/s of the linear's algorithmic
+    bytes."""
+    import oracle
+    import synthetic_inputs as si
+    out = {}
+    cache = {}
+    for label, M, N, K, cfg in ORACLE_CONFIGS:
+        if (N, K, cfg) not in cache:
+            cache.clear()
+            qw, sc, zw = si.layer(si.config_seed(cfg, 0, M), N, K)
+            cache[(N, K, cfg)] = (si.as_u32(qw), si.as_u16(sc), si.as_u32(zw))
+        qw, sc, zw = cache[(N, K, cfg)]
+        x = si.as_u16(si.x(si.config_seed(cfg, 0, M), M, K))
+        by = linear_bytes(M, N, K)
+        runs = [(label, cores)] + ([(label + "_1thread", 1)] if cfg == 1 else [])
+        for name, nt in runs:
+            t0 = time.perf_counter()
+            oracle.linear(x, qw, sc, zw, nthreads=nt)
+            t = time.perf_counter() - t0
+            out[name] = {"ms": t * 1e3, "GBps": by / t / 1e9, "threads": nt}
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -514,7 +607,12 @@ def run_reference(args):
     value = float(np.median(vals))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round_bytes() / (value * 1e9) * 1e3, "higher_is_better": True,
+            # a full round on the host cores would take minutes: each step
+            # times a sample (layer 0's four linears, passed over for about
+            # 6 s), and ms_per_step is a full round's bytes at that rate
+            "ms_per_step": round_bytes() / (value * 1e9) * 1e3,
+            "ms_per_step_extrapolated_from_sample": True,
+            "sample_seconds_per_step": float(np.median(secs)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": base["sample"]},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": base["cores"],
@@ -818,6 +916,14 @@ def main():
         extra["round_bf16_GBps"] = rb / (bms / 1e3) / 1e9
         extra["round_bf16_frac_of_peak"] = rb / (bms / 1e3) / 1e9 / peak
         del blin, bdescs, bxs
+    rounds = None
+    if not args.no_extra and rank == 0:
+        rounds = time_rounds_at(w4, lin, dev, stream, max(10, args.steps // 2), args.warmup, peak,
+                                args.layers)
+        rounds["M4"] = {"ms_per_round": ms, "GBps": value / world, "frac_of_peak": value / world / peak,
+                        "mean_launch_us": roofline["mean_launch_us"],
+                        "launch_frac_of_peak": roofline["frac"], "launches_per_round": per_round,
+                        "round_bytes": rb}
     del lin, descs
     torch.cuda.empty_cache()
 
@@ -862,6 +968,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         cb = cpu_baseline()
         cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["cpu_model"] = cpu_model()
+        cpu["per_config"] = oracle_legs(cb["cores"])
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -873,7 +981,16 @@ def main():
                            "percent_of_hbm_peak": 100.0 * value / world / peak,
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
                 "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-                "clocks": clk, "cpu_baseline": cpu, "extra": extra}
+                "clocks": clk, "cpu_baseline": cpu}
+        # the metric's other parts: the round at M = 1, 4, 8 and the lone
+        # single linears (L2 evicted) at M = 1 / 4 / 8
+        if rounds is not None:
+            line["rounds"] = rounds
+        if "single_linear_l2_flushed" in extra:
+            line["singles"] = {k: {f: v[f] for f in ("us", "GBps", "frac_of_peak", "rung")}
+                               for k, v in extra["single_linear_l2_flushed"].items()
+                               if k.startswith(("cfg1", "cfg2"))}
+        line["extra"] = extra
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
