@@ -53,7 +53,8 @@ def linear_bytes(M: int, N: int, K: int) -> int:
     return N * K // 2 + 2 * N * G + N * G // 2 + 2 * M * K + 2 * M * N
 
 
-def round_bytes(M: int = M_ROUND, layers: int = N_LAYERS) -> int:
+def round_bytes(M: int | None = None, layers: int = N_LAYERS) -> int:
+    M = M_ROUND if M is None else M
     return layers * sum(linear_bytes(M, N, K) for _, K, N in ROUND_SHAPES)
 
 
@@ -133,11 +134,12 @@ class ClockSampler:
 ROUND_KERNEL_TRAFFIC = 11_406_256_640
 
 
-def build_round(dev, M=M_ROUND, layers=N_LAYERS):
+def build_round(dev, M=None, layers=N_LAYERS):
     """The round's linears.  The four inputs are views of one device buffer and
     the 256 outputs views of another (one copy each way per end-to-end step);
     each linear's x and y stay separate tensors to the library."""
     import synthetic_inputs as si
+    M = M_ROUND if M is None else M
     xs = [si.x(si.config_seed(3, 0, 8 + j), M, K) for j, (_, K, _) in enumerate(ROUND_SHAPES)]
     x_all = torch.cat([x.reshape(-1) for x in xs]).to(dev)
     xs_dev, off = [], 0
@@ -157,7 +159,8 @@ def build_round(dev, M=M_ROUND, layers=N_LAYERS):
     return lin, xs, xs_dev
 
 
-def time_round(w4, descs, steps, warmup, stream, M=M_ROUND):
+def time_round(w4, descs, steps, warmup, stream, M=None):
+    M = M_ROUND if M is None else M
     for _ in range(warmup):
         w4.w4a16_decode_round(descs, M, stream=stream)
     torch.cuda.synchronize()
@@ -706,12 +709,16 @@ def run_moe_case(T: int, reps: int):
 
 
 def main():
+    global M_ROUND
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=N_LAYERS)
+    ap.add_argument("--round-m", type=int, default=M_ROUND,
+                    help="tokens of the timed round (the benchmark's workload is M=4; other values "
+                         "are for profiling)")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--case", type=int, nargs=5, metavar=("M", "N", "K", "RUNG", "REPS"),
@@ -739,6 +746,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
         return
+    M_ROUND = args.round_m
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -93,13 +93,18 @@ struct TcPlan {
     bool ok;
     int M;             // real tokens in this launch (1..64)
     int T;             // MMA N: tokens padded to 16, 32 or 64
-    int S;             // K slices
-    int slice_groups;  // groups per slice
+    int S;             // 1: every CTA takes whole 128-row tiles; 2: stream-K (CTAs take equal
+                       // runs of (tile, stage) work and a tile split between CTAs is summed
+                       // by the last of them)
     int n_tiles;       // 128-row weight tiles
-    size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
+    int spt;           // stages (4 groups each) per tile
+    int grid;          // CTAs (one per SM)
+    int stages;        // shared-memory stages in flight per CTA
+    size_t xp_bytes;   // the pair-ordered copy of x the kernel reads
+    size_t ws_bytes;   // workspace: the x copy, then stream-K partial sums
 };
 
-// split: 0 = never split K, 1 = split K, -1 = planner decides.
+// split: 0 = whole tiles only, 1 = stream-K, -1 = planner decides.
 TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev);
 // status: device word the kernel ORs an error code into when a bounded wait expires.
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,

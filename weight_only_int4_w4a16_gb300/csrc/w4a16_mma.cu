@@ -142,7 +142,7 @@ __device__ __forceinline__ void epilogue_store(const Lin &R, size_t o, float h, 
 // rows of the same outputs (the register footprint stays that of 8 sums: the
 // callers keep their registers across this call).
 template <bool kBf16>
-__device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
+__device__ __forceinline__ void reduce_block(const MmaLinDesc &R, int sb) {
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
     const int nrows = min(R.ycols - row0, rows_per_block);
@@ -183,6 +183,96 @@ __device__ __noinline__ void reduce_block(const MmaLinDesc &R, int sb) {
         }
     }
     if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
+}
+
+// The same reduction with the partial sums staged in shared memory.  The sum
+// is latency-bound when each thread loads a few floats per round trip to L2
+// (one slice after another), so each thread first copies its share of the
+// block's slices into shared memory with 16-byte cp.async copies (as many rows
+// at a time as the buffer holds: the staged-x region, free at a unit boundary
+// where x is restaged next), all in flight together and without registers,
+// then each output's slices are summed from shared memory in slice order: the
+// same sums, the same bits as reduce_block.  cp.async goes through the
+// load/store path: bulk copies would queue behind the warps' weight boxes in
+// the SM's copy engine.  Needs rows that start on 16-byte boundaries (N a
+// multiple of 4, 16-byte aligned partial sums); returns false otherwise, or
+// when the buffer holds fewer than 4 rows, without touching anything.
+template <bool kBf16>
+__device__ __forceinline__ bool reduce_block_staged(const MmaLinDesc &R, int sb, uint8_t *buf,
+                                                    uint32_t buf_bytes) {
+    if (R.N % 4 != 0 || ((uintptr_t)R.partials & 15) != 0) return false;
+    const int rows_per_block = kWarps * R.strips_per_warp * 16;
+    const int row0 = sb * rows_per_block;
+    const int nrows = min(R.ycols - row0, rows_per_block);  // a multiple of 4 here
+    const int nh = R.epi == kEpiSiluMul ? 2 : 1;            // gate rows, then up rows
+    const size_t up = (size_t)R.half_strips * 16;
+    const uint32_t per_row = (uint32_t)(R.S * R.M * nh) * 4u;
+    int C = (int)(buf_bytes / per_row) & ~3;
+    if (C < 4) return false;
+    if (C > nrows) C = nrows;
+    const int ncopies = R.S * R.M * nh;
+    const uint32_t buf_s = dev::smem_u32(buf);
+    for (int r0 = 0; r0 < nrows; r0 += C) {
+        const int c = min(C, nrows - r0);
+        const int q4 = c >> 2;  // 16-byte pieces per copied row segment
+        // piece j: segment i = j / q4 (slice s, token t, gate or up rows h, i =
+        // (s * M + t) * nh + h), 4 sums from row r0 + 4 (j % q4); it lands at
+        // buf[i][4 (j % q4) ...]
+        for (int j = threadIdx.x; j < ncopies * q4; j += kThreads) {
+            const int i = j / q4, e = 4 * (j - i * q4);
+            const int h = i % nh, st = i / nh;
+            const float *src = R.partials + (size_t)st * R.N + row0 + r0 + e + (h ? up : 0);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             buf_s + (uint32_t)((i * c + e) * 4)),
+                         "l"(src)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        const float *f = reinterpret_cast<const float *>(buf);
+        for (int i = threadIdx.x; i < R.M * c; i += kThreads) {
+            const int t = i / c, rr = i - t * c;
+            float sum = 0.f, gate = 0.f;
+            for (int s2 = 0; s2 < R.S; ++s2) {
+                const float *b = f + (size_t)((s2 * R.M + t) * nh) * c + rr;
+                if (nh == 2) {
+                    gate += b[0];
+                    sum += b[c];
+                } else {
+                    sum += b[0];
+                }
+            }
+            epilogue_store<kBf16>(R, (size_t)t * R.ycols + row0 + r0 + rr, sum, gate);
+        }
+        // every thread's reads of the chunk come before the next chunk's copies
+        // (and before the next x copy, which writes through the async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) R.counters[sb] = 0u;  // ready for the next launch
+    return true;
+}
+
+// One call site for the kernel, with few arguments (the callers keep their
+// registers across it).  A launch of one linear takes the staged reduction
+// where the staged-x region is free (x_free: the next unit restages x, or
+// none follows) and the rows allow it: there the reduction sits on the
+// launch's critical path (config K 17408, N 5120 at M = 4: 32.8 -> 30.7 us).
+// A fused round keeps the register path: in A/B runs of the 64-layer round
+// the staged form was 1-2% slower at every M (its reductions overlap the
+// other CTAs' streaming, and the copies wait with the weight traffic).  The
+// buffer comes from the CTA's shared-memory layout.
+template <bool kRound, bool kBf16>
+__device__ __noinline__ void reduce_any(const MmaLinDesc &R, int sb, int x_free) {
+    if constexpr (!kRound) {
+        extern __shared__ __align__(128) uint8_t smem[];
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        if (x_free && reduce_block_staged<kBf16>(R, sb, smem + kRingBytes + kBarBytes,
+                                                 dyn - (uint32_t)(kRingBytes + kBarBytes)))
+            return;
+    }
+    reduce_block<kBf16>(R, sb);
 }
 
 template <bool kRound, bool kBf16>
@@ -517,10 +607,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         red_pending = true;
         arr_l = -1;
     };
-    // all threads, after the barrier that follows publish_reduction(boundary)
-    auto maybe_reduce = [&](int boundary) {
+    // all threads, after the barrier that follows publish_reduction(boundary).
+    // x_free: the staged x is not needed again (the next unit restages it, or
+    // no unit follows), so the reduction may stage partial sums over it: every
+    // warp has passed the barrier after its last read, and no x copy is in
+    // flight at a boundary
+    auto maybe_reduce = [&](int boundary, bool x_free) {
         volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
-        if (f[0]) reduce_block<kBf16>(desc(f[1]), f[2]);
+        if (f[0]) reduce_any<kRound, kBf16>(desc(f[1]), f[2], x_free ? 1 : 0);
     };
 
     // boundary b: the barrier at the top of iteration b (b = k), or an extra
@@ -563,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 dead = true;
                 break;
             }
-            maybe_reduce(bnd++);
+            maybe_reduce(bnd++, restage || !have);
         } else if (vflags[kFlagAbort]) {
             dead = true;
             break;
@@ -582,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             count_arrival();
             publish_reduction(bnd);
             __syncthreads();
-            maybe_reduce(bnd++);
+            maybe_reduce(bnd++, restage);  // a new linear: x is restaged
             __syncthreads();
             if (threadIdx.x == 0) {
                 __threadfence();
@@ -858,11 +952,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         publish_reduction(bnd);
         red_pending = false;
         __syncthreads();
-        maybe_reduce(bnd++);
+        maybe_reduce(bnd++, true);
         count_arrival();
         publish_reduction(bnd);
         __syncthreads();
-        maybe_reduce(bnd++);
+        maybe_reduce(bnd++, true);
     }
     if (P.dynamic || (kRound && P.done)) {
         __syncthreads();

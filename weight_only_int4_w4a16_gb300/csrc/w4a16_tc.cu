@@ -1,41 +1,50 @@
-// tcgen05 dequant-GEMM for W4A16 (rungs "tc" and "tc_splitk").
+// tcgen05 dequant-GEMM for W4A16 (rungs "tc" and "tc_splitk"), 9..64 tokens.
 //
-// The method is the same linear as the CUDA-core rungs (forum.sourcefind.cn
+// The method is the same linear as the other rungs (forum.sourcefind.cn
 // thread "vLLM on Hygon Z100", section 四: unpack the INT4 words, restore
 // (q - z) * s, multiply-accumulate with fp16 activations in fp32).  Section 七
 // of the thread notes that once M grows the GEMV is no longer the right shape
 // and the crossover to a GEMM path has to be measured; this is the GEMM path,
-// written for the sm_103a tensor cores:
+// written for the sm_103a tensor cores.
 //
-//   MMA shape (swap AB): the MMA's M = 128 weight rows n of one tile, its
-//   N = T tokens (16, 32 or 64; M is padded up with zero rows of x), K = 16
-//   per instruction, fp16 inputs, fp32 accumulation in tensor memory.
+//   MMA shape (swap AB): the MMA's M = 128 weight rows of one tile, its N = T
+//   tokens (16, 32 or 64; missing tokens are zero rows of x), K = 16 per
+//   instruction, fp16 inputs, fp32 accumulation in tensor memory.
 //
-//   warp 20 (one thread) streams packed weights with TMA: one box of
-//     128 rows x 64 bytes (one 128-wide group) per stage, 64-byte swizzle;
-//   warps 4..19, two teams of 8 taking alternate groups, unpack a stage:
-//     thread = one row (its TMEM lane), two warps per 32-lane quarter split
-//     the group's 128 k in halves.  The nibble
-//     unpack is the exponent-bias one of the CUDA-core rung ((1024 + q) and
-//     (64 + q) spliced into fp16, minus (1024 + z) / (64 + z), exact), and
-//     the exact fp16 (q - z) values go to tensor memory with tcgen05.st as
-//     the MMA's A operand.  The same warps stage the group's slice of x in
-//     shared memory (canonical K-major layout, no swizzle), in the pair order
-//     the unpack produces, as the MMA's B operand;
+//   The restore step writes A = (q - z) * s as fp16, rounded once from the
+//   exact product (the pages' "restore to fp16" before the multiply, and the
+//   fp16 result w4a16_dequant defines): the scale is inside the MMA operand,
+//   so one accumulator collects every group of a K range and is read once,
+//   where a per-group fp32 scale would read the accumulator after every group.
+//   The product fits fp16 while |s| < 4096; a row whose scales reach that
+//   (or are Inf or NaN) has its outputs of the K range recomputed exactly on
+//   the CUDA cores by its epilogue thread (w = (q - z) * s in fp32, exact), so
+//   every finite scale gives the method's result.
+//
+//   Roles (one CTA per SM, 736 threads):
+//   warp 20 (one thread) streams with TMA, per stage, a box of 128 rows x 4
+//     groups of packed weights (each row a 256-byte run of memory, 64-byte
+//     swizzle; L2 evict-first, read once) and the stage's 512 inputs of x for
+//     all T tokens.  x comes from a copy made by tc_prep_kernel just before,
+//     with each 8-element chunk in the order the unpack yields the nibbles of
+//     a word, (x0,x4) (x1,x5) (x2,x6) (x3,x7), so the TMA box lands in the
+//     MMA's canonical K-major layout;
+//   warps 4..19, two teams of 8 taking alternate groups, restore a group:
+//     thread = one row (its TMEM lane) and 64 inputs; the nibble unpack splices
+//     (1024 + q) or (64 + q) into fp16, subtracts the matching (1024 + z) /
+//     (64 + z) exactly and multiplies by s (one rounding); tcgen05.st puts the
+//     values in tensor memory as the MMA's A operand (a ring of 4 buffers);
 //   warps 21 and 22 (one thread each) take alternate groups and issue a
-//     group's 8 tcgen05.mma into a fresh fp32 accumulator in tensor memory
-//     (one accumulator per group, ring of 4), then commit to mbarriers.  At
-//     N = 16 one issuing thread spends ~85 cycles per instruction while the
-//     tensor pipe idles most of the time; two issuers cut M = 16 from 63.5
-//     to 49 us.  Each A buffer (ring of 4) and each accumulator belongs to
-//     one team and one issuer, so every barrier's phases are consumed in
-//     order by a single waiter;
-//   warps 0..3 read each group's accumulator with tcgen05.ld and add
-//     s[n, g] * acc into fp32 registers.  The scale is applied in fp32 per
-//     group, so the tensor-core products (q - z) * x are exact and only the
-//     fp32 sums round;
-//   split K: slices of whole groups per CTA; the last CTA of a tile sums the
-//     fp32 partials in slice order (same scheme as the CUDA-core rung).
+//     group's 8 tcgen05.mma into their own accumulator chain (so the sums of
+//     each chain come in a fixed order), then commit;
+//   warps 0..3 (thread = row) read both chains once per K range, add them,
+//     and write y, or, for a K range that is part of a tile, fp32 partial sums
+//     that the last CTA of the tile adds in K order.
+//
+//   Work: CTAs take equal runs of the (tile, stage) sequence ("stream-K"), so
+//   that every SM streams the same number of bytes however the tiles divide
+//   among the SMs; a tile split between CTAs is summed by the last of them in
+//   K order (deterministic).  Without the split, CTAs take whole tiles in turn.
 //
 // Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
 // an error code in device memory, every role drains what it has in flight
@@ -49,79 +58,75 @@
 namespace w4a16 {
 namespace {
 
-constexpr int kTileN = 128;                      // weight rows per tile (MMA M)
-constexpr int kChunkWords = kGroup / 8;          // 16 words = 64 bytes per row per group
-constexpr int kStageBytes = kTileN * kChunkWords * 4;  // 8 KB per TMA stage
-constexpr int kPStages = 12;                     // packed-weight stages in flight (96 KB)
-constexpr int kAStages = 4;                      // A (dequantised group) buffers in TMEM
-constexpr int kDStages = 4;                      // per-group accumulator sets in TMEM
-constexpr int kDCols = 64;                       // TMEM columns per accumulator set
-constexpr int kACols = kGroup / 2;               // TMEM columns per A buffer (2 fp16 / column)
-constexpr int kXAhead = 2;                       // a team's groups of x fetched ahead (cp.async)
+constexpr int kTileN = 128;                    // weight rows per tile (MMA M)
+constexpr int kSG = 4;                         // groups per stage (one TMA box)
+constexpr int kGroupBytes = kTileN * 64;       // 8 KB of packed weights per group
+constexpr int kStageW = kSG * kGroupBytes;     // 32 KB
+constexpr int kAStages = 4;                    // A (restored group) buffers in TMEM
+constexpr int kACols = kGroup / 2;             // 64 TMEM columns per A buffer
 constexpr int kEpiWarps = 4;
-constexpr int kDeqTeams = 2;                     // dequant teams take alternate groups
-constexpr int kDeqWarps = 8;                     // warps per team (2 per TMEM lane quarter)
+constexpr int kDeqTeams = 2;                   // restore teams take alternate groups
+constexpr int kDeqWarps = 8;                   // warps per team (2 per TMEM lane quarter)
 constexpr int kTmaWarp = kEpiWarps + kDeqTeams * kDeqWarps;  // 20
-constexpr int kMmaWarp = kTmaWarp + 1;                       // 21
-constexpr int kMmaWarps = 2;                                 // MMA issuers, alternate groups
-constexpr int kThreads = (kMmaWarp + kMmaWarps) * 32;        // 736
+constexpr int kMmaWarp = kTmaWarp + 1;                       // 21 .. 24
+constexpr int kMmaWarps = 4;                                 // MMA issuers: group c to c % 4
+constexpr int kThreads = (kMmaWarp + kMmaWarps) * 32;        // 800
+constexpr int kTmemCols = 512;
+constexpr int kMaxStages = 6;
+constexpr int kSmemBudget = 220 * 1024;        // weight stages and the x ring
+static_assert(kMmaWarps == kAStages, "issuer i owns A buffer i (and x slot i)");
+// the mbarriers (full, empty per stage; a_full, a_empty, x_full per A buffer;
+// d_full, d_empty; done), then the tensor-memory address, abort and last flags
+constexpr int kBarBytes = (2 * kMaxStages + 3 * kAStages + 5) * 8 + 16;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
+constexpr uint32_t kBigScale = 0x6C00u;        // |s| >= 4096 (bits of |s|): exact path
 
 // error codes recorded in the device status word (bit flags)
 constexpr int kErrWaitFull = 1, kErrWaitAFull = 2, kErrWaitDFull = 4, kErrWaitEmpty = 8,
               kErrWaitAEmpty = 16, kErrWaitDEmpty = 32, kErrDrain = 64;
 
 struct TcParams {
-    CUtensorMap tmap;  // qweight as a 2-D tensor of uint32: {K/8, N}
-    const __half *x;
+    CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 128, 4}
+    CUtensorMap xmap;  // pair-ordered x 3-D: (8 halves, M tokens, K/8 chunks), box {8, T, 64}
+    const __half *x;   // x as given (the exact path)
+    const uint32_t *qw;
     const __half *scales;
     const uint32_t *zeros;
     __half *y;
-    float *partials;
-    unsigned *counters;
+    float *partials;     // stream-K: [2 * grid][M][128] fp32
+    unsigned *counters;  // stream-K: one per tile, zero between launches
     int *status;
-    int N, K, G, ZW;
-    int M;             // real tokens in this launch (<= T)
-    int S, slice_groups;
+    int N, K, G, ZW, M;
+    int n_tiles, spt;  // tiles, stages per tile
+    int streamk;
+    int n_stages;      // shared-memory stages
+    long long total;   // n_tiles * spt
 };
 
 template <int T>
 struct TcConfig {
-    static constexpr int kXBytes = T * kGroup * 2;          // one group of x, T tokens
-    // A group's 8 MMAs go round-robin into kChains independent accumulators
-    // (T columns each) so that consecutive MMAs do not wait on one another;
-    // the epilogue adds the chains.
-    static constexpr int kChains = kDCols / T;               // 4, 2, 1
-    static constexpr int kDBase = kAStages * kACols;         // 192
-    static constexpr int kColsUsed = kDBase + kDStages * kDCols;
-    static constexpr int kTmemCols = kColsUsed <= 256 ? 256 : 512;
-    static constexpr int kSmemP = kPStages * kStageBytes;
-    static constexpr int kSmemX = kAStages * kXBytes;
-    static constexpr int kSmemXRaw = kDeqTeams * kXAhead * kXBytes;  // x copies in flight
-    static constexpr int kSmemBar = 1024;
-    static constexpr int kSmemBytes = 1024 /*align slack*/ + kSmemP + kSmemX + kSmemXRaw + kSmemBar;
-    static constexpr int kPiecesPerThread = T * 16 / (kDeqWarps * 32);  // 16-byte x pieces
+    // x of one group for T tokens: a slot of the x ring (one per A buffer)
+    static constexpr int kXSlot = T * kGroup * 2;
+    static constexpr int kXRing = kAStages * kXSlot;
+    // per row: the 3 aligned words holding its 4 scales of the stage, then the
+    // zeros word holding its 4 zeros
+    static constexpr int kMeta = kTileN * 16;
+    static constexpr int kStageBytes = kStageW + kMeta;
+    static constexpr int kDBase = kAStages * kACols;      // 256: accumulators after A
+    // Each issuer spreads a group's 8 MMAs over kChains independent
+    // accumulators (k step kk into chain kk % kChains), so that consecutive MMAs
+    // do not wait on one another's sums; an accumulator set holds every
+    // issuer's chains, [issuer][chain][T columns]: 128 columns for T <= 32
+    // (two sets, so that a K range's sums are read while the next one's run),
+    // 256 for T = 64 (one set)
+    static constexpr int kChains = T == 16 ? 2 : 1;
+    static constexpr int kDBuf = kMmaWarps * kChains * T;
+    static constexpr int kDSets = T == 64 ? 1 : 2;
+    static_assert(kDBase + kDSets * kDBuf <= kTmemCols, "tensor memory");
     // instruction descriptor: D f32, A f16, B f16, both K-major, N = T, M = 128
     static constexpr uint32_t kIdesc =
         (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
 };
-
-// Optional section timers (build with -DW4A16_TRACE): CTA (0, 0) records the
-// SM cycle counter at each pipeline event of its first kTraceChunks groups.
-#ifdef W4A16_TRACE
-constexpr int kTraceChunks = 32;
-constexpr int kTraceEvents = 9;
-__device__ unsigned long long g_trace[kTraceEvents * kTraceChunks];
-#define W4A16_TR(ev, c)                                                                   \
-    do {                                                                                  \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < kTraceChunks)                     \
-            g_trace[(ev) * kTraceChunks + (c)] = clock64();                               \
-    } while (0)
-#else
-#define W4A16_TR(ev, c) \
-    do {                \
-    } while (0)
-#endif
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -175,18 +180,38 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// The same wait, bounded by time alone (draining after an abort).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kWaitNs) return false;
+    return true;
+}
+
 __device__ __forceinline__ void fail(volatile int *abort, int *status, int code) {
     *abort = 1;
     atomicOr(status, code);
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// 4-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// the barrier's pending count drops by one once this thread's earlier cp.async
+// copies have landed
+__device__ __forceinline__ void cp_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -225,29 +250,29 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
-
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
 
-__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&v)[32]) {
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-        "%29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        "r"(v[15])
         : "memory");
 }
 
@@ -264,21 +289,6 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-// 16-byte global -> shared copy that bypasses registers; src_bytes 0 writes zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -286,15 +296,122 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 8 consecutive fp16 x values -> (x0,x4) (x1,x5) (x2,x6) (x3,x7): the order in
-// which the unpack yields the nibbles of one word.
-__device__ __forceinline__ uint4 pair_order(uint4 v) {
-    uint4 o;
-    o.x = prmt(v.x, v.z, 0x5410);
-    o.y = prmt(v.x, v.z, 0x7632);
-    o.z = prmt(v.y, v.w, 0x5410);
-    o.w = prmt(v.y, v.w, 0x7632);
-    return o;
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// the CTA's work: segments (a tile and a run of its stages), in order
+// ---------------------------------------------------------------------------
+struct Walk {
+    long long pos, end;  // stream-K: the CTA's stage range
+    int tile;            // whole tiles: the current tile
+    bool started;
+};
+
+__device__ __forceinline__ long long range_begin(const TcParams &p, int b) {
+    return (long long)b * p.total / gridDim.x;
+}
+
+__device__ __forceinline__ void walk_init(const TcParams &p, Walk &w) {
+    w.pos = range_begin(p, blockIdx.x);
+    w.end = range_begin(p, blockIdx.x + 1);
+    w.tile = blockIdx.x;
+    w.started = false;
+}
+
+// next segment: tile t, stages [j0, j1) of it; false when the CTA is done
+__device__ __forceinline__ bool walk_next(const TcParams &p, Walk &w, int &t, int &j0, int &j1) {
+    if (p.streamk) {
+        if (w.pos >= w.end) return false;
+        t = (int)(w.pos / p.spt);
+        j0 = (int)(w.pos - (long long)t * p.spt);
+        const long long tile_end = (long long)(t + 1) * p.spt;
+        const long long e = tile_end < w.end ? tile_end : w.end;
+        j1 = (int)(e - (long long)t * p.spt);
+        w.pos = e;
+        return true;
+    }
+    if (w.started) w.tile += gridDim.x;
+    w.started = true;
+    if (w.tile >= p.n_tiles) return false;
+    t = w.tile;
+    j0 = 0;
+    j1 = p.spt;
+    return true;
+}
+
+// groups of stage j: [4j, min(4j + 4, G))
+__device__ __forceinline__ int stage_groups(const TcParams &p, int j) {
+    return min(kSG, p.G - kSG * j);
+}
+
+// The CTA whose range holds stage st (stream-K).
+__device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
+    return (int)(((st + 1) * (long long)gridDim.x - 1) / p.total);
+}
+
+// ---------------------------------------------------------------------------
+// x in the unpack's pair order: the copy tc_kernel reads
+// ---------------------------------------------------------------------------
+__global__ void tc_prep_kernel(const __half *__restrict__ x, __half *__restrict__ xp, int M, int K) {
+    grid_dependents_launch();
+    // the previous kernel in the stream may still read xp
+    grid_dependency_wait();
+    const long long chunks = (long long)M * (K / 8);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
+         i += (long long)gridDim.x * blockDim.x) {
+        const uint4 v = reinterpret_cast<const uint4 *>(x)[i];
+        uint4 o;
+        o.x = prmt(v.x, v.z, 0x5410);  // (x0, x4)
+        o.y = prmt(v.x, v.z, 0x7632);  // (x1, x5)
+        o.z = prmt(v.y, v.w, 0x5410);  // (x2, x6)
+        o.w = prmt(v.y, v.w, 0x7632);  // (x3, x7)
+        reinterpret_cast<uint4 *>(xp)[i] = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The outputs of row n over groups [g0, g1) for every token, exactly: w =
+// (q - z) * s in fp32 (at most 15 significant bits), summed in increasing k,
+// 16 tokens at a time; to y (a whole tile) or to the partial-sum slot `part`
+// (row n's column of it).  For rows whose scales reach 4096 (or are Inf or
+// NaN), where the fp16 restore of the tensor-core path may overflow.  Kept
+// out of line: it is rare, and its registers stay out of the kernel's.
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1, bool whole,
+                                       float *part) {
+    const uint32_t *qrow = p.qw + (size_t)n * (p.K / 8);
+    for (int t0 = 0; t0 < p.M; t0 += 16) {
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int g = g0; g < g1; ++g) {
+            const float sc = __half2float(p.scales[(size_t)n * p.G + g]);
+            const int z = (int)((p.zeros[(size_t)n * p.ZW + (g >> 3)] >> (4 * (g & 7))) & 0xfu);
+            for (int wd = 0; wd < kGroup / 8; ++wd) {
+                const uint32_t word = qrow[g * (kGroup / 8) + wd];
+                for (int nb = 0; nb < 8; ++nb) {
+                    const int k = g * kGroup + wd * 8 + nb;
+                    const float wv = (float)((int)((word >> (4 * nb)) & 0xfu) - z) * sc;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (t0 + i < p.M)
+                            acc[i] = fmaf(wv, __half2float(p.x[(size_t)(t0 + i) * p.K + k]), acc[i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int tt = t0 + i;
+            if (tt >= p.M) break;
+            if (whole) p.y[(size_t)tt * p.N + n] = __float2half_rn(acc[i]);
+            else part[(size_t)tt * kTileN] = acc[i];
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -305,50 +422,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     using C = TcConfig<T>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sm_p = smem;                   // packed stages
-    uint8_t *sm_x = smem + C::kSmemP;       // x buffers (MMA operand layout)
-    uint8_t *sm_xraw = sm_x + C::kSmemX;    // x copies in flight (row-major pieces)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_xraw + C::kSmemXRaw);
-    uint64_t *full = bars;                          // [kPStages]
-    uint64_t *empty = full + kPStages;              // [kPStages]
-    uint64_t *a_full = empty + kPStages;            // [kAStages]
-    uint64_t *a_empty = a_full + kAStages;          // [kAStages]
-    uint64_t *d_full = a_empty + kAStages;          // [kDStages]
-    uint64_t *d_empty = d_full + kDStages;          // [kDStages]
-    uint64_t *done = d_empty + kDStages;            // [1]
+    const int NS = p.n_stages;
+    uint8_t *sm_x = smem;                   // the x ring: kAStages slots of one group
+    uint8_t *sm_stage = smem + C::kXRing;   // NS weight stages (32 KB, then the metadata)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm_stage + (size_t)NS * C::kStageBytes);
+    uint64_t *full = bars;                     // [kMaxStages] weight stage landed
+    uint64_t *empty = full + kMaxStages;       // [kMaxStages] weight stage read
+    uint64_t *a_full = empty + kMaxStages;     // [kAStages] A restored
+    uint64_t *a_empty = a_full + kAStages;     // [kAStages] A and x slot free (MMAs done)
+    uint64_t *x_full = a_empty + kAStages;     // [kAStages] x slot landed
+    uint64_t *d_full = x_full + kAStages;      // [2]
+    uint64_t *d_empty = d_full + 2;            // [2]
+    uint64_t *done = d_empty + 2;              // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *s_last = const_cast<int *>(abort + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x, slice = blockIdx.y;
-    const int g0 = slice * p.slice_groups;
-    const int g1 = min(p.G, g0 + p.slice_groups);
-    const int nchunks = g1 - g0;
+    grid_dependents_launch();
 
     if (threadIdx.x == kTmaWarp * 32) {
-        for (int i = 0; i < kPStages; ++i) {
-            mbar_init(smem_u32(full + i), 1);
-            mbar_init(smem_u32(empty + i), kDeqWarps);
+        for (int i = 0; i < NS; ++i) {
+            // the TMA bytes (one arrival), then each producer lane's metadata copies
+            mbar_init(smem_u32(full + i), 1 + 32);
+            mbar_init(smem_u32(empty + i), kDeqTeams * kDeqWarps);  // every restore warp
         }
         for (int i = 0; i < kAStages; ++i) {
             mbar_init(smem_u32(a_full + i), kDeqWarps);
             mbar_init(smem_u32(a_empty + i), 1);
+            mbar_init(smem_u32(x_full + i), 1);
         }
-        for (int i = 0; i < kDStages; ++i) {
-            mbar_init(smem_u32(d_full + i), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(d_full + i), kMmaWarps);
             mbar_init(smem_u32(d_empty + i), kEpiWarps);
         }
         mbar_init(smem_u32(done), kMmaWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmap))
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.wmap))
+                     : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap))
                      : "memory");
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_slot)),
-                     "r"(C::kTmemCols)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -357,284 +476,362 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    Walk wk;
+    walk_init(p, wk);
+    int t = 0, j0 = 0, j1 = 0;
+
     if (warp == kTmaWarp) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kPStages;
-                if (!mbar_wait(smem_u32(empty + s), ((c / kPStages) & 1) ^ 1, abort)) {
-                    fail(abort, p.status, kErrWaitEmpty);
+        // ------------------------------------------------ weight producer
+        // Lane 0 issues the TMA boxes; every lane copies, for 4 rows of the
+        // tile, the stage's scale and zeros words (cp.async, completing on the
+        // stage's barrier like the boxes).  A scale word past the end of the
+        // array, or of a row past N, becomes zeros and reads nothing.
+        uint64_t pol = 0;
+        if (lane == 0)  // the weights are read once
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+        const uintptr_t s_end = (uintptr_t)(p.scales + (size_t)p.N * p.G);
+        const void *s_any = p.scales;  // a valid source for zero-byte copies
+        int sc = 0;  // stages issued
+        bool ok = true;
+        while (ok && walk_next(p, wk, t, j0, j1)) {
+            for (int j = j0; j < j1; ++j, ++sc) {
+                const int s = sc % NS;
+                if (sc >= NS &&
+                    !__all_sync(0xffffffffu, mbar_wait(smem_u32(empty + s), ((sc / NS) - 1) & 1,
+                                                       abort))) {
+                    if (lane == 0) fail(abort, p.status, kErrWaitEmpty);
+                    ok = false;
                     break;
                 }
-                W4A16_TR(0, c);
-                mbar_arrive_expect_tx(smem_u32(full + s), kStageBytes);
-                tma_load_2d(smem_u32(sm_p + s * kStageBytes), &p.tmap, (g0 + c) * kChunkWords,
-                            tile * kTileN, smem_u32(full + s));
-                issued = c + 1;
-            }
-            // drain: every issued copy must have landed before the CTA exits
-            for (int c = issued - kPStages > 0 ? issued - kPStages : 0; c < issued; ++c) {
-                if (!mbar_wait(smem_u32(full + c % kPStages), (c / kPStages) & 1, abort) &&
-                    !mbar_try_wait(smem_u32(full + c % kPStages), (c / kPStages) & 1)) {
-                    // bounded second chance independent of the abort flag
-                    const unsigned long long t0 = globaltimer();
-                    bool ok = false;
-                    while (!ok && globaltimer() - t0 < kWaitNs)
-                        ok = mbar_try_wait(smem_u32(full + c % kPStages), (c / kPStages) & 1);
-                    if (!ok) atomicOr(p.status, kErrDrain);
+                const uint32_t bar = smem_u32(full + s);
+                uint8_t *st = sm_stage + (size_t)s * C::kStageBytes;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, (uint32_t)kStageW);
+                    tma_load_3d(smem_u32(st), &p.wmap, 0, t * kTileN, kSG * j, bar, pol);
                 }
+                uint8_t *m = st + kStageW;
+#pragma unroll
+                for (int i = 0; i < kTileN / 32; ++i) {
+                    const int r = lane + 32 * i, n = t * kTileN + r;
+                    const uint32_t dst = smem_u32(m + r * 16);
+                    if (n < p.N) {
+                        const uintptr_t a0 =
+                            (uintptr_t)(p.scales + (size_t)n * p.G + kSG * j) & ~(uintptr_t)3;
+#pragma unroll
+                        for (int w = 0; w < 3; ++w) {
+                            const uintptr_t a = a0 + 4 * w;
+                            cp4(dst + 4 * w, a < s_end ? (const void *)a : s_any,
+                                a < s_end ? 4u : 0u);
+                        }
+                        cp4(dst + 12, p.zeros + (size_t)n * p.ZW + (kSG * j) / 8, 4u);
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) cp4(dst + 4 * w, s_any, 0u);
+                    }
+                }
+                cp_arrive_noinc(bar);
             }
         }
+        // drain: every issued copy must have landed before the CTA exits
+        if (lane == 0)
+            for (int c = sc - NS > 0 ? sc - NS : 0; c < sc; ++c)
+                if (!mbar_wait_drain(smem_u32(full + c % NS), (c / NS) & 1))
+                    atomicOr(p.status, kErrDrain);
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp >= kMmaWarp) {
-        // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuers
         if (lane == 0) {
-            for (int c = warp - kMmaWarp; c < nchunks; c += kMmaWarps) {
-                const int a = c % kAStages, d = c % kDStages;
-                if (!mbar_wait(smem_u32(a_full + a), (c / kAStages) & 1, abort)) {
-                    fail(abort, p.status, kErrWaitAFull);
-                    break;
-                }
-                W4A16_TR(4, c);
-                if (!mbar_wait(smem_u32(d_empty + d), ((c / kDStages) & 1) ^ 1, abort)) {
+            const int me = warp - kMmaWarp;  // groups c with c % 4 == me: A buffer and x slot me
+            int c = 0, q = 0;                // groups, segments seen
+            bool ok = true;
+            const uint32_t xb = smem_u32(sm_x + me * C::kXSlot);
+            while (ok && walk_next(p, wk, t, j0, j1)) {
+                const int dset = q % C::kDSets, duse = q / C::kDSets;
+                if (!mbar_wait(smem_u32(d_empty + dset), (duse & 1) ^ 1, abort)) {
                     fail(abort, p.status, kErrWaitDEmpty);
                     break;
                 }
                 tc_fence_after();
-                W4A16_TR(5, c);
-                const uint32_t xb = smem_u32(sm_x + a * C::kXBytes);
-                const uint32_t d_tmem = tmem + C::kDBase + d * kDCols;
-                const uint64_t bdesc0 = smem_desc_kmajor(xb, 128, 2048);
+                const uint32_t d_tmem =
+                    tmem + C::kDBase + dset * C::kDBuf + me * C::kChains * T;
+                bool first = true;  // this issuer's first MMAs of the segment start its chains
+                const int ng = min(p.G, kSG * j1) - kSG * j0;
+                for (int gi = 0; gi < ng; ++gi, ++c) {
+                    if ((c & (kMmaWarps - 1)) != me) continue;
+                    const uint32_t use = (uint32_t)(c / kAStages) & 1;
+                    if (!mbar_wait(smem_u32(a_full + me), use, abort)) {
+                        fail(abort, p.status, kErrWaitAFull);
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(smem_u32(x_full + me), use, abort)) {
+                        fail(abort, p.status, kErrWaitFull);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < kGroup / 16; ++j) {
-                    // k step j: B advances 256 bytes (two 8x8 core matrices);
-                    // accumulator chain j % kChains starts fresh on its first step
-                    mma_f16_ts(d_tmem + (j % C::kChains) * T, tmem + a * kACols + 8 * j,
-                               bdesc0 + (uint64_t)(16 * j), C::kIdesc, j >= C::kChains);
+                    for (int kk = 0; kk < kGroup / 16; ++kk) {
+                        // x chunks 2 kk, 2 kk + 1 of the slot: core matrices T x 16
+                        // bytes apart along K, 8 tokens 128 bytes apart along N
+                        const uint64_t bdesc =
+                            smem_desc_kmajor(xb + (uint32_t)(2 * kk * T * 16), T * 16, 128);
+                        // chain kk % kChains starts fresh with this issuer's first
+                        // MMA of it in the segment
+                        mma_f16_ts(d_tmem + (kk % C::kChains) * T, tmem + me * kACols + 8 * kk,
+                                   bdesc, C::kIdesc, first && kk < C::kChains ? 0u : 1u);
+                    }
+                    first = false;
+                    // the A buffer and the x slot are free once these MMAs are done
+                    mma_commit(smem_u32(a_empty + me));
                 }
-                mma_commit(smem_u32(a_empty + a));
-                mma_commit(smem_u32(d_full + d));
-                W4A16_TR(6, c);
+                if (!ok) break;
+                mma_commit(smem_u32(d_full + dset));
+                ++q;
             }
-            // all MMAs of this CTA complete before the tensor memory is freed
+            // all MMAs of this issuer complete before the tensor memory is freed
             mma_commit(smem_u32(done));
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait(smem_u32(done), 0)) {
-                if (globaltimer() - t0 > kWaitNs) {
-                    atomicOr(p.status, kErrDrain);
-                    break;
-                }
-            }
+            if (!mbar_wait_drain(smem_u32(done), 0)) atomicOr(p.status, kErrDrain);
         }
     } else if (warp >= kEpiWarps) {
-        // ------------------------------------------------ dequantise + stage x
-        const int team = (warp - kEpiWarps) / kDeqWarps;  // groups team, team+2, ...
+        // ------------------------------------------------ restore teams
+        const int team = (warp - kEpiWarps) / kDeqWarps;  // groups c with c % 2 == team
         const int dw = (warp - kEpiWarps) % kDeqWarps;    // 0..7 within the team
-        const int quarter = warp & 3;         // TMEM lanes 32*quarter ..
-        const int half = dw >> 2;             // which 64 k of the group
-        const int r = quarter * 32 + lane;    // row within the tile
-        const int n = tile * kTileN + r;
-        const uint32_t *zrow = p.zeros + (size_t)(n < p.N ? n : 0) * p.ZW;
-        const int dt = dw * 32 + lane;        // 0..255 among dequant threads
-        // x pieces this thread moves: piece pc = dt + 256 i is (token pc % T,
-        // 8-block pc / T) of a group; copied kXAhead groups ahead with cp.async
-        // into a raw ring, then re-ordered into the MMA layout when its group
-        // comes up.
-        uint8_t *team_raw = sm_xraw + team * kXAhead * C::kXBytes;
-        // the team's li-th group is c = team + kDeqTeams * li
-        auto issue_x = [&](int li) {
-            const int c = team + kDeqTeams * li;
-            if (c < nchunks) {
-                const int g = g0 + c;
-                uint8_t *raw = team_raw + (li % kXAhead) * C::kXBytes;
-#pragma unroll
-                for (int i = 0; i < C::kPiecesPerThread; ++i) {
-                    const int pc = dt + i * kDeqWarps * 32;
-                    const int t = pc % T, kb = pc / T;
-                    const __half *src =
-                        t < p.M ? p.x + (size_t)t * p.K + (size_t)g * kGroup + 8 * kb : p.x;
-                    cp_async16(smem_u32(raw + pc * 16), src, t < p.M ? 16u : 0u);
+        const int quarter = warp & 3;                     // TMEM lanes 32 * quarter ..
+        const int half = dw >> 2;                         // which 64 inputs of the group
+        const int r = quarter * 32 + lane;                // row within the tile
+        const bool x_issuer = dw == 0 && lane == 0;       // loads x of the team's groups
+        uint64_t pol_x = 0;
+        if (x_issuer)  // x is read by every CTA
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+        bool dep_waited = false;
+        int xuse[kAStages] = {0, 0, 0, 0};  // x copies this thread issued per slot
+        int c = 0, sc = 0;
+        bool ok = true;
+        while (ok && walk_next(p, wk, t, j0, j1)) {
+            const int n = t * kTileN + r;
+            const __half *srow = p.scales + (size_t)(n < p.N ? n : 0) * p.G;
+            for (int j = j0; j < j1 && ok; ++j, ++sc) {
+                const int s = sc % NS, ng = stage_groups(p, j);
+                const uint8_t *st = sm_stage + (size_t)s * C::kStageBytes;
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (sc / NS) & 1, abort))) {
+                    fail(abort, p.status, kErrWaitFull);
+                    ok = false;
+                    break;
                 }
-            }
-            cp_async_commit();
-        };
+                // this row's words of the team's groups of the stage (at most
+                // two: the stage's groups alternate between the teams), read
+                // at once so that the stage is free for the next box early;
+                // 16-byte chunks 2 half and 2 half + 1 of a row, stored 64-byte
+                // swizzled (chunk ^= (row >> 1) & 3)
+                const int gfirst = ((c & 1) == team) ? 0 : 1;
+                const int sw = (r >> 1) & 3;
+                uint4 w[2][2];
 #pragma unroll
-        for (int li = 0; li < kXAhead; ++li) issue_x(li);
-        const int c_first = team;
-        uint32_t zw_cur = (n < p.N && c_first < nchunks) ? __ldg(zrow + ((g0 + c_first) >> 3)) : 0u;
-        uint32_t zw_next = (n < p.N && c_first + kDeqTeams < nchunks)
-                               ? __ldg(zrow + ((g0 + c_first + kDeqTeams) >> 3))
-                               : 0u;
-        int li = 0;
-        for (int c = c_first; c < nchunks; c += kDeqTeams, ++li) {
-            const int s = c % kPStages, a = c % kAStages;
-            const int g = g0 + c;
-            const uint32_t zw = zw_cur;
-            zw_cur = zw_next;
-            zw_next = (n < p.N && c + 2 * kDeqTeams < nchunks)
-                          ? __ldg(zrow + ((g + 2 * kDeqTeams) >> 3))
-                          : 0u;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (c / kPStages) & 1, abort))) {
-                fail(abort, p.status, kErrWaitFull);
-                break;
-            }
-            if (dw == 0 && lane == 0) W4A16_TR(1, c);
-            // this row's 32 bytes of the stage: 16-byte chunks 2*half, 2*half+1,
-            // stored 64-byte swizzled (chunk ^= (row >> 1) & 3)
-            const uint8_t *st = sm_p + s * kStageBytes + r * 64;
-            const int sw = (r >> 1) & 3;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(st + 16 * ((2 * half) ^ sw));
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(st + 16 * ((2 * half + 1) ^ sw));
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(smem_u32(a_empty + a), ((c / kAStages) & 1) ^ 1, abort))) {
-                fail(abort, p.status, kErrWaitAEmpty);
-                break;
-            }
-            // the MMAs that read A[a] and x[a] have completed (commit); order
-            // this warp's tensor-memory stores after that observation
-            tc_fence_after();
-            if (dw == 0 && lane == 0) W4A16_TR(2, c);
-            const uint32_t z = (zw >> (4 * (g & 7))) & 0xfu;
-            const uint32_t zz_hi = 0x64006400u | z | (z << 16);
-            const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            uint32_t v[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t w = words[u], w8 = w >> 8;
-                v[4 * u + 0] = hsub2(lop3_and_or(w, 0x000f000fu, 0x64006400u), zz_hi);
-                v[4 * u + 1] = hsub2(lop3_and_or(w, 0x00f000f0u, 0x54005400u), zz_lo);
-                v[4 * u + 2] = hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi);
-                v[4 * u + 3] = hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo);
-            }
-            // every lane has consumed its words of the stage: release it
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(empty + s));
-            tmem_st_x32(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols + 32 * half, v);
-            // x of this group: this thread's pieces arrived (own cp.async group);
-            // re-order to pair order at (t/8)*2048 + kb*128 + (t%8)*16
-            cp_async_wait<kXAhead - 1>();
-            {
-                const uint8_t *raw = team_raw + (li % kXAhead) * C::kXBytes;
-                uint8_t *xb = sm_x + a * C::kXBytes;
-#pragma unroll
-                for (int i = 0; i < C::kPiecesPerThread; ++i) {
-                    const int pc = dt + i * kDeqWarps * 32;
-                    const int t = pc % T, kb = pc / T;
-                    const uint4 v4 = pair_order(*reinterpret_cast<const uint4 *>(raw + pc * 16));
-                    *reinterpret_cast<uint4 *>(xb + (t >> 3) * 2048 + kb * 128 + (t & 7) * 16) = v4;
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int gi = gfirst + 2 * k2;
+                    if (gi < ng) {
+                        const uint8_t *rowp = st + gi * kGroupBytes + r * 64;
+                        w[k2][0] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half) ^ sw));
+                        w[k2][1] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half + 1) ^ sw));
+                    }
                 }
+                // its scale words and zeros word; its 4 scales start at byte
+                // `off` of the words (rows past N: all zero)
+                const uint4 md = *reinterpret_cast<const uint4 *>(st + kStageW + r * 16);
+                // every read of the stage comes before the next copies into it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(empty + s));
+                const uint32_t mw[3] = {md.x, md.y, md.z};
+                const uint32_t off = (uint32_t)((uintptr_t)(srow + kSG * j) & 2);
+                const uint32_t zsh = 4u * (uint32_t)((kSG * j) & 7);  // the stage's first nibble
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int gi = gfirst + 2 * k2;
+                    if (gi >= ng) break;
+                    const int cg = c + gi;  // the group's number in the CTA's sequence
+                    const int a = cg % kAStages;
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(a_empty + a),
+                                                           ((cg / kAStages) & 1) ^ 1, abort))) {
+                        fail(abort, p.status, kErrWaitAEmpty);
+                        ok = false;
+                        break;
+                    }
+                    // the MMAs that read A[a] and x slot a have completed (commit)
+                    tc_fence_after();
+                    if (x_issuer) {
+                        // x of this group into slot a; x is written by the
+                        // preceding kernel: wait for it once
+                        if (!dep_waited) {
+                            grid_dependency_wait();
+                            dep_waited = true;
+                        }
+                        const uint32_t xbar = smem_u32(x_full + a);
+                        mbar_arrive_expect_tx(xbar, (uint32_t)C::kXSlot);
+                        tma_load_3d(smem_u32(sm_x + a * C::kXSlot), &p.xmap, 0, 0,
+                                    (kSG * j + gi) * (kGroup / 8), xbar, pol_x);
+                        ++xuse[a];
+                    }
+                    const uint32_t bp = off + 2u * gi;  // byte of the scale in the words
+                    const uint32_t sbits = (mw[bp >> 2] >> (8u * (bp & 2u))) & 0xffffu;
+                    const uint32_t z = (md.w >> (zsh + 4u * gi)) & 0xfu;
+                    const uint32_t zz_hi = 0x64006400u | z | (z << 16);
+                    const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
+                    const uint32_t ss = sbits | (sbits << 16);
+                    // 16 columns (4 words) per store, so that few values are live
+#pragma unroll
+                    for (int hw = 0; hw < 2; ++hw) {
+                        const uint32_t words[4] = {w[k2][hw].x, w[k2][hw].y, w[k2][hw].z,
+                                                   w[k2][hw].w};
+                        uint32_t v[16];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t wd = words[u], w8 = wd >> 8;
+                            // (q - z) exact, then times s rounded once: (q0,q4) (q1,q5)
+                            // (q2,q6) (q3,q7) of the word, the order of the x copy
+                            v[4 * u + 0] = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                            v[4 * u + 1] = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            v[4 * u + 2] = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                            v[4 * u + 3] = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                        }
+                        tmem_st_x16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols +
+                                        32 * half + 16 * hw, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(a_full + a));
+                }
+                c += ng;
             }
-            issue_x(li + kXAhead);  // refills the raw slot just read
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(a_full + a));
-            if (dw == 0 && lane == 0) W4A16_TR(3, c);
         }
-        cp_async_wait<0>();
+        // the x copies this thread issued land before the CTA exits: each is
+        // waited for by its MMA issuer, or, after an abort, here (bounded)
+        if (x_issuer && !ok)
+            for (int a = 0; a < kAStages; ++a)
+                if (xuse[a] > 0 && !mbar_wait_drain(smem_u32(x_full + a), (xuse[a] - 1) & 1))
+                    atomicOr(p.status, kErrDrain);
     } else {
         // ------------------------------------------------ epilogue (warps 0..3)
-        const int quarter = warp;  // warp % 4 == warp here
-        const int r = quarter * 32 + lane;
-        const int n = tile * kTileN + r;
-        const __half *srow = p.scales + (size_t)(n < p.N ? n : 0) * p.G;
-        float acc[T];
-#pragma unroll
-        for (int t = 0; t < T; ++t) acc[t] = 0.f;
-        // scales fetched four groups ahead (a rotating set of registers)
-        auto ld_scale = [&](int c) {
-            return (n < p.N && c < nchunks) ? __half2float(srow[g0 + c]) : 0.f;
-        };
-        float s0 = ld_scale(0), s1 = ld_scale(1), s2 = ld_scale(2), s3 = ld_scale(3);
-        for (int c = 0; c < nchunks; ++c) {
-            const int d = c % kDStages;
-            const float sc = s0;
-            s0 = s1;
-            s1 = s2;
-            s2 = s3;
-            s3 = ld_scale(c + 4);
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(d_full + d), (c / kDStages) & 1, abort))) {
+        const int r = warp * 32 + lane;  // row within the tile; TMEM lanes of this warp
+        // outputs, partial sums and counters may belong to the preceding kernel
+        grid_dependency_wait();
+        int c = 0, q = 0;
+        bool ok = true;
+        while (ok && walk_next(p, wk, t, j0, j1)) {
+            const int dset = q % C::kDSets, duse = q / C::kDSets;
+            const int n = t * kTileN + r;
+            const bool vrow = n < p.N;
+            const int g0 = kSG * j0, g1 = min(p.G, kSG * j1);
+            const int c0 = c;
+            c += g1 - g0;
+            // while the MMAs run: does a scale of this row in the range reach
+            // 4096 (or Inf, NaN)?  Then the fp16 restore may overflow, and the
+            // row is recomputed exactly below.
+            bool big = false;
+            if (vrow) {
+                const unsigned short *sr =
+                    reinterpret_cast<const unsigned short *>(p.scales) + (size_t)n * p.G;
+                for (int g = g0; g < g1; ++g) big |= (sr[g] & 0x7fffu) >= kBigScale;
+            }
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(d_full + dset), duse & 1, abort))) {
                 fail(abort, p.status, kErrWaitDFull);
+                ok = false;
                 break;
             }
             tc_fence_after();
-            if (warp == 0 && lane == 0) W4A16_TR(7, c);
+            const bool whole = j0 == 0 && j1 == p.spt;
+            // part of a tile: this CTA's partial-sum slot (the last CTA of the
+            // tile adds the slots in K order, which is CTA order)
+            const int slot =
+                2 * (int)blockIdx.x + (range_begin(p, blockIdx.x) / p.spt == t ? 0 : 1);
+            float *part = p.partials + (size_t)slot * p.M * kTileN + r;
+            auto put = [&](int tt, float v) {
+                if (tt >= p.M) return;
+                if (whole) {
+                    if (vrow) p.y[(size_t)tt * p.N + n] = __float2half_rn(v);
+                } else {
+                    part[(size_t)tt * kTileN] = v;
+                }
+            };
             const uint32_t taddr =
-                tmem + ((uint32_t)(quarter * 32) << 16) + C::kDBase + d * kDCols;
-            if constexpr (C::kChains == 1) {
+                tmem + ((uint32_t)(warp * 32) << 16) + C::kDBase + dset * C::kDBuf;
 #pragma unroll
-                for (int t0 = 0; t0 < T; t0 += 32) {
-                    float v[16], w[16];
-                    tmem_ld_x16(taddr + t0, v);
-                    tmem_ld_x16(taddr + t0 + 16, w);
-                    tmem_wait_ld();
+            for (int t0 = 0; t0 < T; t0 += 16) {
+                // issuer 0's chains in order, then issuer 1's, ... (a fixed
+                // order); issuer i holds sums when the range has a group c with
+                // c % 4 == i
+                float sum[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[t0 + i] = fmaf(sc, v[i], acc[t0 + i]);
+                for (int i = 0; i < 16; ++i) sum[i] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[t0 + 16 + i] = fmaf(sc, w[i], acc[t0 + 16 + i]);
+                for (int iss = 0; iss < kMmaWarps; ++iss) {
+                    const bool valid = g1 - g0 >= kMmaWarps ||
+                                       ((iss - c0) % kMmaWarps + kMmaWarps) % kMmaWarps < g1 - g0;
+#pragma unroll
+                    for (int ch = 0; ch < C::kChains; ++ch) {
+                        float a0[16];
+                        tmem_ld_x16(taddr + (iss * C::kChains + ch) * T + t0, a0);
+                        tmem_wait_ld();
+                        if (valid) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) sum[i] += a0[i];
+                        }
+                    }
                 }
-            } else {
-                float sum[T];
+                if (!big) {
 #pragma unroll
-                for (int t = 0; t < T; ++t) sum[t] = 0.f;
-#pragma unroll
-                for (int b = 0; b < kDCols / 16; b += 2) {
-                    float v[16], w[16];
-                    tmem_ld_x16(taddr + 16 * b, v);
-                    tmem_ld_x16(taddr + 16 * b + 16, w);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) sum[(16 * b + i) % T] += v[i];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) sum[(16 * b + 16 + i) % T] += w[i];
+                    for (int i = 0; i < 16; ++i) put(t0 + i, sum[i]);
                 }
-#pragma unroll
-                for (int t = 0; t < T; ++t) acc[t] = fmaf(sc, sum[t], acc[t]);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(d_empty + d));
-            if (warp == 0 && lane == 0) W4A16_TR(8, c);
-        }
-        // one reader decides for all four epilogue warps (named barrier 1)
-        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-        if (threadIdx.x == 0) *s_last = *abort ? -1 : 0;
-        asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-        if (*s_last == 0) {
-            if (p.S == 1) {
-                if (n < p.N) {
-#pragma unroll
-                    for (int t = 0; t < T; ++t)
-                        if (t < p.M) p.y[(size_t)t * p.N + n] = __float2half_rn(acc[t]);
-                }
-            } else {
-                if (n < p.N) {
-#pragma unroll
-                    for (int t = 0; t < T; ++t)
-                        if (t < p.M) p.partials[((size_t)slice * p.M + t) * p.N + n] = acc[t];
-                }
+            if (lane == 0) mbar_arrive(smem_u32(d_empty + dset));
+            // a row whose scales may overflow the fp16 restore: exact on the CUDA cores
+            if (big) exact_row(p, n, g0, g1, whole, part);
+            if (!whole) {
                 __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                const long long ts0 = (long long)t * p.spt;
+                const int b0 = cta_of(p, ts0), b1 = cta_of(p, ts0 + p.spt - 1);
                 if (threadIdx.x == 0) {
-                    const unsigned prev = atomicAdd(p.counters + tile, 1u);
-                    *s_last = (prev == (unsigned)(p.S - 1)) ? 1 : 0;
+                    const unsigned prev = atomicAdd(p.counters + t, 1u);
+                    *s_last = prev == (unsigned)(b1 - b0) ? 1 : 0;
                 }
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-                if (*s_last == 1) {
+                if (*s_last) {
                     __threadfence();
-                    if (n < p.N) {
-                        for (int t = 0; t < p.M; ++t) {
-                            float sum = 0.f;
-                            for (int s2 = 0; s2 < p.S; ++s2)
-                                sum += __ldcg(p.partials + ((size_t)s2 * p.M + t) * p.N + n);
-                            p.y[(size_t)t * p.N + n] = __float2half_rn(sum);
+                    if (vrow) {
+                        // the pieces' sums in K order (CTA order), 16 tokens per
+                        // batch of independent loads (one round trip each, not
+                        // one per token and piece)
+                        for (int t0 = 0; t0 < p.M; t0 += 16) {
+                            float sum[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) sum[i] = 0.f;
+                            for (int b = b0; b <= b1; ++b) {
+                                const int sl = 2 * b + (range_begin(p, b) / p.spt == t ? 0 : 1);
+                                const float *src = p.partials + ((size_t)sl * p.M + t0) * kTileN + r;
+                                float v[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    v[i] = t0 + i < p.M ? __ldcg(src + (size_t)i * kTileN) : 0.f;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) sum[i] += v[i];
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __float2half_rn(sum[i]);
                         }
                     }
-                    if (threadIdx.x == 0) p.counters[tile] = 0u;
+                    if (threadIdx.x == 0) p.counters[t] = 0u;  // ready for the next launch
                 }
+                // s_last is written again only after the next such segment's first
+                // barrier, which every epilogue thread reaches after reading it
             }
+            ++q;
         }
     }
 
@@ -643,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(C::kTmemCols)
+                     "r"(kTmemCols)
                      : "memory");
     }
 }
@@ -651,11 +848,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+template <int T>
+int stages_for() {
+    int ns = (kSmemBudget - TcConfig<T>::kXRing - kBarBytes) / TcConfig<T>::kStageBytes;
+    return ns > kMaxStages ? kMaxStages : ns;
+}
 
 template <int T>
-cudaError_t launch_t(const TcParams &p, dim3 grid, cudaStream_t stream) {
-    tc_kernel<T><<<grid, kThreads, TcConfig<T>::kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+int smem_for(int ns) {
+    return 1024 /*align slack*/ + TcConfig<T>::kXRing + ns * TcConfig<T>::kStageBytes + kBarBytes;
+}
+
+cudaLaunchConfig_t pdl_config(dim3 grid, int threads, int smem, cudaStream_t stream,
+                              cudaLaunchAttribute *attr) {
+    // programmatic dependent launch: the grid may start while the previous
+    // kernel in the stream drains; it waits for it (griddepcontrol) before
+    // touching what that kernel may read or write
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int T>
+cudaError_t launch_t(const TcParams &p, int grid, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), kThreads, smem_for<T>(p.n_stages), stream, attr);
+    return cudaLaunchKernelEx(&cfg, tc_kernel<T>, p);
 }
 
 }  // namespace
@@ -666,22 +891,23 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.T = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int G = K / kGroup;
     pl.n_tiles = (N + kTileN - 1) / kTileN;
-    const int slots = dev.sm_count;  // one CTA of 448 threads per SM
-    int S = 1;
-    if (split != 0) {
-        // whole groups per slice, at least 4 groups each; fill the SMs
-        if (pl.n_tiles < slots) {
-            S = slots / pl.n_tiles;
-            int cap = G / 4 > 0 ? G / 4 : 1;
-            if (S > cap) S = cap;
-        }
-        if (split == 1 && S < 2 && G >= 2) S = 2;
-        if (S < 1) S = 1;
+    pl.spt = (G + kSG - 1) / kSG;
+    pl.stages = pl.T == 16 ? stages_for<16>() : (pl.T == 32 ? stages_for<32>() : stages_for<64>());
+    const long long total = (long long)pl.n_tiles * pl.spt;
+    const int slots = dev.sm_count;  // one CTA per SM
+    // whole tiles unless they leave SMs idle for long: with n tiles on s SMs
+    // the busiest SM streams ceil(n / s) tiles against n / s on average
+    bool streamk = split == 1;
+    if (split < 0) {
+        const double rounds = (double)((pl.n_tiles + slots - 1) / slots);
+        streamk = (double)pl.n_tiles / slots < 0.9 * rounds && pl.spt > 1;
     }
-    pl.slice_groups = (G + S - 1) / S;
-    pl.S = (G + pl.slice_groups - 1) / pl.slice_groups;
-    pl.ws_bytes = pl.S > 1 ? (size_t)pl.S * M * N * sizeof(float) : 0;
-    pl.ok = G >= 1 && pl.S <= 65535;
+    pl.S = streamk ? 2 : 1;
+    if (streamk) pl.grid = total < slots ? (int)total : slots;
+    else pl.grid = pl.n_tiles < slots ? pl.n_tiles : slots;
+    pl.xp_bytes = ((size_t)M * K * 2 + 255) & ~(size_t)255;
+    pl.ws_bytes = pl.xp_bytes + (streamk ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0);
+    pl.ok = G >= 1 && pl.stages >= 2;
     return pl;
 }
 
@@ -689,22 +915,15 @@ cudaError_t tc_init(const DeviceInfo &dev) {
     (void)dev;
     if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcConfig<16>::kSmemBytes);
+                                         smem_for<16>(stages_for<16>()));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcConfig<32>::kSmemBytes);
+                                 smem_for<32>(stages_for<32>()));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcConfig<64>::kSmemBytes);
+                                 smem_for<64>(stages_for<64>()));
     return e;
 }
-
-#ifdef W4A16_TRACE
-extern "C" int w4a16_debug_trace(unsigned long long *out, int n) {
-    if (n > kTraceEvents * kTraceChunks) n = kTraceEvents * kTraceChunks;
-    return (int)cudaMemcpyFromSymbol(out, g_trace, n * sizeof(unsigned long long));
-}
-#endif
 
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream) {
@@ -712,33 +931,65 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     if (!encode) return cudaErrorInitializationError;
     TcParams p;
     memset(&p, 0, sizeof(p));
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8) * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)kChunkWords, (cuuint32_t)kTileN};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, (void *)a.qw, dims, strides,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const int G = a.K / kGroup;
+    __half *xp = reinterpret_cast<__half *>(ws.partials);  // the pair-ordered copy of x
+    {
+        // qweight as (word in group, row, group): a box of 128 rows x 4 groups
+        const cuuint64_t dims[3] = {16, (cuuint64_t)a.N, (cuuint64_t)G};
+        const cuuint64_t strides[2] = {(cuuint64_t)a.K / 2, 64};
+        const cuuint32_t box[3] = {16, (cuuint32_t)kTileN, (cuuint32_t)kSG};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = encode(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        // the x copy as (8 halves, token, chunk of 8): a box of T tokens x 16
+        // chunks (one group) lands as [chunk][token][16 bytes]; tokens past M
+        // read zeros
+        const cuuint64_t dims[3] = {8, (cuuint64_t)a.M, (cuuint64_t)(a.K / 8)};
+        const cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, 16};
+        const cuuint32_t box[3] = {8, (cuuint32_t)plan.T, (cuuint32_t)(kGroup / 8)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void *)xp, dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     p.x = a.x;
+    p.qw = a.qw;
     p.scales = a.scales;
     p.zeros = a.zeros;
     p.y = a.y;
-    p.partials = ws.partials;
+    p.partials = reinterpret_cast<float *>(reinterpret_cast<char *>(ws.partials) + plan.xp_bytes);
     p.counters = ws.counters;
     p.status = status;
     p.N = a.N;
     p.K = a.K;
-    p.G = a.K / kGroup;
-    p.ZW = (p.G + 7) / 8;
+    p.G = G;
+    p.ZW = (G + 7) / 8;
     p.M = a.M;
-    p.S = plan.S;
-    p.slice_groups = plan.slice_groups;
-    dim3 grid(plan.n_tiles, plan.S);
+    p.n_tiles = plan.n_tiles;
+    p.spt = plan.spt;
+    p.streamk = plan.S > 1;
+    p.n_stages = plan.stages;
+    p.total = (long long)plan.n_tiles * plan.spt;
+    // x in pair order, then the GEMM (each may start while its predecessor drains)
+    {
+        const long long chunks = (long long)a.M * (a.K / 8);
+        const int threads = 256;
+        long long blocks = (chunks + threads - 1) / threads;
+        if (blocks > 1024) blocks = 1024;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), threads, 0, stream, attr);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, tc_prep_kernel, a.x, xp, a.M, a.K);
+        if (e != cudaSuccess) return e;
+    }
     switch (plan.T) {
-        case 16: return launch_t<16>(p, grid, stream);
-        case 32: return launch_t<32>(p, grid, stream);
-        case 64: return launch_t<64>(p, grid, stream);
+        case 16: return launch_t<16>(p, plan.grid, stream);
+        case 32: return launch_t<32>(p, plan.grid, stream);
+        case 64: return launch_t<64>(p, plan.grid, stream);
     }
     return cudaErrorInvalidValue;
 }
