@@ -100,8 +100,7 @@ struct TcPlan {
     int spt;           // stages (4 groups each) per tile
     int grid;          // CTAs (one per SM)
     int stages;        // shared-memory stages in flight per CTA
-    size_t xp_bytes;   // the pair-ordered copy of x the kernel reads
-    size_t ws_bytes;   // workspace: the x copy, then stream-K partial sums
+    size_t ws_bytes;   // workspace: stream-K partial sums
 };
 
 // split: 0 = whole tiles only, 1 = stream-K, -1 = planner decides.

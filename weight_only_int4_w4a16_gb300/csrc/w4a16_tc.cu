@@ -21,25 +21,27 @@
 //   the CUDA cores by its epilogue thread (w = (q - z) * s in fp32, exact), so
 //   every finite scale gives the method's result.
 //
-//   Roles (one CTA per SM, 736 threads):
-//   warp 20 (one thread) streams with TMA, per stage, a box of 128 rows x 4
-//     groups of packed weights (each row a 256-byte run of memory, 64-byte
-//     swizzle; L2 evict-first, read once) and the stage's 512 inputs of x for
-//     all T tokens.  x comes from a copy made by tc_prep_kernel just before,
-//     with each 8-element chunk in the order the unpack yields the nibbles of
-//     a word, (x0,x4) (x1,x5) (x2,x6) (x3,x7), so the TMA box lands in the
-//     MMA's canonical K-major layout;
+//   Roles (one CTA per SM, 800 threads):
+//   warp 20 streams, per stage, a TMA box of 128 rows x 4 groups of packed
+//     weights (each row a 256-byte run of memory, 64-byte swizzle; L2
+//     evict-first, read once), and its lanes copy the rows' scale and zeros
+//     words (cp.async) next to it;
 //   warps 4..19, two teams of 8 taking alternate groups, restore a group:
-//     thread = one row (its TMEM lane) and 64 inputs; the nibble unpack splices
-//     (1024 + q) or (64 + q) into fp16, subtracts the matching (1024 + z) /
-//     (64 + z) exactly and multiplies by s (one rounding); tcgen05.st puts the
-//     values in tensor memory as the MMA's A operand (a ring of 4 buffers);
-//   warps 21 and 22 (one thread each) take alternate groups and issue a
-//     group's 8 tcgen05.mma into their own accumulator chain (so the sums of
-//     each chain come in a fixed order), then commit;
-//   warps 0..3 (thread = row) read both chains once per K range, add them,
-//     and write y, or, for a K range that is part of a tile, fp32 partial sums
-//     that the last CTA of the tile adds in K order.
+//     thread = one row (its TMEM lane) and 64 inputs; it reads its words of
+//     the stage at once (so the stage is free for the next box early), then
+//     the nibble unpack splices (1024 + q) or (64 + q) into fp16, subtracts the
+//     matching (1024 + z) / (64 + z) exactly, multiplies by s (one rounding)
+//     and puts the pairs in k order; tcgen05.st puts the values in tensor
+//     memory as the MMA's A operand (a ring of 4 buffers).  One lane of each
+//     team loads the group's x for all T tokens by TMA straight from the
+//     caller's x into the matching x slot: a box of T rows x 256 bytes lands
+//     as the MMA's canonical K-major layout;
+//   warps 21..24 (one thread each) take groups c with c % 4 == their index and
+//     issue a group's 8 tcgen05.mma into their own accumulator chains (so the
+//     sums of each chain come in a fixed order), then commit;
+//   warps 0..3 (thread = row) read the chains once per K range, add them in a
+//     fixed order, and write y, or, for a K range that is part of a tile, fp32
+//     partial sums that the last CTA of the tile adds in K order.
 //
 //   Work: CTAs take equal runs of the (tile, stage) sequence ("stream-K"), so
 //   that every SM streams the same number of bytes however the tiles divide
@@ -87,7 +89,7 @@ constexpr int kErrWaitFull = 1, kErrWaitAFull = 2, kErrWaitDFull = 4, kErrWaitEm
 
 struct TcParams {
     CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 128, 4}
-    CUtensorMap xmap;  // pair-ordered x 3-D: (8 halves, M tokens, K/8 chunks), box {8, T, 64}
+    CUtensorMap xmap;  // x 3-D: (8 halves, M tokens, K/8 chunks), box {8, T, 16}: one group
     const __half *x;   // x as given (the exact path)
     const uint32_t *qw;
     const __half *scales;
@@ -352,26 +354,6 @@ __device__ __forceinline__ int stage_groups(const TcParams &p, int j) {
 // The CTA whose range holds stage st (stream-K).
 __device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
     return (int)(((st + 1) * (long long)gridDim.x - 1) / p.total);
-}
-
-// ---------------------------------------------------------------------------
-// x in the unpack's pair order: the copy tc_kernel reads
-// ---------------------------------------------------------------------------
-__global__ void tc_prep_kernel(const __half *__restrict__ x, __half *__restrict__ xp, int M, int K) {
-    grid_dependents_launch();
-    // the previous kernel in the stream may still read xp
-    grid_dependency_wait();
-    const long long chunks = (long long)M * (K / 8);
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < chunks;
-         i += (long long)gridDim.x * blockDim.x) {
-        const uint4 v = reinterpret_cast<const uint4 *>(x)[i];
-        uint4 o;
-        o.x = prmt(v.x, v.z, 0x5410);  // (x0, x4)
-        o.y = prmt(v.x, v.z, 0x7632);  // (x1, x5)
-        o.z = prmt(v.y, v.w, 0x5410);  // (x2, x6)
-        o.w = prmt(v.y, v.w, 0x7632);  // (x3, x7)
-        reinterpret_cast<uint4 *>(xp)[i] = o;
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -646,6 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 const uint32_t mw[3] = {md.x, md.y, md.z};
                 const uint32_t off = (uint32_t)((uintptr_t)(srow + kSG * j) & 2);
                 const uint32_t zsh = 4u * (uint32_t)((kSG * j) & 7);  // the stage's first nibble
+                // the team's groups of the stage are restored one after the
+                // other and their tensor-memory stores waited for once: the
+                // store latency is paid once per stage, not per group
+                int done_a[2] = {-1, -1};
 #pragma unroll
                 for (int k2 = 0; k2 < 2; ++k2) {
                     const int gi = gfirst + 2 * k2;
@@ -688,20 +674,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const uint32_t wd = words[u], w8 = wd >> 8;
-                            // (q - z) exact, then times s rounded once: (q0,q4) (q1,q5)
-                            // (q2,q6) (q3,q7) of the word, the order of the x copy
-                            v[4 * u + 0] = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                            v[4 * u + 1] = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
-                            v[4 * u + 2] = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                            v[4 * u + 3] = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            // (q - z) exact, then times s rounded once: the pairs
+                            // (q0,q4) (q1,q5) (q2,q6) (q3,q7) of the word ...
+                            const uint32_t r0 = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                            const uint32_t r1 = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            const uint32_t r2 = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                            const uint32_t r3 = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            // ... in k order, (q0,q1) (q2,q3) (q4,q5) (q6,q7): the
+                            // order of x in memory, which the TMA box keeps
+                            v[4 * u + 0] = prmt(r0, r1, 0x5410);
+                            v[4 * u + 1] = prmt(r2, r3, 0x5410);
+                            v[4 * u + 2] = prmt(r0, r1, 0x7632);
+                            v[4 * u + 3] = prmt(r2, r3, 0x7632);
                         }
                         tmem_st_x16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols +
                                         32 * half + 16 * hw, v);
                     }
+                    done_a[k2] = a;
+                }
+                if (done_a[0] >= 0) {
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(a_full + a));
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(a_full + done_a[0]));
+                        if (done_a[1] >= 0) mbar_arrive(smem_u32(a_full + done_a[1]));
+                    }
                 }
                 c += ng;
             }
@@ -905,8 +903,7 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.S = streamk ? 2 : 1;
     if (streamk) pl.grid = total < slots ? (int)total : slots;
     else pl.grid = pl.n_tiles < slots ? pl.n_tiles : slots;
-    pl.xp_bytes = ((size_t)M * K * 2 + 255) & ~(size_t)255;
-    pl.ws_bytes = pl.xp_bytes + (streamk ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0);
+    pl.ws_bytes = streamk ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0;
     pl.ok = G >= 1 && pl.stages >= 2;
     return pl;
 }
@@ -932,7 +929,6 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     TcParams p;
     memset(&p, 0, sizeof(p));
     const int G = a.K / kGroup;
-    __half *xp = reinterpret_cast<__half *>(ws.partials);  // the pair-ordered copy of x
     {
         // qweight as (word in group, row, group): a box of 128 rows x 4 groups
         const cuuint64_t dims[3] = {16, (cuuint64_t)a.N, (cuuint64_t)G};
@@ -945,14 +941,14 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
-        // the x copy as (8 halves, token, chunk of 8): a box of T tokens x 16
-        // chunks (one group) lands as [chunk][token][16 bytes]; tokens past M
-        // read zeros
+        // x as (8 halves, token, chunk of 8): a box of T tokens x 16 chunks
+        // (one group) lands as [chunk][token][16 bytes], the MMA's K-major
+        // layout; tokens past M read zeros
         const cuuint64_t dims[3] = {8, (cuuint64_t)a.M, (cuuint64_t)(a.K / 8)};
         const cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, 16};
         const cuuint32_t box[3] = {8, (cuuint32_t)plan.T, (cuuint32_t)(kGroup / 8)};
         const cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void *)xp, dims, strides,
+        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void *)a.x, dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -962,7 +958,7 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     p.scales = a.scales;
     p.zeros = a.zeros;
     p.y = a.y;
-    p.partials = reinterpret_cast<float *>(reinterpret_cast<char *>(ws.partials) + plan.xp_bytes);
+    p.partials = ws.partials;
     p.counters = ws.counters;
     p.status = status;
     p.N = a.N;
@@ -975,17 +971,6 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     p.streamk = plan.S > 1;
     p.n_stages = plan.stages;
     p.total = (long long)plan.n_tiles * plan.spt;
-    // x in pair order, then the GEMM (each may start while its predecessor drains)
-    {
-        const long long chunks = (long long)a.M * (a.K / 8);
-        const int threads = 256;
-        long long blocks = (chunks + threads - 1) / threads;
-        if (blocks > 1024) blocks = 1024;
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), threads, 0, stream, attr);
-        cudaError_t e = cudaLaunchKernelEx(&cfg, tc_prep_kernel, a.x, xp, a.M, a.K);
-        if (e != cudaSuccess) return e;
-    }
     switch (plan.T) {
         case 16: return launch_t<16>(p, plan.grid, stream);
         case 32: return launch_t<32>(p, plan.grid, stream);
