@@ -1042,9 +1042,12 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi,
         // within 1.5% of the best plan on average): per unit a CTA pays
         // ~2.2 us (barrier, x staging) plus its stages, a stage per warp
         // 0.85 us plus 0.45 us at full load (16 warps share an SM's issue
-        // slots); a split adds ~4.5 us plus 2 us per slice (partials, the
-        // reducing CTA on the critical path).  Fewer, longer units win unless
-        // the staged x needs the slices or many SMs would sit idle.
+        // slots); a split adds ~3 us plus 0.75 us per slice (partials, the
+        // reducing CTA on the critical path; the reduction stages the slices'
+        // partial sums through shared memory: with its earlier charge of 4.5 us
+        // plus 2 us per slice, K 17408, N 5120 at M = 4 took 30.7 us, now 27.3).
+        // Fewer, longer units win unless the staged x needs the slices or many
+        // SMs would sit idle.
         int s_lo = s_min;
         if (split == 1 && s_lo < 2 && G > kStageGroups) s_lo = 2;
         int s_hi = split == 0 ? 1 : (G + kStageGroups - 1) / kStageGroups;
@@ -1065,7 +1068,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi,
                 // (SiLU-and-mul reduces through the workspace at any S)
                 const bool reduces = S_eff > 1 || epi == kEpiSiluMul;
                 const double cost = (double)per_cta * (2.2 + stages * (0.85 + 0.45 * load)) +
-                                    (reduces ? 4.5 + 2.0 * S_eff : 0.0);
+                                    (reduces ? 3.0 + 0.75 * S_eff : 0.0);
                 if (cost < best_cost - 1e-9) {
                     best_cost = cost;
                     best_sg = sg;
