@@ -76,7 +76,7 @@ typedef enum {
     W4A16_RUNG_GEMV = 0,        /* CUDA cores: warp per output row, whole K per CTA */
     W4A16_RUNG_GEMV_SPLITK = 1, /* CUDA cores: K split across CTAs, fixed-order fp32 reduce */
     W4A16_RUNG_TC = 2,          /* tcgen05 dequant-GEMM, tokens as the MMA N dimension */
-    W4A16_RUNG_TC_SPLITK = 3,   /* tcgen05 dequant-GEMM with K split across CTAs */
+    W4A16_RUNG_TC_SPLITK = 3,   /* tcgen05 dequant-GEMM, CTAs take equal runs of (tile, K stage) work */
     W4A16_RUNG_MMA = 4,         /* warp MMA (m16n8k16), A = weights dequantised in registers, M <= 8 */
     W4A16_RUNG_MMA_SPLITK = 5,  /* the same with K split across CTAs */
     W4A16_NUM_RUNGS = 6
@@ -193,9 +193,11 @@ typedef struct {
 
 /* y = epilogue(x @ W^T): w4a16_linear followed, in the same kernel, by the
  * step `epilogue` names (w4a16_epilogue).  W4A16_EPILOGUE_NONE is exactly
- * w4a16_linear.  The other epilogues run on the warp-MMA rungs only (a forced
- * rung other than those: W4A16_ERR_UNSUPPORTED); more than 8 tokens run as
- * tiles of 8, each of which reads the weights.
+ * w4a16_linear.  The residual add runs on the warp-MMA rungs (up to 8 tokens)
+ * and on the tcgen05 rungs (more than 8 tokens: one reading of the weights
+ * for up to 64); SiLU-and-mul runs on the warp-MMA rungs only, more than 8
+ * tokens as tiles of 8, each of which reads the weights.  A forced rung that
+ * cannot take the epilogue: W4A16_ERR_UNSUPPORTED.
  *   residual  [M, N] fp16, 2-byte aligned, for W4A16_EPILOGUE_RESIDUAL (NULL
  *             otherwise: INVALID_ARG); it may be y itself (y += x @ W^T) but
  *             must not otherwise overlap y.
@@ -211,14 +213,17 @@ int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint
                           const uint16_t *residual, uint16_t *y, void *stream);
 
 /* w4a16_linear_epilogue with the 16-bit type `dtype` (w4a16_dtype) of x,
- * scales, residual and y.  bf16 runs on the warp-MMA rungs only, with the
- * same rules as the epilogues.  Each token's slice of x is staged as fp16
- * scaled by a power of two chosen from its largest exponent (so any bf16
- * magnitude fits; bf16's 8 significant bits fit fp16's 11, so the staged
- * values are exact but for those 2^29 below the token's largest), the fp16
- * tensor-core path runs unchanged, and the scale is removed in fp32 before
- * the one rounding of y to bf16.  W4A16_DTYPE_F16 is exactly
- * w4a16_linear_epilogue.  An invalid dtype is INVALID_ARG. */
+ * scales, residual and y.  bf16 runs on the rungs the epilogue allows, not on
+ * the CUDA-core rungs.  On the warp-MMA rungs (up to 8 tokens) each token's
+ * slice of x is staged as fp16 scaled by a power of two chosen from its
+ * largest exponent (so any bf16 magnitude fits; bf16's 8 significant bits fit
+ * fp16's 11, so the staged values are exact but for those 2^29 below the
+ * token's largest), the fp16 tensor-core path runs unchanged, and the scale
+ * is removed in fp32 before the one rounding of y to bf16.  On the tcgen05
+ * rungs (more than 8 tokens) each weight is restored to bf16 ((q - z) * s,
+ * rounded once) and multiplied with the bf16 activations on the tensor cores
+ * (fp32 sums).  W4A16_DTYPE_F16 is exactly w4a16_linear_epilogue.  An invalid
+ * dtype is INVALID_ARG. */
 int w4a16_linear_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                     const uint32_t *zeros, int M, int N, int K, int group, int dtype,
                     int epilogue, const uint16_t *residual, uint16_t *y, void *stream);

@@ -191,12 +191,18 @@ def test_bf16_decode_round(w4, graph):
         assert_close(L["y"][:, torch.from_numpy(rows).to(DEV)], ref, "bf16 in a mixed round")
 
 
-def test_bf16_needs_the_mma_rungs(w4):
+def test_bf16_on_forced_rungs(w4):
+    # the CUDA-core rungs have no bf16 path; the tcgen05 rung has one (bf16
+    # restore and bf16 tensor-core products), also below 9 tokens when forced
     x, qw, s, zw = case(1, 2, 64, 256)
-    prev = w4.w4a16_set_forced_rung(2)  # the tcgen05 rung has no bf16 path
+    prev = w4.w4a16_set_forced_rung(0)
     try:
         with pytest.raises(w4.W4A16Error) as e:
             w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV))
         assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+        w4.w4a16_set_forced_rung(2)
+        y = w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV))
+        torch.cuda.synchronize()
+        assert_close(y, reference(x, qw, s, zw), "bf16 on the forced tcgen05 rung")
     finally:
         w4.w4a16_set_forced_rung(prev)

@@ -121,10 +121,20 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi 
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
     const int G = K / kGroup;
     if (epi != kEpiNone || dtype != kDtypeF16) {
-        // the epilogues and bf16 data run in the warp-MMA kernel only (tiles
-        // of up to 8 tokens, each reading the weights)
-        if (forced != W4A16_RUNG_AUTO && !is_mma(forced)) return {forced, W4A16_ERR_UNSUPPORTED};
+        // the epilogues and bf16 data run in the warp-MMA kernel (tiles of up
+        // to 8 tokens, each reading the weights) and, the residual add and bf16,
+        // in the tcgen05 kernel (up to 64 tokens per reading of the weights);
+        // SiLU-and-mul combines rows N/2 apart, which a 128-row tcgen05 tile
+        // does not hold
+        const bool tc_ok = epi != kEpiSiluMul;
+        if (forced != W4A16_RUNG_AUTO && !is_mma(forced) && !(is_tc(forced) && tc_ok))
+            return {forced, W4A16_ERR_UNSUPPORTED};
         if (forced == W4A16_RUNG_AUTO) {
+            if (M > kMmaMaxTokens && tc_ok) {
+                const int Mtc = M < kTcMaxTokens ? M : kTcMaxTokens;
+                TcPlan t = plan_tc(Mtc, N, K, -1, dev);
+                return {t.S > 1 ? W4A16_RUNG_TC_SPLITK : W4A16_RUNG_TC, W4A16_OK};
+            }
             MmaPlan p = plan_mma(Mt, N, K, -1, dev, epi);
             return {p.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, W4A16_OK};
         }

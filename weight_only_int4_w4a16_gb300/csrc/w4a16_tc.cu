@@ -81,7 +81,10 @@ static_assert(kMmaWarps == kAStages, "issuer i owns A buffer i (and x slot i)");
 // d_full, d_empty; done), then the tensor-memory address, abort and last flags
 constexpr int kBarBytes = (2 * kMaxStages + 3 * kAStages + 5) * 8 + 16;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
-constexpr uint32_t kBigScale = 0x6C00u;        // |s| >= 4096 (bits of |s|): exact path
+// scales whose 16-bit restore may overflow: |s| >= 4096 in fp16, |s| >= 2^120
+// in bf16 (bits of |s|; Inf and NaN included): those rows take the exact path
+constexpr uint32_t kBigScale = 0x6C00u;
+constexpr uint32_t kBigScaleBf16 = 0x7B80u;
 
 // error codes recorded in the device status word (bit flags)
 constexpr int kErrWaitFull = 1, kErrWaitAFull = 2, kErrWaitDFull = 4, kErrWaitEmpty = 8,
@@ -95,6 +98,7 @@ struct TcParams {
     const __half *scales;
     const uint32_t *zeros;
     __half *y;
+    const __half *residual;  // y = h + residual (the residual epilogue), else null
     float *partials;     // stream-K: [2 * grid][M][128] fp32
     unsigned *counters;  // stream-K: one per tile, zero between launches
     int *status;
@@ -105,7 +109,7 @@ struct TcParams {
     long long total;   // n_tiles * spt
 };
 
-template <int T>
+template <int T, bool kBf16 = false>
 struct TcConfig {
     // x of one group for T tokens: a slot of the x ring (one per A buffer)
     static constexpr int kXSlot = T * kGroup * 2;
@@ -125,9 +129,10 @@ struct TcConfig {
     static constexpr int kDBuf = kMmaWarps * kChains * T;
     static constexpr int kDSets = T == 64 ? 1 : 2;
     static_assert(kDBase + kDSets * kDBuf <= kTmemCols, "tensor memory");
-    // instruction descriptor: D f32, A f16, B f16, both K-major, N = T, M = 128
-    static constexpr uint32_t kIdesc =
-        (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+    // instruction descriptor: D f32, A and B f16 (or both bf16), both K-major,
+    // N = T, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | (kBf16 ? (1u << 7) | (1u << 10) : 0u) |
+                                       ((uint32_t)(T >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
 };
 
 // ---------------------------------------------------------------------------
@@ -262,6 +267,29 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+__device__ __forceinline__ uint32_t sub_bf2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t mul_bf2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// 16-bit activations, scales, residuals and outputs: IEEE binary16, or
+// bfloat16 (the top half of a binary32); storage is 16-bit either way
+template <bool kBf16>
+__device__ __forceinline__ float f16_to_float(__half h) {
+    if constexpr (kBf16) return __uint_as_float((uint32_t)__half_as_ushort(h) << 16);
+    else return __half2float(h);
+}
+template <bool kBf16>
+__device__ __forceinline__ __half float_to_f16(float v) {  // nearest, ties to even
+    if constexpr (kBf16) return __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v)));
+    else return __float2half_rn(v);
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -359,11 +387,12 @@ __device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
 // ---------------------------------------------------------------------------
 // The outputs of row n over groups [g0, g1) for every token, exactly: w =
 // (q - z) * s in fp32 (at most 15 significant bits), summed in increasing k,
-// 16 tokens at a time; to y (a whole tile) or to the partial-sum slot `part`
-// (row n's column of it).  For rows whose scales reach 4096 (or are Inf or
+// 16 tokens at a time; to y (a whole tile: plus the residual, if any, then one
+// rounding) or to the partial-sum slot `part` (row n's column of it).  For rows whose scales reach 4096 (or are Inf or
 // NaN), where the fp16 restore of the tensor-core path may overflow.  Kept
 // out of line: it is rare, and its registers stay out of the kernel's.
 // ---------------------------------------------------------------------------
+template <bool kBf16>
 __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1, bool whole,
                                        float *part) {
     const uint32_t *qrow = p.qw + (size_t)n * (p.K / 8);
@@ -372,7 +401,7 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
         for (int g = g0; g < g1; ++g) {
-            const float sc = __half2float(p.scales[(size_t)n * p.G + g]);
+            const float sc = f16_to_float<kBf16>(p.scales[(size_t)n * p.G + g]);
             const int z = (int)((p.zeros[(size_t)n * p.ZW + (g >> 3)] >> (4 * (g & 7))) & 0xfu);
             for (int wd = 0; wd < kGroup / 8; ++wd) {
                 const uint32_t word = qrow[g * (kGroup / 8) + wd];
@@ -382,7 +411,8 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (t0 + i < p.M)
-                            acc[i] = fmaf(wv, __half2float(p.x[(size_t)(t0 + i) * p.K + k]), acc[i]);
+                            acc[i] = fmaf(wv, f16_to_float<kBf16>(p.x[(size_t)(t0 + i) * p.K + k]),
+                                          acc[i]);
                 }
             }
         }
@@ -390,8 +420,13 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
         for (int i = 0; i < 16; ++i) {
             const int tt = t0 + i;
             if (tt >= p.M) break;
-            if (whole) p.y[(size_t)tt * p.N + n] = __float2half_rn(acc[i]);
-            else part[(size_t)tt * kTileN] = acc[i];
+            if (!whole) {
+                part[(size_t)tt * kTileN] = acc[i];
+            } else {
+                const size_t o = (size_t)tt * p.N + n;
+                const float r = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
+                p.y[o] = float_to_f16<kBf16>(acc[i] + r);
+            }
         }
     }
 }
@@ -399,9 +434,9 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int T>
+template <int T, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ TcParams p) {
-    using C = TcConfig<T>;
+    using C = TcConfig<T, kBf16>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = p.n_stages;
@@ -664,6 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     const uint32_t z = (md.w >> (zsh + 4u * gi)) & 0xfu;
                     const uint32_t zz_hi = 0x64006400u | z | (z << 16);
                     const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
+                    const uint32_t zz_b = 0x43004300u | z | (z << 16);  // bf16 (128 + z) pair
                     const uint32_t ss = sbits | (sbits << 16);
                     // 16 columns (4 words) per store, so that few values are live
 #pragma unroll
@@ -676,10 +712,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             const uint32_t wd = words[u], w8 = wd >> 8;
                             // (q - z) exact, then times s rounded once: the pairs
                             // (q0,q4) (q1,q5) (q2,q6) (q3,q7) of the word ...
-                            const uint32_t r0 = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                            const uint32_t r1 = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
-                            const uint32_t r2 = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                            const uint32_t r3 = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            uint32_t r0, r1, r2, r3;
+                            if constexpr (kBf16) {
+                                // a nibble at mantissa bits 0..3 of bf16 128.0 is
+                                // 128 + q (bf16 has 7 mantissa bits); minus 128 + z
+                                r0 = mul_bf2(sub_bf2(lop3_and_or(wd, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r1 = mul_bf2(sub_bf2(lop3_and_or(wd >> 4, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r2 = mul_bf2(sub_bf2(lop3_and_or(w8, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r3 = mul_bf2(sub_bf2(lop3_and_or(wd >> 12, 0x000f000fu, 0x43004300u), zz_b), ss);
+                            } else {
+                                r0 = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                                r1 = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                                r2 = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                                r3 = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                            }
                             // ... in k order, (q0,q1) (q2,q3) (q4,q5) (q6,q7): the
                             // order of x in memory, which the TMA box keeps
                             v[4 * u + 0] = prmt(r0, r1, 0x5410);
@@ -731,7 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             if (vrow) {
                 const unsigned short *sr =
                     reinterpret_cast<const unsigned short *>(p.scales) + (size_t)n * p.G;
-                for (int g = g0; g < g1; ++g) big |= (sr[g] & 0x7fffu) >= kBigScale;
+                const uint32_t lim = kBf16 ? kBigScaleBf16 : kBigScale;
+                for (int g = g0; g < g1; ++g) big |= (sr[g] & 0x7fffu) >= lim;
             }
             if (!__all_sync(0xffffffffu,
                             mbar_wait(smem_u32(d_full + dset), duse & 1, abort))) {
@@ -749,7 +796,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             auto put = [&](int tt, float v) {
                 if (tt >= p.M) return;
                 if (whole) {
-                    if (vrow) p.y[(size_t)tt * p.N + n] = __float2half_rn(v);
+                    if (vrow) {
+                        // y = h (+ residual), one rounding
+                        const size_t o = (size_t)tt * p.N + n;
+                        if (p.residual) v += f16_to_float<kBf16>(p.residual[o]);
+                        p.y[o] = float_to_f16<kBf16>(v);
+                    }
                 } else {
                     part[(size_t)tt * kTileN] = v;
                 }
@@ -788,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(d_empty + dset));
             // a row whose scales may overflow the fp16 restore: exact on the CUDA cores
-            if (big) exact_row(p, n, g0, g1, whole, part);
+            if (big) exact_row<kBf16>(p, n, g0, g1, whole, part);
             if (!whole) {
                 __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -820,8 +872,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                                 for (int i = 0; i < 16; ++i) sum[i] += v[i];
                             }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = __float2half_rn(sum[i]);
+                            for (int i = 0; i < 16; ++i) {
+                                if (t0 + i >= p.M) continue;
+                                const size_t o = (size_t)(t0 + i) * p.N + n;
+                                const float r = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
+                                p.y[o] = float_to_f16<kBf16>(sum[i] + r);
+                            }
                         }
                     }
                     if (threadIdx.x == 0) p.counters[t] = 0u;  // ready for the next launch
@@ -875,10 +931,11 @@ cudaLaunchConfig_t pdl_config(dim3 grid, int threads, int smem, cudaStream_t str
 }
 
 template <int T>
-cudaError_t launch_t(const TcParams &p, int grid, cudaStream_t stream) {
+cudaError_t launch_t(const TcParams &p, bool bf16, int grid, cudaStream_t stream) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), kThreads, smem_for<T>(p.n_stages), stream, attr);
-    return cudaLaunchKernelEx(&cfg, tc_kernel<T>, p);
+    return bf16 ? cudaLaunchKernelEx(&cfg, tc_kernel<T, true>, p)
+                : cudaLaunchKernelEx(&cfg, tc_kernel<T, false>, p);
 }
 
 }  // namespace
@@ -911,19 +968,22 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
 cudaError_t tc_init(const DeviceInfo &dev) {
     (void)dev;
     if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_for<16>(stages_for<16>()));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_for<32>(stages_for<32>()));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_for<64>(stages_for<64>()));
+    const void *fns[6] = {(const void *)tc_kernel<16, false>, (const void *)tc_kernel<32, false>,
+                          (const void *)tc_kernel<64, false>, (const void *)tc_kernel<16, true>,
+                          (const void *)tc_kernel<32, true>,  (const void *)tc_kernel<64, true>};
+    const int smem[3] = {smem_for<16>(stages_for<16>()), smem_for<32>(stages_for<32>()),
+                         smem_for<64>(stages_for<64>())};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+        e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i % 3]);
     return e;
 }
 
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream) {
+    // SiLU-and-mul combines rows N/2 apart, which a 128-row tile does not hold
+    if (a.epi == kEpiSiluMul) return cudaErrorInvalidValue;
+    const bool bf16 = a.dtype == kDtypeBf16;
     const EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorInitializationError;
     TcParams p;
@@ -958,6 +1018,7 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     p.scales = a.scales;
     p.zeros = a.zeros;
     p.y = a.y;
+    p.residual = a.epi == kEpiResidual ? a.residual : nullptr;
     p.partials = ws.partials;
     p.counters = ws.counters;
     p.status = status;
@@ -972,9 +1033,9 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     p.n_stages = plan.stages;
     p.total = (long long)plan.n_tiles * plan.spt;
     switch (plan.T) {
-        case 16: return launch_t<16>(p, plan.grid, stream);
-        case 32: return launch_t<32>(p, plan.grid, stream);
-        case 64: return launch_t<64>(p, plan.grid, stream);
+        case 16: return launch_t<16>(p, bf16, plan.grid, stream);
+        case 32: return launch_t<32>(p, bf16, plan.grid, stream);
+        case 64: return launch_t<64>(p, bf16, plan.grid, stream);
     }
     return cudaErrorInvalidValue;
 }
