@@ -193,11 +193,10 @@ typedef struct {
 
 /* y = epilogue(x @ W^T): w4a16_linear followed, in the same kernel, by the
  * step `epilogue` names (w4a16_epilogue).  W4A16_EPILOGUE_NONE is exactly
- * w4a16_linear.  The residual add runs on the warp-MMA rungs (up to 8 tokens)
- * and on the tcgen05 rungs (more than 8 tokens: one reading of the weights
- * for up to 64); SiLU-and-mul runs on the warp-MMA rungs only, more than 8
- * tokens as tiles of 8, each of which reads the weights.  A forced rung that
- * cannot take the epilogue: W4A16_ERR_UNSUPPORTED.
+ * w4a16_linear.  The other epilogues run on the warp-MMA rungs (up to 8
+ * tokens) and on the tcgen05 rungs (more than 8 tokens: one reading of the
+ * weights for up to 64; a SiLU-and-mul tile holds 64 outputs' gate and up
+ * rows), not on the CUDA-core rungs (a forced one: W4A16_ERR_UNSUPPORTED).
  *   residual  [M, N] fp16, 2-byte aligned, for W4A16_EPILOGUE_RESIDUAL (NULL
  *             otherwise: INVALID_ARG); it may be y itself (y += x @ W^T) but
  *             must not otherwise overlap y.
@@ -205,15 +204,16 @@ typedef struct {
  *             of 32: W4A16_ERR_UNSUPPORTED otherwise).
  * With split K the partial sums of h are reduced first and the epilogue applied
  * once to each output.  SiLU-and-mul always passes h through the split-K
- * workspace (S x M x N fp32, S >= 1 K slices, and one arrival counter per
- * block of rows) and applies the epilogue where a block's sums meet:
+ * workspace (on the warp-MMA rungs S x M x N fp32, S >= 1 K slices, and one
+ * arrival counter per block of rows; on the tcgen05 rungs two 128-row slots
+ * per CTA) and applies the epilogue where an output's gate and up sums meet:
  * W4A16_ERR_WORKSPACE if w4a16_init reserved too little. */
 int w4a16_linear_epilogue(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                           const uint32_t *zeros, int M, int N, int K, int group, int epilogue,
                           const uint16_t *residual, uint16_t *y, void *stream);
 
 /* w4a16_linear_epilogue with the 16-bit type `dtype` (w4a16_dtype) of x,
- * scales, residual and y.  bf16 runs on the rungs the epilogue allows, not on
+ * scales, residual and y.  bf16 runs on the warp-MMA and tcgen05 rungs, not on
  * the CUDA-core rungs.  On the warp-MMA rungs (up to 8 tokens) each token's
  * slice of x is staged as fp16 scaled by a power of two chosen from its
  * largest exponent (so any bf16 magnitude fits; bf16's 8 significant bits fit

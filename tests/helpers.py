@@ -19,6 +19,11 @@ ATOL = 1e-3
 # bf16 outputs: one rounding to 8 significant bits costs up to 2^-9 |y|, more
 # than the fp16 rule's relative term allows; the bound doubles that rounding
 RTOL_BF16 = 2.0 ** -8
+# bf16 outputs of the tcgen05 rungs, which round each restored weight once to
+# bf16 ((q - z) * s to 8 significant bits, as a bf16 dequantisation does):
+# the output's rounding (up to 2^-8 |y| just above a power of two) plus the
+# weights' roundings (up to 2^-9 each, summed with the products)
+RTOL_BF16_TC = 2.0 ** -7
 
 
 def tolerance(y_ref: np.ndarray, rtol: float = RTOL) -> float:

@@ -4,7 +4,9 @@ bf16 decode rounds) against the oracle's bf16 linear.
 x, scales, residual and y are bfloat16; the oracle decodes the same bit
 patterns and works in binary64.  Tolerance: the linear's rule with the
 relative term raised to 2^-8 (helpers.RTOL_BF16), since one rounding of y to
-bf16's 8 significant bits already costs up to 2^-9 |y|.
+bf16's 8 significant bits already costs up to 2^-9 |y|.  Layers of more than 8
+tokens run on the tcgen05 rung, which also rounds each restored weight once to
+bf16: there the relative term is 2^-7 (helpers.RTOL_BF16_TC).
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ import torch
 
 import oracle
 import synthetic_inputs as si
-from helpers import assert_close, sample_rows
+from helpers import RTOL_BF16_TC, assert_close, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -87,7 +89,9 @@ def test_bf16_linear_matches_oracle(w4, rung, M, N, K):
     y = run(w4, rung, x, qw, s, zw)
     if y is None:
         pytest.skip("rung cannot run this shape")
-    assert_close(y, reference(x, qw, s, zw), f"bf16 M={M} N={N} K={K} rung={rung}")
+    # more than 8 tokens run on the tcgen05 rung (weights restored to bf16)
+    rtol = RTOL_BF16_TC if rung == AUTO and M > 8 else None
+    assert_close(y, reference(x, qw, s, zw), f"bf16 M={M} N={N} K={K} rung={rung}", rtol=rtol)
 
 
 def test_bf16_range_beyond_fp16(w4):
@@ -203,6 +207,7 @@ def test_bf16_on_forced_rungs(w4):
         w4.w4a16_set_forced_rung(2)
         y = w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV))
         torch.cuda.synchronize()
-        assert_close(y, reference(x, qw, s, zw), "bf16 on the forced tcgen05 rung")
+        assert_close(y, reference(x, qw, s, zw), "bf16 on the forced tcgen05 rung",
+                     rtol=RTOL_BF16_TC)
     finally:
         w4.w4a16_set_forced_rung(prev)

@@ -130,9 +130,8 @@ def test_silu_mul_full_gate_up_sampled(w4, rung, M):
 
 @pytest.mark.parametrize("M", [9, 20])
 def test_epilogues_beyond_8_tokens(w4, M):
-    # more than 8 tokens: the residual add on the tcgen05 rung (one reading
-    # of the weights for up to 64 tokens), SiLU-and-mul in tiles of 8 on the
-    # warp-MMA rungs (the output rows offset per tile)
+    # more than 8 tokens: both epilogues on the tcgen05 rung (one reading of
+    # the weights for up to 64 tokens)
     N, K = 1024, 2048
     seed = si.config_seed(86, 0, M)
     x = si.x(seed, M, K)
@@ -147,7 +146,7 @@ def test_epilogues_beyond_8_tokens(w4, M):
     w4.w4a16_probe_reset()
     y = _epilogue(w4, AUTO, x.to(DEV), qw, s, zw, w4.EPILOGUE_SILU_MUL, None, _nan(M, N // 2))
     c = w4.w4a16_probe_counts()
-    assert c[w4.RUNG_MMA] + c[w4.RUNG_MMA_SPLITK] == (M + 7) // 8 and sum(c) == (M + 7) // 8
+    assert c[w4.RUNG_TC] + c[w4.RUNG_TC_SPLITK] == 1 and sum(c) == 1
     assert_close(y, oracle.silu_mul(h), f"silu_mul M={M}")
 
 

@@ -29,7 +29,7 @@ import torch
 
 import oracle
 import synthetic_inputs as si
-from helpers import assert_close
+from helpers import RTOL_BF16_TC, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -324,7 +324,8 @@ def test_invariants_through_linear_ex(w4, dtype, M):
     y = w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV))
     y8 = w4.w4a16_linear_ex(x8.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV))
     torch.cuda.synchronize()
-    assert_close(y, _ref(x, qw, s, zw, name), f"linear_ex {name} M={M}")
+    rtol = RTOL_BF16_TC if dtype == torch.bfloat16 and M > 8 else None  # the tcgen05 rung
+    assert_close(y, _ref(x, qw, s, zw, name), f"linear_ex {name} M={M}", rtol=rtol)
     a, b = y.double().cpu().numpy(), y8.double().cpu().numpy()
     lo = 2.0 ** -14 if dtype == torch.float16 else 2.0 ** -126
     mask = (np.abs(8 * a) >= lo) & (np.abs(a) >= lo) & (np.abs(8 * a) < 60000)

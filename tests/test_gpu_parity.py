@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import synthetic_inputs as si
-from helpers import Case, assert_close, sample_rows, sampled_reference
+from helpers import RTOL_BF16_TC, Case, assert_close, sample_rows, sampled_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -459,4 +459,5 @@ def test_random_sweep_every_path(w4):
             ref = oracle.add_residual(ref, bits(res), name)
         elif epi == w4.EPILOGUE_SILU_MUL:
             ref = oracle.silu_mul(ref)
-        assert_close(y, ref, f"M={M} N={N} K={K} epi={epi} {name}")
+        rtol = RTOL_BF16_TC if name == "bf16" and M > 8 else None  # the tcgen05 rung
+        assert_close(y, ref, f"M={M} N={N} K={K} epi={epi} {name}", rtol=rtol)

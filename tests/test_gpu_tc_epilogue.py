@@ -1,13 +1,15 @@
-"""The residual add and bf16 layers on the tcgen05 rung (more than 8 tokens).
+"""The fused epilogues and bf16 layers on the tcgen05 rung (more than 8 tokens).
 
-A layer of more than 8 tokens with a residual add (the output projections:
-haowenji.com V100 decode article, the add-back merged into the matmul's
-output stage) or with bf16 activations and scales (forum.sourcefind.cn thread
-"vLLM on Hygon Z100": activations "fp16 or bf16") runs on the tcgen05 rung,
-which reads the weights once for up to 64 tokens.  It restores each weight to
-the layer's 16-bit type ((q - z) * s rounded once) and accumulates the
-tensor-core products in fp32.  The probe counters show which rung computed
-the layer; every output is compared with the oracle.
+A layer of more than 8 tokens runs on the tcgen05 rung, which reads the
+weights once for up to 64 tokens.  That holds for a residual add (the output
+projections: haowenji.com V100 decode article, the add-back merged into the
+matmul's output stage), for SiLU-and-mul after a fused gate+up projection
+(forum.sourcefind.cn thread "vLLM on Hygon Z100", section 二), and for bf16
+activations and scales (the same thread: activations "fp16 or bf16").  The
+rung restores each weight to the layer's 16-bit type ((q - z) * s rounded
+once) and accumulates the tensor-core products in fp32.  A SiLU-and-mul tile
+holds 64 gate rows and their up rows N/2 below.  The probe counters show which
+rung computed the layer; every output is compared with the oracle.
 """
 import numpy as np
 import pytest
@@ -15,7 +17,7 @@ import torch
 
 import oracle
 import synthetic_inputs as si
-from helpers import assert_close
+from helpers import RTOL_BF16_TC, assert_close
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -58,6 +60,11 @@ def _reference(x, qw, s, zw, dt, residual=None):
     return h if residual is None else oracle.add_residual(h, _bits(residual), name)
 
 
+def _rtol(dt):
+    # bf16 on this rung: each weight is restored to bf16 once
+    return RTOL_BF16_TC if dt == torch.bfloat16 else None
+
+
 def _tc_count(w4):
     c = w4.w4a16_probe_counts()
     return c[w4.RUNG_TC] + c[w4.RUNG_TC_SPLITK], sum(c)
@@ -82,7 +89,8 @@ def test_residual_on_the_tc_rung(w4, dt, M, N, K):
     torch.cuda.synchronize()
     tc, total = _tc_count(w4)
     assert tc == total == (M + 63) // 64, "the layer ran on another rung"
-    assert_close(y, _reference(x, qw, s, zw, dt, r), f"residual {dt} M={M} N={N} K={K}")
+    assert_close(y, _reference(x, qw, s, zw, dt, r), f"residual {dt} M={M} N={N} K={K}",
+                 rtol=_rtol(dt))
     # in place: the residual is y itself (y += x W^T)
     y2 = r.to(DEV).clone()
     w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV),
@@ -101,14 +109,36 @@ def test_bf16_on_the_tc_rung(w4, M, N, K):
     torch.cuda.synchronize()
     tc, total = _tc_count(w4)
     assert tc == total == (M + 63) // 64
-    assert_close(y, _reference(x, qw, s, zw, dt), f"bf16 M={M} N={N} K={K}")
+    assert_close(y, _reference(x, qw, s, zw, dt), f"bf16 M={M} N={N} K={K}", rtol=_rtol(dt))
+
+
+# SiLU-and-mul tiles: 64 outputs each (N/2 a multiple of 16; ragged last
+# tile), the fused gate+up shape of the 27B decode layer, tiles of 64 tokens
+SILU_SHAPES = [(9, 320, 1024), (16, 2048, 2048), (33, 1056, 1408), (64, 34816, 5120),
+               (100, 640, 6144)]
+
+
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("M,N,K", SILU_SHAPES)
+def test_silu_mul_on_the_tc_rung(w4, dt, M, N, K):
+    seed = si.config_seed(91, M, N % 16)
+    x, qw, s, zw = _case(seed, M, N, K, dt)
+    y = torch.full((M, N // 2), float("nan"), dtype=dt, device=DEV)
+    w4.w4a16_probe_reset()
+    w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV),
+                       epilogue=w4.EPILOGUE_SILU_MUL, y=y)
+    torch.cuda.synchronize()
+    tc, total = _tc_count(w4)
+    assert tc == total == (M + 63) // 64, "the layer ran on another rung"
+    ref = oracle.silu_mul(_reference(x, qw, s, zw, dt))
+    assert_close(y, ref, f"silu_mul {dt} M={M} N={N} K={K}", rtol=_rtol(dt))
 
 
 @pytest.mark.parametrize("rung", [2, 3])
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 def test_forced_tc_rungs_with_epilogue_and_bf16(w4, rung, dt):
     # whole tiles (tc) and stream-K (tc_splitk), from 4 tokens up
-    for M, N, K in [(4, 1000, 2048), (24, 300, 5120)]:
+    for M, N, K in [(4, 1024, 2048), (24, 320, 5120)]:
         seed = si.config_seed(89, M, rung)
         x, qw, s, zw = _case(seed, M, N, K, dt)
         r = si.residual(seed, M, N).float().to(dt)
@@ -119,20 +149,21 @@ def test_forced_tc_rungs_with_epilogue_and_bf16(w4, rung, dt):
                                    epilogue=w4.EPILOGUE_RESIDUAL, residual=r.to(DEV))
             torch.cuda.synchronize()
             assert w4.w4a16_probe_counts()[rung] >= 1
-            # SiLU-and-mul is not this rung's
-            with pytest.raises(w4.W4A16Error) as e:
-                w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV),
-                                   epilogue=w4.EPILOGUE_SILU_MUL)
-            assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+            ys = w4.w4a16_linear_ex(x.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV),
+                                    epilogue=w4.EPILOGUE_SILU_MUL)
+            torch.cuda.synchronize()
         finally:
             w4.w4a16_set_forced_rung(prev)
-        assert_close(y, _reference(x, qw, s, zw, dt, r), f"forced rung {rung} {dt} M={M}")
+        assert_close(y, _reference(x, qw, s, zw, dt, r), f"forced rung {rung} {dt} M={M}",
+                     rtol=_rtol(dt))
+        assert_close(ys, oracle.silu_mul(_reference(x, qw, s, zw, dt)),
+                     f"forced rung {rung} {dt} M={M} SiLU-and-mul", rtol=_rtol(dt))
 
 
 def test_large_scales_with_residual_on_the_tc_rung(w4):
     # scales that the fp16 restore cannot hold ((q - z) * 65504 overflows):
     # those rows are recomputed exactly on the CUDA cores, residual included
-    M, N, K = 16, 300, 1024
+    M, N, K = 16, 320, 1024
     rng = np.random.default_rng(90)
     seed = si.config_seed(90)
     qw, s, zw = si.layer(seed, N, K)
@@ -150,3 +181,11 @@ def test_large_scales_with_residual_on_the_tc_rung(w4):
     ref = _reference(x, qw, s, zw, torch.float16, r)
     assert np.isfinite(ref).all() and np.abs(ref).max() < 60000
     assert_close(y, ref, "large scales with the residual")
+    # and through SiLU-and-mul (the exact rows' sums meet their partner rows)
+    x2 = (x.double() / 64.0).to(torch.float16)
+    ys = w4.w4a16_linear_ex(x2.to(DEV), qw.to(DEV), s.to(DEV), zw.to(DEV),
+                            epilogue=w4.EPILOGUE_SILU_MUL)
+    torch.cuda.synchronize()
+    refs = oracle.silu_mul(_reference(x2, qw, s, zw, torch.float16))
+    assert np.isfinite(refs).all() and np.abs(refs).max() < 60000
+    assert_close(ys, refs, "large scales with SiLU-and-mul")

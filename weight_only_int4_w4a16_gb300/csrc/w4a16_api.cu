@@ -122,17 +122,14 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi 
     const int G = K / kGroup;
     if (epi != kEpiNone || dtype != kDtypeF16) {
         // the epilogues and bf16 data run in the warp-MMA kernel (tiles of up
-        // to 8 tokens, each reading the weights) and, the residual add and bf16,
-        // in the tcgen05 kernel (up to 64 tokens per reading of the weights);
-        // SiLU-and-mul combines rows N/2 apart, which a 128-row tcgen05 tile
-        // does not hold
-        const bool tc_ok = epi != kEpiSiluMul;
-        if (forced != W4A16_RUNG_AUTO && !is_mma(forced) && !(is_tc(forced) && tc_ok))
+        // to 8 tokens, each reading the weights) and in the tcgen05 kernel (up
+        // to 64 tokens per reading of the weights), not on the CUDA cores
+        if (forced != W4A16_RUNG_AUTO && !is_mma(forced) && !is_tc(forced))
             return {forced, W4A16_ERR_UNSUPPORTED};
         if (forced == W4A16_RUNG_AUTO) {
-            if (M > kMmaMaxTokens && tc_ok) {
+            if (M > kMmaMaxTokens) {
                 const int Mtc = M < kTcMaxTokens ? M : kTcMaxTokens;
-                TcPlan t = plan_tc(Mtc, N, K, -1, dev);
+                TcPlan t = plan_tc(Mtc, N, K, -1, dev, epi);
                 return {t.S > 1 ? W4A16_RUNG_TC_SPLITK : W4A16_RUNG_TC, W4A16_OK};
             }
             MmaPlan p = plan_mma(Mt, N, K, -1, dev, epi);
@@ -183,7 +180,7 @@ int split_rule(int rung) {
 bool launch_needs(int rung, int Mt, int N, int K, const DeviceInfo &dev, size_t *bytes,
                   int *counters, int epi) {
     if (is_tc(rung)) {
-        TcPlan p = plan_tc(Mt, N, K, split_rule(rung), dev);
+        TcPlan p = plan_tc(Mt, N, K, split_rule(rung), dev, epi);
         *bytes = p.ws_bytes;
         *counters = p.S > 1 ? p.n_tiles : 0;
         return p.ok;
@@ -241,7 +238,7 @@ int launch_linear(const LinearArgs &a, int rung, const State &st, cudaStream_t s
         if (a.residual) t.residual = a.residual + (size_t)m0 * ycols;
         t.M = Mt;
         if (is_tc(rung)) {
-            TcPlan p = plan_tc(Mt, a.N, a.K, split_rule(rung), st.dev);
+            TcPlan p = plan_tc(Mt, a.N, a.K, split_rule(rung), st.dev, a.epi);
             e = launch_tc(t, p, st.ws, st.ws.status, stream);
         } else if (is_mma(rung)) {
             MmaPlan p = plan_mma(Mt, a.N, a.K, split_rule(rung), st.dev, a.epi);

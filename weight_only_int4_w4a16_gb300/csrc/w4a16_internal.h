@@ -103,8 +103,9 @@ struct TcPlan {
     size_t ws_bytes;   // workspace: stream-K partial sums
 };
 
-// split: 0 = whole tiles only, 1 = stream-K, -1 = planner decides.
-TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev);
+// split: 0 = whole tiles only, 1 = stream-K, -1 = planner decides.  epi: the
+// linear's epilogue (SiLU-and-mul tiles hold 64 outputs' gate and up rows).
+TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev, int epi = kEpiNone);
 // status: device word the kernel ORs an error code into when a bounded wait expires.
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream);

@@ -103,6 +103,7 @@ struct TcParams {
     unsigned *counters;  // stream-K: one per tile, zero between launches
     int *status;
     int N, K, G, ZW, M;
+    int silu;          // SiLU-and-mul: a tile is 64 gate rows and the 64 up rows N/2 below
     int n_tiles, spt;  // tiles, stages per tile
     int streamk;
     int n_stages;      // shared-memory stages
@@ -379,6 +380,20 @@ __device__ __forceinline__ int stage_groups(const TcParams &p, int j) {
     return min(kSG, p.G - kSG * j);
 }
 
+// Weight row of tile row r (0..127): rows 0..63 and 64..127 of a tile come as
+// two TMA boxes of 64 rows.  A plain tile is 128 consecutive rows; with
+// SiLU-and-mul it is 64 gate rows and the matching up rows N/2 below, so that
+// both halves of 64 outputs meet in one tile.
+__device__ __forceinline__ int tile_row(const TcParams &p, int t, int r) {
+    if (p.silu) return (r < 64 ? 0 : p.N / 2) + 64 * t + (r & 63);
+    return kTileN * t + r;
+}
+// whether tile row r of tile t is a row of the weight matrix
+__device__ __forceinline__ bool tile_row_valid(const TcParams &p, int t, int r) {
+    if (p.silu) return 64 * t + (r & 63) < p.N / 2;
+    return kTileN * t + r < p.N;
+}
+
 // The CTA whose range holds stage st (stream-K).
 __device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
     return (int)(((st + 1) * (long long)gridDim.x - 1) / p.total);
@@ -424,8 +439,8 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
                 part[(size_t)tt * kTileN] = acc[i];
             } else {
                 const size_t o = (size_t)tt * p.N + n;
-                const float r = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
-                p.y[o] = float_to_f16<kBf16>(acc[i] + r);
+                const float res = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
+                p.y[o] = float_to_f16<kBf16>(acc[i] + res);
             }
         }
     }
@@ -523,15 +538,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 const uint32_t bar = smem_u32(full + s);
                 uint8_t *st = sm_stage + (size_t)s * C::kStageBytes;
                 if (lane == 0) {
+                    // tile rows 0..63, then 64..127: [half][group][64 rows][64 bytes]
                     mbar_arrive_expect_tx(bar, (uint32_t)kStageW);
-                    tma_load_3d(smem_u32(st), &p.wmap, 0, t * kTileN, kSG * j, bar, pol);
+                    tma_load_3d(smem_u32(st), &p.wmap, 0, tile_row(p, t, 0), kSG * j, bar, pol);
+                    tma_load_3d(smem_u32(st + kStageW / 2), &p.wmap, 0, tile_row(p, t, 64), kSG * j,
+                                bar, pol);
                 }
                 uint8_t *m = st + kStageW;
 #pragma unroll
                 for (int i = 0; i < kTileN / 32; ++i) {
-                    const int r = lane + 32 * i, n = t * kTileN + r;
+                    const int r = lane + 32 * i, n = tile_row(p, t, r);
                     const uint32_t dst = smem_u32(m + r * 16);
-                    if (n < p.N) {
+                    if (tile_row_valid(p, t, r)) {
                         const uintptr_t a0 =
                             (uintptr_t)(p.scales + (size_t)n * p.G + kSG * j) & ~(uintptr_t)3;
 #pragma unroll
@@ -626,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         int c = 0, sc = 0;
         bool ok = true;
         while (ok && walk_next(p, wk, t, j0, j1)) {
-            const int n = t * kTileN + r;
-            const __half *srow = p.scales + (size_t)(n < p.N ? n : 0) * p.G;
+            const int n = tile_row(p, t, r);
+            const __half *srow = p.scales + (size_t)(tile_row_valid(p, t, r) ? n : 0) * p.G;
             for (int j = j0; j < j1 && ok; ++j, ++sc) {
                 const int s = sc % NS, ng = stage_groups(p, j);
                 const uint8_t *st = sm_stage + (size_t)s * C::kStageBytes;
@@ -648,7 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 for (int k2 = 0; k2 < 2; ++k2) {
                     const int gi = gfirst + 2 * k2;
                     if (gi < ng) {
-                        const uint8_t *rowp = st + gi * kGroupBytes + r * 64;
+                        const uint8_t *rowp =
+                            st + (r >> 6) * (kStageW / 2) + gi * (kGroupBytes / 2) + (r & 63) * 64;
                         w[k2][0] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half) ^ sw));
                         w[k2][1] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half + 1) ^ sw));
                     }
@@ -765,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         bool ok = true;
         while (ok && walk_next(p, wk, t, j0, j1)) {
             const int dset = q % C::kDSets, duse = q / C::kDSets;
-            const int n = t * kTileN + r;
-            const bool vrow = n < p.N;
+            const int n = tile_row(p, t, r);
+            const bool vrow = tile_row_valid(p, t, r);
             const int g0 = kSG * j0, g1 = min(p.G, kSG * j1);
             const int c0 = c;
             c += g1 - g0;
@@ -788,14 +807,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             }
             tc_fence_after();
             const bool whole = j0 == 0 && j1 == p.spt;
-            // part of a tile: this CTA's partial-sum slot (the last CTA of the
-            // tile adds the slots in K order, which is CTA order)
+            // y straight from the sums: a whole tile without SiLU-and-mul.  Else
+            // the sums go to this CTA's partial-sum slot: part of a tile (the
+            // last CTA of the tile adds the slots in K order, which is CTA
+            // order), or a whole SiLU-and-mul tile, whose gate and up rows
+            // meet there (slot 2b + 1 for it: this CTA's last partial segment,
+            // which also uses it, comes after every whole one)
+            const bool direct = whole && !p.silu;
             const int slot =
-                2 * (int)blockIdx.x + (range_begin(p, blockIdx.x) / p.spt == t ? 0 : 1);
+                2 * (int)blockIdx.x +
+                (whole || range_begin(p, blockIdx.x) / p.spt != t ? 1 : 0);
             float *part = p.partials + (size_t)slot * p.M * kTileN + r;
             auto put = [&](int tt, float v) {
                 if (tt >= p.M) return;
-                if (whole) {
+                if (direct) {
                     if (vrow) {
                         // y = h (+ residual), one rounding
                         const size_t o = (size_t)tt * p.N + n;
@@ -840,50 +865,79 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(d_empty + dset));
             // a row whose scales may overflow the fp16 restore: exact on the CUDA cores
-            if (big) exact_row<kBf16>(p, n, g0, g1, whole, part);
-            if (!whole) {
+            if (big) exact_row<kBf16>(p, n, g0, g1, direct, part);
+            if (!direct) {
                 __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                // the CTAs whose slots hold the tile's sums: this one (a whole
+                // tile), or every CTA whose range meets the tile
                 const long long ts0 = (long long)t * p.spt;
-                const int b0 = cta_of(p, ts0), b1 = cta_of(p, ts0 + p.spt - 1);
-                if (threadIdx.x == 0) {
-                    const unsigned prev = atomicAdd(p.counters + t, 1u);
-                    *s_last = prev == (unsigned)(b1 - b0) ? 1 : 0;
+                const int b0 = whole ? (int)blockIdx.x : cta_of(p, ts0);
+                const int b1 = whole ? (int)blockIdx.x : cta_of(p, ts0 + p.spt - 1);
+                if (!whole) {
+                    if (threadIdx.x == 0) {
+                        const unsigned prev = atomicAdd(p.counters + t, 1u);
+                        *s_last = prev == (unsigned)(b1 - b0) ? 1 : 0;
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
                 }
-                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
-                if (*s_last) {
+                if (whole || *s_last) {
                     __threadfence();
-                    if (vrow) {
-                        // the pieces' sums in K order (CTA order), 16 tokens per
-                        // batch of independent loads (one round trip each, not
-                        // one per token and piece)
-                        for (int t0 = 0; t0 < p.M; t0 += 16) {
-                            float sum[16];
+                    // the sums of tile row rr over the slots in K order (CTA
+                    // order), 16 tokens per batch of independent loads (one
+                    // round trip each, not one per token and piece)
+                    auto gather = [&](int rr, int t0, float (&sum)[16]) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) sum[i] = 0.f;
-                            for (int b = b0; b <= b1; ++b) {
-                                const int sl = 2 * b + (range_begin(p, b) / p.spt == t ? 0 : 1);
-                                const float *src = p.partials + ((size_t)sl * p.M + t0) * kTileN + r;
-                                float v[16];
+                        for (int i = 0; i < 16; ++i) sum[i] = 0.f;
+                        for (int b = b0; b <= b1; ++b) {
+                            const int sl = 2 * b + (whole || range_begin(p, b) / p.spt != t ? 1 : 0);
+                            const float *src = p.partials + ((size_t)sl * p.M + t0) * kTileN + rr;
+                            float v[16];
 #pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    v[i] = t0 + i < p.M ? __ldcg(src + (size_t)i * kTileN) : 0.f;
+                            for (int i = 0; i < 16; ++i)
+                                v[i] = t0 + i < p.M ? __ldcg(src + (size_t)i * kTileN) : 0.f;
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) sum[i] += v[i];
+                            for (int i = 0; i < 16; ++i) sum[i] += v[i];
+                        }
+                    };
+                    if (!p.silu) {
+                        if (vrow) {
+                            for (int t0 = 0; t0 < p.M; t0 += 16) {
+                                float sum[16];
+                                gather(r, t0, sum);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    if (t0 + i >= p.M) continue;
+                                    const size_t o = (size_t)(t0 + i) * p.N + n;
+                                    const float res =
+                                        p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
+                                    p.y[o] = float_to_f16<kBf16>(sum[i] + res);
+                                }
                             }
+                        }
+                    } else if (r < 64 && vrow) {
+                        // SiLU-and-mul: the gate row's thread takes its up row
+                        // (tile row r + 64): y = silu(g) * u, silu(g) = g / (1 + e^-g)
+                        const int ycols = p.N / 2, jcol = 64 * t + r;
+                        for (int t0 = 0; t0 < p.M; t0 += 16) {
+                            float gs[16], us[16];
+                            gather(r, t0, gs);
+                            gather(r + 64, t0, us);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 if (t0 + i >= p.M) continue;
-                                const size_t o = (size_t)(t0 + i) * p.N + n;
-                                const float r = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
-                                p.y[o] = float_to_f16<kBf16>(sum[i] + r);
+                                const float g = gs[i];
+                                p.y[(size_t)(t0 + i) * ycols + jcol] =
+                                    float_to_f16<kBf16>(us[i] * (g / (1.f + expf(-g))));
                             }
                         }
                     }
-                    if (threadIdx.x == 0) p.counters[t] = 0u;  // ready for the next launch
+                    if (!whole && threadIdx.x == 0) p.counters[t] = 0u;  // ready for the next launch
                 }
-                // s_last is written again only after the next such segment's first
-                // barrier, which every epilogue thread reaches after reading it
+                // the slot and s_last are written again only after the next such
+                // segment's first barrier, which every epilogue thread reaches
+                // after its reads
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
             }
             ++q;
         }
@@ -940,12 +994,14 @@ cudaError_t launch_t(const TcParams &p, bool bf16, int grid, cudaStream_t stream
 
 }  // namespace
 
-TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
+TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
     TcPlan pl{};
     pl.M = M;
     pl.T = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int G = K / kGroup;
-    pl.n_tiles = (N + kTileN - 1) / kTileN;
+    const bool silu = epi == kEpiSiluMul;
+    // SiLU-and-mul: 64 outputs (their gate and up rows) per tile
+    pl.n_tiles = silu ? (N / 2 + 63) / 64 : (N + kTileN - 1) / kTileN;
     pl.spt = (G + kSG - 1) / kSG;
     pl.stages = pl.T == 16 ? stages_for<16>() : (pl.T == 32 ? stages_for<32>() : stages_for<64>());
     const long long total = (long long)pl.n_tiles * pl.spt;
@@ -960,7 +1016,9 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.S = streamk ? 2 : 1;
     if (streamk) pl.grid = total < slots ? (int)total : slots;
     else pl.grid = pl.n_tiles < slots ? pl.n_tiles : slots;
-    pl.ws_bytes = streamk ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0;
+    // partial-sum slots: split tiles, and whole SiLU-and-mul tiles (where the
+    // gate and up rows meet)
+    pl.ws_bytes = streamk || silu ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0;
     pl.ok = G >= 1 && pl.stages >= 2;
     return pl;
 }
@@ -981,8 +1039,6 @@ cudaError_t tc_init(const DeviceInfo &dev) {
 
 cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
                       cudaStream_t stream) {
-    // SiLU-and-mul combines rows N/2 apart, which a 128-row tile does not hold
-    if (a.epi == kEpiSiluMul) return cudaErrorInvalidValue;
     const bool bf16 = a.dtype == kDtypeBf16;
     const EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorInitializationError;
@@ -990,10 +1046,11 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     memset(&p, 0, sizeof(p));
     const int G = a.K / kGroup;
     {
-        // qweight as (word in group, row, group): a box of 128 rows x 4 groups
+        // qweight as (word in group, row, group): a box of 64 rows x 4 groups
+        // (a tile's stage is two of them)
         const cuuint64_t dims[3] = {16, (cuuint64_t)a.N, (cuuint64_t)G};
         const cuuint64_t strides[2] = {(cuuint64_t)a.K / 2, 64};
-        const cuuint32_t box[3] = {16, (cuuint32_t)kTileN, (cuuint32_t)kSG};
+        const cuuint32_t box[3] = {16, (cuuint32_t)(kTileN / 2), (cuuint32_t)kSG};
         const cuuint32_t estr[3] = {1, 1, 1};
         CUresult r = encode(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1027,6 +1084,7 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
     p.G = G;
     p.ZW = (G + 7) / 8;
     p.M = a.M;
+    p.silu = a.epi == kEpiSiluMul;
     p.n_tiles = plan.n_tiles;
     p.spt = plan.spt;
     p.streamk = plan.S > 1;
