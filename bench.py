@@ -959,7 +959,11 @@ def main():
         for label, M, N, K, epi in [("gate_up_silu_M1_K5120_N34816", 1, 34816, 5120, 2),
                                     ("gate_up_silu_M4_K5120_N34816", 4, 34816, 5120, 2),
                                     ("gate_up_silu_M8_K5120_N34816", 8, 34816, 5120, 2),
+                                    ("gate_up_silu_M16_K5120_N34816", 16, 34816, 5120, 2),
+                                    ("gate_up_silu_M64_K5120_N34816", 64, 34816, 5120, 2),
                                     ("down_residual_M4_K17408_N5120", 4, 5120, 17408, 1),
+                                    ("down_residual_M16_K17408_N5120", 16, 5120, 17408, 1),
+                                    ("down_residual_M64_K17408_N5120", 64, 5120, 17408, 1),
                                     ("o_residual_M4_K6144_N5120", 4, 5120, 6144, 1)]:
             t = time_single(w4, M, N, K, 5, dev, flush=flush, epi=epi)[-1]
             t0 = time_single(w4, M, N, K, 5, dev, flush=flush)[-1]
