@@ -399,12 +399,30 @@ __device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
     return (int)(((st + 1) * (long long)gridDim.x - 1) / p.total);
 }
 
+// y[t0 .. t0 + 15][n] = v (+ residual), one rounding each.  The residual may
+// be y itself (in place), so every residual value is read before any output
+// is written: sixteen independent loads, one round trip, where a load after
+// each store would wait for the store (the compiler must assume they alias).
+template <bool kBf16>
+__device__ __forceinline__ void store_y16(const TcParams &p, int n, int t0, const float (&v)[16]) {
+    float res[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        res[i] = p.residual && t0 + i < p.M
+                     ? f16_to_float<kBf16>(p.residual[(size_t)(t0 + i) * p.N + n])
+                     : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = float_to_f16<kBf16>(v[i] + res[i]);
+}
+
 // ---------------------------------------------------------------------------
 // The outputs of row n over groups [g0, g1) for every token, exactly: w =
 // (q - z) * s in fp32 (at most 15 significant bits), summed in increasing k,
 // 16 tokens at a time; to y (a whole tile: plus the residual, if any, then one
-// rounding) or to the partial-sum slot `part` (row n's column of it).  For rows whose scales reach 4096 (or are Inf or
-// NaN), where the fp16 restore of the tensor-core path may overflow.  Kept
+// rounding) or to the partial-sum slot `part` (row n's column of it).  For
+// rows whose scales reach 4096 (or are Inf or NaN), where the fp16 restore of
+// the tensor-core path may overflow.  Kept
 // out of line: it is rare, and its registers stay out of the kernel's.
 // ---------------------------------------------------------------------------
 template <bool kBf16>
@@ -818,17 +836,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 2 * (int)blockIdx.x +
                 (whole || range_begin(p, blockIdx.x) / p.spt != t ? 1 : 0);
             float *part = p.partials + (size_t)slot * p.M * kTileN + r;
-            auto put = [&](int tt, float v) {
-                if (tt >= p.M) return;
+            // 16 tokens' outputs of this row: y = h (+ residual), one rounding,
+            // or the partial sums
+            auto put16 = [&](int t0, float (&v)[16]) {
                 if (direct) {
-                    if (vrow) {
-                        // y = h (+ residual), one rounding
-                        const size_t o = (size_t)tt * p.N + n;
-                        if (p.residual) v += f16_to_float<kBf16>(p.residual[o]);
-                        p.y[o] = float_to_f16<kBf16>(v);
-                    }
+                    if (vrow) store_y16<kBf16>(p, n, t0, v);
                 } else {
-                    part[(size_t)tt * kTileN] = v;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (t0 + i < p.M) part[(size_t)(t0 + i) * kTileN] = v[i];
                 }
             };
             const uint32_t taddr =
@@ -856,10 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                         }
                     }
                 }
-                if (!big) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) put(t0 + i, sum[i]);
-                }
+                if (!big) put16(t0, sum);
             }
             tc_fence_before();
             __syncwarp();
@@ -905,14 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             for (int t0 = 0; t0 < p.M; t0 += 16) {
                                 float sum[16];
                                 gather(r, t0, sum);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    if (t0 + i >= p.M) continue;
-                                    const size_t o = (size_t)(t0 + i) * p.N + n;
-                                    const float res =
-                                        p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
-                                    p.y[o] = float_to_f16<kBf16>(sum[i] + res);
-                                }
+                                store_y16<kBf16>(p, n, t0, sum);
                             }
                         }
                     } else if (r < 64 && vrow) {
