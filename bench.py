@@ -938,7 +938,8 @@ def main():
     if not args.no_extra and rank == 0:
         flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
         singles = {}
-        for label, M, N, K, cfg in [("cfg1_M1_K5120_N34816", 1, 34816, 5120, 1),
+        for label, M, N, K, cfg in [("cfg0_M1_K512_N1024", 1, 1024, 512, 0),
+                                    ("cfg1_M1_K5120_N34816", 1, 34816, 5120, 1),
                                     ("cfg2_M4_K17408_N5120", 4, 5120, 17408, 2),
                                     ("cfg2_M8_K17408_N5120", 8, 5120, 17408, 2)] + \
                 [(f"cfg4_M{m}_K5120_N27648", m, 27648, 5120, 4) for m in (1, 2, 4, 8, 16, 32, 64)]:
@@ -1001,7 +1002,7 @@ def main():
         if "single_linear_l2_flushed" in extra:
             line["singles"] = {k: {f: v[f] for f in ("us", "GBps", "frac_of_peak", "rung")}
                                for k, v in extra["single_linear_l2_flushed"].items()
-                               if k.startswith(("cfg1", "cfg2"))}
+                               if k.startswith(("cfg0", "cfg1", "cfg2"))}
         line["extra"] = extra
         print(json.dumps(line), flush=True)
     if world > 1:
