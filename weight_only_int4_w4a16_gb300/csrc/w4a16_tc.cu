@@ -26,9 +26,12 @@
 //     weights (each row a 256-byte run of memory, 64-byte swizzle; L2
 //     evict-first, read once), and its lanes copy the rows' scale and zeros
 //     words (cp.async) next to it;
-//   warps 4..19, two teams of 8 taking alternate groups, restore a group:
-//     thread = one row (its TMEM lane) and 64 inputs; it reads its words of
-//     the stage at once (so the stage is free for the next box early), then
+//   warps 4..19, four teams of 4 (team i takes the groups c with c % 4 == i),
+//     restore a group: thread = one row (its TMEM lane) and its 128 inputs
+//     (a team of 4 warps has more registers per thread and fewer handoffs
+//     per group than two teams of 8 with 64 inputs a thread: 43.3 -> 41.1 us
+//     at M = 16, 48.7 -> 45.3 at M = 32); it reads its words of the stage at
+//     once (so the stage is free for the next box early), then
 //     the nibble unpack splices (1024 + q) or (64 + q) into fp16, subtracts the
 //     matching (1024 + z) / (64 + z) exactly, multiplies by s (one rounding)
 //     and puts the pairs in k order; tcgen05.st puts the values in tensor
@@ -67,8 +70,10 @@ constexpr int kStageW = kSG * kGroupBytes;     // 32 KB
 constexpr int kAStages = 4;                    // A (restored group) buffers in TMEM
 constexpr int kACols = kGroup / 2;             // 64 TMEM columns per A buffer
 constexpr int kEpiWarps = 4;
-constexpr int kDeqTeams = 2;                   // restore teams take alternate groups
-constexpr int kDeqWarps = 8;                   // warps per team (2 per TMEM lane quarter)
+constexpr int kDeqTeams = 4;                   // restore teams: group c to team c % 4
+constexpr int kDeqWarps = 4;                   // warps per team (one per TMEM lane quarter)
+constexpr int kHalves = 8 / kDeqWarps;         // 64-input halves of a group row per thread
+constexpr int kPerTeam = kSG / kDeqTeams;      // a team's groups per stage
 constexpr int kTmaWarp = kEpiWarps + kDeqTeams * kDeqWarps;  // 20
 constexpr int kMmaWarp = kTmaWarp + 1;                       // 21 .. 24
 constexpr int kMmaWarps = 4;                                 // MMA issuers: group c to c % 4
@@ -648,10 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         }
     } else if (warp >= kEpiWarps) {
         // ------------------------------------------------ restore teams
-        const int team = (warp - kEpiWarps) / kDeqWarps;  // groups c with c % 2 == team
-        const int dw = (warp - kEpiWarps) % kDeqWarps;    // 0..7 within the team
+        const int team = (warp - kEpiWarps) / kDeqWarps;  // groups c with c % kDeqTeams == team
+        const int dw = (warp - kEpiWarps) % kDeqWarps;    // warp within the team
         const int quarter = warp & 3;                     // TMEM lanes 32 * quarter ..
-        const int half = dw >> 2;                         // which 64 inputs of the group
+        const int half0 = (dw >> 2) * kHalves;            // its first 64 inputs of the group
         const int r = quarter * 32 + lane;                // row within the tile
         const bool x_issuer = dw == 0 && lane == 0;       // loads x of the team's groups
         uint64_t pol_x = 0;
@@ -672,22 +677,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     ok = false;
                     break;
                 }
-                // this row's words of the team's groups of the stage (at most
-                // two: the stage's groups alternate between the teams), read
-                // at once so that the stage is free for the next box early;
+                // this row's words of the team's group of the stage (at most
+                // kPerTeam: group gi of the stage is team (c + gi) % kDeqTeams's),
+                // read at once so that the stage is free for the next box early;
                 // 16-byte chunks 2 half and 2 half + 1 of a row, stored 64-byte
                 // swizzled (chunk ^= (row >> 1) & 3)
-                const int gfirst = ((c & 1) == team) ? 0 : 1;
+                const int gfirst = ((team - c) % kDeqTeams + kDeqTeams) % kDeqTeams;
                 const int sw = (r >> 1) & 3;
-                uint4 w[2][2];
+                uint4 w[kPerTeam][kHalves][2];
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int gi = gfirst + 2 * k2;
+                for (int k2 = 0; k2 < kPerTeam; ++k2) {
+                    const int gi = gfirst + kDeqTeams * k2;
                     if (gi < ng) {
                         const uint8_t *rowp =
                             st + (r >> 6) * (kStageW / 2) + gi * (kGroupBytes / 2) + (r & 63) * 64;
-                        w[k2][0] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half) ^ sw));
-                        w[k2][1] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half + 1) ^ sw));
+#pragma unroll
+                        for (int hf = 0; hf < kHalves; ++hf) {
+                            const int half = half0 + hf;
+                            w[k2][hf][0] = *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half) ^ sw));
+                            w[k2][hf][1] =
+                                *reinterpret_cast<const uint4 *>(rowp + 16 * ((2 * half + 1) ^ sw));
+                        }
                     }
                 }
                 // its scale words and zeros word; its 4 scales start at byte
@@ -703,10 +713,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 // the team's groups of the stage are restored one after the
                 // other and their tensor-memory stores waited for once: the
                 // store latency is paid once per stage, not per group
-                int done_a[2] = {-1, -1};
+                int done_a[kPerTeam];
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int gi = gfirst + 2 * k2;
+                for (int k2 = 0; k2 < kPerTeam; ++k2) done_a[k2] = -1;
+#pragma unroll
+                for (int k2 = 0; k2 < kPerTeam; ++k2) {
+                    const int gi = gfirst + kDeqTeams * k2;
                     if (gi >= ng) break;
                     const int cg = c + gi;  // the group's number in the CTA's sequence
                     const int a = cg % kAStages;
@@ -740,9 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     const uint32_t ss = sbits | (sbits << 16);
                     // 16 columns (4 words) per store, so that few values are live
 #pragma unroll
-                    for (int hw = 0; hw < 2; ++hw) {
-                        const uint32_t words[4] = {w[k2][hw].x, w[k2][hw].y, w[k2][hw].z,
-                                                   w[k2][hw].w};
+                    for (int hh = 0; hh < 2 * kHalves; ++hh) {
+                        const int hf = hh >> 1, hw = hh & 1;
+                        const uint32_t words[4] = {w[k2][hf][hw].x, w[k2][hf][hw].y,
+                                                   w[k2][hf][hw].z, w[k2][hf][hw].w};
                         uint32_t v[16];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -771,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             v[4 * u + 3] = prmt(r2, r3, 0x7632);
                         }
                         tmem_st_x16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols +
-                                        32 * half + 16 * hw, v);
+                                        32 * (half0 + hf) + 16 * hw, v);
                     }
                     done_a[k2] = a;
                 }
@@ -780,8 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(smem_u32(a_full + done_a[0]));
-                        if (done_a[1] >= 0) mbar_arrive(smem_u32(a_full + done_a[1]));
+#pragma unroll
+                        for (int k2 = 0; k2 < kPerTeam; ++k2)
+                            if (done_a[k2] >= 0) mbar_arrive(smem_u32(a_full + done_a[k2]));
                     }
                 }
                 c += ng;
