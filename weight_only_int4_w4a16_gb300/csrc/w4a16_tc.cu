@@ -37,8 +37,8 @@
 //     and puts the pairs in k order; tcgen05.st puts the values in tensor
 //     memory as the MMA's A operand (a ring of 4 buffers).  One lane of each
 //     team loads the group's x for all T tokens by TMA straight from the
-//     caller's x into the matching x slot: a box of T rows x 256 bytes lands
-//     as the MMA's canonical K-major layout;
+//     caller's x into the matching x slot: two boxes of T rows x 128 bytes
+//     land in the MMA's 128-byte swizzled K-major layout;
 //   warps 21..24 (one thread each) take groups c with c % 4 == their index and
 //     issue a group's 8 tcgen05.mma into their own accumulator chains (so the
 //     sums of each chain come in a fixed order), then commit;
@@ -97,7 +97,7 @@ constexpr int kErrWaitFull = 1, kErrWaitAFull = 2, kErrWaitDFull = 4, kErrWaitEm
 
 struct TcParams {
     CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 128, 4}
-    CUtensorMap xmap;  // x 3-D: (8 halves, M tokens, K/8 chunks), box {8, T, 16}: one group
+    CUtensorMap xmap;  // x 2-D: (K, M), box {64, T}, 128-byte swizzle: half a group
     const __half *x;   // x as given (the exact path)
     const uint32_t *qw;
     const __half *scales;
@@ -215,6 +215,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 4-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing
 __device__ __forceinline__ void cp4(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
@@ -234,12 +243,16 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    // tcgen05 shared-memory matrix descriptor, no swizzle: start address,
-    // leading byte offset (between core matrices along K), stride byte offset
-    // (between 8-row groups along M/N), fixed version field 1 at bit 46.
-    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
-           ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
+__device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t addr) {
+    // tcgen05 shared-memory matrix descriptor of a K-major operand in the
+    // 128-byte swizzled layout (8-row atoms of 128-byte rows, the 16-byte
+    // chunks of row r XOR-ed with r % 8, atoms 1024-byte aligned): start
+    // address, leading byte offset 16 (unused: an MMA's K = 16 halves stay
+    // within one 128-byte row), stride byte offset 1024 (between 8-row
+    // groups along N), version 1 at bit 46, swizzle mode 2 (128 B) at bit 61.
+    // Stepping K inside the atom moves the start address by 32 bytes.
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(16 >> 4) << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -630,10 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kGroup / 16; ++kk) {
-                        // x chunks 2 kk, 2 kk + 1 of the slot: core matrices T x 16
-                        // bytes apart along K, 8 tokens 128 bytes apart along N
-                        const uint64_t bdesc =
-                            smem_desc_kmajor(xb + (uint32_t)(2 * kk * T * 16), T * 16, 128);
+                        // k 16 kk .. 16 kk + 15 of x: half kk / 4 of the slot (T
+                        // rows of 128 bytes, swizzled), 32 bytes per k step
+                        const uint64_t bdesc = smem_desc_kmajor_sw128(
+                            xb + (uint32_t)((kk >> 2) * (T * 128) + (kk & 3) * 32));
                         // chain kk % kChains starts fresh with this issuer's first
                         // MMA of it in the segment
                         mma_f16_ts(d_tmem + (kk % C::kChains) * T, tmem + me * kACols + 8 * kk,
@@ -739,8 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                         }
                         const uint32_t xbar = smem_u32(x_full + a);
                         mbar_arrive_expect_tx(xbar, (uint32_t)C::kXSlot);
-                        tma_load_3d(smem_u32(sm_x + a * C::kXSlot), &p.xmap, 0, 0,
-                                    (kSG * j + gi) * (kGroup / 8), xbar, pol_x);
+                        const int k0 = (kSG * j + gi) * kGroup;
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot), &p.xmap, k0, 0, xbar, pol_x);
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot + T * 128), &p.xmap, k0 + 64, 0,
+                                    xbar, pol_x);
                         ++xuse[a];
                     }
                     const uint32_t bp = off + 2u * gi;  // byte of the scale in the words
@@ -1078,15 +1093,16 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
-        // x as (8 halves, token, chunk of 8): a box of T tokens x 16 chunks
-        // (one group) lands as [chunk][token][16 bytes], the MMA's K-major
-        // layout; tokens past M read zeros
-        const cuuint64_t dims[3] = {8, (cuuint64_t)a.M, (cuuint64_t)(a.K / 8)};
-        const cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, 16};
-        const cuuint32_t box[3] = {8, (cuuint32_t)plan.T, (cuuint32_t)(kGroup / 8)};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void *)a.x, dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+        // x as (K, token): a box of 64 k x T tokens lands as T rows of 128
+        // bytes, 128-byte swizzled, the MMA's K-major swizzled layout (one
+        // 128-byte request per token; 16-byte rows cost 8 requests each);
+        // tokens past M read zeros
+        const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)plan.T};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)a.x, dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
