@@ -316,11 +316,19 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
     size_t partial_floats = 0;
     int counters = 0, units = 0, smem = 0;
     bool waits = false;
+    // one CTA shape for the whole launch
+    std::vector<int> Ks(n), Ns(n);
+    for (int l = 0; l < n; ++l) {
+        Ks[l] = descs[l].K;
+        Ns[l] = descs[l].N;
+    }
+    const int warps = mma_round_warps(M, Ks.data(), Ns.data(), n);
     for (int l = 0; l < n; ++l) {
         const w4a16_linear_desc &d = descs[l];
         // the last linears of a round come in small units: the CTAs then
         // run out of work within a small unit of each other
-        MmaPlan p = plan_mma(M, d.N, d.K, l >= n - kRoundTailLinears ? 3 : 2, st.dev, d.epilogue);
+        MmaPlan p = plan_mma(M, d.N, d.K, l >= n - kRoundTailLinears ? 3 : 2, st.dev, d.epilogue,
+                             1, warps);
         if (!p.ok) return W4A16_ERR_UNSUPPORTED;
         float *part = nullptr;
         unsigned *cnt = nullptr;
@@ -360,6 +368,7 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
     fr->round.smem_bytes = smem;
     fr->round.done = waits ? st.ws.counters + counters : nullptr;
     fr->round.bf16 = descs[0].dtype == W4A16_DTYPE_BF16;
+    fr->round.warps = warps;
     fr->counters_used = counters + (waits ? n : 0);
     return W4A16_OK;
 }
@@ -681,7 +690,8 @@ int w4a16_moe_create(int E, int N, int K, int group, const uint32_t *qweight,
     // one plan for every tile, weighing the tiles expected side by side (one
     // per expert in use, up to the slots)
     const int copies = max_slots < E ? max_slots : E;
-    h->plan = plan_mma(kMmaMaxTokens, N, K, -1, s.dev, epilogue, copies);
+    // (8-warp CTAs: an expert MLP's launch holds the plans of two linears)
+    h->plan = plan_mma(kMmaMaxTokens, N, K, -1, s.dev, epilogue, copies, 8);
     if (!h->plan.ok) {
         delete h;
         return W4A16_ERR_UNSUPPORTED;

@@ -126,13 +126,14 @@ struct MmaPlan {
     int slice_groups;  // groups per slice (a multiple of 4; the last slice may hold fewer)
     int n_strips;      // 16-row strips
     int strips_per_warp;
-    int n_blocks;      // units per slice: ceil(n_strips / (8 * strips_per_warp))
+    int n_blocks;      // units per slice: ceil(n_strips / (warps * strips_per_warp))
     int units;         // S * n_blocks
     bool reduce;       // sums go to the workspace, a block's last CTA reduces them
                        // (S > 1, or SiLU-and-mul); n_blocks arrival counters
     int grid;          // CTAs of a launch of this linear alone
     int smem_bytes;    // dynamic shared memory of such a launch
     size_t ws_bytes;   // split-K partial bytes (0 when S == 1)
+    int warps;         // CTA shape: 8 warps (two CTAs per SM) or 16 (one per SM)
 };
 
 // One linear as the kernel reads it: in the kernel's parameters for a launch
@@ -169,9 +170,11 @@ struct MmaLinDesc {
 // that the CTAs finish together).
 // copies: the number of such linears that run side by side in one launch
 // (the expert tiles of a mixture of experts); the one-linear cost model
-// weighs their units together
+// weighs their units together.
+// warps: the CTA shape, 8 or 16; 0 = chosen for a linear launched alone (a
+// fused round chooses one shape for all its linears: mma_round_warps)
 MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi = kEpiNone,
-                 int copies = 1);
+                 int copies = 1, int warps = 0);
 cudaError_t mma_describe(const LinearArgs &a, const MmaPlan &plan, float *partials,
                          unsigned *counters, int unit_start, int wait_for, MmaLinDesc *d);
 cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace &ws,
@@ -191,13 +194,17 @@ struct MmaRound {
     int smem_bytes;
     unsigned *done;
     bool bf16;  // every linear of the round has bf16 data
+    int warps = 8;  // the CTA shape of every linear's plan
     // expert groups: the descriptors come from the preceding kernel, which
     // writes the linear count and total units here (n and total_units are
     // then upper bounds, for the grid)
     const int *counts = nullptr;
 };
-int mma_round_grid(const DeviceInfo &dev);
-int mma_smem_bytes(int M, int slice_groups);
+int mma_round_grid(const DeviceInfo &dev, int warps);
+int mma_smem_bytes(int M, int slice_groups, int warps);
+// the CTA shape for a fused round of n linears (K[l] x N[l]) at M tokens:
+// 16 warps where their room for x removes the K split from most bytes
+int mma_round_warps(int M, const int *K, const int *N, int n);
 cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const DeviceInfo &dev,
                              cudaStream_t stream);
 cudaError_t mma_init(const DeviceInfo &dev);

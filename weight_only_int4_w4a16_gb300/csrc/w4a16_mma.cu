@@ -67,15 +67,11 @@ namespace {
 
 using namespace warp_mma;
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kCtasPerSm = 2;
 constexpr int kStageGroups = 4;                 // groups per box
 constexpr int kDepth = 2;                       // ring slots per warp
 constexpr int kStageW = kStageGroups * 16 * 64;  // 4 KB of weights
 constexpr int kStageMeta = 16 * 16;             // per row: 3 scale words, 1 zeros word
 constexpr int kStageBytes = kStageW + kStageMeta;
-constexpr int kRingBytes = kWarps * kDepth * kStageBytes;  // 69632
 // A unit of the CTA's queue, decoded once by thread 0 into shared memory:
 // everything the warps need of the unit and of its linear, so that none of
 // them reads a descriptor from global memory on its way.
@@ -97,9 +93,28 @@ struct UnitInfo {
 constexpr int kSlots = 8;  // one per queue position (mod 8)
 // ring barriers, then 16 flag ints, then the barrier of the x copies, then
 // the decoded units
-constexpr int kSlotOffset = kWarps * kDepth * 8 + 64 + 16;
-constexpr int kBarBytes = kSlotOffset + kSlots * (int)sizeof(UnitInfo);
-constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // leaves the per-CTA reserve
+// The CTA's shape: W = 8 warps (two CTAs per SM) or 16 warps (one CTA per SM,
+// with the whole SM's shared memory: room for the x of a K 5120 slice of 8
+// tokens beside the 16 warps' rings, where two 8-warp CTAs must cut it in
+// two).  An SM runs 16 warps either way.
+template <int W>
+struct CtaShape {
+    static constexpr int kWarps = W;
+    static constexpr int kThreads = W * 32;
+    static constexpr int kCtasPerSm = 16 / W;
+    static constexpr int kRingBytes = W * kDepth * kStageBytes;  // 69632 for 8 warps
+    static constexpr int kSlotOffset = W * kDepth * 8 + 64 + 16;
+    static constexpr int kBarBytes = kSlotOffset + kSlots * (int)sizeof(UnitInfo);
+    static constexpr int kSmemPerCta = 228 * 1024 / kCtasPerSm - 1024;  // the per-CTA reserve
+};
+// the shape's constants as locals of a function templated on W
+#define W4A16_CTA_SHAPE(W)                                          \
+    constexpr int kWarps = CtaShape<W>::kWarps;                     \
+    constexpr int kThreads = CtaShape<W>::kThreads;                 \
+    constexpr int kRingBytes = CtaShape<W>::kRingBytes;             \
+    constexpr int kSlotOffset = CtaShape<W>::kSlotOffset;           \
+    constexpr int kBarBytes = CtaShape<W>::kBarBytes;               \
+    (void)kWarps, (void)kThreads, (void)kRingBytes, (void)kSlotOffset, (void)kBarBytes
 constexpr int kMaxSliceGroups = 128;
 constexpr int kRoundStripsPerWarp = 8;  // fused rounds: strips per warp and unit
 constexpr int kErrMmaWait = 128;  // device status bit: a ring wait expired
@@ -141,8 +156,9 @@ __device__ __forceinline__ void epilogue_store(const Lin &R, size_t o, float h, 
 // row: half of the sums a thread keeps are gate rows, the other half the up
 // rows of the same outputs (the register footprint stays that of 8 sums: the
 // callers keep their registers across this call).
-template <bool kBf16>
+template <bool kBf16, int W>
 __device__ __forceinline__ void reduce_block(const MmaLinDesc &R, int sb) {
+    W4A16_CTA_SHAPE(W);
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
     const int nrows = min(R.ycols - row0, rows_per_block);
@@ -197,9 +213,10 @@ __device__ __forceinline__ void reduce_block(const MmaLinDesc &R, int sb) {
 // the SM's copy engine.  Needs rows that start on 16-byte boundaries (N a
 // multiple of 4, 16-byte aligned partial sums); returns false otherwise, or
 // when the buffer holds fewer than 4 rows, without touching anything.
-template <bool kBf16>
+template <bool kBf16, int W>
 __device__ __forceinline__ bool reduce_block_staged(const MmaLinDesc &R, int sb, uint8_t *buf,
                                                     uint32_t buf_bytes) {
+    W4A16_CTA_SHAPE(W);
     if (R.N % 4 != 0 || ((uintptr_t)R.partials & 15) != 0) return false;
     const int rows_per_block = kWarps * R.strips_per_warp * 16;
     const int row0 = sb * rows_per_block;
@@ -262,22 +279,24 @@ __device__ __forceinline__ bool reduce_block_staged(const MmaLinDesc &R, int sb,
 // the staged form was 1-2% slower at every M (its reductions overlap the
 // other CTAs' streaming, and the copies wait with the weight traffic).  The
 // buffer comes from the CTA's shared-memory layout.
-template <bool kRound, bool kBf16>
+template <bool kRound, bool kBf16, int W>
 __device__ __noinline__ void reduce_any(const MmaLinDesc &R, int sb, int x_free) {
+    W4A16_CTA_SHAPE(W);
     if constexpr (!kRound) {
         extern __shared__ __align__(128) uint8_t smem[];
         uint32_t dyn;
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
-        if (x_free && reduce_block_staged<kBf16>(R, sb, smem + kRingBytes + kBarBytes,
+        if (x_free && reduce_block_staged<kBf16, W>(R, sb, smem + kRingBytes + kBarBytes,
                                                  dyn - (uint32_t)(kRingBytes + kBarBytes)))
             return;
     }
-    reduce_block<kBf16>(R, sb);
+    reduce_block<kBf16, W>(R, sb);
 }
 
-template <bool kRound, bool kBf16>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <bool kRound, bool kBf16, int W>
+__global__ void __launch_bounds__(CtaShape<W>::kThreads, CtaShape<W>::kCtasPerSm)
     mma_kernel(const __grid_constant__ MmaKernelParams P) {
+    W4A16_CTA_SHAPE(W);
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -614,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // flight at a boundary
     auto maybe_reduce = [&](int boundary, bool x_free) {
         volatile int *f = vflags + kFlagRed + 3 * (boundary & 1);
-        if (f[0]) reduce_any<kRound, kBf16>(desc(f[1]), f[2], x_free ? 1 : 0);
+        if (f[0]) reduce_any<kRound, kBf16, W>(desc(f[1]), f[2], x_free ? 1 : 0);
     };
 
     // boundary b: the barrier at the top of iteration b (b = k), or an extra
@@ -980,14 +999,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 int xstride_for(int slice_groups) { return slice_groups * kGroup * 2 + 16; }
 
 
-cudaLaunchConfig_t launch_config(int grid, int smem, cudaStream_t stream,
+cudaLaunchConfig_t launch_config(int grid, int threads, int smem, cudaStream_t stream,
                                  cudaLaunchAttribute *attr) {
     // programmatic dependent launch: the grid may start while the previous
     // kernel in the stream drains; the kernel waits for it (griddepcontrol)
     // before touching activations, outputs or the workspace
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -997,19 +1016,64 @@ cudaLaunchConfig_t launch_config(int grid, int smem, cudaStream_t stream,
     return cfg;
 }
 
-}  // namespace
+// the shape's sizes on the host, by width (8 or 16 warps)
+int ring_bytes(int w) { return w == 16 ? CtaShape<16>::kRingBytes : CtaShape<8>::kRingBytes; }
+int bar_bytes(int w) { return w == 16 ? CtaShape<16>::kBarBytes : CtaShape<8>::kBarBytes; }
+int smem_per_cta(int w) { return w == 16 ? CtaShape<16>::kSmemPerCta : CtaShape<8>::kSmemPerCta; }
+int ctas_per_sm(int w) { return 16 / w; }
 
-int mma_smem_bytes(int M, int slice_groups) {
-    return kRingBytes + kBarBytes + M * xstride_for(slice_groups) + slice_groups * 8 * 4 +
-           kMmaMaxTokens * 4;
+// the largest slice (a whole number of stages) whose staged x and sums fit
+// beside the rings of a CTA of w warps
+int max_slice_groups(int M, int w) {
+    const int budget = smem_per_cta(w) - ring_bytes(w) - bar_bytes(w);
+    int g = (budget - 16 * M - kMmaMaxTokens * 4) / (kGroup * 2 * M + 32);
+    g = g / kStageGroups * kStageGroups;
+    if (g > kMaxSliceGroups) g = kMaxSliceGroups;
+    if (g < kStageGroups) g = kStageGroups;
+    return g;
 }
 
-int mma_round_grid(const DeviceInfo &dev) { return kCtasPerSm * dev.sm_count; }
+}  // namespace
 
-MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi, int copies) {
+int mma_smem_bytes(int M, int slice_groups, int warps) {
+    return ring_bytes(warps) + bar_bytes(warps) + M * xstride_for(slice_groups) +
+           slice_groups * 8 * 4 + kMmaMaxTokens * 4;
+}
+
+int mma_round_grid(const DeviceInfo &dev, int warps) { return ctas_per_sm(warps) * dev.sm_count; }
+
+int mma_round_warps(int M, const int *K, const int *N, int n) {
+    // The 16-warp CTA pays for its one-CTA-per-SM shape (a unit boundary
+    // stalls all 16 warps of the SM, where two 8-warp CTAs cover each other's
+    // barriers and x staging): in the 64-layer round at M = 1..4 it ran
+    // 3-6% slower.  It wins where its room for x removes the K split from
+    // most of the round's bytes: at M = 5..8 the K 5120 linears no longer fit
+    // an 8-warp CTA unsplit (2.18-2.30 ms on 8 warps, 2.01-2.08 ms on 16).
+    double all = 0, split8 = 0, split16 = 0;
+    for (int l = 0; l < n; ++l) {
+        const int G = K[l] / kGroup;
+        const double b = (double)N[l] * K[l];
+        all += b;
+        if (G > max_slice_groups(M, 8)) split8 += b;
+        if (G > max_slice_groups(M, 16)) split16 += b;
+    }
+    return all > 0 && split8 - split16 > 0.5 * all ? 16 : 8;
+}
+
+MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi, int copies,
+                 int warps) {
     MmaPlan pl{};
     pl.M = M;
     const int G = K / kGroup;
+    if (warps == 0) {
+        // one linear alone: 16 warps when that CTA holds the whole K's x and
+        // the 8-warp CTA would have to split K for room (K 5120, N 27648 at
+        // M = 8: 36.9 -> 28.7 us); else 8 (where both split, as K 17408 at
+        // M = 4 and 8, the 8-warp plans measured 2 us faster)
+        warps = G > max_slice_groups(M, 8) && G <= max_slice_groups(M, 16) ? 16 : 8;
+    }
+    pl.warps = warps;
+    const int kWarps = warps;
     // SiLU-and-mul: a logical strip is a gate strip and its up strip (N/2 a
     // multiple of 16), twice the work of a strip
     const int work = epi == kEpiSiluMul ? 2 : 1;
@@ -1017,18 +1081,13 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi,
     pl.strips_per_warp = split == 2 ? kRoundStripsPerWarp / work : 1;
     if (split == 3) split = 2;  // a round's last linears: fewest slices, small units
     pl.n_blocks = (pl.n_strips + kWarps * pl.strips_per_warp - 1) / (kWarps * pl.strips_per_warp);
-    // largest slice (a whole number of stages) whose staged x and sums fit
-    const int budget = kSmemPerCta - kRingBytes - kBarBytes;
-    int max_groups = (budget - 16 * M - kMmaMaxTokens * 4) / (kGroup * 2 * M + 32);
-    max_groups = max_groups / kStageGroups * kStageGroups;
-    if (max_groups > kMaxSliceGroups) max_groups = kMaxSliceGroups;
-    if (max_groups < kStageGroups) max_groups = kStageGroups;
+    const int max_groups = max_slice_groups(M, warps);
     const int s_min = (G + max_groups - 1) / max_groups;
     if (split == 0 && s_min > 1) {
         pl.ok = false;
         return pl;
     }
-    const int grid_max = kCtasPerSm * dev.sm_count;
+    const int grid_max = ctas_per_sm(warps) * dev.sm_count;
     int best_sg = 0;
     if (split == 2) {
         // fewest slices: spread evenly over whole stages
@@ -1086,7 +1145,7 @@ MmaPlan plan_mma(int M, int N, int K, int split, const DeviceInfo &dev, int epi,
     pl.S = (G + best_sg - 1) / best_sg;
     pl.units = pl.S * pl.n_blocks;
     pl.grid = pl.units < grid_max ? pl.units : grid_max;
-    pl.smem_bytes = mma_smem_bytes(M, pl.slice_groups);
+    pl.smem_bytes = mma_smem_bytes(M, pl.slice_groups, warps);
     // split K, and SiLU-and-mul with any number of slices: the partial sums
     pl.reduce = pl.S > 1 || epi == kEpiSiluMul;
     pl.ws_bytes = pl.reduce ? (size_t)pl.S * M * N * sizeof(float) : 0;
@@ -1152,9 +1211,12 @@ cudaError_t launch_mma(const LinearArgs &a, const MmaPlan &plan, const Workspace
     P.total_units = plan.units;
     P.dynamic = 0;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config(plan.grid, plan.smem_bytes, stream, attr);
-    return bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<false, true>, P)
-                : cudaLaunchKernelEx(&cfg, mma_kernel<false, false>, P);
+    cudaLaunchConfig_t cfg = launch_config(plan.grid, plan.warps * 32, plan.smem_bytes, stream, attr);
+    if (plan.warps == 16)
+        return bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<false, true, 16>, P)
+                    : cudaLaunchKernelEx(&cfg, mma_kernel<false, false, 16>, P);
+    return bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<false, true, 8>, P)
+                : cudaLaunchKernelEx(&cfg, mma_kernel<false, false, 8>, P);
 }
 
 cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const DeviceInfo &dev,
@@ -1169,18 +1231,21 @@ cudaError_t launch_mma_round(const MmaRound &r, const Workspace &ws, const Devic
     P.total_units = r.total_units;
     P.counts = r.counts;
     P.dynamic = 1;
-    int grid = mma_round_grid(dev);
+    int grid = mma_round_grid(dev, r.warps);
     if (grid > r.total_units) grid = r.total_units;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config(grid, r.smem_bytes, stream, attr);
+    cudaLaunchConfig_t cfg = launch_config(grid, r.warps * 32, r.smem_bytes, stream, attr);
     if (r.done) {
         // linears wait for earlier ones: every CTA must be resident at once
         attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
         attr[cfg.numAttrs].val.cooperative = 1;
         cfg.numAttrs += 1;
     }
-    return r.bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<true, true>, P)
-                  : cudaLaunchKernelEx(&cfg, mma_kernel<true, false>, P);
+    if (r.warps == 16)
+        return r.bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<true, true, 16>, P)
+                      : cudaLaunchKernelEx(&cfg, mma_kernel<true, false, 16>, P);
+    return r.bf16 ? cudaLaunchKernelEx(&cfg, mma_kernel<true, true, 8>, P)
+                  : cudaLaunchKernelEx(&cfg, mma_kernel<true, false, 8>, P);
 }
 
 EncodeTiledFn tensor_map_encoder() {
@@ -1198,15 +1263,19 @@ EncodeTiledFn tensor_map_encoder() {
 
 cudaError_t mma_init(const DeviceInfo &dev) {
     if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
-    int dyn = kSmemPerCta;
-    if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
     cudaError_t e = cudaSuccess;
-    const void *fns[4] = {(const void *)mma_kernel<false, false>,
-                          (const void *)mma_kernel<true, false>,
-                          (const void *)mma_kernel<false, true>,
-                          (const void *)mma_kernel<true, true>};
-    for (int k = 0; k < 4 && e == cudaSuccess; ++k) {
+    const void *fns[8] = {(const void *)mma_kernel<false, false, 8>,
+                          (const void *)mma_kernel<true, false, 8>,
+                          (const void *)mma_kernel<false, true, 8>,
+                          (const void *)mma_kernel<true, true, 8>,
+                          (const void *)mma_kernel<false, false, 16>,
+                          (const void *)mma_kernel<true, false, 16>,
+                          (const void *)mma_kernel<false, true, 16>,
+                          (const void *)mma_kernel<true, true, 16>};
+    for (int k = 0; k < 8 && e == cudaSuccess; ++k) {
         const void *fn = fns[k];
+        int dyn = smem_per_cta(k < 4 ? 8 : 16);
+        if (dyn > dev.max_smem_optin - 1024) dyn = dev.max_smem_optin - 1024;
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
