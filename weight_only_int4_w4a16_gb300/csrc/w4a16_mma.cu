@@ -41,11 +41,16 @@
 //     when x is staged).  Per group
 //         acc += s * (16 * D_lo + D_hi - z * S * 2^-20)
 //     and y = 2^20 * acc, which is sum_g s_g * sum_k (q - z) x;
-//   * work comes in units: one K slice of 8 strips, a strip per warp.  CTAs
-//     are persistent and take units round-robin; per unit a CTA stages that
-//     slice of x (with each group's sums of x) and its warps stream their
-//     strips, while each warp's copy stream already runs ahead into its next
-//     unit;
+//   * work comes in units: one K slice of R strips per warp.  CTAs are
+//     persistent and take units round-robin (or from a shared counter in a
+//     fused round); per unit a CTA stages that slice of x (with each group's
+//     sums of x) and its warps stream their strips, while each warp's copy
+//     stream already runs ahead into its next unit;
+//   * a CTA is 8 warps, two per SM, or 16 warps, one per SM: the larger CTA
+//     has twice the shared memory for staged x (the x of a K 5120 slice of 8
+//     tokens fits beside its 16 rings, where an 8-warp CTA must cut K in
+//     two), the smaller lets one CTA stream while the other crosses a unit
+//     boundary;
 //   * a fused decode round is one launch over the units of all its linears
 //     in order: the weight stream does not stop between linears.  Where a
 //     linear reads activations an earlier one writes (or the like), it waits
