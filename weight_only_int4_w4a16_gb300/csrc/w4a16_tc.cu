@@ -74,7 +74,6 @@ constexpr int kDeqTeams = 4;                   // restore teams: group c to team
 constexpr int kDeqWarps = 4;                   // warps per team (one per TMEM lane quarter)
 constexpr int kHalves = 8 / kDeqWarps;         // 64-input halves of a group row per thread
 constexpr int kPerTeam = kSG / kDeqTeams;      // a team's groups per stage
-static_assert(kHalves == 2, "a restore thread holds both halves of its row (the A halves)");
 constexpr int kTmaWarp = kEpiWarps + kDeqTeams * kDeqWarps;  // 20
 constexpr int kMmaWarp = kTmaWarp + 1;                       // 21 .. 24
 constexpr int kMmaWarps = 4;                                 // MMA issuers: group c to c % 4
@@ -83,10 +82,9 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxStages = 6;
 constexpr int kSmemBudget = 220 * 1024;        // weight stages and the x ring
 static_assert(kMmaWarps == kAStages, "issuer i owns A buffer i (and x slot i)");
-// the mbarriers (full, empty per stage; a_full, a_empty, x_full per half of an
-// A buffer (k 0..63 and 64..127 of its group);
+// the mbarriers (full, empty per stage; a_full, a_empty, x_full per A buffer;
 // d_full, d_empty; done), then the tensor-memory address, abort and last flags
-constexpr int kBarBytes = (2 * kMaxStages + 3 * 2 * kAStages + 5) * 8 + 16;
+constexpr int kBarBytes = (2 * kMaxStages + 3 * kAStages + 5) * 8 + 16;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms per wait
 // scales whose 16-bit restore may overflow: |s| >= 4096 in fp16, |s| >= 2^120
 // in bf16 (bits of |s|; Inf and NaN included): those rows take the exact path
@@ -498,11 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm_stage + (size_t)NS * C::kStageBytes);
     uint64_t *full = bars;                     // [kMaxStages] weight stage landed
     uint64_t *empty = full + kMaxStages;       // [kMaxStages] weight stage read
-    // per half (h) of A buffer a, index 2 a + h: k 0..63 or 64..127 of the group
-    uint64_t *a_full = empty + kMaxStages;       // [2 kAStages] A half restored
-    uint64_t *a_empty = a_full + 2 * kAStages;   // [2 kAStages] A half and x half free (MMAs done)
-    uint64_t *x_full = a_empty + 2 * kAStages;   // [2 kAStages] x half landed
-    uint64_t *d_full = x_full + 2 * kAStages;    // [2]
+    uint64_t *a_full = empty + kMaxStages;     // [kAStages] A restored
+    uint64_t *a_empty = a_full + kAStages;     // [kAStages] A and x slot free (MMAs done)
+    uint64_t *x_full = a_empty + kAStages;     // [kAStages] x slot landed
+    uint64_t *d_full = x_full + kAStages;      // [2]
     uint64_t *d_empty = d_full + 2;            // [2]
     uint64_t *done = d_empty + 2;              // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
@@ -518,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             mbar_init(smem_u32(full + i), 1 + 32);
             mbar_init(smem_u32(empty + i), kDeqTeams * kDeqWarps);  // every restore warp
         }
-        for (int i = 0; i < 2 * kAStages; ++i) {
+        for (int i = 0; i < kAStages; ++i) {
             mbar_init(smem_u32(a_full + i), kDeqWarps);
             mbar_init(smem_u32(a_empty + i), 1);
             mbar_init(smem_u32(x_full + i), 1);
@@ -633,40 +630,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 for (int gi = 0; gi < ng; ++gi, ++c) {
                     if ((c & (kMmaWarps - 1)) != me) continue;
                     const uint32_t use = (uint32_t)(c / kAStages) & 1;
-                    // the group's halves (k 0..63, 64..127) as they are restored:
-                    // the MMAs of one half run while the team restores the other
-#pragma unroll
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        const int ab = 2 * me + h;
-                        if (!mbar_wait(smem_u32(a_full + ab), use, abort)) {
-                            fail(abort, p.status, kErrWaitAFull);
-                            ok = false;
-                            break;
-                        }
-                        if (!mbar_wait(smem_u32(x_full + ab), use, abort)) {
-                            fail(abort, p.status, kErrWaitFull);
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-#pragma unroll
-                        for (int k4 = 0; k4 < 4; ++k4) {
-                            const int kk = 4 * h + k4;
-                            // k 16 kk .. 16 kk + 15 of x: half h of the slot (T rows
-                            // of 128 bytes, swizzled), 32 bytes per k step
-                            const uint64_t bdesc = smem_desc_kmajor_sw128(
-                                xb + (uint32_t)(h * (T * 128) + k4 * 32));
-                            // chain kk % kChains starts fresh with this issuer's
-                            // first MMA of it in the segment
-                            mma_f16_ts(d_tmem + (kk % C::kChains) * T,
-                                       tmem + me * kACols + 8 * kk, bdesc, C::kIdesc,
-                                       first && kk < C::kChains ? 0u : 1u);
-                        }
-                        // the A half and the x half are free once these MMAs are done
-                        mma_commit(smem_u32(a_empty + ab));
+                    if (!mbar_wait(smem_u32(a_full + me), use, abort)) {
+                        fail(abort, p.status, kErrWaitAFull);
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
+                    if (!mbar_wait(smem_u32(x_full + me), use, abort)) {
+                        fail(abort, p.status, kErrWaitFull);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kGroup / 16; ++kk) {
+                        // k 16 kk .. 16 kk + 15 of x: half kk / 4 of the slot (T
+                        // rows of 128 bytes, swizzled), 32 bytes per k step
+                        const uint64_t bdesc = smem_desc_kmajor_sw128(
+                            xb + (uint32_t)((kk >> 2) * (T * 128) + (kk & 3) * 32));
+                        // chain kk % kChains starts fresh with this issuer's first
+                        // MMA of it in the segment
+                        mma_f16_ts(d_tmem + (kk % C::kChains) * T, tmem + me * kACols + 8 * kk,
+                                   bdesc, C::kIdesc, first && kk < C::kChains ? 0u : 1u);
+                    }
                     first = false;
+                    // the A buffer and the x slot are free once these MMAs are done
+                    mma_commit(smem_u32(a_empty + me));
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(d_full + dset));
@@ -688,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         if (x_issuer)  // x is read by every CTA
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
         bool dep_waited = false;
-        int xuse[2 * kAStages] = {};  // x copies this thread issued per half slot
+        int xuse[kAStages] = {0, 0, 0, 0};  // x copies this thread issued per slot
         int c = 0, sc = 0;
         bool ok = true;
         while (ok && walk_next(p, wk, t, j0, j1)) {
@@ -735,13 +723,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 const uint32_t mw[3] = {md.x, md.y, md.z};
                 const uint32_t off = (uint32_t)((uintptr_t)(srow + kSG * j) & 2);
                 const uint32_t zsh = 4u * (uint32_t)((kSG * j) & 7);  // the stage's first nibble
-                // the team's groups of the stage, one after the other
+                // the team's groups of the stage are restored one after the
+                // other and their tensor-memory stores waited for once: the
+                // store latency is paid once per stage, not per group
+                int done_a[kPerTeam];
 #pragma unroll
-                for (int k2 = 0; k2 < kPerTeam && ok; ++k2) {
+                for (int k2 = 0; k2 < kPerTeam; ++k2) done_a[k2] = -1;
+#pragma unroll
+                for (int k2 = 0; k2 < kPerTeam; ++k2) {
                     const int gi = gfirst + kDeqTeams * k2;
                     if (gi >= ng) break;
                     const int cg = c + gi;  // the group's number in the CTA's sequence
                     const int a = cg % kAStages;
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(a_empty + a),
+                                                           ((cg / kAStages) & 1) ^ 1, abort))) {
+                        fail(abort, p.status, kErrWaitAEmpty);
+                        ok = false;
+                        break;
+                    }
+                    // the MMAs that read A[a] and x slot a have completed (commit)
+                    tc_fence_after();
+                    if (x_issuer) {
+                        // x of this group into slot a; x is written by the
+                        // preceding kernel: wait for it once
+                        if (!dep_waited) {
+                            grid_dependency_wait();
+                            dep_waited = true;
+                        }
+                        const uint32_t xbar = smem_u32(x_full + a);
+                        mbar_arrive_expect_tx(xbar, (uint32_t)C::kXSlot);
+                        const int k0 = (kSG * j + gi) * kGroup;
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot), &p.xmap, k0, 0, xbar, pol_x);
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot + T * 128), &p.xmap, k0 + 64, 0,
+                                    xbar, pol_x);
+                        ++xuse[a];
+                    }
                     const uint32_t bp = off + 2u * gi;  // byte of the scale in the words
                     const uint32_t sbits = (mw[bp >> 2] >> (8u * (bp & 2u))) & 0xffffu;
                     const uint32_t z = (md.w >> (zsh + 4u * gi)) & 0xfu;
@@ -749,75 +765,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                     const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
                     const uint32_t zz_b = 0x43004300u | z | (z << 16);  // bf16 (128 + z) pair
                     const uint32_t ss = sbits | (sbits << 16);
-                    // the group's two halves (k 0..63, 64..127) one after the
-                    // other, each handed to the MMAs as soon as it is in tensor
-                    // memory, so that one half's MMAs run while the other is
-                    // restored
+                    // 16 columns (4 words) per store, so that few values are live
 #pragma unroll
-                    for (int hf = 0; hf < kHalves; ++hf) {
-                        const int ab = 2 * a + hf;
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait(smem_u32(a_empty + ab),
-                                                  ((cg / kAStages) & 1) ^ 1, abort))) {
-                            fail(abort, p.status, kErrWaitAEmpty);
-                            ok = false;
-                            break;
-                        }
-                        // the MMAs that read this half of A[a] and of x slot a
-                        // have completed (commit)
-                        tc_fence_after();
-                        if (x_issuer) {
-                            // this half of the group's x into slot a; x is written
-                            // by the preceding kernel: wait for it once
-                            if (!dep_waited) {
-                                grid_dependency_wait();
-                                dep_waited = true;
+                    for (int hh = 0; hh < 2 * kHalves; ++hh) {
+                        const int hf = hh >> 1, hw = hh & 1;
+                        const uint32_t words[4] = {w[k2][hf][hw].x, w[k2][hf][hw].y,
+                                                   w[k2][hf][hw].z, w[k2][hf][hw].w};
+                        uint32_t v[16];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t wd = words[u], w8 = wd >> 8;
+                            // (q - z) exact, then times s rounded once: the pairs
+                            // (q0,q4) (q1,q5) (q2,q6) (q3,q7) of the word ...
+                            uint32_t r0, r1, r2, r3;
+                            if constexpr (kBf16) {
+                                // a nibble at mantissa bits 0..3 of bf16 128.0 is
+                                // 128 + q (bf16 has 7 mantissa bits); minus 128 + z
+                                r0 = mul_bf2(sub_bf2(lop3_and_or(wd, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r1 = mul_bf2(sub_bf2(lop3_and_or(wd >> 4, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r2 = mul_bf2(sub_bf2(lop3_and_or(w8, 0x000f000fu, 0x43004300u), zz_b), ss);
+                                r3 = mul_bf2(sub_bf2(lop3_and_or(wd >> 12, 0x000f000fu, 0x43004300u), zz_b), ss);
+                            } else {
+                                r0 = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                                r1 = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
+                                r2 = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
+                                r3 = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
                             }
-                            const uint32_t xbar = smem_u32(x_full + ab);
-                            mbar_arrive_expect_tx(xbar, (uint32_t)(C::kXSlot / 2));
-                            tma_load_2d(smem_u32(sm_x + a * C::kXSlot + hf * (T * 128)), &p.xmap,
-                                        (kSG * j + gi) * kGroup + 64 * hf, 0, xbar, pol_x);
-                            ++xuse[ab];
+                            // ... in k order, (q0,q1) (q2,q3) (q4,q5) (q6,q7): the
+                            // order of x in memory, which the TMA box keeps
+                            v[4 * u + 0] = prmt(r0, r1, 0x5410);
+                            v[4 * u + 1] = prmt(r2, r3, 0x5410);
+                            v[4 * u + 2] = prmt(r0, r1, 0x7632);
+                            v[4 * u + 3] = prmt(r2, r3, 0x7632);
                         }
-                        // 16 columns (4 words) per store, so that few values are live
+                        tmem_st_x16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols +
+                                        32 * (half0 + hf) + 16 * hw, v);
+                    }
+                    done_a[k2] = a;
+                }
+                if (done_a[0] >= 0) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                        for (int hw = 0; hw < 2; ++hw) {
-                            const uint32_t words[4] = {w[k2][hf][hw].x, w[k2][hf][hw].y,
-                                                       w[k2][hf][hw].z, w[k2][hf][hw].w};
-                            uint32_t v[16];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const uint32_t wd = words[u], w8 = wd >> 8;
-                                // (q - z) exact, then times s rounded once: the
-                                // pairs (q0,q4) (q1,q5) (q2,q6) (q3,q7) of the word ...
-                                uint32_t r0, r1, r2, r3;
-                                if constexpr (kBf16) {
-                                    // a nibble at mantissa bits 0..3 of bf16 128.0 is
-                                    // 128 + q (bf16 has 7 mantissa bits); minus 128 + z
-                                    r0 = mul_bf2(sub_bf2(lop3_and_or(wd, 0x000f000fu, 0x43004300u), zz_b), ss);
-                                    r1 = mul_bf2(sub_bf2(lop3_and_or(wd >> 4, 0x000f000fu, 0x43004300u), zz_b), ss);
-                                    r2 = mul_bf2(sub_bf2(lop3_and_or(w8, 0x000f000fu, 0x43004300u), zz_b), ss);
-                                    r3 = mul_bf2(sub_bf2(lop3_and_or(wd >> 12, 0x000f000fu, 0x43004300u), zz_b), ss);
-                                } else {
-                                    r0 = hmul2(hsub2(lop3_and_or(wd, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                                    r1 = hmul2(hsub2(lop3_and_or(wd, 0x00f000f0u, 0x54005400u), zz_lo), ss);
-                                    r2 = hmul2(hsub2(lop3_and_or(w8, 0x000f000fu, 0x64006400u), zz_hi), ss);
-                                    r3 = hmul2(hsub2(lop3_and_or(w8, 0x00f000f0u, 0x54005400u), zz_lo), ss);
-                                }
-                                // ... in k order, (q0,q1) (q2,q3) (q4,q5) (q6,q7): the
-                                // order of x in memory, which the TMA box keeps
-                                v[4 * u + 0] = prmt(r0, r1, 0x5410);
-                                v[4 * u + 1] = prmt(r2, r3, 0x5410);
-                                v[4 * u + 2] = prmt(r0, r1, 0x7632);
-                                v[4 * u + 3] = prmt(r2, r3, 0x7632);
-                            }
-                            tmem_st_x16(tmem + ((uint32_t)(quarter * 32) << 16) + a * kACols +
-                                            32 * hf + 16 * hw, v);
-                        }
-                        tmem_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(a_full + ab));
+                        for (int k2 = 0; k2 < kPerTeam; ++k2)
+                            if (done_a[k2] >= 0) mbar_arrive(smem_u32(a_full + done_a[k2]));
                     }
                 }
                 c += ng;
@@ -826,8 +819,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         // the x copies this thread issued land before the CTA exits: each is
         // waited for by its MMA issuer, or, after an abort, here (bounded)
         if (x_issuer && !ok)
-            for (int ab = 0; ab < 2 * kAStages; ++ab)
-                if (xuse[ab] > 0 && !mbar_wait_drain(smem_u32(x_full + ab), (xuse[ab] - 1) & 1))
+            for (int a = 0; a < kAStages; ++a)
+                if (xuse[a] > 0 && !mbar_wait_drain(smem_u32(x_full + a), (xuse[a] - 1) & 1))
                     atomicOr(p.status, kErrDrain);
     } else {
         // ------------------------------------------------ epilogue (warps 0..3)
