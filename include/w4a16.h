@@ -397,6 +397,17 @@ int w4a16_moe_sum(const uint16_t *y_sorted, const int32_t *pos, const float *wei
  * -1 for an invalid shape.  Pure host query. */
 int w4a16_select_rung(int M, int N, int K, int group);
 
+/* The plan of the first tile of a linear (of up to 8 tokens on the mma and
+ * gemv rungs, 64 on the tc rungs) as w4a16_linear_ex / w4a16_linear_epilogue
+ * would launch it now (honouring a forced rung): info[0] the rung, info[1]
+ * threads per CTA (the warp-MMA kernel: 256 = 8 warps, two CTAs per SM, or
+ * 512 = 16 warps, one CTA per SM), info[2] K slices (the tc rungs: 1 = whole
+ * tiles, 2 = stream-K), info[3] CTAs in the launch.  Pure host query; before
+ * w4a16_init it assumes 152 SMs.  Returns INVALID_ARG for a bad shape,
+ * epilogue or dtype (or a null info), UNSUPPORTED if a forced rung cannot run
+ * the shape. */
+int w4a16_plan_info(int M, int N, int K, int group, int epilogue, int dtype, int32_t *info);
+
 /* Force a rung for later calls (W4A16_RUNG_AUTO restores the table).  A forced
  * rung that cannot run a shape makes that call return W4A16_ERR_UNSUPPORTED.
  * Returns the previous setting, or -2 for an invalid rung.  Host state only:

@@ -209,6 +209,29 @@ def test_dispatch_table_host_queries(w4):
         w4.w4a16_set_forced_rung(9)
 
 
+def test_plan_info_names_the_cta_shape(w4):
+    # Pure host queries (152 SMs assumed before init).  Up to 4 tokens the
+    # warp-MMA kernel runs 8-warp CTAs; at 8 tokens a K 5120 linear's x only
+    # fits a 16-warp CTA (one per SM), which keeps K whole; K 17408 splits
+    # either way and stays on 8 warps.
+    assert w4.w4a16_set_forced_rung(w4.RUNG_AUTO) == w4.RUNG_AUTO
+    p = w4.w4a16_plan_info(4, 27648, 5120)
+    assert p["rung"] == w4.RUNG_MMA and p["threads"] == 256 and p["k_slices"] == 1
+    p = w4.w4a16_plan_info(8, 27648, 5120)
+    assert p["rung"] == w4.RUNG_MMA and p["threads"] == 512 and p["k_slices"] == 1
+    assert p["grid"] <= 152
+    p = w4.w4a16_plan_info(8, 5120, 17408)
+    assert p["rung"] == w4.RUNG_MMA_SPLITK and p["threads"] == 256 and p["k_slices"] > 1
+    p = w4.w4a16_plan_info(8, 34816, 5120, epilogue=w4.EPILOGUE_SILU_MUL)
+    assert p["threads"] == 512
+    p = w4.w4a16_plan_info(16, 27648, 5120)
+    assert p["rung"] in (w4.RUNG_TC, w4.RUNG_TC_SPLITK) and p["threads"] == 800
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_plan_info(4, 1024, 500)
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_plan_info(4, 1000, 512, epilogue=w4.EPILOGUE_SILU_MUL)  # N/2 not a multiple of 16
+
+
 def test_probe_counters_reset(w4):
     w4.w4a16_probe_reset()
     assert w4.w4a16_probe_counts() == [0] * 6

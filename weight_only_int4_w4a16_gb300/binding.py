@@ -104,6 +104,7 @@ _sig("w4a16_round_graph_create", [ctypes.POINTER(LinearDesc), _I, _I, ctypes.POI
 _sig("w4a16_round_graph_launch", [_P, _P])
 _sig("w4a16_round_graph_destroy", [_P])
 _sig("w4a16_select_rung", [_I, _I, _I, _I])
+_sig("w4a16_plan_info", [_I, _I, _I, _I, _I, _I, ctypes.POINTER(ctypes.c_int32)])
 _sig("w4a16_set_forced_rung", [_I])
 _sig("w4a16_probe_counts", [ctypes.POINTER(ctypes.c_uint64), _I])
 _sig("w4a16_probe_reset", [], None)
@@ -123,7 +124,7 @@ EXPORTED = ["w4a16_init", "w4a16_shutdown", "w4a16_workspace_bytes", "w4a16_pack
             "w4a16_moe_mlp_set_path", "w4a16_moe_mlp_path", "w4a16_moe_mlp_buffers",
             "w4a16_decode_round",
             "w4a16_round_graph_create", "w4a16_round_graph_launch", "w4a16_round_graph_destroy",
-            "w4a16_select_rung", "w4a16_set_forced_rung", "w4a16_probe_counts",
+            "w4a16_select_rung", "w4a16_plan_info", "w4a16_set_forced_rung", "w4a16_probe_counts",
             "w4a16_probe_reset", "w4a16_kernel_launches", "w4a16_rung_name", "w4a16_status_string",
             "w4a16_device_status", "w4a16_wait_probe", "w4a16_last_cuda_error",
             "w4a16_device_sm_count"]
@@ -507,6 +508,14 @@ class RoundGraph:
 
 def w4a16_select_rung(M: int, N: int, K: int, group: int = GROUP) -> int:
     return int(lib.w4a16_select_rung(M, N, K, group))
+
+
+def w4a16_plan_info(M: int, N: int, K: int, group: int = GROUP, epilogue: int = 0,
+                    dtype: int = 0) -> dict:
+    """The plan of a linear's first tile: rung, threads per CTA, K slices, CTAs."""
+    info = (ctypes.c_int32 * 4)()
+    _check(lib.w4a16_plan_info(M, N, K, group, epilogue, dtype, info), "w4a16_plan_info")
+    return {"rung": info[0], "threads": info[1], "k_slices": info[2], "grid": info[3]}
 
 
 def w4a16_set_forced_rung(rung: int) -> int:

@@ -1138,6 +1138,39 @@ int w4a16_select_rung(int M, int N, int K, int group) {
     return d.status ? -1 : d.rung;
 }
 
+int w4a16_plan_info(int M, int N, int K, int group, int epilogue, int dtype, int32_t *info) {
+    if (!info || M < 1 || M > kMaxM || check_shape(N, K, group)) return W4A16_ERR_INVALID_ARG;
+    if (epilogue < kEpiNone || epilogue > kEpiSiluMul || (dtype != kDtypeF16 && dtype != kDtypeBf16))
+        return W4A16_ERR_INVALID_ARG;
+    if (epilogue == kEpiSiluMul && N % 32 != 0) return W4A16_ERR_INVALID_ARG;
+    DeviceInfo dev = g_state.dev;
+    if (!g_state.initialized) dev.sm_count = 152;
+    const Decision d = decide(M, N, K, dev, g_state.forced_rung, epilogue, dtype);
+    if (d.status) return d.status;
+    const int Mt = M < tile_tokens(d.rung) ? M : tile_tokens(d.rung);
+    info[0] = d.rung;
+    if (is_mma(d.rung)) {
+        const MmaPlan p = plan_mma(Mt, N, K, split_rule(d.rung), dev, epilogue);
+        if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+        info[1] = p.warps * 32;
+        info[2] = p.S;
+        info[3] = p.grid;
+    } else if (is_tc(d.rung)) {
+        const TcPlan p = plan_tc(Mt, N, K, split_rule(d.rung), dev, epilogue);
+        if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+        info[1] = p.threads;
+        info[2] = p.S;
+        info[3] = p.grid;
+    } else {
+        const GemvPlan p = plan_gemv(Mt, N, K, split_rule(d.rung), dev);
+        if (!p.ok) return W4A16_ERR_UNSUPPORTED;
+        info[1] = p.threads;
+        info[2] = p.S;
+        info[3] = p.grid_x * p.S;
+    }
+    return W4A16_OK;
+}
+
 int w4a16_set_forced_rung(int rung) {
     if (rung < W4A16_RUNG_AUTO || rung >= W4A16_NUM_RUNGS) return -2;
     std::lock_guard<std::mutex> lock(g_mutex);

@@ -415,6 +415,7 @@ GemvPlan plan_gemv(int M, int N, int K, int split, const DeviceInfo &dev) {
     pl.grid_x = (N + pl.rows_per_cta - 1) / pl.rows_per_cta;
     pl.n_row_blocks = pl.grid_x;
     pl.ws_bytes = S > 1 ? (size_t)S * M * N * sizeof(float) : 0;
+    pl.threads = kThreads;
     pl.ok = true;
     return pl;
 }

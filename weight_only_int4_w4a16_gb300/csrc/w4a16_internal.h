@@ -77,6 +77,7 @@ struct GemvPlan {
     int grid_x;         // CTAs per slice (grid-stride over row blocks)
     int smem_bytes;     // dynamic shared memory (staged activations)
     size_t ws_bytes;    // split-K partial bytes (0 when S == 1)
+    int threads;        // per CTA
 };
 
 // split: 0 = never split K, 1 = split K (at least 2 slices when G >= 2),
@@ -101,6 +102,7 @@ struct TcPlan {
     int grid;          // CTAs (one per SM)
     int stages;        // shared-memory stages in flight per CTA
     size_t ws_bytes;   // workspace: stream-K partial sums
+    int threads;       // per CTA
 };
 
 // split: 0 = whole tiles only, 1 = stream-K, -1 = planner decides.  epi: the

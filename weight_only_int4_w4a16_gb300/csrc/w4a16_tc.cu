@@ -1054,6 +1054,7 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
     // partial-sum slots: split tiles, and whole SiLU-and-mul tiles (where the
     // gate and up rows meet)
     pl.ws_bytes = streamk || silu ? (size_t)2 * pl.grid * M * kTileN * sizeof(float) : 0;
+    pl.threads = kThreads;
     pl.ok = G >= 1 && pl.stages >= 2;
     return pl;
 }
