@@ -927,8 +927,9 @@ def main():
         del blin, bdescs, bxs
     rounds = None
     if not args.no_extra and rank == 0:
+        # M = 1 and 8 (the mma rungs), 16 and 64 (one tcgen05 launch per round)
         rounds = time_rounds_at(w4, lin, dev, stream, max(10, args.steps // 2), args.warmup, peak,
-                                args.layers)
+                                args.layers, Ms=(1, 8, 16, 64))
         rounds["M4"] = {"ms_per_round": ms, "GBps": value / world, "frac_of_peak": value / world / peak,
                         "mean_launch_us": roofline["mean_launch_us"],
                         "launch_frac_of_peak": roofline["frac"], "launches_per_round": per_round,

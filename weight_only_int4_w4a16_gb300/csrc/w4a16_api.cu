@@ -26,8 +26,8 @@ struct State {
     DeviceInfo dev{};
     Workspace ws{};
     void *ws_base = nullptr;
-    MmaLinDesc *round_descs = nullptr;     // device copy of the last fused round's descriptors
-    std::vector<MmaLinDesc> round_uploaded;  // what that copy holds
+    void *round_descs = nullptr;  // device copy of the last fused round's descriptors
+    std::vector<unsigned char> round_uploaded;  // what that copy holds
     int forced_rung = W4A16_RUNG_AUTO;
     bool log = false;
 };
@@ -297,22 +297,102 @@ int linear_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
 // the latest such linear to finish: the results are those of running the
 // linears one after another.
 struct FusedRound {
-    std::vector<MmaLinDesc> descs;
+    bool tc = false;                  // a tcgen05 round (9..64 tokens), else warp-MMA
+    std::vector<MmaLinDesc> descs;    // the warp-MMA round
     MmaRound round{};
-    int counters_used = 0;  // split-K counters, then n + 1 completion counters if waits exist
+    std::vector<TcLinDesc> tc_descs;  // the tcgen05 round
+    TcRound tc_round{};
+    int counters_used = 0;  // split-K counters, then the completion counters if waits exist
+    const void *desc_data() const {
+        return tc ? (const void *)tc_descs.data() : (const void *)descs.data();
+    }
+    size_t desc_bytes() const {
+        return tc ? tc_descs.size() * sizeof(TcLinDesc) : descs.size() * sizeof(MmaLinDesc);
+    }
+    size_t done_words() const {  // completion counters a graph of this round owns
+        if (tc) return tc_round.done ? tc_descs.size() + 1 : 0;
+        return round.done ? descs.size() : 0;
+    }
 };
 
 size_t bytes_of(int rows, int cols) { return (size_t)rows * cols * 2; }
 
+// The latest earlier linear of a round that linear l must wait for: one whose
+// output l reads (x, the residual), or whose input or output l writes over;
+// -1 if none.
+int round_wait_for(const w4a16_linear_desc *descs, int l, int M) {
+    const w4a16_linear_desc &d = descs[l];
+    const size_t dy = bytes_of(M, out_cols(d.N, d.epilogue));
+    for (int j = l - 1; j >= 0; --j) {
+        const w4a16_linear_desc &e = descs[j];
+        const size_t ey = bytes_of(M, out_cols(e.N, e.epilogue));
+        if (overlaps(e.y, ey, d.x, bytes_of(M, d.K)) ||
+            (d.residual && overlaps(e.y, ey, d.residual, dy)) ||
+            overlaps(e.x, bytes_of(M, e.K), d.y, dy) ||
+            (e.residual && overlaps(e.residual, ey, d.y, dy)) || overlaps(e.y, ey, d.y, dy))
+            return j;
+    }
+    return -1;
+}
+
+// A round of 9..64 tokens as one tcgen05 launch: one stream-K sequence over
+// every linear's tiles and stages.
+int plan_tc_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &st,
+                        FusedRound *fr) {
+    if (M > kTcMaxTokens) return W4A16_ERR_UNSUPPORTED;
+    fr->tc = true;
+    fr->tc_descs.resize(n);
+    std::vector<int> Ns(n), Ks(n), epis(n);
+    bool waits = false;
+    for (int l = 0; l < n; ++l) {
+        const w4a16_linear_desc &d = descs[l];
+        Ns[l] = d.N;
+        Ks[l] = d.K;
+        epis[l] = d.epilogue;
+    }
+    TcRound &r = fr->tc_round;
+    size_t ws_floats = 0;
+    std::vector<TcLinDesc> plan(n);
+    if (!plan_tc_round(M, Ns.data(), Ks.data(), epis.data(), n, st.dev, &r, plan.data(),
+                       &ws_floats))
+        return W4A16_ERR_UNSUPPORTED;
+    if (ws_floats * sizeof(float) > st.ws.partial_bytes) return W4A16_ERR_WORKSPACE;
+    int counters = 0;
+    for (int l = 0; l < n; ++l) {
+        const w4a16_linear_desc &d = descs[l];
+        LinearArgs a{reinterpret_cast<const __half *>(d.x), d.qweight,
+                     reinterpret_cast<const __half *>(d.scales), d.zeros,
+                     reinterpret_cast<__half *>(d.y), M, d.N, d.K, d.epilogue,
+                     reinterpret_cast<const __half *>(d.residual), d.dtype};
+        TcLinDesc &t = fr->tc_descs[l];
+        cudaError_t e = tc_describe(a, r.T, &t);
+        if (e != cudaSuccess) return cuda_fail(e);
+        t.n_tiles = plan[l].n_tiles;
+        t.spt = plan[l].spt;
+        t.start = plan[l].start;
+        t.counters = st.ws.counters + counters;  // one arrival counter per tile
+        counters += t.n_tiles;
+        t.wait_for = round_wait_for(descs, l, M);
+        waits |= t.wait_for >= 0;
+    }
+    if (counters + (waits ? n + 1 : 0) > st.ws.n_counters - kMmaSchedWords)
+        return W4A16_ERR_WORKSPACE;
+    r.partials = st.ws.partials;
+    r.done = waits ? st.ws.counters + counters : nullptr;
+    r.bf16 = descs[0].dtype == W4A16_DTYPE_BF16;
+    fr->counters_used = counters + (waits ? n + 1 : 0);
+    return W4A16_OK;
+}
+
 // OK, UNSUPPORTED (the round is not eligible: launch linear by linear), or an error.
 int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &st,
                      FusedRound *fr) {
-    if (st.forced_rung != W4A16_RUNG_AUTO || M > kMmaMaxTokens || n > kMaxRoundLinears)
-        return W4A16_ERR_UNSUPPORTED;
-    fr->descs.resize(n);
+    if (st.forced_rung != W4A16_RUNG_AUTO || n > kMaxRoundLinears) return W4A16_ERR_UNSUPPORTED;
     // one launch instantiates one 16-bit type
     for (int l = 1; l < n; ++l)
         if (descs[l].dtype != descs[0].dtype) return W4A16_ERR_UNSUPPORTED;
+    if (M > kMmaMaxTokens) return plan_tc_fused_round(descs, n, M, st, fr);
+    fr->descs.resize(n);
     size_t partial_floats = 0;
     int counters = 0, units = 0, smem = 0;
     bool waits = false;
@@ -339,18 +419,7 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
             counters += p.n_blocks;
         }
         // what a linear reads (x, the residual) and writes (y)
-        int wait_for = -1;
-        const size_t dy = bytes_of(M, out_cols(d.N, d.epilogue));
-        for (int j = l - 1; j >= 0 && wait_for < 0; --j) {
-            const w4a16_linear_desc &e = descs[j];
-            const size_t ey = bytes_of(M, out_cols(e.N, e.epilogue));
-            if (overlaps(e.y, ey, d.x, bytes_of(M, d.K)) ||
-                (d.residual && overlaps(e.y, ey, d.residual, dy)) ||
-                overlaps(e.x, bytes_of(M, e.K), d.y, dy) ||
-                (e.residual && overlaps(e.residual, ey, d.y, dy)) ||
-                overlaps(e.y, ey, d.y, dy))
-                wait_for = j;
-        }
+        const int wait_for = round_wait_for(descs, l, M);
         waits |= wait_for >= 0;
         LinearArgs a{reinterpret_cast<const __half *>(d.x), d.qweight,
                      reinterpret_cast<const __half *>(d.scales), d.zeros,
@@ -374,9 +443,26 @@ int plan_fused_round(const w4a16_linear_desc *descs, int n, int M, const State &
 }
 
 void count_fused_probes(const FusedRound &fr) {
+    if (fr.tc) {
+        // every linear of a tcgen05 round is a part of one stream-K sequence
+        g_probe[W4A16_RUNG_TC_SPLITK].fetch_add(fr.tc_descs.size(), std::memory_order_relaxed);
+        return;
+    }
     for (const MmaLinDesc &d : fr.descs)
         g_probe[d.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA].fetch_add(
             1, std::memory_order_relaxed);
+}
+
+cudaError_t launch_fused(FusedRound &fr, const void *descs_dev, unsigned *done_dev,
+                         const State &s, cudaStream_t stream) {
+    if (fr.tc) {
+        fr.tc_round.descs = (const TcLinDesc *)descs_dev;
+        if (done_dev && fr.tc_round.done) fr.tc_round.done = done_dev;
+        return launch_tc_round(fr.tc_round, s.ws.status, stream);
+    }
+    fr.round.descs = (const MmaLinDesc *)descs_dev;
+    if (done_dev && fr.round.done) fr.round.done = done_dev;
+    return launch_mma_round(fr.round, s.ws, s.dev, stream);
 }
 
 int validate_round(const w4a16_linear_desc *descs, int n_descs, int M) {
@@ -498,7 +584,9 @@ int w4a16_init(int device, size_t workspace_bytes) {
     // counters, then one status word (kept 256-byte aligned), then the fused
     // round descriptors
     const size_t counter_bytes = (size_t)kCounters * sizeof(unsigned) + 256;
-    const size_t desc_bytes = (size_t)kMaxRoundLinears * sizeof(MmaLinDesc);
+    const size_t desc_bytes =
+        (size_t)kMaxRoundLinears *
+        (sizeof(MmaLinDesc) > sizeof(TcLinDesc) ? sizeof(MmaLinDesc) : sizeof(TcLinDesc));
     void *base = nullptr;
     e = cudaMalloc(&base, workspace_bytes + counter_bytes + desc_bytes);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -520,7 +608,7 @@ int w4a16_init(int device, size_t workspace_bytes) {
     s.ws.counters = (unsigned *)((char *)base + workspace_bytes);
     s.ws.n_counters = kCounters;
     s.ws.status = (int *)((char *)base + workspace_bytes + (size_t)kCounters * sizeof(unsigned));
-    s.round_descs = (MmaLinDesc *)((char *)base + workspace_bytes + counter_bytes);
+    s.round_descs = (char *)base + workspace_bytes + counter_bytes;
     s.round_uploaded.clear();
     s.forced_rung = parse_rung(getenv("W4A16_FORCE_RUNG"));
     const char *lg = getenv("W4A16_LOG");
@@ -1035,24 +1123,25 @@ int w4a16_decode_round(const w4a16_linear_desc *descs, int n_descs, int M, void 
     if (st) return st;
     // upload the descriptors unless the device copy already holds these
     // (the copy is ordered on the stream after earlier rounds that read it)
-    const size_t bytes = fr.descs.size() * sizeof(MmaLinDesc);
-    if (s.round_uploaded.size() != fr.descs.size() ||
-        memcmp(s.round_uploaded.data(), fr.descs.data(), bytes) != 0) {
-        cudaError_t e = cudaMemcpyAsync(s.round_descs, fr.descs.data(), bytes,
-                                        cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    const size_t bytes = fr.desc_bytes();
+    const unsigned char *src = (const unsigned char *)fr.desc_data();
+    if (s.round_uploaded.size() != bytes || memcmp(s.round_uploaded.data(), src, bytes) != 0) {
+        cudaError_t e = cudaMemcpyAsync(s.round_descs, src, bytes, cudaMemcpyHostToDevice,
+                                        (cudaStream_t)stream);
         if (e != cudaSuccess) {
             s.round_uploaded.clear();
             return cuda_fail(e);
         }
-        s.round_uploaded = fr.descs;
+        s.round_uploaded.assign(src, src + bytes);
     }
-    fr.round.descs = s.round_descs;
-    cudaError_t e = launch_mma_round(fr.round, s.ws, s.dev, (cudaStream_t)stream);
+    cudaError_t e = launch_fused(fr, s.round_descs, nullptr, s, (cudaStream_t)stream);
     count_fused_probes(fr);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (s.log)
-        fprintf(stderr, "[w4a16] decode round of %d linears M=%d -> fused mma, %d units%s\n",
-                n_descs, M, fr.round.total_units, fr.round.done ? ", with waits" : "");
+        fprintf(stderr, "[w4a16] decode round of %d linears M=%d -> fused %s%s\n", n_descs, M,
+                fr.tc ? "tcgen05" : "mma",
+                (fr.tc ? fr.tc_round.done != nullptr : fr.round.done != nullptr) ? ", with waits"
+                                                                                  : "");
     return e == cudaSuccess ? W4A16_OK : cuda_fail(e);
 }
 
@@ -1068,16 +1157,18 @@ int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M,
     if (st && st != W4A16_ERR_UNSUPPORTED) return st;
     RoundGraphHandle *hd = new RoundGraphHandle();
     cudaError_t e = cudaSuccess;
+    void *graph_descs = nullptr;
+    unsigned *graph_done = nullptr;
     if (fused) {
         // the graph owns its descriptors and completion counters
-        const size_t dbytes = fr.descs.size() * sizeof(MmaLinDesc);
-        const size_t cbytes = fr.round.done ? (size_t)n_descs * sizeof(unsigned) : 0;
+        const size_t dbytes = (fr.desc_bytes() + 255) & ~(size_t)255;
+        const size_t cbytes = fr.done_words() * sizeof(unsigned);
         e = cudaMalloc(&hd->buffer, dbytes + cbytes);
         if (e == cudaSuccess)
-            e = cudaMemcpy(hd->buffer, fr.descs.data(), dbytes, cudaMemcpyHostToDevice);
+            e = cudaMemcpy(hd->buffer, fr.desc_data(), fr.desc_bytes(), cudaMemcpyHostToDevice);
         if (e == cudaSuccess && cbytes) e = cudaMemset((char *)hd->buffer + dbytes, 0, cbytes);
-        fr.round.descs = (const MmaLinDesc *)hd->buffer;
-        if (fr.round.done) fr.round.done = (unsigned *)((char *)hd->buffer + dbytes);
+        graph_descs = hd->buffer;
+        graph_done = cbytes ? (unsigned *)((char *)hd->buffer + dbytes) : nullptr;
     }
     cudaStream_t cs = nullptr;
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
@@ -1089,7 +1180,7 @@ int w4a16_round_graph_create(const w4a16_linear_desc *descs, int n_descs, int M,
         return cuda_fail(e);
     }
     if (fused) {
-        cudaError_t le = launch_mma_round(fr.round, s.ws, s.dev, cs);
+        cudaError_t le = launch_fused(fr, graph_descs, graph_done, s, cs);
         st = le == cudaSuccess ? W4A16_OK : cuda_fail(le);
         if (!st) count_fused_probes(fr);
     } else {

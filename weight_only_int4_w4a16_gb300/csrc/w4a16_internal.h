@@ -113,6 +113,47 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
                       cudaStream_t stream);
 cudaError_t tc_init(const DeviceInfo &dev);
 
+// One linear of a fused tcgen05 round, as the kernel reads it (device memory;
+// the tensor maps are written by the host only).  A round is one stream-K
+// sequence of (linear, tile, stage) work: linear l owns stages [start, start
+// + n_tiles * spt).
+struct alignas(64) TcLinDesc {
+    CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 64, 4}
+    CUtensorMap xmap;  // x 2-D: (K, M), box {64, T}, 128-byte swizzle
+    const __half *x;
+    const uint32_t *qw;
+    const __half *scales;
+    const uint32_t *zeros;
+    __half *y;
+    const __half *residual;  // y = h + residual, else null
+    unsigned *counters;      // this linear's per-tile arrival counters (split tiles)
+    long long start;         // its first stage in the round's sequence
+    int N, K, G, ZW;
+    int silu;                // SiLU-and-mul tiles (64 gate rows, their up rows N/2 below)
+    int n_tiles, spt;
+    int wait_for;            // -1, or an earlier linear that must finish first
+};
+// A fused tcgen05 round: n linears of M (9..64) tokens.
+struct TcRound {
+    const TcLinDesc *descs;  // device [n]
+    int n;
+    int M, T;
+    long long total;         // stages of all linears
+    int grid, stages;
+    float *partials;         // [2 * grid][M][128] fp32
+    unsigned *done;          // [n] tiles finished per linear, then 1 word: CTAs finished;
+                             // null when no linear waits for another
+    bool bf16;
+};
+// Fills r (except descs and done) and the descriptors' plan fields (n_tiles,
+// spt, start) for linears of shapes (N[l], K[l], epi[l]); false when the
+// round cannot take them.  ws_floats: the partial sums it needs.
+bool plan_tc_round(int M, const int *N, const int *K, const int *epi, int n, const DeviceInfo &dev,
+                   TcRound *r, TcLinDesc *descs, size_t *ws_floats);
+// The tensor maps and pointers of one linear of a round.
+cudaError_t tc_describe(const LinearArgs &a, int T, TcLinDesc *d);
+cudaError_t launch_tc_round(const TcRound &r, int *status, cudaStream_t stream);
+
 // ---- warp-level tensor-core MMA rungs (w4a16_mma.cu) ----------------------
 constexpr int kMmaMaxTokens = 8;  // tokens per launch (the MMA's N = 8)
 

@@ -93,26 +93,19 @@ constexpr uint32_t kBigScaleBf16 = 0x7B80u;
 
 // error codes recorded in the device status word (bit flags)
 constexpr int kErrWaitFull = 1, kErrWaitAFull = 2, kErrWaitDFull = 4, kErrWaitEmpty = 8,
-              kErrWaitAEmpty = 16, kErrWaitDEmpty = 32, kErrDrain = 64;
+              kErrWaitAEmpty = 16, kErrWaitDEmpty = 32, kErrDrain = 64, kErrWaitLinear = 65536;
 
 struct TcParams {
-    CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 128, 4}
-    CUtensorMap xmap;  // x 2-D: (K, M), box {64, T}, 128-byte swizzle: half a group
-    const __half *x;   // x as given (the exact path)
-    const uint32_t *qw;
-    const __half *scales;
-    const uint32_t *zeros;
-    __half *y;
-    const __half *residual;  // y = h + residual (the residual epilogue), else null
-    float *partials;     // stream-K: [2 * grid][M][128] fp32
-    unsigned *counters;  // stream-K: one per tile, zero between launches
+    TcLinDesc single;       // the linear of a one-linear launch (start 0, no wait)
+    const TcLinDesc *lins;  // a fused round: device [n_lin] linears; null for one linear
+    int n_lin;
+    unsigned *done;         // a round with waits: [n_lin] tiles finished, then CTAs finished
+    float *partials;        // stream-K: [2 * grid][M][128] fp32
     int *status;
-    int N, K, G, ZW, M;
-    int silu;          // SiLU-and-mul: a tile is 64 gate rows and the 64 up rows N/2 below
-    int n_tiles, spt;  // tiles, stages per tile
+    int M;
     int streamk;
-    int n_stages;      // shared-memory stages
-    long long total;   // n_tiles * spt
+    int n_stages;           // shared-memory stages
+    long long total;        // stages of all linears
 };
 
 template <int T, bool kBf16 = false>
@@ -359,6 +352,7 @@ struct Walk {
     long long pos, end;  // stream-K: the CTA's stage range
     int tile;            // whole tiles: the current tile
     bool started;
+    int l;               // the linear of the current segment
 };
 
 __device__ __forceinline__ long long range_begin(const TcParams &p, int b) {
@@ -370,46 +364,55 @@ __device__ __forceinline__ void walk_init(const TcParams &p, Walk &w) {
     w.end = range_begin(p, blockIdx.x + 1);
     w.tile = blockIdx.x;
     w.started = false;
+    w.l = 0;
 }
 
-// next segment: tile t, stages [j0, j1) of it; false when the CTA is done
-__device__ __forceinline__ bool walk_next(const TcParams &p, Walk &w, int &t, int &j0, int &j1) {
+// next segment: linear l, its tile t, stages [j0, j1) of it; false when the
+// CTA is done.  Stream-K runs over the round's sequence of (linear, tile,
+// stage); whole tiles (one linear only) go to the CTAs in turn.
+__device__ __forceinline__ bool walk_next(const TcParams &p, const TcLinDesc *lins, int n_lin,
+                                          Walk &w, int &l, int &t, int &j0, int &j1) {
     if (p.streamk) {
         if (w.pos >= w.end) return false;
-        t = (int)(w.pos / p.spt);
-        j0 = (int)(w.pos - (long long)t * p.spt);
-        const long long tile_end = (long long)(t + 1) * p.spt;
-        const long long e = tile_end < w.end ? tile_end : w.end;
-        j1 = (int)(e - (long long)t * p.spt);
+        while (w.l + 1 < n_lin && w.pos >= lins[w.l + 1].start) ++w.l;
+        l = w.l;
+        const long long base = lins[l].start;
+        const int spt = lins[l].spt;
+        t = (int)((w.pos - base) / spt);
+        const long long t0 = base + (long long)t * spt;
+        j0 = (int)(w.pos - t0);
+        const long long e = t0 + spt < w.end ? t0 + spt : w.end;
+        j1 = (int)(e - t0);
         w.pos = e;
         return true;
     }
     if (w.started) w.tile += gridDim.x;
     w.started = true;
-    if (w.tile >= p.n_tiles) return false;
+    if (w.tile >= lins[0].n_tiles) return false;
+    l = 0;
     t = w.tile;
     j0 = 0;
-    j1 = p.spt;
+    j1 = lins[0].spt;
     return true;
 }
 
 // groups of stage j: [4j, min(4j + 4, G))
-__device__ __forceinline__ int stage_groups(const TcParams &p, int j) {
-    return min(kSG, p.G - kSG * j);
+__device__ __forceinline__ int stage_groups(const TcLinDesc &L, int j) {
+    return min(kSG, L.G - kSG * j);
 }
 
 // Weight row of tile row r (0..127): rows 0..63 and 64..127 of a tile come as
 // two TMA boxes of 64 rows.  A plain tile is 128 consecutive rows; with
 // SiLU-and-mul it is 64 gate rows and the matching up rows N/2 below, so that
 // both halves of 64 outputs meet in one tile.
-__device__ __forceinline__ int tile_row(const TcParams &p, int t, int r) {
-    if (p.silu) return (r < 64 ? 0 : p.N / 2) + 64 * t + (r & 63);
+__device__ __forceinline__ int tile_row(const TcLinDesc &L, int t, int r) {
+    if (L.silu) return (r < 64 ? 0 : L.N / 2) + 64 * t + (r & 63);
     return kTileN * t + r;
 }
 // whether tile row r of tile t is a row of the weight matrix
-__device__ __forceinline__ bool tile_row_valid(const TcParams &p, int t, int r) {
-    if (p.silu) return 64 * t + (r & 63) < p.N / 2;
-    return kTileN * t + r < p.N;
+__device__ __forceinline__ bool tile_row_valid(const TcLinDesc &L, int t, int r) {
+    if (L.silu) return 64 * t + (r & 63) < L.N / 2;
+    return kTileN * t + r < L.N;
 }
 
 // The CTA whose range holds stage st (stream-K).
@@ -422,16 +425,47 @@ __device__ __forceinline__ int cta_of(const TcParams &p, long long st) {
 // is written: sixteen independent loads, one round trip, where a load after
 // each store would wait for the store (the compiler must assume they alias).
 template <bool kBf16>
-__device__ __forceinline__ void store_y16(const TcParams &p, int n, int t0, const float (&v)[16]) {
+__device__ __forceinline__ void store_y16(const TcLinDesc &L, int M, int n, int t0,
+                                          const float (&v)[16]) {
     float res[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        res[i] = p.residual && t0 + i < p.M
-                     ? f16_to_float<kBf16>(p.residual[(size_t)(t0 + i) * p.N + n])
+        res[i] = L.residual && t0 + i < M
+                     ? f16_to_float<kBf16>(L.residual[(size_t)(t0 + i) * L.N + n])
                      : 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-        if (t0 + i < p.M) p.y[(size_t)(t0 + i) * p.N + n] = float_to_f16<kBf16>(v[i] + res[i]);
+        if (t0 + i < M) L.y[(size_t)(t0 + i) * L.N + n] = float_to_f16<kBf16>(v[i] + res[i]);
+}
+
+// Whether CTA b's range begins strictly inside the tile whose first stage is
+// tile0: then its segment of that tile is its first one and uses partial-sum
+// slot 2b; any other partial segment of CTA b (its last one, which starts at a
+// tile's first stage) uses slot 2b + 1.
+__device__ __forceinline__ bool starts_inside(const TcParams &p, int b, long long tile0, int spt) {
+    const long long rb = range_begin(p, b);
+    return rb > tile0 && rb < tile0 + spt;
+}
+
+// A fused round with waits: linear w has finished once every tile of it has
+// its outputs written (p.done[w] counts them).  Bounded: false on expiry.
+__device__ __forceinline__ bool wait_linear(const TcParams &p, const TcLinDesc *lins, int w,
+                                            volatile int *abort) {
+    const volatile unsigned *d = p.done + w;
+    const unsigned need = (unsigned)lins[w].n_tiles;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1; *d < need; ++i) {
+        __nanosleep(64);
+        if ((i & 15) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitNs) return false;
+        }
+    }
+    // the writers fenced before they counted; order this thread's later
+    // reads (and its TMA copies, the async proxy) after the count
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -444,16 +478,16 @@ __device__ __forceinline__ void store_y16(const TcParams &p, int n, int t0, cons
 // out of line: it is rare, and its registers stay out of the kernel's.
 // ---------------------------------------------------------------------------
 template <bool kBf16>
-__device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1, bool whole,
-                                       float *part) {
-    const uint32_t *qrow = p.qw + (size_t)n * (p.K / 8);
-    for (int t0 = 0; t0 < p.M; t0 += 16) {
+__device__ __noinline__ void exact_row(const TcLinDesc &L, int M, int n, int g0, int g1,
+                                       bool whole, float *part) {
+    const uint32_t *qrow = L.qw + (size_t)n * (L.K / 8);
+    for (int t0 = 0; t0 < M; t0 += 16) {
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
         for (int g = g0; g < g1; ++g) {
-            const float sc = f16_to_float<kBf16>(p.scales[(size_t)n * p.G + g]);
-            const int z = (int)((p.zeros[(size_t)n * p.ZW + (g >> 3)] >> (4 * (g & 7))) & 0xfu);
+            const float sc = f16_to_float<kBf16>(L.scales[(size_t)n * L.G + g]);
+            const int z = (int)((L.zeros[(size_t)n * L.ZW + (g >> 3)] >> (4 * (g & 7))) & 0xfu);
             for (int wd = 0; wd < kGroup / 8; ++wd) {
                 const uint32_t word = qrow[g * (kGroup / 8) + wd];
                 for (int nb = 0; nb < 8; ++nb) {
@@ -461,8 +495,8 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
                     const float wv = (float)((int)((word >> (4 * nb)) & 0xfu) - z) * sc;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (t0 + i < p.M)
-                            acc[i] = fmaf(wv, f16_to_float<kBf16>(p.x[(size_t)(t0 + i) * p.K + k]),
+                        if (t0 + i < M)
+                            acc[i] = fmaf(wv, f16_to_float<kBf16>(L.x[(size_t)(t0 + i) * L.K + k]),
                                           acc[i]);
                 }
             }
@@ -470,13 +504,13 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int tt = t0 + i;
-            if (tt >= p.M) break;
+            if (tt >= M) break;
             if (!whole) {
                 part[(size_t)tt * kTileN] = acc[i];
             } else {
-                const size_t o = (size_t)tt * p.N + n;
-                const float res = p.residual ? f16_to_float<kBf16>(p.residual[o]) : 0.f;
-                p.y[o] = float_to_f16<kBf16>(acc[i] + res);
+                const size_t o = (size_t)tt * L.N + n;
+                const float res = L.residual ? f16_to_float<kBf16>(L.residual[o]) : 0.f;
+                L.y[o] = float_to_f16<kBf16>(acc[i] + res);
             }
         }
     }
@@ -485,7 +519,9 @@ __device__ __noinline__ void exact_row(const TcParams &p, int n, int g0, int g1,
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int T, bool kBf16>
+// kRound: a fused round (the linears' descriptors in device memory); else one
+// linear, whose descriptor the kernel reads from its parameters
+template <int T, bool kBf16, bool kRound>
 __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ TcParams p) {
     using C = TcConfig<T, kBf16>;
     extern __shared__ uint8_t smem_raw[];
@@ -527,10 +563,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         mbar_init(smem_u32(done), kMmaWarps);
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.wmap))
-                     : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap))
-                     : "memory");
+        if (!p.lins) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(
+                             reinterpret_cast<uint64_t>(&p.single.wmap))
+                         : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(
+                             reinterpret_cast<uint64_t>(&p.single.xmap))
+                         : "memory");
+        }
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -544,9 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // the linears: the round's, or the one of this launch
+    const TcLinDesc *lins = kRound ? p.lins : &p.single;
+    const int n_lin = kRound ? p.n_lin : 1;
     Walk wk;
     walk_init(p, wk);
-    int t = 0, j0 = 0, j1 = 0;
+    int l = 0, t = 0, j0 = 0, j1 = 0;
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------ weight producer
@@ -557,11 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         uint64_t pol = 0;
         if (lane == 0)  // the weights are read once
             asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-        const uintptr_t s_end = (uintptr_t)(p.scales + (size_t)p.N * p.G);
-        const void *s_any = p.scales;  // a valid source for zero-byte copies
         int sc = 0;  // stages issued
         bool ok = true;
-        while (ok && walk_next(p, wk, t, j0, j1)) {
+        while (ok && walk_next(p, lins, kRound ? n_lin : 1, wk, l, t, j0, j1)) {
+            const TcLinDesc &L = kRound ? p.lins[l] : p.single;
+            const uintptr_t s_end = (uintptr_t)(L.scales + (size_t)L.N * L.G);
+            const void *s_any = L.scales;  // a valid source for zero-byte copies
             for (int j = j0; j < j1; ++j, ++sc) {
                 const int s = sc % NS;
                 if (sc >= NS &&
@@ -576,25 +620,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 if (lane == 0) {
                     // tile rows 0..63, then 64..127: [half][group][64 rows][64 bytes]
                     mbar_arrive_expect_tx(bar, (uint32_t)kStageW);
-                    tma_load_3d(smem_u32(st), &p.wmap, 0, tile_row(p, t, 0), kSG * j, bar, pol);
-                    tma_load_3d(smem_u32(st + kStageW / 2), &p.wmap, 0, tile_row(p, t, 64), kSG * j,
+                    tma_load_3d(smem_u32(st), &L.wmap, 0, tile_row(L, t, 0), kSG * j, bar, pol);
+                    tma_load_3d(smem_u32(st + kStageW / 2), &L.wmap, 0, tile_row(L, t, 64), kSG * j,
                                 bar, pol);
                 }
                 uint8_t *m = st + kStageW;
 #pragma unroll
                 for (int i = 0; i < kTileN / 32; ++i) {
-                    const int r = lane + 32 * i, n = tile_row(p, t, r);
+                    const int r = lane + 32 * i, n = tile_row(L, t, r);
                     const uint32_t dst = smem_u32(m + r * 16);
-                    if (tile_row_valid(p, t, r)) {
+                    if (tile_row_valid(L, t, r)) {
                         const uintptr_t a0 =
-                            (uintptr_t)(p.scales + (size_t)n * p.G + kSG * j) & ~(uintptr_t)3;
+                            (uintptr_t)(L.scales + (size_t)n * L.G + kSG * j) & ~(uintptr_t)3;
 #pragma unroll
                         for (int w = 0; w < 3; ++w) {
                             const uintptr_t a = a0 + 4 * w;
                             cp4(dst + 4 * w, a < s_end ? (const void *)a : s_any,
                                 a < s_end ? 4u : 0u);
                         }
-                        cp4(dst + 12, p.zeros + (size_t)n * p.ZW + (kSG * j) / 8, 4u);
+                        cp4(dst + 12, L.zeros + (size_t)n * L.ZW + (kSG * j) / 8, 4u);
                     } else {
 #pragma unroll
                         for (int w = 0; w < 4; ++w) cp4(dst + 4 * w, s_any, 0u);
@@ -616,7 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             int c = 0, q = 0;                // groups, segments seen
             bool ok = true;
             const uint32_t xb = smem_u32(sm_x + me * C::kXSlot);
-            while (ok && walk_next(p, wk, t, j0, j1)) {
+            while (ok && walk_next(p, lins, kRound ? n_lin : 1, wk, l, t, j0, j1)) {
+            const TcLinDesc &L = kRound ? p.lins[l] : p.single;
                 const int dset = q % C::kDSets, duse = q / C::kDSets;
                 if (!mbar_wait(smem_u32(d_empty + dset), (duse & 1) ^ 1, abort)) {
                     fail(abort, p.status, kErrWaitDEmpty);
@@ -626,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 const uint32_t d_tmem =
                     tmem + C::kDBase + dset * C::kDBuf + me * C::kChains * T;
                 bool first = true;  // this issuer's first MMAs of the segment start its chains
-                const int ng = min(p.G, kSG * j1) - kSG * j0;
+                const int ng = min(L.G, kSG * j1) - kSG * j0;
                 for (int gi = 0; gi < ng; ++gi, ++c) {
                     if ((c & (kMmaWarps - 1)) != me) continue;
                     const uint32_t use = (uint32_t)(c / kAStages) & 1;
@@ -676,14 +721,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         if (x_issuer)  // x is read by every CTA
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
         bool dep_waited = false;
+        int x_waited = -1;  // the last linear whose wait_for this thread has waited for
         int xuse[kAStages] = {0, 0, 0, 0};  // x copies this thread issued per slot
         int c = 0, sc = 0;
         bool ok = true;
-        while (ok && walk_next(p, wk, t, j0, j1)) {
-            const int n = tile_row(p, t, r);
-            const __half *srow = p.scales + (size_t)(tile_row_valid(p, t, r) ? n : 0) * p.G;
+        while (ok && walk_next(p, lins, kRound ? n_lin : 1, wk, l, t, j0, j1)) {
+            const TcLinDesc &L = kRound ? p.lins[l] : p.single;
+            const int n = tile_row(L, t, r);
+            const __half *srow = L.scales + (size_t)(tile_row_valid(L, t, r) ? n : 0) * L.G;
             for (int j = j0; j < j1 && ok; ++j, ++sc) {
-                const int s = sc % NS, ng = stage_groups(p, j);
+                const int s = sc % NS, ng = stage_groups(L, j);
                 const uint8_t *st = sm_stage + (size_t)s * C::kStageBytes;
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(full + s), (sc / NS) & 1, abort))) {
                     fail(abort, p.status, kErrWaitFull);
@@ -750,11 +797,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             grid_dependency_wait();
                             dep_waited = true;
                         }
+                        // a round with waits: x may be an earlier linear's output
+                        if (kRound && p.done && L.wait_for >= 0 && l != x_waited) {
+                            x_waited = l;
+                            if (!wait_linear(p, lins, L.wait_for, abort))
+                                fail(abort, p.status, kErrWaitLinear);
+                        }
                         const uint32_t xbar = smem_u32(x_full + a);
                         mbar_arrive_expect_tx(xbar, (uint32_t)C::kXSlot);
                         const int k0 = (kSG * j + gi) * kGroup;
-                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot), &p.xmap, k0, 0, xbar, pol_x);
-                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot + T * 128), &p.xmap, k0 + 64, 0,
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot), &L.xmap, k0, 0, xbar, pol_x);
+                        tma_load_2d(smem_u32(sm_x + a * C::kXSlot + T * 128), &L.xmap, k0 + 64, 0,
                                     xbar, pol_x);
                         ++xuse[a];
                     }
@@ -828,12 +881,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         // outputs, partial sums and counters may belong to the preceding kernel
         grid_dependency_wait();
         int c = 0, q = 0;
+        int waited = -1;  // the last linear whose wait_for this role has waited for
         bool ok = true;
-        while (ok && walk_next(p, wk, t, j0, j1)) {
+        while (ok && walk_next(p, lins, kRound ? n_lin : 1, wk, l, t, j0, j1)) {
+            const TcLinDesc &L = kRound ? p.lins[l] : p.single;
             const int dset = q % C::kDSets, duse = q / C::kDSets;
-            const int n = tile_row(p, t, r);
-            const bool vrow = tile_row_valid(p, t, r);
-            const int g0 = kSG * j0, g1 = min(p.G, kSG * j1);
+            const int n = tile_row(L, t, r);
+            const bool vrow = tile_row_valid(L, t, r);
+            const int g0 = kSG * j0, g1 = min(L.G, kSG * j1);
             const int c0 = c;
             c += g1 - g0;
             // while the MMAs run: does a scale of this row in the range reach
@@ -842,9 +897,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             bool big = false;
             if (vrow) {
                 const unsigned short *sr =
-                    reinterpret_cast<const unsigned short *>(p.scales) + (size_t)n * p.G;
+                    reinterpret_cast<const unsigned short *>(L.scales) + (size_t)n * L.G;
                 const uint32_t lim = kBf16 ? kBigScaleBf16 : kBigScale;
                 for (int g = g0; g < g1; ++g) big |= (sr[g] & 0x7fffu) >= lim;
+            }
+            if (kRound && p.done && L.wait_for >= 0 && l != waited) {
+                // a round with waits: what this linear writes (and its residual
+                // and x, which the exact path reads) may belong to an earlier
+                // linear: wait until it has finished
+                waited = l;
+                bool fine = true;
+                if (threadIdx.x == 0) fine = wait_linear(p, lins, L.wait_for, abort);
+                if (!fine) fail(abort, p.status, kErrWaitLinear);
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                if (*abort) {
+                    ok = false;
+                    break;
+                }
             }
             if (!__all_sync(0xffffffffu,
                             mbar_wait(smem_u32(d_full + dset), duse & 1, abort))) {
@@ -853,23 +922,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 break;
             }
             tc_fence_after();
-            const bool whole = j0 == 0 && j1 == p.spt;
+            const bool whole = j0 == 0 && j1 == L.spt;
             // y straight from the sums: a whole tile without SiLU-and-mul.  Else
             // the sums go to this CTA's partial-sum slot: part of a tile (the
             // last CTA of the tile adds the slots in K order, which is CTA
             // order), or a whole SiLU-and-mul tile, whose gate and up rows
             // meet there (slot 2b + 1 for it: this CTA's last partial segment,
             // which also uses it, comes after every whole one)
-            const bool direct = whole && !p.silu;
+            const bool direct = whole && !L.silu;
+            const long long tile0 = L.start + (long long)t * L.spt;  // its first stage
             const int slot =
                 2 * (int)blockIdx.x +
-                (whole || range_begin(p, blockIdx.x) / p.spt != t ? 1 : 0);
+                (whole || !starts_inside(p, blockIdx.x, tile0, L.spt) ? 1 : 0);
             float *part = p.partials + (size_t)slot * p.M * kTileN + r;
             // 16 tokens' outputs of this row: y = h (+ residual), one rounding,
             // or the partial sums
             auto put16 = [&](int t0, float (&v)[16]) {
                 if (direct) {
-                    if (vrow) store_y16<kBf16>(p, n, t0, v);
+                    if (vrow) store_y16<kBf16>(L, p.M, n, t0, v);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -907,18 +977,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(d_empty + dset));
             // a row whose scales may overflow the fp16 restore: exact on the CUDA cores
-            if (big) exact_row<kBf16>(p, n, g0, g1, direct, part);
+            if (big) exact_row<kBf16>(L, p.M, n, g0, g1, direct, part);
+            if (kRound && direct && p.done) {
+                // a round with waits: this tile's outputs are all written
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                if (threadIdx.x == 0) atomicAdd(p.done + l, 1u);
+            }
             if (!direct) {
                 __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
                 // the CTAs whose slots hold the tile's sums: this one (a whole
                 // tile), or every CTA whose range meets the tile
-                const long long ts0 = (long long)t * p.spt;
-                const int b0 = whole ? (int)blockIdx.x : cta_of(p, ts0);
-                const int b1 = whole ? (int)blockIdx.x : cta_of(p, ts0 + p.spt - 1);
+                const int b0 = whole ? (int)blockIdx.x : cta_of(p, tile0);
+                const int b1 = whole ? (int)blockIdx.x : cta_of(p, tile0 + L.spt - 1);
                 if (!whole) {
                     if (threadIdx.x == 0) {
-                        const unsigned prev = atomicAdd(p.counters + t, 1u);
+                        const unsigned prev = atomicAdd(L.counters + t, 1u);
                         *s_last = prev == (unsigned)(b1 - b0) ? 1 : 0;
                     }
                     asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
@@ -932,7 +1007,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 16; ++i) sum[i] = 0.f;
                         for (int b = b0; b <= b1; ++b) {
-                            const int sl = 2 * b + (whole || range_begin(p, b) / p.spt != t ? 1 : 0);
+                            const int sl =
+                                2 * b + (whole || !starts_inside(p, b, tile0, L.spt) ? 1 : 0);
                             const float *src = p.partials + ((size_t)sl * p.M + t0) * kTileN + rr;
                             float v[16];
 #pragma unroll
@@ -942,18 +1018,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             for (int i = 0; i < 16; ++i) sum[i] += v[i];
                         }
                     };
-                    if (!p.silu) {
+                    if (!L.silu) {
                         if (vrow) {
                             for (int t0 = 0; t0 < p.M; t0 += 16) {
                                 float sum[16];
                                 gather(r, t0, sum);
-                                store_y16<kBf16>(p, n, t0, sum);
+                                store_y16<kBf16>(L, p.M, n, t0, sum);
                             }
                         }
                     } else if (r < 64 && vrow) {
                         // SiLU-and-mul: the gate row's thread takes its up row
                         // (tile row r + 64): y = silu(g) * u, silu(g) = g / (1 + e^-g)
-                        const int ycols = p.N / 2, jcol = 64 * t + r;
+                        const int ycols = L.N / 2, jcol = 64 * t + r;
                         for (int t0 = 0; t0 < p.M; t0 += 16) {
                             float gs[16], us[16];
                             gather(r, t0, gs);
@@ -962,17 +1038,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                             for (int i = 0; i < 16; ++i) {
                                 if (t0 + i >= p.M) continue;
                                 const float g = gs[i];
-                                p.y[(size_t)(t0 + i) * ycols + jcol] =
+                                L.y[(size_t)(t0 + i) * ycols + jcol] =
                                     float_to_f16<kBf16>(us[i] * (g / (1.f + expf(-g))));
                             }
                         }
                     }
-                    if (!whole && threadIdx.x == 0) p.counters[t] = 0u;  // ready for the next launch
+                    if (!whole && threadIdx.x == 0) L.counters[t] = 0u;  // ready for the next launch
                 }
                 // the slot and s_last are written again only after the next such
                 // segment's first barrier, which every epilogue thread reaches
                 // after its reads
+                if (kRound && p.done) __threadfence();
                 asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+                // a round with waits: the tile's outputs are all written
+                if (kRound && p.done && threadIdx.x == 0 && (whole || *s_last)) atomicAdd(p.done + l, 1u);
             }
             ++q;
         }
@@ -980,6 +1059,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 
     tc_fence_before();
     __syncthreads();
+    if (kRound && p.done && threadIdx.x == 0) {
+        // a round with waits: the last CTA out zeroes the linears' counters
+        // (every wait of every CTA is over by then) for the next launch
+        __threadfence();
+        if (atomicAdd(p.done + n_lin, 1u) == gridDim.x - 1) {
+            for (int i = 0; i < n_lin; ++i) p.done[i] = 0u;
+            p.done[n_lin] = 0u;
+            __threadfence();
+        }
+    }
     if (warp == 0) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -1020,11 +1109,21 @@ cudaLaunchConfig_t pdl_config(dim3 grid, int threads, int smem, cudaStream_t str
 }
 
 template <int T>
-cudaError_t launch_t(const TcParams &p, bool bf16, int grid, cudaStream_t stream) {
-    cudaLaunchAttribute attr[1];
+cudaError_t launch_t(const TcParams &p, bool bf16, int grid, bool cooperative,
+                     cudaStream_t stream) {
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), kThreads, smem_for<T>(p.n_stages), stream, attr);
-    return bf16 ? cudaLaunchKernelEx(&cfg, tc_kernel<T, true>, p)
-                : cudaLaunchKernelEx(&cfg, tc_kernel<T, false>, p);
+    if (cooperative) {
+        // linears wait for earlier ones: every CTA must be resident at once
+        attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+        attr[cfg.numAttrs].val.cooperative = 1;
+        cfg.numAttrs += 1;
+    }
+    if (p.lins)
+        return bf16 ? cudaLaunchKernelEx(&cfg, tc_kernel<T, true, true>, p)
+                    : cudaLaunchKernelEx(&cfg, tc_kernel<T, false, true>, p);
+    return bf16 ? cudaLaunchKernelEx(&cfg, tc_kernel<T, true, false>, p)
+                : cudaLaunchKernelEx(&cfg, tc_kernel<T, false, false>, p);
 }
 
 }  // namespace
@@ -1062,24 +1161,25 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
 cudaError_t tc_init(const DeviceInfo &dev) {
     (void)dev;
     if (!tensor_map_encoder()) return cudaErrorSymbolNotFound;
-    const void *fns[6] = {(const void *)tc_kernel<16, false>, (const void *)tc_kernel<32, false>,
-                          (const void *)tc_kernel<64, false>, (const void *)tc_kernel<16, true>,
-                          (const void *)tc_kernel<32, true>,  (const void *)tc_kernel<64, true>};
+    const void *fns[12] = {
+        (const void *)tc_kernel<16, false, false>, (const void *)tc_kernel<32, false, false>,
+        (const void *)tc_kernel<64, false, false>, (const void *)tc_kernel<16, true, false>,
+        (const void *)tc_kernel<32, true, false>,  (const void *)tc_kernel<64, true, false>,
+        (const void *)tc_kernel<16, false, true>,  (const void *)tc_kernel<32, false, true>,
+        (const void *)tc_kernel<64, false, true>,  (const void *)tc_kernel<16, true, true>,
+        (const void *)tc_kernel<32, true, true>,   (const void *)tc_kernel<64, true, true>};
     const int smem[3] = {smem_for<16>(stages_for<16>()), smem_for<32>(stages_for<32>()),
                          smem_for<64>(stages_for<64>())};
     cudaError_t e = cudaSuccess;
-    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    for (int i = 0; i < 12 && e == cudaSuccess; ++i)
         e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, smem[i % 3]);
     return e;
 }
 
-cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
-                      cudaStream_t stream) {
-    const bool bf16 = a.dtype == kDtypeBf16;
+cudaError_t tc_describe(const LinearArgs &a, int T, TcLinDesc *d) {
     const EncodeTiledFn encode = tensor_map_encoder();
     if (!encode) return cudaErrorInitializationError;
-    TcParams p;
-    memset(&p, 0, sizeof(p));
+    memset(d, 0, sizeof(*d));
     const int G = a.K / kGroup;
     {
         // qweight as (word in group, row, group): a box of 64 rows x 4 groups
@@ -1088,9 +1188,10 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
         const cuuint64_t strides[2] = {(cuuint64_t)a.K / 2, 64};
         const cuuint32_t box[3] = {16, (cuuint32_t)(kTileN / 2), (cuuint32_t)kSG};
         const cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = encode(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult r = encode(&d->wmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, (void *)a.qw, dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
@@ -1100,37 +1201,100 @@ cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &
         // tokens past M read zeros
         const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
         const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)plan.T};
+        const cuuint32_t box[2] = {64, (cuuint32_t)T};
         const cuuint32_t estr[2] = {1, 1};
-        CUresult r = encode(&p.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)a.x, dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult r = encode(&d->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)a.x, dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    p.x = a.x;
-    p.qw = a.qw;
-    p.scales = a.scales;
-    p.zeros = a.zeros;
-    p.y = a.y;
-    p.residual = a.epi == kEpiResidual ? a.residual : nullptr;
+    d->x = a.x;
+    d->qw = a.qw;
+    d->scales = a.scales;
+    d->zeros = a.zeros;
+    d->y = a.y;
+    d->residual = a.epi == kEpiResidual ? a.residual : nullptr;
+    d->N = a.N;
+    d->K = a.K;
+    d->G = G;
+    d->ZW = (G + 7) / 8;
+    d->silu = a.epi == kEpiSiluMul;
+    d->wait_for = -1;
+    return cudaSuccess;
+}
+
+cudaError_t launch_tc(const LinearArgs &a, const TcPlan &plan, const Workspace &ws, int *status,
+                      cudaStream_t stream) {
+    const bool bf16 = a.dtype == kDtypeBf16;
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    cudaError_t e = tc_describe(a, plan.T, &p.single);
+    if (e != cudaSuccess) return e;
+    p.single.counters = ws.counters;
+    p.single.n_tiles = plan.n_tiles;
+    p.single.spt = plan.spt;
+    p.single.start = 0;
+    p.lins = nullptr;
+    p.n_lin = 1;
+    p.done = nullptr;
     p.partials = ws.partials;
-    p.counters = ws.counters;
     p.status = status;
-    p.N = a.N;
-    p.K = a.K;
-    p.G = G;
-    p.ZW = (G + 7) / 8;
     p.M = a.M;
-    p.silu = a.epi == kEpiSiluMul;
-    p.n_tiles = plan.n_tiles;
-    p.spt = plan.spt;
     p.streamk = plan.S > 1;
     p.n_stages = plan.stages;
     p.total = (long long)plan.n_tiles * plan.spt;
     switch (plan.T) {
-        case 16: return launch_t<16>(p, bf16, plan.grid, stream);
-        case 32: return launch_t<32>(p, bf16, plan.grid, stream);
-        case 64: return launch_t<64>(p, bf16, plan.grid, stream);
+        case 16: return launch_t<16>(p, bf16, plan.grid, false, stream);
+        case 32: return launch_t<32>(p, bf16, plan.grid, false, stream);
+        case 64: return launch_t<64>(p, bf16, plan.grid, false, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+bool plan_tc_round(int M, const int *N, const int *K, const int *epi, int n, const DeviceInfo &dev,
+                   TcRound *r, TcLinDesc *descs, size_t *ws_floats) {
+    if (M < 1 || M > kTcMaxTokens || n < 1) return false;
+    memset(r, 0, sizeof(*r));
+    r->n = n;
+    r->M = M;
+    r->T = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    r->stages = r->T == 16 ? stages_for<16>() : (r->T == 32 ? stages_for<32>() : stages_for<64>());
+    if (r->stages < 2) return false;
+    // one stream-K sequence: linear after linear, tile after tile, stage after stage
+    long long total = 0;
+    for (int l = 0; l < n; ++l) {
+        const int G = K[l] / kGroup;
+        if (G < 1) return false;
+        descs[l].n_tiles = epi[l] == kEpiSiluMul ? (N[l] / 2 + 63) / 64 : (N[l] + kTileN - 1) / kTileN;
+        descs[l].spt = (G + kSG - 1) / kSG;
+        descs[l].start = total;
+        total += (long long)descs[l].n_tiles * descs[l].spt;
+    }
+    r->total = total;
+    r->grid = total < dev.sm_count ? (int)total : dev.sm_count;
+    // partial-sum slots: two per CTA (its first and last segments), shared by the linears
+    *ws_floats = (size_t)2 * r->grid * M * kTileN;
+    return true;
+}
+
+cudaError_t launch_tc_round(const TcRound &r, int *status, cudaStream_t stream) {
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    p.lins = r.descs;
+    p.n_lin = r.n;
+    p.done = r.done;
+    p.partials = r.partials;
+    p.status = status;
+    p.M = r.M;
+    p.streamk = 1;
+    p.n_stages = r.stages;
+    p.total = r.total;
+    const bool coop = r.done != nullptr;
+    switch (r.T) {
+        case 16: return launch_t<16>(p, r.bf16, r.grid, coop, stream);
+        case 32: return launch_t<32>(p, r.bf16, r.grid, coop, stream);
+        case 64: return launch_t<64>(p, r.bf16, r.grid, coop, stream);
     }
     return cudaErrorInvalidValue;
 }
