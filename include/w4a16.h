@@ -235,13 +235,16 @@ int w4a16_linear_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *
  * anything is launched.
  *
  * The results are those of running the linears one after another in array
- * order.  When every linear takes the warp-MMA rungs (M <= 8, no forced rung)
- * the round is ONE kernel launch: the weights of all linears stream without a
- * break, each linear gets its own part of the split-K workspace, and a linear
- * that reads an earlier linear's output, writes an earlier linear's input or
- * output (overlapping device ranges) waits inside the kernel for that linear
- * to complete.  Such a round needs n_descs <= 4096 and workspace for every
- * split linear's partial sums at once (W4A16_ERR_WORKSPACE otherwise).  Its
+ * order.  Without a forced rung, a round of M <= 64 tokens is ONE kernel
+ * launch: M <= 8 on the warp-MMA kernel (each linear gets its own part of the
+ * split-K workspace), 9 <= M <= 64 on the tcgen05 kernel (one stream-K
+ * sequence over every linear's tiles; two partial-sum slots per CTA shared by
+ * all linears, one arrival counter per tile).  The weights of all linears
+ * stream without a break, and a linear that reads an earlier linear's
+ * output, writes an earlier linear's input or output (overlapping device
+ * ranges) waits inside the kernel for that linear to complete.  Such a round
+ * needs n_descs <= 4096, one 16-bit type for all its linears, and workspace
+ * for its partial sums and counters (W4A16_ERR_WORKSPACE otherwise).  Its
  * descriptors are copied to device memory on `stream` when they differ from
  * the previous round's (the copy may briefly block the calling thread while
  * it stages them).  Other rounds, and every round enqueued on a stream that is
