@@ -117,7 +117,7 @@ cudaError_t tc_init(const DeviceInfo &dev);
 // the tensor maps are written by the host only).  A round is one stream-K
 // sequence of (linear, tile, stage) work: linear l owns stages [start, start
 // + n_tiles * spt).
-struct alignas(64) TcLinDesc {
+struct TcLinDesc {
     CUtensorMap wmap;  // qweight 3-D: (16 words, N rows, G groups), box {16, 64, 4}
     CUtensorMap xmap;  // x 2-D: (K, M), box {64, T}, 128-byte swizzle
     const __half *x;
