@@ -181,3 +181,37 @@ def test_tc_round_epilogues(w4, dt):
                                            si.as_u32(ws[2][2]), dtype=name),
                              _bits(h_used), name)
     assert_close(hidden, h2, f"tc round down + residual {dt}", rtol=rtol)
+
+
+def test_tc_round_ragged(w4):
+    # ragged tiles in one stream-K sequence: N not a multiple of 128 (and a
+    # SiLU-and-mul layer whose N/2 is not a multiple of 64), K of 11 groups
+    # (a short last stage), 9 tokens (7 padding columns of the MMA)
+    M = 9
+    specs = [(1408, 777, w4.EPILOGUE_NONE), (1408, 1000, w4.EPILOGUE_RESIDUAL),
+             (1408, 320, w4.EPILOGUE_SILU_MUL), (2048, 4100, w4.EPILOGUE_NONE)]
+    layers, refs = [], []
+    for i, (K, N, epi) in enumerate(specs):
+        seed = si.config_seed(104, i)
+        qw, s, zw = si.layer(seed, N, K)
+        x = si.x(seed, M, K)
+        cols = N // 2 if epi == w4.EPILOGUE_SILU_MUL else N
+        r = si.residual(seed, M, N) if epi == w4.EPILOGUE_RESIDUAL else None
+        h = oracle.linear(_bits(x), si.as_u32(qw), _bits(s), si.as_u32(zw))
+        if epi == w4.EPILOGUE_RESIDUAL:
+            h = oracle.add_residual(h, _bits(r))
+        elif epi == w4.EPILOGUE_SILU_MUL:
+            h = oracle.silu_mul(h)
+        refs.append(h)
+        layers.append(dict(x=x.to(DEV), qweight=qw.to(DEV), scales=s.to(DEV), zeros=zw.to(DEV),
+                           y=torch.full((M, cols), float("nan"), dtype=torch.float16, device=DEV),
+                           epilogue=epi, residual=None if r is None else r.to(DEV)))
+    descs = w4.make_descs(layers)
+    w4.w4a16_probe_reset()
+    launches0 = w4.w4a16_kernel_launches()
+    w4.w4a16_decode_round(descs, M)
+    torch.cuda.synchronize()
+    assert w4.w4a16_kernel_launches() - launches0 == 1
+    assert w4.w4a16_probe_counts()[w4.RUNG_TC_SPLITK] == len(layers)
+    for L, ref, (K, N, epi) in zip(layers, refs, specs):
+        assert_close(L["y"], ref, f"ragged tc round K={K} N={N} epilogue={epi}")
