@@ -12,8 +12,9 @@ Printed (one JSON line on rank 0):
   ms_per_step   milliseconds per round
   roofline      the dominant kernel: algorithmic bytes per launch / its mean
                 CUDA-event duration, against the measured HBM copy bandwidth
-  e2e           the same round through the C ABI with host buffers: x copied
-                in from pinned memory and every y copied back, each step
+  e2e           the same round through the C ABI with host buffers, each step:
+                x copied in from pinned memory, and every y written by the
+                kernels straight into pinned host memory (one captured round)
   cpu_baseline  the oracle on the host cores, on a bounded sample of the round
   extra         single-linear numbers for the M = 1 / 4 / 8 shapes and the
                 M sweep (L2 flushed between timed launches)
@@ -240,44 +241,58 @@ def per_kernel_durations(w4, lin, steps, stream):
     return stats
 
 
-def time_e2e(w4, lin, xs, steps, warmup, stream, parts=1):
-    """x from pinned host memory in, decode round, every y back to pinned host
-    memory, waited for every step.  With parts > 1 the round runs as that
-    many w4a16_decode_round calls over consecutive layers, and each part's
-    outputs (final once its call ends) go back on a second stream while the
-    next part runs; the step still ends only when every output is on the
-    host."""
+def time_e2e(w4, lin, xs, steps, warmup, stream, parts=1, host_y=True):
+    """x from pinned host memory in, decode round, every y on the host, waited
+    for every step.  host_y: the round's descriptors point y at pinned host
+    memory, so the kernels store every output there themselves (no copy
+    back), and the round is one captured launch.  Otherwise each y goes back
+    by copy: with parts > 1 the round runs as that many captured rounds over
+    consecutive layers, and each part's outputs (final once its round ends)
+    go back on a second stream while the next part runs; the step still ends
+    only when every output is on the host."""
     x_all, y_all = lin[0]["x_all"], lin[0]["y_all"]
     pinned_x = torch.cat([x.reshape(-1) for x in xs]).pin_memory()
     pinned_y = torch.empty(y_all.shape, dtype=torch.float16).pin_memory()
     h2d = pinned_x.numel() * 2
     d2h = pinned_y.numel() * 2
-    # the linears of each part, and the span of y_all their outputs fill
-    # (several parts: each a captured round with descriptors of its own, so
-    # that no call re-uploads descriptors the previous part replaced)
-    per = (len(lin) + parts - 1) // parts
-    chunks = []
-    for i in range(0, len(lin), per):
-        group = lin[i:i + per]
-        lo = group[0]["y"].data_ptr() - y_all.data_ptr()
-        hi = group[-1]["y"].data_ptr() + group[-1]["y"].numel() * 2 - y_all.data_ptr()
-        descs = w4.make_descs(group)
-        run = (w4.RoundGraph(descs, M_ROUND).launch if parts > 1 else
-               (lambda d=descs, st=stream: w4.w4a16_decode_round(d, M_ROUND, stream=st)))
-        chunks.append((run, lo // 2, hi // 2))
-    copier = torch.cuda.Stream(device=y_all.device)
-    done = [torch.cuda.Event() for _ in chunks]
+    if host_y:
+        layers = []
+        for L in lin:
+            off = (L["y"].data_ptr() - y_all.data_ptr()) // 2
+            layers.append(dict(L, y=pinned_y[off:off + L["y"].numel()].view(L["y"].shape)))
+        g = w4.RoundGraph(w4.make_descs(layers), M_ROUND)
 
-    def step():
-        x_all.copy_(pinned_x, non_blocking=True)
-        for (run, lo, hi), ev in zip(chunks, done):
-            run(stream) if parts > 1 else run()
-            ev.record(stream)
-            copier.wait_event(ev)
-            with torch.cuda.stream(copier):
-                pinned_y[lo:hi].copy_(y_all[lo:hi], non_blocking=True)
-        copier.synchronize()
-        stream.synchronize()
+        def step():
+            x_all.copy_(pinned_x, non_blocking=True)
+            g.launch(stream)
+            stream.synchronize()
+    else:
+        # the linears of each part, and the span of y_all their outputs fill
+        # (several parts: each a captured round with descriptors of its own,
+        # so that no call re-uploads descriptors the previous part replaced)
+        per = (len(lin) + parts - 1) // parts
+        chunks = []
+        for i in range(0, len(lin), per):
+            group = lin[i:i + per]
+            lo = group[0]["y"].data_ptr() - y_all.data_ptr()
+            hi = group[-1]["y"].data_ptr() + group[-1]["y"].numel() * 2 - y_all.data_ptr()
+            descs = w4.make_descs(group)
+            run = (w4.RoundGraph(descs, M_ROUND).launch if parts > 1 else
+                   (lambda d=descs, st=stream: w4.w4a16_decode_round(d, M_ROUND, stream=st)))
+            chunks.append((run, lo // 2, hi // 2))
+        copier = torch.cuda.Stream(device=y_all.device)
+        done = [torch.cuda.Event() for _ in chunks]
+
+        def step():
+            x_all.copy_(pinned_x, non_blocking=True)
+            for (run, lo, hi), ev in zip(chunks, done):
+                run(stream) if parts > 1 else run()
+                ev.record(stream)
+                copier.wait_event(ev)
+                with torch.cuda.stream(copier):
+                    pinned_y[lo:hi].copy_(y_all[lo:hi], non_blocking=True)
+            copier.synchronize()
+            stream.synchronize()
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -287,6 +302,14 @@ def time_e2e(w4, lin, xs, steps, warmup, stream, parts=1):
         for _ in range(steps):
             step()
         t1 = time.perf_counter()
+    if host_y:
+        g.destroy()
+        # the host copy holds what the same round writes into device memory
+        # (run once more: the per-linear launches since then split K differently)
+        w4.w4a16_decode_round(w4.make_descs(lin), M_ROUND, stream=stream)
+        torch.cuda.synchronize()
+        if not torch.equal(pinned_y.view(torch.int16), y_all.cpu().view(torch.int16)):
+            raise RuntimeError("outputs written to host memory differ from the device round's")
     return (t1 - t0), h2d, d2h
 
 
@@ -839,15 +862,18 @@ def main():
                   for r, (n, t, by) in stats.items()}
 
     # ---- end to end through the C ABI with host buffers ----------------------
-    # two parts: the first half's outputs go back while the second half runs
-    # (measured: 2.12 ms against 2.19 for one part; four parts pay two more
-    # round fill-and-drains than they save)
-    e2e_s, h2d, d2h = time_e2e(w4, lin, xs, max(3, args.steps // 2), 2, stream, parts=2)
+    # the kernels write every y into pinned host memory (measured: 1.97 ms
+    # against 2.12 ms for the best copy-back schedule, two parts with the
+    # first half's outputs copied back while the second half runs)
     e2e_steps = max(3, args.steps // 2)
+    e2e_s, h2d, d2h = time_e2e(w4, lin, xs, e2e_steps, 2, stream)
     e2e_value, e2e_s = job_rate(e2e_s, rb, e2e_steps, world, dev)
     e2e = {"value": e2e_value, "unit": "GB/s",
            "ms_per_step": e2e_s / e2e_steps * 1e3, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+           "d2h_bytes_per_step": d2h,
+           "d2h_by": "the round's kernels store every y into pinned host memory"}
+    cb_s, _, _ = time_e2e(w4, lin, xs, e2e_steps, 2, stream, parts=2, host_y=False)
+    e2e["copy_back_ms_per_step"] = cb_s / e2e_steps * 1e3
 
     # ---- graph replay of the same round --------------------------------------
     g = w4.RoundGraph(descs, M_ROUND)

@@ -30,6 +30,16 @@
  *   - Pointers are DEVICE pointers unless a parameter says "host".  The caller
  *     owns every buffer; the library never frees or keeps caller pointers past
  *     the call (a captured graph keeps them, see w4a16_round_graph_create).
+ *   - One exception: the output y of w4a16_linear, w4a16_linear_noalloc,
+ *     w4a16_linear_epilogue, w4a16_linear_ex and of a decode round's
+ *     descriptors may be page-locked host memory that the device addresses at
+ *     the same pointer (cudaHostAlloc / cudaMallocHost, on a system with
+ *     unified addressing).  The kernels then store y straight into host memory
+ *     (on a Grace-Blackwell part, over the NVLink-C2C link), and the result is
+ *     on the host once the stream has passed the call: no copy back.  Every
+ *     other pointer stays device memory, so such a y can be neither a residual
+ *     nor another linear's x.  The library does not inspect pointer kinds: a
+ *     host y that the device cannot address faults like any bad pointer.
  *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
  *     default stream.  Work is enqueued asynchronously; nothing synchronises.
  *   - Arguments are validated on the host before anything is enqueued.  A

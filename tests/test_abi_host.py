@@ -235,3 +235,23 @@ def test_plan_info_names_the_cta_shape(w4):
 def test_probe_counters_reset(w4):
     w4.w4a16_probe_reset()
     assert w4.w4a16_probe_counts() == [0] * 6
+
+
+def test_binding_output_may_be_pinned_host_memory_inputs_may_not(w4):
+    # Only an output may live in (page-locked) host memory; the check runs in
+    # the binding before the library is called.  Here nothing is pinned (no
+    # GPU), so every CPU tensor is refused, and the message names the rule.
+    import torch
+    x = torch.zeros((1, 256), dtype=torch.float16)
+    qw = torch.zeros((64, 32), dtype=torch.int32)
+    s = torch.zeros((64, 2), dtype=torch.float16)
+    z = torch.zeros((64, 1), dtype=torch.int32)
+    y = torch.zeros((1, 64), dtype=torch.float16)
+    with pytest.raises(ValueError, match="page-locked host memory"):
+        w4.binding._dev(y, torch.float16, "y", True)
+    with pytest.raises(ValueError, match="must live on a CUDA device$"):
+        w4.binding._dev(x, torch.float16, "x")
+    with pytest.raises(ValueError, match="x must live on a CUDA device$"):
+        w4.w4a16_linear(x, qw, s, z, y=y)
+    with pytest.raises(ValueError, match="x must live on a CUDA device$"):
+        w4.make_descs([dict(x=x, qweight=qw, scales=s, zeros=z, y=y)])

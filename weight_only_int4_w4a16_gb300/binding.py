@@ -150,11 +150,14 @@ def _stream_ptr(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _dev(t: torch.Tensor, dtype, name: str):
+def _dev(t: torch.Tensor, dtype, name: str, host_ok: bool = False):
+    """The tensor's address after checks.  host_ok: an output that may also be
+    page-locked host memory (pin_memory()), which the kernels write directly."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must live on a CUDA device" +
+                         (" or in page-locked host memory" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -248,14 +251,19 @@ def w4a16_transpose_f16(src: torch.Tensor, dst=None, stream=None) -> torch.Tenso
 
 def w4a16_linear(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
                  zeros: torch.Tensor, group: int = GROUP, y=None, stream=None) -> torch.Tensor:
-    """y [M, N] fp16 = x [M, K] fp16 @ dequant(qweight, scales, zeros)^T."""
+    """y [M, N] fp16 = x [M, K] fp16 @ dequant(qweight, scales, zeros)^T.
+
+    y (here and in the other linear calls and round descriptors) may be a
+    pinned host tensor: the kernels then store the result straight into host
+    memory, and it is there once the stream has passed the call."""
     M, K = x.shape
     N = qweight.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check(lib.w4a16_linear(_dev(x, torch.float16, "x"), _dev(qweight, torch.int32, "qweight"),
                             _dev(scales, torch.float16, "scales"), _dev(zeros, torch.int32, "zeros"),
-                            M, N, K, group, _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+                            M, N, K, group, _dev(y, torch.float16, "y", True),
+                            _stream_ptr(stream)),
            "w4a16_linear")
     return y
 
@@ -271,7 +279,7 @@ def w4a16_linear_noalloc(x: torch.Tensor, qweight: torch.Tensor, scales: torch.T
                                     _dev(qweight, torch.int32, "qweight"),
                                     _dev(scales, torch.float16, "scales"),
                                     _dev(zeros, torch.int32, "zeros"), M, N, K, group,
-                                    _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+                                    _dev(y, torch.float16, "y", True), _stream_ptr(stream)),
            "w4a16_linear_noalloc")
     return y
 
@@ -292,7 +300,7 @@ def w4a16_linear_epilogue(x: torch.Tensor, qweight: torch.Tensor, scales: torch.
                                      _dev(qweight, torch.int32, "qweight"),
                                      _dev(scales, torch.float16, "scales"),
                                      _dev(zeros, torch.int32, "zeros"), M, N, K, group, epilogue,
-                                     r, _dev(y, torch.float16, "y"), _stream_ptr(stream)),
+                                     r, _dev(y, torch.float16, "y", True), _stream_ptr(stream)),
            "w4a16_linear_epilogue")
     return y
 
@@ -313,7 +321,7 @@ def w4a16_linear_ex(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor
     r = _dev(residual, dt, "residual") if residual is not None else None
     _check(lib.w4a16_linear_ex(_dev(x, dt, "x"), _dev(qweight, torch.int32, "qweight"),
                                _dev(scales, dt, "scales"), _dev(zeros, torch.int32, "zeros"),
-                               M, N, K, group, _DTYPE_OF[dt], epilogue, r, _dev(y, dt, "y"),
+                               M, N, K, group, _DTYPE_OF[dt], epilogue, r, _dev(y, dt, "y", True),
                                _stream_ptr(stream)),
            "w4a16_linear_ex")
     return y
@@ -464,7 +472,9 @@ def w4a16_moe_sum(y_sorted: torch.Tensor, pos: torch.Tensor, weights: torch.Tens
 
 def make_descs(layers) -> ctypes.Array:
     """layers: iterable of dicts with x, qweight, scales, zeros, y tensors (and
-    optionally an epilogue code and a residual tensor) -> host desc array."""
+    optionally an epilogue code and a residual tensor) -> host desc array.
+    A y may be a pinned host tensor (never another layer's x or residual:
+    those must be CUDA tensors)."""
     layers = list(layers)
     arr = (LinearDesc * len(layers))()
     for i, L in enumerate(layers):
@@ -475,7 +485,7 @@ def make_descs(layers) -> ctypes.Array:
             raise TypeError(f"x must be float16 or bfloat16, got {dt}")
         arr[i] = LinearDesc(_dev(L["x"], dt, "x"), _dev(L["qweight"], torch.int32, "qweight"),
                             _dev(L["scales"], dt, "scales"),
-                            _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], dt, "y"),
+                            _dev(L["zeros"], torch.int32, "zeros"), _dev(L["y"], dt, "y", True),
                             N, K, L.get("group", GROUP), L.get("epilogue", EPILOGUE_NONE),
                             _dev(res, dt, "residual") if res is not None else None,
                             _DTYPE_OF[dt])
