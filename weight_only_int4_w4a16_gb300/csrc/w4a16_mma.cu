@@ -749,12 +749,17 @@ __global__ void __launch_bounds__(CtaShape<W>::kThreads, CtaShape<W>::kCtasPerSm
             const int nunits = ng * (kGroup / 8);
             const int xtotal = M * nunits;  // a multiple of 16
             int *xexp = token_exps(xs, M, D.xstride, D.slice_groups);
+            // Unit i = t * nunits + J of this thread: 32 warp + lane, then
+            // kThreads further per pass.  With bf16, t and J step without a
+            // division (the fp16 kernel keeps the division: the stepped form
+            // costs it registers elsewhere)
+            const int i0 = warp * 32 + lane;
+            const int dt = kThreads / nunits, dJ = kThreads - dt * nunits;
             if (kBf16) {
                 // each token's largest exponent: a half warp holds 16 units of
                 // one token (nunits is a multiple of 16)
-                for (int base = warp * 32; base < xtotal; base += kThreads) {
-                    const int i = base + lane;
-                    const int t = i / nunits, J = i - t * nunits;
+                for (int i = i0, t = i0 / nunits, J = i0 - t * nunits; i - lane < xtotal;
+                     i += kThreads) {
                     int e = 0;
                     if (i < xtotal)
                         e = max_bf16_exp(*reinterpret_cast<const uint4 *>(
@@ -762,13 +767,33 @@ __global__ void __launch_bounds__(CtaShape<W>::kThreads, CtaShape<W>::kCtasPerSm
 #pragma unroll
                     for (int off = 8; off > 0; off >>= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, off));
                     if (i < xtotal && (J & 15) == 0) atomicMax(xexp + t, e);
+                    t += dt;
+                    J += dJ;
+                    if (J >= nunits) {
+                        J -= nunits;
+                        ++t;
+                    }
                 }
                 __syncthreads();
             }
-            for (int base = warp * 32; base < xtotal; base += kThreads) {
+            for (int base = warp * 32, ts = i0 / nunits, Js = i0 - ts * nunits; base < xtotal;
+                 base += kThreads) {
                 const int i = base + lane;
                 const bool valid = i < xtotal;
-                const int t = i / nunits, J = i - t * nunits;
+                int t, J;
+                if constexpr (kBf16) {
+                    t = ts;
+                    J = Js;
+                    ts += dt;
+                    Js += dJ;
+                    if (Js >= nunits) {
+                        Js -= nunits;
+                        ++ts;
+                    }
+                } else {
+                    t = i / nunits;
+                    J = i - t * nunits;
+                }
                 uint8_t *row = xs + (size_t)t * D.xstride;
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid) v = *reinterpret_cast<const uint4 *>(row + 16 * J);
@@ -862,7 +887,6 @@ __global__ void __launch_bounds__(CtaShape<W>::kThreads, CtaShape<W>::kCtasPerSm
                         }
                         const float sA = bits_to_float<kBf16>(hA & 0xffffu);
                         const float sB = bits_to_float<kBf16>(hB & 0xffffu);
-                        // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
                         // zero points of rows ra and rb as floats (2^23 + z, minus 2^23)
                         const float zA =
                             __uint_as_float(0x4b000000u | ((zwA >> (4 * i)) & 0xfu)) - 8388608.f;

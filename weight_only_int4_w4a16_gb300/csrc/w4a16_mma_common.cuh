@@ -38,11 +38,11 @@ __device__ __forceinline__ int bf16_stage_shift(int E) { return max(-126, min(12
 __device__ __forceinline__ float pow2(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 // largest exponent field among the 8 bf16 values of a 16-byte unit
 __device__ __forceinline__ int max_bf16_exp(uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    int e = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) e = max(e, max((int)((w[i] >> 7) & 0xffu), (int)((w[i] >> 23) & 0xffu)));
-    return e;
+    // the exponent fields in place (sign cleared), the largest by 16-bit
+    // SIMD max: the unsigned order of the masked halves is that of the fields
+    constexpr uint32_t kExp = 0x7f807f80u;
+    const uint32_t m = __vmaxu2(__vmaxu2(v.x & kExp, v.y & kExp), __vmaxu2(v.z & kExp, v.w & kExp));
+    return (int)(max(m & 0xffffu, m >> 16) >> 7);
 }
 // 8 bf16 values times 2^k, rounded to fp16 (exact but for the subnormal tail)
 __device__ __forceinline__ uint4 bf16_to_scaled_f16(uint4 v, float scale) {
