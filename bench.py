@@ -693,6 +693,31 @@ def run_dense_case(M: int, N: int, K: int, reps: int):
         raise SystemExit(1)
 
 
+def run_round_case(dtype: str, layers: int, reps: int, M: int):
+    """The bench's decode round (its shapes, `layers` layers, M tokens) with
+    fp16 or bf16 activations and scales, `reps` rounds on one stream: the
+    target of ncu captures."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import weight_only_int4_w4a16_gb300 as w4
+    dev = torch.device("cuda:0")
+    w4.w4a16_init(0, 512 << 20)
+    lin, _, _ = build_round(dev, M=M, layers=layers)
+    if dtype == "bf16":
+        bxs = {id(L["x"]): L["x"].to(torch.bfloat16) for L in lin}
+        lin = [dict(x=bxs[id(L["x"])], qweight=L["qweight"], zeros=L["zeros"],
+                    scales=L["scales"].to(torch.bfloat16),
+                    y=torch.empty_like(L["y"], dtype=torch.bfloat16)) for L in lin]
+    descs = w4.make_descs(lin)
+    for _ in range(reps):
+        w4.w4a16_decode_round(descs, M)
+    torch.cuda.synchronize()
+    status = w4.w4a16_device_status()
+    print(f"round case dtype={dtype} layers={layers} M={M} reps={reps} device_status={status}")
+    if status:
+        raise SystemExit(1)
+
+
 def run_moe_case(T: int, reps: int):
     """The expert MLP of the bench's MoE entry (E 128, top 8, hidden 2048,
     intermediate 768) for T tokens on its default path, `reps` calls: the
@@ -753,6 +778,9 @@ def main():
                     help="run the expert MLP for T tokens REPS times and exit (for ncu)")
     ap.add_argument("--dense-case", type=int, nargs=4, metavar=("M", "N", "K", "REPS"),
                     help="profiling helper: run one dense fp16 linear REPS times and exit")
+    ap.add_argument("--round-case", nargs=3, metavar=("DTYPE", "LAYERS", "REPS"),
+                    help="profiling helper: run the decode round (f16 or bf16, at --round-m "
+                         "tokens) REPS times and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -765,6 +793,12 @@ def main():
         return
     if args.dense_case:
         run_dense_case(*args.dense_case)
+        return
+    if args.round_case:
+        dt, nl, reps = args.round_case
+        if dt not in ("f16", "bf16"):
+            raise SystemExit("--round-case DTYPE is f16 or bf16")
+        run_round_case(dt, int(nl), int(reps), args.round_m)
         return
     if args.impl == "reference":
         run_reference(args)
