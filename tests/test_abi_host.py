@@ -199,6 +199,22 @@ def test_dispatch_table_host_queries(w4):
     assert w4.w4a16_select_rung(16, 27648, 5120) in (w4.RUNG_TC, w4.RUNG_TC_SPLITK)
     assert w4.w4a16_select_rung(1, 1024, 500) == -1
     assert w4.w4a16_select_rung(0, 1024, 512) == -1
+    # small fp16 linears launched alone take the CUDA-core gemv kernel: up to
+    # 24 Mi weights at 1..2 tokens, 16 Mi at 3..4, 8 Mi at 5..8 (K split
+    # where one warp cannot hold the whole K); larger ones the warp-MMA kernel
+    gemv = (w4.RUNG_GEMV, w4.RUNG_GEMV_SPLITK)
+    mma = (w4.RUNG_MMA, w4.RUNG_MMA_SPLITK)
+    assert w4.w4a16_select_rung(1, 1024, 512) == w4.RUNG_GEMV
+    assert w4.w4a16_select_rung(2, 6144, 4096) in gemv
+    assert w4.w4a16_select_rung(2, 8192, 4096) in mma
+    assert w4.w4a16_select_rung(4, 4096, 4096) in gemv
+    assert w4.w4a16_select_rung(4, 6144, 4096) in mma
+    assert w4.w4a16_select_rung(8, 512, 16384) in gemv
+    assert w4.w4a16_select_rung(8, 4096, 4096) in mma
+    assert w4.w4a16_select_rung(1, 34816, 5120) in mma
+    # epilogues and bf16 stay on the MMA kernels
+    assert w4.w4a16_plan_info(1, 1024, 512, epilogue=w4.EPILOGUE_RESIDUAL)["rung"] in mma
+    assert w4.w4a16_plan_info(1, 1024, 512, dtype=w4.DTYPE_BF16)["rung"] in mma
     prev = w4.w4a16_set_forced_rung(w4.RUNG_GEMV_SPLITK)
     try:
         assert w4.w4a16_select_rung(4, 5120, 17408) == w4.RUNG_GEMV_SPLITK

@@ -116,6 +116,21 @@ int tile_tokens(int rung) {
     return is_tc(rung) ? kTcMaxTokens : (is_mma(rung) ? kMmaMaxTokens : kGemvMaxTokens);
 }
 
+// A small fp16 linear without an epilogue, launched alone, runs faster on the
+// CUDA-core gemv kernel: its launch is lighter than the warp-MMA kernel's
+// (no tensor maps, no staged x, no mbarrier ring), and the weights are too few
+// for the MMA kernel's per-weight advantage to pay that back.  The weight
+// counts up to which it wins come from single launches with L2 evicted (one
+// GB300): at 1..2 tokens up to 24 Mi weights (N 6144, K 4096: 14.3 against
+// 16.4 us; a tie at 32 Mi), at 3..4 tokens up to 16 Mi (N 4096, K 4096: 16.4
+// against 18.4 us; slower at 24 Mi), at 5..8 tokens up to 8 Mi (N 512, K 16384
+// split: 18.4 against 24.5 us; slower at 16 Mi on most shapes).
+bool gemv_small(int M, int N, int K) {
+    const long long w = (long long)N * K;
+    const long long lim = M <= 2 ? (24ll << 20) : M <= 4 ? (16ll << 20) : (8ll << 20);
+    return M <= kMmaMaxTokens && w <= lim;
+}
+
 Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi = kEpiNone,
                 int dtype = kDtypeF16) {
     const int Mt = M < kGemvMaxTokens ? M : kGemvMaxTokens;
@@ -155,6 +170,12 @@ Decision decide(int M, int N, int K, const DeviceInfo &dev, int forced, int epi 
             break;
     }
     if (M <= kMmaMaxTokens) {
+        if (gemv_small(M, N, K)) {
+            // the whole K per warp where the plan allows it (faster on every
+            // small shape measured), else K split
+            if (plan_gemv(Mt, N, K, 0, dev).ok) return {W4A16_RUNG_GEMV, W4A16_OK};
+            if (G >= 2) return {W4A16_RUNG_GEMV_SPLITK, W4A16_OK};
+        }
         MmaPlan p = plan_mma(Mt, N, K, -1, dev, epi);
         return {p.S > 1 ? W4A16_RUNG_MMA_SPLITK : W4A16_RUNG_MMA, W4A16_OK};
     }
