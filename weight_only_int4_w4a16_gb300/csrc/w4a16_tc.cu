@@ -1141,11 +1141,18 @@ TcPlan plan_tc(int M, int N, int K, int split, const DeviceInfo &dev, int epi) {
     const long long total = (long long)pl.n_tiles * pl.spt;
     const int slots = dev.sm_count;  // one CTA per SM
     // whole tiles unless they leave SMs idle for long: with n tiles on s SMs
-    // the busiest SM streams ceil(n / s) tiles against n / s on average
+    // the busiest SM streams ceil(n / s) tiles against n / s on average.  From
+    // 17 tokens on, a single wave of tiles with few stages each stays whole:
+    // there the pieces' partial sums (M x 128 fp32 per piece) cost more than
+    // the idle SMs (one launch, L2 evicted, M = 24: N 8192, K 4096, 8 stages a
+    // tile: 24.8 us whole against 30.7 split; N 4096, K 2048: 17.9 against
+    // 20.7), while 16 stages a tile and more still gain from the split (N 1024,
+    // K 8192: 31.0 split against 42.0)
     bool streamk = split == 1;
     if (split < 0) {
         const double rounds = (double)((pl.n_tiles + slots - 1) / slots);
         streamk = (double)pl.n_tiles / slots < 0.9 * rounds && pl.spt > 1;
+        if (M > 16 && pl.n_tiles <= slots && pl.spt < 12) streamk = false;
     }
     pl.S = streamk ? 2 : 1;
     if (streamk) pl.grid = total < slots ? (int)total : slots;
