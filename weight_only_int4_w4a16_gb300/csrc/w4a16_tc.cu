@@ -722,7 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
             asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
         bool dep_waited = false;
         int x_waited = -1;  // the last linear whose wait_for this thread has waited for
-        int xuse[kAStages] = {0, 0, 0, 0};  // x copies this thread issued per slot
+        // x copies this thread issued, per slot: whether any (bit a of xused) and
+        // the parity of their count (bit a of xpar); bit masks, not an array
+        // indexed at run time, which would live in local memory
+        uint32_t xused = 0, xpar = 0;
         int c = 0, sc = 0;
         bool ok = true;
         while (ok && walk_next(p, lins, kRound ? n_lin : 1, wk, l, t, j0, j1)) {
@@ -767,7 +770,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(empty + s));
-                const uint32_t mw[3] = {md.x, md.y, md.z};
                 const uint32_t off = (uint32_t)((uintptr_t)(srow + kSG * j) & 2);
                 const uint32_t zsh = 4u * (uint32_t)((kSG * j) & 7);  // the stage's first nibble
                 // the team's groups of the stage are restored one after the
@@ -809,10 +811,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
                         tma_load_2d(smem_u32(sm_x + a * C::kXSlot), &L.xmap, k0, 0, xbar, pol_x);
                         tma_load_2d(smem_u32(sm_x + a * C::kXSlot + T * 128), &L.xmap, k0 + 64, 0,
                                     xbar, pol_x);
-                        ++xuse[a];
+                        xused |= 1u << a;
+                        xpar ^= 1u << a;
                     }
                     const uint32_t bp = off + 2u * gi;  // byte of the scale in the words
-                    const uint32_t sbits = (mw[bp >> 2] >> (8u * (bp & 2u))) & 0xffffu;
+                    // the word holding it (selected, not indexed: no local memory)
+                    const uint32_t sw4 = bp >> 2;
+                    const uint32_t sword = sw4 == 0 ? md.x : (sw4 == 1 ? md.y : md.z);
+                    const uint32_t sbits = (sword >> (8u * (bp & 2u))) & 0xffffu;
                     const uint32_t z = (md.w >> (zsh + 4u * gi)) & 0xfu;
                     const uint32_t zz_hi = 0x64006400u | z | (z << 16);
                     const uint32_t zz_lo = 0x54005400u | (z << 4) | (z << 20);
@@ -873,7 +879,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
         // waited for by its MMA issuer, or, after an abort, here (bounded)
         if (x_issuer && !ok)
             for (int a = 0; a < kAStages; ++a)
-                if (xuse[a] > 0 && !mbar_wait_drain(smem_u32(x_full + a), (xuse[a] - 1) & 1))
+                if (((xused >> a) & 1u) &&
+                    !mbar_wait_drain(smem_u32(x_full + a), ((xpar >> a) & 1u) ^ 1u))
                     atomicOr(p.status, kErrDrain);
     } else {
         // ------------------------------------------------ epilogue (warps 0..3)
