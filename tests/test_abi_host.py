@@ -248,6 +248,18 @@ def test_plan_info_names_the_cta_shape(w4):
         w4.w4a16_plan_info(4, 1000, 512, epilogue=w4.EPILOGUE_SILU_MUL)  # N/2 not a multiple of 16
 
 
+def test_tc_plan_keeps_short_single_wave_tiles_whole(w4):
+    # From 17 tokens on, a single wave of tiles with fewer than 12 stages
+    # stays whole (the pieces' partial sums cost more than idle SMs); long
+    # tiles, and shapes of more than one wave, are split (stream-K)
+    assert w4.w4a16_set_forced_rung(w4.RUNG_AUTO) == w4.RUNG_AUTO
+    assert w4.w4a16_plan_info(24, 8192, 4096)["rung"] == w4.RUNG_TC          # 64 tiles, 8 stages
+    assert w4.w4a16_plan_info(64, 2048, 5120)["rung"] == w4.RUNG_TC          # 16 tiles, 10 stages
+    assert w4.w4a16_plan_info(24, 1024, 8192)["rung"] == w4.RUNG_TC_SPLITK   # 16 stages a tile
+    assert w4.w4a16_plan_info(32, 27648, 5120)["rung"] == w4.RUNG_TC_SPLITK  # 216 tiles
+    assert w4.w4a16_plan_info(16, 8192, 4096)["rung"] == w4.RUNG_TC_SPLITK   # 16 tokens: split
+
+
 def test_probe_counters_reset(w4):
     w4.w4a16_probe_reset()
     assert w4.w4a16_probe_counts() == [0] * 6
