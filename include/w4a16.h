@@ -407,7 +407,11 @@ int w4a16_moe_sum(const uint16_t *y_sorted, const int32_t *pos, const float *wei
                   int k, int N, int dtype, uint16_t *out, void *stream);
 
 /* The rung the dispatch table picks for a shape (honouring a forced rung), or
- * -1 for an invalid shape.  Pure host query. */
+ * -1 for an invalid shape.  Pure host query.  Unforced: M <= 8 takes the warp
+ * MMA rungs, except small fp16 linears without an epilogue, which take the
+ * CUDA-core rungs (where the lighter launch wins: up to 24 Mi weights N*K at
+ * M <= 2, 16 Mi at M <= 4, 8 Mi at M <= 8); M >= 9 takes the tcgen05 rungs.
+ * The _SPLITK variant is the plan's choice for the shape. */
 int w4a16_select_rung(int M, int N, int K, int group);
 
 /* The plan of the first tile of a linear (of up to 8 tokens on the mma and
